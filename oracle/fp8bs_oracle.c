@@ -1,0 +1,476 @@
+/*
+ * fp8bs_oracle.c -- plain, slow CPU oracle for the fine-grained FP8 linear layer.
+ *
+ * TEST INFRASTRUCTURE. Only the tests, the smoke check and the benchmark's CPU
+ * baseline may load this file's library. It shares no code, header, table or
+ * constant with the CUDA library; each side is written from the sources below.
+ *
+ * What it computes, and where each step is stated:
+ *   - E4M3 number format: OCP 8-bit Floating Point Specification (OFP8), E4M3
+ *     encoding (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits,
+ *     subnormals at exponent 0, no infinities, only S.1111.111 is NaN).
+ *     The pages fix the largest finite value 448 (TransformerEngine PR #3573,
+ *     "Changes": the E4M3 bound is 448 unless 4over6 asks for 256) and the two
+ *     zero payloads +0 = 0x00, -0 = 0x80 (prime-rl PR #4073, conventions
+ *     table, row "Negative zero").
+ *   - Fine-grained dynamic scaling: "FP8 动态量化里的 partial sum 漂移", section 3,
+ *     table row (a): tiles of N_c = 128, a dynamic scale per tile from the
+ *     tile's absmax, values rounded to FP8 inside the tile.
+ *   - Tile shapes 1x128 (activations, gradients), 128x128 (weights) and the
+ *     128x1 re-tiling of saved operands for Wgrad: "scratch: the backward pass,
+ *     unrolled", "What is asserted, and from where", bullets 1 and 2.
+ *   - Per-128 promotion: same partial-sum page, section 3 row (b) and section 5:
+ *     the partial over 128 elements of K is flushed into an FP32 accumulator
+ *     after being multiplied by s_x * s_w.
+ *   - Unpromoted accumulation (drift model): same page, section 4,
+ *     s_hat_t = round(s_hat_{t-1} + round(p_t)).
+ *
+ * Readings where the pages are silent (each one is also listed in the design
+ * notes of the repository):
+ *   - s = amax / 448 is a true IEEE fp32 division, and q = E4M3_RN(fp32(v / s))
+ *     (the quotient is rounded to fp32 first, then to E4M3).
+ *   - E4M3 rounding is round-to-nearest, ties to the even code, saturating to
+ *     +-448, and a result of zero keeps the sign of its input.
+ *   - An all-zero tile stores s = 1 and signed zeros.
+ *   - Partial tiles at a ragged edge take the absmax over their valid elements.
+ *   - The per-block partial sum P_b is exact (accumulated in fp64, which holds
+ *     every sum of 128 E4M3 products exactly), rounded once to fp32, multiplied
+ *     by the fp32 product s_a * s_b, and added to the fp32 accumulator in block
+ *     order. Compile with -ffp-contract=off so that no FMA fuses these steps.
+ *
+ * Build: gcc -std=c99 -O2 -fPIC -shared -ffp-contract=off [-fopenmp]
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+typedef int64_t i64;
+
+/* ------------------------------------------------------------------------- */
+/* E4M3 table (OCP OFP8 E4M3 definition).                                     */
+/* ------------------------------------------------------------------------- */
+
+static float g_dec[256];
+static int g_dec_ready = 0;
+
+/* Planted-mistake switch, used only by the negative-control tests: each value
+ * makes one plausible implementation error on purpose so that the tests can
+ * show that the pins catch it. 0 (the default) is the correct oracle. */
+enum {
+    FAULT_NONE = 0,
+    FAULT_DROP_LAST_BLOCK = 1,   /* promoted sum skips the last K-block */
+    FAULT_SCALE_NEXT_BLOCK = 2,  /* B scale taken from the next K-block */
+    FAULT_TIES_AWAY = 3,         /* E4M3 ties round away from zero */
+    FAULT_SIGNED_AMAX = 4,       /* tile scale from max(v) instead of max|v| */
+    FAULT_TRANSPOSED_W = 5,      /* fprop reads W transposed */
+    FAULT_DROP_NEG_ZERO = 6,     /* -0 results encoded as 0x00 */
+    FAULT_RECIPROCAL = 7,        /* v * (1/s) instead of v / s */
+    FAULT_SIGN_FLIP_TERM = 8     /* one K-block's term subtracted */
+};
+static int g_fault = FAULT_NONE;
+
+void oracle_set_fault(int f) { g_fault = f; }
+
+static void build_table(void)
+{
+    if (g_dec_ready) return;
+    for (int c = 0; c < 256; ++c) {
+        int sign = (c >> 7) & 1;
+        int e = (c >> 3) & 0xF;
+        int m = c & 0x7;
+        double mag;
+        if (e == 0xF && m == 0x7) {      /* S.1111.111 is the only NaN */
+            g_dec[c] = NAN;
+            continue;
+        }
+        if (e == 0)
+            mag = ldexp((double)m, -9);  /* subnormal: (m/8) * 2^(1-7) */
+        else
+            mag = ldexp(8.0 + m, e - 10); /* (1 + m/8) * 2^(e-7) */
+        g_dec[c] = (float)(sign ? -mag : mag);
+    }
+    g_dec_ready = 1;
+}
+
+void oracle_e4m3_table(float out[256])
+{
+    build_table();
+    memcpy(out, g_dec, sizeof(g_dec));
+}
+
+/* Nearest finite E4M3 by search over the table: the positive codes
+ * 0x00..0x7E are ascending in value, so bisect for the largest code not above
+ * |v| and compare |v| with the midpoint to the next one. Ties take the even
+ * code (mantissa LSB 0). |v| >= 448 saturates to 448. Zero keeps v's sign. */
+uint8_t oracle_e4m3_encode(float v)
+{
+    build_table();
+    if (isnan(v)) return 0x7F;
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs((double)v);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    int lo = 0, hi = 0x7E;               /* g_dec[lo] <= a < g_dec[hi] */
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if ((double)g_dec[mid] <= a) lo = mid; else hi = mid;
+    }
+    /* midpoint comparison done exactly: both sides are exact in double */
+    double twice = 2.0 * a;
+    double msum = (double)g_dec[lo] + (double)g_dec[lo + 1];
+    int c;
+    if (twice < msum) c = lo;
+    else if (twice > msum) c = lo + 1;
+    else if (g_fault == FAULT_TIES_AWAY) c = lo + 1;
+    else c = (lo % 2 == 0) ? lo : lo + 1;
+    if (c == 0 && g_fault == FAULT_DROP_NEG_ZERO) sign = 0;
+    return (uint8_t)(sign | c);
+}
+
+void oracle_e4m3_encode_array(const float* v, i64 n, uint8_t* out)
+{
+    for (i64 i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(v[i]);
+}
+
+float oracle_e4m3_decode(uint8_t c)
+{
+    build_table();
+    return g_dec[c];
+}
+
+/* bf16 bits -> fp32 (exact). */
+static float bf16_to_f32(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* fp32 -> bf16 bits, round to nearest even (finite inputs; NaN -> quiet NaN). */
+uint16_t oracle_f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return 0x7FC0;
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7FFFu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+void oracle_f32_to_bf16_array(const float* in, i64 n, uint16_t* out)
+{
+    for (i64 i = 0; i < n; ++i) out[i] = oracle_f32_to_bf16(in[i]);
+}
+
+/* ------------------------------------------------------------------------- */
+/* One quantization tile: amax, scale, codes.                                 */
+/* ------------------------------------------------------------------------- */
+
+/* Scale of a tile whose values are v[0..n): amax / 448 in fp32, or 1 for an
+ * all-zero tile. */
+static float tile_scale(const float* v, int n)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float a = (g_fault == FAULT_SIGNED_AMAX) ? v[i] : fabsf(v[i]);
+        if (a > amax) amax = a;
+    }
+    if (amax == 0.0f) return 1.0f;
+    return amax / 448.0f;
+}
+
+static void tile_encode(const float* v, int n, float s, uint8_t* out, i64 out_step)
+{
+    for (int i = 0; i < n; ++i) {
+        float quot = (g_fault == FAULT_RECIPROCAL) ? v[i] * (1.0f / s) : v[i] / s;
+        out[i * out_step] = oracle_e4m3_encode(quot);
+    }
+}
+
+/* S1: 1x128 tiles along each row.
+ * x: bf16 [rows x cols], row stride ldx (elements).
+ * q: E4M3 [rows x cols], row stride ldq.
+ * scale of (row r, tile t) is written to sc[r * sc_rs + t * sc_ts]. */
+void oracle_quant_1x128(const uint16_t* x, i64 rows, i64 cols, i64 ldx,
+                        uint8_t* q, i64 ldq, float* sc, i64 sc_rs, i64 sc_ts)
+{
+    i64 ntiles = (cols + 127) / 128;
+#pragma omp parallel for schedule(static)
+    for (i64 r = 0; r < rows; ++r) {
+        float v[128];
+        for (i64 t = 0; t < ntiles; ++t) {
+            i64 c0 = t * 128;
+            int n = (int)((cols - c0) < 128 ? (cols - c0) : 128);
+            for (int i = 0; i < n; ++i) v[i] = bf16_to_f32(x[r * ldx + c0 + i]);
+            float s = tile_scale(v, n);
+            sc[r * sc_rs + t * sc_ts] = s;
+            tile_encode(v, n, s, q + r * ldq + c0, 1);
+        }
+    }
+}
+
+/* S2: 128x128 blocks. Scale of block (bi, bj) goes to sc[bi * ldsc + bj]. */
+void oracle_quant_128x128(const uint16_t* x, i64 rows, i64 cols, i64 ldx,
+                          uint8_t* q, i64 ldq, float* sc, i64 ldsc)
+{
+    i64 nbr = (rows + 127) / 128, nbc = (cols + 127) / 128;
+#pragma omp parallel for schedule(static)
+    for (i64 blk = 0; blk < nbr * nbc; ++blk) {
+        i64 bi = blk / nbc, bj = blk % nbc;
+        i64 r0 = bi * 128, c0 = bj * 128;
+        int nr = (int)((rows - r0) < 128 ? (rows - r0) : 128);
+        int nc = (int)((cols - c0) < 128 ? (cols - c0) : 128);
+        float v[128 * 128];
+        for (int i = 0; i < nr; ++i)
+            for (int j = 0; j < nc; ++j)
+                v[i * nc + j] = bf16_to_f32(x[(r0 + i) * ldx + c0 + j]);
+        float s = tile_scale(v, nr * nc);
+        sc[bi * ldsc + bj] = s;
+        for (int i = 0; i < nr; ++i)
+            tile_encode(v + i * nc, nc, s, q + (r0 + i) * ldq + c0, 1);
+    }
+}
+
+/* Number of token columns the transposed output holds: each group's token
+ * count rounded up to a whole number of 128-token tiles. */
+i64 oracle_padded_tokens(const int32_t* offsets, int groups, i64 rows)
+{
+    if (!offsets || groups <= 0) return ((rows + 127) / 128) * 128;
+    i64 tot = 0;
+    for (int g = 0; g < groups; ++g) {
+        i64 n = (i64)offsets[g + 1] - (i64)offsets[g];
+        tot += ((n + 127) / 128) * 128;
+    }
+    return tot;
+}
+
+/* S3: 128x1 tiles along the token (row) axis, transposed output.
+ *   mode 0 (B): src is bf16 [rows x cols] with row stride ld_src.
+ *   mode 1 (Q): src is E4M3 [rows x cols] with row stride ld_src and 1x128
+ *               scales src_sc[r * src_rs + t * src_ts]; an element is
+ *               decoded as fp32(dec(q) * s) before requantization.
+ * groups > 0 splits the rows at offsets[0..groups] (offsets[0] = 0); each
+ * group's tiles start at its own first row and the group's segment in the
+ * output starts at a multiple of 128 (padded token index).
+ * qT: E4M3 [cols x Mpad], row stride ldqT; padding bytes are 0x00.
+ * scT: fp32 [Mpad/128 x cols], row stride ldscT. */
+void oracle_requant_128x1_T(int mode, const void* src, i64 ld_src,
+                            const float* src_sc, i64 src_rs, i64 src_ts,
+                            i64 rows, i64 cols, const int32_t* offsets, int groups,
+                            uint8_t* qT, i64 ldqT, float* scT, i64 ldscT)
+{
+    build_table();
+    int ng = (offsets && groups > 0) ? groups : 1;
+    i64 pstart = 0;
+    for (int g = 0; g < ng; ++g) {
+        i64 r_begin = (offsets && groups > 0) ? offsets[g] : 0;
+        i64 r_end = (offsets && groups > 0) ? offsets[g + 1] : rows;
+        i64 n = r_end - r_begin;
+        i64 ntiles = (n + 127) / 128;
+#pragma omp parallel for schedule(static)
+        for (i64 c = 0; c < cols; ++c) {
+            float v[128];
+            for (i64 t = 0; t < ntiles; ++t) {
+                i64 r0 = r_begin + t * 128;
+                int len = (int)((r_end - r0) < 128 ? (r_end - r0) : 128);
+                for (int i = 0; i < len; ++i) {
+                    i64 r = r0 + i;
+                    if (mode == 0) {
+                        v[i] = bf16_to_f32(((const uint16_t*)src)[r * ld_src + c]);
+                    } else {
+                        uint8_t code = ((const uint8_t*)src)[r * ld_src + c];
+                        float s1 = src_sc[r * src_rs + (c / 128) * src_ts];
+                        v[i] = g_dec[code] * s1;
+                    }
+                }
+                float s = tile_scale(v, len);
+                scT[(pstart / 128 + t) * ldscT + c] = s;
+                uint8_t* dst = qT + c * ldqT + pstart + t * 128;
+                tile_encode(v, len, s, dst, 1);
+                for (int i = len; i < 128; ++i) dst[i] = 0x00;
+            }
+        }
+        pstart += ntiles * 128;
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Promoted block-scaled GEMM.                                               */
+/* ------------------------------------------------------------------------- */
+
+/* Exact partial sum of one K-block: sum of dec(a[k]) * dec(b[k]) for k in
+ * [k0, k1), accumulated in fp64 (exact for at most 128 E4M3 products). */
+static double block_partial(const uint8_t* a, i64 a_step, const uint8_t* b, i64 b_step,
+                            i64 k0, i64 k1)
+{
+    double p = 0.0;
+    for (i64 k = k0; k < k1; ++k)
+        p += (double)g_dec[a[k * a_step]] * (double)g_dec[b[k * b_step]];
+    return p;
+}
+
+/* Generic promoted dot product for one output element.
+ *   a[k * a_step], b[k * b_step] for k in [0, K): the E4M3 operand codes;
+ *   sa[blk * sa_step], sb[blk * sb_step]: the scales of K-block blk.
+ * acc = sum over blocks, in block order, of fp32(P_b) * fp32(s_a * s_b). */
+static float promoted_dot(const uint8_t* a, i64 a_step, const uint8_t* b, i64 b_step,
+                          i64 K, const float* sa, i64 sa_step, const float* sb, i64 sb_step)
+{
+    float acc = 0.0f;
+    i64 nb = (K + 127) / 128;
+    for (i64 blk = 0; blk < nb; ++blk) {
+        if (g_fault == FAULT_DROP_LAST_BLOCK && blk == nb - 1) break;
+        i64 k0 = blk * 128, k1 = (k0 + 128 < K) ? k0 + 128 : K;
+        double p = block_partial(a, a_step, b, b_step, k0, k1);
+        i64 bblk = (g_fault == FAULT_SCALE_NEXT_BLOCK) ? (blk + 1) % nb : blk;
+        float s = sa[blk * sa_step] * sb[bblk * sb_step];
+        float term = (float)p * s;
+        if (g_fault == FAULT_SIGN_FLIP_TERM && blk == 0 && nb > 1) term = -term;
+        acc = acc + term;
+    }
+    return acc;
+}
+
+/* Fprop, Y = X W:
+ *   Y[i,j] = sum_b s_x[i,b] * s_w[b, j/128] * P_b[i,j],
+ *   P_b[i,j] = sum_{k in block b} dec(xq[i,k]) * dec(wq[k,j]).
+ * xq: [M x K] row stride ldx; sx(i, b) = sx[i * sx_rs + b * sx_ts].
+ * wq: [K x N] row stride ldw; sw(bk, bn) = sw[bk * ldsw + bn].
+ * Output (fp32, before the BF16 rounding) for n_out elements at (ii[e], jj[e]),
+ * or the whole M x N row-major when ii is NULL. */
+void oracle_fprop(const uint8_t* xq, i64 ldx, const float* sx, i64 sx_rs, i64 sx_ts,
+                  const uint8_t* wq, i64 ldw, const float* sw, i64 ldsw,
+                  i64 M, i64 N, i64 K, const i64* ii, const i64* jj, i64 n_out,
+                  float* out)
+{
+    build_table();
+    i64 total = ii ? n_out : M * N;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (i64 e = 0; e < total; ++e) {
+        i64 i = ii ? ii[e] : e / N;
+        i64 j = ii ? jj[e] : e % N;
+        if (g_fault == FAULT_TRANSPOSED_W)   /* reads W[j, k]: only meaningful for K == N */
+            out[e] = promoted_dot(xq + i * ldx, 1, wq + j * ldw, 1, K,
+                                  sx + i * sx_rs, sx_ts, sw + (j / 128), ldsw);
+        else
+            out[e] = promoted_dot(xq + i * ldx, 1, wq + j, ldw, K,
+                                  sx + i * sx_rs, sx_ts, sw + (j / 128), ldsw);
+    }
+}
+
+/* Dgrad, dX = dY W^T (contraction over the N outputs of the layer):
+ *   dX[i,k] = sum_b s_dy[i,b] * s_w[k/128, b] * P_b[i,k],
+ *   P_b[i,k] = sum_{n in block b} dec(dyq[i,n]) * dec(wq[k,n]).
+ * dyq: [M x N] row stride lddy; sdy(i, b) = sdy[i * sdy_rs + b * sdy_ts].
+ * wq: [K x N] row stride ldw; sw(bk, bn) = sw[bk * ldsw + bn].
+ * Output index (i, k) over M x K. */
+void oracle_dgrad(const uint8_t* dyq, i64 lddy, const float* sdy, i64 sdy_rs, i64 sdy_ts,
+                  const uint8_t* wq, i64 ldw, const float* sw, i64 ldsw,
+                  i64 M, i64 N, i64 K, const i64* ii, const i64* kk, i64 n_out,
+                  float* out)
+{
+    build_table();
+    i64 total = ii ? n_out : M * K;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (i64 e = 0; e < total; ++e) {
+        i64 i = ii ? ii[e] : e / K;
+        i64 k = ii ? kk[e] : e % K;
+        out[e] = promoted_dot(dyq + i * lddy, 1, wq + k * ldw, 1, N,
+                              sdy + i * sdy_rs, sdy_ts, sw + (k / 128) * ldsw, 1);
+    }
+}
+
+/* Wgrad, dW = dY^T X (contraction over tokens), on the 128x1 re-tiled,
+ * transposed operands:
+ *   dW[n,k] = sum_b s_dyT[b,n] * s_xT[b,k] * P_b[n,k],
+ *   P_b[n,k] = sum_{t in block b} dec(dyqT[n,t]) * dec(xqT[k,t]).
+ * dyqT: [N x T] row stride lddyT, sdyT(b, n) = sdyT[b * ldsdyT + n].
+ * xqT:  [K x T] row stride ldxT,  sxT(b, k) = sxT[b * ldsxT + k].
+ * T is the (padded) token count. Output index (n, k) over N x K. */
+void oracle_wgrad(const uint8_t* dyqT, i64 lddyT, const float* sdyT, i64 ldsdyT,
+                  const uint8_t* xqT, i64 ldxT, const float* sxT, i64 ldsxT,
+                  i64 T, i64 N, i64 K, const i64* nn, const i64* kk, i64 n_out,
+                  float* out)
+{
+    build_table();
+    i64 total = nn ? n_out : N * K;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (i64 e = 0; e < total; ++e) {
+        i64 n = nn ? nn[e] : e / K;
+        i64 k = nn ? kk[e] : e % K;
+        out[e] = promoted_dot(dyqT + n * lddyT, 1, xqT + k * ldxT, 1, T,
+                              sdyT + n, ldsdyT, sxT + k, ldsxT);
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Reference sums for the pins: fp64 over dequantized operands, and the      */
+/* unpromoted low-precision accumulation of the drift model.                 */
+/* ------------------------------------------------------------------------- */
+
+/* Round v to m significant bits (m counts the leading bit). mode 0: nearest,
+ * ties to even; mode 1: toward zero. No exponent limit (a model of an
+ * accumulator's significand width only). */
+double oracle_round_sig(double v, int m, int mode)
+{
+    if (v == 0.0 || isnan(v) || isinf(v)) return v;
+    int e;
+    double f = frexp(v, &e);             /* v = f * 2^e, 0.5 <= |f| < 1 */
+    double scaled = ldexp(f, m);         /* |scaled| in [2^(m-1), 2^m) */
+    double r = (mode == 1) ? trunc(scaled) : nearbyint(scaled);
+    return ldexp(r, e - m);
+}
+
+/* Fprop element computed two more ways, for the pins:
+ *   out_fp64[e]  = sum_k (dec(xq)*s_x) * (dec(wq)*s_w) in fp64 (dequantized truth)
+ *   out_unpr[e]  = the drift model with an m-bit accumulator and no promotion:
+ *                  s_t = round(s_{t-1} + round(p_t)),
+ *                  p_t = dec(xq[i,t]) * dec(wq[t,j]) * (s_x * s_w)   (fp64).
+ * Same argument layout as oracle_fprop; element list is required. */
+void oracle_fprop_reference_sums(const uint8_t* xq, i64 ldx, const float* sx, i64 sx_rs, i64 sx_ts,
+                                 const uint8_t* wq, i64 ldw, const float* sw, i64 ldsw,
+                                 i64 K, const i64* ii, const i64* jj, i64 n_out,
+                                 int m_bits, int mode, double* out_fp64, double* out_unpr)
+{
+    build_table();
+#pragma omp parallel for schedule(dynamic, 1)
+    for (i64 e = 0; e < n_out; ++e) {
+        i64 i = ii[e], j = jj[e];
+        double truth = 0.0, acc = 0.0;
+        for (i64 k = 0; k < K; ++k) {
+            double a = (double)g_dec[xq[i * ldx + k]];
+            double b = (double)g_dec[wq[k * ldw + j]];
+            double s_a = (double)sx[i * sx_rs + (k / 128) * sx_ts];
+            double s_b = (double)sw[(k / 128) * ldsw + j / 128];
+            truth += (a * s_a) * (b * s_b);
+            if (out_unpr) {
+                double p = a * b * (double)((float)s_a * (float)s_b);
+                acc = oracle_round_sig(acc + oracle_round_sig(p, m_bits, mode), m_bits, mode);
+            }
+        }
+        out_fp64[e] = truth;
+        if (out_unpr) out_unpr[e] = acc;
+    }
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

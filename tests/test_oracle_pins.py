@@ -1,0 +1,530 @@
+"""Pins for the CPU oracle: checks against what the pages and the mathematics
+fix, never against the oracle's own formulas retyped.
+
+  - printed constants (tests/golden/page_constants.txt, each line cited);
+  - the E4M3 table against PyTorch's float8_e4m3fn decoding (a library
+    implementation of the OCP format) and against its structure;
+  - the encoder against hand-worked OCP cases (tests/golden), a brute-force
+    nearest search over all BF16 inputs, and PyTorch's float8 cast;
+  - the quantizers against the same steps written with torch CPU ops and the
+    library cast, plus invariants that hold for any input;
+  - the transposed requant against closed-form identities;
+  - the promoted GEMMs against fp64 matmuls of the dequantized operands
+    within the fp32 rounding bound, and an exact single-block case;
+  - the drift behaviour of the partial-sum page (unpromoted error grows with
+    K, promoted error stays flat);
+  - negative controls: a planted mistake in the oracle makes a pin fail.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    rows = []
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.split("#")[0].strip()
+        if line:
+            rows.append(line.split())
+    return rows
+
+
+def _f(s):
+    return float.fromhex(s) if "p" in s else float(s)
+
+
+def _torch_e4m3_values():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(torch.float8_e4m3fn).to(torch.float32).numpy()
+
+
+def _torch_cast_codes(v_f32):
+    t = torch.from_numpy(np.ascontiguousarray(v_f32, np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+# ---------------------------------------------------------------------------
+# E4M3 table and encoder
+# ---------------------------------------------------------------------------
+
+def test_page_constants():
+    c = {r[0]: r[1] for r in _golden("page_constants.txt")}
+    t = oracle.e4m3_table()
+    finite = t[~np.isnan(t)]
+    assert float(c["e4m3_max"]) == 448.0
+    assert finite.max() == 448.0 and t[0x7E] == 448.0 and t[0xFE] == -448.0
+    pz, nz = int(c["pos_zero_byte"], 16), int(c["neg_zero_byte"], 16)
+    assert t[pz] == 0.0 and not np.signbit(t[pz])
+    assert t[nz] == 0.0 and np.signbit(t[nz])
+    assert oracle.e4m3_encode(0.0) == pz and oracle.e4m3_encode(-0.0) == nz
+    n_c = int(c["n_c"])
+    assert n_c == 128
+    # tile geometry: number of scales per tiling
+    for (R, C) in [(1, 1), (5, 300), (128, 128), (129, 257), (300, 16)]:
+        x = np.zeros((R, C), np.uint16)
+        _, s1 = oracle.quant_1x128(x, sc_layout="row_major")
+        assert s1.shape == (R, -(-C // n_c))
+        _, s2 = oracle.quant_128x128(x)
+        assert s2.shape == (-(-R // n_c), -(-C // n_c))
+        _, s3 = oracle.requant_128x1_T(x)
+        assert s3.shape == (-(-R // n_c), C)
+    assert c["act_tile"] == "1x128" and c["weight_tile"] == "128x128" and c["wgrad_tile"] == "128x1"
+
+
+def test_table_matches_torch_float8():
+    ours = oracle.e4m3_table()
+    ref = _torch_e4m3_values()
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(ours[fin].view(np.uint32), ref[fin].view(np.uint32))
+
+
+def test_table_structure():
+    t = oracle.e4m3_table()
+    assert np.isnan(t[0x7F]) and np.isnan(t[0xFF])
+    assert np.count_nonzero(~np.isnan(t)) == 254
+    pos = t[:0x7F]
+    assert np.all(np.diff(pos) > 0)                      # monotone over positive codes
+    assert np.array_equal(t[0x80:0xFF], -t[:0x7F])       # sign-magnitude
+    assert t[0x01] == 2.0 ** -9 and t[0x08] == 2.0 ** -6  # smallest subnormal / normal
+    assert t[0x07] == 7 * 2.0 ** -9
+
+
+def test_encoder_golden_cases():
+    for v, code in _golden("e4m3_rounding_cases.txt"):
+        assert oracle.e4m3_encode(_f(v)) == int(code, 16), v
+
+
+def test_encoder_roundtrip():
+    t = oracle.e4m3_table()
+    for c in range(256):
+        if not np.isnan(t[c]):
+            assert oracle.e4m3_encode(t[c]) == c
+
+
+def _bruteforce_encode(v):
+    """Nearest finite E4M3 by exhaustive search (ties to the even code),
+    saturating, zero keeps the sign. Independent of the oracle's bisection."""
+    t = _torch_e4m3_values().astype(np.float64)
+    pos_codes = np.arange(0x7F)
+    vals = t[pos_codes]
+    a = np.abs(v.astype(np.float64))
+    d = np.abs(a[:, None] - vals[None, :])
+    best = d.min(axis=1, keepdims=True)
+    cand = d == best
+    even = cand & (pos_codes[None, :] % 2 == 0)
+    pick = np.where(even.any(axis=1), even.argmax(axis=1), cand.argmax(axis=1))
+    pick = np.where(a >= 448.0, 0x7E, pick)
+    return (pick | np.where(np.signbit(v), 0x80, 0)).astype(np.uint8)
+
+
+def test_encoder_bruteforce_all_bf16():
+    h = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    v = oracle.bf16_to_f32(h)
+    v = v[np.isfinite(v)]
+    ours = oracle.e4m3_encode_array(v)
+    for chunk in range(0, v.size, 8192):
+        sl = slice(chunk, chunk + 8192)
+        assert np.array_equal(ours[sl], _bruteforce_encode(v[sl]))
+
+
+def test_encoder_matches_torch_cast_fp32():
+    g = np.random.default_rng(1)
+    # random fp32 bit patterns over the E4M3 range plus midpoints
+    mags = np.exp2(g.uniform(-12, np.log2(460), 400000)).astype(np.float32)
+    t = _torch_e4m3_values()
+    fin = t[:0x7E]
+    mids = ((fin[:-1].astype(np.float64) + fin[1:]) / 2).astype(np.float32)
+    v = np.concatenate([mags, -mags, mids, -mids,
+                        np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(1e9))])
+    v = v[np.abs(v) < 464.0]  # torch's cast is not saturating beyond
+    assert np.array_equal(oracle.e4m3_encode_array(v), _torch_cast_codes(v))
+
+
+def test_bf16_rounding_matches_torch():
+    g = np.random.default_rng(2)
+    v = np.concatenate([g.standard_normal(100000).astype(np.float32) * 1e3,
+                        np.array([0.0, -0.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 3.4e38], np.float32)])
+    ours = oracle.f32_to_bf16(v)
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+# ---------------------------------------------------------------------------
+# Quantizers
+# ---------------------------------------------------------------------------
+
+def _tile_inputs(R, C, seed):
+    """N(0,1) BF16 with outliers, an all-zero tile, a tile of tiny negatives,
+    and a tile whose absmax element is negative."""
+    x = wl.with_outliers((R, C), fraction=0.01, seed=seed)
+    x[0, :128] = 0.0
+    if R > 1:
+        x[1, :128] = -1e-30
+        x[1, 0] = 1.0
+    if R > 2:
+        x[2, :128] = torch.linspace(-300.0, 2.0, 128).to(torch.bfloat16)
+    return wl.bits(x)
+
+
+def _torch_quant_rows(v):
+    """Reference steps with torch CPU ops: amax, s = amax / 448 (fp32 div),
+    q = float8_e4m3fn cast of fp32(v / s)."""
+    t = torch.from_numpy(v)
+    amax = t.abs().amax(dim=-1, keepdim=True)
+    s = torch.where(amax == 0, torch.ones_like(amax), amax / torch.tensor(448.0))
+    q = (t / s).to(torch.float8_e4m3fn).view(torch.uint8)
+    return q.numpy(), s.squeeze(-1).numpy()
+
+
+def test_quant_1x128_matches_torch_steps():
+    R, C = 37, 128 * 5
+    x = _tile_inputs(R, C, seed=3)
+    q, sc = oracle.quant_1x128(x, sc_layout="row_major")
+    v = oracle.bf16_to_f32(x).reshape(R, C // 128, 128)
+    qr, sr = _torch_quant_rows(v)
+    assert np.array_equal(q.reshape(R, C // 128, 128), qr)
+    assert np.array_equal(sc.view(np.uint32), sr.view(np.uint32))
+    # the tile-major layout holds the same numbers, row index contiguous
+    q2, sc2 = oracle.quant_1x128(x)
+    assert np.array_equal(q2, q)
+    assert sc2.shape == (C // 128, 40)
+    assert np.array_equal(sc2[:, :R].T, sc) and np.all(sc2[:, R:] == 0)
+
+
+def test_quant_1x128_ragged_last_tile():
+    R, C = 9, 128 * 2 + 48
+    x = _tile_inputs(R, C, seed=4)
+    q, sc = oracle.quant_1x128(x, sc_layout="row_major")
+    v = oracle.bf16_to_f32(x)
+    qr, sr = _torch_quant_rows(np.ascontiguousarray(v[:, 256:]))
+    assert np.array_equal(q[:, 256:], qr)
+    assert np.array_equal(sc[:, 2], sr)
+
+
+def test_quant_128x128_matches_torch_steps():
+    R, C = 256 + 40, 384
+    x = _tile_inputs(R, C, seed=5)
+    q, sc = oracle.quant_128x128(x)
+    v = oracle.bf16_to_f32(x)
+    for bi in range(sc.shape[0]):
+        for bj in range(sc.shape[1]):
+            blk = np.ascontiguousarray(v[bi * 128:(bi + 1) * 128, bj * 128:(bj + 1) * 128])
+            qr, sr = _torch_quant_rows(blk.reshape(1, -1))
+            assert sc[bi, bj] == sr[0]
+            assert np.array_equal(q[bi * 128:(bi + 1) * 128, bj * 128:(bj + 1) * 128].ravel(), qr[0])
+
+
+def test_quant_invariants():
+    R, C = 64, 128 * 4
+    x = _tile_inputs(R, C, seed=6)
+    q, sc = oracle.quant_1x128(x, sc_layout="row_major")
+    t = oracle.e4m3_table()
+    v = oracle.bf16_to_f32(x).reshape(R, -1, 128)
+    dq = t[q].reshape(R, -1, 128)
+    assert np.all(np.abs(dq) <= 448.0)
+    nz = np.abs(v).max(-1) > 0
+    # zero tiles: s = 1, signed zeros
+    assert np.all(sc[~nz] == 1.0)
+    zq = q.reshape(R, -1, 128)[~nz]
+    zv = v[~nz]
+    assert np.array_equal(zq, np.where(np.signbit(zv), 0x80, 0x00).astype(np.uint8))
+    # the absmax element of each non-zero tile encodes to +-448
+    idx = np.abs(v).argmax(-1)
+    top = np.take_along_axis(dq, idx[..., None], -1)[..., 0]
+    normal = sc >= np.finfo(np.float32).tiny
+    assert np.all(np.abs(top[nz & normal]) == 448.0)
+    # relative error of each element within half an E4M3 step (2^-4) in the normal range
+    quot = v / sc[..., None]
+    sel = np.abs(quot) >= 2.0 ** -6
+    assert np.all(np.abs(dq[sel] - quot[sel]) <= 2.0 ** -4 * np.abs(quot[sel]))
+    # signs agree (including zeros)
+    assert np.array_equal(np.signbit(dq), np.signbit(v))
+
+
+def test_quant_reciprocal_case_is_distinguished():
+    """A tile where v * (1/s) and v / s round to different E4M3 codes: the
+    torch-steps pin must see the true division."""
+    v = _find_reciprocal_mismatch()
+    x = oracle.f32_to_bf16(v.reshape(1, 128))
+    q, sc = oracle.quant_1x128(x, sc_layout="row_major")
+    qr, sr = _torch_quant_rows(oracle.bf16_to_f32(x))
+    assert np.array_equal(q, qr) and sc[0, 0] == sr[0]
+
+
+def _find_reciprocal_mismatch():
+    """Search bf16 tiles (amax and one probe value) until fp32 division and
+    multiplication by the fp32 reciprocal give different E4M3 codes."""
+    g = np.random.default_rng(7)
+    amaxes = oracle.bf16_to_f32(oracle.f32_to_bf16(g.uniform(1.0, 1000.0, 4000).astype(np.float32)))
+    probes = oracle.bf16_to_f32(np.arange(0x3C00, 0x4400, dtype=np.uint16))
+    for a in amaxes:
+        s = np.float32(a) / np.float32(448.0)
+        d = _torch_cast_codes(probes / s)
+        m = _torch_cast_codes(probes * (np.float32(1.0) / s))
+        bad = np.nonzero(d != m)[0]
+        if bad.size:
+            v = np.zeros(128, np.float32)
+            v[0] = a
+            v[1] = probes[bad[0]]
+            return v
+    raise AssertionError("no mismatching case found")
+
+
+def test_requant_mode_b_is_1x128_of_transpose():
+    """128x1 tiles of X along tokens = 1x128 tiles of X^T along its rows."""
+    M, C = 300, 200
+    x = _tile_inputs(M, C, seed=8)
+    qT, scT = oracle.requant_128x1_T(x)
+    q1, s1 = oracle.quant_1x128(np.ascontiguousarray(x.T), sc_layout="row_major")
+    mp = oracle.padded_tokens(M)
+    assert qT.shape == (C, mp) and scT.shape == (mp // 128, C)
+    assert np.array_equal(qT[:, :M], q1)
+    assert np.all(qT[:, M:] == 0)
+    assert np.array_equal(scT.T, s1)
+
+
+def test_requant_mode_q_power_of_two_is_transpose():
+    """If a 128x128 block's 1x128 scales are one power of two and every token
+    column holds a +-448 code, the 128x1 requant keeps the scale and the
+    payload is the byte transpose."""
+    g = np.random.default_rng(9)
+    M, C = 256, 256
+    t = oracle.e4m3_table()
+    fin = np.nonzero(~np.isnan(t))[0]
+    q = g.choice(fin, size=(M, C)).astype(np.uint8)
+    for tile in range(M // 128):
+        rows = tile * 128 + g.integers(0, 128, size=C)
+        q[rows, np.arange(C)] = np.where(g.random(C) < 0.5, 0x7E, 0xFE)
+    s = np.float32(2.0 ** -7)
+    sc = np.full((C // 128, M), s, np.float32)
+    qT, scT = oracle.requant_128x1_T(q, sc)
+    assert np.all(scT == s)
+    assert np.array_equal(qT, q.T)
+
+
+def test_requant_groups_geometry_and_padding():
+    M, C = 400, 128
+    counts = [0, 129, 1, 0, 270]
+    off = wl.offsets_from_counts(counts)
+    x = _tile_inputs(M, C, seed=10)
+    qT, scT = oracle.requant_128x1_T(x, offsets=off)
+    mp = sum(-(-n // 128) * 128 for n in counts)
+    assert qT.shape == (C, mp) and scT.shape == (mp // 128, C)
+    p = 0
+    for e, n in enumerate(counts):
+        if n == 0:
+            continue
+        seg = np.ascontiguousarray(x[off[e]:off[e + 1]])
+        qe, se = oracle.requant_128x1_T(seg)
+        w = qe.shape[1]
+        assert np.array_equal(qT[:, p:p + w], qe)
+        assert np.array_equal(scT[p // 128:(p + w) // 128], se)
+        p += w
+
+
+# ---------------------------------------------------------------------------
+# Promoted GEMMs against fp64 of the dequantized operands
+# ---------------------------------------------------------------------------
+
+def _deq_rows(q, sc_row_major, tile_axis_len=128):
+    t = oracle.e4m3_table().astype(np.float64)
+    v = t[q]
+    s = np.repeat(sc_row_major.astype(np.float64), tile_axis_len, axis=1)[:, :q.shape[1]]
+    return v * s
+
+
+def _deq_blocks(q, sc):
+    t = oracle.e4m3_table().astype(np.float64)
+    s = np.repeat(np.repeat(sc.astype(np.float64), 128, 0), 128, 1)[:q.shape[0], :q.shape[1]]
+    return t[q] * s
+
+
+def _bound(absprod, nblocks):
+    return (nblocks + 3) * 2.0 ** -23 * absprod + 1e-30
+
+
+def _fprop_case(M, K, N, seed):
+    x = _tile_inputs(M, K, seed)
+    w = wl.bits(wl.normal((K, N), std=0.02, seed=seed + 50))
+    xq, sx = oracle.quant_1x128(x)
+    wq, sw = oracle.quant_128x128(w)
+    return xq, sx, wq, sw
+
+
+def _check_fprop(M, K, N, seed):
+    xq, sx, wq, sw = _fprop_case(M, K, N, seed)
+    y = oracle.fprop(xq, sx, wq, sw)
+    a = _deq_rows(xq, np.ascontiguousarray(sx[:, :M].T))
+    b = _deq_blocks(wq, sw)
+    ref = a @ b
+    absprod = np.abs(a) @ np.abs(b)
+    return np.all(np.abs(y - ref) <= _bound(absprod, -(-K // 128)))
+
+
+@pytest.mark.parametrize("M,K,N", [(3, 128, 128), (130, 384, 256), (64, 200, 136)])
+def test_fprop_vs_fp64_dequantized(M, K, N):
+    assert _check_fprop(M, K, N, seed=11)
+
+
+def _check_dgrad(M, N, K, seed):
+    dy = _tile_inputs(M, N, seed)
+    w = wl.bits(wl.normal((K, N), std=0.02, seed=seed + 60))
+    dyq, sdy = oracle.quant_1x128(dy)
+    wq, sw = oracle.quant_128x128(w)
+    dx = oracle.dgrad(dyq, sdy, wq, sw)
+    a = _deq_rows(dyq, np.ascontiguousarray(sdy[:, :M].T))
+    b = _deq_blocks(wq, sw)
+    ref = a @ b.T
+    absprod = np.abs(a) @ np.abs(b).T
+    return np.all(np.abs(dx - ref) <= _bound(absprod, -(-N // 128)))
+
+
+@pytest.mark.parametrize("M,N,K", [(5, 256, 128), (129, 384, 256)])
+def test_dgrad_vs_fp64_dequantized(M, N, K):
+    assert _check_dgrad(M, N, K, seed=12)
+
+
+def _check_wgrad(T, N, K, seed):
+    dy = _tile_inputs(T, N, seed)
+    x = _tile_inputs(T, K, seed + 1)
+    dyqT, sdyT = oracle.requant_128x1_T(dy)
+    xqT, sxT = oracle.requant_128x1_T(x)
+    dw = oracle.wgrad(dyqT, sdyT, xqT, sxT)
+    t = oracle.e4m3_table().astype(np.float64)
+    a = t[dyqT] * np.repeat(sdyT.T.astype(np.float64), 128, axis=1)   # [N x Tpad]
+    b = t[xqT] * np.repeat(sxT.T.astype(np.float64), 128, axis=1)     # [K x Tpad]
+    ref = a @ b.T
+    absprod = np.abs(a) @ np.abs(b).T
+    return np.all(np.abs(dw - ref) <= _bound(absprod, dyqT.shape[1] // 128))
+
+
+@pytest.mark.parametrize("T,N,K", [(128, 128, 256), (300, 256, 128)])
+def test_wgrad_vs_fp64_dequantized(T, N, K):
+    assert _check_wgrad(T, N, K, seed=13)
+
+
+def test_single_block_reduces_to_plain_dot():
+    """One K-block with unit scales: the promoted GEMM is the plain dot
+    product of the decoded codes, which is exact in fp32 here."""
+    g = np.random.default_rng(14)
+    t = oracle.e4m3_table()
+    small = np.nonzero((~np.isnan(t)) & (np.abs(t) <= 4) & (np.abs(t) >= 2 ** -3))[0]
+    xq = g.choice(small, size=(8, 128)).astype(np.uint8)
+    wq = g.choice(small, size=(128, 16)).astype(np.uint8)
+    sx = np.ones((1, 8), np.float32)
+    sw = np.ones((1, 1), np.float32)
+    y = oracle.fprop(xq, sx, wq, sw)
+    ref = t[xq].astype(np.float64) @ t[wq].astype(np.float64)
+    assert np.array_equal(y, ref.astype(np.float32))
+
+
+def test_fprop_sampled_elements_match_full():
+    xq, sx, wq, sw = _fprop_case(70, 256, 256, seed=15)
+    full = oracle.fprop(xq, sx, wq, sw)
+    ii = np.array([0, 69, 33, 5]); jj = np.array([255, 0, 128, 17])
+    assert np.array_equal(oracle.fprop(xq, sx, wq, sw, ii, jj), full[ii, jj])
+
+
+def test_grouped_fprop_is_per_expert_dense():
+    counts = [3, 0, 130]
+    off = wl.offsets_from_counts(counts)
+    M, K, N = sum(counts), 256, 128
+    x = _tile_inputs(M, K, 16)
+    xq, sx = oracle.quant_1x128(x)
+    ws = [oracle.quant_128x128(wl.bits(wl.normal((K, N), 0.02, seed=17 + e))) for e in range(3)]
+    wq = np.stack([w[0] for w in ws]); sw = np.stack([w[1] for w in ws])
+    y = oracle.grouped_fprop(xq, sx, wq, sw, off)
+    for e in range(3):
+        r0, r1 = off[e], off[e + 1]
+        if r1 > r0:
+            a = _deq_rows(xq[r0:r1], np.ascontiguousarray(sx[:, r0:r1].T))
+            ref = a @ _deq_blocks(wq[e], sw[e])
+            assert np.allclose(y[r0:r1], ref, rtol=1e-5, atol=1e-6)
+
+
+# ---------------------------------------------------------------------------
+# Drift (partial-sum page, sections 2, 4 and 5)
+# ---------------------------------------------------------------------------
+
+def test_round_sig_closed_forms():
+    assert oracle.round_sig(1.0 + 2 ** -20, 14) == 1.0
+    assert oracle.round_sig(1.0 + 3 * 2 ** -14, 14) == 1.0 + 4 * 2 ** -14   # tie to even
+    assert oracle.round_sig(1.0 + 2 ** -14, 14) == 1.0                      # tie to even
+    assert oracle.round_sig(1.999, 8, mode=1) == 1.9921875                  # toward zero
+    assert oracle.round_sig(-3.0, 1) == -4.0
+
+
+@pytest.mark.slow
+def test_drift_grows_with_k_only_without_promotion():
+    promoted, unpromoted = [], []
+    ii = np.arange(8) * 31 % 256
+    jj = np.arange(8) * 17 % 256
+    for K in wl.LONGK_VALUES:
+        d = wl.longk(K)
+        xq, sx = oracle.quant_1x128(wl.bits(d["X"]))
+        wq, sw = oracle.quant_128x128(wl.bits(d["W"]))
+        y = oracle.fprop(xq, sx, wq, sw, ii, jj).astype(np.float64)
+        truth, unpr = oracle.fprop_reference_sums(xq, sx, wq, sw, ii, jj, m_bits=14)
+        promoted.append(np.max(np.abs(y - truth) / np.abs(truth)))
+        unpromoted.append(np.max(np.abs(unpr - truth) / np.abs(truth)))
+    promoted, unpromoted = np.array(promoted), np.array(unpromoted)
+    assert np.all(promoted < 1e-6)                   # bounded by fp32 rounding
+    assert np.all(np.diff(unpromoted) > 0)           # grows with K
+    assert unpromoted[-1] > 1e-2                     # stagnation at K = 65536
+    ratio = unpromoted / np.maximum(promoted, 1e-12)
+    assert np.all(np.diff(ratio) > 0)
+
+
+# ---------------------------------------------------------------------------
+# Negative controls: each planted mistake must make a pin fail
+# ---------------------------------------------------------------------------
+
+def _pin_encoder():
+    try:
+        test_encoder_golden_cases()
+        return True
+    except AssertionError:
+        return False
+
+
+def _pin_quant():
+    try:
+        test_quant_1x128_matches_torch_steps()
+        test_quant_reciprocal_case_is_distinguished()
+        return True
+    except AssertionError:
+        return False
+
+
+def _pin_gemm():
+    return (_check_fprop(130, 384, 256, 21) and _check_dgrad(129, 384, 256, 22)
+            and _check_wgrad(300, 256, 128, 23) and _check_fprop(64, 256, 256, 24))
+
+
+@pytest.mark.parametrize("fault,pin", [
+    (oracle.FAULT_DROP_LAST_BLOCK, "gemm"),
+    (oracle.FAULT_SCALE_NEXT_BLOCK, "gemm"),
+    (oracle.FAULT_TIES_AWAY, "encoder"),
+    (oracle.FAULT_SIGNED_AMAX, "quant"),
+    (oracle.FAULT_TRANSPOSED_W, "gemm"),
+    (oracle.FAULT_DROP_NEG_ZERO, "encoder"),
+    (oracle.FAULT_RECIPROCAL, "quant"),
+    (oracle.FAULT_SIGN_FLIP_TERM, "gemm"),
+])
+def test_planted_mistake_is_caught(fault, pin):
+    check = {"encoder": _pin_encoder, "quant": _pin_quant, "gemm": _pin_gemm}[pin]
+    assert check()
+    oracle.set_fault(fault)
+    try:
+        assert not check()
+    finally:
+        oracle.set_fault(oracle.FAULT_NONE)
+    assert check()
