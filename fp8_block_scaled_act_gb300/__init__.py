@@ -1,0 +1,304 @@
+"""GB300 (sm_103a) fine-grained FP8 linear layer: Python binding of libfp8bs.
+
+Thin ctypes binding of the C ABI declared in ``include/fp8bs.h``. Each function
+has the name of its C entry point and only marshals arguments: torch tensors
+supply device pointers and sizes, the current torch CUDA stream supplies the
+stream, and every step of the computation runs in the library's CUDA
+kernels. There is no fallback: if ``libfp8bs.so`` is missing or fails to load,
+every call raises.
+
+PyTorch is used here for device memory and streams only. Allocation helpers
+(``empty_*``) return correctly shaped output tensors for each entry point.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import _build_lib
+
+__all__ = [
+    "Fp8bsError", "build", "lib", "lib_path",
+    "fp8_quant_1x128", "fp8_quant_128x128", "fp8_requant_128x1_T",
+    "fp8_block_gemm_fprop", "fp8_block_gemm_dgrad", "fp8_block_gemm_wgrad",
+    "fp8_block_gemm_grouped", "fp8bs_device_status", "fp8bs_set_wait_limit_ns",
+    "fp8bs_selftest_wait_timeout", "fp8bs_scale_ld", "fp8bs_padded_tokens",
+    "fp8bs_status_str", "fp8bs_version",
+    "empty_quant_1x128", "empty_quant_128x128", "empty_requant_128x1_T",
+    "SRC_BF16", "SRC_E4M3", "OP_FPROP", "OP_DGRAD", "OP_WGRAD", "MAX_GROUPS",
+]
+
+SRC_BF16, SRC_E4M3 = 0, 1
+OP_FPROP, OP_DGRAD, OP_WGRAD = 0, 1, 2
+MAX_GROUPS = 256
+STATUS_NAMES = {0: "OK", 1: "ERR_ARG", 2: "ERR_ALIGN", 3: "ERR_SHAPE", 4: "ERR_LAUNCH",
+                5: "ERR_TIMEOUT", 6: "ERR_UNSUPPORTED", 7: "ERR_DEVICE"}
+
+_lib = None
+
+
+class Fp8bsError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = int(code)
+        super().__init__(f"{fn}: {STATUS_NAMES.get(self.code, self.code)}")
+
+
+def lib_path() -> str:
+    return _build_lib.LIB
+
+
+def build(force: bool = False) -> str:
+    """Compile libfp8bs.so for sm_103a (nvcc) if its sources changed."""
+    return _build_lib.build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library. Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libfp8bs.so not found at {path}: run "
+                           "fp8_block_scaled_act_gb300.build() (nvcc, sm_103a) first")
+    L = ctypes.CDLL(path)
+    P, I64, I32, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int
+    S = ctypes.c_int
+    sigs = {
+        "fp8bs_status_str": ([S], ctypes.c_char_p),
+        "fp8bs_version": ([], I),
+        "fp8bs_scale_ld": ([I64], I64),
+        "fp8bs_padded_tokens": ([I64, P, I32], I64),
+        "fp8_quant_1x128": ([P, I64, I64, I64, P, P, P], S),
+        "fp8_quant_128x128": ([P, I64, I64, I64, I64, P, P, P, P], S),
+        "fp8_requant_128x1_T": ([I, P, P, I64, I64, P, I32, P, P, P], S),
+        "fp8_block_gemm_fprop": ([P, P, P, P, I64, I64, I64, P, P], S),
+        "fp8_block_gemm_dgrad": ([P, P, P, P, I64, I64, I64, P, P], S),
+        "fp8_block_gemm_wgrad": ([P, P, P, P, I64, I64, I64, P, I, P], S),
+        "fp8_block_gemm_grouped": ([I, I32, P, P, P, P, P, I64, I64, P, I, P], S),
+        "fp8bs_device_status": ([I], S),
+        "fp8bs_set_wait_limit_ns": ([ctypes.c_uint64], None),
+        "fp8bs_selftest_wait_timeout": ([ctypes.c_uint64, P], S),
+    }
+    for name, (args, res) in sigs.items():
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = res
+    _lib = L
+    return L
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(name: str, code: int) -> None:
+    if code != 0:
+        raise Fp8bsError(name, code)
+
+
+def _need(t: torch.Tensor, dtype, name: str):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _offsets_host(offsets) -> np.ndarray:
+    if isinstance(offsets, torch.Tensor):
+        offsets = offsets.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(offsets, dtype=np.int32))
+
+
+# ---------------------------------------------------------------------------
+# helpers without device work
+# ---------------------------------------------------------------------------
+
+def fp8bs_status_str(code: int) -> str:
+    return lib().fp8bs_status_str(int(code)).decode()
+
+
+def fp8bs_version() -> int:
+    return int(lib().fp8bs_version())
+
+
+def fp8bs_scale_ld(rows: int) -> int:
+    return int(lib().fp8bs_scale_ld(int(rows)))
+
+
+def fp8bs_padded_tokens(rows: int, offsets: Optional[Sequence[int]] = None) -> int:
+    if offsets is None:
+        return int(lib().fp8bs_padded_tokens(int(rows), None, 0))
+    off = _offsets_host(offsets)
+    v = int(lib().fp8bs_padded_tokens(int(rows), off.ctypes.data_as(ctypes.c_void_p), off.size - 1))
+    if v < 0:
+        raise ValueError("invalid group offsets")
+    return v
+
+
+def empty_quant_1x128(rows: int, cols: int, device="cuda"):
+    """(q uint8 [rows x cols], scales float32 [ceil(cols/128) x scale_ld(rows)])."""
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=device)
+    sc = torch.empty(((cols + 127) // 128, max(fp8bs_scale_ld(rows), 0)), dtype=torch.float32,
+                     device=device)
+    return q, sc
+
+
+def empty_quant_128x128(rows: int, cols: int, batch: int = 1, with_transpose: bool = True,
+                        device="cuda"):
+    """(q [batch x rows x cols], qT [batch x cols x rows] or None, scales
+    [batch x ceil(rows/128) x ceil(cols/128)]); the batch dim is dropped when batch == 1."""
+    shp = (batch,) if batch > 1 else ()
+    q = torch.empty(shp + (rows, cols), dtype=torch.uint8, device=device)
+    qT = torch.empty(shp + (cols, rows), dtype=torch.uint8, device=device) if with_transpose else None
+    sc = torch.empty(shp + ((rows + 127) // 128, (cols + 127) // 128), dtype=torch.float32,
+                     device=device)
+    return q, qT, sc
+
+
+def empty_requant_128x1_T(rows: int, cols: int, offsets=None, device="cuda"):
+    """(qT uint8 [cols x Mpad], scalesT float32 [Mpad/128 x cols])."""
+    mp = fp8bs_padded_tokens(rows, offsets)
+    qT = torch.empty((cols, mp), dtype=torch.uint8, device=device)
+    sc = torch.empty((mp // 128, cols), dtype=torch.float32, device=device)
+    return qT, sc
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+
+def fp8_quant_1x128(x: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, stream=None) -> None:
+    """1x128 absmax quantization of BF16 x [rows x cols] into q / scales."""
+    _need(x, torch.bfloat16, "x"); _need(q, torch.uint8, "q"); _need(scales, torch.float32, "scales")
+    rows, cols = x.shape
+    if q.shape != (rows, cols) or scales.shape != ((cols + 127) // 128, fp8bs_scale_ld(rows)):
+        raise ValueError("output shapes do not match empty_quant_1x128")
+    _check("fp8_quant_1x128", lib().fp8_quant_1x128(_ptr(x), rows, cols, cols, _ptr(q),
+                                                    _ptr(scales), _stream(stream)))
+
+
+def fp8_quant_128x128(w: torch.Tensor, q: torch.Tensor, qT: Optional[torch.Tensor],
+                      scales: torch.Tensor, stream=None) -> None:
+    """128x128 absmax quantization of BF16 w [rows x cols] (or [batch x rows x cols])."""
+    _need(w, torch.bfloat16, "w"); _need(q, torch.uint8, "q"); _need(scales, torch.float32, "scales")
+    if qT is not None:
+        _need(qT, torch.uint8, "qT")
+    batch = w.shape[0] if w.dim() == 3 else 1
+    rows, cols = w.shape[-2:]
+    if q.shape != w.shape or (qT is not None and qT.shape[-2:] != (cols, rows)):
+        raise ValueError("output shapes do not match empty_quant_128x128")
+    _check("fp8_quant_128x128", lib().fp8_quant_128x128(_ptr(w), batch, rows, cols, cols, _ptr(q),
+                                                        _ptr(qT), _ptr(scales), _stream(stream)))
+
+
+def fp8_requant_128x1_T(src: torch.Tensor, src_scales: Optional[torch.Tensor], qT: torch.Tensor,
+                        scalesT: torch.Tensor, offsets=None, stream=None) -> None:
+    """128x1 transposed requantization. src BF16 (mode B) or uint8 E4M3 with
+    its 1x128 scales (mode Q); optional host group offsets."""
+    if src.dtype == torch.bfloat16:
+        mode = SRC_BF16
+        _need(src, torch.bfloat16, "src")
+    else:
+        mode = SRC_E4M3
+        _need(src, torch.uint8, "src"); _need(src_scales, torch.float32, "src_scales")
+    _need(qT, torch.uint8, "qT"); _need(scalesT, torch.float32, "scalesT")
+    rows, cols = src.shape
+    if offsets is not None:
+        off = _offsets_host(offsets)
+        optr, groups = off.ctypes.data_as(ctypes.c_void_p), off.size - 1
+    else:
+        off, optr, groups = None, None, 0
+    mp = fp8bs_padded_tokens(rows, offsets)
+    if qT.shape != (cols, mp) or scalesT.shape != (mp // 128, cols):
+        raise ValueError("output shapes do not match empty_requant_128x1_T")
+    _check("fp8_requant_128x1_T", lib().fp8_requant_128x1_T(
+        mode, _ptr(src), _ptr(src_scales if mode == SRC_E4M3 else None), rows, cols, optr, groups,
+        _ptr(qT), _ptr(scalesT), _stream(stream)))
+
+
+def fp8_block_gemm_fprop(xq, sx, wqT, sw, y, stream=None) -> None:
+    """Y[M x N] (BF16) = X W from xq [M x K], sx, wqT [N x K], sw [K/128 x N/128]."""
+    for t, n, d in ((xq, "xq", torch.uint8), (sx, "sx", torch.float32), (wqT, "wqT", torch.uint8),
+                    (sw, "sw", torch.float32), (y, "y", torch.bfloat16)):
+        _need(t, d, n)
+    M, K = xq.shape
+    N = wqT.shape[0]
+    if wqT.shape != (N, K) or y.shape != (M, N):
+        raise ValueError("shape mismatch")
+    _check("fp8_block_gemm_fprop", lib().fp8_block_gemm_fprop(
+        _ptr(xq), _ptr(sx), _ptr(wqT), _ptr(sw), M, N, K, _ptr(y), _stream(stream)))
+
+
+def fp8_block_gemm_dgrad(dyq, sdy, wq, sw, dx, stream=None) -> None:
+    """dX[M x K] (BF16) = dY W^T from dyq [M x N], sdy, wq [K x N], sw."""
+    for t, n, d in ((dyq, "dyq", torch.uint8), (sdy, "sdy", torch.float32), (wq, "wq", torch.uint8),
+                    (sw, "sw", torch.float32), (dx, "dx", torch.bfloat16)):
+        _need(t, d, n)
+    M, N = dyq.shape
+    K = wq.shape[0]
+    if wq.shape != (K, N) or dx.shape != (M, K):
+        raise ValueError("shape mismatch")
+    _check("fp8_block_gemm_dgrad", lib().fp8_block_gemm_dgrad(
+        _ptr(dyq), _ptr(sdy), _ptr(wq), _ptr(sw), M, N, K, _ptr(dx), _stream(stream)))
+
+
+def fp8_block_gemm_wgrad(dyqT, sdyT, xqT, sxT, dw, accumulate: bool = False, stream=None) -> None:
+    """dW[N x K] (FP32) = dY^T X from dyqT [N x T], sdyT [T/128 x N], xqT [K x T], sxT [T/128 x K]."""
+    for t, n, d in ((dyqT, "dyqT", torch.uint8), (sdyT, "sdyT", torch.float32),
+                    (xqT, "xqT", torch.uint8), (sxT, "sxT", torch.float32), (dw, "dw", torch.float32)):
+        _need(t, d, n)
+    N, T = dyqT.shape
+    K = xqT.shape[0]
+    if xqT.shape != (K, T) or dw.shape != (N, K):
+        raise ValueError("shape mismatch")
+    _check("fp8_block_gemm_wgrad", lib().fp8_block_gemm_wgrad(
+        _ptr(dyqT), _ptr(sdyT), _ptr(xqT), _ptr(sxT), T, N, K, _ptr(dw), int(bool(accumulate)),
+        _stream(stream)))
+
+
+def fp8_block_gemm_grouped(op: int, offsets, a, sa, b, sb, out, N: int, K: int,
+                           accumulate: bool = False, stream=None) -> None:
+    """Grouped (MoE) GEMM; see fp8bs.h for the operand layouts of each op."""
+    off = _offsets_host(offsets)
+    for t, n, d in ((a, "a", torch.uint8), (sa, "sa", torch.float32), (b, "b", torch.uint8),
+                    (sb, "sb", torch.float32)):
+        _need(t, d, n)
+    _need(out, torch.float32 if op == OP_WGRAD else torch.bfloat16, "out")
+    _check("fp8_block_gemm_grouped", lib().fp8_block_gemm_grouped(
+        int(op), off.size - 1, off.ctypes.data_as(ctypes.c_void_p), _ptr(a), _ptr(sa), _ptr(b),
+        _ptr(sb), int(N), int(K), _ptr(out), int(bool(accumulate)), _stream(stream)))
+
+
+def fp8bs_device_status(reset: bool = True) -> int:
+    """Synchronize and return the device status word (0 = OK)."""
+    return int(lib().fp8bs_device_status(int(bool(reset))))
+
+
+def fp8bs_set_wait_limit_ns(ns: int) -> None:
+    lib().fp8bs_set_wait_limit_ns(int(ns))
+
+
+def fp8bs_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    _check("fp8bs_selftest_wait_timeout",
+           lib().fp8bs_selftest_wait_timeout(int(limit_ns), _stream(stream)))

@@ -1,0 +1,441 @@
+// api.cu -- the extern "C" entry points declared in fp8bs.h: argument
+// validation, per-device setup, TMA tensor maps and kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "fp8bs.h"
+#include "internal.h"
+
+namespace fp8bs {
+namespace {
+
+// Device-side status word: the first error a kernel records (0 = none).
+__device__ unsigned int g_device_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    bool supported = false;
+    int num_sms = 0;
+    unsigned int* status = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+uint64_t g_wait_limit_ns = 2000000000ull;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Per-device setup on first use: capability check, SM count, the address of
+// the status word. Runs once per device (it makes CUDA runtime calls that a
+// stream capture would reject, so the first call on a device should come
+// before any capture).
+fp8bs_status device_state(DeviceState** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return FP8BS_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState& st = g_devices[dev];
+    if (!st.ready) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return FP8BS_ERR_UNSUPPORTED;
+        st.supported = (prop.major == 10 && prop.minor == 3);
+        st.num_sms = prop.multiProcessorCount;
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) return FP8BS_ERR_UNSUPPORTED;
+        st.status = static_cast<unsigned int*>(ptr);
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) == cudaSuccess &&
+                q == cudaDriverEntryPointSuccess)
+                g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+        st.ready = true;
+    }
+    if (!st.supported || !g_encode) return FP8BS_ERR_UNSUPPORTED;
+    *out = &st;
+    return FP8BS_OK;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline fp8bs_status launch_status(cudaError_t e) { return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_LAUNCH; }
+
+// 2D E4M3 tensor map over a row-major [outer x inner] byte matrix, box
+// [box_outer x 128 bytes], 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+              uint32_t box_outer)
+{
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {128u, box_outer};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+void init_params(GemmParams& p, DeviceState* st, int n_cols)
+{
+    std::memset(&p, 0, sizeof(p));
+    p.n_cols = n_cols;
+    p.n_tiles = (n_cols + kBN - 1) / kBN;
+    p.wait_limit_ns = g_wait_limit_ns;
+    p.status = st->status;
+}
+
+// Validates group offsets (host array of groups + 1 entries).
+bool valid_offsets(const int32_t* off, int32_t groups)
+{
+    if (!off || groups < 1 || groups > kMaxGroups || off[0] != 0) return false;
+    for (int g = 0; g < groups; ++g)
+        if (off[g + 1] < off[g]) return false;
+    return true;
+}
+
+int64_t padded_tokens(int64_t rows, const int32_t* off, int32_t groups)
+{
+    if (!off || groups == 0) return (rows + 127) / 128 * 128;
+    int64_t tot = 0;
+    for (int g = 0; g < groups; ++g) tot += (static_cast<int64_t>(off[g + 1] - off[g]) + 127) / 128 * 128;
+    return tot;
+}
+
+// Fprop / Dgrad, dense or grouped. For Fprop the contraction length is K and
+// the output width N; for Dgrad they are N and K. `contr` and `width` are
+// those two; b rows per group = width.
+fp8bs_status run_rowwise_gemm(bool dgrad, int32_t groups, const int32_t* off, const uint8_t* a,
+                              const float* sa, const uint8_t* b, const float* sb, int64_t N,
+                              int64_t K, void* out, void* stream)
+{
+    DeviceState* st = nullptr;
+    fp8bs_status s = device_state(&st);
+    if (s != FP8BS_OK) return s;
+    const int64_t contr = dgrad ? N : K;
+    const int64_t width = dgrad ? K : N;
+    const int64_t M = off[groups];
+    if (M == 0) return FP8BS_OK;
+    if (M > 0x7FFFFFFF - kBM || width * groups > 0x7FFFFFFF || contr > 0x7FFFFFFF)
+        return FP8BS_ERR_SHAPE;
+
+    GemmParams p;
+    init_params(p, st, static_cast<int>(width));
+    p.num_groups = groups;
+    int tiles = 0;
+    for (int g = 0; g < groups; ++g) {
+        const int rows = off[g + 1] - off[g];
+        p.tile_start[g] = tiles;
+        p.a_row0[g] = off[g];
+        p.a_rows[g] = rows;
+        p.k0[g] = 0;
+        p.kblocks[g] = static_cast<int>(contr / kBK);
+        p.b_row0[g] = static_cast<int>(g * width);
+        p.sa_kb0[g] = 0;
+        p.sb_off[g] = static_cast<int64_t>(g) * (K / 128) * (N / 128);
+        p.out_off[g] = 0;
+        tiles += ((rows + kBM - 1) / kBM) * p.n_tiles;
+    }
+    p.tile_start[groups] = tiles;
+    p.total_tiles = tiles;
+    p.sa = sa;
+    p.sa_ld = fp8bs_scale_ld(M);
+    p.sa_rows = static_cast<int>(p.sa_ld);
+    p.sb = sb;
+    // sw is [K/128 x N/128]: Fprop walks K-blocks along its rows, Dgrad along its columns
+    p.sb_kstride = dgrad ? 1 : N / 128;
+    p.sb_cstride = dgrad ? N / 128 : 1;
+    p.out = out;
+    p.out_ld = width;
+    p.accumulate = 0;
+
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, a, contr, M, contr, kBM) ||
+        !make_map(&mb, b, contr, width * groups, contr, kBN))
+        return FP8BS_ERR_ARG;
+    return launch_status(launch_gemm(GemmKind::kBlockScaleBf16, ma, mb, p, st->num_sms,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+// Wgrad, dense (groups = 1 over all T tokens) or grouped (padded segments).
+fp8bs_status run_wgrad(int32_t groups, const int32_t* off, int64_t T, const uint8_t* a,
+                       const float* sa, const uint8_t* b, const float* sb, int64_t N, int64_t K,
+                       float* out, int accumulate, void* stream)
+{
+    DeviceState* st = nullptr;
+    fp8bs_status s = device_state(&st);
+    if (s != FP8BS_OK) return s;
+    if (N > 0x7FFFFFFF || K > 0x7FFFFFFF || T > 0x7FFFFFFF) return FP8BS_ERR_SHAPE;
+    if (T == 0) {
+        if (accumulate) return FP8BS_OK;
+        return launch_status(cudaMemsetAsync(out, 0, sizeof(float) * N * K * groups,
+                                             static_cast<cudaStream_t>(stream)));
+    }
+    GemmParams p;
+    init_params(p, st, static_cast<int>(K));
+    p.num_groups = groups;
+    const int tiles_per_group = static_cast<int>((N / kBM) * p.n_tiles);
+    int64_t pstart = 0;
+    for (int g = 0; g < groups; ++g) {
+        const int64_t tg = off ? static_cast<int64_t>(off[g + 1] - off[g]) : T;
+        const int64_t kb = (tg + 127) / 128;
+        p.tile_start[g] = g * tiles_per_group;
+        p.a_row0[g] = 0;
+        p.a_rows[g] = static_cast<int>(N);
+        p.k0[g] = static_cast<int>(pstart);
+        p.kblocks[g] = static_cast<int>(kb);
+        p.b_row0[g] = 0;
+        p.sa_kb0[g] = static_cast<int>(pstart / 128);
+        p.sb_off[g] = (pstart / 128) * K;
+        p.out_off[g] = static_cast<int64_t>(g) * N * K;
+        pstart += kb * 128;
+    }
+    if (pstart != T) return FP8BS_ERR_SHAPE;
+    p.tile_start[groups] = groups * tiles_per_group;
+    p.total_tiles = groups * tiles_per_group;
+    p.sa = sa;
+    p.sa_ld = N;
+    p.sa_rows = static_cast<int>(N);
+    p.sb = sb;
+    p.sb_kstride = K;
+    p.sb_cstride = 1;
+    p.out = out;
+    p.out_ld = K;
+    p.accumulate = accumulate ? 1 : 0;
+
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, a, T, N, T, kBM) || !make_map(&mb, b, T, K, T, kBN)) return FP8BS_ERR_ARG;
+    return launch_status(launch_gemm(GemmKind::kVectorScaleF32, ma, mb, p, st->num_sms,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+}  // namespace fp8bs
+
+using namespace fp8bs;
+
+extern "C" {
+
+const char* fp8bs_status_str(fp8bs_status s)
+{
+    switch (s) {
+    case FP8BS_OK: return "ok";
+    case FP8BS_ERR_ARG: return "invalid argument";
+    case FP8BS_ERR_ALIGN: return "misaligned pointer or stride";
+    case FP8BS_ERR_SHAPE: return "unsupported shape";
+    case FP8BS_ERR_LAUNCH: return "kernel launch failed";
+    case FP8BS_ERR_TIMEOUT: return "device wait timed out";
+    case FP8BS_ERR_UNSUPPORTED: return "unsupported device (needs sm_103a)";
+    case FP8BS_ERR_DEVICE: return "device-side check failed";
+    }
+    return "unknown status";
+}
+
+int fp8bs_version(void) { return 100; }
+
+int64_t fp8bs_scale_ld(int64_t rows) { return rows <= 0 ? 0 : (rows + 3) / 4 * 4; }
+
+int64_t fp8bs_padded_tokens(int64_t rows, const int32_t* group_offsets_host, int32_t groups)
+{
+    if (rows < 0) return -1;
+    if (group_offsets_host && groups > 0) {
+        if (!valid_offsets(group_offsets_host, groups) || group_offsets_host[groups] != rows) return -1;
+    }
+    return padded_tokens(rows, group_offsets_host, groups);
+}
+
+fp8bs_status fp8_quant_1x128(const void* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q,
+                             float* scales, void* stream)
+{
+    if (rows < 0 || cols <= 0 || ldx < cols) return FP8BS_ERR_ARG;
+    if (cols % 16 != 0) return FP8BS_ERR_SHAPE;
+    if (rows == 0) return FP8BS_OK;
+    if (!x || !q || !scales) return FP8BS_ERR_ARG;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(scales) || ldx % 8 != 0) return FP8BS_ERR_ALIGN;
+    DeviceState* st = nullptr;
+    fp8bs_status s = device_state(&st);
+    if (s != FP8BS_OK) return s;
+    return launch_status(launch_quant_1x128(static_cast<const uint16_t*>(x), rows, cols, ldx, q,
+                                            scales, fp8bs_scale_ld(rows), st->num_sms,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+fp8bs_status fp8_quant_128x128(const void* w, int64_t batch, int64_t rows, int64_t cols,
+                               int64_t ldw, uint8_t* q, uint8_t* qT, float* scales, void* stream)
+{
+    if (batch < 1 || rows <= 0 || cols <= 0 || ldw < cols) return FP8BS_ERR_ARG;
+    if (rows % 16 != 0 || cols % 16 != 0) return FP8BS_ERR_SHAPE;
+    if (!w || !q || !scales) return FP8BS_ERR_ARG;
+    if (!aligned16(w) || !aligned16(q) || (qT && !aligned16(qT)) || ldw % 8 != 0)
+        return FP8BS_ERR_ALIGN;
+    DeviceState* st = nullptr;
+    fp8bs_status s = device_state(&st);
+    if (s != FP8BS_OK) return s;
+    return launch_status(launch_quant_128x128(static_cast<const uint16_t*>(w), batch, rows, cols,
+                                              ldw, q, qT, scales, static_cast<cudaStream_t>(stream)));
+}
+
+fp8bs_status fp8_requant_128x1_T(int src_mode, const void* src, const float* src_scales,
+                                 int64_t rows, int64_t cols, const int32_t* group_offsets_host,
+                                 int32_t groups, uint8_t* qT, float* scalesT, void* stream)
+{
+    if (src_mode != FP8BS_SRC_BF16 && src_mode != FP8BS_SRC_E4M3) return FP8BS_ERR_ARG;
+    if (rows < 0 || cols <= 0 || groups < 0) return FP8BS_ERR_ARG;
+    if (cols % 16 != 0) return FP8BS_ERR_SHAPE;
+    if (rows > 0x7FFFFFFF) return FP8BS_ERR_SHAPE;
+    const bool grouped = group_offsets_host && groups > 0;
+    if (grouped && (!valid_offsets(group_offsets_host, groups) || group_offsets_host[groups] != rows))
+        return FP8BS_ERR_ARG;
+    const int64_t mpad = padded_tokens(rows, grouped ? group_offsets_host : nullptr, grouped ? groups : 0);
+    if (mpad == 0) return FP8BS_OK;
+    if (!src || !qT || !scalesT || (src_mode == FP8BS_SRC_E4M3 && !src_scales)) return FP8BS_ERR_ARG;
+    if (!aligned16(src) || !aligned16(qT) || !aligned16(scalesT) ||
+        (src_scales && !aligned16(src_scales)))
+        return FP8BS_ERR_ALIGN;
+    DeviceState* st = nullptr;
+    fp8bs_status s = device_state(&st);
+    if (s != FP8BS_OK) return s;
+
+    RequantParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.mode = src_mode;
+    p.src = src;
+    p.src_scales = src_scales;
+    p.src_scale_ld = fp8bs_scale_ld(rows);
+    p.rows = rows;
+    p.cols = cols;
+    p.qT = qT;
+    p.scT = scalesT;
+    p.mpad = mpad;
+    if (grouped) {
+        p.num_groups = groups;
+        int tiles = 0;
+        for (int g = 0; g <= groups; ++g) p.off[g] = group_offsets_host[g];
+        for (int g = 0; g < groups; ++g) {
+            p.tile_start[g] = tiles;
+            tiles += (group_offsets_host[g + 1] - group_offsets_host[g] + 127) / 128;
+        }
+        p.tile_start[groups] = tiles;
+    } else {
+        p.num_groups = 1;
+        p.off[0] = 0;
+        p.off[1] = static_cast<int32_t>(rows);
+        p.tile_start[0] = 0;
+        p.tile_start[1] = static_cast<int32_t>(mpad / 128);
+    }
+    return launch_status(launch_requant_128x1_T(p, static_cast<cudaStream_t>(stream)));
+}
+
+fp8bs_status fp8_block_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wqT,
+                                  const float* sw, int64_t M, int64_t N, int64_t K, void* y,
+                                  void* stream)
+{
+    if (M < 0 || N <= 0 || K <= 0) return FP8BS_ERR_ARG;
+    if (K % 128 != 0 || N % 128 != 0 || M > 0x7FFFFF00) return FP8BS_ERR_SHAPE;
+    if (M == 0) return FP8BS_OK;
+    if (!xq || !sx || !wqT || !sw || !y) return FP8BS_ERR_ARG;
+    if (!aligned16(xq) || !aligned16(sx) || !aligned16(wqT) || !aligned16(sw) || !aligned16(y))
+        return FP8BS_ERR_ALIGN;
+    const int32_t off[2] = {0, static_cast<int32_t>(M)};
+    return run_rowwise_gemm(false, 1, off, xq, sx, wqT, sw, N, K, y, stream);
+}
+
+fp8bs_status fp8_block_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wq,
+                                  const float* sw, int64_t M, int64_t N, int64_t K, void* dx,
+                                  void* stream)
+{
+    if (M < 0 || N <= 0 || K <= 0) return FP8BS_ERR_ARG;
+    if (K % 128 != 0 || N % 128 != 0 || M > 0x7FFFFF00) return FP8BS_ERR_SHAPE;
+    if (M == 0) return FP8BS_OK;
+    if (!dyq || !sdy || !wq || !sw || !dx) return FP8BS_ERR_ARG;
+    if (!aligned16(dyq) || !aligned16(sdy) || !aligned16(wq) || !aligned16(sw) || !aligned16(dx))
+        return FP8BS_ERR_ALIGN;
+    const int32_t off[2] = {0, static_cast<int32_t>(M)};
+    return run_rowwise_gemm(true, 1, off, dyq, sdy, wq, sw, N, K, dx, stream);
+}
+
+fp8bs_status fp8_block_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT,
+                                  const float* sxT, int64_t T, int64_t N, int64_t K, float* dw,
+                                  int accumulate, void* stream)
+{
+    if (T < 0 || N <= 0 || K <= 0) return FP8BS_ERR_ARG;
+    if (T % 128 != 0 || N % 128 != 0 || K % 128 != 0) return FP8BS_ERR_SHAPE;
+    if (!dw) return FP8BS_ERR_ARG;
+    if (T > 0 && (!dyqT || !sdyT || !xqT || !sxT)) return FP8BS_ERR_ARG;
+    if (!aligned16(dw) || (T > 0 && (!aligned16(dyqT) || !aligned16(sdyT) || !aligned16(xqT) ||
+                                     !aligned16(sxT))))
+        return FP8BS_ERR_ALIGN;
+    return run_wgrad(1, nullptr, T, dyqT, sdyT, xqT, sxT, N, K, dw, accumulate, stream);
+}
+
+fp8bs_status fp8_block_gemm_grouped(int op, int32_t groups, const int32_t* offsets_host,
+                                    const uint8_t* a, const float* sa, const uint8_t* b,
+                                    const float* sb, int64_t N, int64_t K, void* out,
+                                    int accumulate, void* stream)
+{
+    if (op != FP8BS_OP_FPROP && op != FP8BS_OP_DGRAD && op != FP8BS_OP_WGRAD) return FP8BS_ERR_ARG;
+    if (!valid_offsets(offsets_host, groups)) return FP8BS_ERR_ARG;
+    if (N <= 0 || K <= 0) return FP8BS_ERR_ARG;
+    if (N % 128 != 0 || K % 128 != 0) return FP8BS_ERR_SHAPE;
+    if (!out) return FP8BS_ERR_ARG;
+    const int64_t M = offsets_host[groups];
+    if (op == FP8BS_OP_WGRAD) {
+        const int64_t T = padded_tokens(M, offsets_host, groups);
+        if (T > 0 && (!a || !sa || !b || !sb)) return FP8BS_ERR_ARG;
+        if (!aligned16(out) || (T > 0 && (!aligned16(a) || !aligned16(sa) || !aligned16(b) ||
+                                          !aligned16(sb))))
+            return FP8BS_ERR_ALIGN;
+        return run_wgrad(groups, offsets_host, T, a, sa, b, sb, N, K, static_cast<float*>(out),
+                         accumulate, stream);
+    }
+    if (M == 0) return FP8BS_OK;
+    if (!a || !sa || !b || !sb) return FP8BS_ERR_ARG;
+    if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(out))
+        return FP8BS_ERR_ALIGN;
+    if (M > 0x7FFFFF00) return FP8BS_ERR_SHAPE;
+    return run_rowwise_gemm(op == FP8BS_OP_DGRAD, groups, offsets_host, a, sa, b, sb, N, K, out,
+                            stream);
+}
+
+fp8bs_status fp8bs_device_status(int reset)
+{
+    DeviceState* st = nullptr;
+    fp8bs_status s = device_state(&st);
+    if (s != FP8BS_OK) return s;
+    if (cudaDeviceSynchronize() != cudaSuccess) return FP8BS_ERR_LAUNCH;
+    unsigned int v = 0;
+    if (cudaMemcpy(&v, st->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return FP8BS_ERR_LAUNCH;
+    if (reset) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(st->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return FP8BS_ERR_LAUNCH;
+    }
+    return static_cast<fp8bs_status>(v);
+}
+
+void fp8bs_set_wait_limit_ns(uint64_t ns)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    g_wait_limit_ns = ns;
+}
+
+fp8bs_status fp8bs_selftest_wait_timeout(uint64_t limit_ns, void* stream)
+{
+    DeviceState* st = nullptr;
+    fp8bs_status s = device_state(&st);
+    if (s != FP8BS_OK) return s;
+    return launch_status(launch_selftest_wait(st->status, limit_ns, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,381 @@
+// gemm.cu -- block-scaled E4M3 GEMM with per-128-K fp32 promotion on tcgen05.
+//
+// What it computes ("FP8 动态量化里的 partial sum 漂移", sections 3 and 5;
+// "scratch: the backward pass, unrolled", "What is asserted, and from where",
+// bullet 1): for every output element and every 128-element block b of the
+// contraction, the tensor core forms the partial P_b over that block only;
+// the partial is multiplied by s_a * s_b and added to an fp32 accumulator;
+// the next block starts from zero. Output is BF16 (Fprop, Dgrad) or FP32
+// (Wgrad).
+//
+// The pages describe this on Hopper (WGMMA into registers, promotion on the
+// CUDA cores of the same warps). On sm_103a the partial lives in tensor
+// memory instead, which decouples the two halves of the work:
+//
+//   warp 0      TMA producer: one thread streams 128x128 (A) and 256x128 (B)
+//               E4M3 tiles (K-major, 128-byte swizzle) into a 4-stage
+//               shared-memory ring.
+//   warp 1      MMA issuer: one thread issues four tcgen05.mma (K = 32 each)
+//               per K-block into a fresh TMEM accumulator (the first with
+//               accumulate = 0), double-buffered over 2 x 256 TMEM columns,
+//               and commits to mbarriers that free the smem stage and hand
+//               the partial to the epilogue.
+//   warps 2-3   idle (they complete the first warpgroup, which gives its
+//               registers to the epilogue with setmaxnreg).
+//   warps 4-11  promotion epilogue: each warp owns 32 TMEM lanes (rows) and
+//               128 columns; per K-block it loads the fp32 partial with
+//               tcgen05.ld, releases the TMEM buffer, and does
+//               acc = fma(P_b, s_a * s_b, acc) in registers; at the end of a
+//               tile it converts and stores the accumulator.
+//
+// The kernel is persistent (one CTA per SM, 128x256 output tiles in a
+// grid-stride order) and handles groups (MoE experts) through a per-group
+// table in its parameter block. Every wait is bounded: when one gives up the
+// kernel records FP8BS_ERR_TIMEOUT, stops issuing work, drains its in-flight
+// copies and MMAs, frees its tensor memory and returns.
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8bs {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * kBK;  // 16 KB
+constexpr int kBBytes = kBN * kBK;  // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kEpiWarps = 8;
+constexpr int kFirstEpiWarp = 4;
+constexpr int kThreads = (kFirstEpiWarp + kEpiWarps) * 32;  // 384: three warpgroups
+// Register split: the kernel is launched with kLaunchRegs per thread (the
+// __launch_bounds__ budget); the producer warpgroup gives registers back and
+// the two epilogue warpgroups take them. The host checks the launch count
+// before the first launch so that the split never asks for more than exists.
+constexpr uint32_t kLaunchRegs = 168;
+constexpr uint32_t kProducerRegs = 64;
+constexpr uint32_t kEpilogueRegs = 216;
+static_assert(128 * kProducerRegs + 256 * kEpilogueRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
+constexpr int kTmemCols = 2 * kBN;              // two accumulator buffers
+// Waits that drain in-flight copies and MMAs before exit use at least this
+// limit, so that a small user limit never lets a CTA exit with work in flight.
+constexpr uint64_t kDrainLimitNs = 1000000000ull;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 /* alignment */ + 256 /* barriers */;
+
+struct SharedCtl {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint32_t tmem_base;
+    volatile int abort;
+};
+
+__device__ __forceinline__ void record_status(unsigned int* status, unsigned int code)
+{
+    atomicCAS(status, 0u, code);
+}
+
+__device__ __forceinline__ void decode_tile(const GemmParams& p, int t, int& g, int& mt, int& nt)
+{
+    int lo = 0, hi = p.num_groups - 1;  // last g with tile_start[g] <= t
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.tile_start[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    g = lo;
+    const int local = t - p.tile_start[g];
+    mt = local / p.n_tiles;
+    nt = local - mt * p.n_tiles;
+}
+
+template <GemmKind kKind>
+__global__ void __launch_bounds__(kThreads, 1)
+    block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
+                             const __grid_constant__ CUtensorMap map_b,
+                             const __grid_constant__ GemmParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + kStages * kABytes;
+    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + kStages * kStageBytes);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&ctl->tfull[a], 1);
+            mbar_init(&ctl->tempty[a], kEpiWarps);
+        }
+        ctl->abort = 0;
+        fence_mbarrier_init();
+        tma_prefetch_desc(&map_a);
+        tma_prefetch_desc(&map_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(&ctl->tmem_base, kTmemCols);
+        tmem_relinquish();
+        tc_fence_before_sync();
+    }
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = ctl->tmem_base;
+    const uint64_t limit = p.wait_limit_ns;
+
+    if (warp < kFirstEpiWarp) {
+        setmaxnreg_dec<kProducerRegs>();
+    }
+    if (warp == 0) {
+        // ------------------------------------------------------------------
+        // TMA producer
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+                int g, mt, nt;
+                decode_tile(p, t, g, mt, nt);
+                const int nkb = p.kblocks[g];
+                const int ya = p.a_row0[g] + mt * kBM;
+                const int yb = p.b_row0[g] + nt * kBN;
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const uint32_t s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1u;
+                    if (ctl->abort || !mbar_wait(&ctl->empty[s], ph ^ 1u, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&ctl->full[s], kStageBytes);
+                    const int x = p.k0[g] + kb * kBK;
+                    tma_load_2d(sA + s * kABytes, &map_a, &ctl->full[s], x, ya);
+                    tma_load_2d(sB + s * kBBytes, &map_b, &ctl->full[s], x, yb);
+                }
+            }
+            if (!ok) {
+                record_status(p.status, FP8BS_ERR_TIMEOUT);
+                ctl->abort = 1;
+            }
+            // drain: every issued copy has landed before the CTA can exit
+            const uint32_t first = it > kStages ? it - kStages : 0u;
+            const uint64_t drain = limit > kDrainLimitNs ? limit : kDrainLimitNs;
+            for (uint32_t j = first; j < it; ++j)
+                mbar_wait(&ctl->full[j % kStages], (j / kStages) & 1u, drain);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------
+        // MMA issuer
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kBN);
+            uint32_t it = 0, acc_it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+                int g, mt, nt;
+                decode_tile(p, t, g, mt, nt);
+                const int nkb = p.kblocks[g];
+                for (int kb = 0; kb < nkb; ++kb, ++it, ++acc_it) {
+                    const uint32_t s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1u;
+                    const uint32_t buf = acc_it & 1u;
+                    const uint32_t aph = (acc_it >> 1) & 1u;
+                    if (ctl->abort || !mbar_wait(&ctl->tempty[buf], aph ^ 1u, limit) ||
+                        !mbar_wait(&ctl->full[s], ph, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint64_t adesc = sdesc_kmajor_sw128(smem_addr(sA + s * kABytes));
+                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_addr(sB + s * kBBytes));
+                    const uint32_t d = tmem_base + buf * kBN;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 32; ++kk)
+                        mma_e4m3(d, adesc + 2u * kk, bdesc + 2u * kk, idesc, kk > 0 ? 1u : 0u);
+                    mma_commit(&ctl->empty[s]);
+                    mma_commit(&ctl->tfull[buf]);
+                }
+            }
+            if (!ok) {
+                record_status(p.status, FP8BS_ERR_TIMEOUT);
+                ctl->abort = 1;
+            }
+            // drain: the last committed MMA group has completed
+            if (it > 0) {
+                const uint32_t j = it - 1;
+                const uint64_t drain = limit > kDrainLimitNs ? limit : kDrainLimitNs;
+                mbar_wait(&ctl->empty[j % kStages], (j / kStages) & 1u, drain);
+            }
+        }
+    } else if (warp >= kFirstEpiWarp) {
+        // ------------------------------------------------------------------
+        // Promotion epilogue
+        // ------------------------------------------------------------------
+        setmaxnreg_inc<kEpilogueRegs>();
+        const int ew = warp - kFirstEpiWarp;
+        const int quarter = warp & 3;   // TMEM lanes this warp may access
+        const int half = ew >> 2;       // 128-column half of the tile
+        const int r_in_tile = quarter * 32 + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+        uint32_t acc_it = 0;
+        bool ok = true;
+
+        for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+            int g, mt, nt;
+            decode_tile(p, t, g, mt, nt);
+            const int nkb = p.kblocks[g];
+            const int row = p.a_row0[g] + mt * kBM + r_in_tile;   // A row = output row
+            const bool row_ok = (mt * kBM + r_in_tile) < p.a_rows[g];
+            const int col0 = nt * kBN + half * 128;
+            const bool cols_ok = col0 < p.n_cols;                  // n_cols % 128 == 0
+            const bool sa_ok = row < p.sa_rows;
+            const float* sa_ptr = p.sa + static_cast<int64_t>(p.sa_kb0[g]) * p.sa_ld + row;
+            const float* sb_ptr = p.sb + p.sb_off[g] +
+                                  (kKind == GemmKind::kBlockScaleBf16
+                                       ? static_cast<int64_t>(col0 / 128) * p.sb_cstride
+                                       : static_cast<int64_t>(col0));
+
+            float acc[128];
+#pragma unroll
+            for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+
+            for (int kb = 0; kb < nkb; ++kb, ++acc_it) {
+                const float s_a = sa_ok ? __ldg(sa_ptr + static_cast<int64_t>(kb) * p.sa_ld) : 0.0f;
+                float s_blk = 0.0f;
+                if constexpr (kKind == GemmKind::kBlockScaleBf16)
+                    s_blk = cols_ok ? s_a * __ldg(sb_ptr + static_cast<int64_t>(kb) * p.sb_kstride) : 0.0f;
+                const uint32_t buf = acc_it & 1u;
+                const uint32_t aph = (acc_it >> 1) & 1u;
+                if (ctl->abort || !mbar_wait(&ctl->tfull[buf], aph, limit)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t taddr = tmem_base + lane_addr + buf * kBN + half * 128;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_x32(taddr + c * 32, r);
+                    tmem_ld_wait(r);
+                    if (c == 3) {
+                        tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
+                    }
+                    if constexpr (kKind == GemmKind::kBlockScaleBf16) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            acc[c * 32 + j] = fmaf(__uint_as_float(r[j]), s_blk, acc[c * 32 + j]);
+                    } else {
+                        const float4* sbv = reinterpret_cast<const float4*>(
+                            sb_ptr + static_cast<int64_t>(kb) * p.sb_kstride + c * 32);
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; ++q4) {
+                            const float4 v = cols_ok ? __ldg(sbv + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            const int j = c * 32 + q4 * 4;
+                            acc[j + 0] = fmaf(__uint_as_float(r[q4 * 4 + 0]), s_a * v.x, acc[j + 0]);
+                            acc[j + 1] = fmaf(__uint_as_float(r[q4 * 4 + 1]), s_a * v.y, acc[j + 1]);
+                            acc[j + 2] = fmaf(__uint_as_float(r[q4 * 4 + 2]), s_a * v.z, acc[j + 2]);
+                            acc[j + 3] = fmaf(__uint_as_float(r[q4 * 4 + 3]), s_a * v.w, acc[j + 3]);
+                        }
+                    }
+                }
+            }
+            if (!ok) break;
+
+            if (row_ok && cols_ok) {
+                if constexpr (kKind == GemmKind::kBlockScaleBf16) {
+                    uint16_t* y = static_cast<uint16_t*>(p.out) + p.out_off[g] +
+                                  static_cast<int64_t>(row) * p.out_ld + col0;
+#pragma unroll
+                    for (int v = 0; v < 16; ++v) {
+                        uint4 pk;
+                        pk.x = pack_bf16x2(acc[8 * v + 0], acc[8 * v + 1]);
+                        pk.y = pack_bf16x2(acc[8 * v + 2], acc[8 * v + 3]);
+                        pk.z = pack_bf16x2(acc[8 * v + 4], acc[8 * v + 5]);
+                        pk.w = pack_bf16x2(acc[8 * v + 6], acc[8 * v + 7]);
+                        reinterpret_cast<uint4*>(y)[v] = pk;
+                    }
+                } else {
+                    float* y = static_cast<float*>(p.out) + p.out_off[g] +
+                               static_cast<int64_t>(row) * p.out_ld + col0;
+                    float4* y4 = reinterpret_cast<float4*>(y);
+#pragma unroll
+                    for (int v = 0; v < 32; ++v) {
+                        float4 o = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+                        if (p.accumulate) {
+                            const float4 prev = y4[v];
+                            o.x += prev.x; o.y += prev.y; o.z += prev.z; o.w += prev.w;
+                        }
+                        y4[v] = o;
+                    }
+                }
+            }
+        }
+        if (!ok) {
+            record_status(p.status, FP8BS_ERR_TIMEOUT);
+            ctl->abort = 1;
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+__global__ void selftest_wait_kernel(unsigned int* status, uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+    // nothing ever arrives: phase 0 never completes, so the wait must give up
+    if (threadIdx.x == 0 && !mbar_wait(&bar, 0u, limit_ns)) record_status(status, FP8BS_ERR_TIMEOUT);
+}
+
+template <GemmKind kKind>
+cudaError_t launch_kind(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmParams& p,
+                        int num_sms, cudaStream_t stream)
+{
+    static_assert(sizeof(SharedCtl) <= 256, "control block");
+    auto kernel = block_scaled_gemm_kernel<kKind>;
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, kernel);
+    if (e != cudaSuccess) return e;
+    // the setmaxnreg split assumes this launch allocation (see kLaunchRegs)
+    if (static_cast<uint32_t>(attr.numRegs) != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = p.total_tiles < num_sms ? p.total_tiles : num_sms;
+    kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_a, map_b, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(GemmKind kind, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                        const GemmParams& p, int num_sms, cudaStream_t stream)
+{
+    if (p.total_tiles <= 0) return cudaSuccess;
+    if (kind == GemmKind::kBlockScaleBf16)
+        return launch_kind<GemmKind::kBlockScaleBf16>(map_a, map_b, p, num_sms, stream);
+    return launch_kind<GemmKind::kVectorScaleF32>(map_a, map_b, p, num_sms, stream);
+}
+
+cudaError_t launch_selftest_wait(unsigned int* status, uint64_t limit_ns, cudaStream_t stream)
+{
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace fp8bs

@@ -1,0 +1,91 @@
+// internal.h -- declarations shared by the library's translation units
+// (kernel launchers and their parameter blocks). Not part of the C ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fp8bs.h"
+
+namespace fp8bs {
+
+constexpr int kMaxGroups = FP8BS_MAX_GROUPS;
+
+// ---------------------------------------------------------------------------
+// Quantizers
+// ---------------------------------------------------------------------------
+
+cudaError_t launch_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
+                               uint8_t* q, float* scales, int64_t scale_ld, int num_sms,
+                               cudaStream_t stream);
+
+cudaError_t launch_quant_128x128(const uint16_t* w, int64_t batch, int64_t rows, int64_t cols,
+                                 int64_t ldw, uint8_t* q, uint8_t* qT, float* scales,
+                                 cudaStream_t stream);
+
+struct RequantParams {
+    int mode;                  // FP8BS_SRC_BF16 or FP8BS_SRC_E4M3
+    const void* src;           // [rows x cols], dense
+    const float* src_scales;   // mode E4M3: 1x128 scales, tile-major
+    int64_t src_scale_ld;
+    int64_t rows, cols;
+    uint8_t* qT;               // [cols x mpad]
+    float* scT;                // [mpad/128 x cols]
+    int64_t mpad;
+    int num_groups;
+    int32_t off[kMaxGroups + 1];         // row offsets of the groups
+    int32_t tile_start[kMaxGroups + 1];  // first padded token tile of each group
+};
+
+cudaError_t launch_requant_128x1_T(const RequantParams& p, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// Block-scaled GEMM (tcgen05)
+// ---------------------------------------------------------------------------
+
+// One output problem of the persistent GEMM kernel is a set of groups; each
+// group g has a rectangle of output rows, a K range and its own offsets into
+// the operands, scales and output. Dense GEMMs are one group.
+struct GemmParams {
+    int num_groups;
+    int n_cols;        // output columns (same for all groups)
+    int n_tiles;       // column tiles of BN per group
+    int total_tiles;
+    int32_t tile_start[kMaxGroups + 1];
+    int32_t a_row0[kMaxGroups];   // first A row (= first output row) of the group
+    int32_t a_rows[kMaxGroups];   // output rows of the group
+    int32_t k0[kMaxGroups];       // first K element (TMA x coordinate)
+    int32_t kblocks[kMaxGroups];  // 128-element K blocks
+    int32_t b_row0[kMaxGroups];   // first B row (TMA y coordinate)
+    int32_t sa_kb0[kMaxGroups];   // first scale K-block of A
+    int64_t sb_off[kMaxGroups];   // float offset of the group's B scales
+    int64_t out_off[kMaxGroups];  // element offset of the group's output origin
+    const float* sa;              // A scale of (row, kb): sa[(sa_kb0 + kb) * sa_ld + row]
+    int64_t sa_ld;
+    int32_t sa_rows;              // rows that may be read from sa
+    const float* sb;              // B scale: see GemmKind
+    int64_t sb_kstride, sb_cstride;
+    void* out;
+    int64_t out_ld;
+    int accumulate;
+    uint64_t wait_limit_ns;
+    unsigned int* status;
+};
+
+enum class GemmKind {
+    kBlockScaleBf16,   // B scale per (K-block, 128-column block), BF16 output (Fprop, Dgrad)
+    kVectorScaleF32,   // B scale per (K-block, column), FP32 output (Wgrad)
+};
+
+cudaError_t launch_gemm(GemmKind kind, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                        const GemmParams& p, int num_sms, cudaStream_t stream);
+
+// GEMM tile shape and pipeline depth (exported for host-side planning).
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 128;
+
+cudaError_t launch_selftest_wait(unsigned int* status, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace fp8bs

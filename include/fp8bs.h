@@ -1,0 +1,261 @@
+/*
+ * fp8bs.h -- C ABI of the GB300 (sm_103a) fine-grained FP8 linear-layer library.
+ *
+ * The library implements the data path of a linear layer under the
+ * DeepSeek-V3 FP8 training recipe:
+ *   - dynamic absmax quantization to E4M3 with fp32 scales, in 1x128 tiles
+ *     (activations, gradients), 128x128 tiles (weights) and a transposed 128x1
+ *     re-tiling of saved operands for the weight gradient;
+ *   - the three E4M3 GEMMs of a linear (Fprop Y = X W, Dgrad dX = dY W^T,
+ *     Wgrad dW = dY^T X), each promoting its per-128-K partial sums to fp32
+ *     scaled by s_a * s_b, with BF16 (Y, dX) or FP32 (dW) output;
+ *   - a grouped variant of the GEMMs for MoE experts.
+ * Sources for the definitions:
+ *   [P1] "scratch: the backward pass, unrolled" (deepseek-v3.ezyang.com),
+ *        section "What is asserted, and from where", bullets 1-2 and
+ *        "Where casts are drawn".
+ *   [P2] "FP8 动态量化里的 partial sum 漂移" (foosynaptic DeepSeek tech notes),
+ *        section 3 (fine-grained scale and FP32 promotion table) and
+ *        section 5 (promotion every N_c = 128).
+ *   [P3] TransformerEngine PR #3573, "Changes" (E4M3 bound 448) and the
+ *        all-zero-gradient test patterns.
+ *   [P4] prime-rl PR #4073, quantization-conventions table, row
+ *        "Negative zero" (E4M3 -0 is 0x80, kept apart from +0 = 0x00).
+ *
+ * Common conventions
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     allocates nothing and keeps no reference after the call returns.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL is the legacy default stream). The returned status covers argument
+ *     validation and launch errors only. Errors detected on the device (a
+ *     bounded pipeline wait that gave up) are recorded in a per-device status
+ *     word read by fp8bs_device_status().
+ *   - Matrices are row-major. "ld" arguments are row strides in elements.
+ *   - BF16 data is passed as `const void*` (IEEE bfloat16 bit patterns), E4M3
+ *     payloads as `uint8_t*` (OCP E4M3, "fn" variant: max 448, no infinities).
+ *   - Quantization: for a tile with values v (fp32 from BF16 or from a
+ *     dequantized E4M3 stash): amax = max |v|; s = amax / 448 (IEEE fp32
+ *     division) or s = 1 when amax = 0; q = E4M3_RN_satfinite(fp32(v / s)),
+ *     ties to even, saturating at +-448, a zero result keeps the sign of v.
+ *     Results are bit-identical to the CPU oracle of this repository.
+ *   - Pointers must be 16-byte aligned (FP8BS_ERR_ALIGN otherwise).
+ *   - Inputs must be finite; NaN/Inf inputs give unspecified payloads.
+ */
+#ifndef FP8BS_H
+#define FP8BS_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FP8BS_API __attribute__((visibility("default")))
+#else
+#define FP8BS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8BS_OK = 0,
+    FP8BS_ERR_ARG = 1,          /* null pointer, negative size or bad enum value */
+    FP8BS_ERR_ALIGN = 2,        /* pointer not 16-byte aligned or stride not a multiple of 16 bytes */
+    FP8BS_ERR_SHAPE = 3,        /* size outside the documented constraints */
+    FP8BS_ERR_LAUNCH = 4,       /* CUDA reported an error launching the kernel */
+    FP8BS_ERR_TIMEOUT = 5,      /* device: a bounded pipeline wait gave up (kernel returned early) */
+    FP8BS_ERR_UNSUPPORTED = 6,  /* device is not sm_103a-capable, or a driver entry point is missing */
+    FP8BS_ERR_DEVICE = 7        /* device: a kernel's own consistency check failed */
+} fp8bs_status;
+
+typedef enum {
+    FP8BS_SRC_BF16 = 0,         /* requant source is BF16 ("mode B") */
+    FP8BS_SRC_E4M3 = 1          /* requant source is an E4M3 stash with 1x128 scales ("mode Q") */
+} fp8bs_src_mode;
+
+typedef enum {
+    FP8BS_OP_FPROP = 0,
+    FP8BS_OP_DGRAD = 1,
+    FP8BS_OP_WGRAD = 2
+} fp8bs_op;
+
+/* Largest number of groups (experts) accepted by the grouped entry points. */
+#define FP8BS_MAX_GROUPS 256
+
+/* ------------------------------------------------------------------------ */
+/* Helpers (host only, no device work)                                       */
+/* ------------------------------------------------------------------------ */
+
+/* Human-readable name of a status code (static string). */
+FP8BS_API const char* fp8bs_status_str(fp8bs_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+FP8BS_API int fp8bs_version(void);
+
+/* Row stride of a 1x128 scale array: `rows` rounded up to a multiple of 4
+ * (so that every tile row of scales starts on a 16-byte boundary). */
+FP8BS_API int64_t fp8bs_scale_ld(int64_t rows);
+
+/* Token count of the transposed 128x1 output: each group's token count
+ * rounded up to a multiple of 128, summed. With group_offsets_host == NULL
+ * (or groups == 0) the whole `rows` is one group. Returns -1 for invalid
+ * offsets. */
+FP8BS_API int64_t fp8bs_padded_tokens(int64_t rows, const int32_t* group_offsets_host, int32_t groups);
+
+/* ------------------------------------------------------------------------ */
+/* S1. 1x128 activation / gradient quantizer                                 */
+/* [P1] bullet 1 (1x128 activation tiles) and bullet 2 (dY is quantized to    */
+/* E4M3 before Dgrad and Wgrad); [P2] section 3 row (a).                      */
+/* ------------------------------------------------------------------------ */
+/* x       : BF16 [rows x cols], row stride ldx (ldx >= cols, ldx % 8 == 0).
+ * q       : E4M3 [rows x cols], dense (row stride cols).
+ * scales  : fp32 [ceil(cols/128) x fp8bs_scale_ld(rows)], tile-major: the
+ *           scale of row r, column tile t is scales[t * fp8bs_scale_ld(rows) + r].
+ *           The padding entries (r >= rows) are not written.
+ * Tiles cover columns [128 t, min(128 t + 128, cols)); a ragged last tile
+ * takes the absmax over its valid columns.
+ * Constraints: rows >= 0, cols > 0, cols % 16 == 0 (FP8BS_ERR_SHAPE). */
+FP8BS_API fp8bs_status fp8_quant_1x128(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                             uint8_t* q, float* scales, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* S2. 128x128 weight quantizer                                              */
+/* [P1] bullet 1 (128x128 weight tiles); [P2] section 3 row (a).              */
+/* ------------------------------------------------------------------------ */
+/* w       : BF16 [batch x rows x cols]; matrix b starts at w + b * rows * ldw,
+ *           row stride ldw (ldw >= cols, ldw % 8 == 0). For a layer weight
+ *           W [K x N] (Y = X W), rows = K and cols = N; batch > 1 stacks the
+ *           weights of several experts.
+ * q       : E4M3 [batch x rows x cols], dense. This orientation is the Dgrad operand.
+ * qT      : optional (may be NULL) E4M3 [batch x cols x rows], dense: the byte
+ *           transpose of each matrix of q. This K-contiguous orientation is the
+ *           Fprop operand. Because the tiles are square, the transpose needs no
+ *           requantization.
+ * scales  : fp32 [batch x ceil(rows/128) x ceil(cols/128)], row-major, shared by
+ *           q and qT.
+ * Constraints: batch >= 1, rows > 0, cols > 0, rows % 16 == 0, cols % 16 == 0. */
+FP8BS_API fp8bs_status fp8_quant_128x128(const void* w, int64_t batch, int64_t rows, int64_t cols,
+                               int64_t ldw, uint8_t* q, uint8_t* qT, float* scales,
+                               void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* S3. 128x1 transposed requantization for the weight gradient               */
+/* [P1] bullet 2 (Wgrad takes its transposed operands re-tiled 128x1 from    */
+/* what the forward saved) and "Where casts are drawn" (a small requant box   */
+/* on the stash edge; backward vector kernels emit dY in both orientations).  */
+/* ------------------------------------------------------------------------ */
+/* Re-tiles a token-major tensor [rows x cols] (rows = tokens) into 128-token
+ * x 1-channel tiles and writes the payload transposed (tokens contiguous).
+ * src_mode FP8BS_SRC_BF16: src is BF16 [rows x cols], dense, src_scales NULL.
+ * src_mode FP8BS_SRC_E4M3: src is the E4M3 stash [rows x cols] written by
+ *           fp8_quant_1x128, src_scales its 1x128 scales (layout as above);
+ *           each element is decoded as fp32(dec(q) * s) before requantizing.
+ * group_offsets_host: optional HOST array of groups + 1 int32 row offsets
+ *           (offsets[0] = 0, non-decreasing, offsets[groups] = rows). Each
+ *           group's token tiles start at its own first row; a group's last
+ *           tile may be ragged. NULL (or groups == 0) means one group.
+ * qT      : E4M3 [cols x Mpad], Mpad = fp8bs_padded_tokens(rows, offsets, groups).
+ *           Group g occupies padded columns [P_g, P_g + 128 * ceil(T_g / 128))
+ *           with P_g the sum of the earlier groups' padded counts; the padding
+ *           bytes are written as 0x00.
+ * scalesT : fp32 [Mpad/128 x cols]; row j holds the scales of padded token tile j.
+ * Constraints: rows >= 0, cols > 0, cols % 16 == 0, groups <= FP8BS_MAX_GROUPS. */
+FP8BS_API fp8bs_status fp8_requant_128x1_T(int src_mode, const void* src, const float* src_scales,
+                                 int64_t rows, int64_t cols,
+                                 const int32_t* group_offsets_host, int32_t groups,
+                                 uint8_t* qT, float* scalesT, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* S4-S6. Block-scaled E4M3 GEMMs with per-128-K fp32 promotion              */
+/* [P1] bullet 1 (all three GEMMs E4M3; BF16 activations and input grads,     */
+/* FP32 weight grads); [P2] section 3 rows (a)-(b) and section 5: the tensor  */
+/* core accumulates 128 elements of K, the partial is scaled by s_a * s_b and */
+/* added to an fp32 accumulator, and the next 128 start from zero.            */
+/* The tensor-core partial over one 128-K block and the fp32 accumulation     */
+/* order are implementation details; results agree with the oracle within     */
+/* |d| <= 2e-3 * sum_k |a_k b_k| + 1e-6 (dequantized operands), plus one BF16 */
+/* rounding step for BF16 outputs.                                            */
+/* ------------------------------------------------------------------------ */
+
+/* Fprop: Y[i,j] = sum_b s_x[i,b] * s_w[b, j/128] * P_b[i,j].
+ * xq  : E4M3 [M x K] (fp8_quant_1x128 of X), sx its scales.
+ * wqT : E4M3 [N x K], the qT output of fp8_quant_128x128 on W [K x N].
+ * sw  : fp32 [K/128 x N/128] (the scales of that call).
+ * y   : BF16 [M x N], dense, overwritten.
+ * Constraints: M >= 0, K > 0, N > 0, K % 128 == 0, N % 128 == 0. */
+FP8BS_API fp8bs_status fp8_block_gemm_fprop(const uint8_t* xq, const float* sx,
+                                  const uint8_t* wqT, const float* sw,
+                                  int64_t M, int64_t N, int64_t K, void* y, void* stream);
+
+/* Dgrad: dX[i,k] = sum_b s_dy[i,b] * s_w[k/128, b] * P_b[i,k], contraction
+ * over the layer's N outputs.
+ * dyq : E4M3 [M x N] (fp8_quant_1x128 of dY), sdy its scales.
+ * wq  : E4M3 [K x N], the q output of fp8_quant_128x128 on W [K x N].
+ * sw  : fp32 [K/128 x N/128].
+ * dx  : BF16 [M x K], dense, overwritten.
+ * Constraints: M >= 0, K % 128 == 0, N % 128 == 0, K, N > 0. */
+FP8BS_API fp8bs_status fp8_block_gemm_dgrad(const uint8_t* dyq, const float* sdy,
+                                  const uint8_t* wq, const float* sw,
+                                  int64_t M, int64_t N, int64_t K, void* dx, void* stream);
+
+/* Wgrad: dW[n,k] = sum_b s_dyT[b,n] * s_xT[b,k] * P_b[n,k], contraction over
+ * T (padded) tokens, on the outputs of fp8_requant_128x1_T.
+ * dyqT : E4M3 [N x T], sdyT fp32 [T/128 x N].
+ * xqT  : E4M3 [K x T], sxT  fp32 [T/128 x K].
+ * dw   : FP32 [N x K], dense. accumulate = 0 overwrites, 1 adds into dw.
+ * Constraints: T >= 0, T % 128 == 0, N % 128 == 0, K % 128 == 0, N, K > 0.
+ * With T == 0 the result is zero (dw is zeroed unless accumulate). */
+FP8BS_API fp8bs_status fp8_block_gemm_wgrad(const uint8_t* dyqT, const float* sdyT,
+                                  const uint8_t* xqT, const float* sxT,
+                                  int64_t T, int64_t N, int64_t K, float* dw,
+                                  int accumulate, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* S7. Grouped (MoE expert) GEMMs                                             */
+/* The dense definitions above applied to each group (expert) g, whose token  */
+/* rows are [offsets[g], offsets[g+1]) (HOST int32 array, groups + 1 entries, */
+/* offsets[0] = 0, non-decreasing). Empty groups are allowed: they produce no */
+/* rows (Fprop, Dgrad) or a zero weight gradient (Wgrad).                     */
+/* ------------------------------------------------------------------------ */
+/* op = FP8BS_OP_FPROP:
+ *   a  = Xq [M x K] (M = offsets[groups]), sa its 1x128 scales;
+ *   b  = stacked WqT [groups x N x K], sb = stacked sw [groups x K/128 x N/128];
+ *   out = Y BF16 [M x N].
+ * op = FP8BS_OP_DGRAD (N is the contraction, K the output width):
+ *   a  = dYq [M x N], sa its 1x128 scales;
+ *   b  = stacked Wq [groups x K x N], sb = stacked sw [groups x K/128 x N/128];
+ *   out = dX BF16 [M x K].
+ * op = FP8BS_OP_WGRAD:
+ *   a  = dYqT [N x Mpad], sa = sdyT [Mpad/128 x N]  (fp8_requant_128x1_T with
+ *        the same offsets), b = XqT [K x Mpad], sb = sxT [Mpad/128 x K];
+ *   out = dW FP32 [groups x N x K]; accumulate as in fp8_block_gemm_wgrad.
+ * Constraints: 1 <= groups <= FP8BS_MAX_GROUPS, N % 128 == 0, K % 128 == 0. */
+FP8BS_API fp8bs_status fp8_block_gemm_grouped(int op, int32_t groups, const int32_t* offsets_host,
+                                    const uint8_t* a, const float* sa,
+                                    const uint8_t* b, const float* sb,
+                                    int64_t N, int64_t K, void* out, int accumulate,
+                                    void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Device status and failure detection                                       */
+/* ------------------------------------------------------------------------ */
+
+/* Synchronizes the current device, then returns the first device-side error
+ * recorded since the last reset (FP8BS_OK if none). reset != 0 clears it. */
+FP8BS_API fp8bs_status fp8bs_device_status(int reset);
+
+/* Upper bound, in nanoseconds, on any single pipeline wait inside the GEMM
+ * kernels (default 2e9). A wait that exceeds it records FP8BS_ERR_TIMEOUT,
+ * the kernel drains its in-flight copies and returns. Host-global setting. */
+FP8BS_API void fp8bs_set_wait_limit_ns(uint64_t ns);
+
+/* Launches one CTA that waits on a barrier nothing will arrive on, bounded
+ * by limit_ns; the wait gives up, records FP8BS_ERR_TIMEOUT in the device
+ * status word and the kernel returns. Exercises the timeout path without a
+ * fault; the context stays usable. */
+FP8BS_API fp8bs_status fp8bs_selftest_wait_timeout(uint64_t limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BS_H */

@@ -1,0 +1,116 @@
+"""CPU-side checks of the C ABI: the library builds for sm_103a, loads, exports
+every function declared in include/fp8bs.h, and its host-side logic (shape
+helpers, argument validation that runs before any device work) behaves as
+documented. No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import fp8_block_scaled_act_gb300 as fp8bs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8bs.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    fp8bs.build()
+    return fp8bs.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b([A-Za-z_0-9]+)\s*\(", text)
+    skip = {"if", "sizeof", "defined"}
+    return sorted({n for n in names if n.startswith("fp8") and n not in skip})
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ["fp8_quant_1x128", "fp8_quant_128x128", "fp8_requant_128x1_T",
+              "fp8_block_gemm_fprop", "fp8_block_gemm_dgrad", "fp8_block_gemm_wgrad",
+              "fp8_block_gemm_grouped", "fp8bs_device_status"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in _declared_functions():
+        assert hasattr(L, n), n
+        assert n in fp8bs.__all__, n
+
+
+def test_host_helpers(L):
+    assert fp8bs.fp8bs_version() >= 100
+    assert fp8bs.fp8bs_status_str(0) == "ok"
+    assert fp8bs.fp8bs_status_str(5) == "device wait timed out"
+    assert [fp8bs.fp8bs_scale_ld(r) for r in (0, 1, 4, 5, 4096)] == [0, 4, 4, 8, 4096]
+    assert fp8bs.fp8bs_padded_tokens(0) == 0
+    assert fp8bs.fp8bs_padded_tokens(1) == 128
+    assert fp8bs.fp8bs_padded_tokens(4096) == 4096
+    assert fp8bs.fp8bs_padded_tokens(400, [0, 0, 129, 130, 130, 400]) == 256 + 128 + 384
+    with pytest.raises(ValueError):
+        fp8bs.fp8bs_padded_tokens(10, [0, 5, 3, 10])       # decreasing
+    with pytest.raises(ValueError):
+        fp8bs.fp8bs_padded_tokens(10, [0, 5, 9])           # does not end at rows
+
+
+def test_padded_tokens_agrees_with_oracle_geometry():
+    import oracle
+    g = np.random.default_rng(0)
+    for _ in range(20):
+        counts = g.integers(0, 300, size=g.integers(1, 40))
+        off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+        assert fp8bs.fp8bs_padded_tokens(int(off[-1]), off) == oracle.padded_tokens(int(off[-1]), off)
+
+
+def test_argument_validation_before_device_work(L):
+    """Invalid shapes and pointers are rejected on the host, before any CUDA call."""
+    P = ctypes.c_void_p
+    buf = ctypes.create_string_buffer(1 << 12)
+    a16 = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
+    mis = ctypes.c_void_p(a16.value + 4)
+    ERR_ARG, ERR_ALIGN, ERR_SHAPE = 1, 2, 3
+    # quant 1x128
+    assert L.fp8_quant_1x128(a16, 4, 24, 24, a16, a16, None) == ERR_SHAPE   # cols % 16
+    assert L.fp8_quant_1x128(a16, -1, 32, 32, a16, a16, None) == ERR_ARG
+    assert L.fp8_quant_1x128(a16, 4, 32, 16, a16, a16, None) == ERR_ARG     # ld < cols
+    assert L.fp8_quant_1x128(None, 4, 32, 32, a16, a16, None) == ERR_ARG
+    assert L.fp8_quant_1x128(mis, 4, 32, 32, a16, a16, None) == ERR_ALIGN
+    assert L.fp8_quant_1x128(a16, 0, 32, 32, None, None, None) == 0         # empty: no work
+    # quant 128x128
+    assert L.fp8_quant_128x128(a16, 1, 24, 32, 32, a16, None, a16, None) == ERR_SHAPE
+    assert L.fp8_quant_128x128(a16, 0, 32, 32, 32, a16, None, a16, None) == ERR_ARG
+    assert L.fp8_quant_128x128(a16, 1, 32, 32, 32, a16, mis, a16, None) == ERR_ALIGN
+    # requant
+    assert L.fp8_requant_128x1_T(7, a16, None, 4, 32, None, 0, a16, a16, None) == ERR_ARG
+    assert L.fp8_requant_128x1_T(1, a16, None, 4, 32, None, 0, a16, a16, None) == ERR_ARG  # Q needs scales
+    bad = (ctypes.c_int32 * 3)(0, 5, 3)
+    assert L.fp8_requant_128x1_T(0, a16, None, 3, 32, bad, 2, a16, a16, None) == ERR_ARG
+    # gemms
+    assert L.fp8_block_gemm_fprop(a16, a16, a16, a16, 128, 256, 100, a16, None) == ERR_SHAPE
+    assert L.fp8_block_gemm_fprop(a16, a16, a16, a16, 128, 200, 128, a16, None) == ERR_SHAPE
+    assert L.fp8_block_gemm_fprop(a16, a16, a16, a16, 0, 256, 128, None, None) == 0
+    assert L.fp8_block_gemm_fprop(mis, a16, a16, a16, 8, 256, 128, a16, None) == ERR_ALIGN
+    assert L.fp8_block_gemm_dgrad(a16, a16, a16, a16, 8, 100, 128, a16, None) == ERR_SHAPE
+    assert L.fp8_block_gemm_wgrad(a16, a16, a16, a16, 100, 128, 128, a16, 0, None) == ERR_SHAPE
+    assert L.fp8_block_gemm_wgrad(a16, a16, a16, a16, 128, 128, 128, None, 0, None) == ERR_ARG
+    off = (ctypes.c_int32 * 3)(0, 4, 8)
+    assert L.fp8_block_gemm_grouped(9, 2, off, a16, a16, a16, a16, 128, 128, a16, 0, None) == ERR_ARG
+    assert L.fp8_block_gemm_grouped(0, 0, off, a16, a16, a16, a16, 128, 128, a16, 0, None) == ERR_ARG
+    assert L.fp8_block_gemm_grouped(0, 300, off, a16, a16, a16, a16, 128, 128, a16, 0, None) == ERR_ARG
+    assert L.fp8_block_gemm_grouped(0, 2, off, a16, a16, a16, a16, 128, 100, a16, 0, None) == ERR_SHAPE
+
+
+def test_product_path_does_not_import_oracle():
+    """The CUDA path's Python package never references the oracle."""
+    pkg = os.path.join(ROOT, "fp8_block_scaled_act_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "fp8bs_oracle" not in text, f

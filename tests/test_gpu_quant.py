@@ -1,0 +1,200 @@
+"""GPU parity of the quantizers (S1 1x128, S2 128x128, S3 128x1 transposed)
+against the CPU oracle: payload bytes and fp32 scale bits must be identical.
+Inputs are seeded (workloads.py); sizes span several tiles and ragged tails,
+plus the full-size tensors of the dense, backward and bandwidth workloads."""
+import numpy as np
+import pytest
+import torch
+
+import fp8_block_scaled_act_gb300 as fp8bs
+import oracle
+import workloads as wl
+from parity import np_, u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    fp8bs.build()
+    fp8bs.lib()
+    torch.cuda.init()
+    yield
+    assert fp8bs.fp8bs_device_status(reset=True) == 0
+
+
+def _special_inputs(R, C, seed):
+    """N(0,1) with 1% outliers, an all-zero tile, a tile of tiny negatives
+    (-0 results), a tile whose absmax is negative, and a tile with amax 448
+    (scale 1) holding exact E4M3 midpoints (ties to even)."""
+    x = wl.with_outliers((R, C), fraction=0.01, seed=seed)
+    w = min(C, 128)
+    if R > 0:
+        x[0, :w] = 0.0
+    if R > 1:
+        x[1, :w] = -1e-30
+        x[1, 0] = 1.0
+    if R > 2:
+        x[2, :w] = torch.linspace(-300.0, 2.0, w).to(torch.bfloat16)
+    if R > 3:
+        t = oracle.e4m3_table()
+        fin = t[:0x7E].astype(np.float64)
+        mids = ((fin[:-1] + fin[1:]) / 2)
+        mids = mids[(mids > 0.01) & (mids < 448)]
+        bf = torch.tensor(mids, dtype=torch.float32).to(torch.bfloat16)
+        exact = bf.float().numpy() == mids.astype(np.float32)
+        vals = bf[torch.from_numpy(exact)][: w - 1]
+        row = torch.zeros(w, dtype=torch.bfloat16)
+        row[0] = 448.0
+        row[1:1 + vals.numel()] = vals * torch.where(torch.arange(vals.numel()) % 2 == 0, 1.0, -1.0).to(torch.bfloat16)
+        x[3, :w] = row
+    return x
+
+
+def _gpu_quant_1x128(x):
+    xd = x.cuda()
+    q, sc = fp8bs.empty_quant_1x128(*x.shape)
+    fp8bs.fp8_quant_1x128(xd, q, sc)
+    torch.cuda.synchronize()
+    return np_(q), np_(sc)
+
+
+def _check_1x128(x):
+    R, C = x.shape
+    q, sc = _gpu_quant_1x128(x)
+    oq, osc = oracle.quant_1x128(u16(x))
+    assert np.array_equal(q, oq)
+    assert np.array_equal(sc[:, :R].view(np.uint32), osc[:, :R].view(np.uint32))
+
+
+@pytest.mark.parametrize("R,C", [(1, 128), (4, 16), (37, 640), (129, 304), (300, 16), (64, 1024)])
+def test_quant_1x128_small(R, C):
+    _check_1x128(_special_inputs(R, C, seed=R * 7 + C))
+
+
+def test_quant_1x128_negative_zero_and_ties():
+    x = _special_inputs(8, 256, seed=3)
+    q, sc = _gpu_quant_1x128(x)
+    assert np.all(q[1, 1:128] == 0x80)                 # tiny negatives -> -0
+    assert q[1, 0] == 0x7E
+    assert sc[0, 0] == 1.0 and np.all(q[0, :128] == 0) # all-zero tile
+    assert sc[0, 3] == 1.0                             # amax 448 -> scale 1
+    oq, _ = oracle.quant_1x128(u16(x))
+    assert np.array_equal(q[3], oq[3])                 # exact midpoints: ties to even
+
+
+def test_quant_1x128_dense_activation_full():
+    x = wl.dense(K=7168, M=4096, N=128)["X"]
+    _check_1x128(x)
+
+
+def test_quant_1x128_backward_grad_full():
+    _check_1x128(wl.normal((4096, 2048), std=wl.DY_STD, seed=2))
+
+
+@pytest.mark.slow
+def test_quant_1x128_stream_16k_full():
+    _check_1x128(wl.quant_stream()["X"])
+
+
+def _gpu_quant_128x128(w):
+    wd = w.cuda()
+    batch = w.shape[0] if w.dim() == 3 else 1
+    q, qT, sc = fp8bs.empty_quant_128x128(w.shape[-2], w.shape[-1], batch=batch)
+    fp8bs.fp8_quant_128x128(wd, q, qT, sc)
+    torch.cuda.synchronize()
+    return np_(q), np_(qT), np_(sc)
+
+
+@pytest.mark.parametrize("R,C", [(128, 128), (512, 256), (144, 400), (16, 16), (384, 1040)])
+def test_quant_128x128_small(R, C):
+    w = _special_inputs(R, C, seed=R + C)
+    q, qT, sc = _gpu_quant_128x128(w)
+    oq, osc = oracle.quant_128x128(u16(w))
+    assert np.array_equal(q, oq)
+    assert np.array_equal(sc.view(np.uint32), osc.view(np.uint32))
+    assert np.array_equal(qT, oq.T)
+
+
+def test_quant_128x128_batched_experts():
+    w = wl.normal((3, 256, 384), std=wl.W_STD, seed=5)
+    q, qT, sc = _gpu_quant_128x128(w)
+    for e in range(3):
+        oq, osc = oracle.quant_128x128(u16(w[e]))
+        assert np.array_equal(q[e], oq)
+        assert np.array_equal(qT[e], oq.T)
+        assert np.array_equal(sc[e], osc)
+
+
+def test_quant_128x128_dense_weight_full():
+    w = wl.dense(M=128)["W"]
+    q, qT, sc = _gpu_quant_128x128(w)
+    oq, osc = oracle.quant_128x128(u16(w))
+    assert np.array_equal(q, oq)
+    assert np.array_equal(sc.view(np.uint32), osc.view(np.uint32))
+    assert np.array_equal(qT, oq.T)
+
+
+def _gpu_requant(src, src_scales=None, offsets=None):
+    qT, scT = fp8bs.empty_requant_128x1_T(src.shape[0], src.shape[1], offsets)
+    fp8bs.fp8_requant_128x1_T(src, src_scales, qT, scT, offsets=offsets)
+    torch.cuda.synchronize()
+    return np_(qT), np_(scT)
+
+
+@pytest.mark.parametrize("M,C,counts", [
+    (128, 128, None), (300, 256, None), (1, 16, None), (257, 400, None),
+    (400, 128, [0, 129, 1, 0, 270]), (131, 144, [131]), (260, 256, [0, 0, 260, 0]),
+])
+def test_requant_bf16_source(M, C, counts):
+    x = _special_inputs(M, C, seed=M + 3 * C)
+    off = None if counts is None else wl.offsets_from_counts(counts)
+    qT, scT = _gpu_requant(x.cuda(), None, off)
+    oqT, oscT = oracle.requant_128x1_T(u16(x), offsets=off)
+    assert np.array_equal(qT, oqT)
+    assert np.array_equal(scT.view(np.uint32), oscT.view(np.uint32))
+
+
+@pytest.mark.parametrize("M,C,counts", [
+    (128, 128, None), (300, 256, None), (257, 400, None), (400, 128, [0, 129, 1, 0, 270]),
+])
+def test_requant_e4m3_stash_source(M, C, counts):
+    x = _special_inputs(M, C, seed=M + 5 * C)
+    xq, sx = fp8bs.empty_quant_1x128(M, C)
+    fp8bs.fp8_quant_1x128(x.cuda(), xq, sx)
+    off = None if counts is None else wl.offsets_from_counts(counts)
+    qT, scT = _gpu_requant(xq, sx, off)
+    oq, osc = oracle.quant_1x128(u16(x))
+    oqT, oscT = oracle.requant_128x1_T(oq, osc, offsets=off)
+    assert np.array_equal(qT, oqT)
+    assert np.array_equal(scT.view(np.uint32), oscT.view(np.uint32))
+
+
+def test_requant_backward_full():
+    """The backward workload's two requants: X from its E4M3 stash, dY from BF16."""
+    d = wl.backward()
+    x, dy = d["X"], d["dY"]
+    xq, sx = fp8bs.empty_quant_1x128(*x.shape)
+    fp8bs.fp8_quant_1x128(x.cuda(), xq, sx)
+    qT, scT = _gpu_requant(xq, sx)
+    oq, osc = oracle.quant_1x128(u16(x))
+    oqT, oscT = oracle.requant_128x1_T(oq, osc)
+    assert np.array_equal(qT, oqT) and np.array_equal(scT, oscT)
+    qT, scT = _gpu_requant(dy.cuda())
+    oqT, oscT = oracle.requant_128x1_T(u16(dy))
+    assert np.array_equal(qT, oqT) and np.array_equal(scT, oscT)
+
+
+def test_requant_moe_grouped_full_tokens():
+    d = wl.moe(with_weights=False)
+    dy = d["dY"]
+    qT, scT = _gpu_requant(dy.cuda(), None, d["offsets"])
+    oqT, oscT = oracle.requant_128x1_T(u16(dy), offsets=d["offsets"])
+    assert np.array_equal(qT, oqT) and np.array_equal(scT, oscT)
+
+
+def test_quantizers_are_deterministic():
+    x = _special_inputs(300, 512, seed=9)
+    a = _gpu_quant_1x128(x)
+    b = _gpu_quant_1x128(x)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
