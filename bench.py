@@ -1,0 +1,595 @@
+"""Benchmark of the fine-grained FP8 linear layer on GB300.
+
+One step is one pass of the layer's whole data path over one batch of
+synthetic input: the weight's 128x128 quantization (with its transposed
+copy), the 1x128 quantization of X, Fprop, the 1x128 quantization of dY,
+Dgrad, the 128x1 transposed requants of X (from its E4M3 stash) and dY (from
+BF16), and Wgrad. Default workload: X 4096x7168 (N(0,1) with 0.1% outliers),
+W 7168x2048 (N(0,0.02^2)), dY 4096x2048 (N(0,1e-3^2)). ``--workload moe``
+runs the grouped MoE expert pass instead (32 experts, 8192 routed rows).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Timing: W untimed warm-up steps, then exactly K steps, each bracketed by CUDA
+events on the launching stream with an L2 flush (a 256 MiB write) between
+steps outside the events; per-kernel events inside each step give the
+roofline figures. Under torchrun each rank runs its own replica (weak
+scaling, no collective on the data path); the step time is the max over
+ranks. Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FP8 block-scaled GEMM TFLOP/s (% FP8 peak); quantize GB/s (% HBM BW)"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0    # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ---------------------------------------------------------------------------
+# workload description (shared by both arms)
+# ---------------------------------------------------------------------------
+
+def dense_shapes():
+    return {"M": 4096, "K": 7168, "N": 2048}
+
+
+def step_work(M, K, N):
+    """Algorithmic FLOPs of the three GEMMs and algorithmic bytes of each
+    kernel of one dense step (bytes read + written, scales included)."""
+    gemm_flops = 2.0 * M * N * K
+    s_ld = (M + 3) // 4 * 4
+    b = {
+        "quant_128x128(W)": K * N * 2 + 2 * K * N + 4 * (K // 128) * (N // 128),
+        "quant_1x128(X)": M * K * 2 + M * K + 4 * (K // 128) * s_ld,
+        "fprop": M * K + N * K + 4 * (K // 128) * (s_ld + N // 128) + 2 * M * N,
+        "quant_1x128(dY)": M * N * 2 + M * N + 4 * (N // 128) * s_ld,
+        "dgrad": M * N + K * N + 4 * (N // 128) * s_ld + 4 * (K // 128) * (N // 128) + 2 * M * K,
+        "requant_128x1_T(Xq)": M * K + 4 * (K // 128) * s_ld + M * K + 4 * (M // 128) * K,
+        "requant_128x1_T(dY)": M * N * 2 + M * N + 4 * (M // 128) * N,
+        "wgrad": N * M + K * M + 4 * (M // 128) * (N + K) + 4 * N * K,
+    }
+    flops = {"fprop": gemm_flops, "dgrad": gemm_flops, "wgrad": gemm_flops}
+    return flops, b
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (host logic; gloo-testable on CPU)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device="cpu") -> float:
+    """Max of a per-rank float over all ranks (identity without a group)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_throughput(per_rank_work: float, world: int, max_seconds: float) -> float:
+    """Work all ranks processed divided by the slowest rank's time."""
+    return per_rank_work * world / max_seconds
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+def smi_gpu_id(local: int) -> str:
+    """nvidia-smi's id for this rank's GPU (CUDA_VISIBLE_DEVICES remaps indices)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local < len(ids):
+            return ids[local]
+    return str(local)
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [v for v in sm if mx and v >= 0.3 * max(mx)]
+        return {"sm_mhz": statistics.median(loaded or sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+class DenseStep:
+    """Buffers and the launch sequence of one dense fwd+bwd step."""
+
+    def __init__(self, fp8bs, torch, device, M, K, N, seed=0):
+        self.fp8bs, self.torch, self.dev = fp8bs, torch, device
+        self.M, self.K, self.N = M, K, N
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        X = torch.randn(M, K, device=device, generator=g)
+        n_out = int(round(1e-3 * M * K))
+        pos = torch.randperm(M * K, device=device, generator=g)[:n_out]
+        mag = torch.rand(n_out, device=device, generator=g) * 150.0 + 50.0
+        sgn = torch.where(torch.rand(n_out, device=device, generator=g) < 0.5, -1.0, 1.0)
+        X.view(-1)[pos] = mag * sgn
+        self.X = X.to(torch.bfloat16)
+        self.W = (torch.randn(K, N, device=device, generator=g) * 0.02).to(torch.bfloat16)
+        self.dY = (torch.randn(M, N, device=device, generator=g) * 1e-3).to(torch.bfloat16)
+        e = fp8bs
+        self.xq, self.sx = e.empty_quant_1x128(M, K, device)
+        self.wq, self.wqT, self.sw = e.empty_quant_128x128(K, N, device=device)
+        self.Y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+        self.dyq, self.sdy = e.empty_quant_1x128(M, N, device)
+        self.dX = torch.empty(M, K, dtype=torch.bfloat16, device=device)
+        self.xT, self.sxT = e.empty_requant_128x1_T(M, K, device=device)
+        self.dyT, self.sdyT = e.empty_requant_128x1_T(M, N, device=device)
+        self.dW = torch.empty(N, K, dtype=torch.float32, device=device)
+        self.names = ["quant_128x128(W)", "quant_1x128(X)", "fprop", "quant_1x128(dY)", "dgrad",
+                      "requant_128x1_T(Xq)", "requant_128x1_T(dY)", "wgrad"]
+
+    def work(self):
+        return step_work(self.M, self.K, self.N)
+
+    def io(self):
+        return (self.X, self.W, self.dY), (self.Y, self.dX, self.dW)
+
+    def describe(self):
+        M, K, N = self.M, self.K, self.N
+        return {"workload": f"dense FP8 linear fwd+bwd X {M}x{K}, W {K}x{N}, dY {M}x{N}",
+                "M": M, "K": K, "N": N}
+
+    def launches(self):
+        e = self.fp8bs
+        return [
+            lambda: e.fp8_quant_128x128(self.W, self.wq, self.wqT, self.sw),
+            lambda: e.fp8_quant_1x128(self.X, self.xq, self.sx),
+            lambda: e.fp8_block_gemm_fprop(self.xq, self.sx, self.wqT, self.sw, self.Y),
+            lambda: e.fp8_quant_1x128(self.dY, self.dyq, self.sdy),
+            lambda: e.fp8_block_gemm_dgrad(self.dyq, self.sdy, self.wq, self.sw, self.dX),
+            lambda: e.fp8_requant_128x1_T(self.xq, self.sx, self.xT, self.sxT),
+            lambda: e.fp8_requant_128x1_T(self.dY, None, self.dyT, self.sdyT),
+            lambda: e.fp8_block_gemm_wgrad(self.dyT, self.sdyT, self.xT, self.sxT, self.dW),
+        ]
+
+
+class MoeStep:
+    """Grouped MoE expert pass: 1x128 quantization of X, A and dY, batched
+    128x128 quantization of the expert weights, Fprop of the up and down
+    projections, Dgrad and Wgrad of the down projection (with the grouped
+    128x1 requants of dY and A)."""
+
+    def __init__(self, fp8bs, torch, device, tokens=8192, experts=32, hidden=7168, inter=2048,
+                 up=4096, seed=0):
+        import workloads as wl
+        self.fp8bs, self.torch, self.dev = fp8bs, torch, device
+        counts = wl.expert_counts(tokens, experts, seed=seed)
+        self.offsets = wl.offsets_from_counts(counts)
+        self.counts = counts
+        self.T, self.G, self.H, self.I, self.U = tokens, experts, hidden, inter, up
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        bf = torch.bfloat16
+        self.X = torch.randn(tokens, hidden, device=device, generator=g).to(bf)
+        self.A = torch.randn(tokens, inter, device=device, generator=g).to(bf)
+        self.dY = (torch.randn(tokens, hidden, device=device, generator=g) * 1e-3).to(bf)
+        self.Wu = (torch.randn(experts, hidden, up, device=device, generator=g) * 0.02).to(bf)
+        self.Wd = (torch.randn(experts, inter, hidden, device=device, generator=g) * 0.02).to(bf)
+        e = fp8bs
+        self.xq, self.sx = e.empty_quant_1x128(tokens, hidden, device)
+        self.aq, self.sa = e.empty_quant_1x128(tokens, inter, device)
+        self.dyq, self.sdy = e.empty_quant_1x128(tokens, hidden, device)
+        self.wuq, self.wuqT, self.swu = e.empty_quant_128x128(hidden, up, batch=experts, device=device)
+        self.wdq, self.wdqT, self.swd = e.empty_quant_128x128(inter, hidden, batch=experts, device=device)
+        self.Yu = torch.empty(tokens, up, dtype=bf, device=device)
+        self.Yd = torch.empty(tokens, hidden, dtype=bf, device=device)
+        self.dA = torch.empty(tokens, inter, dtype=bf, device=device)
+        self.dyT, self.sdyT = e.empty_requant_128x1_T(tokens, hidden, self.offsets, device)
+        self.aT, self.saT = e.empty_requant_128x1_T(tokens, inter, self.offsets, device)
+        self.dWd = torch.empty(experts, hidden, inter, dtype=torch.float32, device=device)
+        self.names = ["quant_128x128(W_up)", "quant_128x128(W_down)", "quant_1x128(X)",
+                      "grouped_fprop_up", "quant_1x128(A)", "grouped_fprop_down", "quant_1x128(dY)",
+                      "grouped_dgrad_down", "requant_128x1_T(dY)", "requant_128x1_T(Aq)",
+                      "grouped_wgrad_down"]
+
+    def work(self):
+        T, G, H, I, U = self.T, self.G, self.H, self.I, self.U
+        s_ld = (T + 3) // 4 * 4
+        mp = int(self.fp8bs.fp8bs_padded_tokens(T, self.offsets))
+        flops = {"grouped_fprop_up": 2.0 * T * H * U, "grouped_fprop_down": 2.0 * T * I * H,
+                 "grouped_dgrad_down": 2.0 * T * H * I, "grouped_wgrad_down": 2.0 * T * H * I}
+        b = {
+            "quant_128x128(W_up)": G * H * U * 4 + 4 * G * (H // 128) * (U // 128),
+            "quant_128x128(W_down)": G * I * H * 4 + 4 * G * (I // 128) * (H // 128),
+            "quant_1x128(X)": T * H * 3 + 4 * (H // 128) * s_ld,
+            "grouped_fprop_up": T * H + G * U * H + 2 * T * U,
+            "quant_1x128(A)": T * I * 3 + 4 * (I // 128) * s_ld,
+            "grouped_fprop_down": T * I + G * H * I + 2 * T * H,
+            "quant_1x128(dY)": T * H * 3 + 4 * (H // 128) * s_ld,
+            "grouped_dgrad_down": T * H + G * I * H + 2 * T * I,
+            "requant_128x1_T(dY)": T * H * 2 + H * mp + 4 * (mp // 128) * H,
+            "requant_128x1_T(Aq)": T * I + 4 * (I // 128) * s_ld + I * mp + 4 * (mp // 128) * I,
+            "grouped_wgrad_down": (H + I) * mp + 4 * G * H * I,
+        }
+        return flops, b
+
+    def launches(self):
+        e, off, G, H, I, U = self.fp8bs, self.offsets, self.G, self.H, self.I, self.U
+        return [
+            lambda: e.fp8_quant_128x128(self.Wu, self.wuq, self.wuqT, self.swu),
+            lambda: e.fp8_quant_128x128(self.Wd, self.wdq, self.wdqT, self.swd),
+            lambda: e.fp8_quant_1x128(self.X, self.xq, self.sx),
+            lambda: e.fp8_block_gemm_grouped(e.OP_FPROP, off, self.xq, self.sx, self.wuqT, self.swu,
+                                             self.Yu, U, H),
+            lambda: e.fp8_quant_1x128(self.A, self.aq, self.sa),
+            lambda: e.fp8_block_gemm_grouped(e.OP_FPROP, off, self.aq, self.sa, self.wdqT, self.swd,
+                                             self.Yd, H, I),
+            lambda: e.fp8_quant_1x128(self.dY, self.dyq, self.sdy),
+            lambda: e.fp8_block_gemm_grouped(e.OP_DGRAD, off, self.dyq, self.sdy, self.wdq, self.swd,
+                                             self.dA, H, I),
+            lambda: e.fp8_requant_128x1_T(self.dY, None, self.dyT, self.sdyT, offsets=off),
+            lambda: e.fp8_requant_128x1_T(self.aq, self.sa, self.aT, self.saT, offsets=off),
+            lambda: e.fp8_block_gemm_grouped(e.OP_WGRAD, off, self.dyT, self.sdyT, self.aT, self.saT,
+                                             self.dWd, H, I),
+        ]
+
+    def io(self):
+        return (self.X, self.A, self.dY, self.Wu, self.Wd), (self.Yu, self.Yd, self.dA, self.dWd)
+
+    def describe(self):
+        return {"workload": (f"grouped MoE experts: {self.G} experts, {self.T} routed rows "
+                             f"(Dirichlet(0.5) counts), W_up {self.H}x{self.U}, W_down {self.I}x{self.H}"),
+                "experts": self.G, "tokens": self.T, "hidden": self.H, "inter": self.I, "up": self.U}
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import fp8_block_scaled_act_gb300 as fp8bs
+
+    fp8bs.build()
+    fp8bs.lib()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    M, K, N = dense_shapes().values()
+    if args.workload == "moe":
+        step = MoeStep(fp8bs, torch, device, seed=rank)
+    else:
+        step = DenseStep(fp8bs, torch, device, M, K, N, seed=rank)
+    launches = step.launches()
+    flops, kbytes = step.work()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        for f in launches:
+            f()
+    torch.cuda.synchronize()
+    if fp8bs.fp8bs_device_status(reset=True) != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    nk = len(launches)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    clocks = ClockSampler(smi_gpu_id(local))
+    barrier(dist, local)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for s in range(args.steps):
+        flush.fill_(s & 0xFF)                      # L2 flush, outside the step's events
+        ev[s][0].record(stream)
+        for i, f in enumerate(launches):
+            f()
+            ev[s][i + 1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(dist, local)
+    status = fp8bs.fp8bs_device_status(reset=True)
+    if status != 0:
+        raise RuntimeError(f"device status {status} during the timed steps")
+
+    step_ms = [ev[s][0].elapsed_time(ev[s][nk]) for s in range(args.steps)]
+    kern_ms = {step.names[i]: [ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps)]
+               for i in range(nk)}
+    total_s = max_over_ranks(dist, sum(step_ms) / 1e3, device=device)
+    step_flops = sum(flops.values())
+    value = whole_job_throughput(step_flops * args.steps, world, total_s) / 1e12
+
+    peaks, peak_src = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    hbm_peak = peaks["hbm_gbs"]
+    kernels = {}
+    for name, ts in kern_ms.items():
+        avg = sum(ts) / len(ts)
+        d = {"ms": round(avg, 5), "share": round(sum(ts) / sum(step_ms), 4)}
+        if name in flops:
+            tf = flops[name] / (avg * 1e-3) / 1e12
+            d.update(tflops=round(tf, 1), frac_fp8_peak=round(tf / fp8_peak, 4))
+        else:
+            gbs = kbytes[name] / (avg * 1e-3) / 1e9
+            d.update(gbs=round(gbs, 1), frac_hbm=round(gbs / hbm_peak, 4))
+        kernels[name] = d
+    dom = max(kern_ms, key=lambda n: sum(kern_ms[n]))
+    dom_avg = sum(kern_ms[dom]) / len(kern_ms[dom])
+    traffic = load_traffic(dom)
+    if dom in flops:
+        ach = flops[dom] / (dom_avg * 1e-3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": round(fp8_peak, 1),
+                "unit": "TFLOP/s", "frac": round(ach / fp8_peak, 4), "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 burst x {FP8_OVER_BF16:g} (nominal fp8/bf16 ratio)"}
+    else:
+        ach = kbytes[dom] / (dom_avg * 1e-3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak,
+                "unit": "GB/s", "frac": round(ach / hbm_peak, 4), "traffic": traffic,
+                "peak_source": peak_src}
+
+    quant_names = [n for n in step.names if n not in flops]
+    q_bytes = sum(kbytes[n] for n in quant_names)
+    q_ms = sum(sum(kern_ms[n]) for n in quant_names) / args.steps
+    e2e = measure_e2e(args, fp8bs, torch, step, device, step_flops, world, dist)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_s * 1e3 / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic (seeded normal; 0.1% outliers in X)" if args.workload == "dense"
+                else "synthetic (seeded normal; Dirichlet(0.5) expert counts)",
+        "config": dict(step.describe(),
+                       parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
+                       l2="flushed between steps (256 MiB write outside the step events)"),
+        "quantize_gbs": round(q_bytes / (q_ms * 1e-3) / 1e9, 1),
+        "quantize_frac_hbm": round(q_bytes / (q_ms * 1e-3) / 1e9 / hbm_peak, 4),
+        "gemm_frac_fp8_peak": round(value / fp8_peak, 4),
+        "roofline": roof, "kernels": kernels, "e2e": e2e,
+        "gpu_launches": nk * args.steps, "clocks": clk,
+    }
+    if rank == 0:
+        if args.workload == "dense":
+            line["cpu_baseline"] = cpu_baseline(M, K, N, args.cpu_sample)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def load_traffic(kernel_name):
+    """DRAM bytes per launch of `kernel_name` from the committed ncu summary,
+    if one exists for the current sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    return t.get(kernel_name)
+
+
+def measure_e2e(args, fp8bs, torch, step, device, step_flops, world, dist):
+    """Same step through the public API with host buffers: pinned-host inputs
+    copied in, the step, and the outputs (Y, dX, dW) copied back, per step."""
+    d_in, d_out = step.io()
+    h_in = [t.cpu().pin_memory() for t in d_in]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in d_out]
+    launches = step.launches()
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for h, d in zip(h_in, d_in):
+            d.copy_(h, non_blocking=True)
+        for f in launches:
+            f()
+        for h, d in zip(h_out, d_out):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    n = max(1, args.steps)
+    barrier(dist, device.index)
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(n):
+        one()
+    e.record(stream)
+    torch.cuda.synchronize()
+    sec = max_over_ranks(dist, s.elapsed_time(e) / 1e3, device=device)
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    return {"value": round(whole_job_throughput(step_flops * n, world, sec) / 1e12, 2), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(sec * 1e3 / n, 4)}
+
+
+# ---------------------------------------------------------------------------
+# the oracle as CPU baseline / reference arm
+# ---------------------------------------------------------------------------
+
+def oracle_step_sample(M, K, N, frac_rows, seed=0):
+    """The dense step on the CPU oracle, restricted to a leading fraction of
+    the rows of every output (and of every quantizer input). Returns
+    (seconds, fraction of the full step's work it covers, cores)."""
+    import numpy as np
+    import oracle
+    import workloads as wl
+
+    m = max(128, int(M * frac_rows) // 128 * 128)
+    nrows_w = max(128, int(N * frac_rows) // 128 * 128)
+    d = wl.backward(M=m, K=K, N=N, seed=seed)
+    x, w, dy = wl.bits(d["X"]), wl.bits(d["W"]), wl.bits(d["dY"])
+    t0 = time.perf_counter()
+    wq, sw = oracle.quant_128x128(w)
+    xq, sx = oracle.quant_1x128(x)
+    oracle.fprop(xq, sx, wq, sw)
+    dyq, sdy = oracle.quant_1x128(dy)
+    oracle.dgrad(dyq, sdy, wq, sw)
+    xT, sxT = oracle.requant_128x1_T(xq, sx)
+    dyT, sdyT = oracle.requant_128x1_T(dy)
+    # Wgrad: rows [0, nrows_w) of dW over the m sampled tokens
+    nn = np.repeat(np.arange(nrows_w), K)
+    kk = np.tile(np.arange(K), nrows_w)
+    oracle.wgrad(dyT, sdyT, xT, sxT, nn, kk)
+    sec = time.perf_counter() - t0
+    # fraction of the full step's GEMM work done (the quantizers scale alike)
+    work_full = 3.0 * M * N * K
+    work_done = 2.0 * m * N * K + nrows_w * K * m
+    return sec, work_done / work_full, oracle.num_threads(), m, nrows_w
+
+
+def cpu_baseline(M, K, N, frac):
+    import oracle
+    oracle.build()
+    sec, covered, cores, m, nw = oracle_step_sample(M, K, N, frac)
+    flops = 3 * 2.0 * M * N * K * covered
+    return {"value": round(flops / sec / 1e12, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"dense step on {m} of {M} token rows (all quantizers and Fprop/Dgrad), "
+                       f"Wgrad rows [0,{nw}) of dW over those tokens; {covered:.4f} of the step's "
+                       f"GEMM work in {sec:.2f} s; throughput = covered FLOPs / wall time")}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    M, K, N = dense_shapes().values()
+    for _ in range(args.warmup):
+        oracle_step_sample(M, K, N, args.cpu_sample)
+    secs, covs = [], []
+    cores = 1
+    for s in range(args.steps):
+        sec, cov, cores, m, nw = oracle_step_sample(M, K, N, args.cpu_sample, seed=s)
+        secs.append(sec)
+        covs.append(cov)
+    flops = sum(3 * 2.0 * M * N * K * c for c in covs)
+    value = flops / sum(secs) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sum(secs) * 1e3 / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": f"dense FP8 linear fwd+bwd X {M}x{K}, W {K}x{N}, dY {M}x{N}",
+                   "M": M, "K": K, "N": N, "parallelism": "CPU oracle on rank 0"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"each step: the dense step on {m} of {M} token rows and "
+                                   f"{nw} rows of dW ({covs[0]:.4f} of the GEMM work)"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["dense", "moe"], default="dense",
+                    help="dense: the linear layer's fwd+bwd (default); moe: grouped expert pass")
+    ap.add_argument("--cpu-sample", type=float, default=1.0 / 32,
+                    help="fraction of token rows the oracle runs per step")
+    args = ap.parse_args(argv)
+    if args.impl == "ours":
+        args.warmup = max(args.warmup, 3)     # timing rule: at least 3 warm-up steps
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

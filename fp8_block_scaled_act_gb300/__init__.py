@@ -164,11 +164,12 @@ def empty_quant_1x128(rows: int, cols: int, device="cuda"):
     return q, sc
 
 
-def empty_quant_128x128(rows: int, cols: int, batch: int = 1, with_transpose: bool = True,
-                        device="cuda"):
+def empty_quant_128x128(rows: int, cols: int, batch: Optional[int] = None,
+                        with_transpose: bool = True, device="cuda"):
     """(q [batch x rows x cols], qT [batch x cols x rows] or None, scales
-    [batch x ceil(rows/128) x ceil(cols/128)]); the batch dim is dropped when batch == 1."""
-    shp = (batch,) if batch > 1 else ()
+    [batch x ceil(rows/128) x ceil(cols/128)]); without ``batch`` the tensors
+    have no batch dimension."""
+    shp = (int(batch),) if batch is not None else ()
     q = torch.empty(shp + (rows, cols), dtype=torch.uint8, device=device)
     qT = torch.empty(shp + (cols, rows), dtype=torch.uint8, device=device) if with_transpose else None
     sc = torch.empty(shp + ((rows + 127) // 128, (cols + 127) // 128), dtype=torch.float32,
@@ -206,7 +207,9 @@ def fp8_quant_128x128(w: torch.Tensor, q: torch.Tensor, qT: Optional[torch.Tenso
         _need(qT, torch.uint8, "qT")
     batch = w.shape[0] if w.dim() == 3 else 1
     rows, cols = w.shape[-2:]
-    if q.shape != w.shape or (qT is not None and qT.shape[-2:] != (cols, rows)):
+    nb = ((rows + 127) // 128) * ((cols + 127) // 128)
+    if (q.numel() != w.numel() or q.shape[-2:] != (rows, cols) or scales.numel() != batch * nb
+            or (qT is not None and (qT.numel() != w.numel() or qT.shape[-2:] != (cols, rows)))):
         raise ValueError("output shapes do not match empty_quant_128x128")
     _check("fp8_quant_128x128", lib().fp8_quant_128x128(_ptr(w), batch, rows, cols, cols, _ptr(q),
                                                         _ptr(qT), _ptr(scales), _stream(stream)))

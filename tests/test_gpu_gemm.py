@@ -43,7 +43,7 @@ def q1x128(x_cpu):
 
 
 def q128(w_cpu):
-    batch = w_cpu.shape[0] if w_cpu.dim() == 3 else 1
+    batch = w_cpu.shape[0] if w_cpu.dim() == 3 else None
     q, qT, s = fp8bs.empty_quant_128x128(w_cpu.shape[-2], w_cpu.shape[-1], batch=batch)
     fp8bs.fp8_quant_128x128(w_cpu.cuda(), q, qT, s)
     return q, qT, s

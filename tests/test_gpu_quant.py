@@ -99,7 +99,7 @@ def test_quant_1x128_stream_16k_full():
 
 def _gpu_quant_128x128(w):
     wd = w.cuda()
-    batch = w.shape[0] if w.dim() == 3 else 1
+    batch = w.shape[0] if w.dim() == 3 else None
     q, qT, sc = fp8bs.empty_quant_128x128(w.shape[-2], w.shape[-1], batch=batch)
     fp8bs.fp8_quant_128x128(wd, q, qT, sc)
     torch.cuda.synchronize()
