@@ -571,6 +571,72 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+NCU_CASES = ("fprop", "dgrad", "wgrad", "quant_1x128", "quant_128x128", "requant_e4m3",
+             "requant_bf16")
+
+
+def run_ncu_case(name):
+    """One kernel kind, launched three times on a small case for ncu (inputs
+    larger than L2, well under a few GB on the device)."""
+    import torch
+    import fp8_block_scaled_act_gb300 as e
+    e.build()
+    e.lib()
+    dev = "cuda"
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    bf = torch.bfloat16
+
+    def rnd(*shape, std=1.0):
+        return (torch.randn(*shape, device=dev, generator=g) * std).to(bf)
+
+    M, K, N = 16384, 7168, 2048
+    if name == "fprop":
+        xq, sx = e.empty_quant_1x128(M, K)
+        e.fp8_quant_1x128(rnd(M, K), xq, sx)
+        wq, wqT, sw = e.empty_quant_128x128(K, N)
+        e.fp8_quant_128x128(rnd(K, N, std=0.02), wq, wqT, sw)
+        y = torch.empty(M, N, dtype=bf, device=dev)
+        runs = lambda: e.fp8_block_gemm_fprop(xq, sx, wqT, sw, y)
+    elif name == "dgrad":
+        dyq, sdy = e.empty_quant_1x128(M, N)
+        e.fp8_quant_1x128(rnd(M, N, std=1e-3), dyq, sdy)
+        wq, wqT, sw = e.empty_quant_128x128(K, N)
+        e.fp8_quant_128x128(rnd(K, N, std=0.02), wq, wqT, sw)
+        dx = torch.empty(M, K, dtype=bf, device=dev)
+        runs = lambda: e.fp8_block_gemm_dgrad(dyq, sdy, wq, sw, dx)
+    elif name == "wgrad":
+        xT, sxT = e.empty_requant_128x1_T(M, K)
+        e.fp8_requant_128x1_T(rnd(M, K), None, xT, sxT)
+        dyT, sdyT = e.empty_requant_128x1_T(M, N)
+        e.fp8_requant_128x1_T(rnd(M, N, std=1e-3), None, dyT, sdyT)
+        dw = torch.empty(N, K, dtype=torch.float32, device=dev)
+        runs = lambda: e.fp8_block_gemm_wgrad(dyT, sdyT, xT, sxT, dw)
+    elif name == "quant_1x128":
+        x = rnd(16384, 16384)
+        q, s = e.empty_quant_1x128(16384, 16384)
+        runs = lambda: e.fp8_quant_1x128(x, q, s)
+    elif name == "quant_128x128":
+        w = rnd(32, 2048, 7168, std=0.02)
+        q, qT, s = e.empty_quant_128x128(2048, 7168, batch=32)
+        runs = lambda: e.fp8_quant_128x128(w, q, qT, s)
+    elif name == "requant_e4m3":
+        xq, sx = e.empty_quant_1x128(M, K)
+        e.fp8_quant_1x128(rnd(M, K), xq, sx)
+        xT, sxT = e.empty_requant_128x1_T(M, K)
+        runs = lambda: e.fp8_requant_128x1_T(xq, sx, xT, sxT)
+    else:
+        x = rnd(M, K)
+        xT, sxT = e.empty_requant_128x1_T(M, K)
+        runs = lambda: e.fp8_requant_128x1_T(x, None, xT, sxT)
+    for _ in range(3):
+        runs()
+    torch.cuda.synchronize()
+    if e.fp8bs_device_status(reset=True) != 0:
+        raise RuntimeError("device status error")
+    print(f"ncu case {name}: ok")
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -581,7 +647,12 @@ def main(argv=None):
                     help="dense: the linear layer's fwd+bwd (default); moe: grouped expert pass")
     ap.add_argument("--cpu-sample", type=float, default=1.0 / 32,
                     help="fraction of token rows the oracle runs per step")
+    ap.add_argument("--ncu-case", choices=NCU_CASES, default=None,
+                    help="run one kernel kind three times on a small case (for ncu) and exit")
     args = ap.parse_args(argv)
+    if args.ncu_case:
+        run_ncu_case(args.ncu_case)
+        return
     if args.impl == "ours":
         args.warmup = max(args.warmup, 3)     # timing rule: at least 3 warm-up steps
     world, rank, local = dist_env()
