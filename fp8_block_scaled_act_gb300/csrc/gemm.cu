@@ -53,21 +53,26 @@ constexpr int kThreads = (kFirstEpiWarp + kEpiWarps) * 32;  // 384: three warpgr
 // the two epilogue warpgroups take them. The host checks the launch count
 // before the first launch so that the split never asks for more than exists.
 constexpr uint32_t kLaunchRegs = 168;
-constexpr uint32_t kProducerRegs = 64;
-constexpr uint32_t kEpilogueRegs = 216;
+constexpr uint32_t kProducerRegs = 40;
+constexpr uint32_t kEpilogueRegs = 232;
 static_assert(128 * kProducerRegs + 256 * kEpilogueRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr int kTmemCols = 2 * kBN;              // two accumulator buffers
 // Waits that drain in-flight copies and MMAs before exit use at least this
 // limit, so that a small user limit never lets a CTA exit with work in flight.
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /* alignment */ + 256 /* barriers */;
+constexpr int kCtlBytes = 256;                  // barriers and flags
+constexpr int kVecSlots = 3;                    // Wgrad scale ring depth
+constexpr int kSlotFloats = 32 + 128;           // A scales of the warp's 32 rows + 128 column scales
+constexpr int kVecBytes = kEpiWarps * kVecSlots * kSlotFloats * 4;
+constexpr int kSmemBytes = kStages * kStageBytes + kCtlBytes + kVecBytes + 1024 /* alignment */;
 
 struct SharedCtl {
     uint64_t full[kStages];
     uint64_t empty[kStages];
     uint64_t tfull[2];
     uint64_t tempty[2];
+    uint64_t mma_done;        // final commit of the MMA thread (drain before exit)
     uint32_t tmem_base;
     volatile int abort;
 };
@@ -115,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&ctl->tfull[a], 1);
             mbar_init(&ctl->tempty[a], kEpiWarps);
         }
+        mbar_init(&ctl->mma_done, 1);
         ctl->abort = 0;
         fence_mbarrier_init();
         tma_prefetch_desc(&map_a);
@@ -206,12 +212,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 record_status(p.status, FP8BS_ERR_TIMEOUT);
                 ctl->abort = 1;
             }
-            // drain: the last committed MMA group has completed
-            if (it > 0) {
-                const uint32_t j = it - 1;
-                const uint64_t drain = limit > kDrainLimitNs ? limit : kDrainLimitNs;
-                mbar_wait(&ctl->empty[j % kStages], (j / kStages) & 1u, drain);
-            }
+            // drain: every MMA this thread issued has completed
+            mma_commit(&ctl->mma_done);
+            const uint64_t drain = limit > kDrainLimitNs ? limit : kDrainLimitNs;
+            mbar_wait(&ctl->mma_done, 0u, drain);
         }
     } else if (warp >= kFirstEpiWarp) {
         // ------------------------------------------------------------------
@@ -223,6 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int half = ew >> 2;       // 128-column half of the tile
         const int r_in_tile = quarter * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+        // Wgrad's per-column B scales: a 3-slot ring per warp, filled two
+        // K-blocks ahead (lane l holds columns 4l .. 4l + 3 of a slot)
+        float* vring = reinterpret_cast<float*>(smem + kStages * kStageBytes + kCtlBytes) +
+                       ew * (kVecSlots * kSlotFloats);
         uint32_t acc_it = 0;
         bool ok = true;
 
@@ -239,17 +247,69 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float* sb_ptr = p.sb + p.sb_off[g] +
                                   (kKind == GemmKind::kBlockScaleBf16
                                        ? static_cast<int64_t>(col0 / 128) * p.sb_cstride
-                                       : static_cast<int64_t>(col0));
+                                       : static_cast<int64_t>(col0 + 4 * lane));
 
-            float acc[128];
+            auto load_sa = [&](int kb) -> float {
+                return (sa_ok && kb < nkb) ? __ldg(sa_ptr + static_cast<int64_t>(kb) * p.sa_ld) : 0.0f;
+            };
+            auto load_sb = [&](int kb) -> float {
+                return (cols_ok && kb < nkb) ? __ldg(sb_ptr + static_cast<int64_t>(kb) * p.sb_kstride) : 0.0f;
+            };
+            auto load_vec = [&](int kb) -> float4 {
+                return (cols_ok && kb < nkb)
+                           ? __ldg(reinterpret_cast<const float4*>(sb_ptr + static_cast<int64_t>(kb) * p.sb_kstride))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            };
+
+            uint64_t acc[64];   // 128 fp32 accumulators as 64 packed pairs
 #pragma unroll
-            for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+            for (int j = 0; j < 64; ++j) acc[j] = 0ull;
+
+            // Fprop/Dgrad: scalar scales two K-blocks ahead in registers.
+            // Wgrad: per-warp smem ring filled by cp.async two K-blocks ahead.
+            float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
+            auto prefetch = [&](int kb) {
+                if (kb < nkb) {
+                    float* slot = vring + (kb % kVecSlots) * kSlotFloats;
+                    cp_async_4(slot + lane, sa_ok ? sa_ptr + static_cast<int64_t>(kb) * p.sa_ld : p.sa,
+                               sa_ok ? 4u : 0u);
+                    cp_async_16(slot + 32 + 4 * lane,
+                                cols_ok ? sb_ptr + static_cast<int64_t>(kb) * p.sb_kstride : p.sb,
+                                cols_ok ? 16u : 0u);
+                }
+                cp_async_commit();
+            };
+            if constexpr (kKind == GemmKind::kBlockScaleBf16) {
+                sa0 = load_sa(0);
+                sa1 = load_sa(1);
+                sb0 = load_sb(0);
+                sb1 = load_sb(1);
+            } else {
+                prefetch(0);
+                prefetch(1);
+            }
 
             for (int kb = 0; kb < nkb; ++kb, ++acc_it) {
-                const float s_a = sa_ok ? __ldg(sa_ptr + static_cast<int64_t>(kb) * p.sa_ld) : 0.0f;
-                float s_blk = 0.0f;
-                if constexpr (kKind == GemmKind::kBlockScaleBf16)
-                    s_blk = cols_ok ? s_a * __ldg(sb_ptr + static_cast<int64_t>(kb) * p.sb_kstride) : 0.0f;
+                float s_a = 0.f, s_blk = 0.f;
+                const float4* vslot = nullptr;
+                if constexpr (kKind == GemmKind::kBlockScaleBf16) {
+                    s_a = sa0;
+                    s_blk = sa0 * sb0;
+                    sa0 = sa1;
+                    sa1 = load_sa(kb + 2);
+                    sb0 = sb1;
+                    sb1 = load_sb(kb + 2);
+                } else {
+                    prefetch(kb + 2);
+                    cp_async_wait<2>();   // K-block kb's scales have landed
+                    __syncwarp();
+                    const float* slot = vring + (kb % kVecSlots) * kSlotFloats;
+                    s_a = slot[lane];
+                    vslot = reinterpret_cast<const float4*>(slot + 32);
+                }
+                const uint64_t s_blk2 = f2_pack(s_blk, s_blk);
+                const uint64_t s_a2 = f2_pack(s_a, s_a);
+
                 const uint32_t buf = acc_it & 1u;
                 const uint32_t aph = (acc_it >> 1) & 1u;
                 if (ctl->abort || !mbar_wait(&ctl->tfull[buf], aph, limit)) {
@@ -258,35 +318,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t taddr = tmem_base + lane_addr + buf * kBN + half * 128;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r[32];
-                    tmem_ld_x32(taddr + c * 32, r);
-                    tmem_ld_wait(r);
-                    if (c == 3) {
-                        tc_fence_before_sync();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
-                    }
+
+                // promote one 32-column chunk of the partial held in r
+                auto promote = [&](int c, uint32_t (&r)[32]) {
                     if constexpr (kKind == GemmKind::kBlockScaleBf16) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            acc[c * 32 + j] = fmaf(__uint_as_float(r[j]), s_blk, acc[c * 32 + j]);
+                        for (int i = 0; i < 16; ++i)
+                            acc[c * 16 + i] =
+                                f2_fma(f2_pack_bits(r[2 * i], r[2 * i + 1]), s_blk2, acc[c * 16 + i]);
                     } else {
-                        const float4* sbv = reinterpret_cast<const float4*>(
-                            sb_ptr + static_cast<int64_t>(kb) * p.sb_kstride + c * 32);
 #pragma unroll
-                        for (int q4 = 0; q4 < 8; ++q4) {
-                            const float4 v = cols_ok ? __ldg(sbv + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
-                            const int j = c * 32 + q4 * 4;
-                            acc[j + 0] = fmaf(__uint_as_float(r[q4 * 4 + 0]), s_a * v.x, acc[j + 0]);
-                            acc[j + 1] = fmaf(__uint_as_float(r[q4 * 4 + 1]), s_a * v.y, acc[j + 1]);
-                            acc[j + 2] = fmaf(__uint_as_float(r[q4 * 4 + 2]), s_a * v.z, acc[j + 2]);
-                            acc[j + 3] = fmaf(__uint_as_float(r[q4 * 4 + 3]), s_a * v.w, acc[j + 3]);
+                        for (int i = 0; i < 8; ++i) {
+                            const float4 sbv = vslot[c * 8 + i];
+                            const uint64_t sc0 = f2_mul(s_a2, f2_pack(sbv.x, sbv.y));
+                            const uint64_t sc1 = f2_mul(s_a2, f2_pack(sbv.z, sbv.w));
+                            acc[c * 16 + 2 * i] =
+                                f2_fma(f2_pack_bits(r[4 * i], r[4 * i + 1]), sc0, acc[c * 16 + 2 * i]);
+                            acc[c * 16 + 2 * i + 1] =
+                                f2_fma(f2_pack_bits(r[4 * i + 2], r[4 * i + 3]), sc1, acc[c * 16 + 2 * i + 1]);
                         }
                     }
-                }
+                };
+                // TMEM loads double-buffered: chunk c + 1 is in flight while
+                // chunk c is promoted
+                uint32_t ra[32], rb[32];
+                tmem_ld_x32(taddr + 0, ra);
+                tmem_ld_wait(ra);
+                tmem_ld_x32(taddr + 32, rb);
+                promote(0, ra);
+                tmem_ld_wait(rb);
+                tmem_ld_x32(taddr + 64, ra);
+                promote(1, rb);
+                tmem_ld_wait(ra);
+                tmem_ld_x32(taddr + 96, rb);
+                promote(2, ra);
+                tmem_ld_wait(rb);
+                // the partial is in registers: hand the TMEM buffer back
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
+                promote(3, rb);
             }
+            if constexpr (kKind == GemmKind::kVectorScaleF32) cp_async_wait<0>();
             if (!ok) break;
 
             if (row_ok && cols_ok) {
@@ -295,11 +368,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   static_cast<int64_t>(row) * p.out_ld + col0;
 #pragma unroll
                     for (int v = 0; v < 16; ++v) {
+                        const float2 a0 = f2_unpack(acc[4 * v + 0]);
+                        const float2 a1 = f2_unpack(acc[4 * v + 1]);
+                        const float2 a2 = f2_unpack(acc[4 * v + 2]);
+                        const float2 a3 = f2_unpack(acc[4 * v + 3]);
                         uint4 pk;
-                        pk.x = pack_bf16x2(acc[8 * v + 0], acc[8 * v + 1]);
-                        pk.y = pack_bf16x2(acc[8 * v + 2], acc[8 * v + 3]);
-                        pk.z = pack_bf16x2(acc[8 * v + 4], acc[8 * v + 5]);
-                        pk.w = pack_bf16x2(acc[8 * v + 6], acc[8 * v + 7]);
+                        pk.x = pack_bf16x2(a0.x, a0.y);
+                        pk.y = pack_bf16x2(a1.x, a1.y);
+                        pk.z = pack_bf16x2(a2.x, a2.y);
+                        pk.w = pack_bf16x2(a3.x, a3.y);
                         reinterpret_cast<uint4*>(y)[v] = pk;
                     }
                 } else {
@@ -308,7 +385,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float4* y4 = reinterpret_cast<float4*>(y);
 #pragma unroll
                     for (int v = 0; v < 32; ++v) {
-                        float4 o = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+                        const float2 a0 = f2_unpack(acc[2 * v + 0]);
+                        const float2 a1 = f2_unpack(acc[2 * v + 1]);
+                        float4 o = make_float4(a0.x, a0.y, a1.x, a1.y);
                         if (p.accumulate) {
                             const float4 prev = y4[v];
                             o.x += prev.x; o.y += prev.y; o.z += prev.z; o.w += prev.w;
@@ -347,7 +426,7 @@ template <GemmKind kKind>
 cudaError_t launch_kind(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmParams& p,
                         int num_sms, cudaStream_t stream)
 {
-    static_assert(sizeof(SharedCtl) <= 256, "control block");
+    static_assert(sizeof(SharedCtl) <= kCtlBytes, "control block");
     auto kernel = block_scaled_gemm_kernel<kKind>;
     cudaFuncAttributes attr;
     cudaError_t e = cudaFuncGetAttributes(&attr, kernel);

@@ -38,20 +38,105 @@ __device__ __forceinline__ float scale_from_amax(float amax)
     return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
 }
 
-// Sign bits of the four bf16 values held in (w0, w1), moved to bit 7 of the
-// corresponding code bytes.
-__device__ __forceinline__ uint32_t sign_bits_4(uint32_t w0, uint32_t w1)
+// E4M3 codes of fp32(v / s) for a pair of values, by exact IEEE division.
+// Out of line: the fast path below falls back to it only for quotients that
+// sit within a few fp32 ulps of an E4M3 rounding boundary (rare), and
+// keeping it out of line stops the compiler from predicating it into every
+// element.
+__device__ __noinline__ uint32_t encode2_exact(float v0, float v1, float s)
 {
-    return ((w0 >> 8) & 0x80u) | ((w0 >> 16) & 0x8000u) | ((w1 << 8) & 0x800000u) |
-           (w1 & 0x80000000u);
+    return cvt_e4m3x2(__fdiv_rn(v0, s), __fdiv_rn(v1, s));
 }
 
-// Four bf16 values (two words) divided by s and encoded, low element first.
-__device__ __forceinline__ uint32_t quant4(uint32_t w0, uint32_t w1, float s)
+// One value's quotient fp32(v / s) without a division, and whether it is
+// certain to be the correctly rounded one.
+//
+// q = RN(v * r) with r = RN(1/s) is within ~1.5 ulp of v/s. One correction
+// step (Markstein's method, IBM J. Res. Dev. 34(1), 1990) with the exact
+// FMA residual e = v - q s gives q1 = RN(q + e r), whose error is a few
+// 2^-24 ulp: q1 = RN(v/s) except when v/s lies within that distance of a
+// rounding boundary between two fp32 values. The check makes this exact:
+// with e1 = v - q1 s computed exactly by an FMA, |e1| < ulp(q1) s / 2 means
+// |v/s - q1| < ulp(q1) / 2, so q1 = RN(v/s). (For s not a power of two, v/s
+// is never exactly halfway between two floats; for a power of two, e1 = 0.
+// When q1 is a power of two the ulp below it is half as large, but a value
+// that close to a power of two has the same E4M3 code, which is all the
+// caller uses.) Below 2^-102 the ulp bound is clamped to 2^-126: such
+// quotients encode to a signed zero whatever their rounding. The caller
+// keeps s in [2^-60, 2^100] so that every quantity here stays normal.
+__device__ __forceinline__ float quotient_checked(float v, float s, float r, uint32_t& bad)
 {
-    uint32_t c01 = cvt_e4m3x2(__fdiv_rn(bf16_lo(w0), s), __fdiv_rn(bf16_hi(w0), s));
-    uint32_t c23 = cvt_e4m3x2(__fdiv_rn(bf16_lo(w1), s), __fdiv_rn(bf16_hi(w1), s));
-    return (c01 | (c23 << 16)) | sign_bits_4(w0, w1);
+    const float q0 = __fmul_rn(v, r);
+    const float q1 = __fmaf_rn(__fmaf_rn(-q0, s, v), r, q0);
+    const float e1 = __fmaf_rn(-q1, s, v);
+    const int half_ulp_bits = __viaddmax_s32(static_cast<int>(__float_as_uint(q1) & 0x7F800000u),
+                                             -(24 << 23), 0x00800000);
+    const float bound = __fmul_rn(s, __int_as_float(half_ulp_bits));
+    bad |= (fabsf(e1) < bound) ? 0u : 1u;
+    return q1;
+}
+
+// E4M3 codes of fp32(v0 / s), fp32(v1 / s) (low byte = v0); `bad` becomes
+// non-zero when a quotient could not be certified and the caller must redo
+// the group with exact division (rare: only near fp32 rounding boundaries).
+__device__ __forceinline__ uint32_t encode2_fast(float v0, float v1, float s, float r, uint32_t& bad)
+{
+    const float q0 = quotient_checked(v0, s, r, bad);
+    const float q1 = quotient_checked(v1, s, r, bad);
+    return cvt_e4m3x2(q0, q1);
+}
+
+// Scale of a tile: s and its reciprocal for the fast path (r = 0 when s is
+// outside [2^-100, 2^100] and only the exact path may be used).
+struct TileScale {
+    float s;
+    float r;
+};
+
+__device__ __forceinline__ TileScale tile_scale_from_s(float s)
+{
+    TileScale t;
+    t.s = s;
+    t.r = (s >= 0x1p-60f && s <= 0x1p100f) ? __frcp_rn(s) : 0.0f;
+    return t;
+}
+
+__device__ __forceinline__ TileScale tile_scale(float amax)
+{
+    return tile_scale_from_s(scale_from_amax(amax));
+}
+
+// Sign bits of the four bf16 values in (w0, w1) at bit 7 of the matching
+// code bytes: the high byte of each bf16 carries its sign.
+__device__ __forceinline__ uint32_t sign_bits_4(uint32_t w0, uint32_t w1)
+{
+    return __byte_perm(w0, w1, 0x7531) & 0x80808080u;
+}
+
+__device__ __noinline__ uint2 quant8_exact(uint4 d, float s)
+{
+    uint2 o;
+    o.x = encode2_exact(bf16_lo(d.x), bf16_hi(d.x), s) | (encode2_exact(bf16_lo(d.y), bf16_hi(d.y), s) << 16);
+    o.y = encode2_exact(bf16_lo(d.z), bf16_hi(d.z), s) | (encode2_exact(bf16_lo(d.w), bf16_hi(d.w), s) << 16);
+    return o;
+}
+
+// Eight bf16 values (one 16-byte load) divided by s and encoded, low
+// element first; the input's sign bit is copied into every code so that -0
+// (0x80) survives for tiny negatives. One branch per eight values: the rare
+// group with a quotient near a rounding boundary is redone exactly.
+__device__ __forceinline__ uint2 quant8(const uint4& d, const TileScale& t)
+{
+    uint32_t bad = t.r == 0.0f ? 1u : 0u;
+    const uint32_t c0 = encode2_fast(bf16_lo(d.x), bf16_hi(d.x), t.s, t.r, bad);
+    const uint32_t c1 = encode2_fast(bf16_lo(d.y), bf16_hi(d.y), t.s, t.r, bad);
+    const uint32_t c2 = encode2_fast(bf16_lo(d.z), bf16_hi(d.z), t.s, t.r, bad);
+    const uint32_t c3 = encode2_fast(bf16_lo(d.w), bf16_hi(d.w), t.s, t.r, bad);
+    uint2 o = make_uint2(__byte_perm(c0, c1, 0x5410), __byte_perm(c2, c3, 0x5410));
+    if (bad != 0u) o = quant8_exact(d, t.s);
+    o.x |= sign_bits_4(d.x, d.y);
+    o.y |= sign_bits_4(d.z, d.w);
+    return o;
 }
 
 // ---------------------------------------------------------------------------
@@ -93,29 +178,39 @@ __global__ void __launch_bounds__(kQ1Threads) quant_1x128_kernel(
                 d[i] = make_uint4(0u, 0u, 0u, 0u);
         }
 
-        float my_scale = 1.0f;
+        // Per-row absmax by a reduce-scatter butterfly inside each half-warp:
+        // at each level a lane swaps half of its running maxima with the lane
+        // `off` away and keeps the half selected by its own lane bit, so after
+        // four levels lane (h, j) holds the absmax of row 2j + h (15 shuffles
+        // instead of a separate 4-shuffle reduction per row pair).
+        const int lh = lane & 15;
+        uint32_t m[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            uint32_t m = absmax_bits_8(d[i]);
-            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
-            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-            const float s = scale_from_amax(__uint_as_float(m << 16));
-            // row 2i + h's scale goes to lane 2i + h
-            const float t = __shfl_sync(0xFFFFFFFFu, s, (lane & 1) * 16);
-            if (i == (lane >> 1)) my_scale = t;
-
-            const int64_t r = row0 + 2 * i + half;
-            if (col_ok && r < rows) {
-                uint2 out;
-                out.x = quant4(d[i].x, d[i].y, s);
-                out.y = quant4(d[i].z, d[i].w, s);
-                *reinterpret_cast<uint2*>(q + r * cols + col) = out;
+        for (int i = 0; i < 16; ++i) m[i] = absmax_bits_8(d[i]);
+#pragma unroll
+        for (int off = 8; off >= 1; off >>= 1) {
+            const bool upper = (lh & off) != 0;
+#pragma unroll
+            for (int j = 0; j < off; ++j) {
+                const uint32_t send = upper ? m[j] : m[j + off];
+                const uint32_t keep = upper ? m[j + off] : m[j];
+                m[j] = max(keep, __shfl_xor_sync(0xFFFFFFFFu, send, off));
             }
         }
-        const int64_t r = row0 + lane;
-        if (r < rows) scales[tc * scale_ld + r] = my_scale;
+        const float amax_mine = __uint_as_float(m[0] << 16);
+        const int my_row = 2 * lh + half;
+        // one scale (and reciprocal) per lane: lane (h, j) owns row 2j + h
+        const TileScale mine = tile_scale(amax_mine);
+        if (row0 + my_row < rows) scales[tc * scale_ld + row0 + my_row] = mine.s;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int src = (lane & 16) | i;    // the lane holding row 2i + h
+            TileScale ts;
+            ts.s = __shfl_sync(0xFFFFFFFFu, mine.s, src);
+            ts.r = __shfl_sync(0xFFFFFFFFu, mine.r, src);
+            const int64_t r = row0 + 2 * i + half;
+            if (col_ok && r < rows) *reinterpret_cast<uint2*>(q + r * cols + col) = quant8(d[i], ts);
+        }
     }
 }
 
@@ -167,17 +262,15 @@ __global__ void __launch_bounds__(kQ2Threads) quant_128x128_kernel(
     m = 0;
 #pragma unroll
     for (int i = 0; i < kQ2Threads / 32; ++i) m = max(m, red[i]);
-    const float s = scale_from_amax(__uint_as_float(m << 16));
-    if (threadIdx.x == 0) scales[b * nbr * nbc + bi * nbc + bj] = s;
+    const TileScale ts = tile_scale(__uint_as_float(m << 16));
+    if (threadIdx.x == 0) scales[b * nbr * nbc + bi * nbc + bj] = ts.s;
 
     uint8_t* qb = q + b * rows * cols;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int rl = rgrp + 16 * i;
         const int64_t r = r0 + rl;
-        uint2 out;
-        out.x = quant4(d[i].x, d[i].y, s);
-        out.y = quant4(d[i].z, d[i].w, s);
+        const uint2 out = quant8(d[i], ts);
         if (col_ok && r < rows) *reinterpret_cast<uint2*>(qb + r * cols + col) = out;
         if (qT != nullptr) {
             uint32_t* tp = reinterpret_cast<uint32_t*>(tile + rl * kQ2Pitch + chunk * 8);
@@ -220,6 +313,122 @@ __global__ void __launch_bounds__(kQ2Threads) quant_128x128_kernel(
 // 128 tokens down the staged block and writes them as one 128-byte row of qT.
 // ---------------------------------------------------------------------------
 constexpr int kQ3Threads = 256;
+
+// Sign bytes of the four 32-bit words x0..x3, byte b of each: returns
+// [x0.b, x1.b, x2.b, x3.b] with only bit 7 of each byte kept.
+__device__ __forceinline__ uint32_t column_signs(uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3,
+                                                 int b)
+{
+    const uint32_t lo = __byte_perm(x0, x1, (4 + b) << 4 | b);        // [x0.b, x1.b, ...]
+    const uint32_t hi = __byte_perm(x2, x3, (4 + b) << 4 | b);        // [x2.b, x3.b, ...]
+    return __byte_perm(lo, hi, 0x5410) & 0x80808080u;
+}
+
+// Mode B, phase 3 for one channel pair (j, j + 1) and 32 tokens of the staged
+// BF16 block [128 tokens x 128 channels]: each 32-bit shared load holds both
+// channels of one token. Returns false if any quotient needs the exact path.
+__device__ __forceinline__ bool requant_pair_bf16(const uint8_t* stage, int part, int j,
+                                                  const TileScale& t0, const TileScale& t1,
+                                                  uint32_t (&w0)[8], uint32_t (&w1)[8])
+{
+    uint32_t bad = (t0.r == 0.0f || t1.r == 0.0f) ? 1u : 0u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        uint32_t x[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            x[e] = *reinterpret_cast<const uint32_t*>(stage + ((part * 32 + 4 * k + e) * 128 + j) * 2);
+        const uint32_t a01 = encode2_fast(bf16_lo(x[0]), bf16_lo(x[1]), t0.s, t0.r, bad);
+        const uint32_t a23 = encode2_fast(bf16_lo(x[2]), bf16_lo(x[3]), t0.s, t0.r, bad);
+        const uint32_t b01 = encode2_fast(bf16_hi(x[0]), bf16_hi(x[1]), t1.s, t1.r, bad);
+        const uint32_t b23 = encode2_fast(bf16_hi(x[2]), bf16_hi(x[3]), t1.s, t1.r, bad);
+        w0[k] = __byte_perm(a01, a23, 0x5410) | column_signs(x[0], x[1], x[2], x[3], 1);
+        w1[k] = __byte_perm(b01, b23, 0x5410) | column_signs(x[0], x[1], x[2], x[3], 3);
+    }
+    return bad == 0u;
+}
+
+// Exact-division version of requant_pair_bf16 that stores its results
+// itself (kept out of line; it runs only when the fast path reports a
+// quotient near an E4M3 rounding boundary).
+__device__ __noinline__ void requant_pair_bf16_exact(const uint8_t* stage, int part, int j, float s0,
+                                                     float s1, uint8_t* dst0, uint8_t* dst1)
+{
+    for (int k = 0; k < 8; ++k) {
+        uint32_t x[4];
+        for (int e = 0; e < 4; ++e)
+            x[e] = *reinterpret_cast<const uint32_t*>(stage + ((part * 32 + 4 * k + e) * 128 + j) * 2);
+        reinterpret_cast<uint32_t*>(dst0)[k] =
+            (encode2_exact(bf16_lo(x[0]), bf16_lo(x[1]), s0) |
+             (encode2_exact(bf16_lo(x[2]), bf16_lo(x[3]), s0) << 16)) |
+            column_signs(x[0], x[1], x[2], x[3], 1);
+        reinterpret_cast<uint32_t*>(dst1)[k] =
+            (encode2_exact(bf16_hi(x[0]), bf16_hi(x[1]), s1) |
+             (encode2_exact(bf16_hi(x[2]), bf16_hi(x[3]), s1) << 16)) |
+            column_signs(x[0], x[1], x[2], x[3], 3);
+    }
+}
+
+// Decoded values of the four E4M3 codes in x (channel c = byte c), each
+// multiplied by the token's 1x128 scale in fp32.
+__device__ __forceinline__ void decode4_scaled(uint32_t x, float s1, float (&v)[4])
+{
+    const float2 a = e4m3x2_to_f32(static_cast<uint16_t>(x & 0xFFFFu));
+    const float2 b = e4m3x2_to_f32(static_cast<uint16_t>(x >> 16));
+    v[0] = __fmul_rn(a.x, s1);
+    v[1] = __fmul_rn(a.y, s1);
+    v[2] = __fmul_rn(b.x, s1);
+    v[3] = __fmul_rn(b.y, s1);
+}
+
+// Mode Q, phase 3 for one channel quad (j .. j + 3) and 16 tokens of the
+// staged E4M3 block: each 32-bit shared load holds the quad of one token.
+__device__ __forceinline__ bool requant_quad_e4m3(const uint8_t* stage, const float* row_scale,
+                                                  int part, int j, const TileScale (&ts)[4],
+                                                  uint32_t (&w)[4][4])
+{
+    uint32_t bad = (ts[0].r == 0.0f || ts[1].r == 0.0f || ts[2].r == 0.0f || ts[3].r == 0.0f) ? 1u : 0u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        uint32_t x[4];
+        float v[4][4];   // [token][channel]
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int rl = part * 16 + 4 * k + e;
+            x[e] = *reinterpret_cast<const uint32_t*>(stage + rl * 128 + j);
+            decode4_scaled(x[e], row_scale[rl], v[e]);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t c01 = encode2_fast(v[0][c], v[1][c], ts[c].s, ts[c].r, bad);
+            const uint32_t c23 = encode2_fast(v[2][c], v[3][c], ts[c].s, ts[c].r, bad);
+            w[c][k] = __byte_perm(c01, c23, 0x5410) | column_signs(x[0], x[1], x[2], x[3], c);
+        }
+    }
+    return bad == 0u;
+}
+
+// Exact-division version of requant_quad_e4m3 that stores its results
+// itself (channel c goes to dst + c * mpad).
+__device__ __noinline__ void requant_quad_e4m3_exact(const uint8_t* stage, const float* row_scale,
+                                                     int part, int j, float s0, float s1, float s2,
+                                                     float s3, uint8_t* dst, int64_t mpad)
+{
+    const float sc[4] = {s0, s1, s2, s3};
+    for (int k = 0; k < 4; ++k) {
+        uint32_t x[4];
+        float v[4][4];
+        for (int e = 0; e < 4; ++e) {
+            const int rl = part * 16 + 4 * k + e;
+            x[e] = *reinterpret_cast<const uint32_t*>(stage + rl * 128 + j);
+            decode4_scaled(x[e], row_scale[rl], v[e]);
+        }
+        for (int c = 0; c < 4; ++c)
+            reinterpret_cast<uint32_t*>(dst + c * mpad)[k] =
+                (encode2_exact(v[0][c], v[1][c], sc[c]) | (encode2_exact(v[2][c], v[3][c], sc[c]) << 16)) |
+                column_signs(x[0], x[1], x[2], x[3], c);
+    }
+}
 
 __device__ __forceinline__ int find_group(const int32_t* tile_start, int ng, int tile)
 {
@@ -330,43 +539,44 @@ __global__ void __launch_bounds__(kQ3Threads) requant_128x1_T_kernel(const __gri
     }
     __syncthreads();
 
-    // unit = (channel j, 32-token part): 512 units, two per thread
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        const int unit = threadIdx.x + u * kQ3Threads;
-        const int j = unit & 127;
-        const int part = unit >> 7;  // 0..3
-        if (j >= nch) continue;
-        const float s = col_scale[j];
-        uint32_t outw[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            float v[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int rl = part * 32 + 4 * k + e;
-                if (p.mode == FP8BS_SRC_BF16) {
-                    const uint16_t h = *reinterpret_cast<const uint16_t*>(stage + (rl * 128 + j) * 2);
-                    v[e] = __uint_as_float(static_cast<uint32_t>(h) << 16);
-                } else {
-                    const uint8_t c = stage[rl * 128 + j];
-                    const float2 dv = e4m3x2_to_f32(static_cast<uint16_t>(c));
-                    v[e] = __fmul_rn(dv.x, row_scale[rl]);
-                }
+    if (p.mode == FP8BS_SRC_BF16) {
+        // unit = (channel pair 2jp, 2jp + 1; 32-token part): 64 x 4 = 256 units
+        const int j = 2 * (threadIdx.x & 63);
+        const int part = threadIdx.x >> 6;
+        if (j < nch) {   // nch % 16 == 0: pairs are all-in or all-out
+            const TileScale t0 = tile_scale_from_s(col_scale[j]);
+            const TileScale t1 = tile_scale_from_s(col_scale[j + 1]);
+            uint8_t* dst0 = p.qT + (c0 + j) * p.mpad + (int64_t)tile * 128 + part * 32;
+            uint8_t* dst1 = dst0 + p.mpad;
+            uint32_t w0[8], w1[8];
+            if (requant_pair_bf16(stage, part, j, t0, t1, w0, w1)) {
+                reinterpret_cast<uint4*>(dst0)[0] = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+                reinterpret_cast<uint4*>(dst0)[1] = make_uint4(w0[4], w0[5], w0[6], w0[7]);
+                reinterpret_cast<uint4*>(dst1)[0] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+                reinterpret_cast<uint4*>(dst1)[1] = make_uint4(w1[4], w1[5], w1[6], w1[7]);
+            } else {
+                requant_pair_bf16_exact(stage, part, j, t0.s, t1.s, dst0, dst1);
             }
-            uint32_t w = cvt_e4m3x2(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s)) |
-                         (cvt_e4m3x2(__fdiv_rn(v[2], s), __fdiv_rn(v[3], s)) << 16);
-            w |= ((__float_as_uint(v[0]) >> 24) & 0x80u) | ((__float_as_uint(v[1]) >> 16) & 0x8000u) |
-                 ((__float_as_uint(v[2]) >> 8) & 0x800000u) | (__float_as_uint(v[3]) & 0x80000000u);
-            // tokens past the group's end are padding: 0x00
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (part * 32 + 4 * k + e >= len) w &= ~(0xFFu << (8 * e));
-            outw[k] = w;
         }
-        uint8_t* dst = p.qT + (c0 + j) * p.mpad + (int64_t)tile * 128 + part * 32;
-        reinterpret_cast<uint4*>(dst)[0] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
-        reinterpret_cast<uint4*>(dst)[1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
+    } else {
+        // unit = (channel quad 4jq .. 4jq + 3; 16-token part): 32 x 8 = 256 units
+        const int j = 4 * (threadIdx.x & 31);
+        const int part = threadIdx.x >> 5;
+        if (j < nch) {
+            TileScale ts[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) ts[c] = tile_scale_from_s(col_scale[j + c]);
+            uint8_t* dst = p.qT + (c0 + j) * p.mpad + (int64_t)tile * 128 + part * 16;
+            uint32_t w[4][4];
+            if (requant_quad_e4m3(stage, row_scale, part, j, ts, w)) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4*>(dst + c * p.mpad) = make_uint4(w[c][0], w[c][1], w[c][2], w[c][3]);
+            } else {
+                requant_quad_e4m3_exact(stage, row_scale, part, j, ts[0].s, ts[1].s, ts[2].s, ts[3].s,
+                                        dst, p.mpad);
+            }
+        }
     }
 }
 

@@ -25,8 +25,10 @@ def _lib():
 
 def _special_inputs(R, C, seed):
     """N(0,1) with 1% outliers, an all-zero tile, a tile of tiny negatives
-    (-0 results), a tile whose absmax is negative, and a tile with amax 448
-    (scale 1) holding exact E4M3 midpoints (ties to even)."""
+    (-0 results), a tile whose absmax is negative, a tile with amax 448
+    (scale 1) holding exact E4M3 midpoints (ties to even), and a tile of
+    values around 1e-20 (a scale below 2^-60, where the kernels divide
+    exactly instead of using the reciprocal path)."""
     x = wl.with_outliers((R, C), fraction=0.01, seed=seed)
     w = min(C, 128)
     if R > 0:
@@ -48,6 +50,8 @@ def _special_inputs(R, C, seed):
         row[0] = 448.0
         row[1:1 + vals.numel()] = vals * torch.where(torch.arange(vals.numel()) % 2 == 0, 1.0, -1.0).to(torch.bfloat16)
         x[3, :w] = row
+    if R > 4:
+        x[4, :w] = (wl.normal((w,), seed=seed + 99).float() * 1e-20).to(torch.bfloat16)
     return x
 
 
