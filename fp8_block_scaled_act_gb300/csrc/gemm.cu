@@ -77,6 +77,22 @@ struct SharedCtl {
     volatile int abort;
 };
 
+// 32-byte global store / load (one full sector per thread).
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8])
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void ld_global_v8(const void* p, uint32_t (&w)[8])
+{
+    asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "l"(p)
+                 : "memory");
+}
+
 __device__ __forceinline__ void record_status(unsigned int* status, unsigned int code)
 {
     atomicCAS(status, 0u, code);
@@ -261,9 +277,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                            : make_float4(0.f, 0.f, 0.f, 0.f);
             };
 
-            uint64_t acc[64];   // 128 fp32 accumulators as 64 packed pairs
+            float2 acc[64];     // 128 fp32 accumulators as 64 pairs (packed f32x2 math)
 #pragma unroll
-            for (int j = 0; j < 64; ++j) acc[j] = 0ull;
+            for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.f, 0.f);
 
             // Fprop/Dgrad: scalar scales two K-blocks ahead in registers.
             // Wgrad: per-warp smem ring filled by cp.async two K-blocks ahead.
@@ -307,8 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     s_a = slot[lane];
                     vslot = reinterpret_cast<const float4*>(slot + 32);
                 }
-                const uint64_t s_blk2 = f2_pack(s_blk, s_blk);
-                const uint64_t s_a2 = f2_pack(s_a, s_a);
+                const float2 s_blk2 = make_float2(s_blk, s_blk);
+                const float2 s_a2 = make_float2(s_a, s_a);
 
                 const uint32_t buf = acc_it & 1u;
                 const uint32_t aph = (acc_it >> 1) & 1u;
@@ -324,18 +340,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (kKind == GemmKind::kBlockScaleBf16) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            acc[c * 16 + i] =
-                                f2_fma(f2_pack_bits(r[2 * i], r[2 * i + 1]), s_blk2, acc[c * 16 + i]);
+                            acc[c * 16 + i] = __ffma2_rn(
+                                make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), s_blk2,
+                                acc[c * 16 + i]);
                     } else {
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const float4 sbv = vslot[c * 8 + i];
-                            const uint64_t sc0 = f2_mul(s_a2, f2_pack(sbv.x, sbv.y));
-                            const uint64_t sc1 = f2_mul(s_a2, f2_pack(sbv.z, sbv.w));
-                            acc[c * 16 + 2 * i] =
-                                f2_fma(f2_pack_bits(r[4 * i], r[4 * i + 1]), sc0, acc[c * 16 + 2 * i]);
-                            acc[c * 16 + 2 * i + 1] =
-                                f2_fma(f2_pack_bits(r[4 * i + 2], r[4 * i + 3]), sc1, acc[c * 16 + 2 * i + 1]);
+                            const float2 sc0 = __fmul2_rn(s_a2, make_float2(sbv.x, sbv.y));
+                            const float2 sc1 = __fmul2_rn(s_a2, make_float2(sbv.z, sbv.w));
+                            acc[c * 16 + 2 * i] = __ffma2_rn(
+                                make_float2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])), sc0,
+                                acc[c * 16 + 2 * i]);
+                            acc[c * 16 + 2 * i + 1] = __ffma2_rn(
+                                make_float2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])), sc1,
+                                acc[c * 16 + 2 * i + 1]);
                         }
                     }
                 };
@@ -368,10 +387,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   static_cast<int64_t>(row) * p.out_ld + col0;
 #pragma unroll
                     for (int v = 0; v < 16; ++v) {
-                        const float2 a0 = f2_unpack(acc[4 * v + 0]);
-                        const float2 a1 = f2_unpack(acc[4 * v + 1]);
-                        const float2 a2 = f2_unpack(acc[4 * v + 2]);
-                        const float2 a3 = f2_unpack(acc[4 * v + 3]);
+                        const float2 a0 = acc[4 * v + 0];
+                        const float2 a1 = acc[4 * v + 1];
+                        const float2 a2 = acc[4 * v + 2];
+                        const float2 a3 = acc[4 * v + 3];
                         uint4 pk;
                         pk.x = pack_bf16x2(a0.x, a0.y);
                         pk.y = pack_bf16x2(a1.x, a1.y);
@@ -382,17 +401,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     float* y = static_cast<float*>(p.out) + p.out_off[g] +
                                static_cast<int64_t>(row) * p.out_ld + col0;
-                    float4* y4 = reinterpret_cast<float4*>(y);
 #pragma unroll
-                    for (int v = 0; v < 32; ++v) {
-                        const float2 a0 = f2_unpack(acc[2 * v + 0]);
-                        const float2 a1 = f2_unpack(acc[2 * v + 1]);
-                        float4 o = make_float4(a0.x, a0.y, a1.x, a1.y);
-                        if (p.accumulate) {
-                            const float4 prev = y4[v];
-                            o.x += prev.x; o.y += prev.y; o.z += prev.z; o.w += prev.w;
+                    for (int v = 0; v < 16; ++v) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            w[2 * e] = __float_as_uint(acc[4 * v + e].x);
+                            w[2 * e + 1] = __float_as_uint(acc[4 * v + e].y);
                         }
-                        y4[v] = o;
+                        if (p.accumulate) {
+                            uint32_t prev[8];
+                            ld_global_v8(y + 8 * v, prev);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(__uint_as_float(w[e]) + __uint_as_float(prev[e]));
+                        }
+                        st_global_v8(y + 8 * v, w);
                     }
                 }
             }

@@ -264,46 +264,6 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N)
 }
 
 // ---------------------------------------------------------------------------
-// Packed fp32 pairs (f32x2): one instruction does two IEEE fp32 operations.
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
-{
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-
-__device__ __forceinline__ uint64_t f2_pack_bits(uint32_t lo, uint32_t hi)
-{
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
-    return r;
-}
-
-__device__ __forceinline__ float2 f2_unpack(uint64_t v)
-{
-    float2 r;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-    return r;
-}
-
-// d = a * b + c, lane-wise, round to nearest
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
-{
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
-{
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-// ---------------------------------------------------------------------------
 // Number formats
 // ---------------------------------------------------------------------------
 
