@@ -7,8 +7,9 @@
 // tile shapes from "scratch: the backward pass, unrolled", "What is asserted,
 // and from where" (1x128 activations and gradients, 128x128 weights, 128x1
 // re-tiling for Wgrad). E4M3 -0 (0x80) is kept apart from +0 (prime-rl PR
-// #4073, conventions table, row "Negative zero"): the sign bit of every code
-// is the sign of its input.
+// #4073, conventions table, row "Negative zero"): the E4M3 conversion keeps
+// the sign of a result that rounds to zero, so every code carries the sign
+// of its input (the parity tests include tiles of tiny negatives).
 //
 // All three kernels are HBM streams: 16-byte vector loads, warp-shuffle
 // absmax reductions, coalesced payload and scale stores.
@@ -48,69 +49,86 @@ __device__ __noinline__ uint32_t encode2_exact(float v0, float v1, float s)
     return cvt_e4m3x2(__fdiv_rn(v0, s), __fdiv_rn(v1, s));
 }
 
-// One value's quotient fp32(v / s) without a division, and whether it is
-// certain to be the correctly rounded one.
+// Quotients fp32(v / s) of a pair of values without a division, with a
+// certificate that they are the correctly rounded ones, encoded to E4M3.
 //
-// q = RN(v * r) with r = RN(1/s) is within ~1.5 ulp of v/s. One correction
-// step (Markstein's method, IBM J. Res. Dev. 34(1), 1990) with the exact
-// FMA residual e = v - q s gives q1 = RN(q + e r), whose error is a few
+// q0 = RN(v * r) with r = RN(1/s) is within ~1.5 ulp of v/s. One correction
+// step (Markstein's method, IBM J. Res. Dev. 34(1), 1990) with the exact FMA
+// residual e0 = v - q0 s gives q1 = RN(q0 + e0 r), whose error is a few
 // 2^-24 ulp: q1 = RN(v/s) except when v/s lies within that distance of a
-// rounding boundary between two fp32 values. The check makes this exact:
-// with e1 = v - q1 s computed exactly by an FMA, |e1| < ulp(q1) s / 2 means
-// |v/s - q1| < ulp(q1) / 2, so q1 = RN(v/s). (For s not a power of two, v/s
-// is never exactly halfway between two floats; for a power of two, e1 = 0.
-// When q1 is a power of two the ulp below it is half as large, but a value
-// that close to a power of two has the same E4M3 code, which is all the
-// caller uses.) Below 2^-102 the ulp bound is clamped to 2^-126: such
-// quotients encode to a signed zero whatever their rounding. The caller
-// keeps s in [2^-60, 2^100] so that every quantity here stays normal.
-__device__ __forceinline__ float quotient_checked(float v, float s, float r, uint32_t& bad)
+// rounding boundary between two fp32 values. The certificate makes this
+// exact: with e1 = v - q1 s computed exactly by an FMA, |e1| < ulp(q1) s / 2
+// means |v/s - q1| < ulp(q1) / 2, so q1 = RN(v/s). (For s not a power of
+// two, v/s is never exactly halfway between two floats; for a power of two,
+// e1 = 0. When q1 is a power of two the ulp below it is half as large, but a
+// value that close to a power of two has the same E4M3 code, which is all
+// that is used here.) Below 2^-102 the ulp bound is clamped to 2^-126: such
+// quotients encode to a signed zero whatever their rounding. The caller keeps
+// s in [2^-60, 2^100] so that every quantity stays normal; `bad` becomes
+// non-zero when a certificate fails and the caller redoes the group with
+// exact division.
+//
+// The steps take the negated inputs nv = -v and nr = -r and form the
+// negated residuals (q s - v): then a zero input keeps its sign through the
+// chain (v = -0 gives q1 = -0 + -0), where the textbook order would turn it
+// into +0. The E4M3 conversion keeps the sign of a zero result, so -0 inputs
+// and tiny negatives both encode to 0x80. Pairs use the packed fp32x2
+// instructions.
+__device__ __forceinline__ int half_ulp_bits(float q)
 {
-    const float q0 = __fmul_rn(v, r);
-    const float q1 = __fmaf_rn(__fmaf_rn(-q0, s, v), r, q0);
-    const float e1 = __fmaf_rn(-q1, s, v);
-    const int half_ulp_bits = __viaddmax_s32(static_cast<int>(__float_as_uint(q1) & 0x7F800000u),
-                                             -(24 << 23), 0x00800000);
-    const float bound = __fmul_rn(s, __int_as_float(half_ulp_bits));
-    bad |= (fabsf(e1) < bound) ? 0u : 1u;
-    return q1;
+    return __viaddmax_s32(static_cast<int>(__float_as_uint(q) & 0x7F800000u), -(24 << 23), 0x00800000);
 }
 
-// E4M3 codes of fp32(v0 / s), fp32(v1 / s) (low byte = v0); `bad` becomes
-// non-zero when a quotient could not be certified and the caller must redo
-// the group with exact division (rare: only near fp32 rounding boundaries).
-__device__ __forceinline__ uint32_t encode2_fast(float v0, float v1, float s, float r, uint32_t& bad)
+__device__ __forceinline__ uint32_t encode2_fast(float2 nv, float s, float nr, uint32_t& bad)
 {
-    const float q0 = quotient_checked(v0, s, r, bad);
-    const float q1 = quotient_checked(v1, s, r, bad);
-    return cvt_e4m3x2(q0, q1);
+    const float2 s2 = make_float2(s, s);
+    const float2 nr2 = make_float2(nr, nr);
+    const float2 q0 = __fmul2_rn(nv, nr2);
+    const float2 q1 = __ffma2_rn(__ffma2_rn(q0, s2, nv), nr2, q0);
+    const float2 ne1 = __ffma2_rn(q1, s2, nv);
+    const float2 bound = __fmul2_rn(s2, make_float2(__int_as_float(half_ulp_bits(q1.x)),
+                                                    __int_as_float(half_ulp_bits(q1.y))));
+    bad |= (fabsf(ne1.x) < bound.x && fabsf(ne1.y) < bound.y) ? 0u : 1u;
+    return cvt_e4m3x2(q1.x, q1.y);
 }
 
-// Scale of a tile: s and its reciprocal for the fast path (r = 0 when s is
-// outside [2^-100, 2^100] and only the exact path may be used).
+// Negated bf16 halves of a word as fp32: -lo is (w << 16) with its top bit
+// flipped, which one integer multiply-add gives (adding 2^31 flips bit 31).
+__device__ __forceinline__ float neg_bf16_lo(uint32_t w)
+{
+    uint32_t r;
+    asm("mad.lo.u32 %0, %1, 65536, 0x80000000;" : "=r"(r) : "r"(w));
+    return __uint_as_float(r);
+}
+
+__device__ __forceinline__ float neg_bf16_hi(uint32_t w)
+{
+    return __uint_as_float((w & 0xFFFF0000u) ^ 0x80000000u);
+}
+
+__device__ __forceinline__ float2 neg_bf16x2(uint32_t w)
+{
+    return make_float2(neg_bf16_lo(w), neg_bf16_hi(w));
+}
+
+// Scale of a tile: s and the negated reciprocal for the fast path (nr = 0
+// when s is outside [2^-60, 2^100] and only the exact path may be used).
 struct TileScale {
     float s;
-    float r;
+    float nr;
 };
 
 __device__ __forceinline__ TileScale tile_scale_from_s(float s)
 {
     TileScale t;
     t.s = s;
-    t.r = (s >= 0x1p-60f && s <= 0x1p100f) ? __frcp_rn(s) : 0.0f;
+    t.nr = (s >= 0x1p-60f && s <= 0x1p100f) ? -__frcp_rn(s) : 0.0f;
     return t;
 }
 
 __device__ __forceinline__ TileScale tile_scale(float amax)
 {
     return tile_scale_from_s(scale_from_amax(amax));
-}
-
-// Sign bits of the four bf16 values in (w0, w1) at bit 7 of the matching
-// code bytes: the high byte of each bf16 carries its sign.
-__device__ __forceinline__ uint32_t sign_bits_4(uint32_t w0, uint32_t w1)
-{
-    return __byte_perm(w0, w1, 0x7531) & 0x80808080u;
 }
 
 __device__ __noinline__ uint2 quant8_exact(uint4 d, float s)
@@ -122,20 +140,17 @@ __device__ __noinline__ uint2 quant8_exact(uint4 d, float s)
 }
 
 // Eight bf16 values (one 16-byte load) divided by s and encoded, low
-// element first; the input's sign bit is copied into every code so that -0
-// (0x80) survives for tiny negatives. One branch per eight values: the rare
-// group with a quotient near a rounding boundary is redone exactly.
+// element first. One branch per eight values: the rare group with an
+// uncertified quotient is redone with exact division.
 __device__ __forceinline__ uint2 quant8(const uint4& d, const TileScale& t)
 {
-    uint32_t bad = t.r == 0.0f ? 1u : 0u;
-    const uint32_t c0 = encode2_fast(bf16_lo(d.x), bf16_hi(d.x), t.s, t.r, bad);
-    const uint32_t c1 = encode2_fast(bf16_lo(d.y), bf16_hi(d.y), t.s, t.r, bad);
-    const uint32_t c2 = encode2_fast(bf16_lo(d.z), bf16_hi(d.z), t.s, t.r, bad);
-    const uint32_t c3 = encode2_fast(bf16_lo(d.w), bf16_hi(d.w), t.s, t.r, bad);
+    uint32_t bad = t.nr == 0.0f ? 1u : 0u;
+    const uint32_t c0 = encode2_fast(neg_bf16x2(d.x), t.s, t.nr, bad);
+    const uint32_t c1 = encode2_fast(neg_bf16x2(d.y), t.s, t.nr, bad);
+    const uint32_t c2 = encode2_fast(neg_bf16x2(d.z), t.s, t.nr, bad);
+    const uint32_t c3 = encode2_fast(neg_bf16x2(d.w), t.s, t.nr, bad);
     uint2 o = make_uint2(__byte_perm(c0, c1, 0x5410), __byte_perm(c2, c3, 0x5410));
     if (bad != 0u) o = quant8_exact(d, t.s);
-    o.x |= sign_bits_4(d.x, d.y);
-    o.y |= sign_bits_4(d.z, d.w);
     return o;
 }
 
@@ -207,7 +222,7 @@ __global__ void __launch_bounds__(kQ1Threads) quant_1x128_kernel(
             const int src = (lane & 16) | i;    // the lane holding row 2i + h
             TileScale ts;
             ts.s = __shfl_sync(0xFFFFFFFFu, mine.s, src);
-            ts.r = __shfl_sync(0xFFFFFFFFu, mine.r, src);
+            ts.nr = __shfl_sync(0xFFFFFFFFu, mine.nr, src);
             const int64_t r = row0 + 2 * i + half;
             if (col_ok && r < rows) *reinterpret_cast<uint2*>(q + r * cols + col) = quant8(d[i], ts);
         }
@@ -314,16 +329,6 @@ __global__ void __launch_bounds__(kQ2Threads) quant_128x128_kernel(
 // ---------------------------------------------------------------------------
 constexpr int kQ3Threads = 256;
 
-// Sign bytes of the four 32-bit words x0..x3, byte b of each: returns
-// [x0.b, x1.b, x2.b, x3.b] with only bit 7 of each byte kept.
-__device__ __forceinline__ uint32_t column_signs(uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3,
-                                                 int b)
-{
-    const uint32_t lo = __byte_perm(x0, x1, (4 + b) << 4 | b);        // [x0.b, x1.b, ...]
-    const uint32_t hi = __byte_perm(x2, x3, (4 + b) << 4 | b);        // [x2.b, x3.b, ...]
-    return __byte_perm(lo, hi, 0x5410) & 0x80808080u;
-}
-
 // Mode B, phase 3 for one channel pair (j, j + 1) and 32 tokens of the staged
 // BF16 block [128 tokens x 128 channels]: each 32-bit shared load holds both
 // channels of one token. Returns false if any quotient needs the exact path.
@@ -331,19 +336,19 @@ __device__ __forceinline__ bool requant_pair_bf16(const uint8_t* stage, int part
                                                   const TileScale& t0, const TileScale& t1,
                                                   uint32_t (&w0)[8], uint32_t (&w1)[8])
 {
-    uint32_t bad = (t0.r == 0.0f || t1.r == 0.0f) ? 1u : 0u;
+    uint32_t bad = (t0.nr == 0.0f || t1.nr == 0.0f) ? 1u : 0u;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         uint32_t x[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
             x[e] = *reinterpret_cast<const uint32_t*>(stage + ((part * 32 + 4 * k + e) * 128 + j) * 2);
-        const uint32_t a01 = encode2_fast(bf16_lo(x[0]), bf16_lo(x[1]), t0.s, t0.r, bad);
-        const uint32_t a23 = encode2_fast(bf16_lo(x[2]), bf16_lo(x[3]), t0.s, t0.r, bad);
-        const uint32_t b01 = encode2_fast(bf16_hi(x[0]), bf16_hi(x[1]), t1.s, t1.r, bad);
-        const uint32_t b23 = encode2_fast(bf16_hi(x[2]), bf16_hi(x[3]), t1.s, t1.r, bad);
-        w0[k] = __byte_perm(a01, a23, 0x5410) | column_signs(x[0], x[1], x[2], x[3], 1);
-        w1[k] = __byte_perm(b01, b23, 0x5410) | column_signs(x[0], x[1], x[2], x[3], 3);
+        const uint32_t a01 = encode2_fast(make_float2(neg_bf16_lo(x[0]), neg_bf16_lo(x[1])), t0.s, t0.nr, bad);
+        const uint32_t a23 = encode2_fast(make_float2(neg_bf16_lo(x[2]), neg_bf16_lo(x[3])), t0.s, t0.nr, bad);
+        const uint32_t b01 = encode2_fast(make_float2(neg_bf16_hi(x[0]), neg_bf16_hi(x[1])), t1.s, t1.nr, bad);
+        const uint32_t b23 = encode2_fast(make_float2(neg_bf16_hi(x[2]), neg_bf16_hi(x[3])), t1.s, t1.nr, bad);
+        w0[k] = __byte_perm(a01, a23, 0x5410);
+        w1[k] = __byte_perm(b01, b23, 0x5410);
     }
     return bad == 0u;
 }
@@ -359,18 +364,15 @@ __device__ __noinline__ void requant_pair_bf16_exact(const uint8_t* stage, int p
         for (int e = 0; e < 4; ++e)
             x[e] = *reinterpret_cast<const uint32_t*>(stage + ((part * 32 + 4 * k + e) * 128 + j) * 2);
         reinterpret_cast<uint32_t*>(dst0)[k] =
-            (encode2_exact(bf16_lo(x[0]), bf16_lo(x[1]), s0) |
-             (encode2_exact(bf16_lo(x[2]), bf16_lo(x[3]), s0) << 16)) |
-            column_signs(x[0], x[1], x[2], x[3], 1);
+            encode2_exact(bf16_lo(x[0]), bf16_lo(x[1]), s0) | (encode2_exact(bf16_lo(x[2]), bf16_lo(x[3]), s0) << 16);
         reinterpret_cast<uint32_t*>(dst1)[k] =
-            (encode2_exact(bf16_hi(x[0]), bf16_hi(x[1]), s1) |
-             (encode2_exact(bf16_hi(x[2]), bf16_hi(x[3]), s1) << 16)) |
-            column_signs(x[0], x[1], x[2], x[3], 3);
+            encode2_exact(bf16_hi(x[0]), bf16_hi(x[1]), s1) | (encode2_exact(bf16_hi(x[2]), bf16_hi(x[3]), s1) << 16);
     }
 }
 
 // Decoded values of the four E4M3 codes in x (channel c = byte c), each
-// multiplied by the token's 1x128 scale in fp32.
+// multiplied by the token's 1x128 scale in fp32 (the fast path passes the
+// negated scale, which negates the products exactly).
 __device__ __forceinline__ void decode4_scaled(uint32_t x, float s1, float (&v)[4])
 {
     const float2 a = e4m3x2_to_f32(static_cast<uint16_t>(x & 0xFFFFu));
@@ -387,22 +389,22 @@ __device__ __forceinline__ bool requant_quad_e4m3(const uint8_t* stage, const fl
                                                   int part, int j, const TileScale (&ts)[4],
                                                   uint32_t (&w)[4][4])
 {
-    uint32_t bad = (ts[0].r == 0.0f || ts[1].r == 0.0f || ts[2].r == 0.0f || ts[3].r == 0.0f) ? 1u : 0u;
+    uint32_t bad = (ts[0].nr == 0.0f || ts[1].nr == 0.0f || ts[2].nr == 0.0f || ts[3].nr == 0.0f) ? 1u : 0u;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         uint32_t x[4];
-        float v[4][4];   // [token][channel]
+        float nv[4][4];   // [token][channel], negated
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int rl = part * 16 + 4 * k + e;
             x[e] = *reinterpret_cast<const uint32_t*>(stage + rl * 128 + j);
-            decode4_scaled(x[e], row_scale[rl], v[e]);
+            decode4_scaled(x[e], -row_scale[rl], nv[e]);
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            const uint32_t c01 = encode2_fast(v[0][c], v[1][c], ts[c].s, ts[c].r, bad);
-            const uint32_t c23 = encode2_fast(v[2][c], v[3][c], ts[c].s, ts[c].r, bad);
-            w[c][k] = __byte_perm(c01, c23, 0x5410) | column_signs(x[0], x[1], x[2], x[3], c);
+            const uint32_t c01 = encode2_fast(make_float2(nv[0][c], nv[1][c]), ts[c].s, ts[c].nr, bad);
+            const uint32_t c23 = encode2_fast(make_float2(nv[2][c], nv[3][c]), ts[c].s, ts[c].nr, bad);
+            w[c][k] = __byte_perm(c01, c23, 0x5410);
         }
     }
     return bad == 0u;
@@ -425,8 +427,7 @@ __device__ __noinline__ void requant_quad_e4m3_exact(const uint8_t* stage, const
         }
         for (int c = 0; c < 4; ++c)
             reinterpret_cast<uint32_t*>(dst + c * mpad)[k] =
-                (encode2_exact(v[0][c], v[1][c], sc[c]) | (encode2_exact(v[2][c], v[3][c], sc[c]) << 16)) |
-                column_signs(x[0], x[1], x[2], x[3], c);
+                encode2_exact(v[0][c], v[1][c], sc[c]) | (encode2_exact(v[2][c], v[3][c], sc[c]) << 16);
     }
 }
 
@@ -587,10 +588,13 @@ cudaError_t launch_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, in
                                cudaStream_t stream)
 {
     if (rows == 0) return cudaSuccess;
+    // One unit (32 rows x 128 columns) per warp: blocks run in as many waves
+    // as the tensor needs, which balances better than a capped grid-stride
+    // loop when the unit count is a few times the resident warp count.
     const int64_t units = ((cols + 127) / 128) * ((rows + 31) / 32);
     const int64_t warps_per_block = kQ1Threads / 32;
     int64_t blocks = (units + warps_per_block - 1) / warps_per_block;
-    const int64_t cap = (int64_t)num_sms * 4;  // grid-stride beyond a few resident waves
+    const int64_t cap = (int64_t)num_sms * 512;  // grid-stride only for very large tensors
     if (blocks > cap) blocks = cap;
     quant_1x128_kernel<<<(unsigned)blocks, kQ1Threads, 0, stream>>>(x, rows, cols, ldx, q, scales,
                                                                    scale_ld);

@@ -25,7 +25,8 @@ def _lib():
 
 def _special_inputs(R, C, seed):
     """N(0,1) with 1% outliers, an all-zero tile, a tile of tiny negatives
-    (-0 results), a tile whose absmax is negative, a tile with amax 448
+    and exact -0 inputs (-0 results), a tile whose absmax is negative (with
+    a +0 and a -0 input), a tile with amax 448
     (scale 1) holding exact E4M3 midpoints (ties to even), and a tile of
     values around 1e-20 (a scale below 2^-60, where the kernels divide
     exactly instead of using the reciprocal path)."""
@@ -35,9 +36,13 @@ def _special_inputs(R, C, seed):
         x[0, :w] = 0.0
     if R > 1:
         x[1, :w] = -1e-30
+        x[1, 2:w:3] = -0.0
         x[1, 0] = 1.0
     if R > 2:
         x[2, :w] = torch.linspace(-300.0, 2.0, w).to(torch.bfloat16)
+        if w > 6:
+            x[2, 5] = 0.0
+            x[2, 6] = -0.0
     if R > 3:
         t = oracle.e4m3_table()
         fin = t[:0x7E].astype(np.float64)
