@@ -77,22 +77,6 @@ struct SharedCtl {
     volatile int abort;
 };
 
-// 32-byte global store / load (one full sector per thread).
-__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8])
-{
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
-                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-                 : "memory");
-}
-
-__device__ __forceinline__ void ld_global_v8(const void* p, uint32_t (&w)[8])
-{
-    asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
-                 : "l"(p)
-                 : "memory");
-}
-
 __device__ __forceinline__ void record_status(unsigned int* status, unsigned int code)
 {
     atomicCAS(status, 0u, code);
@@ -109,6 +93,244 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, int t, int& g, 
     const int local = t - p.tile_start[g];
     mt = local / p.n_tiles;
     nt = local - mt * p.n_tiles;
+}
+
+// ---------------------------------------------------------------------------
+// Promotion epilogues (warps 4-11). Each warp owns the 32 TMEM lanes (tile
+// rows) of its quarter and one 128-column half of the tile. Both return
+// false when a wait gave up.
+// ---------------------------------------------------------------------------
+
+// Fprop / Dgrad: s_b is one value per 128 output columns, so a K-block's
+// scale is one scalar per thread (row) and half. Layout 32x32b: thread =
+// row, 128 columns in registers; BF16 output in 16-byte row segments.
+__device__ __forceinline__ bool epilogue_block_scale(const GemmParams& p, SharedCtl* ctl, uint32_t tmem_base,
+                                                     int warp, int lane, uint64_t limit)
+{
+    const int ew = warp - kFirstEpiWarp;
+    const int quarter = warp & 3;   // TMEM lanes this warp may access
+    const int half = ew >> 2;       // 128-column half of the tile
+    const int r_in_tile = quarter * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    uint32_t acc_it = 0;
+
+    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        int g, mt, nt;
+        decode_tile(p, t, g, mt, nt);
+        const int nkb = p.kblocks[g];
+        const int row = p.a_row0[g] + mt * kBM + r_in_tile;   // A row = output row
+        const bool row_ok = (mt * kBM + r_in_tile) < p.a_rows[g];
+        const int col0 = nt * kBN + half * 128;
+        const bool cols_ok = col0 < p.n_cols;                  // n_cols % 128 == 0
+        const bool sa_ok = row < p.sa_rows;
+        const float* sa_ptr = p.sa + static_cast<int64_t>(p.sa_kb0[g]) * p.sa_ld + row;
+        const float* sb_ptr = p.sb + p.sb_off[g] + static_cast<int64_t>(col0 / 128) * p.sb_cstride;
+
+        auto load_sa = [&](int kb) -> float {
+            return (sa_ok && kb < nkb) ? __ldg(sa_ptr + static_cast<int64_t>(kb) * p.sa_ld) : 0.0f;
+        };
+        auto load_sb = [&](int kb) -> float {
+            return (cols_ok && kb < nkb) ? __ldg(sb_ptr + static_cast<int64_t>(kb) * p.sb_kstride) : 0.0f;
+        };
+
+        float2 acc[64];     // 128 fp32 accumulators as 64 pairs (packed f32x2 math)
+#pragma unroll
+        for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.f, 0.f);
+
+        // scalar scales two K-blocks ahead in registers
+        float sa0 = load_sa(0), sa1 = load_sa(1), sb0 = load_sb(0), sb1 = load_sb(1);
+
+        for (int kb = 0; kb < nkb; ++kb, ++acc_it) {
+            const float s_blk = sa0 * sb0;
+            sa0 = sa1;
+            sa1 = load_sa(kb + 2);
+            sb0 = sb1;
+            sb1 = load_sb(kb + 2);
+            const float2 s_blk2 = make_float2(s_blk, s_blk);
+
+            const uint32_t buf = acc_it & 1u;
+            const uint32_t aph = (acc_it >> 1) & 1u;
+            if (ctl->abort || !mbar_wait(&ctl->tfull[buf], aph, limit)) return false;
+            tc_fence_after_sync();
+            const uint32_t taddr = tmem_base + lane_addr + buf * kBN + half * 128;
+
+            // promote one 32-column chunk of the partial held in r
+            auto promote = [&](int c, uint32_t (&r)[32]) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    acc[c * 16 + i] = __ffma2_rn(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
+                                                 s_blk2, acc[c * 16 + i]);
+            };
+            // TMEM loads double-buffered: chunk c + 1 is in flight while
+            // chunk c is promoted
+            uint32_t ra[32], rb[32];
+            tmem_ld_x32(taddr + 0, ra);
+            tmem_ld_wait(ra);
+            tmem_ld_x32(taddr + 32, rb);
+            promote(0, ra);
+            tmem_ld_wait(rb);
+            tmem_ld_x32(taddr + 64, ra);
+            promote(1, rb);
+            tmem_ld_wait(ra);
+            tmem_ld_x32(taddr + 96, rb);
+            promote(2, ra);
+            tmem_ld_wait(rb);
+            // the partial is in registers: hand the TMEM buffer back
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
+            promote(3, rb);
+        }
+
+        if (row_ok && cols_ok) {
+            uint16_t* y = static_cast<uint16_t*>(p.out) + p.out_off[g] + static_cast<int64_t>(row) * p.out_ld + col0;
+#pragma unroll
+            for (int v = 0; v < 16; ++v) {
+                const float2 a0 = acc[4 * v + 0];
+                const float2 a1 = acc[4 * v + 1];
+                const float2 a2 = acc[4 * v + 2];
+                const float2 a3 = acc[4 * v + 3];
+                uint4 pk;
+                pk.x = pack_bf16x2(a0.x, a0.y);
+                pk.y = pack_bf16x2(a1.x, a1.y);
+                pk.z = pack_bf16x2(a2.x, a2.y);
+                pk.w = pack_bf16x2(a3.x, a3.y);
+                reinterpret_cast<uint4*>(y)[v] = pk;
+            }
+        }
+    }
+    return true;
+}
+
+// Wgrad: both scales are vectors (one per output row and one per output
+// column for every K-block), so every element needs its own s_a * s_b. With
+// the 32x32b layout each thread would need all 128 column scales of its half
+// every K-block, read as shared-memory broadcasts that cost more load
+// bandwidth than the MMA leaves room for. The 16x256b layout spreads the
+// tile as 4 rows x 32 columns per thread: a K-block then needs 4 row scales
+// and 16 column-scale pairs per thread. Scales arrive in a per-warp 3-slot
+// shared-memory ring filled by cp.async two K-blocks ahead (slot: the 32 row
+// scales of the warp's quarter, then its 128 column scales).
+__device__ __forceinline__ bool epilogue_vector_scale(const GemmParams& p, SharedCtl* ctl, uint8_t* vec_smem,
+                                                      uint32_t tmem_base, int warp, int lane, uint64_t limit)
+{
+    const int ew = warp - kFirstEpiWarp;
+    const int quarter = warp & 3;
+    const int half = ew >> 2;
+    const int g4 = lane >> 2;       // row within each group of 8
+    const int t4 = lane & 3;        // column pair within each group of 8
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    float* vring = reinterpret_cast<float*>(vec_smem) + ew * (kVecSlots * kSlotFloats);
+    uint32_t acc_it = 0;
+
+    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        int g, mt, nt;
+        decode_tile(p, t, g, mt, nt);
+        const int nkb = p.kblocks[g];
+        const int qrow0 = mt * kBM + quarter * 32;             // first tile row of this quarter
+        const int col0 = nt * kBN + half * 128;
+        const bool cols_ok = col0 < p.n_cols;                  // n_cols % 128 == 0
+        // cp.async sources: lane l fetches the A scale of row qrow0 + l and
+        // the B scales of columns col0 + 4l .. 4l + 3
+        const int srow = p.a_row0[g] + qrow0 + lane;
+        const bool sa_ok = srow < p.sa_rows;
+        const float* sa_ptr = p.sa + static_cast<int64_t>(p.sa_kb0[g]) * p.sa_ld + srow;
+        const float* sb_ptr = p.sb + p.sb_off[g] + static_cast<int64_t>(col0 + 4 * lane);
+        auto prefetch = [&](int kb) {
+            if (kb < nkb) {
+                float* slot = vring + (kb % kVecSlots) * kSlotFloats;
+                cp_async_4(slot + lane, sa_ok ? sa_ptr + static_cast<int64_t>(kb) * p.sa_ld : p.sa, sa_ok ? 4u : 0u);
+                cp_async_16(slot + 32 + 4 * lane, cols_ok ? sb_ptr + static_cast<int64_t>(kb) * p.sb_kstride : p.sb,
+                            cols_ok ? 16u : 0u);
+            }
+            cp_async_commit();
+        };
+
+        float2 acc[4][16];   // [row i: g4 + 8 i][column group j: 8 j + 2 t4, + 1]
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[i][j] = make_float2(0.f, 0.f);
+
+        prefetch(0);
+        prefetch(1);
+        for (int kb = 0; kb < nkb; ++kb, ++acc_it) {
+            prefetch(kb + 2);
+            cp_async_wait<2>();   // K-block kb's scales have landed
+            __syncwarp();
+            const float* slot = vring + (kb % kVecSlots) * kSlotFloats;
+            float2 sa2[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float v = slot[g4 + 8 * i];
+                sa2[i] = make_float2(v, v);
+            }
+            const float2* sbp = reinterpret_cast<const float2*>(slot + 32) + t4;
+
+            const uint32_t buf = acc_it & 1u;
+            const uint32_t aph = (acc_it >> 1) & 1u;
+            if (ctl->abort || !mbar_wait(&ctl->tfull[buf], aph, limit)) {
+                cp_async_wait<0>();
+                return false;
+            }
+            tc_fence_after_sync();
+            const uint32_t taddr = tmem_base + lane_addr + buf * kBN + half * 128;
+
+            // promote the 32-column group c (rows g4, g4 + 8 in r[0..15],
+            // rows g4 + 16, g4 + 24 in r[16..31])
+            auto promote = [&](int c, uint32_t (&r)[32]) {
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int j = 4 * c + jj;
+                    const float2 sb = sbp[4 * j];     // columns 8 j + 2 t4, + 1
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int k = 16 * (i >> 1) + 4 * jj + 2 * (i & 1);
+                        acc[i][j] = __ffma2_rn(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])),
+                                               __fmul2_rn(sa2[i], sb), acc[i][j]);
+                    }
+                }
+            };
+            uint32_t ra[32], rb[32];
+            tmem_ld_16x256b_x4_pair(taddr + 0, ra);
+            tmem_ld_wait(ra);
+            tmem_ld_16x256b_x4_pair(taddr + 32, rb);
+            promote(0, ra);
+            tmem_ld_wait(rb);
+            tmem_ld_16x256b_x4_pair(taddr + 64, ra);
+            promote(1, rb);
+            tmem_ld_wait(ra);
+            tmem_ld_16x256b_x4_pair(taddr + 96, rb);
+            promote(2, ra);
+            tmem_ld_wait(rb);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
+            promote(3, rb);
+        }
+        cp_async_wait<0>();
+
+        if (cols_ok) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r_tile = qrow0 + g4 + 8 * i;
+                if (r_tile >= p.a_rows[g]) continue;
+                float* y = static_cast<float*>(p.out) + p.out_off[g] +
+                           static_cast<int64_t>(p.a_row0[g] + r_tile) * p.out_ld + col0 + 2 * t4;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    float2 v = acc[i][j];
+                    float2* dst = reinterpret_cast<float2*>(y + 8 * j);
+                    if (p.accumulate) {
+                        const float2 prev = *dst;
+                        v = __fadd2_rn(v, prev);
+                    }
+                    *dst = v;
+                }
+            }
+        }
+    }
+    return true;
 }
 
 template <GemmKind kKind>
@@ -238,188 +460,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Promotion epilogue
         // ------------------------------------------------------------------
         setmaxnreg_inc<kEpilogueRegs>();
-        const int ew = warp - kFirstEpiWarp;
-        const int quarter = warp & 3;   // TMEM lanes this warp may access
-        const int half = ew >> 2;       // 128-column half of the tile
-        const int r_in_tile = quarter * 32 + lane;
-        const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-        // Wgrad's per-column B scales: a 3-slot ring per warp, filled two
-        // K-blocks ahead (lane l holds columns 4l .. 4l + 3 of a slot)
-        float* vring = reinterpret_cast<float*>(smem + kStages * kStageBytes + kCtlBytes) +
-                       ew * (kVecSlots * kSlotFloats);
-        uint32_t acc_it = 0;
-        bool ok = true;
-
-        for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
-            int g, mt, nt;
-            decode_tile(p, t, g, mt, nt);
-            const int nkb = p.kblocks[g];
-            const int row = p.a_row0[g] + mt * kBM + r_in_tile;   // A row = output row
-            const bool row_ok = (mt * kBM + r_in_tile) < p.a_rows[g];
-            const int col0 = nt * kBN + half * 128;
-            const bool cols_ok = col0 < p.n_cols;                  // n_cols % 128 == 0
-            const bool sa_ok = row < p.sa_rows;
-            const float* sa_ptr = p.sa + static_cast<int64_t>(p.sa_kb0[g]) * p.sa_ld + row;
-            const float* sb_ptr = p.sb + p.sb_off[g] +
-                                  (kKind == GemmKind::kBlockScaleBf16
-                                       ? static_cast<int64_t>(col0 / 128) * p.sb_cstride
-                                       : static_cast<int64_t>(col0 + 4 * lane));
-
-            auto load_sa = [&](int kb) -> float {
-                return (sa_ok && kb < nkb) ? __ldg(sa_ptr + static_cast<int64_t>(kb) * p.sa_ld) : 0.0f;
-            };
-            auto load_sb = [&](int kb) -> float {
-                return (cols_ok && kb < nkb) ? __ldg(sb_ptr + static_cast<int64_t>(kb) * p.sb_kstride) : 0.0f;
-            };
-            auto load_vec = [&](int kb) -> float4 {
-                return (cols_ok && kb < nkb)
-                           ? __ldg(reinterpret_cast<const float4*>(sb_ptr + static_cast<int64_t>(kb) * p.sb_kstride))
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-            };
-
-            float2 acc[64];     // 128 fp32 accumulators as 64 pairs (packed f32x2 math)
-#pragma unroll
-            for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.f, 0.f);
-
-            // Fprop/Dgrad: scalar scales two K-blocks ahead in registers.
-            // Wgrad: per-warp smem ring filled by cp.async two K-blocks ahead.
-            float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
-            auto prefetch = [&](int kb) {
-                if (kb < nkb) {
-                    float* slot = vring + (kb % kVecSlots) * kSlotFloats;
-                    cp_async_4(slot + lane, sa_ok ? sa_ptr + static_cast<int64_t>(kb) * p.sa_ld : p.sa,
-                               sa_ok ? 4u : 0u);
-                    cp_async_16(slot + 32 + 4 * lane,
-                                cols_ok ? sb_ptr + static_cast<int64_t>(kb) * p.sb_kstride : p.sb,
-                                cols_ok ? 16u : 0u);
-                }
-                cp_async_commit();
-            };
-            if constexpr (kKind == GemmKind::kBlockScaleBf16) {
-                sa0 = load_sa(0);
-                sa1 = load_sa(1);
-                sb0 = load_sb(0);
-                sb1 = load_sb(1);
-            } else {
-                prefetch(0);
-                prefetch(1);
-            }
-
-            for (int kb = 0; kb < nkb; ++kb, ++acc_it) {
-                float s_a = 0.f, s_blk = 0.f;
-                const float4* vslot = nullptr;
-                if constexpr (kKind == GemmKind::kBlockScaleBf16) {
-                    s_a = sa0;
-                    s_blk = sa0 * sb0;
-                    sa0 = sa1;
-                    sa1 = load_sa(kb + 2);
-                    sb0 = sb1;
-                    sb1 = load_sb(kb + 2);
-                } else {
-                    prefetch(kb + 2);
-                    cp_async_wait<2>();   // K-block kb's scales have landed
-                    __syncwarp();
-                    const float* slot = vring + (kb % kVecSlots) * kSlotFloats;
-                    s_a = slot[lane];
-                    vslot = reinterpret_cast<const float4*>(slot + 32);
-                }
-                const float2 s_blk2 = make_float2(s_blk, s_blk);
-                const float2 s_a2 = make_float2(s_a, s_a);
-
-                const uint32_t buf = acc_it & 1u;
-                const uint32_t aph = (acc_it >> 1) & 1u;
-                if (ctl->abort || !mbar_wait(&ctl->tfull[buf], aph, limit)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-                const uint32_t taddr = tmem_base + lane_addr + buf * kBN + half * 128;
-
-                // promote one 32-column chunk of the partial held in r
-                auto promote = [&](int c, uint32_t (&r)[32]) {
-                    if constexpr (kKind == GemmKind::kBlockScaleBf16) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            acc[c * 16 + i] = __ffma2_rn(
-                                make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), s_blk2,
-                                acc[c * 16 + i]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float4 sbv = vslot[c * 8 + i];
-                            const float2 sc0 = __fmul2_rn(s_a2, make_float2(sbv.x, sbv.y));
-                            const float2 sc1 = __fmul2_rn(s_a2, make_float2(sbv.z, sbv.w));
-                            acc[c * 16 + 2 * i] = __ffma2_rn(
-                                make_float2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])), sc0,
-                                acc[c * 16 + 2 * i]);
-                            acc[c * 16 + 2 * i + 1] = __ffma2_rn(
-                                make_float2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])), sc1,
-                                acc[c * 16 + 2 * i + 1]);
-                        }
-                    }
-                };
-                // TMEM loads double-buffered: chunk c + 1 is in flight while
-                // chunk c is promoted
-                uint32_t ra[32], rb[32];
-                tmem_ld_x32(taddr + 0, ra);
-                tmem_ld_wait(ra);
-                tmem_ld_x32(taddr + 32, rb);
-                promote(0, ra);
-                tmem_ld_wait(rb);
-                tmem_ld_x32(taddr + 64, ra);
-                promote(1, rb);
-                tmem_ld_wait(ra);
-                tmem_ld_x32(taddr + 96, rb);
-                promote(2, ra);
-                tmem_ld_wait(rb);
-                // the partial is in registers: hand the TMEM buffer back
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
-                promote(3, rb);
-            }
-            if constexpr (kKind == GemmKind::kVectorScaleF32) cp_async_wait<0>();
-            if (!ok) break;
-
-            if (row_ok && cols_ok) {
-                if constexpr (kKind == GemmKind::kBlockScaleBf16) {
-                    uint16_t* y = static_cast<uint16_t*>(p.out) + p.out_off[g] +
-                                  static_cast<int64_t>(row) * p.out_ld + col0;
-#pragma unroll
-                    for (int v = 0; v < 16; ++v) {
-                        const float2 a0 = acc[4 * v + 0];
-                        const float2 a1 = acc[4 * v + 1];
-                        const float2 a2 = acc[4 * v + 2];
-                        const float2 a3 = acc[4 * v + 3];
-                        uint4 pk;
-                        pk.x = pack_bf16x2(a0.x, a0.y);
-                        pk.y = pack_bf16x2(a1.x, a1.y);
-                        pk.z = pack_bf16x2(a2.x, a2.y);
-                        pk.w = pack_bf16x2(a3.x, a3.y);
-                        reinterpret_cast<uint4*>(y)[v] = pk;
-                    }
-                } else {
-                    float* y = static_cast<float*>(p.out) + p.out_off[g] +
-                               static_cast<int64_t>(row) * p.out_ld + col0;
-#pragma unroll
-                    for (int v = 0; v < 16; ++v) {
-                        uint32_t w[8];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            w[2 * e] = __float_as_uint(acc[4 * v + e].x);
-                            w[2 * e + 1] = __float_as_uint(acc[4 * v + e].y);
-                        }
-                        if (p.accumulate) {
-                            uint32_t prev[8];
-                            ld_global_v8(y + 8 * v, prev);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(__uint_as_float(w[e]) + __uint_as_float(prev[e]));
-                        }
-                        st_global_v8(y + 8 * v, w);
-                    }
-                }
-            }
-        }
+        bool ok;
+        if constexpr (kKind == GemmKind::kBlockScaleBf16)
+            ok = epilogue_block_scale(p, ctl, tmem_base, warp, lane, limit);
+        else
+            ok = epilogue_vector_scale(p, ctl, smem + kStages * kStageBytes + kCtlBytes, tmem_base, warp,
+                                       lane, limit);
         if (!ok) {
             record_status(p.status, FP8BS_ERR_TIMEOUT);
             ctl->abort = 1;

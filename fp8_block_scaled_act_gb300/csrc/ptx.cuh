@@ -209,6 +209,32 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32])
 // Waits for this thread's outstanding TMEM loads. The registers written by
 // those loads are tied to the wait as in/out operands so that the compiler
 // cannot move their uses above it.
+// Two 16-lane x 32-column loads (shape 16x256b, four repetitions): the
+// lower 16 lanes of the warp's quarter at taddr into r[0..15], the upper 16
+// at taddr + (16 << 16) into r[16..31]. In each 8-column repetition j,
+// thread t holds row t / 4 at columns 2 (t % 4) and 2 (t % 4) + 1 in
+// registers 4j and 4j + 1, and row t / 4 + 8 at the same columns in 4j + 2
+// and 4j + 3.
+__device__ __forceinline__ void tmem_ld_16x256b_x4_pair(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr + (16u << 16))
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32])
 {
     asm volatile(
