@@ -25,7 +25,8 @@ __all__ = [
     "Fp8bsError", "build", "lib", "lib_path",
     "fp8_quant_1x128", "fp8_quant_128x128", "fp8_requant_128x1_T",
     "fp8_block_gemm_fprop", "fp8_block_gemm_dgrad", "fp8_block_gemm_wgrad",
-    "fp8_block_gemm_grouped", "fp8bs_device_status", "fp8bs_set_wait_limit_ns",
+    "fp8_block_gemm_grouped", "fp8_block_gemm_splitk", "fp8bs_splitk_workspace_size",
+    "fp8bs_splitk_default_splits", "fp8bs_device_status", "fp8bs_set_wait_limit_ns",
     "fp8bs_selftest_wait_timeout", "fp8bs_scale_ld", "fp8bs_padded_tokens",
     "fp8bs_status_str", "fp8bs_version",
     "empty_quant_1x128", "empty_quant_128x128", "empty_requant_128x1_T",
@@ -80,6 +81,9 @@ def lib() -> ctypes.CDLL:
         "fp8_block_gemm_dgrad": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_block_gemm_wgrad": ([P, P, P, P, I64, I64, I64, P, I, P], S),
         "fp8_block_gemm_grouped": ([I, I32, P, P, P, P, P, I64, I64, P, I, P], S),
+        "fp8bs_splitk_workspace_size": ([I, I64, I64, I64, I32], ctypes.c_size_t),
+        "fp8bs_splitk_default_splits": ([I, I64, I64, I64], I32),
+        "fp8_block_gemm_splitk": ([I, P, P, P, P, I64, I64, I64, I32, P, P, ctypes.c_size_t, P], S),
         "fp8bs_device_status": ([I], S),
         "fp8bs_set_wait_limit_ns": ([ctypes.c_uint64], None),
         "fp8bs_selftest_wait_timeout": ([ctypes.c_uint64, P], S),
@@ -291,6 +295,55 @@ def fp8_block_gemm_grouped(op: int, offsets, a, sa, b, sb, out, N: int, K: int,
     _check("fp8_block_gemm_grouped", lib().fp8_block_gemm_grouped(
         int(op), off.size - 1, off.ctypes.data_as(ctypes.c_void_p), _ptr(a), _ptr(sa), _ptr(b),
         _ptr(sb), int(N), int(K), _ptr(out), int(bool(accumulate)), _stream(stream)))
+
+
+def _splitk_dims(op: int, a, b):
+    """(M, N, K) of a split-K call from its operands (see fp8bs.h)."""
+    if op == OP_FPROP:      # a = xq [M x K], b = wqT [N x K]
+        M, K = a.shape
+        N = b.shape[0]
+        if b.shape != (N, K):
+            raise ValueError("shape mismatch")
+        return M, N, K, (M, N)
+    if op == OP_DGRAD:      # a = dyq [M x N], b = wq [K x N]
+        M, N = a.shape
+        K = b.shape[0]
+        if b.shape != (K, N):
+            raise ValueError("shape mismatch")
+        return M, N, K, (M, K)
+    raise ValueError("split-K supports OP_FPROP and OP_DGRAD")
+
+
+def fp8bs_splitk_workspace_size(op: int, M: int, N: int, K: int, splits: int) -> int:
+    return int(lib().fp8bs_splitk_workspace_size(int(op), int(M), int(N), int(K), int(splits)))
+
+
+def fp8bs_splitk_default_splits(op: int, M: int, N: int, K: int) -> int:
+    return int(lib().fp8bs_splitk_default_splits(int(op), int(M), int(N), int(K)))
+
+
+def fp8_block_gemm_splitk(op: int, a, sa, b, sb, out, splits: Optional[int] = None,
+                          workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Split-K Fprop (a = xq, b = wqT) or Dgrad (a = dyq, b = wq) into BF16 `out`.
+
+    `splits` defaults to fp8bs_splitk_default_splits. `workspace` is a device
+    buffer of at least fp8bs_splitk_workspace_size bytes; if None, one is
+    allocated here with torch (memory plumbing only)."""
+    for t, n, d in ((a, "a", torch.uint8), (sa, "sa", torch.float32), (b, "b", torch.uint8),
+                    (sb, "sb", torch.float32), (out, "out", torch.bfloat16)):
+        _need(t, d, n)
+    M, N, K, out_shape = _splitk_dims(op, a, b)
+    if tuple(out.shape) != out_shape:
+        raise ValueError("shape mismatch")
+    if splits is None:
+        splits = fp8bs_splitk_default_splits(op, M, N, K)
+    need = fp8bs_splitk_workspace_size(op, M, N, K, splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=a.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("fp8_block_gemm_splitk", lib().fp8_block_gemm_splitk(
+        int(op), _ptr(a), _ptr(sa), _ptr(b), _ptr(sb), M, N, K, int(splits), _ptr(out),
+        _ptr(workspace), wbytes, _stream(stream)))
 
 
 def fp8bs_device_status(reset: bool = True) -> int:

@@ -91,6 +91,8 @@ void init_params(GemmParams& p, DeviceState* st, int n_cols)
     std::memset(&p, 0, sizeof(p));
     p.n_cols = n_cols;
     p.n_tiles = (n_cols + kBN - 1) / kBN;
+    p.splits = 1;
+    p.kb_per_split = 1 << 30;
     p.wait_limit_ns = g_wait_limit_ns;
     p.status = st->status;
 }
@@ -115,9 +117,23 @@ int64_t padded_tokens(int64_t rows, const int32_t* off, int32_t groups)
 // Fprop / Dgrad, dense or grouped. For Fprop the contraction length is K and
 // the output width N; for Dgrad they are N and K. `contr` and `width` are
 // those two; b rows per group = width.
+// Split-K shape: with `splits` requested over nkb K-blocks, each range takes
+// kps = ceil(nkb / splits) blocks and `used` = ceil(nkb / kps) ranges are
+// non-empty.
+void splitk_shape(int64_t nkb, int64_t splits, int& used, int& kps)
+{
+    if (splits > nkb) splits = nkb;
+    if (splits < 1) splits = 1;
+    kps = static_cast<int>((nkb + splits - 1) / splits);
+    used = static_cast<int>((nkb + kps - 1) / kps);
+}
+
+// Fprop / Dgrad, dense or grouped; with splits > 1 (dense only) the
+// K-blocks of every tile are cut into ranges whose fp32 sums go to the
+// workspace `ws`, followed by the reduction kernel.
 fp8bs_status run_rowwise_gemm(bool dgrad, int32_t groups, const int32_t* off, const uint8_t* a,
                               const float* sa, const uint8_t* b, const float* sb, int64_t N,
-                              int64_t K, void* out, void* stream)
+                              int64_t K, void* out, void* stream, int32_t splits = 1, float* ws = nullptr)
 {
     DeviceState* st = nullptr;
     fp8bs_status s = device_state(&st);
@@ -158,13 +174,25 @@ fp8bs_status run_rowwise_gemm(bool dgrad, int32_t groups, const int32_t* off, co
     p.out = out;
     p.out_ld = width;
     p.accumulate = 0;
+    int used = 1, kps = 1 << 30;
+    if (splits > 1 && groups == 1) splitk_shape(contr / kBK, splits, used, kps);
+    if (used > 1) {
+        if (!ws) return FP8BS_ERR_ARG;
+        p.splits = used;
+        p.kb_per_split = kps;
+        p.ws = ws;
+        p.ws_split_stride = M * width;
+    }
 
     CUtensorMap ma, mb;
     if (!make_map(&ma, a, contr, M, contr, kBM) ||
         !make_map(&mb, b, contr, width * groups, contr, kBN))
         return FP8BS_ERR_ARG;
-    return launch_status(launch_gemm(GemmKind::kBlockScaleBf16, ma, mb, p, st->num_sms,
-                                     static_cast<cudaStream_t>(stream)));
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const fp8bs_status r = launch_status(launch_gemm(GemmKind::kBlockScaleBf16, ma, mb, p, st->num_sms, cs));
+    if (r != FP8BS_OK || used <= 1) return r;
+    return launch_status(
+        launch_splitk_reduce(ws, used, M * width, M * width, static_cast<uint16_t*>(out), st->num_sms, cs));
 }
 
 // Wgrad, dense (groups = 1 over all T tokens) or grouped (padded segments).
@@ -362,6 +390,56 @@ fp8bs_status fp8_block_gemm_dgrad(const uint8_t* dyq, const float* sdy, const ui
         return FP8BS_ERR_ALIGN;
     const int32_t off[2] = {0, static_cast<int32_t>(M)};
     return run_rowwise_gemm(true, 1, off, dyq, sdy, wq, sw, N, K, dx, stream);
+}
+
+size_t fp8bs_splitk_workspace_size(int op, int64_t M, int64_t N, int64_t K, int32_t splits)
+{
+    if ((op != FP8BS_OP_FPROP && op != FP8BS_OP_DGRAD) || M <= 0 || N <= 0 || K <= 0 || splits <= 1)
+        return 0;
+    const int64_t contr = op == FP8BS_OP_DGRAD ? N : K;
+    const int64_t width = op == FP8BS_OP_DGRAD ? K : N;
+    if (contr % 128 != 0) return 0;
+    int used = 1, kps = 1;
+    splitk_shape(contr / 128, splits, used, kps);
+    if (used <= 1) return 0;
+    return static_cast<size_t>(used) * static_cast<size_t>(M) * static_cast<size_t>(width) * sizeof(float);
+}
+
+int32_t fp8bs_splitk_default_splits(int op, int64_t M, int64_t N, int64_t K)
+{
+    if ((op != FP8BS_OP_FPROP && op != FP8BS_OP_DGRAD) || M <= 0 || N <= 0 || K <= 0) return 1;
+    DeviceState* st = nullptr;
+    if (device_state(&st) != FP8BS_OK) return 1;
+    const int64_t contr = op == FP8BS_OP_DGRAD ? N : K;
+    const int64_t width = op == FP8BS_OP_DGRAD ? K : N;
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((width + kBN - 1) / kBN);
+    const int64_t nkb = contr / kBK;
+    // enough tiles to occupy the SMs, or too little K to be worth splitting
+    if (tiles * 2 > st->num_sms || nkb < 16) return 1;
+    int64_t sp = st->num_sms / tiles;
+    if (sp > nkb / 4) sp = nkb / 4;   // at least four K-blocks per range
+    return sp < 1 ? 1 : static_cast<int32_t>(sp);
+}
+
+fp8bs_status fp8_block_gemm_splitk(int op, const uint8_t* a, const float* sa, const uint8_t* b,
+                                   const float* sb, int64_t M, int64_t N, int64_t K, int32_t splits,
+                                   void* out, void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (op != FP8BS_OP_FPROP && op != FP8BS_OP_DGRAD) return FP8BS_ERR_ARG;
+    if (M < 0 || N <= 0 || K <= 0 || splits < 1) return FP8BS_ERR_ARG;
+    if (K % 128 != 0 || N % 128 != 0 || M > 0x7FFFFF00) return FP8BS_ERR_SHAPE;
+    if (M == 0) return FP8BS_OK;
+    if (!a || !sa || !b || !sb || !out) return FP8BS_ERR_ARG;
+    if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(out))
+        return FP8BS_ERR_ALIGN;
+    const size_t need = fp8bs_splitk_workspace_size(op, M, N, K, splits);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return FP8BS_ERR_ARG;
+        if (!aligned16(workspace)) return FP8BS_ERR_ALIGN;
+    }
+    const int32_t off[2] = {0, static_cast<int32_t>(M)};
+    return run_rowwise_gemm(op == FP8BS_OP_DGRAD, 1, off, a, sa, b, sb, N, K, out, stream,
+                            need > 0 ? splits : 1, static_cast<float*>(workspace));
 }
 
 fp8bs_status fp8_block_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT,

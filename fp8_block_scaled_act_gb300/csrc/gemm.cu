@@ -95,6 +95,21 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, int t, int& g, 
     nt = local - mt * p.n_tiles;
 }
 
+// Work unit u -> tile (group, row tile, column tile) and the range of the
+// tile's K-blocks it covers: split-K divides every tile's K-blocks into
+// p.splits contiguous ranges of p.kb_per_split (the last may be shorter);
+// without split-K a unit is a whole tile.
+__device__ __forceinline__ void decode_unit(const GemmParams& p, int u, int& g, int& mt, int& nt, int& split,
+                                            int& kb0, int& nkb)
+{
+    const int t = u / p.splits;
+    split = u - t * p.splits;
+    decode_tile(p, t, g, mt, nt);
+    kb0 = split * p.kb_per_split;
+    const int end = min(p.kblocks[g], kb0 + p.kb_per_split);
+    nkb = max(0, end - kb0);
+}
+
 // ---------------------------------------------------------------------------
 // Promotion epilogues (warps 4-11). Each warp owns the 32 TMEM lanes (tile
 // rows) of its quarter and one 128-column half of the tile. Both return
@@ -114,17 +129,18 @@ __device__ __forceinline__ bool epilogue_block_scale(const GemmParams& p, Shared
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t acc_it = 0;
 
-    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-        int g, mt, nt;
-        decode_tile(p, t, g, mt, nt);
-        const int nkb = p.kblocks[g];
+    const int units = p.total_tiles * p.splits;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        int g, mt, nt, split, kb0, nkb;
+        decode_unit(p, u, g, mt, nt, split, kb0, nkb);
         const int row = p.a_row0[g] + mt * kBM + r_in_tile;   // A row = output row
         const bool row_ok = (mt * kBM + r_in_tile) < p.a_rows[g];
         const int col0 = nt * kBN + half * 128;
         const bool cols_ok = col0 < p.n_cols;                  // n_cols % 128 == 0
         const bool sa_ok = row < p.sa_rows;
-        const float* sa_ptr = p.sa + static_cast<int64_t>(p.sa_kb0[g]) * p.sa_ld + row;
-        const float* sb_ptr = p.sb + p.sb_off[g] + static_cast<int64_t>(col0 / 128) * p.sb_cstride;
+        const float* sa_ptr = p.sa + static_cast<int64_t>(p.sa_kb0[g] + kb0) * p.sa_ld + row;
+        const float* sb_ptr = p.sb + p.sb_off[g] + static_cast<int64_t>(col0 / 128) * p.sb_cstride +
+                              static_cast<int64_t>(kb0) * p.sb_kstride;
 
         auto load_sa = [&](int kb) -> float {
             return (sa_ok && kb < nkb) ? __ldg(sa_ptr + static_cast<int64_t>(kb) * p.sa_ld) : 0.0f;
@@ -182,7 +198,14 @@ __device__ __forceinline__ bool epilogue_block_scale(const GemmParams& p, Shared
             promote(3, rb);
         }
 
-        if (row_ok && cols_ok) {
+        if (row_ok && cols_ok && p.ws != nullptr) {
+            // split-K: this range's fp32 sum goes to its own slice of the workspace
+            float* w = p.ws + static_cast<int64_t>(split) * p.ws_split_stride + static_cast<int64_t>(row) * p.out_ld + col0;
+#pragma unroll
+            for (int v = 0; v < 32; ++v)
+                reinterpret_cast<float4*>(w)[v] =
+                    make_float4(acc[2 * v].x, acc[2 * v].y, acc[2 * v + 1].x, acc[2 * v + 1].y);
+        } else if (row_ok && cols_ok) {
             uint16_t* y = static_cast<uint16_t*>(p.out) + p.out_off[g] + static_cast<int64_t>(row) * p.out_ld + col0;
 #pragma unroll
             for (int v = 0; v < 16; ++v) {
@@ -223,10 +246,10 @@ __device__ __forceinline__ bool epilogue_vector_scale(const GemmParams& p, Share
     float* vring = reinterpret_cast<float*>(vec_smem) + ew * (kVecSlots * kSlotFloats);
     uint32_t acc_it = 0;
 
-    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-        int g, mt, nt;
-        decode_tile(p, t, g, mt, nt);
-        const int nkb = p.kblocks[g];
+    const int units = p.total_tiles * p.splits;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        int g, mt, nt, split, kb0, nkb;
+        decode_unit(p, u, g, mt, nt, split, kb0, nkb);
         const int qrow0 = mt * kBM + quarter * 32;             // first tile row of this quarter
         const int col0 = nt * kBN + half * 128;
         const bool cols_ok = col0 < p.n_cols;                  // n_cols % 128 == 0
@@ -234,8 +257,9 @@ __device__ __forceinline__ bool epilogue_vector_scale(const GemmParams& p, Share
         // the B scales of columns col0 + 4l .. 4l + 3
         const int srow = p.a_row0[g] + qrow0 + lane;
         const bool sa_ok = srow < p.sa_rows;
-        const float* sa_ptr = p.sa + static_cast<int64_t>(p.sa_kb0[g]) * p.sa_ld + srow;
-        const float* sb_ptr = p.sb + p.sb_off[g] + static_cast<int64_t>(col0 + 4 * lane);
+        const float* sa_ptr = p.sa + static_cast<int64_t>(p.sa_kb0[g] + kb0) * p.sa_ld + srow;
+        const float* sb_ptr = p.sb + p.sb_off[g] + static_cast<int64_t>(col0 + 4 * lane) +
+                              static_cast<int64_t>(kb0) * p.sb_kstride;
         auto prefetch = [&](int kb) {
             if (kb < nkb) {
                 float* slot = vring + (kb % kVecSlots) * kSlotFloats;
@@ -384,10 +408,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
-                int g, mt, nt;
-                decode_tile(p, t, g, mt, nt);
-                const int nkb = p.kblocks[g];
+            const int units = p.total_tiles * p.splits;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                int g, mt, nt, split, kb0, nkb;
+                decode_unit(p, u, g, mt, nt, split, kb0, nkb);
                 const int ya = p.a_row0[g] + mt * kBM;
                 const int yb = p.b_row0[g] + nt * kBN;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
@@ -398,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&ctl->full[s], kStageBytes);
-                    const int x = p.k0[g] + kb * kBK;
+                    const int x = p.k0[g] + (kb0 + kb) * kBK;
                     tma_load_2d(sA + s * kABytes, &map_a, &ctl->full[s], x, ya);
                     tma_load_2d(sB + s * kBBytes, &map_b, &ctl->full[s], x, yb);
                 }
@@ -421,10 +445,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kBN);
             uint32_t it = 0, acc_it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
-                int g, mt, nt;
-                decode_tile(p, t, g, mt, nt);
-                const int nkb = p.kblocks[g];
+            const int units = p.total_tiles * p.splits;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                int g, mt, nt, split, kb0, nkb;
+                decode_unit(p, u, g, mt, nt, split, kb0, nkb);
                 for (int kb = 0; kb < nkb; ++kb, ++it, ++acc_it) {
                     const uint32_t s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1u;
@@ -479,6 +503,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Split-K reduction: out = BF16(sum over splits s = 0, 1, ... of ws[s]), in
+// that order (the result does not depend on scheduling). Eight elements per
+// thread: two 16-byte loads per split, one 16-byte store.
+__global__ void __launch_bounds__(256) splitk_reduce_bf16_kernel(const float* __restrict__ ws, int splits,
+                                                                 int64_t split_stride, int64_t count,
+                                                                 uint16_t* __restrict__ out)
+{
+    const int64_t n8 = count / 8;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        float4 a = __ldcs(reinterpret_cast<const float4*>(ws) + 2 * i);
+        float4 b = __ldcs(reinterpret_cast<const float4*>(ws) + 2 * i + 1);
+        for (int s = 1; s < splits; ++s) {
+            const float4* w = reinterpret_cast<const float4*>(ws + s * split_stride) + 2 * i;
+            const float4 c = __ldcs(w), d = __ldcs(w + 1);
+            a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
+            b.x += d.x; b.y += d.y; b.z += d.z; b.w += d.w;
+        }
+        uint4 o;
+        o.x = pack_bf16x2(a.x, a.y);
+        o.y = pack_bf16x2(a.z, a.w);
+        o.z = pack_bf16x2(b.x, b.y);
+        o.w = pack_bf16x2(b.z, b.w);
+        reinterpret_cast<uint4*>(out)[i] = o;
+    }
+}
+
 __global__ void selftest_wait_kernel(unsigned int* status, uint64_t limit_ns)
 {
     __shared__ uint64_t bar;
@@ -504,12 +555,26 @@ cudaError_t launch_kind(const CUtensorMap& map_a, const CUtensorMap& map_b, cons
     if (static_cast<uint32_t>(attr.numRegs) != kLaunchRegs) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int grid = p.total_tiles < num_sms ? p.total_tiles : num_sms;
+    const int units = p.total_tiles * p.splits;
+    const int grid = units < num_sms ? units : num_sms;
     kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_a, map_b, p);
     return cudaGetLastError();
 }
 
 }  // namespace
+
+cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t split_stride, int64_t count,
+                                 uint16_t* out, int num_sms, cudaStream_t stream)
+{
+    if (count <= 0) return cudaSuccess;
+    const int64_t n8 = count / 8;
+    int64_t blocks = (n8 + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    splitk_reduce_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ws, splits, split_stride, count,
+                                                                                  out);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_gemm(GemmKind kind, const CUtensorMap& map_a, const CUtensorMap& map_b,
                         const GemmParams& p, int num_sms, cudaStream_t stream)

@@ -69,6 +69,10 @@ struct GemmParams {
     void* out;
     int64_t out_ld;
     int accumulate;
+    int splits;                   // split-K ranges per tile (1: none)
+    int kb_per_split;             // K-blocks per range
+    float* ws;                    // split-K: fp32 range sums [splits][rows x out_ld], else null
+    int64_t ws_split_stride;      // floats between consecutive ranges' slices
     uint64_t wait_limit_ns;
     unsigned int* status;
 };
@@ -85,6 +89,10 @@ cudaError_t launch_gemm(GemmKind kind, const CUtensorMap& map_a, const CUtensorM
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 128;
+
+// out[i] = BF16(sum_s ws[s * split_stride + i]) for i < count (count % 8 == 0).
+cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t split_stride, int64_t count,
+                                 uint16_t* out, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_selftest_wait(unsigned int* status, uint64_t limit_ns, cudaStream_t stream);
 

@@ -44,6 +44,7 @@
 #ifndef FP8BS_H
 #define FP8BS_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #if defined(__GNUC__)
@@ -208,6 +209,42 @@ FP8BS_API fp8bs_status fp8_block_gemm_wgrad(const uint8_t* dyqT, const float* sd
                                   const uint8_t* xqT, const float* sxT,
                                   int64_t T, int64_t N, int64_t K, float* dw,
                                   int accumulate, void* stream);
+
+/* Split-K Fprop / Dgrad, for outputs too small to occupy the GPU (few      */
+/* output tiles, long contraction; e.g. 256 x 256 outputs with K = 65536).   */
+/* The contraction's 128-blocks are cut into `splits` contiguous ranges (at  */
+/* most one range per block). Each range is computed exactly like the unsplit */
+/* GEMM ([P2] section 5: per-block partials scaled by s_a * s_b, added in     */
+/* fp32); the ranges' fp32 sums are then added in range order and rounded to */
+/* BF16 once. The pages' promotion recipe fixes the per-block scaling, not    */
+/* the fp32 addition order, so the result differs from the unsplit call only  */
+/* by fp32 rounding and stays within the tolerance above. Deterministic.      */
+/*                                                                           */
+/* op        : FP8BS_OP_FPROP or FP8BS_OP_DGRAD; a, sa, b, sb, M, N, K, out  */
+/*             as for fp8_block_gemm_fprop (a = xq, b = wqT) or               */
+/*             fp8_block_gemm_dgrad (a = dyq, b = wq).                        */
+/* splits    : >= 1; values above the number of 128-blocks are clamped.      */
+/* workspace : caller-owned device buffer of at least                        */
+/*             fp8bs_splitk_workspace_size(op, M, N, K, splits) bytes,        */
+/*             16-byte aligned (may be NULL when that size is 0). Contents on */
+/*             entry are ignored and undefined afterwards; it must not be     */
+/*             used by anything else until the call has completed on stream.  */
+/* Errors: FP8BS_ERR_ARG (bad op, splits < 1, NULL or too small workspace),   */
+/* FP8BS_ERR_SHAPE / FP8BS_ERR_ALIGN as for the unsplit calls.                */
+FP8BS_API size_t fp8bs_splitk_workspace_size(int op, int64_t M, int64_t N, int64_t K, int32_t splits);
+
+/* A split count for this device: about one range per idle SM when the       */
+/* output has fewer tiles than half the SMs and the contraction has at least  */
+/* 16 128-blocks, keeping at least four 128-blocks per range; 1 (no split)    */
+/* otherwise (below that the extra reduction pass costs more than it saves). */
+/* Uses the current device.                                                   */
+FP8BS_API int32_t fp8bs_splitk_default_splits(int op, int64_t M, int64_t N, int64_t K);
+
+FP8BS_API fp8bs_status fp8_block_gemm_splitk(int op, const uint8_t* a, const float* sa,
+                                   const uint8_t* b, const float* sb,
+                                   int64_t M, int64_t N, int64_t K, int32_t splits,
+                                   void* out, void* workspace, size_t workspace_bytes,
+                                   void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* S7. Grouped (MoE expert) GEMMs                                             */

@@ -114,3 +114,22 @@ def test_product_path_does_not_import_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "fp8bs_oracle" not in text, f
+
+
+def test_splitk_workspace_arithmetic_and_argument_errors():
+    """Workspace size = ranges actually used x M x output width x 4 bytes, with
+    ranges = ceil(nblocks / ceil(nblocks / splits)); bad arguments are
+    rejected before any device work."""
+    L = fp8bs.lib()
+    ws = fp8bs.fp8bs_splitk_workspace_size
+    assert ws(fp8bs.OP_FPROP, 256, 256, 65536, 76) == 74 * 256 * 256 * 4    # 512 blocks: 7 per range
+    assert ws(fp8bs.OP_FPROP, 256, 256, 1024, 1) == 0
+    assert ws(fp8bs.OP_FPROP, 256, 256, 1024, 100) == 8 * 256 * 256 * 4     # clamped to 8 blocks
+    assert ws(fp8bs.OP_DGRAD, 256, 256, 1024, 4) == 2 * 256 * 1024 * 4      # contraction N = 256
+    assert ws(fp8bs.OP_WGRAD, 256, 256, 1024, 4) == 0
+    assert ws(fp8bs.OP_FPROP, 0, 256, 1024, 4) == 0
+    assert ws(fp8bs.OP_FPROP, 100, 256, 1000, 4) == 0                        # K % 128 != 0
+    null = ctypes.c_void_p(0)
+    assert L.fp8_block_gemm_splitk(7, null, null, null, null, 128, 128, 128, 2, null, null, 0, null) == 1
+    assert L.fp8_block_gemm_splitk(0, null, null, null, null, 128, 128, 128, 0, null, null, 0, null) == 1
+    assert L.fp8_block_gemm_splitk(0, null, null, null, null, 128, 100, 128, 2, null, null, 0, null) == 3
