@@ -26,7 +26,8 @@ __all__ = [
     "fp8_quant_1x128", "fp8_quant_128x128", "fp8_requant_128x1_T",
     "fp8_block_gemm_fprop", "fp8_block_gemm_dgrad", "fp8_block_gemm_wgrad",
     "fp8_block_gemm_grouped", "fp8_block_gemm_splitk", "fp8bs_splitk_workspace_size",
-    "fp8bs_splitk_default_splits", "fp8bs_device_status", "fp8bs_set_wait_limit_ns",
+    "fp8bs_splitk_default_splits", "fp8_block_gemm_splitk_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "fp8bs_device_status", "fp8bs_set_wait_limit_ns",
     "fp8bs_selftest_wait_timeout", "fp8bs_scale_ld", "fp8bs_padded_tokens",
     "fp8bs_status_str", "fp8bs_version",
     "empty_quant_1x128", "empty_quant_128x128", "empty_requant_128x1_T",
@@ -36,6 +37,7 @@ __all__ = [
 SRC_BF16, SRC_E4M3 = 0, 1
 OP_FPROP, OP_DGRAD, OP_WGRAD = 0, 1, 2
 MAX_GROUPS = 256
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024   # FP8BS_NOALLOC_SCRATCH_BYTES
 STATUS_NAMES = {0: "OK", 1: "ERR_ARG", 2: "ERR_ALIGN", 3: "ERR_SHAPE", 4: "ERR_LAUNCH",
                 5: "ERR_TIMEOUT", 6: "ERR_UNSUPPORTED", 7: "ERR_DEVICE"}
 
@@ -84,6 +86,7 @@ def lib() -> ctypes.CDLL:
         "fp8bs_splitk_workspace_size": ([I, I64, I64, I64, I32], ctypes.c_size_t),
         "fp8bs_splitk_default_splits": ([I, I64, I64, I64], I32),
         "fp8_block_gemm_splitk": ([I, P, P, P, P, I64, I64, I64, I32, P, P, ctypes.c_size_t, P], S),
+        "fp8_block_gemm_splitk_noalloc": ([I, P, P, P, P, I64, I64, I64, I32, P, P], S),
         "fp8bs_device_status": ([I], S),
         "fp8bs_set_wait_limit_ns": ([ctypes.c_uint64], None),
         "fp8bs_selftest_wait_timeout": ([ctypes.c_uint64, P], S),
@@ -344,6 +347,30 @@ def fp8_block_gemm_splitk(op: int, a, sa, b, sb, out, splits: Optional[int] = No
     _check("fp8_block_gemm_splitk", lib().fp8_block_gemm_splitk(
         int(op), _ptr(a), _ptr(sa), _ptr(b), _ptr(sb), M, N, K, int(splits), _ptr(out),
         _ptr(workspace), wbytes, _stream(stream)))
+
+
+def fp8_block_gemm_splitk_noalloc(op: int, a, sa, b, sb, out, splits: Optional[int] = None,
+                                  stream=None) -> None:
+    """fp8_block_gemm_splitk with the library's fixed scratch array instead of
+    a workspace (for callers that cannot allocate; see fp8bs.h for the size
+    limit and the rule that overlapping calls must be serialized)."""
+    for t, n, d in ((a, "a", torch.uint8), (sa, "sa", torch.float32), (b, "b", torch.uint8),
+                    (sb, "sb", torch.float32), (out, "out", torch.bfloat16)):
+        _need(t, d, n)
+    M, N, K, out_shape = _splitk_dims(op, a, b)
+    if tuple(out.shape) != out_shape:
+        raise ValueError("shape mismatch")
+    if splits is None:
+        splits = fp8bs_splitk_default_splits(op, M, N, K)
+    need = fp8bs_splitk_workspace_size(op, M, N, K, splits)
+    if need > NOALLOC_SCRATCH_BYTES:
+        raise ValueError(f"fp8_block_gemm_splitk_noalloc: {splits} ranges of {M} x "
+                         f"{out_shape[1]} fp32 need {need} bytes, more than the fixed "
+                         f"{NOALLOC_SCRATCH_BYTES}-byte scratch; use fewer splits or "
+                         "fp8_block_gemm_splitk with a workspace")
+    _check("fp8_block_gemm_splitk_noalloc", lib().fp8_block_gemm_splitk_noalloc(
+        int(op), _ptr(a), _ptr(sa), _ptr(b), _ptr(sb), M, N, K, int(splits), _ptr(out),
+        _stream(stream)))
 
 
 def fp8bs_device_status(reset: bool = True) -> int:

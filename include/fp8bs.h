@@ -246,6 +246,31 @@ FP8BS_API fp8bs_status fp8_block_gemm_splitk(int op, const uint8_t* a, const flo
                                    void* out, void* workspace, size_t workspace_bytes,
                                    void* stream);
 
+/* Split-K without a caller workspace. No counterpart in the pages          */
+/* ([P1]-[P4]): it exists for callers that cannot allocate device memory     */
+/* (an allocator-free runtime, a loop that must not call cudaMalloc because  */
+/* it can synchronize the device, a plugin without a memory pool). Same       */
+/* arguments and result as fp8_block_gemm_splitk; the range sums go to a     */
+/* fixed array of FP8BS_NOALLOC_SCRATCH_BYTES compiled into the library, and */
+/* the call allocates nothing.                                                */
+/* - Requests needing more than FP8BS_NOALLOC_SCRATCH_BYTES                   */
+/*   (fp8bs_splitk_workspace_size(op, M, N, K, splits)) return               */
+/*   FP8BS_ERR_SHAPE before any work; lower `splits` or use                  */
+/*   fp8_block_gemm_splitk with a workspace.                                  */
+/* - The first call on each device (with that device current) does a one-    */
+/*   time set-up (it looks up the array's device address); make that first   */
+/*   call before any stream capture begins.                                   */
+/* - One array serves all calls on a device: calls whose executions overlap   */
+/*   (different streams without ordering, several host threads) race on it    */
+/*   and give undefined results. Serialize them (one stream, or events).      */
+/* - Nothing in the array needs to start at zero.                             */
+#define FP8BS_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+FP8BS_API fp8bs_status fp8_block_gemm_splitk_noalloc(int op, const uint8_t* a, const float* sa,
+                                           const uint8_t* b, const float* sb,
+                                           int64_t M, int64_t N, int64_t K, int32_t splits,
+                                           void* out, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* S7. Grouped (MoE expert) GEMMs                                             */
 /* The dense definitions above applied to each group (expert) g, whose token  */
