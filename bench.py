@@ -6,7 +6,9 @@ copy), the 1x128 quantization of X, Fprop, the 1x128 quantization of dY,
 Dgrad, the 128x1 transposed requants of X (from its E4M3 stash) and dY (from
 BF16), and Wgrad. Default workload: X 4096x7168 (N(0,1) with 0.1% outliers),
 W 7168x2048 (N(0,0.02^2)), dY 4096x2048 (N(0,1e-3^2)). ``--workload moe``
-runs the grouped MoE expert pass instead (32 experts, 8192 routed rows).
+runs the grouped MoE expert pass instead (32 experts, 8192 routed rows);
+``--workload longk`` the 256 x K x 256 split-K Fprop of the long-contraction
+workload (K = 1024 ... 65536).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -333,6 +335,67 @@ class MoeStep:
                 "experts": self.G, "tokens": self.T, "hidden": self.H, "inter": self.I, "up": self.U}
 
 
+class LongKStep:
+    """The long-contraction drift workload: X 256xK and W Kx256, U(0.5, 1.5),
+    for K in 1024, 4096, 16384, 65536; per K the 1x128 and 128x128
+    quantizations and a split-K Fprop with the library's default split (two
+    128x256 output tiles would otherwise occupy two SMs)."""
+
+    KS = (1024, 4096, 16384, 65536)
+
+    def __init__(self, fp8bs, torch, device, M=256, N=256, seed=0):
+        self.fp8bs, self.torch, self.dev = fp8bs, torch, device
+        self.M, self.N = M, N
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        e = fp8bs
+        self.cases = []
+        for K in self.KS:
+            X = (torch.rand(M, K, device=device, generator=g) + 0.5).to(torch.bfloat16)
+            W = (torch.rand(K, N, device=device, generator=g) + 0.5).to(torch.bfloat16)
+            xq, sx = e.empty_quant_1x128(M, K, device)
+            wq, wqT, sw = e.empty_quant_128x128(K, N, device=device)
+            sp = e.fp8bs_splitk_default_splits(e.OP_FPROP, M, N, K)
+            ws = torch.empty(max(16, e.fp8bs_splitk_workspace_size(e.OP_FPROP, M, N, K, sp)),
+                             dtype=torch.uint8, device=device)
+            Y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+            self.cases.append(dict(K=K, X=X, W=W, xq=xq, sx=sx, wq=wq, wqT=wqT, sw=sw, sp=sp, ws=ws, Y=Y))
+        self.names = []
+        for c in self.cases:
+            self.names += [f"quant_1x128(X,K={c['K']})", f"quant_128x128(W,K={c['K']})",
+                           f"splitk_fprop(K={c['K']},splits={c['sp']})"]
+
+    def work(self):
+        M, N = self.M, self.N
+        s_ld = (M + 3) // 4 * 4
+        flops, b = {}, {}
+        for c in self.cases:
+            K = c["K"]
+            b[f"quant_1x128(X,K={K})"] = M * K * 3 + 4 * (K // 128) * s_ld
+            b[f"quant_128x128(W,K={K})"] = K * N * 4 + 4 * (K // 128) * (N // 128)
+            flops[f"splitk_fprop(K={K},splits={c['sp']})"] = 2.0 * M * N * K
+        return flops, b
+
+    def launches(self):
+        e = self.fp8bs
+        out = []
+        for c in self.cases:
+            out += [lambda c=c: e.fp8_quant_1x128(c["X"], c["xq"], c["sx"]),
+                    lambda c=c: e.fp8_quant_128x128(c["W"], c["wq"], c["wqT"], c["sw"]),
+                    lambda c=c: e.fp8_block_gemm_splitk(e.OP_FPROP, c["xq"], c["sx"], c["wqT"], c["sw"],
+                                                        c["Y"], splits=c["sp"], workspace=c["ws"])]
+        return out
+
+    def io(self):
+        return (tuple(t for c in self.cases for t in (c["X"], c["W"])),
+                tuple(c["Y"] for c in self.cases))
+
+    def describe(self):
+        return {"workload": (f"long-K drift workload: X {self.M}xK, W Kx{self.N}, U(0.5,1.5), "
+                             f"K in {list(self.KS)}, split-K Fprop"),
+                "M": self.M, "N": self.N, "K": list(self.KS)}
+
+
 def run_ours(args, world, rank, local):
     import torch
     import fp8_block_scaled_act_gb300 as fp8bs
@@ -345,6 +408,8 @@ def run_ours(args, world, rank, local):
     M, K, N = dense_shapes().values()
     if args.workload == "moe":
         step = MoeStep(fp8bs, torch, device, seed=rank)
+    elif args.workload == "longk":
+        step = LongKStep(fp8bs, torch, device, seed=rank)
     else:
         step = DenseStep(fp8bs, torch, device, M, K, N, seed=rank)
     launches = step.launches()
@@ -424,8 +489,9 @@ def run_ours(args, world, rank, local):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total_s * 1e3 / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
-        "data": "synthetic (seeded normal; 0.1% outliers in X)" if args.workload == "dense"
-                else "synthetic (seeded normal; Dirichlet(0.5) expert counts)",
+        "data": {"dense": "synthetic (seeded normal; 0.1% outliers in X)",
+                 "moe": "synthetic (seeded normal; Dirichlet(0.5) expert counts)",
+                 "longk": "synthetic (seeded uniform U(0.5, 1.5))"}[args.workload],
         "config": dict(step.describe(),
                        parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
                        l2="flushed between steps (256 MiB write outside the step events)"),
@@ -643,8 +709,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["dense", "moe"], default="dense",
-                    help="dense: the linear layer's fwd+bwd (default); moe: grouped expert pass")
+    ap.add_argument("--workload", choices=["dense", "moe", "longk"], default="dense",
+                    help="dense: the linear layer's fwd+bwd (default); moe: grouped expert pass; "
+                         "longk: 256xKx256 split-K Fprop for K up to 65536")
     ap.add_argument("--cpu-sample", type=float, default=1.0 / 32,
                     help="fraction of token rows the oracle runs per step")
     ap.add_argument("--ncu-case", choices=NCU_CASES, default=None,
