@@ -40,56 +40,46 @@ __device__ __forceinline__ float scale_from_amax(float amax)
 }
 
 // E4M3 codes of fp32(v / s) for a pair of values, by exact IEEE division.
-// Out of line: the fast path below falls back to it only for quotients that
-// sit within a few fp32 ulps of an E4M3 rounding boundary (rare), and
-// keeping it out of line stops the compiler from predicating it into every
-// element.
+// Used only for tiles whose scale lies outside the fast path's range (below
+// 2^-60 or above 2^100); kept out of line so that it does not weigh on the
+// fast path's code.
 __device__ __noinline__ uint32_t encode2_exact(float v0, float v1, float s)
 {
     return cvt_e4m3x2(__fdiv_rn(v0, s), __fdiv_rn(v1, s));
 }
 
-// Quotients fp32(v / s) of a pair of values without a division, with a
-// certificate that they are the correctly rounded ones, encoded to E4M3.
+// Quotients fp32(v / s) of a pair of values without a division, encoded to
+// E4M3; the result is the correctly rounded quotient RN(v / s) for every
+// input, so the codes equal those of an IEEE division.
 //
-// q0 = RN(v * r) with r = RN(1/s) is within ~1.5 ulp of v/s. One correction
-// step (Markstein's method, IBM J. Res. Dev. 34(1), 1990) with the exact FMA
-// residual e0 = v - q0 s gives q1 = RN(q0 + e0 r), whose error is a few
-// 2^-24 ulp: q1 = RN(v/s) except when v/s lies within that distance of a
-// rounding boundary between two fp32 values. The certificate makes this
-// exact: with e1 = v - q1 s computed exactly by an FMA, |e1| < ulp(q1) s / 2
-// means |v/s - q1| < ulp(q1) / 2, so q1 = RN(v/s). (For s not a power of
-// two, v/s is never exactly halfway between two floats; for a power of two,
-// e1 = 0. When q1 is a power of two the ulp below it is half as large, but a
-// value that close to a power of two has the same E4M3 code, which is all
-// that is used here.) Below 2^-102 the ulp bound is clamped to 2^-126: such
-// quotients encode to a signed zero whatever their rounding. The caller keeps
-// s in [2^-60, 2^100] so that every quantity stays normal; `bad` becomes
-// non-zero when a certificate fails and the caller redoes the group with
-// exact division.
+// With r = RN(1/s) (within half an ulp of 1/s):
+//   q0 = RN(v r)                    within 1.5 ulp of v/s;
+//   q1 = RN(q0 + (v - q0 s) r)      the residual v - q0 s is exact in one FMA,
+//                                   and q1 is within 1/2 ulp + 2^-23 ulp of
+//                                   v/s, hence a faithful approximation;
+//   q2 = RN(q1 + (v - q1 s) r)      = RN(v/s) by Markstein's theorem (a
+//                                   faithful quotient corrected once with an
+//                                   exact FMA residual and a reciprocal within
+//                                   half an ulp is correctly rounded; IBM J.
+//                                   Res. Dev. 34(1), 1990).
+// The theorem assumes no underflow; quotients small enough to underflow are
+// far below 2^-10 and encode to a signed zero whatever their rounding. The
+// caller keeps s in [2^-60, 2^100] (other tiles take exact division) so the
+// reciprocal and the residuals stay normal.
 //
-// The steps take the negated inputs nv = -v and nr = -r and form the
-// negated residuals (q s - v): then a zero input keeps its sign through the
-// chain (v = -0 gives q1 = -0 + -0), where the textbook order would turn it
-// into +0. The E4M3 conversion keeps the sign of a zero result, so -0 inputs
-// and tiny negatives both encode to 0x80. Pairs use the packed fp32x2
-// instructions.
-__device__ __forceinline__ int half_ulp_bits(float q)
-{
-    return __viaddmax_s32(static_cast<int>(__float_as_uint(q) & 0x7F800000u), -(24 << 23), 0x00800000);
-}
-
-__device__ __forceinline__ uint32_t encode2_fast(float2 nv, float s, float nr, uint32_t& bad)
+// The steps take the negated inputs nv = -v and nr = -r and form the negated
+// residuals (q s - v): a zero input then keeps its sign through the chain
+// (v = -0 gives q = -0 + -0), where the textbook order would turn it into
+// +0. The E4M3 conversion keeps the sign of a zero result, so -0 inputs and
+// tiny negatives encode to 0x80. Pairs use the packed fp32x2 instructions.
+__device__ __forceinline__ uint32_t encode2_fast(float2 nv, float s, float nr)
 {
     const float2 s2 = make_float2(s, s);
     const float2 nr2 = make_float2(nr, nr);
     const float2 q0 = __fmul2_rn(nv, nr2);
     const float2 q1 = __ffma2_rn(__ffma2_rn(q0, s2, nv), nr2, q0);
-    const float2 ne1 = __ffma2_rn(q1, s2, nv);
-    const float2 bound = __fmul2_rn(s2, make_float2(__int_as_float(half_ulp_bits(q1.x)),
-                                                    __int_as_float(half_ulp_bits(q1.y))));
-    bad |= (fabsf(ne1.x) < bound.x && fabsf(ne1.y) < bound.y) ? 0u : 1u;
-    return cvt_e4m3x2(q1.x, q1.y);
+    const float2 q2 = __ffma2_rn(__ffma2_rn(q1, s2, nv), nr2, q1);
+    return cvt_e4m3x2(q2.x, q2.y);
 }
 
 // Negated bf16 halves of a word as fp32: -lo is (w << 16) with its top bit
@@ -140,18 +130,16 @@ __device__ __noinline__ uint2 quant8_exact(uint4 d, float s)
 }
 
 // Eight bf16 values (one 16-byte load) divided by s and encoded, low
-// element first. One branch per eight values: the rare group with an
-// uncertified quotient is redone with exact division.
+// element first. Tiles whose scale is outside the fast path's range (nr = 0)
+// use exact division.
 __device__ __forceinline__ uint2 quant8(const uint4& d, const TileScale& t)
 {
-    uint32_t bad = t.nr == 0.0f ? 1u : 0u;
-    const uint32_t c0 = encode2_fast(neg_bf16x2(d.x), t.s, t.nr, bad);
-    const uint32_t c1 = encode2_fast(neg_bf16x2(d.y), t.s, t.nr, bad);
-    const uint32_t c2 = encode2_fast(neg_bf16x2(d.z), t.s, t.nr, bad);
-    const uint32_t c3 = encode2_fast(neg_bf16x2(d.w), t.s, t.nr, bad);
-    uint2 o = make_uint2(__byte_perm(c0, c1, 0x5410), __byte_perm(c2, c3, 0x5410));
-    if (bad != 0u) o = quant8_exact(d, t.s);
-    return o;
+    if (t.nr == 0.0f) return quant8_exact(d, t.s);
+    const uint32_t c0 = encode2_fast(neg_bf16x2(d.x), t.s, t.nr);
+    const uint32_t c1 = encode2_fast(neg_bf16x2(d.y), t.s, t.nr);
+    const uint32_t c2 = encode2_fast(neg_bf16x2(d.z), t.s, t.nr);
+    const uint32_t c3 = encode2_fast(neg_bf16x2(d.w), t.s, t.nr);
+    return make_uint2(__byte_perm(c0, c1, 0x5410), __byte_perm(c2, c3, 0x5410));
 }
 
 // ---------------------------------------------------------------------------
@@ -331,7 +319,8 @@ constexpr int kQ3Threads = 256;
 
 // Mode B, phase 3 for one channel pair (j, j + 1) and 32 tokens of the staged
 // BF16 block [128 tokens x 128 channels]: each 32-bit shared load holds both
-// channels of one token. Returns false if any quotient needs the exact path.
+// channels of one token. Returns false when a channel's scale is outside the
+// fast path's range; the caller then redoes the pair with exact division.
 __device__ __forceinline__ bool requant_pair_bf16(const uint8_t* stage, int part, int j,
                                                   const TileScale& t0, const TileScale& t1,
                                                   uint32_t (&w0)[8], uint32_t (&w1)[8])
@@ -343,10 +332,10 @@ __device__ __forceinline__ bool requant_pair_bf16(const uint8_t* stage, int part
 #pragma unroll
         for (int e = 0; e < 4; ++e)
             x[e] = *reinterpret_cast<const uint32_t*>(stage + ((part * 32 + 4 * k + e) * 128 + j) * 2);
-        const uint32_t a01 = encode2_fast(make_float2(neg_bf16_lo(x[0]), neg_bf16_lo(x[1])), t0.s, t0.nr, bad);
-        const uint32_t a23 = encode2_fast(make_float2(neg_bf16_lo(x[2]), neg_bf16_lo(x[3])), t0.s, t0.nr, bad);
-        const uint32_t b01 = encode2_fast(make_float2(neg_bf16_hi(x[0]), neg_bf16_hi(x[1])), t1.s, t1.nr, bad);
-        const uint32_t b23 = encode2_fast(make_float2(neg_bf16_hi(x[2]), neg_bf16_hi(x[3])), t1.s, t1.nr, bad);
+        const uint32_t a01 = encode2_fast(make_float2(neg_bf16_lo(x[0]), neg_bf16_lo(x[1])), t0.s, t0.nr);
+        const uint32_t a23 = encode2_fast(make_float2(neg_bf16_lo(x[2]), neg_bf16_lo(x[3])), t0.s, t0.nr);
+        const uint32_t b01 = encode2_fast(make_float2(neg_bf16_hi(x[0]), neg_bf16_hi(x[1])), t1.s, t1.nr);
+        const uint32_t b23 = encode2_fast(make_float2(neg_bf16_hi(x[2]), neg_bf16_hi(x[3])), t1.s, t1.nr);
         w0[k] = __byte_perm(a01, a23, 0x5410);
         w1[k] = __byte_perm(b01, b23, 0x5410);
     }
@@ -385,6 +374,7 @@ __device__ __forceinline__ void decode4_scaled(uint32_t x, float s1, float (&v)[
 
 // Mode Q, phase 3 for one channel quad (j .. j + 3) and 16 tokens of the
 // staged E4M3 block: each 32-bit shared load holds the quad of one token.
+// Returns false when a channel's scale is outside the fast path's range.
 __device__ __forceinline__ bool requant_quad_e4m3(const uint8_t* stage, const float* row_scale,
                                                   int part, int j, const TileScale (&ts)[4],
                                                   uint32_t (&w)[4][4])
@@ -402,8 +392,8 @@ __device__ __forceinline__ bool requant_quad_e4m3(const uint8_t* stage, const fl
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            const uint32_t c01 = encode2_fast(make_float2(nv[0][c], nv[1][c]), ts[c].s, ts[c].nr, bad);
-            const uint32_t c23 = encode2_fast(make_float2(nv[2][c], nv[3][c]), ts[c].s, ts[c].nr, bad);
+            const uint32_t c01 = encode2_fast(make_float2(nv[0][c], nv[1][c]), ts[c].s, ts[c].nr);
+            const uint32_t c23 = encode2_fast(make_float2(nv[2][c], nv[3][c]), ts[c].s, ts[c].nr);
             w[c][k] = __byte_perm(c01, c23, 0x5410);
         }
     }
