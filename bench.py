@@ -2,9 +2,9 @@
 
 One step is one pass of the layer's whole data path over one batch of
 synthetic input: the weight's 128x128 quantization (with its transposed
-copy), the 1x128 quantization of X, Fprop, the 1x128 quantization of dY,
-Dgrad, the 128x1 transposed requants of X (from its E4M3 stash) and dY (from
-BF16), and Wgrad. Default workload: X 4096x7168 (N(0,1) with 0.1% outliers),
+copy), the 1x128 quantization of X, Fprop, the dual-orientation cast of dY
+(its 1x128 and 128x1 transposed quantizations from one read), Dgrad, the
+128x1 transposed requant of X from its E4M3 stash, and Wgrad. Default workload: X 4096x7168 (N(0,1) with 0.1% outliers),
 W 7168x2048 (N(0,0.02^2)), dY 4096x2048 (N(0,1e-3^2)). ``--workload moe``
 runs the grouped MoE expert pass instead (32 experts, 8192 routed rows);
 ``--workload longk`` the 256 x K x 256 split-K Fprop of the long-contraction
@@ -57,10 +57,9 @@ def step_work(M, K, N):
         "quant_128x128(W)": K * N * 2 + 2 * K * N + 4 * (K // 128) * (N // 128),
         "quant_1x128(X)": M * K * 2 + M * K + 4 * (K // 128) * s_ld,
         "fprop": M * K + N * K + 4 * (K // 128) * (s_ld + N // 128) + 2 * M * N,
-        "quant_1x128(dY)": M * N * 2 + M * N + 4 * (N // 128) * s_ld,
+        "quant_dual(dY)": M * N * 2 + M * N + 4 * (N // 128) * s_ld + M * N + 4 * (M // 128) * N,
         "dgrad": M * N + K * N + 4 * (N // 128) * s_ld + 4 * (K // 128) * (N // 128) + 2 * M * K,
         "requant_128x1_T(Xq)": M * K + 4 * (K // 128) * s_ld + M * K + 4 * (M // 128) * K,
-        "requant_128x1_T(dY)": M * N * 2 + M * N + 4 * (M // 128) * N,
         "wgrad": N * M + K * M + 4 * (M // 128) * (N + K) + 4 * N * K,
     }
     flops = {"fprop": gemm_flops, "dgrad": gemm_flops, "wgrad": gemm_flops}
@@ -218,8 +217,8 @@ class DenseStep:
         self.xT, self.sxT = e.empty_requant_128x1_T(M, K, device=device)
         self.dyT, self.sdyT = e.empty_requant_128x1_T(M, N, device=device)
         self.dW = torch.empty(N, K, dtype=torch.float32, device=device)
-        self.names = ["quant_128x128(W)", "quant_1x128(X)", "fprop", "quant_1x128(dY)", "dgrad",
-                      "requant_128x1_T(Xq)", "requant_128x1_T(dY)", "wgrad"]
+        self.names = ["quant_128x128(W)", "quant_1x128(X)", "fprop", "quant_dual(dY)", "dgrad",
+                      "requant_128x1_T(Xq)", "wgrad"]
 
     def work(self):
         return step_work(self.M, self.K, self.N)
@@ -238,10 +237,9 @@ class DenseStep:
             lambda: e.fp8_quant_128x128(self.W, self.wq, self.wqT, self.sw),
             lambda: e.fp8_quant_1x128(self.X, self.xq, self.sx),
             lambda: e.fp8_block_gemm_fprop(self.xq, self.sx, self.wqT, self.sw, self.Y),
-            lambda: e.fp8_quant_1x128(self.dY, self.dyq, self.sdy),
+            lambda: e.fp8_quant_dual(self.dY, self.dyq, self.sdy, self.dyT, self.sdyT),
             lambda: e.fp8_block_gemm_dgrad(self.dyq, self.sdy, self.wq, self.sw, self.dX),
             lambda: e.fp8_requant_128x1_T(self.xq, self.sx, self.xT, self.sxT),
-            lambda: e.fp8_requant_128x1_T(self.dY, None, self.dyT, self.sdyT),
             lambda: e.fp8_block_gemm_wgrad(self.dyT, self.sdyT, self.xT, self.sxT, self.dW),
         ]
 
@@ -281,8 +279,8 @@ class MoeStep:
         self.aT, self.saT = e.empty_requant_128x1_T(tokens, inter, self.offsets, device)
         self.dWd = torch.empty(experts, hidden, inter, dtype=torch.float32, device=device)
         self.names = ["quant_128x128(W_up)", "quant_128x128(W_down)", "quant_1x128(X)",
-                      "grouped_fprop_up", "quant_1x128(A)", "grouped_fprop_down", "quant_1x128(dY)",
-                      "grouped_dgrad_down", "requant_128x1_T(dY)", "requant_128x1_T(Aq)",
+                      "grouped_fprop_up", "quant_1x128(A)", "grouped_fprop_down", "quant_dual(dY)",
+                      "grouped_dgrad_down", "requant_128x1_T(Aq)",
                       "grouped_wgrad_down"]
 
     def work(self):
@@ -298,9 +296,8 @@ class MoeStep:
             "grouped_fprop_up": T * H + G * U * H + 2 * T * U,
             "quant_1x128(A)": T * I * 3 + 4 * (I // 128) * s_ld,
             "grouped_fprop_down": T * I + G * H * I + 2 * T * H,
-            "quant_1x128(dY)": T * H * 3 + 4 * (H // 128) * s_ld,
+            "quant_dual(dY)": T * H * 3 + 4 * (H // 128) * s_ld + H * mp + 4 * (mp // 128) * H,
             "grouped_dgrad_down": T * H + G * I * H + 2 * T * I,
-            "requant_128x1_T(dY)": T * H * 2 + H * mp + 4 * (mp // 128) * H,
             "requant_128x1_T(Aq)": T * I + 4 * (I // 128) * s_ld + I * mp + 4 * (mp // 128) * I,
             "grouped_wgrad_down": (H + I) * mp + 4 * G * H * I,
         }
@@ -317,10 +314,9 @@ class MoeStep:
             lambda: e.fp8_quant_1x128(self.A, self.aq, self.sa),
             lambda: e.fp8_block_gemm_grouped(e.OP_FPROP, off, self.aq, self.sa, self.wdqT, self.swd,
                                              self.Yd, H, I),
-            lambda: e.fp8_quant_1x128(self.dY, self.dyq, self.sdy),
+            lambda: e.fp8_quant_dual(self.dY, self.dyq, self.sdy, self.dyT, self.sdyT, offsets=off),
             lambda: e.fp8_block_gemm_grouped(e.OP_DGRAD, off, self.dyq, self.sdy, self.wdq, self.swd,
                                              self.dA, H, I),
-            lambda: e.fp8_requant_128x1_T(self.dY, None, self.dyT, self.sdyT, offsets=off),
             lambda: e.fp8_requant_128x1_T(self.aq, self.sa, self.aT, self.saT, offsets=off),
             lambda: e.fp8_block_gemm_grouped(e.OP_WGRAD, off, self.dyT, self.sdyT, self.aT, self.saT,
                                              self.dWd, H, I),

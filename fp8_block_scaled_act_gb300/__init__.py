@@ -23,7 +23,7 @@ from . import _build_lib
 
 __all__ = [
     "Fp8bsError", "build", "lib", "lib_path",
-    "fp8_quant_1x128", "fp8_quant_128x128", "fp8_requant_128x1_T",
+    "fp8_quant_1x128", "fp8_quant_128x128", "fp8_requant_128x1_T", "fp8_quant_dual",
     "fp8_block_gemm_fprop", "fp8_block_gemm_dgrad", "fp8_block_gemm_wgrad",
     "fp8_block_gemm_grouped", "fp8_block_gemm_splitk", "fp8bs_splitk_workspace_size",
     "fp8bs_splitk_default_splits", "fp8_block_gemm_splitk_noalloc", "NOALLOC_SCRATCH_BYTES",
@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
         "fp8_quant_1x128": ([P, I64, I64, I64, P, P, P], S),
         "fp8_quant_128x128": ([P, I64, I64, I64, I64, P, P, P, P], S),
         "fp8_requant_128x1_T": ([I, P, P, I64, I64, P, I32, P, P, P], S),
+        "fp8_quant_dual": ([P, I64, I64, P, I32, P, P, P, P, P], S),
         "fp8_block_gemm_fprop": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_block_gemm_dgrad": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_block_gemm_wgrad": ([P, P, P, P, I64, I64, I64, P, I, P], S),
@@ -245,6 +246,32 @@ def fp8_requant_128x1_T(src: torch.Tensor, src_scales: Optional[torch.Tensor], q
     _check("fp8_requant_128x1_T", lib().fp8_requant_128x1_T(
         mode, _ptr(src), _ptr(src_scales if mode == SRC_E4M3 else None), rows, cols, optr, groups,
         _ptr(qT), _ptr(scalesT), _stream(stream)))
+
+
+def fp8_quant_dual(x: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, qT: torch.Tensor,
+                   scalesT: torch.Tensor, offsets=None, stream=None) -> None:
+    """One read of BF16 x [rows x cols]: its 1x128 cast (q, scales, as
+    fp8_quant_1x128) and its 128x1 transposed cast (qT, scalesT, as
+    fp8_requant_128x1_T from BF16), optional host group offsets."""
+    _need(x, torch.bfloat16, "x")
+    for t, n, d in ((q, "q", torch.uint8), (scales, "scales", torch.float32), (qT, "qT", torch.uint8),
+                    (scalesT, "scalesT", torch.float32)):
+        _need(t, d, n)
+    rows, cols = x.shape
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    if q.shape != (rows, cols) or scales.shape != ((cols + 127) // 128, fp8bs_scale_ld(rows)):
+        raise ValueError("q / scales shapes do not match empty_quant_1x128")
+    if offsets is not None:
+        off = _offsets_host(offsets)
+        optr, groups = off.ctypes.data_as(ctypes.c_void_p), off.size - 1
+    else:
+        off, optr, groups = None, None, 0
+    mp = fp8bs_padded_tokens(rows, offsets)
+    if qT.shape != (cols, mp) or scalesT.shape != (mp // 128, cols):
+        raise ValueError("qT / scalesT shapes do not match empty_requant_128x1_T")
+    _check("fp8_quant_dual", lib().fp8_quant_dual(
+        _ptr(x), rows, cols, optr, groups, _ptr(q), _ptr(scales), _ptr(qT), _ptr(scalesT), _stream(stream)))
 
 
 def fp8_block_gemm_fprop(xq, sx, wqT, sw, y, stream=None) -> None:

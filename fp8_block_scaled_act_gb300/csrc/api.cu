@@ -313,9 +313,16 @@ fp8bs_status fp8_quant_128x128(const void* w, int64_t batch, int64_t rows, int64
                                               ldw, q, qT, scales, static_cast<cudaStream_t>(stream)));
 }
 
-fp8bs_status fp8_requant_128x1_T(int src_mode, const void* src, const float* src_scales,
-                                 int64_t rows, int64_t cols, const int32_t* group_offsets_host,
-                                 int32_t groups, uint8_t* qT, float* scalesT, void* stream)
+}  // extern "C"
+
+namespace fp8bs {
+namespace {
+
+// The 128x1 transposed cast (S3), optionally with the same pass's 1x128 cast
+// of a BF16 source (q, q_scales non-null).
+fp8bs_status requant_common(int src_mode, const void* src, const float* src_scales, int64_t rows, int64_t cols,
+                            const int32_t* group_offsets_host, int32_t groups, uint8_t* qT, float* scalesT,
+                            uint8_t* q, float* q_scales, void* stream)
 {
     if (src_mode != FP8BS_SRC_BF16 && src_mode != FP8BS_SRC_E4M3) return FP8BS_ERR_ARG;
     if (rows < 0 || cols <= 0 || groups < 0) return FP8BS_ERR_ARG;
@@ -328,7 +335,7 @@ fp8bs_status fp8_requant_128x1_T(int src_mode, const void* src, const float* src
     if (mpad == 0) return FP8BS_OK;
     if (!src || !qT || !scalesT || (src_mode == FP8BS_SRC_E4M3 && !src_scales)) return FP8BS_ERR_ARG;
     if (!aligned16(src) || !aligned16(qT) || !aligned16(scalesT) ||
-        (src_scales && !aligned16(src_scales)))
+        (src_scales && !aligned16(src_scales)) || (q && !aligned16(q)) || (q_scales && !aligned16(q_scales)))
         return FP8BS_ERR_ALIGN;
     DeviceState* st = nullptr;
     fp8bs_status s = device_state(&st);
@@ -345,6 +352,9 @@ fp8bs_status fp8_requant_128x1_T(int src_mode, const void* src, const float* src
     p.qT = qT;
     p.scT = scalesT;
     p.mpad = mpad;
+    p.q = q;
+    p.q_scales = q_scales;
+    p.q_scale_ld = fp8bs_scale_ld(rows);
     if (grouped) {
         p.num_groups = groups;
         int tiles = 0;
@@ -362,6 +372,28 @@ fp8bs_status fp8_requant_128x1_T(int src_mode, const void* src, const float* src
         p.tile_start[1] = static_cast<int32_t>(mpad / 128);
     }
     return launch_status(launch_requant_128x1_T(p, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+}  // namespace fp8bs
+
+extern "C" {
+
+fp8bs_status fp8_requant_128x1_T(int src_mode, const void* src, const float* src_scales,
+                                 int64_t rows, int64_t cols, const int32_t* group_offsets_host,
+                                 int32_t groups, uint8_t* qT, float* scalesT, void* stream)
+{
+    return requant_common(src_mode, src, src_scales, rows, cols, group_offsets_host, groups, qT, scalesT,
+                          nullptr, nullptr, stream);
+}
+
+fp8bs_status fp8_quant_dual(const void* x, int64_t rows, int64_t cols, const int32_t* group_offsets_host,
+                            int32_t groups, uint8_t* q, float* scales, uint8_t* qT, float* scalesT,
+                            void* stream)
+{
+    if (rows > 0 && (!q || !scales)) return FP8BS_ERR_ARG;
+    return requant_common(FP8BS_SRC_BF16, x, nullptr, rows, cols, group_offsets_host, groups, qT, scalesT, q,
+                          scales, stream);
 }
 
 fp8bs_status fp8_block_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wqT,

@@ -36,6 +36,11 @@ struct RequantParams {
     int num_groups;
     int32_t off[kMaxGroups + 1];         // row offsets of the groups
     int32_t tile_start[kMaxGroups + 1];  // first padded token tile of each group
+    // Optional, BF16 source only: the same block's 1x128 (row-wise) cast in
+    // the same pass, q [rows x cols] and its scales [cols/128 x q_scale_ld].
+    uint8_t* q;
+    float* q_scales;
+    int64_t q_scale_ld;
 };
 
 cudaError_t launch_requant_128x1_T(const RequantParams& p, cudaStream_t stream);

@@ -431,7 +431,9 @@ __device__ __forceinline__ int find_group(const int32_t* tile_start, int ng, int
     return lo;
 }
 
-__global__ void __launch_bounds__(kQ3Threads) requant_128x1_T_kernel(const __grid_constant__ RequantParams p)
+// kDual: also the 1x128 cast of the same BF16 rows (p.q, p.q_scales).
+template <bool kDual>
+__global__ void __launch_bounds__(kQ3Threads, kDual ? 3 : 4) requant_128x1_T_kernel(const __grid_constant__ RequantParams p)
 {
     // staging: BF16 source 128 x 128 x 2 bytes, or E4M3 128 x 128 bytes + row scales
     __shared__ __align__(16) uint8_t stage[128 * 128 * 2];
@@ -461,6 +463,27 @@ __global__ void __launch_bounds__(kQ3Threads) requant_128x1_T_kernel(const __gri
             else
                 d[i] = make_uint4(0u, 0u, 0u, 0u);
             *reinterpret_cast<uint4*>(stage + (rl * 128 + chunk * 8) * 2) = d[i];
+        }
+        if constexpr (kDual) {
+            // Row-wise (1x128) cast of the same rows from the registers: a
+            // row's 128 channels are the 16 chunks held by 16 consecutive
+            // lanes, so its absmax is a 4-step xor-shuffle over those lanes.
+            uint32_t rm[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) rm[i] = absmax_bits_8(d[i]);
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) rm[i] = max(rm[i], __shfl_xor_sync(0xFFFFFFFFu, rm[i], off));
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int rl = rg * 8 + i;
+                if (rl >= len) continue;
+                const TileScale ts = tile_scale(__uint_as_float(rm[i] << 16));
+                if (chunk == 0) p.q_scales[(c0 / 128) * p.q_scale_ld + r0 + rl] = ts.s;
+                if (ch_ok)
+                    *reinterpret_cast<uint2*>(p.q + (r0 + rl) * p.cols + c0 + chunk * 8) = quant8(d[i], ts);
+            }
         }
         uint32_t mw[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
@@ -610,7 +633,10 @@ cudaError_t launch_requant_128x1_T(const RequantParams& p, cudaStream_t stream)
     if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
     const dim3 grid((unsigned)tiles, (unsigned)((p.cols + 127) / 128));
     if (grid.y > 65535) return cudaErrorInvalidValue;
-    requant_128x1_T_kernel<<<grid, kQ3Threads, 0, stream>>>(p);
+    if (p.q != nullptr)
+        requant_128x1_T_kernel<true><<<grid, kQ3Threads, 0, stream>>>(p);
+    else
+        requant_128x1_T_kernel<false><<<grid, kQ3Threads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -165,6 +165,25 @@ FP8BS_API fp8bs_status fp8_requant_128x1_T(int src_mode, const void* src, const 
                                  const int32_t* group_offsets_host, int32_t groups,
                                  uint8_t* qT, float* scalesT, void* stream);
 
+/* NEXT-1: dual-orientation cast of one BF16 tensor in a single read: the    */
+/* 1x128 cast of fp8_quant_1x128 and the 128x1 transposed cast of            */
+/* fp8_requant_128x1_T (FP8BS_SRC_BF16), both outputs byte-identical to the  */
+/* two separate calls. [P1] "What is asserted, and from where": the output   */
+/* gradient is quantized once in both tile orientations (row-wise for Dgrad, */
+/* column-wise for Wgrad); [P3] "Performance" measures the separate casts as */
+/* an extra read of the gradient, which this call removes.                   */
+/* x        : BF16 [rows x cols], dense (row stride = cols), cols % 16 == 0.  */
+/* group_offsets_host, groups : as for fp8_requant_128x1_T (NULL/0 = dense);  */
+/*            the 1x128 outputs do not depend on the grouping.               */
+/* q, scales: as fp8_quant_1x128 (E4M3 [rows x cols]; fp32 tile-major        */
+/*            [cols/128 x fp8bs_scale_ld(rows)]).                             */
+/* qT, scalesT : as fp8_requant_128x1_T.                                      */
+/* Errors as for those two calls.                                             */
+FP8BS_API fp8bs_status fp8_quant_dual(const void* x, int64_t rows, int64_t cols,
+                                      const int32_t* group_offsets_host, int32_t groups,
+                                      uint8_t* q, float* scales, uint8_t* qT, float* scalesT,
+                                      void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* S4-S6. Block-scaled E4M3 GEMMs with per-128-K fp32 promotion              */
 /* [P1] bullet 1 (all three GEMMs E4M3; BF16 activations and input grads,     */

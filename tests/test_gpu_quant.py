@@ -207,3 +207,44 @@ def test_quantizers_are_deterministic():
     a = _gpu_quant_1x128(x)
     b = _gpu_quant_1x128(x)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def _gpu_dual(x_dev, offsets=None):
+    R, C = x_dev.shape
+    q, sc = fp8bs.empty_quant_1x128(R, C)
+    qT, scT = fp8bs.empty_requant_128x1_T(R, C, offsets)
+    fp8bs.fp8_quant_dual(x_dev, q, sc, qT, scT, offsets=offsets)
+    torch.cuda.synchronize()
+    return np_(q), np_(sc), np_(qT), np_(scT)
+
+
+def _check_dual(x, offsets=None):
+    R, C = x.shape
+    q, sc, qT, scT = _gpu_dual(x.cuda(), offsets)
+    oq, osc = oracle.quant_1x128(u16(x))
+    assert np.array_equal(q, oq)
+    assert np.array_equal(sc[:, :R].view(np.uint32), osc[:, :R].view(np.uint32))
+    oqT, oscT = oracle.requant_128x1_T(u16(x), offsets=offsets)
+    assert np.array_equal(qT, oqT)
+    assert np.array_equal(scT.view(np.uint32), oscT.view(np.uint32))
+
+
+@pytest.mark.parametrize("M,C,counts", [
+    (128, 128, None), (300, 256, None), (1, 16, None), (257, 400, None), (129, 2048, None),
+    (400, 128, [0, 129, 1, 0, 270]), (131, 144, [131]), (260, 256, [0, 0, 260, 0]),
+])
+def test_quant_dual_matches_both_casts(M, C, counts):
+    """One read of BF16 dY gives the 1x128 cast and the 128x1 transposed cast,
+    byte-identical to the oracle's two quantizations (special tiles included:
+    zeros, -0 and tiny negatives, exact E4M3 midpoints, tiny scales)."""
+    x = _special_inputs(M, C, seed=M + 7 * C)
+    _check_dual(x, None if counts is None else wl.offsets_from_counts(counts))
+
+
+def test_quant_dual_backward_grad_full():
+    _check_dual(wl.backward()["dY"])
+
+
+def test_quant_dual_moe_grouped_full():
+    d = wl.moe(with_weights=False)
+    _check_dual(d["dY"], d["offsets"])
