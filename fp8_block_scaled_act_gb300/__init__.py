@@ -32,9 +32,12 @@ __all__ = [
     "fp8bs_status_str", "fp8bs_version",
     "empty_quant_1x128", "empty_quant_128x128", "empty_requant_128x1_T",
     "SRC_BF16", "SRC_E4M3", "OP_FPROP", "OP_DGRAD", "OP_WGRAD", "MAX_GROUPS",
+    "SCALE_FP32", "SCALE_UE8M0", "ScaleOpts", "fp8_quant_1x128_opts", "fp8_quant_128x128_opts",
+    "fp8_requant_128x1_T_opts", "fp8_quant_dual_opts",
 ]
 
 SRC_BF16, SRC_E4M3 = 0, 1
+SCALE_FP32, SCALE_UE8M0 = 0, 1
 OP_FPROP, OP_DGRAD, OP_WGRAD = 0, 1, 2
 MAX_GROUPS = 256
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024   # FP8BS_NOALLOC_SCRATCH_BYTES
@@ -42,6 +45,11 @@ STATUS_NAMES = {0: "OK", 1: "ERR_ARG", 2: "ERR_ALIGN", 3: "ERR_SHAPE", 4: "ERR_L
                 5: "ERR_TIMEOUT", 6: "ERR_UNSUPPORTED", 7: "ERR_DEVICE"}
 
 _lib = None
+
+
+class ScaleOpts(ctypes.Structure):
+    """fp8bs_scale_opts: the quantizers' scale rule (see fp8bs.h)."""
+    _fields_ = [("rule", ctypes.c_int32), ("amax_floor", ctypes.c_float), ("scale_floor", ctypes.c_float)]
 
 
 class Fp8bsError(RuntimeError):
@@ -80,6 +88,10 @@ def lib() -> ctypes.CDLL:
         "fp8_quant_128x128": ([P, I64, I64, I64, I64, P, P, P, P], S),
         "fp8_requant_128x1_T": ([I, P, P, I64, I64, P, I32, P, P, P], S),
         "fp8_quant_dual": ([P, I64, I64, P, I32, P, P, P, P, P], S),
+        "fp8_quant_1x128_opts": ([P, I64, I64, I64, P, P, P, P], S),
+        "fp8_quant_128x128_opts": ([P, I64, I64, I64, I64, P, P, P, P, P], S),
+        "fp8_requant_128x1_T_opts": ([I, P, P, I64, I64, P, I32, P, P, P, P], S),
+        "fp8_quant_dual_opts": ([P, I64, I64, P, I32, P, P, P, P, P, P], S),
         "fp8_block_gemm_fprop": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_block_gemm_dgrad": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_block_gemm_wgrad": ([P, P, P, P, I64, I64, I64, P, I, P], S),
@@ -114,6 +126,13 @@ def _stream(stream) -> ctypes.c_void_p:
     if isinstance(stream, torch.cuda.Stream):
         return ctypes.c_void_p(stream.cuda_stream)
     return ctypes.c_void_p(int(stream))
+
+
+def _opts(rule: int, amax_floor: float, scale_floor: float):
+    """ctypes pointer to a ScaleOpts, or None for the default rule."""
+    if rule == SCALE_FP32 and amax_floor == 0.0 and scale_floor == 0.0:
+        return None
+    return ctypes.pointer(ScaleOpts(int(rule), float(amax_floor), float(scale_floor)))
 
 
 def _check(name: str, code: int) -> None:
@@ -197,18 +216,21 @@ def empty_requant_128x1_T(rows: int, cols: int, offsets=None, device="cuda"):
 # entry points
 # ---------------------------------------------------------------------------
 
-def fp8_quant_1x128(x: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, stream=None) -> None:
-    """1x128 absmax quantization of BF16 x [rows x cols] into q / scales."""
+def fp8_quant_1x128(x: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, stream=None,
+                    rule: int = SCALE_FP32, amax_floor: float = 0.0, scale_floor: float = 0.0) -> None:
+    """1x128 absmax quantization of BF16 x [rows x cols] into q / scales
+    (optional scale rule: UE8M0 rounding, amax / scale floors)."""
     _need(x, torch.bfloat16, "x"); _need(q, torch.uint8, "q"); _need(scales, torch.float32, "scales")
     rows, cols = x.shape
     if q.shape != (rows, cols) or scales.shape != ((cols + 127) // 128, fp8bs_scale_ld(rows)):
         raise ValueError("output shapes do not match empty_quant_1x128")
-    _check("fp8_quant_1x128", lib().fp8_quant_1x128(_ptr(x), rows, cols, cols, _ptr(q),
-                                                    _ptr(scales), _stream(stream)))
+    _check("fp8_quant_1x128", lib().fp8_quant_1x128_opts(_ptr(x), rows, cols, cols, _ptr(q), _ptr(scales),
+                                                         _opts(rule, amax_floor, scale_floor), _stream(stream)))
 
 
 def fp8_quant_128x128(w: torch.Tensor, q: torch.Tensor, qT: Optional[torch.Tensor],
-                      scales: torch.Tensor, stream=None) -> None:
+                      scales: torch.Tensor, stream=None, rule: int = SCALE_FP32, amax_floor: float = 0.0,
+                      scale_floor: float = 0.0) -> None:
     """128x128 absmax quantization of BF16 w [rows x cols] (or [batch x rows x cols])."""
     _need(w, torch.bfloat16, "w"); _need(q, torch.uint8, "q"); _need(scales, torch.float32, "scales")
     if qT is not None:
@@ -219,12 +241,14 @@ def fp8_quant_128x128(w: torch.Tensor, q: torch.Tensor, qT: Optional[torch.Tenso
     if (q.numel() != w.numel() or q.shape[-2:] != (rows, cols) or scales.numel() != batch * nb
             or (qT is not None and (qT.numel() != w.numel() or qT.shape[-2:] != (cols, rows)))):
         raise ValueError("output shapes do not match empty_quant_128x128")
-    _check("fp8_quant_128x128", lib().fp8_quant_128x128(_ptr(w), batch, rows, cols, cols, _ptr(q),
-                                                        _ptr(qT), _ptr(scales), _stream(stream)))
+    _check("fp8_quant_128x128", lib().fp8_quant_128x128_opts(_ptr(w), batch, rows, cols, cols, _ptr(q),
+                                                             _ptr(qT), _ptr(scales),
+                                                             _opts(rule, amax_floor, scale_floor), _stream(stream)))
 
 
 def fp8_requant_128x1_T(src: torch.Tensor, src_scales: Optional[torch.Tensor], qT: torch.Tensor,
-                        scalesT: torch.Tensor, offsets=None, stream=None) -> None:
+                        scalesT: torch.Tensor, offsets=None, stream=None, rule: int = SCALE_FP32,
+                        amax_floor: float = 0.0, scale_floor: float = 0.0) -> None:
     """128x1 transposed requantization. src BF16 (mode B) or uint8 E4M3 with
     its 1x128 scales (mode Q); optional host group offsets."""
     if src.dtype == torch.bfloat16:
@@ -243,13 +267,14 @@ def fp8_requant_128x1_T(src: torch.Tensor, src_scales: Optional[torch.Tensor], q
     mp = fp8bs_padded_tokens(rows, offsets)
     if qT.shape != (cols, mp) or scalesT.shape != (mp // 128, cols):
         raise ValueError("output shapes do not match empty_requant_128x1_T")
-    _check("fp8_requant_128x1_T", lib().fp8_requant_128x1_T(
+    _check("fp8_requant_128x1_T", lib().fp8_requant_128x1_T_opts(
         mode, _ptr(src), _ptr(src_scales if mode == SRC_E4M3 else None), rows, cols, optr, groups,
-        _ptr(qT), _ptr(scalesT), _stream(stream)))
+        _ptr(qT), _ptr(scalesT), _opts(rule, amax_floor, scale_floor), _stream(stream)))
 
 
 def fp8_quant_dual(x: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, qT: torch.Tensor,
-                   scalesT: torch.Tensor, offsets=None, stream=None) -> None:
+                   scalesT: torch.Tensor, offsets=None, stream=None, rule: int = SCALE_FP32,
+                   amax_floor: float = 0.0, scale_floor: float = 0.0) -> None:
     """One read of BF16 x [rows x cols]: its 1x128 cast (q, scales, as
     fp8_quant_1x128) and its 128x1 transposed cast (qT, scalesT, as
     fp8_requant_128x1_T from BF16), optional host group offsets."""
@@ -270,8 +295,37 @@ def fp8_quant_dual(x: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, qT: t
     mp = fp8bs_padded_tokens(rows, offsets)
     if qT.shape != (cols, mp) or scalesT.shape != (mp // 128, cols):
         raise ValueError("qT / scalesT shapes do not match empty_requant_128x1_T")
-    _check("fp8_quant_dual", lib().fp8_quant_dual(
-        _ptr(x), rows, cols, optr, groups, _ptr(q), _ptr(scales), _ptr(qT), _ptr(scalesT), _stream(stream)))
+    _check("fp8_quant_dual", lib().fp8_quant_dual_opts(
+        _ptr(x), rows, cols, optr, groups, _ptr(q), _ptr(scales), _ptr(qT), _ptr(scalesT),
+        _opts(rule, amax_floor, scale_floor), _stream(stream)))
+
+
+def _rule_kwargs(opts: Optional[ScaleOpts]) -> dict:
+    if opts is None:
+        return {}
+    return dict(rule=int(opts.rule), amax_floor=float(opts.amax_floor), scale_floor=float(opts.scale_floor))
+
+
+def fp8_quant_1x128_opts(x, q, scales, opts: Optional[ScaleOpts], stream=None) -> None:
+    """fp8_quant_1x128 under the scale rule `opts` (None: default)."""
+    fp8_quant_1x128(x, q, scales, stream=stream, **_rule_kwargs(opts))
+
+
+def fp8_quant_128x128_opts(w, q, qT, scales, opts: Optional[ScaleOpts], stream=None) -> None:
+    """fp8_quant_128x128 under the scale rule `opts` (None: default)."""
+    fp8_quant_128x128(w, q, qT, scales, stream=stream, **_rule_kwargs(opts))
+
+
+def fp8_requant_128x1_T_opts(src, src_scales, qT, scalesT, opts: Optional[ScaleOpts], offsets=None,
+                             stream=None) -> None:
+    """fp8_requant_128x1_T under the scale rule `opts` (None: default)."""
+    fp8_requant_128x1_T(src, src_scales, qT, scalesT, offsets=offsets, stream=stream, **_rule_kwargs(opts))
+
+
+def fp8_quant_dual_opts(x, q, scales, qT, scalesT, opts: Optional[ScaleOpts], offsets=None,
+                        stream=None) -> None:
+    """fp8_quant_dual under the scale rule `opts` (None: default)."""
+    fp8_quant_dual(x, q, scales, qT, scalesT, offsets=offsets, stream=stream, **_rule_kwargs(opts))
 
 
 def fp8_block_gemm_fprop(xq, sx, wqT, sw, y, stream=None) -> None:

@@ -70,6 +70,22 @@ fp8bs_status device_state(DeviceState** out)
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Public scale options -> kernel rule; false for invalid options.
+bool to_rule(const fp8bs_scale_opts* o, ScaleRule* r)
+{
+    r->ue8m0 = 0;
+    r->amax_floor = 0.0f;
+    r->scale_floor = 0.0f;
+    if (!o) return true;
+    if (o->rule != FP8BS_SCALE_FP32 && o->rule != FP8BS_SCALE_UE8M0) return false;
+    if (!(o->amax_floor >= 0.0f && o->amax_floor <= 3.0e38f)) return false;     // also rejects NaN
+    if (!(o->scale_floor >= 0.0f && o->scale_floor <= 3.0e38f)) return false;
+    r->ue8m0 = o->rule == FP8BS_SCALE_UE8M0 ? 1 : 0;
+    r->amax_floor = o->amax_floor;
+    r->scale_floor = o->scale_floor;
+    return true;
+}
+
 inline fp8bs_status launch_status(cudaError_t e) { return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_LAUNCH; }
 
 // 2D E4M3 tensor map over a row-major [outer x inner] byte matrix, box
@@ -285,6 +301,14 @@ int64_t fp8bs_padded_tokens(int64_t rows, const int32_t* group_offsets_host, int
 fp8bs_status fp8_quant_1x128(const void* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q,
                              float* scales, void* stream)
 {
+    return fp8_quant_1x128_opts(x, rows, cols, ldx, q, scales, nullptr, stream);
+}
+
+fp8bs_status fp8_quant_1x128_opts(const void* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q,
+                                  float* scales, const fp8bs_scale_opts* opts, void* stream)
+{
+    ScaleRule rule;
+    if (!to_rule(opts, &rule)) return FP8BS_ERR_ARG;
     if (rows < 0 || cols <= 0 || ldx < cols) return FP8BS_ERR_ARG;
     if (cols % 16 != 0) return FP8BS_ERR_SHAPE;
     if (rows == 0) return FP8BS_OK;
@@ -294,13 +318,22 @@ fp8bs_status fp8_quant_1x128(const void* x, int64_t rows, int64_t cols, int64_t 
     fp8bs_status s = device_state(&st);
     if (s != FP8BS_OK) return s;
     return launch_status(launch_quant_1x128(static_cast<const uint16_t*>(x), rows, cols, ldx, q,
-                                            scales, fp8bs_scale_ld(rows), st->num_sms,
+                                            scales, fp8bs_scale_ld(rows), rule, st->num_sms,
                                             static_cast<cudaStream_t>(stream)));
 }
 
 fp8bs_status fp8_quant_128x128(const void* w, int64_t batch, int64_t rows, int64_t cols,
                                int64_t ldw, uint8_t* q, uint8_t* qT, float* scales, void* stream)
 {
+    return fp8_quant_128x128_opts(w, batch, rows, cols, ldw, q, qT, scales, nullptr, stream);
+}
+
+fp8bs_status fp8_quant_128x128_opts(const void* w, int64_t batch, int64_t rows, int64_t cols, int64_t ldw,
+                                    uint8_t* q, uint8_t* qT, float* scales, const fp8bs_scale_opts* opts,
+                                    void* stream)
+{
+    ScaleRule rule;
+    if (!to_rule(opts, &rule)) return FP8BS_ERR_ARG;
     if (batch < 1 || rows <= 0 || cols <= 0 || ldw < cols) return FP8BS_ERR_ARG;
     if (rows % 16 != 0 || cols % 16 != 0) return FP8BS_ERR_SHAPE;
     if (!w || !q || !scales) return FP8BS_ERR_ARG;
@@ -310,7 +343,7 @@ fp8bs_status fp8_quant_128x128(const void* w, int64_t batch, int64_t rows, int64
     fp8bs_status s = device_state(&st);
     if (s != FP8BS_OK) return s;
     return launch_status(launch_quant_128x128(static_cast<const uint16_t*>(w), batch, rows, cols,
-                                              ldw, q, qT, scales, static_cast<cudaStream_t>(stream)));
+                                              ldw, q, qT, scales, rule, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"
@@ -322,8 +355,10 @@ namespace {
 // of a BF16 source (q, q_scales non-null).
 fp8bs_status requant_common(int src_mode, const void* src, const float* src_scales, int64_t rows, int64_t cols,
                             const int32_t* group_offsets_host, int32_t groups, uint8_t* qT, float* scalesT,
-                            uint8_t* q, float* q_scales, void* stream)
+                            uint8_t* q, float* q_scales, const fp8bs_scale_opts* opts, void* stream)
 {
+    ScaleRule rule;
+    if (!to_rule(opts, &rule)) return FP8BS_ERR_ARG;
     if (src_mode != FP8BS_SRC_BF16 && src_mode != FP8BS_SRC_E4M3) return FP8BS_ERR_ARG;
     if (rows < 0 || cols <= 0 || groups < 0) return FP8BS_ERR_ARG;
     if (cols % 16 != 0) return FP8BS_ERR_SHAPE;
@@ -355,6 +390,7 @@ fp8bs_status requant_common(int src_mode, const void* src, const float* src_scal
     p.q = q;
     p.q_scales = q_scales;
     p.q_scale_ld = fp8bs_scale_ld(rows);
+    p.rule = rule;
     if (grouped) {
         p.num_groups = groups;
         int tiles = 0;
@@ -384,16 +420,31 @@ fp8bs_status fp8_requant_128x1_T(int src_mode, const void* src, const float* src
                                  int32_t groups, uint8_t* qT, float* scalesT, void* stream)
 {
     return requant_common(src_mode, src, src_scales, rows, cols, group_offsets_host, groups, qT, scalesT,
-                          nullptr, nullptr, stream);
+                          nullptr, nullptr, nullptr, stream);
+}
+
+fp8bs_status fp8_requant_128x1_T_opts(int src_mode, const void* src, const float* src_scales, int64_t rows,
+                                      int64_t cols, const int32_t* group_offsets_host, int32_t groups,
+                                      uint8_t* qT, float* scalesT, const fp8bs_scale_opts* opts, void* stream)
+{
+    return requant_common(src_mode, src, src_scales, rows, cols, group_offsets_host, groups, qT, scalesT,
+                          nullptr, nullptr, opts, stream);
 }
 
 fp8bs_status fp8_quant_dual(const void* x, int64_t rows, int64_t cols, const int32_t* group_offsets_host,
                             int32_t groups, uint8_t* q, float* scales, uint8_t* qT, float* scalesT,
                             void* stream)
 {
+    return fp8_quant_dual_opts(x, rows, cols, group_offsets_host, groups, q, scales, qT, scalesT, nullptr, stream);
+}
+
+fp8bs_status fp8_quant_dual_opts(const void* x, int64_t rows, int64_t cols, const int32_t* group_offsets_host,
+                                 int32_t groups, uint8_t* q, float* scales, uint8_t* qT, float* scalesT,
+                                 const fp8bs_scale_opts* opts, void* stream)
+{
     if (rows > 0 && (!q || !scales)) return FP8BS_ERR_ARG;
     return requant_common(FP8BS_SRC_BF16, x, nullptr, rows, cols, group_offsets_host, groups, qT, scalesT, q,
-                          scales, stream);
+                          scales, opts, stream);
 }
 
 fp8bs_status fp8_block_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wqT,

@@ -16,13 +16,21 @@ constexpr int kMaxGroups = FP8BS_MAX_GROUPS;
 // Quantizers
 // ---------------------------------------------------------------------------
 
+// How a tile's scale follows from its absmax (the default {0, 0, 0} is the
+// plain rule s = amax / 448, 1 for an all-zero tile).
+struct ScaleRule {
+    int ue8m0;          // 1: round s up to a power of two
+    float amax_floor;   // amax = max(amax, amax_floor) before the division
+    float scale_floor;  // s = max(s, scale_floor)
+};
+
 cudaError_t launch_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
-                               uint8_t* q, float* scales, int64_t scale_ld, int num_sms,
-                               cudaStream_t stream);
+                               uint8_t* q, float* scales, int64_t scale_ld, const ScaleRule& rule,
+                               int num_sms, cudaStream_t stream);
 
 cudaError_t launch_quant_128x128(const uint16_t* w, int64_t batch, int64_t rows, int64_t cols,
                                  int64_t ldw, uint8_t* q, uint8_t* qT, float* scales,
-                                 cudaStream_t stream);
+                                 const ScaleRule& rule, cudaStream_t stream);
 
 struct RequantParams {
     int mode;                  // FP8BS_SRC_BF16 or FP8BS_SRC_E4M3
@@ -41,6 +49,7 @@ struct RequantParams {
     uint8_t* q;
     float* q_scales;
     int64_t q_scale_ld;
+    ScaleRule rule;
 };
 
 cudaError_t launch_requant_128x1_T(const RequantParams& p, cudaStream_t stream);

@@ -34,9 +34,28 @@ __device__ __forceinline__ uint32_t absmax_bits_8(const uint4& d)
     return max(m & 0xFFFFu, m >> 16);
 }
 
-__device__ __forceinline__ float scale_from_amax(float amax)
+// Smallest power of two >= s, for s > 0 (normal or subnormal).
+__device__ __forceinline__ float pow2_ceil(float s)
 {
-    return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+    const uint32_t b = __float_as_uint(s);
+    if ((b & 0x007FFFFFu) == 0u) return s;                              // already 2^e
+    if ((b >> 23) != 0u) return __uint_as_float((b & 0x7F800000u) + 0x00800000u);
+    return __uint_as_float(1u << (32 - __clz(b - 1u)));                 // subnormal
+}
+
+// Scale of a tile from its absmax. Default rule: s = amax / 448 (IEEE fp32
+// division), 1 for an all-zero tile. Options (prime-rl PR #4073, conventions
+// table, rows "Weight floors", "Two-stage weights", "Activation floors",
+// "Compact formats"): an amax floor applied before the division, a scale
+// floor applied after it (a zero tile then gets the floored scale instead of
+// 1), and UE8M0 rounding of s up to a power of two, so that amax / s stays
+// <= 448 and every scale is an exponent byte.
+__device__ __forceinline__ float scale_from_amax(float amax, const ScaleRule& r)
+{
+    const float a = fmaxf(amax, r.amax_floor);
+    float s = (a == 0.0f && r.scale_floor == 0.0f) ? 1.0f : __fdiv_rn(a, 448.0f);
+    s = fmaxf(s, r.scale_floor);
+    return r.ue8m0 ? pow2_ceil(s) : s;
 }
 
 // E4M3 codes of fp32(v / s) for a pair of values, by exact IEEE division.
@@ -116,9 +135,9 @@ __device__ __forceinline__ TileScale tile_scale_from_s(float s)
     return t;
 }
 
-__device__ __forceinline__ TileScale tile_scale(float amax)
+__device__ __forceinline__ TileScale tile_scale(float amax, const ScaleRule& r)
 {
-    return tile_scale_from_s(scale_from_amax(amax));
+    return tile_scale_from_s(scale_from_amax(amax, r));
 }
 
 __device__ __noinline__ uint2 quant8_exact(uint4 d, float s)
@@ -153,7 +172,7 @@ constexpr int kQ1Threads = 256;
 
 __global__ void __launch_bounds__(kQ1Threads) quant_1x128_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
-    uint8_t* __restrict__ q, float* __restrict__ scales, int64_t scale_ld)
+    uint8_t* __restrict__ q, float* __restrict__ scales, int64_t scale_ld, const ScaleRule rule)
 {
     const int lane = threadIdx.x & 31;
     const int half = lane >> 4;
@@ -203,7 +222,7 @@ __global__ void __launch_bounds__(kQ1Threads) quant_1x128_kernel(
         const float amax_mine = __uint_as_float(m[0] << 16);
         const int my_row = 2 * lh + half;
         // one scale (and reciprocal) per lane: lane (h, j) owns row 2j + h
-        const TileScale mine = tile_scale(amax_mine);
+        const TileScale mine = tile_scale(amax_mine, rule);
         if (row0 + my_row < rows) scales[tc * scale_ld + row0 + my_row] = mine.s;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -229,7 +248,7 @@ constexpr int kQ2Pitch = 132;  // bytes per row of the staging tile (bank-confli
 
 __global__ void __launch_bounds__(kQ2Threads) quant_128x128_kernel(
     const uint16_t* __restrict__ w, int64_t rows, int64_t cols, int64_t ldw,
-    uint8_t* __restrict__ q, uint8_t* __restrict__ qT, float* __restrict__ scales)
+    uint8_t* __restrict__ q, uint8_t* __restrict__ qT, float* __restrict__ scales, const ScaleRule rule)
 {
     __shared__ uint32_t red[kQ2Threads / 32];
     __shared__ __align__(16) uint8_t tile[128 * kQ2Pitch];
@@ -265,7 +284,7 @@ __global__ void __launch_bounds__(kQ2Threads) quant_128x128_kernel(
     m = 0;
 #pragma unroll
     for (int i = 0; i < kQ2Threads / 32; ++i) m = max(m, red[i]);
-    const TileScale ts = tile_scale(__uint_as_float(m << 16));
+    const TileScale ts = tile_scale(__uint_as_float(m << 16), rule);
     if (threadIdx.x == 0) scales[b * nbr * nbc + bi * nbc + bj] = ts.s;
 
     uint8_t* qb = q + b * rows * cols;
@@ -479,7 +498,7 @@ __global__ void __launch_bounds__(kQ3Threads, kDual ? 3 : 4) requant_128x1_T_ker
             for (int i = 0; i < 8; ++i) {
                 const int rl = rg * 8 + i;
                 if (rl >= len) continue;
-                const TileScale ts = tile_scale(__uint_as_float(rm[i] << 16));
+                const TileScale ts = tile_scale(__uint_as_float(rm[i] << 16), p.rule);
                 if (chunk == 0) p.q_scales[(c0 / 128) * p.q_scale_ld + r0 + rl] = ts.s;
                 if (ch_ok)
                     *reinterpret_cast<uint2*>(p.q + (r0 + rl) * p.cols + c0 + chunk * 8) = quant8(d[i], ts);
@@ -547,7 +566,7 @@ __global__ void __launch_bounds__(kQ3Threads, kDual ? 3 : 4) requant_128x1_T_ker
         float m = 0.0f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) m = fmaxf(m, col_part[i][threadIdx.x]);
-        const float s = scale_from_amax(m);
+        const float s = scale_from_amax(m, p.rule);
         col_scale[threadIdx.x] = s;
         if (threadIdx.x < nch) p.scT[(int64_t)tile * p.cols + c0 + threadIdx.x] = s;
     }
@@ -597,8 +616,8 @@ __global__ void __launch_bounds__(kQ3Threads, kDual ? 3 : 4) requant_128x1_T_ker
 }  // namespace
 
 cudaError_t launch_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
-                               uint8_t* q, float* scales, int64_t scale_ld, int num_sms,
-                               cudaStream_t stream)
+                               uint8_t* q, float* scales, int64_t scale_ld, const ScaleRule& rule,
+                               int num_sms, cudaStream_t stream)
 {
     if (rows == 0) return cudaSuccess;
     // One unit (32 rows x 128 columns) per warp: blocks run in as many waves
@@ -610,19 +629,19 @@ cudaError_t launch_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, in
     const int64_t cap = (int64_t)num_sms * 512;  // grid-stride only for very large tensors
     if (blocks > cap) blocks = cap;
     quant_1x128_kernel<<<(unsigned)blocks, kQ1Threads, 0, stream>>>(x, rows, cols, ldx, q, scales,
-                                                                   scale_ld);
+                                                                   scale_ld, rule);
     return cudaGetLastError();
 }
 
 cudaError_t launch_quant_128x128(const uint16_t* w, int64_t batch, int64_t rows, int64_t cols,
                                  int64_t ldw, uint8_t* q, uint8_t* qT, float* scales,
-                                 cudaStream_t stream)
+                                 const ScaleRule& rule, cudaStream_t stream)
 {
     const int64_t blocks = batch * ((rows + 127) / 128) * ((cols + 127) / 128);
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
     quant_128x128_kernel<<<(unsigned)blocks, kQ2Threads, 0, stream>>>(w, rows, cols, ldw, q, qT,
-                                                                     scales);
+                                                                     scales, rule);
     return cudaGetLastError();
 }
 

@@ -184,6 +184,44 @@ FP8BS_API fp8bs_status fp8_quant_dual(const void* x, int64_t rows, int64_t cols,
                                       uint8_t* q, float* scales, uint8_t* qT, float* scalesT,
                                       void* stream);
 
+/* NEXT-4: scale rule options for the four quantizers above. The pages name  */
+/* the conventions without fixing every detail ([P4] conventions table, rows */
+/* "Weight floors", "Two-stage weights", "Activation floors", "Compact       */
+/* formats"); the reading implemented here:                                   */
+/*   a = max(amax, amax_floor);                                               */
+/*   s = a / 448 in fp32, or 1 when a == 0 and no scale floor is set;         */
+/*   s = max(s, scale_floor);                                                 */
+/*   FP8BS_SCALE_UE8M0: s = the smallest power of two >= s (an exponent byte; */
+/*   amax / s stays <= 448, and above 224 for a non-floored tile).            */
+/* Scales are still stored as fp32 values (the Hopper container); GEMMs take  */
+/* them unchanged. The default (NULL, or rule FP8BS_SCALE_FP32 with zero      */
+/* floors) is the plain rule of the calls above.                              */
+enum { FP8BS_SCALE_FP32 = 0, FP8BS_SCALE_UE8M0 = 1 };
+typedef struct {
+    int32_t rule;          /* FP8BS_SCALE_FP32 or FP8BS_SCALE_UE8M0 */
+    float amax_floor;      /* >= 0 (0: none) */
+    float scale_floor;     /* >= 0 (0: none) */
+} fp8bs_scale_opts;
+
+/* The calls above with a scale rule; opts == NULL is the default rule.       */
+/* Invalid options (unknown rule, negative or non-finite floors) return       */
+/* FP8BS_ERR_ARG.                                                             */
+FP8BS_API fp8bs_status fp8_quant_1x128_opts(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                                            uint8_t* q, float* scales, const fp8bs_scale_opts* opts,
+                                            void* stream);
+FP8BS_API fp8bs_status fp8_quant_128x128_opts(const void* w, int64_t batch, int64_t rows, int64_t cols,
+                                              int64_t ldw, uint8_t* q, uint8_t* qT, float* scales,
+                                              const fp8bs_scale_opts* opts, void* stream);
+FP8BS_API fp8bs_status fp8_requant_128x1_T_opts(int src_mode, const void* src, const float* src_scales,
+                                                int64_t rows, int64_t cols,
+                                                const int32_t* group_offsets_host, int32_t groups,
+                                                uint8_t* qT, float* scalesT,
+                                                const fp8bs_scale_opts* opts, void* stream);
+FP8BS_API fp8bs_status fp8_quant_dual_opts(const void* x, int64_t rows, int64_t cols,
+                                           const int32_t* group_offsets_host, int32_t groups,
+                                           uint8_t* q, float* scales, uint8_t* qT, float* scalesT,
+                                           const fp8bs_scale_opts* opts, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* S4-S6. Block-scaled E4M3 GEMMs with per-128-K fp32 promotion              */
 /* [P1] bullet 1 (all three GEMMs E4M3; BF16 activations and input grads,     */

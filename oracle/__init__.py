@@ -39,6 +39,8 @@ FAULT_TRANSPOSED_W = 5
 FAULT_DROP_NEG_ZERO = 6
 FAULT_RECIPROCAL = 7
 FAULT_SIGN_FLIP_TERM = 8
+FAULT_UE8M0_DOWN = 9
+FAULT_FLOOR_AFTER = 10
 
 
 def build(force: bool = False) -> str:
@@ -95,6 +97,7 @@ def _load():
         lib.oracle_num_threads.restype = I
         lib.oracle_set_num_threads.argtypes = [I]
         lib.oracle_set_fault.argtypes = [I]
+        lib.oracle_set_scale_rule.argtypes = [I, ctypes.c_float, ctypes.c_float]
         _lib = lib
         return lib
 
@@ -111,6 +114,22 @@ def _c(a, dtype):
 def set_fault(f: int) -> None:
     """Plant one of the FAULT_* mistakes (negative-control tests only)."""
     _load().oracle_set_fault(int(f))
+
+
+class scale_rule:
+    """Context manager: run the quantizers under a scale rule (UE8M0 scales,
+    amax floor, scale floor); the default rule is restored on exit."""
+
+    def __init__(self, ue8m0: bool = False, amax_floor: float = 0.0, scale_floor: float = 0.0):
+        self.args = (int(bool(ue8m0)), float(amax_floor), float(scale_floor))
+
+    def __enter__(self):
+        _load().oracle_set_scale_rule(*self.args)
+        return self
+
+    def __exit__(self, *exc):
+        _load().oracle_set_scale_rule(0, 0.0, 0.0)
+        return False
 
 
 def num_threads() -> int:

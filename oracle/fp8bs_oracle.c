@@ -69,7 +69,9 @@ enum {
     FAULT_TRANSPOSED_W = 5,      /* fprop reads W transposed */
     FAULT_DROP_NEG_ZERO = 6,     /* -0 results encoded as 0x00 */
     FAULT_RECIPROCAL = 7,        /* v * (1/s) instead of v / s */
-    FAULT_SIGN_FLIP_TERM = 8     /* one K-block's term subtracted */
+    FAULT_SIGN_FLIP_TERM = 8,    /* one K-block's term subtracted */
+    FAULT_UE8M0_DOWN = 9,        /* UE8M0 scale rounded down, not up */
+    FAULT_FLOOR_AFTER = 10       /* amax floor applied to s instead of amax */
 };
 static int g_fault = FAULT_NONE;
 
@@ -170,8 +172,36 @@ void oracle_f32_to_bf16_array(const float* in, i64 n, uint16_t* out)
 /* One quantization tile: amax, scale, codes.                                 */
 /* ------------------------------------------------------------------------- */
 
-/* Scale of a tile whose values are v[0..n): amax / 448 in fp32, or 1 for an
- * all-zero tile. */
+/* Scale rule options (prime-rl PR #4073, conventions table, rows "Weight
+ * floors", "Two-stage weights", "Activation floors", "Compact formats"): an
+ * amax floor applied before the division, a scale floor applied after it,
+ * and power-of-two (UE8M0) scales. The table names these conventions without
+ * fixing their order; the reading used here (also stated in the design
+ * notes): a = max(amax, amax_floor); s = a / 448, or 1 when a == 0 and no
+ * scale floor is set; s = max(s, scale_floor); UE8M0: s = the smallest power
+ * of two >= s. Defaults (rule 0, no floors) give the plain rule. */
+static int g_ue8m0 = 0;
+static float g_amax_floor = 0.0f;
+static float g_scale_floor = 0.0f;
+
+void oracle_set_scale_rule(int ue8m0, float amax_floor, float scale_floor)
+{
+    g_ue8m0 = ue8m0;
+    g_amax_floor = amax_floor;
+    g_scale_floor = scale_floor;
+}
+
+/* Smallest power of two that is >= s (s > 0), from frexp's decomposition
+ * s = m * 2^e with m in [0.5, 1): s itself when m == 0.5, else 2^e. */
+static float pow2_at_least(float s)
+{
+    int e;
+    float m = frexpf(s, &e);
+    return (m == 0.5f) ? s : ldexpf(1.0f, e);
+}
+
+/* Scale of a tile whose values are v[0..n) under the current scale rule
+ * (default: amax / 448 in fp32, or 1 for an all-zero tile). */
 static float tile_scale(const float* v, int n)
 {
     float amax = 0.0f;
@@ -179,8 +209,19 @@ static float tile_scale(const float* v, int n)
         float a = (g_fault == FAULT_SIGNED_AMAX) ? v[i] : fabsf(v[i]);
         if (a > amax) amax = a;
     }
-    if (amax == 0.0f) return 1.0f;
-    return amax / 448.0f;
+    if (g_fault != FAULT_FLOOR_AFTER && amax < g_amax_floor) amax = g_amax_floor;
+    float s;
+    if (amax == 0.0f && g_scale_floor == 0.0f && (g_fault != FAULT_FLOOR_AFTER || g_amax_floor == 0.0f))
+        s = 1.0f;
+    else
+        s = amax / 448.0f;
+    if (g_fault == FAULT_FLOOR_AFTER && s < g_amax_floor) s = g_amax_floor;
+    if (s < g_scale_floor) s = g_scale_floor;
+    if (g_ue8m0) {
+        s = pow2_at_least(s);
+        if (g_fault == FAULT_UE8M0_DOWN && amax != 0.0f) s = 0.5f * s;
+    }
+    return s;
 }
 
 static void tile_encode(const float* v, int n, float s, uint8_t* out, i64 out_step)

@@ -248,3 +248,69 @@ def test_quant_dual_backward_grad_full():
 def test_quant_dual_moe_grouped_full():
     d = wl.moe(with_weights=False)
     _check_dual(d["dY"], d["offsets"])
+
+
+RULES = [
+    dict(rule=fp8bs.SCALE_UE8M0),
+    dict(amax_floor=1e-4),
+    dict(scale_floor=2.0 ** -33),
+    dict(rule=fp8bs.SCALE_UE8M0, scale_floor=2.0 ** -33),
+    dict(rule=fp8bs.SCALE_UE8M0, amax_floor=1e-4),
+]
+
+
+def _oracle_rule(r):
+    return oracle.scale_rule(ue8m0=r.get("rule", 0) == fp8bs.SCALE_UE8M0,
+                             amax_floor=r.get("amax_floor", 0.0), scale_floor=r.get("scale_floor", 0.0))
+
+
+@pytest.mark.parametrize("r", RULES)
+def test_scale_rules_all_quantizers(r):
+    """NEXT-4 scale rules (UE8M0 scales, amax and scale floors) on every
+    quantizer, byte- and bit-exact against the oracle under the same rule;
+    the inputs include an all-zero tile, where the floors decide the scale."""
+    M, C = 300, 384
+    x = _special_inputs(M, C, seed=31)
+    xd = x.cuda()
+    q, sc = fp8bs.empty_quant_1x128(M, C)
+    fp8bs.fp8_quant_1x128(xd, q, sc, **r)
+    w = _special_inputs(384, 256, seed=32)
+    wq, wqT, sw = fp8bs.empty_quant_128x128(384, 256)
+    fp8bs.fp8_quant_128x128(w.cuda(), wq, wqT, sw, **r)
+    off = wl.offsets_from_counts([0, 129, 1, 0, 170])
+    qT, scT = fp8bs.empty_requant_128x1_T(M, C, off)
+    fp8bs.fp8_requant_128x1_T(xd, None, qT, scT, offsets=off, **r)
+    xq0, sx0 = fp8bs.empty_quant_1x128(M, C)
+    fp8bs.fp8_quant_1x128(xd, xq0, sx0)                     # default-rule stash
+    qTq, scTq = fp8bs.empty_requant_128x1_T(M, C)
+    fp8bs.fp8_requant_128x1_T(xq0, sx0, qTq, scTq, **r)
+    dq, dsc = fp8bs.empty_quant_1x128(M, C)
+    dqT, dscT = fp8bs.empty_requant_128x1_T(M, C, off)
+    fp8bs.fp8_quant_dual(xd, dq, dsc, dqT, dscT, offsets=off, **r)
+    torch.cuda.synchronize()
+
+    oxq0, osx0 = oracle.quant_1x128(u16(x))
+    with _oracle_rule(r):
+        oq, osc = oracle.quant_1x128(u16(x))
+        owq, osw = oracle.quant_128x128(u16(w))
+        oqT, oscT = oracle.requant_128x1_T(u16(x), offsets=off)
+        oqTq, oscTq = oracle.requant_128x1_T(oxq0, osx0)
+    bits = lambda a: np.ascontiguousarray(a).view(np.uint32)
+    assert np.array_equal(np_(q), oq) and np.array_equal(bits(np_(sc)[:, :M]), bits(osc[:, :M]))
+    assert np.array_equal(np_(wq), owq) and np.array_equal(bits(np_(sw)), bits(osw))
+    assert np.array_equal(np_(wqT), owq.T)
+    assert np.array_equal(np_(qT), oqT) and np.array_equal(bits(np_(scT)), bits(oscT))
+    assert np.array_equal(np_(qTq), oqTq) and np.array_equal(bits(np_(scTq)), bits(oscTq))
+    assert np.array_equal(np_(dq), oq) and np.array_equal(bits(np_(dsc)[:, :M]), bits(osc[:, :M]))
+    assert np.array_equal(np_(dqT), oqT) and np.array_equal(bits(np_(dscT)), bits(oscT))
+    if r.get("rule") == fp8bs.SCALE_UE8M0:
+        mant, _ = np.frexp(np_(sc)[:, :M])
+        assert np.all(mant == 0.5)
+
+
+def test_scale_rule_rejects_bad_options():
+    x = torch.zeros((4, 128), dtype=torch.bfloat16, device="cuda")
+    q, sc = fp8bs.empty_quant_1x128(4, 128)
+    for bad in (dict(rule=7), dict(amax_floor=-1.0), dict(scale_floor=float("nan"))):
+        with pytest.raises(fp8bs.Fp8bsError):
+            fp8bs.fp8_quant_1x128(x, q, sc, **bad)

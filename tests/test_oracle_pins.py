@@ -249,6 +249,66 @@ def test_quant_invariants():
     assert np.array_equal(np.signbit(dq), np.signbit(v))
 
 
+def _ue8m0_quant(x):
+    with oracle.scale_rule(ue8m0=True):
+        return oracle.quant_1x128(x, sc_layout="row_major")
+
+
+def test_ue8m0_scales_are_the_smallest_unsaturating_powers_of_two():
+    """Power-of-two scales (prime-rl PR #4073 conventions table, rows
+    "Two-stage weights" and "Compact formats"): every scale is 2^e; the
+    tile's absmax stays within the E4M3 range after division (up to the fp32
+    rounding of amax / 448 that the rule starts from); half the scale would
+    push it past 448; the absmax element encodes to a code in [224, 448];
+    and since the quotient v / 2^e is exact, every code is the E4M3 rounding
+    of the exact v / s."""
+    R, C = 64, 128 * 4
+    x = _tile_inputs(R, C, seed=8)
+    q, sc = _ue8m0_quant(x)
+    t = oracle.e4m3_table().astype(np.float64)
+    v = oracle.bf16_to_f32(x).reshape(R, -1, 128).astype(np.float64)
+    mant, _ = np.frexp(sc)
+    assert np.all(mant == 0.5)
+    amax = np.abs(v).max(-1)
+    nz = amax > 0
+    s = sc.astype(np.float64)
+    assert np.all(amax[nz] / s[nz] <= 448.0 * (1 + 2.0 ** -23))
+    assert np.all(amax[nz] / (s[nz] / 2) > 448.0 * (1 - 2.0 ** -23))
+    assert np.all(sc[~nz] == 1.0)
+    dq = t[q].reshape(R, -1, 128)
+    top = np.take_along_axis(dq, np.abs(v).argmax(-1)[..., None], -1)[..., 0]
+    assert np.all((np.abs(top[nz]) >= 224.0) & (np.abs(top[nz]) <= 448.0))
+    exact = (v / s[..., None]).astype(np.float32)          # exact: s is a power of two
+    enc = oracle.e4m3_encode_array(exact.ravel()).reshape(exact.shape)
+    assert np.array_equal(enc, q.reshape(R, -1, 128))
+
+
+def test_scale_floors_closed_forms():
+    """Floors (prime-rl PR #4073 conventions table, rows "Weight floors" and
+    "Activation floors"): an amax floor f gives a zero tile the scale
+    fp32(f / 448); a scale floor g gives it g; tiles whose own scale is
+    above a floor are unchanged; the UE8M0 rule applies after the floors."""
+    x = _tile_inputs(8, 256, seed=9)
+    v = oracle.bf16_to_f32(x).reshape(8, -1, 128)
+    nz = np.abs(v).max(-1) > 0
+    tiny = np.zeros((8, 256), np.uint16)                    # all-zero rows
+    _, base = oracle.quant_1x128(x, sc_layout="row_major")
+    with oracle.scale_rule(amax_floor=1e-4):
+        _, s_a = oracle.quant_1x128(tiny, sc_layout="row_major")
+        _, s_ax = oracle.quant_1x128(x, sc_layout="row_major")
+    with oracle.scale_rule(scale_floor=2.0 ** -33):
+        _, s_s = oracle.quant_1x128(tiny, sc_layout="row_major")
+        _, s_sx = oracle.quant_1x128(x, sc_layout="row_major")
+    with oracle.scale_rule(ue8m0=True, amax_floor=1e-4):
+        _, s_u = oracle.quant_1x128(tiny, sc_layout="row_major")
+    assert np.all(s_a == np.float32(np.float32(1e-4) / np.float32(448.0)))
+    assert np.all(s_s == np.float32(2.0 ** -33))
+    big = nz & (base >= np.float32(1e-4) / np.float32(448.0))
+    assert np.array_equal(s_ax[big], base[big]) and np.array_equal(s_sx[big], base[big])
+    # 1e-4 / 448 = 2.23e-7 lies in [2^-23, 2^-22): UE8M0 rounds it up to 2^-22
+    assert np.all(s_u == np.float32(2.0 ** -22))
+
+
 def test_quant_reciprocal_case_is_distinguished():
     """A tile where v * (1/s) and v / s round to different E4M3 codes: the
     torch-steps pin must see the true division."""
@@ -504,6 +564,15 @@ def _pin_quant():
         return False
 
 
+def _pin_scale_rules():
+    try:
+        test_ue8m0_scales_are_the_smallest_unsaturating_powers_of_two()
+        test_scale_floors_closed_forms()
+        return True
+    except AssertionError:
+        return False
+
+
 def _pin_gemm():
     return (_check_fprop(130, 384, 256, 21) and _check_dgrad(129, 384, 256, 22)
             and _check_wgrad(300, 256, 128, 23) and _check_fprop(64, 256, 256, 24))
@@ -518,9 +587,12 @@ def _pin_gemm():
     (oracle.FAULT_DROP_NEG_ZERO, "encoder"),
     (oracle.FAULT_RECIPROCAL, "quant"),
     (oracle.FAULT_SIGN_FLIP_TERM, "gemm"),
+    (oracle.FAULT_UE8M0_DOWN, "scale_rules"),
+    (oracle.FAULT_FLOOR_AFTER, "scale_rules"),
 ])
 def test_planted_mistake_is_caught(fault, pin):
-    check = {"encoder": _pin_encoder, "quant": _pin_quant, "gemm": _pin_gemm}[pin]
+    check = {"encoder": _pin_encoder, "quant": _pin_quant, "gemm": _pin_gemm,
+             "scale_rules": _pin_scale_rules}[pin]
     assert check()
     oracle.set_fault(fault)
     try:
