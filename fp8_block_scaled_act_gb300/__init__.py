@@ -33,7 +33,7 @@ __all__ = [
     "empty_quant_1x128", "empty_quant_128x128", "empty_requant_128x1_T",
     "SRC_BF16", "SRC_E4M3", "OP_FPROP", "OP_DGRAD", "OP_WGRAD", "MAX_GROUPS",
     "SCALE_FP32", "SCALE_UE8M0", "ScaleOpts", "fp8_quant_1x128_opts", "fp8_quant_128x128_opts",
-    "fp8_requant_128x1_T_opts", "fp8_quant_dual_opts",
+    "fp8_requant_128x1_T_opts", "fp8_quant_dual_opts", "fp8_quant_1x128_sr", "fp8_quant_128x128_sr",
 ]
 
 SRC_BF16, SRC_E4M3 = 0, 1
@@ -92,6 +92,8 @@ def lib() -> ctypes.CDLL:
         "fp8_quant_128x128_opts": ([P, I64, I64, I64, I64, P, P, P, P, P], S),
         "fp8_requant_128x1_T_opts": ([I, P, P, I64, I64, P, I32, P, P, P, P], S),
         "fp8_quant_dual_opts": ([P, I64, I64, P, I32, P, P, P, P, P, P], S),
+        "fp8_quant_1x128_sr": ([P, I64, I64, I64, P, P, ctypes.c_uint64, ctypes.c_uint32, P, P], S),
+        "fp8_quant_128x128_sr": ([P, I64, I64, I64, I64, P, P, P, ctypes.c_uint64, ctypes.c_uint32, P, P], S),
         "fp8_block_gemm_fprop": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_block_gemm_dgrad": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_block_gemm_wgrad": ([P, P, P, P, I64, I64, I64, P, I, P], S),
@@ -298,6 +300,35 @@ def fp8_quant_dual(x: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, qT: t
     _check("fp8_quant_dual", lib().fp8_quant_dual_opts(
         _ptr(x), rows, cols, optr, groups, _ptr(q), _ptr(scales), _ptr(qT), _ptr(scalesT),
         _opts(rule, amax_floor, scale_floor), _stream(stream)))
+
+
+def fp8_quant_1x128_sr(x, q, scales, seed: int, salt: int = 0, stream=None, rule: int = SCALE_FP32,
+                       amax_floor: float = 0.0, scale_floor: float = 0.0) -> None:
+    """fp8_quant_1x128 with stochastic rounding under (seed, salt); see fp8bs.h."""
+    _need(x, torch.bfloat16, "x"); _need(q, torch.uint8, "q"); _need(scales, torch.float32, "scales")
+    rows, cols = x.shape
+    if q.shape != (rows, cols) or scales.shape != ((cols + 127) // 128, fp8bs_scale_ld(rows)):
+        raise ValueError("output shapes do not match empty_quant_1x128")
+    _check("fp8_quant_1x128_sr", lib().fp8_quant_1x128_sr(
+        _ptr(x), rows, cols, cols, _ptr(q), _ptr(scales), int(seed) & (2 ** 64 - 1), int(salt) & 0xFFFFFFFF,
+        _opts(rule, amax_floor, scale_floor), _stream(stream)))
+
+
+def fp8_quant_128x128_sr(w, q, qT, scales, seed: int, salt: int = 0, stream=None, rule: int = SCALE_FP32,
+                         amax_floor: float = 0.0, scale_floor: float = 0.0) -> None:
+    """fp8_quant_128x128 with stochastic rounding under (seed, salt); see fp8bs.h."""
+    _need(w, torch.bfloat16, "w"); _need(q, torch.uint8, "q"); _need(scales, torch.float32, "scales")
+    if qT is not None:
+        _need(qT, torch.uint8, "qT")
+    batch = w.shape[0] if w.dim() == 3 else 1
+    rows, cols = w.shape[-2:]
+    nb = ((rows + 127) // 128) * ((cols + 127) // 128)
+    if (q.numel() != w.numel() or q.shape[-2:] != (rows, cols) or scales.numel() != batch * nb
+            or (qT is not None and (qT.numel() != w.numel() or qT.shape[-2:] != (cols, rows)))):
+        raise ValueError("output shapes do not match empty_quant_128x128")
+    _check("fp8_quant_128x128_sr", lib().fp8_quant_128x128_sr(
+        _ptr(w), batch, rows, cols, cols, _ptr(q), _ptr(qT), _ptr(scales), int(seed) & (2 ** 64 - 1),
+        int(salt) & 0xFFFFFFFF, _opts(rule, amax_floor, scale_floor), _stream(stream)))
 
 
 def _rule_kwargs(opts: Optional[ScaleOpts]) -> dict:

@@ -70,6 +70,14 @@ fp8bs_status device_state(DeviceState** out)
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The quantizer entry points with an optional stochastic-rounding key
+// (defined after the extern "C" wrappers).
+fp8bs_status quant_1x128_common(const void* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q,
+                                float* scales, const fp8bs_scale_opts* opts, const SrParams* sr, void* stream);
+fp8bs_status quant_128x128_common(const void* w, int64_t batch, int64_t rows, int64_t cols, int64_t ldw,
+                                  uint8_t* q, uint8_t* qT, float* scales, const fp8bs_scale_opts* opts,
+                                  const SrParams* sr, void* stream);
+
 // Public scale options -> kernel rule; false for invalid options.
 bool to_rule(const fp8bs_scale_opts* o, ScaleRule* r)
 {
@@ -307,6 +315,25 @@ fp8bs_status fp8_quant_1x128(const void* x, int64_t rows, int64_t cols, int64_t 
 fp8bs_status fp8_quant_1x128_opts(const void* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q,
                                   float* scales, const fp8bs_scale_opts* opts, void* stream)
 {
+    return quant_1x128_common(x, rows, cols, ldx, q, scales, opts, nullptr, stream);
+}
+
+fp8bs_status fp8_quant_1x128_sr(const void* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q,
+                                float* scales, uint64_t seed, uint32_t salt, const fp8bs_scale_opts* opts,
+                                void* stream)
+{
+    const SrParams sr{seed, salt};
+    return quant_1x128_common(x, rows, cols, ldx, q, scales, opts, &sr, stream);
+}
+
+}  // extern "C"
+
+namespace fp8bs {
+namespace {
+
+fp8bs_status quant_1x128_common(const void* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q,
+                                float* scales, const fp8bs_scale_opts* opts, const SrParams* sr, void* stream)
+{
     ScaleRule rule;
     if (!to_rule(opts, &rule)) return FP8BS_ERR_ARG;
     if (rows < 0 || cols <= 0 || ldx < cols) return FP8BS_ERR_ARG;
@@ -318,9 +345,14 @@ fp8bs_status fp8_quant_1x128_opts(const void* x, int64_t rows, int64_t cols, int
     fp8bs_status s = device_state(&st);
     if (s != FP8BS_OK) return s;
     return launch_status(launch_quant_1x128(static_cast<const uint16_t*>(x), rows, cols, ldx, q,
-                                            scales, fp8bs_scale_ld(rows), rule, st->num_sms,
+                                            scales, fp8bs_scale_ld(rows), rule, sr, st->num_sms,
                                             static_cast<cudaStream_t>(stream)));
 }
+
+}  // namespace
+}  // namespace fp8bs
+
+extern "C" {
 
 fp8bs_status fp8_quant_128x128(const void* w, int64_t batch, int64_t rows, int64_t cols,
                                int64_t ldw, uint8_t* q, uint8_t* qT, float* scales, void* stream)
@@ -331,6 +363,26 @@ fp8bs_status fp8_quant_128x128(const void* w, int64_t batch, int64_t rows, int64
 fp8bs_status fp8_quant_128x128_opts(const void* w, int64_t batch, int64_t rows, int64_t cols, int64_t ldw,
                                     uint8_t* q, uint8_t* qT, float* scales, const fp8bs_scale_opts* opts,
                                     void* stream)
+{
+    return quant_128x128_common(w, batch, rows, cols, ldw, q, qT, scales, opts, nullptr, stream);
+}
+
+fp8bs_status fp8_quant_128x128_sr(const void* w, int64_t batch, int64_t rows, int64_t cols, int64_t ldw,
+                                  uint8_t* q, uint8_t* qT, float* scales, uint64_t seed, uint32_t salt,
+                                  const fp8bs_scale_opts* opts, void* stream)
+{
+    const SrParams sr{seed, salt};
+    return quant_128x128_common(w, batch, rows, cols, ldw, q, qT, scales, opts, &sr, stream);
+}
+
+}  // extern "C"
+
+namespace fp8bs {
+namespace {
+
+fp8bs_status quant_128x128_common(const void* w, int64_t batch, int64_t rows, int64_t cols, int64_t ldw,
+                                  uint8_t* q, uint8_t* qT, float* scales, const fp8bs_scale_opts* opts,
+                                  const SrParams* sr, void* stream)
 {
     ScaleRule rule;
     if (!to_rule(opts, &rule)) return FP8BS_ERR_ARG;
@@ -343,8 +395,13 @@ fp8bs_status fp8_quant_128x128_opts(const void* w, int64_t batch, int64_t rows, 
     fp8bs_status s = device_state(&st);
     if (s != FP8BS_OK) return s;
     return launch_status(launch_quant_128x128(static_cast<const uint16_t*>(w), batch, rows, cols,
-                                              ldw, q, qT, scales, rule, static_cast<cudaStream_t>(stream)));
+                                              ldw, q, qT, scales, rule, sr, static_cast<cudaStream_t>(stream)));
 }
+
+}  // namespace
+}  // namespace fp8bs
+
+extern "C" {
 
 }  // extern "C"
 

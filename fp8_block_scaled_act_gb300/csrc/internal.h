@@ -24,13 +24,19 @@ struct ScaleRule {
     float scale_floor;  // s = max(s, scale_floor)
 };
 
+// Stochastic rounding key (NULL pointer: round to nearest).
+struct SrParams {
+    uint64_t seed;
+    uint32_t salt;
+};
+
 cudaError_t launch_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
                                uint8_t* q, float* scales, int64_t scale_ld, const ScaleRule& rule,
-                               int num_sms, cudaStream_t stream);
+                               const SrParams* sr, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_quant_128x128(const uint16_t* w, int64_t batch, int64_t rows, int64_t cols,
                                  int64_t ldw, uint8_t* q, uint8_t* qT, float* scales,
-                                 const ScaleRule& rule, cudaStream_t stream);
+                                 const ScaleRule& rule, const SrParams* sr, cudaStream_t stream);
 
 struct RequantParams {
     int mode;                  // FP8BS_SRC_BF16 or FP8BS_SRC_E4M3

@@ -162,6 +162,108 @@ __device__ __forceinline__ uint2 quant8(const uint4& d, const TileScale& t)
 }
 
 // ---------------------------------------------------------------------------
+// Stochastic rounding (NEXT-3). The random word of element idx (its linear
+// index in the quantized tensor) under (seed, salt) is word idx % 4 of
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC 2011) with key (seed low,
+// seed high) and counter (idx / 4 low, idx / 4 high, salt, 0): stateless,
+// independent of launch shape. The quotient x = RN(v / s) then rounds to the
+// upper E4M3 neighbour when the 20-bit fraction of its position between the
+// two neighbours exceeds the word's top 20 bits (probability = the fraction),
+// else to the lower one; |x| >= 448 gives 448; signs (and signed zeros) are
+// kept.
+// ---------------------------------------------------------------------------
+struct SrKey {
+    uint64_t seed;
+    uint32_t salt;
+};
+
+__device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
+                                               uint32_t k1)
+{
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
+        const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
+        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return make_uint4(c0, c1, c2, c3);
+}
+
+// Words of elements 4 blk .. 4 blk + 3.
+__device__ __forceinline__ uint4 sr_words(const SrKey& k, uint64_t blk)
+{
+    return philox4x32_10(static_cast<uint32_t>(blk), static_cast<uint32_t>(blk >> 32), k.salt, 0u,
+                         static_cast<uint32_t>(k.seed), static_cast<uint32_t>(k.seed >> 32));
+}
+
+// E4M3 code of the fp32 quotient x, stochastically rounded with word r.
+__device__ __forceinline__ uint32_t sr_code(float x, uint32_t r)
+{
+    const uint32_t b = __float_as_uint(x);
+    const uint32_t sign = (b >> 24) & 0x80u;
+    const uint32_t a = b & 0x7FFFFFFFu;
+    const uint32_t r20 = r >> 12;
+    if (a >= 0x43E00000u) return sign | 0x7Eu;                // |x| >= 448
+    if (a >= 0x3C800000u) {                                    // E4M3 normal range, |x| >= 2^-6
+        const uint32_t code = (((a >> 23) - 120u) << 3) | ((a >> 20) & 7u);
+        return sign | (code + ((a & 0xFFFFFu) > r20 ? 1u : 0u));
+    }
+    const float t = __uint_as_float(a) * 512.0f;               // position on the 2^-9 grid (exact)
+    const uint32_t n = static_cast<uint32_t>(t);
+    const uint32_t f20 = static_cast<uint32_t>((t - static_cast<float>(n)) * 1048576.0f);
+    return sign | (n + (f20 > r20 ? 1u : 0u));
+}
+
+// Quotients RN(v / s) of a pair (negated inputs, as encode2_fast) without
+// the conversion.
+__device__ __forceinline__ float2 quotient2(float2 nv, float s, float nr)
+{
+    const float2 s2 = make_float2(s, s);
+    const float2 nr2 = make_float2(nr, nr);
+    const float2 q0 = __fmul2_rn(nv, nr2);
+    const float2 q1 = __ffma2_rn(__ffma2_rn(q0, s2, nv), nr2, q0);
+    return __ffma2_rn(__ffma2_rn(q1, s2, nv), nr2, q1);
+}
+
+// Eight bf16 values with stochastic rounding; words w[0..7] for elements
+// 0..7 of the group.
+__device__ __forceinline__ uint2 quant8_sr(const uint4& d, const TileScale& t, const uint32_t (&w)[8])
+{
+    const uint32_t wd[4] = {d.x, d.y, d.z, d.w};
+    uint32_t c[8];
+    if (t.nr == 0.0f) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            c[2 * k] = sr_code(__fdiv_rn(bf16_lo(wd[k]), t.s), w[2 * k]);
+            c[2 * k + 1] = sr_code(__fdiv_rn(bf16_hi(wd[k]), t.s), w[2 * k + 1]);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 qq = quotient2(neg_bf16x2(wd[k]), t.s, t.nr);
+            c[2 * k] = sr_code(qq.x, w[2 * k]);
+            c[2 * k + 1] = sr_code(qq.y, w[2 * k + 1]);
+        }
+    }
+    return make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24),
+                      c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
+}
+
+// Random words of the 8 consecutive elements starting at idx (idx % 8 == 0).
+__device__ __forceinline__ void sr_words8(const SrKey& k, uint64_t idx, uint32_t (&w)[8])
+{
+    const uint4 a = sr_words(k, idx >> 2), b = sr_words(k, (idx >> 2) + 1);
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+}
+
+// ---------------------------------------------------------------------------
 // S1: 1x128 tiles. One warp handles 32 rows x one 128-column tile: each
 // half-warp reads one row's 256 bytes per load (16 lanes x 16 bytes), so a
 // warp covers two rows per instruction and 32 rows in 16 loads, all issued
@@ -170,9 +272,11 @@ __device__ __forceinline__ uint2 quant8(const uint4& d, const TileScale& t)
 // ---------------------------------------------------------------------------
 constexpr int kQ1Threads = 256;
 
+template <bool kSR>
 __global__ void __launch_bounds__(kQ1Threads) quant_1x128_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
-    uint8_t* __restrict__ q, float* __restrict__ scales, int64_t scale_ld, const ScaleRule rule)
+    uint8_t* __restrict__ q, float* __restrict__ scales, int64_t scale_ld, const ScaleRule rule,
+    const SrKey sr)
 {
     const int lane = threadIdx.x & 31;
     const int half = lane >> 4;
@@ -231,7 +335,15 @@ __global__ void __launch_bounds__(kQ1Threads) quant_1x128_kernel(
             ts.s = __shfl_sync(0xFFFFFFFFu, mine.s, src);
             ts.nr = __shfl_sync(0xFFFFFFFFu, mine.nr, src);
             const int64_t r = row0 + 2 * i + half;
-            if (col_ok && r < rows) *reinterpret_cast<uint2*>(q + r * cols + col) = quant8(d[i], ts);
+            if constexpr (kSR) {
+                if (col_ok && r < rows) {
+                    uint32_t w[8];
+                    sr_words8(sr, static_cast<uint64_t>(r * cols + col), w);
+                    *reinterpret_cast<uint2*>(q + r * cols + col) = quant8_sr(d[i], ts, w);
+                }
+            } else {
+                if (col_ok && r < rows) *reinterpret_cast<uint2*>(q + r * cols + col) = quant8(d[i], ts);
+            }
         }
     }
 }
@@ -246,9 +358,11 @@ __global__ void __launch_bounds__(kQ1Threads) quant_1x128_kernel(
 constexpr int kQ2Threads = 256;
 constexpr int kQ2Pitch = 132;  // bytes per row of the staging tile (bank-conflict padding)
 
+template <bool kSR>
 __global__ void __launch_bounds__(kQ2Threads) quant_128x128_kernel(
     const uint16_t* __restrict__ w, int64_t rows, int64_t cols, int64_t ldw,
-    uint8_t* __restrict__ q, uint8_t* __restrict__ qT, float* __restrict__ scales, const ScaleRule rule)
+    uint8_t* __restrict__ q, uint8_t* __restrict__ qT, float* __restrict__ scales, const ScaleRule rule,
+    const SrKey sr)
 {
     __shared__ uint32_t red[kQ2Threads / 32];
     __shared__ __align__(16) uint8_t tile[128 * kQ2Pitch];
@@ -292,7 +406,14 @@ __global__ void __launch_bounds__(kQ2Threads) quant_128x128_kernel(
     for (int i = 0; i < 8; ++i) {
         const int rl = rgrp + 16 * i;
         const int64_t r = r0 + rl;
-        const uint2 out = quant8(d[i], ts);
+        uint2 out;
+        if constexpr (kSR) {
+            uint32_t wr[8];
+            sr_words8(sr, static_cast<uint64_t>(b * rows * cols + r * cols + col), wr);
+            out = quant8_sr(d[i], ts, wr);
+        } else {
+            out = quant8(d[i], ts);
+        }
         if (col_ok && r < rows) *reinterpret_cast<uint2*>(qb + r * cols + col) = out;
         if (qT != nullptr) {
             uint32_t* tp = reinterpret_cast<uint32_t*>(tile + rl * kQ2Pitch + chunk * 8);
@@ -617,7 +738,7 @@ __global__ void __launch_bounds__(kQ3Threads, kDual ? 3 : 4) requant_128x1_T_ker
 
 cudaError_t launch_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
                                uint8_t* q, float* scales, int64_t scale_ld, const ScaleRule& rule,
-                               int num_sms, cudaStream_t stream)
+                               const SrParams* sr, int num_sms, cudaStream_t stream)
 {
     if (rows == 0) return cudaSuccess;
     // One unit (32 rows x 128 columns) per warp: blocks run in as many waves
@@ -628,20 +749,32 @@ cudaError_t launch_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, in
     int64_t blocks = (units + warps_per_block - 1) / warps_per_block;
     const int64_t cap = (int64_t)num_sms * 512;  // grid-stride only for very large tensors
     if (blocks > cap) blocks = cap;
-    quant_1x128_kernel<<<(unsigned)blocks, kQ1Threads, 0, stream>>>(x, rows, cols, ldx, q, scales,
-                                                                   scale_ld, rule);
+    if (sr) {
+        const SrKey key{sr->seed, sr->salt};
+        quant_1x128_kernel<true><<<(unsigned)blocks, kQ1Threads, 0, stream>>>(x, rows, cols, ldx, q, scales,
+                                                                             scale_ld, rule, key);
+    } else {
+        quant_1x128_kernel<false><<<(unsigned)blocks, kQ1Threads, 0, stream>>>(x, rows, cols, ldx, q, scales,
+                                                                              scale_ld, rule, SrKey{0, 0});
+    }
     return cudaGetLastError();
 }
 
 cudaError_t launch_quant_128x128(const uint16_t* w, int64_t batch, int64_t rows, int64_t cols,
                                  int64_t ldw, uint8_t* q, uint8_t* qT, float* scales,
-                                 const ScaleRule& rule, cudaStream_t stream)
+                                 const ScaleRule& rule, const SrParams* sr, cudaStream_t stream)
 {
     const int64_t blocks = batch * ((rows + 127) / 128) * ((cols + 127) / 128);
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    quant_128x128_kernel<<<(unsigned)blocks, kQ2Threads, 0, stream>>>(w, rows, cols, ldw, q, qT,
-                                                                     scales, rule);
+    if (sr) {
+        const SrKey key{sr->seed, sr->salt};
+        quant_128x128_kernel<true><<<(unsigned)blocks, kQ2Threads, 0, stream>>>(w, rows, cols, ldw, q, qT,
+                                                                               scales, rule, key);
+    } else {
+        quant_128x128_kernel<false><<<(unsigned)blocks, kQ2Threads, 0, stream>>>(w, rows, cols, ldw, q, qT,
+                                                                                scales, rule, SrKey{0, 0});
+    }
     return cudaGetLastError();
 }
 

@@ -222,6 +222,34 @@ FP8BS_API fp8bs_status fp8_quant_dual_opts(const void* x, int64_t rows, int64_t 
                                            uint8_t* q, float* scales, uint8_t* qT, float* scalesT,
                                            const fp8bs_scale_opts* opts, void* stream);
 
+/* NEXT-3: stochastic rounding. The 1x128 and 128x128 casts above with the   */
+/* E4M3 rounding step made stochastic under a stateless (seed, salt,         */
+/* element) contract ([P4] "SR agreement": a stateless seed / salt / counter */
+/* scheme with a lower / upper-magnitude rule; [P4] "Remaining differences"  */
+/* and the PR text name a Philox helper). The pages do not print the         */
+/* contract's layout; this library's reading:                               */
+/*   word(idx) = word idx % 4 of Philox4x32-10 (Salmon et al., SC 2011) with */
+/*               key (seed & 0xffffffff, seed >> 32) and counter            */
+/*               (idx / 4 low 32 bits, idx / 4 high 32 bits, salt, 0),      */
+/*               idx = the element's linear index in the logical tensor     */
+/*               (row * cols + col; for batched weights,                    */
+/*               b * rows * cols + row * cols + col);                       */
+/*   x = fp32(v / s) as in the round-to-nearest cast; with L <= |x| < U the  */
+/*   neighbouring E4M3 magnitudes, F = floor(2^20 (|x| - L) / (U - L));      */
+/*   the code is U if F > (word >> 12), else L; |x| >= 448 gives 448; the    */
+/*   sign (and a signed zero) is x's.                                         */
+/* Results depend only on (input, seed, salt), not on the launch or device.  */
+/* Scales are computed exactly as in the round-to-nearest cast (opts as      */
+/* above, NULL = default rule); the transposed qT of the 128x128 cast is the */
+/* transpose of the stochastically rounded q.                                */
+FP8BS_API fp8bs_status fp8_quant_1x128_sr(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                                          uint8_t* q, float* scales, uint64_t seed, uint32_t salt,
+                                          const fp8bs_scale_opts* opts, void* stream);
+FP8BS_API fp8bs_status fp8_quant_128x128_sr(const void* w, int64_t batch, int64_t rows, int64_t cols,
+                                            int64_t ldw, uint8_t* q, uint8_t* qT, float* scales,
+                                            uint64_t seed, uint32_t salt,
+                                            const fp8bs_scale_opts* opts, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* S4-S6. Block-scaled E4M3 GEMMs with per-128-K fp32 promotion              */
 /* [P1] bullet 1 (all three GEMMs E4M3; BF16 activations and input grads,     */

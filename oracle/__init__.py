@@ -41,6 +41,8 @@ FAULT_RECIPROCAL = 7
 FAULT_SIGN_FLIP_TERM = 8
 FAULT_UE8M0_DOWN = 9
 FAULT_FLOOR_AFTER = 10
+FAULT_SR_WORD = 11
+FAULT_SR_NEAREST = 12
 
 
 def build(force: bool = False) -> str:
@@ -98,6 +100,14 @@ def _load():
         lib.oracle_set_num_threads.argtypes = [I]
         lib.oracle_set_fault.argtypes = [I]
         lib.oracle_set_scale_rule.argtypes = [I, ctypes.c_float, ctypes.c_float]
+        U32, U64 = ctypes.c_uint32, ctypes.c_uint64
+        lib.oracle_philox4x32_10.argtypes = [P, P, P]
+        lib.oracle_sr_word.argtypes = [U64, U32, U64]
+        lib.oracle_sr_word.restype = U32
+        lib.oracle_e4m3_encode_sr.argtypes = [ctypes.c_float, U32]
+        lib.oracle_e4m3_encode_sr.restype = ctypes.c_uint8
+        lib.oracle_quant_1x128_sr.argtypes = [P, I64, I64, I64, P, I64, P, I64, I64, U64, U32]
+        lib.oracle_quant_128x128_sr.argtypes = [P, I64, I64, I64, P, I64, P, I64, U64, U32, I64]
         _lib = lib
         return lib
 
@@ -216,6 +226,46 @@ def quant_128x128(w_bf16: np.ndarray):
     q = np.empty((R, C), np.uint8)
     sc = np.zeros(((R + 127) // 128, (C + 127) // 128), np.float32)
     _load().oracle_quant_128x128(_p(w), R, C, C, _p(q), C, _p(sc), sc.shape[1])
+    return q, sc
+
+
+def philox4x32_10(counter, key):
+    """Philox4x32-10 of a 4-word counter and 2-word key -> 4 words."""
+    c = np.ascontiguousarray(counter, dtype=np.uint32)
+    k = np.ascontiguousarray(key, dtype=np.uint32)
+    out = np.zeros(4, np.uint32)
+    _load().oracle_philox4x32_10(_p(c), _p(k), _p(out))
+    return out
+
+
+def sr_word(seed: int, salt: int, idx: int) -> int:
+    return int(_load().oracle_sr_word(int(seed), int(salt), int(idx)))
+
+
+def e4m3_encode_sr(x: float, r: int) -> int:
+    return int(_load().oracle_e4m3_encode_sr(float(x), int(r)))
+
+
+def quant_1x128_sr(x_bf16: np.ndarray, seed: int, salt: int = 0):
+    """quant_1x128 with stochastic rounding (tile-major scales)."""
+    x = _c(x_bf16, np.uint16)
+    R, C = x.shape
+    nt = (C + 127) // 128
+    q = np.empty((R, C), np.uint8)
+    rp = scale_rows_padded(R)
+    sc = np.zeros((nt, rp), np.float32)
+    _load().oracle_quant_1x128_sr(_p(x), R, C, C, _p(q), C, _p(sc), 1, rp, int(seed), int(salt))
+    return q, sc
+
+
+def quant_128x128_sr(w_bf16: np.ndarray, seed: int, salt: int = 0, idx_base: int = 0):
+    """quant_128x128 with stochastic rounding; element indices start at idx_base."""
+    w = _c(w_bf16, np.uint16)
+    R, C = w.shape
+    q = np.empty((R, C), np.uint8)
+    sc = np.zeros(((R + 127) // 128, (C + 127) // 128), np.float32)
+    _load().oracle_quant_128x128_sr(_p(w), R, C, C, _p(q), C, _p(sc), sc.shape[1], int(seed), int(salt),
+                                    int(idx_base))
     return q, sc
 
 

@@ -71,7 +71,9 @@ enum {
     FAULT_RECIPROCAL = 7,        /* v * (1/s) instead of v / s */
     FAULT_SIGN_FLIP_TERM = 8,    /* one K-block's term subtracted */
     FAULT_UE8M0_DOWN = 9,        /* UE8M0 scale rounded down, not up */
-    FAULT_FLOOR_AFTER = 10       /* amax floor applied to s instead of amax */
+    FAULT_FLOOR_AFTER = 10,      /* amax floor applied to s instead of amax */
+    FAULT_SR_WORD = 11,          /* SR takes the next Philox output word */
+    FAULT_SR_NEAREST = 12        /* SR rounds to nearest instead */
 };
 static int g_fault = FAULT_NONE;
 
@@ -169,6 +171,77 @@ void oracle_f32_to_bf16_array(const float* in, i64 n, uint16_t* out)
 }
 
 /* ------------------------------------------------------------------------- */
+/* Stochastic rounding to E4M3.                                               */
+/* ------------------------------------------------------------------------- */
+
+/* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
+ * as 1, 2, 3", SC 2011): ten rounds on a 4-word counter with a 2-word key;
+ * each round multiplies words 0 and 2 by the round multipliers, keeps both
+ * halves of the 64-bit products and mixes them with words 1 and 3 and the
+ * key; the key grows by the Weyl constants between rounds. */
+void oracle_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4])
+{
+    uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint32_t k0 = key_in[0], k1 = key_in[1];
+    for (int round = 0; round < 10; ++round) {
+        uint64_t p0 = (uint64_t)0xD2511F53u * (uint64_t)c0;
+        uint64_t p1 = (uint64_t)0xCD9E8D57u * (uint64_t)c2;
+        uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+        uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+        c0 = hi1 ^ c1 ^ k0;
+        c1 = lo1;
+        c2 = hi0 ^ c3 ^ k1;
+        c3 = lo0;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* The random word of element `idx` (its linear index in the quantized
+ * tensor) under (seed, salt): Philox4x32-10 with key (seed low word, seed
+ * high word) and counter (low and high words of idx / 4, salt, 0); element
+ * idx takes output word idx % 4. Stateless: the word depends on nothing else
+ * (tile shape, launch, thread). This contract is this repository's reading;
+ * the pages name a stateless seed / salt / counter scheme without its
+ * layout. */
+uint32_t oracle_sr_word(uint64_t seed, uint32_t salt, uint64_t idx)
+{
+    uint64_t blk = idx / 4;
+    uint32_t ctr[4] = {(uint32_t)blk, (uint32_t)(blk >> 32), salt, 0u};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t out[4];
+    oracle_philox4x32_10(ctr, key, out);
+    int w = (int)(idx % 4);
+    if (g_fault == FAULT_SR_WORD) w = (w + 1) % 4;
+    return out[w];
+}
+
+/* Stochastic rounding of an fp32 quotient x to E4M3 with the random word r:
+ * with L the largest E4M3 magnitude <= |x| and U the next one, the fraction
+ * f = (|x| - L) / (U - L) in [0, 1) is cut to 20 bits, F = floor(f * 2^20),
+ * and the result is U when F > (r >> 12), else L (so P(U) = F / 2^20). The
+ * sign is x's (a zero result keeps it); |x| >= 448 gives 448. */
+uint8_t oracle_e4m3_encode_sr(float x, uint32_t r)
+{
+    build_table();
+    if (g_fault == FAULT_SR_NEAREST) return oracle_e4m3_encode(x);
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    int lo = 0, hi = 0x7E;               /* g_dec[lo] <= a < g_dec[hi] */
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if ((double)g_dec[mid] <= a) lo = mid; else hi = mid;
+    }
+    double L = g_dec[lo], U = g_dec[lo + 1];
+    double f = (a - L) / (U - L);        /* exact: a, L, U are short dyadic numbers */
+    uint32_t F = (uint32_t)floor(f * 1048576.0);
+    int c = (F > (r >> 12)) ? lo + 1 : lo;
+    return (uint8_t)(sign | c);
+}
+
+/* ------------------------------------------------------------------------- */
 /* One quantization tile: amax, scale, codes.                                 */
 /* ------------------------------------------------------------------------- */
 
@@ -229,6 +302,62 @@ static void tile_encode(const float* v, int n, float s, uint8_t* out, i64 out_st
     for (int i = 0; i < n; ++i) {
         float quot = (g_fault == FAULT_RECIPROCAL) ? v[i] * (1.0f / s) : v[i] / s;
         out[i * out_step] = oracle_e4m3_encode(quot);
+    }
+}
+
+/* tile_encode with stochastic rounding: element i's linear index in the
+ * tensor is idx0 + i * idx_step. */
+static void tile_encode_sr(const float* v, int n, float s, uint8_t* out, i64 out_step,
+                           uint64_t seed, uint32_t salt, i64 idx0, i64 idx_step)
+{
+    for (int i = 0; i < n; ++i) {
+        float quot = v[i] / s;
+        uint32_t r = oracle_sr_word(seed, salt, (uint64_t)(idx0 + (i64)i * idx_step));
+        out[i * out_step] = oracle_e4m3_encode_sr(quot, r);
+    }
+}
+
+/* S1 with stochastic rounding (element index r * cols + c). */
+void oracle_quant_1x128_sr(const uint16_t* x, i64 rows, i64 cols, i64 ldx,
+                           uint8_t* q, i64 ldq, float* sc, i64 sc_rs, i64 sc_ts,
+                           uint64_t seed, uint32_t salt)
+{
+    i64 ntiles = (cols + 127) / 128;
+#pragma omp parallel for schedule(static)
+    for (i64 r = 0; r < rows; ++r) {
+        float v[128];
+        for (i64 t = 0; t < ntiles; ++t) {
+            i64 c0 = t * 128;
+            int n = (int)((cols - c0) < 128 ? (cols - c0) : 128);
+            for (int i = 0; i < n; ++i) v[i] = bf16_to_f32(x[r * ldx + c0 + i]);
+            float s = tile_scale(v, n);
+            sc[r * sc_rs + t * sc_ts] = s;
+            tile_encode_sr(v, n, s, q + r * ldq + c0, 1, seed, salt, r * cols + c0, 1);
+        }
+    }
+}
+
+/* S2 with stochastic rounding (element index idx_base + r * cols + c). */
+void oracle_quant_128x128_sr(const uint16_t* x, i64 rows, i64 cols, i64 ldx,
+                             uint8_t* q, i64 ldq, float* sc, i64 ldsc,
+                             uint64_t seed, uint32_t salt, i64 idx_base)
+{
+    i64 nbr = (rows + 127) / 128, nbc = (cols + 127) / 128;
+#pragma omp parallel for schedule(static)
+    for (i64 blk = 0; blk < nbr * nbc; ++blk) {
+        i64 bi = blk / nbc, bj = blk % nbc;
+        i64 r0 = bi * 128, c0 = bj * 128;
+        int nr = (int)((rows - r0) < 128 ? (rows - r0) : 128);
+        int nc = (int)((cols - c0) < 128 ? (cols - c0) : 128);
+        float v[128 * 128];
+        for (int i = 0; i < nr; ++i)
+            for (int j = 0; j < nc; ++j)
+                v[i * nc + j] = bf16_to_f32(x[(r0 + i) * ldx + c0 + j]);
+        float s = tile_scale(v, nr * nc);
+        sc[bi * ldsc + bj] = s;
+        for (int i = 0; i < nr; ++i)
+            tile_encode_sr(v + i * nc, nc, s, q + (r0 + i) * ldq + c0, 1, seed, salt,
+                           idx_base + (r0 + i) * cols + c0, 1);
     }
 }
 

@@ -314,3 +314,47 @@ def test_scale_rule_rejects_bad_options():
     for bad in (dict(rule=7), dict(amax_floor=-1.0), dict(scale_floor=float("nan"))):
         with pytest.raises(fp8bs.Fp8bsError):
             fp8bs.fp8_quant_1x128(x, q, sc, **bad)
+
+
+@pytest.mark.parametrize("R,C,seed,salt", [(300, 384, 0, 0), (129, 2048, 2 ** 40 + 17, 3), (1, 16, 7, 0xFFFFFFFF)])
+def test_sr_quant_1x128_matches_oracle(R, C, seed, salt):
+    """NEXT-3: stochastic rounding under (seed, salt), byte- and bit-exact
+    against the oracle's independent Philox4x32-10 and rounding rule."""
+    x = _special_inputs(R, C, seed=R + C + 5)
+    q, sc = fp8bs.empty_quant_1x128(R, C)
+    fp8bs.fp8_quant_1x128_sr(x.cuda(), q, sc, seed=seed, salt=salt)
+    torch.cuda.synchronize()
+    oq, osc = oracle.quant_1x128_sr(u16(x), seed=seed, salt=salt)
+    assert np.array_equal(np_(q), oq)
+    assert np.array_equal(np_(sc)[:, :R].view(np.uint32), osc[:, :R].view(np.uint32))
+
+
+def test_sr_quant_128x128_batched_matches_oracle():
+    w = wl.normal((3, 256, 384), std=wl.W_STD, seed=41)
+    w[1, :128, :128] = 0.0
+    q, qT, sc = fp8bs.empty_quant_128x128(256, 384, batch=3)
+    fp8bs.fp8_quant_128x128_sr(w.cuda(), q, qT, sc, seed=99, salt=5)
+    torch.cuda.synchronize()
+    for e in range(3):
+        oq, osc = oracle.quant_128x128_sr(u16(w[e]), seed=99, salt=5, idx_base=e * 256 * 384)
+        assert np.array_equal(np_(q)[e], oq)
+        assert np.array_equal(np_(qT)[e], oq.T)
+        assert np.array_equal(np_(sc)[e].view(np.uint32), osc.view(np.uint32))
+
+
+def test_sr_full_size_and_statistics():
+    """The dense activation in full under SR equals the oracle, differs from
+    round-to-nearest on a sizeable fraction of elements, and another salt
+    gives another draw."""
+    x = wl.dense(K=7168, M=1024, N=128)["X"]
+    R, C = x.shape
+    q, sc = fp8bs.empty_quant_1x128(R, C)
+    fp8bs.fp8_quant_1x128_sr(x.cuda(), q, sc, seed=2024, salt=1)
+    q2, _ = fp8bs.empty_quant_1x128(R, C)
+    fp8bs.fp8_quant_1x128_sr(x.cuda(), q2, sc, seed=2024, salt=2)
+    torch.cuda.synchronize()
+    oq, _ = oracle.quant_1x128_sr(u16(x), seed=2024, salt=1)
+    assert np.array_equal(np_(q), oq)
+    rn, _ = oracle.quant_1x128(u16(x))
+    assert 0.2 < np.mean(np_(q) != rn) < 0.6
+    assert np.mean(np_(q) != np_(q2)) > 0.2

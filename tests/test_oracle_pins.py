@@ -309,6 +309,76 @@ def test_scale_floors_closed_forms():
     assert np.all(s_u == np.float32(2.0 ** -22))
 
 
+def test_philox_known_answers():
+    for row in _golden("philox4x32_10_kat.txt"):
+        w = [int(v, 16) for v in row]
+        assert list(oracle.philox4x32_10(w[0:4], w[4:6])) == w[6:10]
+
+
+def _sr_example_row():
+    x = np.zeros((1, 128), np.float32)
+    x[0, :4] = 1.0625
+    x[0, 127] = 448.0
+    return oracle.f32_to_bf16(x)
+
+
+def test_sr_worked_example():
+    q, sc = oracle.quant_1x128_sr(_sr_example_row(), seed=0, salt=0)
+    assert sc[0, 0] == 1.0
+    want = {int(r[0]): int(r[1], 16) for r in _golden("sr_worked_example.txt")}
+    assert {i: int(q[0, i]) for i in want} == want
+    assert q[0, 127] == 0x7E
+
+
+def test_sr_rule_properties():
+    """Values on the E4M3 grid never move; off the grid the result flips from
+    the upper to the lower neighbour exactly where the 20-bit fraction stops
+    exceeding the random word's top 20 bits; |x| >= 448 saturates; signs and
+    signed zeros are kept; the subnormal range uses the 2^-9 grid."""
+    t = oracle.e4m3_table()
+    rng = np.random.default_rng(3)
+    for c in list(range(0x00, 0x7F)):
+        for r in rng.integers(0, 2 ** 32, 4, dtype=np.uint64):
+            assert oracle.e4m3_encode_sr(float(t[c]), int(r)) == c
+            assert oracle.e4m3_encode_sr(-float(t[c]), int(r)) == (c | 0x80)
+    # 1 + 3/8 * 2^-3: between 1.0 (0x38) and 1.125 (0x39), F = 0.375 * 2^20
+    x = 1.0 + 0.375 * 0.125
+    F = int(0.375 * 2 ** 20)
+    assert oracle.e4m3_encode_sr(x, (F - 1) << 12) == 0x39
+    assert oracle.e4m3_encode_sr(x, F << 12) == 0x38
+    assert oracle.e4m3_encode_sr(-x, 0) == 0xB9
+    # subnormal range: 2.5 * 2^-9 lies between codes 2 and 3 with F = 2^19
+    y = 2.5 * 2.0 ** -9
+    assert oracle.e4m3_encode_sr(y, ((1 << 19) - 1) << 12) == 0x03
+    assert oracle.e4m3_encode_sr(y, (1 << 19) << 12) == 0x02
+    # below the smallest subnormal, including signed zeros
+    assert oracle.e4m3_encode_sr(-1e-30, 0xFFFFFFFF) == 0x80
+    assert oracle.e4m3_encode_sr(-0.0, 0) == 0x80
+    assert oracle.e4m3_encode_sr(1000.0, 0) == 0x7E and oracle.e4m3_encode_sr(-449.0, 0) == 0xFE
+
+
+def test_sr_is_unbiased():
+    """E[dec(q)] equals the quotient up to the 2^-20 cut of the fraction: the
+    mean over 4096 rows (independent counters) of one row pattern stays within
+    five standard errors of each value."""
+    R = 4096
+    vals = np.array([1.0625, 1.03, 0.3, -5.7, 100.2, 0.004, -0.0011, 447.0], np.float32)
+    x = np.zeros((R, 128), np.float32)
+    x[:, :vals.size] = vals
+    x[:, 127] = 448.0                                       # scale exactly 1
+    xb = oracle.f32_to_bf16(x)
+    v = oracle.bf16_to_f32(xb)[0, :vals.size].astype(np.float64)
+    q, _ = oracle.quant_1x128_sr(xb, seed=12345, salt=7)
+    t = oracle.e4m3_table().astype(np.float64)
+    mean = t[q[:, :vals.size]].mean(0)
+    for j, xv in enumerate(v):
+        lo = t[:0x7F][t[:0x7F] <= abs(xv)].max()
+        hi = t[:0x7F][t[:0x7F] > abs(xv)].min() if abs(xv) < 448 else lo
+        f = (abs(xv) - lo) / (hi - lo) if hi > lo else 0.0
+        se = np.sqrt(f * (1 - f) / R) * (hi - lo)
+        assert abs(mean[j] - xv) <= 5 * se + (hi - lo) * 2.0 ** -20 + 1e-12, (j, xv, mean[j])
+
+
 def test_quant_reciprocal_case_is_distinguished():
     """A tile where v * (1/s) and v / s round to different E4M3 codes: the
     torch-steps pin must see the true division."""
@@ -573,6 +643,15 @@ def _pin_scale_rules():
         return False
 
 
+def _pin_sr():
+    try:
+        test_sr_worked_example()
+        test_sr_is_unbiased()
+        return True
+    except AssertionError:
+        return False
+
+
 def _pin_gemm():
     return (_check_fprop(130, 384, 256, 21) and _check_dgrad(129, 384, 256, 22)
             and _check_wgrad(300, 256, 128, 23) and _check_fprop(64, 256, 256, 24))
@@ -589,10 +668,12 @@ def _pin_gemm():
     (oracle.FAULT_SIGN_FLIP_TERM, "gemm"),
     (oracle.FAULT_UE8M0_DOWN, "scale_rules"),
     (oracle.FAULT_FLOOR_AFTER, "scale_rules"),
+    (oracle.FAULT_SR_WORD, "sr"),
+    (oracle.FAULT_SR_NEAREST, "sr"),
 ])
 def test_planted_mistake_is_caught(fault, pin):
     check = {"encoder": _pin_encoder, "quant": _pin_quant, "gemm": _pin_gemm,
-             "scale_rules": _pin_scale_rules}[pin]
+             "scale_rules": _pin_scale_rules, "sr": _pin_sr}[pin]
     assert check()
     oracle.set_fault(fault)
     try:
