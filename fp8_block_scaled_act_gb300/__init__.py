@@ -34,6 +34,7 @@ __all__ = [
     "SRC_BF16", "SRC_E4M3", "OP_FPROP", "OP_DGRAD", "OP_WGRAD", "MAX_GROUPS",
     "SCALE_FP32", "SCALE_UE8M0", "ScaleOpts", "fp8_quant_1x128_opts", "fp8_quant_128x128_opts",
     "fp8_requant_128x1_T_opts", "fp8_quant_dual_opts", "fp8_quant_1x128_sr", "fp8_quant_128x128_sr",
+    "fp8bs_mx_scale_bytes", "fp8_mx_quant_1x32", "fp8_mx_gemm", "empty_mx_quant",
 ]
 
 SRC_BF16, SRC_E4M3 = 0, 1
@@ -93,6 +94,9 @@ def lib() -> ctypes.CDLL:
         "fp8_requant_128x1_T_opts": ([I, P, P, I64, I64, P, I32, P, P, P, P], S),
         "fp8_quant_dual_opts": ([P, I64, I64, P, I32, P, P, P, P, P, P], S),
         "fp8_quant_1x128_sr": ([P, I64, I64, I64, P, P, ctypes.c_uint64, ctypes.c_uint32, P, P], S),
+        "fp8bs_mx_scale_bytes": ([I64, I64], I64),
+        "fp8_mx_quant_1x32": ([P, I64, I64, P, P, P], S),
+        "fp8_mx_gemm": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_quant_128x128_sr": ([P, I64, I64, I64, I64, P, P, P, ctypes.c_uint64, ctypes.c_uint32, P, P], S),
         "fp8_block_gemm_fprop": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_block_gemm_dgrad": ([P, P, P, P, I64, I64, I64, P, P], S),
@@ -329,6 +333,40 @@ def fp8_quant_128x128_sr(w, q, qT, scales, seed: int, salt: int = 0, stream=None
     _check("fp8_quant_128x128_sr", lib().fp8_quant_128x128_sr(
         _ptr(w), batch, rows, cols, cols, _ptr(q), _ptr(qT), _ptr(scales), int(seed) & (2 ** 64 - 1),
         int(salt) & 0xFFFFFFFF, _opts(rule, amax_floor, scale_floor), _stream(stream)))
+
+
+def fp8bs_mx_scale_bytes(rows: int, cols: int) -> int:
+    return int(lib().fp8bs_mx_scale_bytes(int(rows), int(cols)))
+
+
+def empty_mx_quant(rows: int, cols: int, device="cuda"):
+    """(q uint8 [rows x cols], scale atoms uint8 [fp8bs_mx_scale_bytes])."""
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=device)
+    sc = torch.empty(max(fp8bs_mx_scale_bytes(rows, cols), 0), dtype=torch.uint8, device=device)
+    return q, sc
+
+
+def fp8_mx_quant_1x32(x, q, scale_atoms, stream=None) -> None:
+    """MXFP8 1x32 quantization of BF16 x [rows x cols] (cols % 128 == 0)."""
+    _need(x, torch.bfloat16, "x"); _need(q, torch.uint8, "q"); _need(scale_atoms, torch.uint8, "scale_atoms")
+    rows, cols = x.shape
+    if q.shape != (rows, cols) or scale_atoms.numel() < fp8bs_mx_scale_bytes(rows, cols):
+        raise ValueError("output shapes do not match empty_mx_quant")
+    _check("fp8_mx_quant_1x32", lib().fp8_mx_quant_1x32(_ptr(x), rows, cols, _ptr(q), _ptr(scale_atoms),
+                                                        _stream(stream)))
+
+
+def fp8_mx_gemm(a, a_atoms, b, b_atoms, out, stream=None) -> None:
+    """out [M x N] (BF16) = A [M x K] . B [N x K]^T, both MXFP8 along K."""
+    for t, n, d in ((a, "a", torch.uint8), (a_atoms, "a_atoms", torch.uint8), (b, "b", torch.uint8),
+                    (b_atoms, "b_atoms", torch.uint8), (out, "out", torch.bfloat16)):
+        _need(t, d, n)
+    M, K = a.shape
+    N = b.shape[0]
+    if b.shape != (N, K) or out.shape != (M, N):
+        raise ValueError("shape mismatch")
+    _check("fp8_mx_gemm", lib().fp8_mx_gemm(_ptr(a), _ptr(a_atoms), _ptr(b), _ptr(b_atoms), M, N, K,
+                                            _ptr(out), _stream(stream)))
 
 
 def _rule_kwargs(opts: Optional[ScaleOpts]) -> dict:

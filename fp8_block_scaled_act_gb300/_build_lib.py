@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libfp8bs.so")
 
-SOURCES = ["api.cu", "quant.cu", "gemm.cu", "splitk_noalloc.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemm.cu", "splitk_noalloc.cu", "mx.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]

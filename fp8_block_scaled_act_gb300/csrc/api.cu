@@ -532,6 +532,49 @@ fp8bs_status fp8_block_gemm_dgrad(const uint8_t* dyq, const float* sdy, const ui
     return run_rowwise_gemm(true, 1, off, dyq, sdy, wq, sw, N, K, dx, stream);
 }
 
+int64_t fp8bs_mx_scale_bytes(int64_t rows, int64_t cols)
+{
+    if (rows < 0 || cols < 0 || cols % 128 != 0) return -1;
+    return (rows + 127) / 128 * (cols / 128) * 512;
+}
+
+fp8bs_status fp8_mx_quant_1x32(const void* x, int64_t rows, int64_t cols, uint8_t* q, uint8_t* scale_atoms,
+                               void* stream)
+{
+    if (rows < 0 || cols <= 0) return FP8BS_ERR_ARG;
+    if (cols % 128 != 0 || rows > 0x7FFFFF00) return FP8BS_ERR_SHAPE;
+    if (rows == 0) return FP8BS_OK;
+    if (!x || !q || !scale_atoms) return FP8BS_ERR_ARG;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(scale_atoms)) return FP8BS_ERR_ALIGN;
+    DeviceState* st = nullptr;
+    fp8bs_status s = device_state(&st);
+    if (s != FP8BS_OK) return s;
+    return launch_status(launch_mx_quant_1x32(static_cast<const uint16_t*>(x), rows, cols, q, scale_atoms,
+                                              st->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+fp8bs_status fp8_mx_gemm(const uint8_t* a, const uint8_t* a_scale_atoms, const uint8_t* b,
+                         const uint8_t* b_scale_atoms, int64_t M, int64_t N, int64_t K, void* out, void* stream)
+{
+    if (M < 0 || N <= 0 || K <= 0) return FP8BS_ERR_ARG;
+    if (K % 128 != 0 || N % 256 != 0 || M > 0x7FFFFF00 || N > 0x7FFFFFFF || K > 0x7FFFFFFF)
+        return FP8BS_ERR_SHAPE;
+    if (M == 0) return FP8BS_OK;
+    if (!a || !a_scale_atoms || !b || !b_scale_atoms || !out) return FP8BS_ERR_ARG;
+    if (!aligned16(a) || !aligned16(a_scale_atoms) || !aligned16(b) || !aligned16(b_scale_atoms) ||
+        !aligned16(out))
+        return FP8BS_ERR_ALIGN;
+    DeviceState* st = nullptr;
+    fp8bs_status s = device_state(&st);
+    if (s != FP8BS_OK) return s;
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, a, K, M, K, kBM) || !make_map(&mb, b, K, N, K, kBN)) return FP8BS_ERR_ARG;
+    return launch_status(launch_mx_gemm(ma, mb, a_scale_atoms, b_scale_atoms, static_cast<int>(M),
+                                        static_cast<int>(N), static_cast<int>(K), static_cast<uint16_t*>(out),
+                                        g_wait_limit_ns, st->status, st->num_sms,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 size_t fp8bs_splitk_workspace_size(int op, int64_t M, int64_t N, int64_t K, int32_t splits)
 {
     if ((op != FP8BS_OP_FPROP && op != FP8BS_OP_DGRAD) || M <= 0 || N <= 0 || K <= 0 || splits <= 1)

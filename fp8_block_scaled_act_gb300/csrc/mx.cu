@@ -1,0 +1,441 @@
+// mx.cu -- MXFP8 (NEXT-2): 1x32 blocks with power-of-two exponent scales,
+// and a GEMM whose block scaling runs in the tensor core.
+//
+// Format (OCP Microscaling Formats (MX) v1.0): 32 consecutive elements along
+// K share one 8-bit exponent scale X = 2^(E - 127); elements are E4M3. The
+// scale is the smallest power of two >= fp32(amax / 448) (X = 1 for an
+// all-zero block), so no element saturates; q = E4M3_RN(v / X), an exact
+// division. This is the B300 practice the TransformerEngine pages benchmark
+// (PR #3573, "Changes" and "Performance": MXFP8 operands for dgrad) next to
+// the software-promoted recipe of the rest of this library.
+//
+// Scale layout ("scale atoms", the layout tcgen05.cp.32x128b.warpx4 takes):
+// for a matrix of R rows (padded to a multiple of 128) and K columns, atom
+// (r / 128, k / 128) is 512 contiguous bytes; inside it the scale of row
+// m = r % 128 = m0 + 32 m1 (m0 < 32) and 32-block j = (k / 32) % 4 sits at
+// byte 16 m0 + 4 m1 + j. Atoms are ordered [R/128][K/128].
+//
+// GEMM: out[i, j] = sum_k A[i, k] B[j, k] with both operands blocked along
+// K (A = activations [M x K], B = the other operand [N x K]), fp32
+// accumulation in tensor memory over the whole K, BF16 output. One CTA per SM,
+// 128 x 256 tiles, a 4-stage TMA ring of (A, B, A scales, B scales); per
+// 128-K stage one thread copies the scales into tensor memory
+// (tcgen05.cp.32x128b.warpx4) and issues four
+// tcgen05.mma.kind::mxf8f6f4.block_scale (K = 32 each, the scale byte of
+// each 32-block selected through the instruction descriptor). The epilogue
+// runs once per tile.
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8bs {
+namespace {
+
+// ---------------------------------------------------------------------------
+// Quantizer: 16 threads per (row, 128-column group); a thread holds 8
+// consecutive columns, so a 32-block is 4 adjacent lanes.
+// ---------------------------------------------------------------------------
+constexpr int kMxQThreads = 256;
+
+__device__ __forceinline__ uint32_t mx_pow2_at_least(float s)
+{
+    // bits of the smallest power of two >= s > 0
+    const uint32_t b = __float_as_uint(s);
+    if ((b & 0x007FFFFFu) == 0u) return b;
+    if ((b >> 23) != 0u) return (b & 0x7F800000u) + 0x00800000u;
+    return 1u << (32 - __clz(b - 1u));
+}
+
+// Exponent byte E of a block with absmax `amax` (X = 2^(E - 127)).
+__device__ __forceinline__ uint32_t mx_scale_byte(float amax)
+{
+    if (amax == 0.0f) return 127u;
+    const uint32_t b = mx_pow2_at_least(__fdiv_rn(amax, 448.0f));
+    int e;
+    if ((b >> 23) != 0u)
+        e = static_cast<int>(b >> 23) - 127;
+    else
+        e = -118 - __clz(b);              // subnormal power of two 2^(31 - clz - 149)
+    int E = e + 127;
+    E = E < 0 ? 0 : (E > 254 ? 254 : E);
+    return static_cast<uint32_t>(E);
+}
+
+__global__ void __launch_bounds__(kMxQThreads) mx_quant_1x32_kernel(
+    const uint16_t* __restrict__ x, int64_t rows, int64_t rows_pad, int64_t cols, uint8_t* __restrict__ q,
+    uint8_t* __restrict__ atoms)
+{
+    const int64_t groups = cols / 128;
+    const int64_t units = rows_pad * groups;
+    const int t = threadIdx.x & 15;
+    int64_t unit = (static_cast<int64_t>(blockIdx.x) * kMxQThreads + threadIdx.x) >> 4;
+    const int64_t stride = (static_cast<int64_t>(gridDim.x) * kMxQThreads) >> 4;
+    for (; unit < units; unit += stride) {
+        const int64_t r = unit / groups;
+        const int64_t g = unit - r * groups;
+        const int64_t c = g * 128 + t * 8;
+        uint4 d = make_uint4(0u, 0u, 0u, 0u);
+        if (r < rows) d = __ldcs(reinterpret_cast<const uint4*>(x + r * cols + c));
+        uint32_t m = __vmaxu2(__vmaxu2(d.x & 0x7FFF7FFFu, d.y & 0x7FFF7FFFu),
+                              __vmaxu2(d.z & 0x7FFF7FFFu, d.w & 0x7FFF7FFFu));
+        m = max(m & 0xFFFFu, m >> 16);
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        const uint32_t E = mx_scale_byte(__uint_as_float(m << 16));
+        // 1 / X = 2^(127 - E): exact, and v * (1 / X) is the exact quotient v / X
+        // (or its correctly rounded value when it falls below the normal range)
+        const float inv = E >= 1u && E <= 253u ? __uint_as_float((254u - E) << 23) : 0.0f;
+        const float X = __uint_as_float(E >= 1u ? (E << 23) : 0x00400000u);   // 2^(E - 127)
+        uint2 o;
+        const uint32_t wd[4] = {d.x, d.y, d.z, d.w};
+        uint32_t code[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float lo = __uint_as_float(wd[k] << 16), hi = __uint_as_float(wd[k] & 0xFFFF0000u);
+            const float qlo = inv != 0.0f ? __fmul_rn(lo, inv) : __fdiv_rn(lo, X);
+            const float qhi = inv != 0.0f ? __fmul_rn(hi, inv) : __fdiv_rn(hi, X);
+            code[k] = cvt_e4m3x2(qlo, qhi);
+        }
+        o.x = code[0] | (code[1] << 16);
+        o.y = code[2] | (code[3] << 16);
+        if (r < rows) *reinterpret_cast<uint2*>(q + r * cols + c) = o;
+        // the four exponent bytes of this (row, 128-column group) are contiguous in the atom
+        const uint32_t e0 = __shfl_sync(0xFFFFFFFFu, E, (threadIdx.x & 16) | 0);
+        const uint32_t e1 = __shfl_sync(0xFFFFFFFFu, E, (threadIdx.x & 16) | 4);
+        const uint32_t e2 = __shfl_sync(0xFFFFFFFFu, E, (threadIdx.x & 16) | 8);
+        const uint32_t e3 = __shfl_sync(0xFFFFFFFFu, E, (threadIdx.x & 16) | 12);
+        if (t == 0) {
+            const int64_t mrow = r & 127;
+            uint8_t* atom = atoms + ((r >> 7) * groups + g) * 512;
+            *reinterpret_cast<uint32_t*>(atom + 16 * (mrow & 31) + 4 * (mrow >> 5)) =
+                e0 | (e1 << 8) | (e2 << 16) | (e3 << 24);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// GEMM
+// ---------------------------------------------------------------------------
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * kBK;              // 16 KB
+constexpr int kBBytes = kBN * kBK;              // 32 KB
+constexpr int kSfaBytes = 512;                  // one atom: 128 rows x 4 blocks
+constexpr int kSfbBytes = 1024;                 // two atoms: 256 rows
+constexpr int kEpiWarps = 8;
+constexpr int kFirstEpiWarp = 4;
+constexpr int kThreads = (kFirstEpiWarp + kEpiWarps) * 32;
+constexpr uint32_t kLaunchRegs = 168;
+constexpr uint32_t kProducerRegs = 40;
+constexpr uint32_t kEpilogueRegs = 232;
+static_assert(128 * kProducerRegs + 256 * kEpilogueRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
+constexpr int kTmemCols = 512;                  // accumulator 256 + scale slots
+constexpr int kSfCol0 = kBN;                    // first scale column
+constexpr int kSfColsPerStage = 12;             // 4 (A) + 8 (B)
+constexpr uint64_t kDrainLimitNs = 1000000000ull;
+constexpr int kCtlBytes = 256;
+constexpr int kSmemBytes = kStages * (kABytes + kBBytes + kSfaBytes + kSfbBytes) + kCtlBytes + 1024;
+
+struct MxCtl {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tfull;
+    uint64_t tempty;
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    volatile int abort;
+};
+
+struct MxParams {
+    const uint8_t* sfa;   // A scale atoms [ceil(M/128)][K/128][512]
+    const uint8_t* sfb;   // B scale atoms [N/128][K/128][512]
+    int m_tiles, n_tiles, kblocks;
+    int M, N;
+    uint16_t* out;        // BF16 [M x N]
+    uint64_t wait_limit_ns;
+    unsigned int* status;
+};
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// Shared-memory descriptor of a scale atom (32 rows of 16 bytes, no swizzle;
+// 8-row core matrices 128 bytes apart).
+__device__ __forceinline__ uint64_t sdesc_atom(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1u) << 16;                 // leading byte offset (one core matrix wide)
+    d |= static_cast<uint64_t>(128u >> 4) << 32;          // stride byte offset: 8 rows x 16 bytes
+    d |= static_cast<uint64_t>(1u) << 46;                 // descriptor version
+    return d;                                             // swizzle: none
+}
+
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with E4M3 A and B (K-major),
+// UE8M0 scales, shape M x N (x 32); sf_id selects the scale byte of the
+// 32-block inside each 32-bit tensor-memory cell.
+__device__ __forceinline__ uint32_t idesc_mx(int M, int N, uint32_t sf_id)
+{
+    return (sf_id << 4)                                   // B scale byte
+           | (0u << 7) | (0u << 10)                       // A, B: E4M3
+           | (static_cast<uint32_t>(N >> 3) << 17)
+           | (1u << 23)                                   // scale format: UE8M0
+           | (static_cast<uint32_t>(M >> 4) << 24)
+           | (sf_id << 29);                               // A scale byte
+}
+
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %6, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void record_status(unsigned int* status, unsigned int code)
+{
+    atomicCAS(status, 0u, code);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                   const __grid_constant__ MxParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = sA + kStages * kABytes;
+    uint8_t* sSfa = sB + kStages * kBBytes;
+    uint8_t* sSfb = sSfa + kStages * kSfaBytes;
+    MxCtl* ctl = reinterpret_cast<MxCtl*>(sSfb + kStages * kSfbBytes);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int total = p.m_tiles * p.n_tiles;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->empty[s], 1);
+        }
+        mbar_init(&ctl->tfull, 1);
+        mbar_init(&ctl->tempty, kEpiWarps);
+        mbar_init(&ctl->mma_done, 1);
+        ctl->abort = 0;
+        fence_mbarrier_init();
+        tma_prefetch_desc(&map_a);
+        tma_prefetch_desc(&map_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(&ctl->tmem_base, kTmemCols);
+        tmem_relinquish();
+        tc_fence_before_sync();
+    }
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = ctl->tmem_base;
+    const uint64_t limit = p.wait_limit_ns;
+    const int64_t kb_atoms = p.kblocks;   // atoms per 128-row group along K
+
+    if (warp < kFirstEpiWarp) setmaxnreg_dec<kProducerRegs>();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const int mt = t / p.n_tiles, nt = t - (t / p.n_tiles) * p.n_tiles;
+                for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+                    const uint32_t s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1u;
+                    if (ctl->abort || !mbar_wait(&ctl->empty[s], ph ^ 1u, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&ctl->full[s], kABytes + kBBytes + kSfaBytes + kSfbBytes);
+                    tma_load_2d(sA + s * kABytes, &map_a, &ctl->full[s], kb * kBK, mt * kBM);
+                    tma_load_2d(sB + s * kBBytes, &map_b, &ctl->full[s], kb * kBK, nt * kBN);
+                    bulk_load(sSfa + s * kSfaBytes, p.sfa + (static_cast<int64_t>(mt) * kb_atoms + kb) * 512,
+                              kSfaBytes, &ctl->full[s]);
+                    bulk_load(sSfb + s * kSfbBytes, p.sfb + (static_cast<int64_t>(2 * nt) * kb_atoms + kb) * 512,
+                              512, &ctl->full[s]);
+                    bulk_load(sSfb + s * kSfbBytes + 512,
+                              p.sfb + (static_cast<int64_t>(2 * nt + 1) * kb_atoms + kb) * 512, 512, &ctl->full[s]);
+                }
+            }
+            if (!ok) {
+                record_status(p.status, FP8BS_ERR_TIMEOUT);
+                ctl->abort = 1;
+            }
+            const uint32_t first = it > kStages ? it - kStages : 0u;
+            const uint64_t drain = limit > kDrainLimitNs ? limit : kDrainLimitNs;
+            for (uint32_t j = first; j < it; ++j)
+                mbar_wait(&ctl->full[j % kStages], (j / kStages) & 1u, drain);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            uint32_t it = 0, tile_it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tile_it) {
+                // the accumulator is free once the epilogue has read the previous tile
+                if (ctl->abort || !mbar_wait(&ctl->tempty, (tile_it & 1u) ^ 1u, limit)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+                    const uint32_t s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1u;
+                    if (ctl->abort || !mbar_wait(&ctl->full[s], ph, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t sf_a = tmem_base + kSfCol0 + s * kSfColsPerStage;
+                    const uint32_t sf_b = sf_a + 4;
+                    tmem_cp_32x128b_x4(sf_a, sdesc_atom(smem_addr(sSfa + s * kSfaBytes)));
+                    tmem_cp_32x128b_x4(sf_b, sdesc_atom(smem_addr(sSfb + s * kSfbBytes)));
+                    tmem_cp_32x128b_x4(sf_b + 4, sdesc_atom(smem_addr(sSfb + s * kSfbBytes + 512)));
+                    const uint64_t adesc = sdesc_kmajor_sw128(smem_addr(sA + s * kABytes));
+                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_addr(sB + s * kBBytes));
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 32; ++kk)
+                        mma_mx(tmem_base, adesc + 2u * kk, bdesc + 2u * kk, idesc_mx(kBM, kBN, kk), sf_a, sf_b,
+                               (kb > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&ctl->empty[s]);
+                }
+                if (!ok) break;
+                mma_commit(&ctl->tfull);
+            }
+            if (!ok) {
+                record_status(p.status, FP8BS_ERR_TIMEOUT);
+                ctl->abort = 1;
+            }
+            mma_commit(&ctl->mma_done);
+            const uint64_t drain = limit > kDrainLimitNs ? limit : kDrainLimitNs;
+            mbar_wait(&ctl->mma_done, 0u, drain);
+        }
+    } else if (warp >= kFirstEpiWarp) {
+        setmaxnreg_inc<kEpilogueRegs>();
+        const int ew = warp - kFirstEpiWarp;
+        const int quarter = warp & 3;
+        const int half = ew >> 2;
+        const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+        uint32_t tile_it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++tile_it) {
+            const int mt = t / p.n_tiles, nt = t - (t / p.n_tiles) * p.n_tiles;
+            if (ctl->abort || !mbar_wait(&ctl->tfull, tile_it & 1u, limit)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const int row = mt * kBM + quarter * 32 + lane;
+            const int col0 = nt * kBN + half * 128;
+            uint32_t ra[32], rb[32];
+            uint32_t pk[64];
+            tmem_ld_x32(tmem_base + lane_addr + half * 128, ra);
+            tmem_ld_x32(tmem_base + lane_addr + half * 128 + 32, rb);
+            tmem_ld_wait(ra);
+            tmem_ld_wait(rb);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                pk[i] = pack_bf16x2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));
+                pk[16 + i] = pack_bf16x2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1]));
+            }
+            tmem_ld_x32(tmem_base + lane_addr + half * 128 + 64, ra);
+            tmem_ld_x32(tmem_base + lane_addr + half * 128 + 96, rb);
+            tmem_ld_wait(ra);
+            tmem_ld_wait(rb);
+            // the accumulator is in registers: hand it back to the MMA issuer
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->tempty);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                pk[32 + i] = pack_bf16x2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));
+                pk[48 + i] = pack_bf16x2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1]));
+            }
+            if (row < p.M && col0 < p.N) {
+                uint4* y = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(row) * p.N + col0);
+#pragma unroll
+                for (int v = 0; v < 16; ++v) y[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
+        }
+        if (!ok) {
+            record_status(p.status, FP8BS_ERR_TIMEOUT);
+            ctl->abort = 1;
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_mx_quant_1x32(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* q, uint8_t* atoms,
+                                 int num_sms, cudaStream_t stream)
+{
+    const int64_t rows_pad = (rows + 127) / 128 * 128;
+    const int64_t units = rows_pad * (cols / 128);
+    if (units == 0) return cudaSuccess;
+    int64_t blocks = (units * 16 + kMxQThreads - 1) / kMxQThreads;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 64;
+    if (blocks > cap) blocks = cap;
+    mx_quant_1x32_kernel<<<static_cast<unsigned>(blocks), kMxQThreads, 0, stream>>>(x, rows, rows_pad, cols, q,
+                                                                                    atoms);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mx_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const uint8_t* sfa,
+                           const uint8_t* sfb, int M, int N, int K, uint16_t* out, uint64_t wait_limit_ns,
+                           unsigned int* status, int num_sms, cudaStream_t stream)
+{
+    static_assert(sizeof(MxCtl) <= kCtlBytes, "control block");
+    MxParams p;
+    p.sfa = sfa;
+    p.sfb = sfb;
+    p.m_tiles = (M + kBM - 1) / kBM;
+    p.n_tiles = N / kBN;
+    p.kblocks = K / kBK;
+    p.M = M;
+    p.N = N;
+    p.out = out;
+    p.wait_limit_ns = wait_limit_ns;
+    p.status = status;
+    const int total = p.m_tiles * p.n_tiles;
+    if (total == 0) return cudaSuccess;
+    auto kernel = mx_gemm_kernel;
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, kernel);
+    if (e != cudaSuccess) return e;
+    if (static_cast<uint32_t>(attr.numRegs) != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = total < num_sms ? total : num_sms;
+    kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_a, map_b, p);
+    return cudaGetLastError();
+}
+
+}  // namespace fp8bs

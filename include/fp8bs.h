@@ -356,6 +356,35 @@ FP8BS_API fp8bs_status fp8_block_gemm_splitk_noalloc(int op, const uint8_t* a, c
                                            int64_t M, int64_t N, int64_t K, int32_t splits,
                                            void* out, void* stream);
 
+/* NEXT-2: MXFP8, the format TransformerEngine's pages benchmark on B300    */
+/* ([P3] "Changes" and "Performance": MXFP8 operands for dgrad): OCP MX v1.0 */
+/* blocks of 32 elements along K with one 8-bit exponent scale              */
+/* X = 2^(E - 127) each, E4M3 elements, and the block scaling applied by the */
+/* tensor core. Scale choice (a reading; the pages do not print it): X = the */
+/* smallest power of two >= fp32(amax / 448), X = 1 for an all-zero block;   */
+/* q = E4M3_RN(v / X), an exact division.                                     */
+/*                                                                           */
+/* Scale atoms: for R rows (padded up to a multiple of 128) and K columns    */
+/* (K % 128 == 0), atom (r/128, k/128) is 512 contiguous bytes ordered       */
+/* [R/128][K/128]; the byte of row m = r % 128 = m0 + 32 m1 (m0 < 32) and    */
+/* 32-block j = (k/32) % 4 is at 16 m0 + 4 m1 + j. Padding rows hold 127.    */
+FP8BS_API int64_t fp8bs_mx_scale_bytes(int64_t rows, int64_t cols);
+
+/* x: BF16 [rows x cols] dense, cols % 128 == 0. q: E4M3 [rows x cols].      */
+/* scale_atoms: fp8bs_mx_scale_bytes(rows, cols) bytes, 16-byte aligned.     */
+FP8BS_API fp8bs_status fp8_mx_quant_1x32(const void* x, int64_t rows, int64_t cols, uint8_t* q,
+                                         uint8_t* scale_atoms, void* stream);
+
+/* out[i, j] = sum_k A[i, k] B[j, k] (dequantized by the block scales), fp32 */
+/* accumulation over all of K, BF16 output [M x N]. A: [M x K] with its      */
+/* atoms (fp8_mx_quant_1x32 of the activations), B: [N x K] with its atoms   */
+/* (fp8_mx_quant_1x32 of the other operand with K contiguous, e.g. W^T for   */
+/* Fprop). K % 128 == 0, N % 256 == 0. No per-128-K promotion: this is the   */
+/* MX recipe, not the one above.                                              */
+FP8BS_API fp8bs_status fp8_mx_gemm(const uint8_t* a, const uint8_t* a_scale_atoms,
+                                   const uint8_t* b, const uint8_t* b_scale_atoms,
+                                   int64_t M, int64_t N, int64_t K, void* out, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* S7. Grouped (MoE expert) GEMMs                                             */
 /* The dense definitions above applied to each group (expert) g, whose token  */

@@ -108,6 +108,8 @@ def _load():
         lib.oracle_e4m3_encode_sr.restype = ctypes.c_uint8
         lib.oracle_quant_1x128_sr.argtypes = [P, I64, I64, I64, P, I64, P, I64, I64, U64, U32]
         lib.oracle_quant_128x128_sr.argtypes = [P, I64, I64, I64, P, I64, P, I64, U64, U32, I64]
+        lib.oracle_mx_quant_1x32.argtypes = [P, I64, I64, P, P]
+        lib.oracle_mx_gemm.argtypes = [P, P, P, P, I64, I64, I64, P, P, P, I64]
         _lib = lib
         return lib
 
@@ -267,6 +269,35 @@ def quant_128x128_sr(w_bf16: np.ndarray, seed: int, salt: int = 0, idx_base: int
     _load().oracle_quant_128x128_sr(_p(w), R, C, C, _p(q), C, _p(sc), sc.shape[1], int(seed), int(salt),
                                     int(idx_base))
     return q, sc
+
+
+def mx_quant_1x32(x_bf16: np.ndarray):
+    """MXFP8 1x32 blocks along the rows of x [R x C] (C % 32 == 0).
+    Returns (q uint8 [R x C], exponent bytes uint8 [R x C/32])."""
+    x = _c(x_bf16, np.uint16)
+    R, C = x.shape
+    assert C % 32 == 0
+    q = np.empty((R, C), np.uint8)
+    sc = np.empty((R, C // 32), np.uint8)
+    _load().oracle_mx_quant_1x32(_p(x), R, C, _p(q), _p(sc))
+    return q, sc
+
+
+def mx_gemm(a, sa, b, sb, ii=None, jj=None):
+    """MXFP8 GEMM of A [M x K] and B [N x K] (both 1x32-blocked along K):
+    fp32 [M x N] (or the sampled elements)."""
+    a, b = _c(a, np.uint8), _c(b, np.uint8)
+    sa, sb = _c(sa, np.uint8), _c(sb, np.uint8)
+    M, K = a.shape
+    N = b.shape[0]
+    if ii is None:
+        out = np.empty((M, N), np.float32)
+        _load().oracle_mx_gemm(_p(a), _p(sa), _p(b), _p(sb), M, N, K, _p(out), None, None, 0)
+    else:
+        ii, jj = _c(ii, np.int64), _c(jj, np.int64)
+        out = np.empty(ii.size, np.float32)
+        _load().oracle_mx_gemm(_p(a), _p(sa), _p(b), _p(sb), M, N, K, _p(out), _p(ii), _p(jj), ii.size)
+    return out
 
 
 def padded_tokens(rows: int, offsets=None) -> int:

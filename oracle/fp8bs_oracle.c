@@ -405,6 +405,78 @@ void oracle_quant_128x128(const uint16_t* x, i64 rows, i64 cols, i64 ldx,
     }
 }
 
+/* ------------------------------------------------------------------------- */
+/* MXFP8 (NEXT-2): 1x32 blocks with power-of-two (UE8M0) scales.              */
+/* ------------------------------------------------------------------------- */
+
+/* OCP Microscaling Formats (MX) v1.0: a block of 32 consecutive elements
+ * along K shares one 8-bit exponent scale X = 2^(E - 127); elements are E4M3.
+ * Scale choice (this repository's reading, the same power-of-two rule as the
+ * UE8M0 option of the 1x128 casts; the MX spec's own floor(log2 amax) - 8
+ * rule can saturate the block maximum): X = the smallest power of two
+ * >= fp32(amax / 448), X = 1 for an all-zero block; q = E4M3_RN(v / X), exact
+ * division. Scales are returned as exponent bytes E, row-major
+ * [rows x cols/32]. */
+static uint8_t mx_scale_byte(float amax)
+{
+    if (amax == 0.0f) return 127;
+    float s = pow2_at_least(amax / 448.0f);
+    int e;
+    frexpf(s, &e);                        /* s = 0.5 * 2^e = 2^(e - 1) */
+    int E = (e - 1) + 127;
+    if (E < 0) E = 0;
+    if (E > 254) E = 254;
+    return (uint8_t)E;
+}
+
+void oracle_mx_quant_1x32(const uint16_t* x, i64 rows, i64 cols, uint8_t* q, uint8_t* sc)
+{
+    build_table();
+    i64 nb = cols / 32;
+#pragma omp parallel for schedule(static)
+    for (i64 r = 0; r < rows; ++r) {
+        for (i64 b = 0; b < nb; ++b) {
+            float v[32], amax = 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                v[i] = bf16_to_f32(x[r * cols + b * 32 + i]);
+                if (fabsf(v[i]) > amax) amax = fabsf(v[i]);
+            }
+            uint8_t E = mx_scale_byte(amax);
+            sc[r * nb + b] = E;
+            float s = ldexpf(1.0f, (int)E - 127);
+            for (int i = 0; i < 32; ++i) q[r * cols + b * 32 + i] = oracle_e4m3_encode(v[i] / s);
+        }
+    }
+}
+
+/* MXFP8 GEMM: out[i, j] = sum_k dec(a[i, k]) 2^(Ea[i, k/32] - 127) *
+ * dec(b[j, k]) 2^(Eb[j, k/32] - 127), with A [M x K] and B [N x K] both
+ * blocked along K; accumulated in fp64 (every product is exact; the sum is
+ * rounded once, to fp32, at the end). If ii/jj are given, only those n
+ * elements are computed (out[e] for (ii[e], jj[e])); else all M x N. */
+void oracle_mx_gemm(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                    i64 M, i64 N, i64 K, float* out, const i64* ii, const i64* jj, i64 n)
+{
+    build_table();
+    i64 nb = K / 32;
+    i64 total = ii ? n : M * N;
+#pragma omp parallel for schedule(static)
+    for (i64 e = 0; e < total; ++e) {
+        i64 i = ii ? ii[e] : e / N;
+        i64 j = ii ? jj[e] : e % N;
+        double acc = 0.0;
+        for (i64 blk = 0; blk < nb; ++blk) {
+            double part = 0.0;
+            for (int t = 0; t < 32; ++t) {
+                i64 k = blk * 32 + t;
+                part += (double)g_dec[a[i * K + k]] * (double)g_dec[b[j * K + k]];
+            }
+            acc += part * ldexp(1.0, (int)sa[i * nb + blk] - 127) * ldexp(1.0, (int)sb[j * nb + blk] - 127);
+        }
+        out[e] = (float)acc;
+    }
+}
+
 /* Number of token columns the transposed output holds: each group's token
  * count rounded up to a whole number of 128-token tiles. */
 i64 oracle_padded_tokens(const int32_t* offsets, int groups, i64 rows)

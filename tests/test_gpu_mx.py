@@ -1,0 +1,91 @@
+"""GPU parity of the MXFP8 path (NEXT-2) against the oracle: the 1x32
+quantizer byte for byte (codes and exponent bytes, read back from the scale
+atoms), and the hardware block-scaled GEMM within the GEMM tolerance
+|d| <= 2e-3 * sum_k |a_k b_k| + 1e-6 plus one BF16 ulp."""
+import numpy as np
+import pytest
+import torch
+
+import fp8_block_scaled_act_gb300 as fp8bs
+import oracle
+import workloads as wl
+from parity import assert_gemm_close, bf16_values, np_, sample_indices, u16
+from test_gpu_quant import _special_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    fp8bs.build()
+    fp8bs.lib()
+    torch.cuda.init()
+    yield
+    assert fp8bs.fp8bs_device_status(reset=True) == 0
+
+
+def atoms_to_rows(atoms: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    """Exponent bytes [rows x cols/32] from the scale-atom layout."""
+    kb = cols // 128
+    a = atoms[: (rows + 127) // 128 * kb * 512].reshape(-1, kb, 32, 4, 4)   # [r128][kb][m0][m1][j]
+    a = a.transpose(0, 3, 2, 1, 4).reshape(-1, kb * 4)                      # row = 128 r128 + 32 m1 + m0
+    return a[:rows]
+
+
+def mx_quant(x_cpu):
+    R, C = x_cpu.shape
+    q, at = fp8bs.empty_mx_quant(R, C)
+    fp8bs.fp8_mx_quant_1x32(x_cpu.cuda(), q, at)
+    torch.cuda.synchronize()
+    return q, at
+
+
+@pytest.mark.parametrize("R,C", [(1, 128), (5, 256), (300, 384), (129, 1024)])
+def test_mx_quant_matches_oracle(R, C):
+    x = _special_inputs(R, C, seed=R * 3 + C)
+    q, at = mx_quant(x)
+    oq, oe = oracle.mx_quant_1x32(u16(x))
+    assert np.array_equal(np_(q), oq)
+    assert np.array_equal(atoms_to_rows(np_(at), R, C), oe)
+    pad = atoms_to_rows(np_(at), (R + 127) // 128 * 128, C)[R:]
+    assert np.all(pad == 127)
+
+
+def _dequant(q, e):
+    t = oracle.e4m3_table().astype(np.float64)
+    return t[q] * np.repeat(np.ldexp(1.0, e.astype(np.int64) - 127), 32, 1)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (300, 256, 512), (1, 512, 256), (257, 768, 1024)])
+def test_mx_gemm_small(M, N, K):
+    a = wl.with_outliers((M, K), fraction=0.01, seed=M + K)
+    b = wl.normal((N, K), std=wl.W_STD, seed=N + K)
+    qa, aa = mx_quant(a)
+    qb, ab = mx_quant(b)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    fp8bs.fp8_mx_gemm(qa, aa, qb, ab, out)
+    torch.cuda.synchronize()
+    oqa, oea = oracle.mx_quant_1x32(u16(a))
+    oqb, oeb = oracle.mx_quant_1x32(u16(b))
+    ref = oracle.mx_gemm(oqa, oea, oqb, oeb)
+    absprod = np.abs(_dequant(oqa, oea)) @ np.abs(_dequant(oqb, oeb)).T
+    assert_gemm_close(bf16_values(out), ref, absprod, True, f"mx gemm {M}x{N}x{K}")
+
+
+def test_mx_gemm_dense_fprop_sampled():
+    """The dense layer's Fprop in MXFP8: X 4096x7168, W^T 2048x7168."""
+    d = wl.dense()
+    x, wt = d["X"], d["W"].t().contiguous()
+    qa, aa = mx_quant(x)
+    qb, ab = mx_quant(wt)
+    out = torch.empty((4096, 2048), dtype=torch.bfloat16, device="cuda")
+    fp8bs.fp8_mx_gemm(qa, aa, qb, ab, out)
+    torch.cuda.synchronize()
+    oqa, oea = oracle.mx_quant_1x32(u16(x))
+    oqb, oeb = oracle.mx_quant_1x32(u16(wt))
+    assert np.array_equal(np_(qa), oqa) and np.array_equal(np_(qb), oqb)
+    ii, jj = sample_indices(4096, 2048, 8192, seed=3, tiles=((0, 0), (-1, -1)))
+    ref = oracle.mx_gemm(oqa, oea, oqb, oeb, ii, jj)
+    da, db = np.abs(_dequant(oqa, oea)), np.abs(_dequant(oqb, oeb))
+    absprod = np.einsum("ek,ek->e", da[ii], db[jj])
+    assert_gemm_close(bf16_values(out)[ii, jj], ref, absprod, True, "mx dense fprop")

@@ -379,6 +379,47 @@ def test_sr_is_unbiased():
         assert abs(mean[j] - xv) <= 5 * se + (hi - lo) * 2.0 ** -20 + 1e-12, (j, xv, mean[j])
 
 
+def test_mx_quant_scales_and_codes():
+    """MXFP8 (OCP MX v1.0 blocks of 32 with 8-bit exponent scales): each
+    scale 2^(E-127) is the smallest power of two that keeps the block's
+    absmax within 448 (up to the fp32 rounding of amax / 448); a zero block
+    has E = 127; every code is the E4M3 rounding of the exact v / 2^(E-127)."""
+    rng = np.random.default_rng(4)
+    x = (rng.standard_normal((16, 256)) * np.exp(rng.uniform(-8, 8, (16, 1)))).astype(np.float32)
+    x[3, 32:64] = 0.0
+    xb = oracle.f32_to_bf16(x)
+    q, E = oracle.mx_quant_1x32(xb)
+    v = oracle.bf16_to_f32(xb).astype(np.float64).reshape(16, 8, 32)
+    amax = np.abs(v).max(-1)
+    X = np.ldexp(1.0, E.astype(np.int64) - 127)
+    nz = amax > 0
+    assert np.all(E[~nz] == 127)
+    assert np.all(amax[nz] / X[nz] <= 448.0 * (1 + 2.0 ** -23))
+    assert np.all(amax[nz] / (X[nz] / 2) > 448.0 * (1 - 2.0 ** -23))
+    exact = (v / X[..., None]).astype(np.float32)
+    assert np.array_equal(oracle.e4m3_encode_array(exact.ravel()).reshape(16, 256), q)
+
+
+def test_mx_gemm_vs_fp64_dequantized():
+    """The MXFP8 GEMM equals the fp64 product of the dequantized operands up
+    to one fp32 rounding."""
+    rng = np.random.default_rng(5)
+    M, N, K = 48, 40, 512
+    a = oracle.f32_to_bf16(rng.standard_normal((M, K)).astype(np.float32))
+    b = oracle.f32_to_bf16((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    qa, ea = oracle.mx_quant_1x32(a)
+    qb, eb = oracle.mx_quant_1x32(b)
+    t = oracle.e4m3_table().astype(np.float64)
+    da = t[qa] * np.repeat(np.ldexp(1.0, ea.astype(np.int64) - 127), 32, 1)
+    db = t[qb] * np.repeat(np.ldexp(1.0, eb.astype(np.int64) - 127), 32, 1)
+    truth = da @ db.T
+    out = oracle.mx_gemm(qa, ea, qb, eb)
+    bound = 2.0 ** -23 * np.abs(truth) + 1e-12 * (np.abs(da) @ np.abs(db).T)
+    assert np.all(np.abs(out - truth) <= bound)
+    ii, jj = np.array([0, 7, 47]), np.array([39, 3, 0])
+    assert np.array_equal(oracle.mx_gemm(qa, ea, qb, eb, ii, jj), out[ii, jj])
+
+
 def test_quant_reciprocal_case_is_distinguished():
     """A tile where v * (1/s) and v / s round to different E4M3 codes: the
     torch-steps pin must see the true division."""
