@@ -634,7 +634,8 @@ def run_reference(args, world, rank):
 
 
 NCU_CASES = ("fprop", "dgrad", "wgrad", "quant_1x128", "quant_128x128", "requant_e4m3",
-             "requant_bf16")
+             "requant_bf16", "fprop_dense", "dgrad_dense", "wgrad_dense", "quant_dual", "quant_sr",
+             "mx_quant", "mx_gemm", "splitk_longk")
 
 
 def run_ncu_case(name):
@@ -687,10 +688,66 @@ def run_ncu_case(name):
         e.fp8_quant_1x128(rnd(M, K), xq, sx)
         xT, sxT = e.empty_requant_128x1_T(M, K)
         runs = lambda: e.fp8_requant_128x1_T(xq, sx, xT, sxT)
-    else:
+    elif name == "requant_bf16":
         x = rnd(M, K)
         xT, sxT = e.empty_requant_128x1_T(M, K)
         runs = lambda: e.fp8_requant_128x1_T(x, None, xT, sxT)
+    elif name in ("fprop_dense", "dgrad_dense", "wgrad_dense"):
+        # the dense bench workload's shapes exactly (for per-launch DRAM traffic)
+        Md, Kd, Nd = dense_shapes().values()
+        if name == "fprop_dense":
+            xq, sx = e.empty_quant_1x128(Md, Kd)
+            e.fp8_quant_1x128(rnd(Md, Kd), xq, sx)
+            wq, wqT, sw = e.empty_quant_128x128(Kd, Nd)
+            e.fp8_quant_128x128(rnd(Kd, Nd, std=0.02), wq, wqT, sw)
+            y = torch.empty(Md, Nd, dtype=bf, device=dev)
+            runs = lambda: e.fp8_block_gemm_fprop(xq, sx, wqT, sw, y)
+        elif name == "dgrad_dense":
+            dyq, sdy = e.empty_quant_1x128(Md, Nd)
+            e.fp8_quant_1x128(rnd(Md, Nd, std=1e-3), dyq, sdy)
+            wq, wqT, sw = e.empty_quant_128x128(Kd, Nd)
+            e.fp8_quant_128x128(rnd(Kd, Nd, std=0.02), wq, wqT, sw)
+            dx = torch.empty(Md, Kd, dtype=bf, device=dev)
+            runs = lambda: e.fp8_block_gemm_dgrad(dyq, sdy, wq, sw, dx)
+        else:
+            xq, sx = e.empty_quant_1x128(Md, Kd)
+            e.fp8_quant_1x128(rnd(Md, Kd), xq, sx)
+            xT, sxT = e.empty_requant_128x1_T(Md, Kd)
+            e.fp8_requant_128x1_T(xq, sx, xT, sxT)
+            dyT, sdyT = e.empty_requant_128x1_T(Md, Nd)
+            e.fp8_requant_128x1_T(rnd(Md, Nd, std=1e-3), None, dyT, sdyT)
+            dw = torch.empty(Nd, Kd, dtype=torch.float32, device=dev)
+            runs = lambda: e.fp8_block_gemm_wgrad(dyT, sdyT, xT, sxT, dw)
+    elif name == "quant_dual":
+        x = rnd(M, K, std=1e-3)
+        q, s = e.empty_quant_1x128(M, K)
+        qT, sT = e.empty_requant_128x1_T(M, K)
+        runs = lambda: e.fp8_quant_dual(x, q, s, qT, sT)
+    elif name == "quant_sr":
+        x = rnd(M, K)
+        q, s = e.empty_quant_1x128(M, K)
+        runs = lambda: e.fp8_quant_1x128_sr(x, q, s, seed=1, salt=2)
+    elif name == "mx_quant":
+        x = rnd(M, K)
+        q, at = e.empty_mx_quant(M, K)
+        runs = lambda: e.fp8_mx_quant_1x32(x, q, at)
+    elif name == "mx_gemm":
+        qa, aa = e.empty_mx_quant(M, K)
+        e.fp8_mx_quant_1x32(rnd(M, K), qa, aa)
+        qb, ab = e.empty_mx_quant(N, K)
+        e.fp8_mx_quant_1x32(rnd(N, K, std=0.02), qb, ab)
+        y = torch.empty(M, N, dtype=bf, device=dev)
+        runs = lambda: e.fp8_mx_gemm(qa, aa, qb, ab, y)
+    else:   # splitk_longk: 256 x 65536 x 256, default split
+        Kl = 65536
+        xq, sx = e.empty_quant_1x128(256, Kl)
+        e.fp8_quant_1x128(rnd(256, Kl), xq, sx)
+        wq, wqT, sw = e.empty_quant_128x128(Kl, 256)
+        e.fp8_quant_128x128(rnd(Kl, 256, std=0.02), wq, wqT, sw)
+        y = torch.empty(256, 256, dtype=bf, device=dev)
+        sp = e.fp8bs_splitk_default_splits(e.OP_FPROP, 256, 256, Kl)
+        ws = torch.empty(e.fp8bs_splitk_workspace_size(e.OP_FPROP, 256, 256, Kl, sp), dtype=torch.uint8, device=dev)
+        runs = lambda: e.fp8_block_gemm_splitk(e.OP_FPROP, xq, sx, wqT, sw, y, splits=sp, workspace=ws)
     for _ in range(3):
         runs()
     torch.cuda.synchronize()
