@@ -55,11 +55,10 @@ def step_work(M, K, N):
     s_ld = (M + 3) // 4 * 4
     b = {
         "quant_128x128(W)": K * N * 2 + 2 * K * N + 4 * (K // 128) * (N // 128),
-        "quant_1x128(X)": M * K * 2 + M * K + 4 * (K // 128) * s_ld,
+        "quant_dual_stash(X)": M * K * 2 + M * K + 4 * (K // 128) * s_ld + M * K + 4 * (M // 128) * K,
         "fprop": M * K + N * K + 4 * (K // 128) * (s_ld + N // 128) + 2 * M * N,
         "quant_dual(dY)": M * N * 2 + M * N + 4 * (N // 128) * s_ld + M * N + 4 * (M // 128) * N,
         "dgrad": M * N + K * N + 4 * (N // 128) * s_ld + 4 * (K // 128) * (N // 128) + 2 * M * K,
-        "requant_128x1_T(Xq)": M * K + 4 * (K // 128) * s_ld + M * K + 4 * (M // 128) * K,
         "wgrad": N * M + K * M + 4 * (M // 128) * (N + K) + 4 * N * K,
     }
     flops = {"fprop": gemm_flops, "dgrad": gemm_flops, "wgrad": gemm_flops}
@@ -217,8 +216,7 @@ class DenseStep:
         self.xT, self.sxT = e.empty_requant_128x1_T(M, K, device=device)
         self.dyT, self.sdyT = e.empty_requant_128x1_T(M, N, device=device)
         self.dW = torch.empty(N, K, dtype=torch.float32, device=device)
-        self.names = ["quant_128x128(W)", "quant_1x128(X)", "fprop", "quant_dual(dY)", "dgrad",
-                      "requant_128x1_T(Xq)", "wgrad"]
+        self.names = ["quant_128x128(W)", "quant_dual_stash(X)", "fprop", "quant_dual(dY)", "dgrad", "wgrad"]
 
     def work(self):
         return step_work(self.M, self.K, self.N)
@@ -235,11 +233,12 @@ class DenseStep:
         e = self.fp8bs
         return [
             lambda: e.fp8_quant_128x128(self.W, self.wq, self.wqT, self.sw),
-            lambda: e.fp8_quant_1x128(self.X, self.xq, self.sx),
+            # the forward cast of X also writes the Wgrad operand: the 128x1
+            # transposed requant of its E4M3 stash
+            lambda: e.fp8_quant_dual_stash(self.X, self.xq, self.sx, self.xT, self.sxT),
             lambda: e.fp8_block_gemm_fprop(self.xq, self.sx, self.wqT, self.sw, self.Y),
             lambda: e.fp8_quant_dual(self.dY, self.dyq, self.sdy, self.dyT, self.sdyT),
             lambda: e.fp8_block_gemm_dgrad(self.dyq, self.sdy, self.wq, self.sw, self.dX),
-            lambda: e.fp8_requant_128x1_T(self.xq, self.sx, self.xT, self.sxT),
             lambda: e.fp8_block_gemm_wgrad(self.dyT, self.sdyT, self.xT, self.sxT, self.dW),
         ]
 
@@ -279,9 +278,8 @@ class MoeStep:
         self.aT, self.saT = e.empty_requant_128x1_T(tokens, inter, self.offsets, device)
         self.dWd = torch.empty(experts, hidden, inter, dtype=torch.float32, device=device)
         self.names = ["quant_128x128(W_up)", "quant_128x128(W_down)", "quant_1x128(X)",
-                      "grouped_fprop_up", "quant_1x128(A)", "grouped_fprop_down", "quant_dual(dY)",
-                      "grouped_dgrad_down", "requant_128x1_T(Aq)",
-                      "grouped_wgrad_down"]
+                      "grouped_fprop_up", "quant_dual_stash(A)", "grouped_fprop_down", "quant_dual(dY)",
+                      "grouped_dgrad_down", "grouped_wgrad_down"]
 
     def work(self):
         T, G, H, I, U = self.T, self.G, self.H, self.I, self.U
@@ -294,11 +292,10 @@ class MoeStep:
             "quant_128x128(W_down)": G * I * H * 4 + 4 * G * (I // 128) * (H // 128),
             "quant_1x128(X)": T * H * 3 + 4 * (H // 128) * s_ld,
             "grouped_fprop_up": T * H + G * U * H + 2 * T * U,
-            "quant_1x128(A)": T * I * 3 + 4 * (I // 128) * s_ld,
+            "quant_dual_stash(A)": T * I * 3 + 4 * (I // 128) * s_ld + I * mp + 4 * (mp // 128) * I,
             "grouped_fprop_down": T * I + G * H * I + 2 * T * H,
             "quant_dual(dY)": T * H * 3 + 4 * (H // 128) * s_ld + H * mp + 4 * (mp // 128) * H,
             "grouped_dgrad_down": T * H + G * I * H + 2 * T * I,
-            "requant_128x1_T(Aq)": T * I + 4 * (I // 128) * s_ld + I * mp + 4 * (mp // 128) * I,
             "grouped_wgrad_down": (H + I) * mp + 4 * G * H * I,
         }
         return flops, b
@@ -311,13 +308,12 @@ class MoeStep:
             lambda: e.fp8_quant_1x128(self.X, self.xq, self.sx),
             lambda: e.fp8_block_gemm_grouped(e.OP_FPROP, off, self.xq, self.sx, self.wuqT, self.swu,
                                              self.Yu, U, H),
-            lambda: e.fp8_quant_1x128(self.A, self.aq, self.sa),
+            lambda: e.fp8_quant_dual_stash(self.A, self.aq, self.sa, self.aT, self.saT, offsets=off),
             lambda: e.fp8_block_gemm_grouped(e.OP_FPROP, off, self.aq, self.sa, self.wdqT, self.swd,
                                              self.Yd, H, I),
             lambda: e.fp8_quant_dual(self.dY, self.dyq, self.sdy, self.dyT, self.sdyT, offsets=off),
             lambda: e.fp8_block_gemm_grouped(e.OP_DGRAD, off, self.dyq, self.sdy, self.wdq, self.swd,
                                              self.dA, H, I),
-            lambda: e.fp8_requant_128x1_T(self.aq, self.sa, self.aT, self.saT, offsets=off),
             lambda: e.fp8_block_gemm_grouped(e.OP_WGRAD, off, self.dyT, self.sdyT, self.aT, self.saT,
                                              self.dWd, H, I),
         ]
@@ -656,7 +652,7 @@ def run_reference(args, world, rank):
 
 NCU_CASES = ("fprop", "dgrad", "wgrad", "quant_1x128", "quant_128x128", "requant_e4m3",
              "requant_bf16", "fprop_dense", "dgrad_dense", "wgrad_dense", "quant_dual", "quant_sr",
-             "mx_quant", "mx_gemm", "splitk_longk")
+             "mx_quant", "mx_gemm", "splitk_longk", "quant_dual_stash")
 
 
 def run_ncu_case(name):
@@ -744,6 +740,11 @@ def run_ncu_case(name):
         q, s = e.empty_quant_1x128(M, K)
         qT, sT = e.empty_requant_128x1_T(M, K)
         runs = lambda: e.fp8_quant_dual(x, q, s, qT, sT)
+    elif name == "quant_dual_stash":
+        x = rnd(M, K)
+        q, s = e.empty_quant_1x128(M, K)
+        qT, sT = e.empty_requant_128x1_T(M, K)
+        runs = lambda: e.fp8_quant_dual_stash(x, q, s, qT, sT)
     elif name == "quant_sr":
         x = rnd(M, K)
         q, s = e.empty_quant_1x128(M, K)

@@ -34,6 +34,7 @@ __all__ = [
     "SRC_BF16", "SRC_E4M3", "OP_FPROP", "OP_DGRAD", "OP_WGRAD", "MAX_GROUPS",
     "SCALE_FP32", "SCALE_UE8M0", "ScaleOpts", "fp8_quant_1x128_opts", "fp8_quant_128x128_opts",
     "fp8_requant_128x1_T_opts", "fp8_quant_dual_opts", "fp8_quant_1x128_sr", "fp8_quant_128x128_sr",
+    "fp8_quant_dual_stash", "fp8_quant_dual_stash_opts",
     "fp8bs_mx_scale_bytes", "fp8_mx_quant_1x32", "fp8_mx_gemm", "empty_mx_quant",
 ]
 
@@ -93,6 +94,8 @@ def lib() -> ctypes.CDLL:
         "fp8_quant_128x128_opts": ([P, I64, I64, I64, I64, P, P, P, P, P], S),
         "fp8_requant_128x1_T_opts": ([I, P, P, I64, I64, P, I32, P, P, P, P], S),
         "fp8_quant_dual_opts": ([P, I64, I64, P, I32, P, P, P, P, P, P], S),
+        "fp8_quant_dual_stash": ([P, I64, I64, P, I32, P, P, P, P, P], S),
+        "fp8_quant_dual_stash_opts": ([P, I64, I64, P, I32, P, P, P, P, P, P], S),
         "fp8_quant_1x128_sr": ([P, I64, I64, I64, P, P, ctypes.c_uint64, ctypes.c_uint32, P, P], S),
         "fp8bs_mx_scale_bytes": ([I64, I64], I64),
         "fp8_mx_quant_1x32": ([P, I64, I64, P, P, P], S),
@@ -284,6 +287,28 @@ def fp8_quant_dual(x: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, qT: t
     """One read of BF16 x [rows x cols]: its 1x128 cast (q, scales, as
     fp8_quant_1x128) and its 128x1 transposed cast (qT, scalesT, as
     fp8_requant_128x1_T from BF16), optional host group offsets."""
+    _dual_common("fp8_quant_dual_opts", x, q, scales, qT, scalesT, offsets, stream, rule, amax_floor,
+                 scale_floor)
+
+
+def fp8_quant_dual_stash(x: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, qT: torch.Tensor,
+                         scalesT: torch.Tensor, offsets=None, stream=None, rule: int = SCALE_FP32,
+                         amax_floor: float = 0.0, scale_floor: float = 0.0) -> None:
+    """One read of BF16 x [rows x cols]: its 1x128 cast (q, scales, as
+    fp8_quant_1x128) and the 128x1 transposed requant of that E4M3 result
+    (qT, scalesT, as fp8_requant_128x1_T from q, scales), optional host
+    group offsets."""
+    _dual_common("fp8_quant_dual_stash_opts", x, q, scales, qT, scalesT, offsets, stream, rule, amax_floor,
+                 scale_floor)
+
+
+def fp8_quant_dual_stash_opts(x, q, scales, qT, scalesT, opts: Optional["ScaleOpts"], offsets=None,
+                              stream=None) -> None:
+    """fp8_quant_dual_stash under the scale rule `opts` (None: default)."""
+    fp8_quant_dual_stash(x, q, scales, qT, scalesT, offsets=offsets, stream=stream, **_rule_kwargs(opts))
+
+
+def _dual_common(fn, x, q, scales, qT, scalesT, offsets, stream, rule, amax_floor, scale_floor) -> None:
     _need(x, torch.bfloat16, "x")
     for t, n, d in ((q, "q", torch.uint8), (scales, "scales", torch.float32), (qT, "qT", torch.uint8),
                     (scalesT, "scalesT", torch.float32)):
@@ -301,7 +326,7 @@ def fp8_quant_dual(x: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, qT: t
     mp = fp8bs_padded_tokens(rows, offsets)
     if qT.shape != (cols, mp) or scalesT.shape != (mp // 128, cols):
         raise ValueError("qT / scalesT shapes do not match empty_requant_128x1_T")
-    _check("fp8_quant_dual", lib().fp8_quant_dual_opts(
+    _check(fn[:-len("_opts")], getattr(lib(), fn)(
         _ptr(x), rows, cols, optr, groups, _ptr(q), _ptr(scales), _ptr(qT), _ptr(scalesT),
         _opts(rule, amax_floor, scale_floor), _stream(stream)))
 

@@ -412,7 +412,8 @@ namespace {
 // of a BF16 source (q, q_scales non-null).
 fp8bs_status requant_common(int src_mode, const void* src, const float* src_scales, int64_t rows, int64_t cols,
                             const int32_t* group_offsets_host, int32_t groups, uint8_t* qT, float* scalesT,
-                            uint8_t* q, float* q_scales, const fp8bs_scale_opts* opts, void* stream)
+                            uint8_t* q, float* q_scales, const fp8bs_scale_opts* opts, void* stream,
+                            bool stash = false)
 {
     ScaleRule rule;
     if (!to_rule(opts, &rule)) return FP8BS_ERR_ARG;
@@ -447,6 +448,7 @@ fp8bs_status requant_common(int src_mode, const void* src, const float* src_scal
     p.q = q;
     p.q_scales = q_scales;
     p.q_scale_ld = fp8bs_scale_ld(rows);
+    p.stash = stash ? 1 : 0;
     p.rule = rule;
     if (grouped) {
         p.num_groups = groups;
@@ -502,6 +504,23 @@ fp8bs_status fp8_quant_dual_opts(const void* x, int64_t rows, int64_t cols, cons
     if (rows > 0 && (!q || !scales)) return FP8BS_ERR_ARG;
     return requant_common(FP8BS_SRC_BF16, x, nullptr, rows, cols, group_offsets_host, groups, qT, scalesT, q,
                           scales, opts, stream);
+}
+
+fp8bs_status fp8_quant_dual_stash(const void* x, int64_t rows, int64_t cols, const int32_t* group_offsets_host,
+                                  int32_t groups, uint8_t* q, float* scales, uint8_t* qT, float* scalesT,
+                                  void* stream)
+{
+    return fp8_quant_dual_stash_opts(x, rows, cols, group_offsets_host, groups, q, scales, qT, scalesT, nullptr,
+                                     stream);
+}
+
+fp8bs_status fp8_quant_dual_stash_opts(const void* x, int64_t rows, int64_t cols, const int32_t* group_offsets_host,
+                                       int32_t groups, uint8_t* q, float* scales, uint8_t* qT, float* scalesT,
+                                       const fp8bs_scale_opts* opts, void* stream)
+{
+    if (rows > 0 && (!q || !scales)) return FP8BS_ERR_ARG;
+    return requant_common(FP8BS_SRC_BF16, x, nullptr, rows, cols, group_offsets_host, groups, qT, scalesT, q,
+                          scales, opts, stream, true);
 }
 
 fp8bs_status fp8_block_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wqT,

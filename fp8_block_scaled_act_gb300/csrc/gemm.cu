@@ -20,7 +20,14 @@
 //               accumulate = 0), double-buffered over 2 x 256 TMEM columns,
 //               and commits to mbarriers that free the smem stage and hand
 //               the partial to the epilogue.
-//   warps 2-3   idle (they complete the first warpgroup, which gives its
+//   warp 2      Wgrad scale producer: all 32 lanes copy each K-block's
+//               scales (the tile's 128 row scales and 256 column scales)
+//               with cp.async into an 8-slot shared-memory ring, running
+//               ahead of the epilogue; the copies complete on an mbarrier.
+//               (Fprop / Dgrad epilogue threads need one scalar per K-block
+//               and prefetch it themselves, two K-blocks ahead; the warp is
+//               idle there.)
+//   warp 3      idle (it completes the first warpgroup, which gives its
 //               registers to the epilogue with setmaxnreg).
 //   warps 4-11  promotion epilogue: each warp owns 32 TMEM lanes (rows) and
 //               128 columns; per K-block it loads the fp32 partial with
@@ -61,17 +68,21 @@ constexpr int kTmemCols = 2 * kBN;              // two accumulator buffers
 // Waits that drain in-flight copies and MMAs before exit use at least this
 // limit, so that a small user limit never lets a CTA exit with work in flight.
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
-constexpr int kCtlBytes = 256;                  // barriers and flags
-constexpr int kVecSlots = 3;                    // Wgrad scale ring depth
-constexpr int kSlotFloats = 32 + 128;           // A scales of the warp's 32 rows + 128 column scales
-constexpr int kVecBytes = kEpiWarps * kVecSlots * kSlotFloats * 4;
-constexpr int kSmemBytes = kStages * kStageBytes + kCtlBytes + kVecBytes + 1024 /* alignment */;
+constexpr int kCtlBytes = 512;                  // barriers and flags
+// Wgrad scale ring: slot = the K-block's scales of the tile's 128 rows, then
+// of its 256 columns.
+constexpr int kScaleSlots = 8;
+constexpr int kScaleSlotFloats = kBM + kBN;
+constexpr int kScaleBytes = kScaleSlots * kScaleSlotFloats * 4;
+constexpr int kSmemBytes = kStages * kStageBytes + kCtlBytes + kScaleBytes + 1024 /* alignment */;
 
 struct SharedCtl {
     uint64_t full[kStages];
     uint64_t empty[kStages];
     uint64_t tfull[2];
     uint64_t tempty[2];
+    uint64_t sfull[kScaleSlots];   // scale slot landed (one cp.async arrival per producer lane)
+    uint64_t sempty[kScaleSlots];  // scale slot read by every epilogue warp
     uint64_t mma_done;        // final commit of the MMA thread (drain before exit)
     uint32_t tmem_base;
     volatile int abort;
@@ -234,7 +245,7 @@ __device__ __forceinline__ bool epilogue_block_scale(const GemmParams& p, Shared
 // and 16 column-scale pairs per thread. Scales arrive in a per-warp 3-slot
 // shared-memory ring filled by cp.async two K-blocks ahead (slot: the 32 row
 // scales of the warp's quarter, then its 128 column scales).
-__device__ __forceinline__ bool epilogue_vector_scale(const GemmParams& p, SharedCtl* ctl, uint8_t* vec_smem,
+__device__ __forceinline__ bool epilogue_vector_scale(const GemmParams& p, SharedCtl* ctl, const float* ring,
                                                       uint32_t tmem_base, int warp, int lane, uint64_t limit)
 {
     const int ew = warp - kFirstEpiWarp;
@@ -243,7 +254,6 @@ __device__ __forceinline__ bool epilogue_vector_scale(const GemmParams& p, Share
     const int g4 = lane >> 2;       // row within each group of 8
     const int t4 = lane & 3;        // column pair within each group of 8
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    float* vring = reinterpret_cast<float*>(vec_smem) + ew * (kVecSlots * kSlotFloats);
     uint32_t acc_it = 0;
 
     const int units = p.total_tiles * p.splits;
@@ -253,22 +263,6 @@ __device__ __forceinline__ bool epilogue_vector_scale(const GemmParams& p, Share
         const int qrow0 = mt * kBM + quarter * 32;             // first tile row of this quarter
         const int col0 = nt * kBN + half * 128;
         const bool cols_ok = col0 < p.n_cols;                  // n_cols % 128 == 0
-        // cp.async sources: lane l fetches the A scale of row qrow0 + l and
-        // the B scales of columns col0 + 4l .. 4l + 3
-        const int srow = p.a_row0[g] + qrow0 + lane;
-        const bool sa_ok = srow < p.sa_rows;
-        const float* sa_ptr = p.sa + static_cast<int64_t>(p.sa_kb0[g] + kb0) * p.sa_ld + srow;
-        const float* sb_ptr = p.sb + p.sb_off[g] + static_cast<int64_t>(col0 + 4 * lane) +
-                              static_cast<int64_t>(kb0) * p.sb_kstride;
-        auto prefetch = [&](int kb) {
-            if (kb < nkb) {
-                float* slot = vring + (kb % kVecSlots) * kSlotFloats;
-                cp_async_4(slot + lane, sa_ok ? sa_ptr + static_cast<int64_t>(kb) * p.sa_ld : p.sa, sa_ok ? 4u : 0u);
-                cp_async_16(slot + 32 + 4 * lane, cols_ok ? sb_ptr + static_cast<int64_t>(kb) * p.sb_kstride : p.sb,
-                            cols_ok ? 16u : 0u);
-            }
-            cp_async_commit();
-        };
 
         float2 acc[4][16];   // [row i: g4 + 8 i][column group j: 8 j + 2 t4, + 1]
 #pragma unroll
@@ -276,27 +270,23 @@ __device__ __forceinline__ bool epilogue_vector_scale(const GemmParams& p, Share
 #pragma unroll
             for (int j = 0; j < 16; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
-        prefetch(0);
-        prefetch(1);
         for (int kb = 0; kb < nkb; ++kb, ++acc_it) {
-            prefetch(kb + 2);
-            cp_async_wait<2>();   // K-block kb's scales have landed
-            __syncwarp();
-            const float* slot = vring + (kb % kVecSlots) * kSlotFloats;
+            // this K-block's scales from the ring: the warp's 4 row scales in
+            // registers, the column scales read from the slot while promoting
+            const uint32_t ss = acc_it % kScaleSlots;
+            if (ctl->abort || !mbar_wait(&ctl->sfull[ss], (acc_it / kScaleSlots) & 1u, limit)) return false;
+            const float* slot = ring + ss * kScaleSlotFloats;
             float2 sa2[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float v = slot[g4 + 8 * i];
+                const float v = slot[quarter * 32 + g4 + 8 * i];
                 sa2[i] = make_float2(v, v);
             }
-            const float2* sbp = reinterpret_cast<const float2*>(slot + 32) + t4;
+            const float2* sbp = reinterpret_cast<const float2*>(slot + kBM + half * 128) + t4;
 
             const uint32_t buf = acc_it & 1u;
             const uint32_t aph = (acc_it >> 1) & 1u;
-            if (ctl->abort || !mbar_wait(&ctl->tfull[buf], aph, limit)) {
-                cp_async_wait<0>();
-                return false;
-            }
+            if (ctl->abort || !mbar_wait(&ctl->tfull[buf], aph, limit)) return false;
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + lane_addr + buf * kBN + half * 128;
 
@@ -331,8 +321,10 @@ __device__ __forceinline__ bool epilogue_vector_scale(const GemmParams& p, Share
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
             promote(3, rb);
+            // the slot's column scales have been read
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->sempty[ss]);
         }
-        cp_async_wait<0>();
 
         if (cols_ok) {
 #pragma unroll
@@ -369,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sA = smem;
     uint8_t* sB = smem + kStages * kABytes;
     SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + kStages * kStageBytes);
+    float* scale_ring = reinterpret_cast<float*>(smem + kStages * kStageBytes + kCtlBytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -381,6 +374,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int a = 0; a < 2; ++a) {
             mbar_init(&ctl->tfull[a], 1);
             mbar_init(&ctl->tempty[a], kEpiWarps);
+        }
+        for (int a = 0; a < kScaleSlots; ++a) {
+            mbar_init(&ctl->sfull[a], 32);
+            mbar_init(&ctl->sempty[a], kEpiWarps);
         }
         mbar_init(&ctl->mma_done, 1);
         ctl->abort = 0;
@@ -479,6 +476,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t drain = limit > kDrainLimitNs ? limit : kDrainLimitNs;
             mbar_wait(&ctl->mma_done, 0u, drain);
         }
+    } else if (warp == 2 && kKind == GemmKind::kVectorScaleF32) {
+        // ------------------------------------------------------------------
+        // Scale producer (Wgrad): the same K-block sequence as the TMA producer
+        // ------------------------------------------------------------------
+        uint32_t it = 0;
+        bool ok = true;
+        const int units = p.total_tiles * p.splits;
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            int g, mt, nt, split, kb0, nkb;
+            decode_unit(p, u, g, mt, nt, split, kb0, nkb);
+            // lane l copies the A scales of tile rows 4l .. 4l + 3 and the
+            // column scales of tile columns 8l .. 8l + 7
+            const int arow = p.a_row0[g] + mt * kBM + 4 * lane;
+            const float* sa_src = p.sa + static_cast<int64_t>(p.sa_kb0[g] + kb0) * p.sa_ld + arow;
+            const int col = nt * kBN + 8 * lane;
+            const bool sb_in = col < p.n_cols;                 // n_cols % 128 == 0
+            const float* sb_src = p.sb + p.sb_off[g] + col + static_cast<int64_t>(kb0) * p.sb_kstride;
+            for (int kb = 0; kb < nkb; ++kb, ++it) {
+                const uint32_t s = it % kScaleSlots;
+                if (ctl->abort || !mbar_wait(&ctl->sempty[s], ((it / kScaleSlots) & 1u) ^ 1u, limit)) {
+                    ok = false;
+                    break;
+                }
+                float* slot = scale_ring + s * kScaleSlotFloats;
+                const float* a_k = sa_src + static_cast<int64_t>(kb) * p.sa_ld;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const bool in = arow + i < p.sa_rows;
+                    cp_async_4(slot + 4 * lane + i, in ? a_k + i : p.sa, in ? 4u : 0u);
+                }
+                const float* b_k = sb_src + static_cast<int64_t>(kb) * p.sb_kstride;
+                cp_async_16(slot + kBM + 8 * lane, sb_in ? b_k : p.sb, sb_in ? 16u : 0u);
+                cp_async_16(slot + kBM + 8 * lane + 4, sb_in ? b_k + 4 : p.sb, sb_in ? 16u : 0u);
+                cp_async_mbar_arrive_noinc(&ctl->sfull[s]);
+            }
+        }
+        if (!ok) {
+            if (lane == 0) record_status(p.status, FP8BS_ERR_TIMEOUT);
+            ctl->abort = 1;
+        }
+        cp_async_wait_all();   // no copy into the ring outlives the CTA
     } else if (warp >= kFirstEpiWarp) {
         // ------------------------------------------------------------------
         // Promotion epilogue
@@ -488,8 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kKind == GemmKind::kBlockScaleBf16)
             ok = epilogue_block_scale(p, ctl, tmem_base, warp, lane, limit);
         else
-            ok = epilogue_vector_scale(p, ctl, smem + kStages * kStageBytes + kCtlBytes, tmem_base, warp,
-                                       lane, limit);
+            ok = epilogue_vector_scale(p, ctl, scale_ring, tmem_base, warp, lane, limit);
         if (!ok) {
             record_status(p.status, FP8BS_ERR_TIMEOUT);
             ctl->abort = 1;

@@ -55,6 +55,9 @@ struct RequantParams {
     uint8_t* q;
     float* q_scales;
     int64_t q_scale_ld;
+    // With q: take the transposed cast from the E4M3 result q instead of
+    // from the BF16 source (the E4M3 source mode applied to q, q_scales).
+    int stash;
     ScaleRule rule;
 };
 

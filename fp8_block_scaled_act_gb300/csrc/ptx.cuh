@@ -125,6 +125,19 @@ __device__ __forceinline__ void cp_async_commit()
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
+// Arrives on `bar` once every cp.async this thread has issued so far has
+// completed. The arrival does not raise the barrier's expected count, so the
+// barrier's init count includes one such arrival per issuing thread.
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Waits until at most kPending of this thread's most recent groups are pending.
 template <int kPending>
 __device__ __forceinline__ void cp_async_wait()

@@ -572,9 +572,13 @@ __device__ __forceinline__ int find_group(const int32_t* tile_start, int ng, int
 }
 
 // kDual: also the 1x128 cast of the same BF16 rows (p.q, p.q_scales).
-template <bool kDual>
+// kStash (with kDual): the transposed cast is taken from that E4M3 result
+// (decoded with its row scale, as the E4M3 source mode does) instead of
+// from the BF16 values; the 1x128 codes are staged in place of the source.
+template <bool kDual, bool kStash>
 __global__ void __launch_bounds__(kQ3Threads, kDual ? 3 : 4) requant_128x1_T_kernel(const __grid_constant__ RequantParams p)
 {
+    static_assert(kDual || !kStash, "the stash mode is a dual cast");
     // staging: BF16 source 128 x 128 x 2 bytes, or E4M3 128 x 128 bytes + row scales
     __shared__ __align__(16) uint8_t stage[128 * 128 * 2];
     __shared__ float row_scale[128];
@@ -602,8 +606,11 @@ __global__ void __launch_bounds__(kQ3Threads, kDual ? 3 : 4) requant_128x1_T_ker
                 d[i] = __ldcs(reinterpret_cast<const uint4*>(src + (r0 + rl) * p.cols + c0 + chunk * 8));
             else
                 d[i] = make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(stage + (rl * 128 + chunk * 8) * 2) = d[i];
+            if constexpr (!kStash) *reinterpret_cast<uint4*>(stage + (rl * 128 + chunk * 8) * 2) = d[i];
         }
+        float cm[8];   // kStash: column maxima of the decoded 1x128 result
+#pragma unroll
+        for (int e = 0; e < 8; ++e) cm[e] = 0.0f;
         if constexpr (kDual) {
             // Row-wise (1x128) cast of the same rows from the registers: a
             // row's 128 channels are the 16 chunks held by 16 consecutive
@@ -618,25 +625,51 @@ __global__ void __launch_bounds__(kQ3Threads, kDual ? 3 : 4) requant_128x1_T_ker
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int rl = rg * 8 + i;
-                if (rl >= len) continue;
+                if (rl >= len) {
+                    if constexpr (kStash) {
+                        // padding rows: zero codes and scale, as an E4M3 source stages them
+                        *reinterpret_cast<uint2*>(stage + rl * 128 + chunk * 8) = make_uint2(0u, 0u);
+                        if (chunk == 0) row_scale[rl] = 0.0f;
+                    }
+                    continue;
+                }
                 const TileScale ts = tile_scale(__uint_as_float(rm[i] << 16), p.rule);
                 if (chunk == 0) p.q_scales[(c0 / 128) * p.q_scale_ld + r0 + rl] = ts.s;
-                if (ch_ok)
-                    *reinterpret_cast<uint2*>(p.q + (r0 + rl) * p.cols + c0 + chunk * 8) = quant8(d[i], ts);
+                const uint2 codes = quant8(d[i], ts);
+                if (ch_ok) *reinterpret_cast<uint2*>(p.q + (r0 + rl) * p.cols + c0 + chunk * 8) = codes;
+                if constexpr (kStash) {
+                    *reinterpret_cast<uint2*>(stage + rl * 128 + chunk * 8) = codes;
+                    if (chunk == 0) row_scale[rl] = ts.s;
+                    const uint32_t wv[2] = {codes.x, codes.y};
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const float2 lo = e4m3x2_to_f32(static_cast<uint16_t>(wv[k] & 0xFFFFu));
+                        const float2 hi = e4m3x2_to_f32(static_cast<uint16_t>(wv[k] >> 16));
+                        cm[4 * k + 0] = fmaxf(cm[4 * k + 0], fabsf(__fmul_rn(lo.x, ts.s)));
+                        cm[4 * k + 1] = fmaxf(cm[4 * k + 1], fabsf(__fmul_rn(lo.y, ts.s)));
+                        cm[4 * k + 2] = fmaxf(cm[4 * k + 2], fabsf(__fmul_rn(hi.x, ts.s)));
+                        cm[4 * k + 3] = fmaxf(cm[4 * k + 3], fabsf(__fmul_rn(hi.y, ts.s)));
+                    }
+                }
             }
         }
-        uint32_t mw[4] = {0u, 0u, 0u, 0u};
+        if constexpr (kStash) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            mw[0] = __vmaxu2(mw[0], d[i].x & 0x7FFF7FFFu);
-            mw[1] = __vmaxu2(mw[1], d[i].y & 0x7FFF7FFFu);
-            mw[2] = __vmaxu2(mw[2], d[i].z & 0x7FFF7FFFu);
-            mw[3] = __vmaxu2(mw[3], d[i].w & 0x7FFF7FFFu);
-        }
+            for (int e = 0; e < 8; ++e) col_part[rg][chunk * 8 + e] = cm[e];
+        } else {
+            uint32_t mw[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            col_part[rg][chunk * 8 + 2 * k] = __uint_as_float(mw[k] << 16);
-            col_part[rg][chunk * 8 + 2 * k + 1] = __uint_as_float(mw[k] & 0xFFFF0000u);
+            for (int i = 0; i < 8; ++i) {
+                mw[0] = __vmaxu2(mw[0], d[i].x & 0x7FFF7FFFu);
+                mw[1] = __vmaxu2(mw[1], d[i].y & 0x7FFF7FFFu);
+                mw[2] = __vmaxu2(mw[2], d[i].z & 0x7FFF7FFFu);
+                mw[3] = __vmaxu2(mw[3], d[i].w & 0x7FFF7FFFu);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                col_part[rg][chunk * 8 + 2 * k] = __uint_as_float(mw[k] << 16);
+                col_part[rg][chunk * 8 + 2 * k + 1] = __uint_as_float(mw[k] & 0xFFFF0000u);
+            }
         }
     } else {
         // thread: 16-channel chunk t % 8, rows (t / 8) * 4 .. + 3
@@ -693,7 +726,7 @@ __global__ void __launch_bounds__(kQ3Threads, kDual ? 3 : 4) requant_128x1_T_ker
     }
     __syncthreads();
 
-    if (p.mode == FP8BS_SRC_BF16) {
+    if (p.mode == FP8BS_SRC_BF16 && !kStash) {
         // unit = (channel pair 2jp, 2jp + 1; 32-token part): 64 x 4 = 256 units
         const int j = 2 * (threadIdx.x & 63);
         const int part = threadIdx.x >> 6;
@@ -785,10 +818,12 @@ cudaError_t launch_requant_128x1_T(const RequantParams& p, cudaStream_t stream)
     if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
     const dim3 grid((unsigned)tiles, (unsigned)((p.cols + 127) / 128));
     if (grid.y > 65535) return cudaErrorInvalidValue;
-    if (p.q != nullptr)
-        requant_128x1_T_kernel<true><<<grid, kQ3Threads, 0, stream>>>(p);
+    if (p.q != nullptr && p.stash)
+        requant_128x1_T_kernel<true, true><<<grid, kQ3Threads, 0, stream>>>(p);
+    else if (p.q != nullptr)
+        requant_128x1_T_kernel<true, false><<<grid, kQ3Threads, 0, stream>>>(p);
     else
-        requant_128x1_T_kernel<false><<<grid, kQ3Threads, 0, stream>>>(p);
+        requant_128x1_T_kernel<false, false><<<grid, kQ3Threads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -222,6 +222,25 @@ FP8BS_API fp8bs_status fp8_quant_dual_opts(const void* x, int64_t rows, int64_t 
                                            uint8_t* q, float* scales, uint8_t* qT, float* scalesT,
                                            const fp8bs_scale_opts* opts, void* stream);
 
+/* The forward activation cast and its Wgrad requant in one pass: the 1x128  */
+/* cast of fp8_quant_1x128 and the 128x1 transposed requant of that E4M3     */
+/* result (fp8_requant_128x1_T with FP8BS_SRC_E4M3 on q, scales), both       */
+/* outputs byte-identical to those two calls in sequence. [P1] bullet 2 and  */
+/* "Where casts are drawn": Wgrad's transposed activation operand is a       */
+/* requant of the E4M3 stash the forward saved; this call produces it while  */
+/* the forward cast still holds the tile, saving a second read of the stash  */
+/* and a launch, at the cost of keeping qT from the forward on.              */
+/* Arguments, layouts, constraints and errors as for fp8_quant_dual.         */
+FP8BS_API fp8bs_status fp8_quant_dual_stash(const void* x, int64_t rows, int64_t cols,
+                                            const int32_t* group_offsets_host, int32_t groups,
+                                            uint8_t* q, float* scales, uint8_t* qT, float* scalesT,
+                                            void* stream);
+/* The same with a scale rule (see fp8bs_scale_opts); both casts use it.      */
+FP8BS_API fp8bs_status fp8_quant_dual_stash_opts(const void* x, int64_t rows, int64_t cols,
+                                                 const int32_t* group_offsets_host, int32_t groups,
+                                                 uint8_t* q, float* scales, uint8_t* qT, float* scalesT,
+                                                 const fp8bs_scale_opts* opts, void* stream);
+
 /* NEXT-3: stochastic rounding. The 1x128 and 128x128 casts above with the   */
 /* E4M3 rounding step made stochastic under a stateless (seed, salt,         */
 /* element) contract ([P4] "SR agreement": a stateless seed / salt / counter */

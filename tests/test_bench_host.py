@@ -18,12 +18,11 @@ import bench  # noqa: E402
 def test_step_work_figures():
     flops, b = bench.step_work(4096, 7168, 2048)
     assert flops["fprop"] == 2.0 * 4096 * 7168 * 2048
-    assert set(b) == {"quant_128x128(W)", "quant_1x128(X)", "fprop", "quant_dual(dY)", "dgrad",
-                      "requant_128x1_T(Xq)", "wgrad"}
+    assert set(b) == {"quant_128x128(W)", "quant_dual_stash(X)", "fprop", "quant_dual(dY)", "dgrad", "wgrad"}
     # dual cast: one 2-byte read, two 1-byte payloads, both scale arrays
     assert b["quant_dual(dY)"] == 4096 * 2048 * 4 + 4 * 16 * 4096 + 4 * 32 * 2048
-    # 1x128 quantizer: 2 B read + 1 B written per element + one fp32 scale per 128
-    assert b["quant_1x128(X)"] == 4096 * 7168 * 3 + 4 * 56 * 4096
+    # forward cast of X with the stash requant: the same traffic as a dual cast
+    assert b["quant_dual_stash(X)"] == 4096 * 7168 * 4 + 4 * 56 * 4096 + 4 * 32 * 7168
 
 
 def _free_port():

@@ -250,6 +250,63 @@ def test_quant_dual_moe_grouped_full():
     _check_dual(d["dY"], d["offsets"])
 
 
+def _gpu_dual_stash(x_dev, offsets=None, **r):
+    R, C = x_dev.shape
+    q, sc = fp8bs.empty_quant_1x128(R, C)
+    qT, scT = fp8bs.empty_requant_128x1_T(R, C, offsets)
+    fp8bs.fp8_quant_dual_stash(x_dev, q, sc, qT, scT, offsets=offsets, **r)
+    torch.cuda.synchronize()
+    return np_(q), np_(sc), np_(qT), np_(scT)
+
+
+def _check_dual_stash(x, offsets=None):
+    R, C = x.shape
+    q, sc, qT, scT = _gpu_dual_stash(x.cuda(), offsets)
+    oq, osc = oracle.quant_1x128(u16(x))
+    assert np.array_equal(q, oq)
+    assert np.array_equal(sc[:, :R].view(np.uint32), osc[:, :R].view(np.uint32))
+    oqT, oscT = oracle.requant_128x1_T(oq, osc, offsets=offsets)
+    assert np.array_equal(qT, oqT)
+    assert np.array_equal(scT.view(np.uint32), oscT.view(np.uint32))
+
+
+@pytest.mark.parametrize("M,C,counts", [
+    (128, 128, None), (300, 256, None), (1, 16, None), (257, 400, None), (129, 2048, None),
+    (400, 128, [0, 129, 1, 0, 270]), (131, 144, [131]), (260, 256, [0, 0, 260, 0]),
+])
+def test_quant_dual_stash_matches_cast_then_requant(M, C, counts):
+    """One read of BF16 X gives its 1x128 cast and the 128x1 transposed
+    requant of that E4M3 stash, byte-identical to the oracle's cast followed
+    by its requant of the stash (ragged token tiles and groups included)."""
+    x = _special_inputs(M, C, seed=M + 11 * C)
+    _check_dual_stash(x, None if counts is None else wl.offsets_from_counts(counts))
+
+
+def test_quant_dual_stash_equals_two_calls_full():
+    """At the dense workload's X (4096 x 7168): the fused call and the two
+    separate library calls (cast, then requant of the stash) agree byte for
+    byte; the oracle checks a sample of token tiles."""
+    x = wl.backward()["X"]
+    xd = x.cuda()
+    q, sc, qT, scT = _gpu_dual_stash(xd)
+    q2, sc2 = fp8bs.empty_quant_1x128(*x.shape)
+    fp8bs.fp8_quant_1x128(xd, q2, sc2)
+    qT2, scT2 = fp8bs.empty_requant_128x1_T(*x.shape)
+    fp8bs.fp8_requant_128x1_T(q2, sc2, qT2, scT2)
+    torch.cuda.synchronize()
+    assert np.array_equal(q, np_(q2)) and np.array_equal(sc, np_(sc2))
+    assert np.array_equal(qT, np_(qT2)) and np.array_equal(scT.view(np.uint32), np_(scT2).view(np.uint32))
+    rows = slice(1280, 1536)                       # two token tiles
+    oq, osc = oracle.quant_1x128(u16(x[rows]))
+    oqT, oscT = oracle.requant_128x1_T(oq, osc)
+    assert np.array_equal(qT[:, rows], oqT) and np.array_equal(scT[10:12], oscT)
+
+
+def test_quant_dual_stash_moe_grouped_full():
+    d = wl.moe(with_weights=False)
+    _check_dual_stash(d["dY"][:, :1024].contiguous(), d["offsets"])
+
+
 RULES = [
     dict(rule=fp8bs.SCALE_UE8M0),
     dict(amax_floor=1e-4),
@@ -287,6 +344,7 @@ def test_scale_rules_all_quantizers(r):
     dq, dsc = fp8bs.empty_quant_1x128(M, C)
     dqT, dscT = fp8bs.empty_requant_128x1_T(M, C, off)
     fp8bs.fp8_quant_dual(xd, dq, dsc, dqT, dscT, offsets=off, **r)
+    sq, ssc, sqT, sscT = _gpu_dual_stash(xd, off, **r)
     torch.cuda.synchronize()
 
     oxq0, osx0 = oracle.quant_1x128(u16(x))
@@ -295,6 +353,7 @@ def test_scale_rules_all_quantizers(r):
         owq, osw = oracle.quant_128x128(u16(w))
         oqT, oscT = oracle.requant_128x1_T(u16(x), offsets=off)
         oqTq, oscTq = oracle.requant_128x1_T(oxq0, osx0)
+        oqTs, oscTs = oracle.requant_128x1_T(oq, osc, offsets=off)
     bits = lambda a: np.ascontiguousarray(a).view(np.uint32)
     assert np.array_equal(np_(q), oq) and np.array_equal(bits(np_(sc)[:, :M]), bits(osc[:, :M]))
     assert np.array_equal(np_(wq), owq) and np.array_equal(bits(np_(sw)), bits(osw))
@@ -303,6 +362,8 @@ def test_scale_rules_all_quantizers(r):
     assert np.array_equal(np_(qTq), oqTq) and np.array_equal(bits(np_(scTq)), bits(oscTq))
     assert np.array_equal(np_(dq), oq) and np.array_equal(bits(np_(dsc)[:, :M]), bits(osc[:, :M]))
     assert np.array_equal(np_(dqT), oqT) and np.array_equal(bits(np_(dscT)), bits(oscT))
+    assert np.array_equal(sq, oq) and np.array_equal(bits(ssc[:, :M]), bits(osc[:, :M]))
+    assert np.array_equal(sqT, oqTs) and np.array_equal(bits(sscT), bits(oscTs))
     if r.get("rule") == fp8bs.SCALE_UE8M0:
         mant, _ = np.frexp(np_(sc)[:, :M])
         assert np.all(mant == 0.5)
