@@ -74,7 +74,17 @@ constexpr int kCtlBytes = 512;                  // barriers and flags
 constexpr int kScaleSlots = 8;
 constexpr int kScaleSlotFloats = kBM + kBN;
 constexpr int kScaleBytes = kScaleSlots * kScaleSlotFloats * 4;
-constexpr int kSmemBytes = kStages * kStageBytes + kCtlBytes + kScaleBytes + 1024 /* alignment */;
+// Fprop / Dgrad output stage: per epilogue warp 32 rows x 64 BF16 columns.
+constexpr int kOutStageWarpBytes = 32 * 64 * 2;
+constexpr int kOutStageBytes = kEpiWarps * kOutStageWarpBytes;
+// Dynamic shared memory: the operand ring, the control block, then the
+// Wgrad scale ring or the Fprop / Dgrad output stage.
+template <GemmKind kKind>
+constexpr int smem_bytes()
+{
+    return kStages * kStageBytes + kCtlBytes +
+           (kKind == GemmKind::kVectorScaleF32 ? kScaleBytes : kOutStageBytes) + 1024 /* alignment */;
+}
 
 struct SharedCtl {
     uint64_t full[kStages];
@@ -129,9 +139,13 @@ __device__ __forceinline__ void decode_unit(const GemmParams& p, int u, int& g, 
 
 // Fprop / Dgrad: s_b is one value per 128 output columns, so a K-block's
 // scale is one scalar per thread (row) and half. Layout 32x32b: thread =
-// row, 128 columns in registers; BF16 output in 16-byte row segments.
-__device__ __forceinline__ bool epilogue_block_scale(const GemmParams& p, SharedCtl* ctl, uint32_t tmem_base,
-                                                     int warp, int lane, uint64_t limit)
+// row, 128 columns in registers. The BF16 output goes through a per-warp
+// shared-memory stage so that every global store instruction writes four
+// whole 128-byte row segments (the tile ends of all CTAs coincide, and
+// 16-byte pieces of 32 different rows per instruction made those bursts
+// several times longer).
+__device__ __forceinline__ bool epilogue_block_scale(const GemmParams& p, SharedCtl* ctl, uint8_t* out_stage,
+                                                     uint32_t tmem_base, int warp, int lane, uint64_t limit)
 {
     const int ew = warp - kFirstEpiWarp;
     const int quarter = warp & 3;   // TMEM lanes this warp may access
@@ -209,27 +223,49 @@ __device__ __forceinline__ bool epilogue_block_scale(const GemmParams& p, Shared
             promote(3, rb);
         }
 
-        if (row_ok && cols_ok && p.ws != nullptr) {
-            // split-K: this range's fp32 sum goes to its own slice of the workspace
-            float* w = p.ws + static_cast<int64_t>(split) * p.ws_split_stride + static_cast<int64_t>(row) * p.out_ld + col0;
+        if (p.ws != nullptr) {
+            if (row_ok && cols_ok) {
+                // split-K: this range's fp32 sum goes to its own slice of the workspace
+                float* w = p.ws + static_cast<int64_t>(split) * p.ws_split_stride + static_cast<int64_t>(row) * p.out_ld + col0;
 #pragma unroll
-            for (int v = 0; v < 32; ++v)
-                reinterpret_cast<float4*>(w)[v] =
-                    make_float4(acc[2 * v].x, acc[2 * v].y, acc[2 * v + 1].x, acc[2 * v + 1].y);
-        } else if (row_ok && cols_ok) {
-            uint16_t* y = static_cast<uint16_t*>(p.out) + p.out_off[g] + static_cast<int64_t>(row) * p.out_ld + col0;
+                for (int v = 0; v < 32; ++v)
+                    reinterpret_cast<float4*>(w)[v] =
+                        make_float4(acc[2 * v].x, acc[2 * v].y, acc[2 * v + 1].x, acc[2 * v + 1].y);
+            }
+        } else if (cols_ok) {
+            // Two rounds of 64 columns: each thread writes its row's 64 values
+            // as eight 16-byte chunks (chunk c of row r at slot c ^ (r % 8):
+            // conflict-free), then lanes 8q .. 8q + 7 store one row's 128
+            // contiguous bytes, four rows per instruction.
+            const int rows_left = p.a_rows[g] - (mt * kBM + quarter * 32);   // valid rows of this warp
+            uint16_t* y0 = static_cast<uint16_t*>(p.out) + p.out_off[g] +
+                           static_cast<int64_t>(p.a_row0[g] + mt * kBM + quarter * 32) * p.out_ld + col0;
+            const uint32_t st_base = smem_addr(out_stage) + ew * kOutStageWarpBytes;
 #pragma unroll
-            for (int v = 0; v < 16; ++v) {
-                const float2 a0 = acc[4 * v + 0];
-                const float2 a1 = acc[4 * v + 1];
-                const float2 a2 = acc[4 * v + 2];
-                const float2 a3 = acc[4 * v + 3];
-                uint4 pk;
-                pk.x = pack_bf16x2(a0.x, a0.y);
-                pk.y = pack_bf16x2(a1.x, a1.y);
-                pk.z = pack_bf16x2(a2.x, a2.y);
-                pk.w = pack_bf16x2(a3.x, a3.y);
-                reinterpret_cast<uint4*>(y)[v] = pk;
+            for (int rnd = 0; rnd < 2; ++rnd) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const float2 a0 = acc[32 * rnd + 4 * c + 0];
+                    const float2 a1 = acc[32 * rnd + 4 * c + 1];
+                    const float2 a2 = acc[32 * rnd + 4 * c + 2];
+                    const float2 a3 = acc[32 * rnd + 4 * c + 3];
+                    uint4 pk;
+                    pk.x = pack_bf16x2(a0.x, a0.y);
+                    pk.y = pack_bf16x2(a1.x, a1.y);
+                    pk.z = pack_bf16x2(a2.x, a2.y);
+                    pk.w = pack_bf16x2(a3.x, a3.y);
+                    st_shared_v4(st_base + lane * 128 + ((c ^ (lane & 7)) << 4), pk);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int rr = 4 * i + (lane >> 3);
+                    const int c = lane & 7;
+                    const uint4 v = ld_shared_v4(st_base + rr * 128 + ((c ^ (rr & 7)) << 4));
+                    if (rr < rows_left)
+                        *reinterpret_cast<uint4*>(y0 + static_cast<int64_t>(rr) * p.out_ld + 64 * rnd + 8 * c) = v;
+                }
+                __syncwarp();
             }
         }
     }
@@ -361,7 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sA = smem;
     uint8_t* sB = smem + kStages * kABytes;
     SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + kStages * kStageBytes);
-    float* scale_ring = reinterpret_cast<float*>(smem + kStages * kStageBytes + kCtlBytes);
+    uint8_t* extra = smem + kStages * kStageBytes + kCtlBytes;   // scale ring or output stage
+    float* scale_ring = reinterpret_cast<float*>(extra);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -524,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         setmaxnreg_inc<kEpilogueRegs>();
         bool ok;
         if constexpr (kKind == GemmKind::kBlockScaleBf16)
-            ok = epilogue_block_scale(p, ctl, tmem_base, warp, lane, limit);
+            ok = epilogue_block_scale(p, ctl, extra, tmem_base, warp, lane, limit);
         else
             ok = epilogue_vector_scale(p, ctl, scale_ring, tmem_base, warp, lane, limit);
         if (!ok) {
@@ -590,6 +627,8 @@ cudaError_t launch_kind(const CUtensorMap& map_a, const CUtensorMap& map_b, cons
     if (e != cudaSuccess) return e;
     // the setmaxnreg split assumes this launch allocation (see kLaunchRegs)
     if (static_cast<uint32_t>(attr.numRegs) != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    constexpr int kSmemBytes = smem_bytes<kKind>();
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory");
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     const int units = p.total_tiles * p.splits;
