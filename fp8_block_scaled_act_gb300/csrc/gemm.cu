@@ -20,14 +20,12 @@
 //               accumulate = 0), double-buffered over 2 x 256 TMEM columns,
 //               and commits to mbarriers that free the smem stage and hand
 //               the partial to the epilogue.
-//   warp 2      Wgrad scale producer: all 32 lanes copy each K-block's
-//               scales (the tile's 128 row scales and 256 column scales)
-//               with cp.async into an 8-slot shared-memory ring, running
-//               ahead of the epilogue; the copies complete on an mbarrier.
-//               (Fprop / Dgrad epilogue threads need one scalar per K-block
-//               and prefetch it themselves, two K-blocks ahead; the warp is
-//               idle there.)
-//   warp 3      idle (it completes the first warpgroup, which gives its
+//               For Wgrad it also copies each K-block's scales (the
+//               tile's 128 row scales and 256 column scales) into an
+//               8-slot shared-memory ring with two untiled bulk copies per
+//               K-block (Fprop / Dgrad epilogue threads need one scalar per
+//               K-block and prefetch it themselves, two K-blocks ahead).
+//   warps 2-3   idle (they complete the first warpgroup, which gives its
 //               registers to the epilogue with setmaxnreg).
 //   warps 4-11  promotion epilogue: each warp owns 32 TMEM lanes (rows) and
 //               128 columns; per K-block it loads the fp32 partial with
@@ -91,7 +89,6 @@ struct SharedCtl {
     uint64_t empty[kStages];
     uint64_t tfull[2];
     uint64_t tempty[2];
-    uint64_t sfull[kScaleSlots];   // scale slot landed (one cp.async arrival per producer lane)
     uint64_t sempty[kScaleSlots];  // scale slot read by every epilogue warp
     uint64_t mma_done;        // final commit of the MMA thread (drain before exit)
     uint32_t tmem_base;
@@ -307,11 +304,16 @@ __device__ __forceinline__ bool epilogue_vector_scale(const GemmParams& p, Share
             for (int j = 0; j < 16; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
         for (int kb = 0; kb < nkb; ++kb, ++acc_it) {
+            const uint32_t ss = acc_it % kScaleSlots;
+            const float* slot = ring + ss * kScaleSlotFloats;
+            const uint32_t buf = acc_it & 1u;
+            const uint32_t aph = (acc_it >> 1) & 1u;
+            if (ctl->abort || !mbar_wait(&ctl->tfull[buf], aph, limit)) return false;
+            tc_fence_after_sync();
             // this K-block's scales from the ring: the warp's 4 row scales in
             // registers, the column scales read from the slot while promoting
-            const uint32_t ss = acc_it % kScaleSlots;
-            if (ctl->abort || !mbar_wait(&ctl->sfull[ss], (acc_it / kScaleSlots) & 1u, limit)) return false;
-            const float* slot = ring + ss * kScaleSlotFloats;
+            // (the slot landed with the K-block's operand stage, before its
+            // MMAs were issued, so the wait for the partial above orders it)
             float2 sa2[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -319,11 +321,6 @@ __device__ __forceinline__ bool epilogue_vector_scale(const GemmParams& p, Share
                 sa2[i] = make_float2(v, v);
             }
             const float2* sbp = reinterpret_cast<const float2*>(slot + kBM + half * 128) + t4;
-
-            const uint32_t buf = acc_it & 1u;
-            const uint32_t aph = (acc_it >> 1) & 1u;
-            if (ctl->abort || !mbar_wait(&ctl->tfull[buf], aph, limit)) return false;
-            tc_fence_after_sync();
             const uint32_t taddr = tmem_base + lane_addr + buf * kBN + half * 128;
 
             // promote the 32-column group c (rows g4, g4 + 8 in r[0..15],
@@ -412,10 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&ctl->tfull[a], 1);
             mbar_init(&ctl->tempty[a], kEpiWarps);
         }
-        for (int a = 0; a < kScaleSlots; ++a) {
-            mbar_init(&ctl->sfull[a], 32);
-            mbar_init(&ctl->sempty[a], kEpiWarps);
-        }
+        for (int a = 0; a < kScaleSlots; ++a) mbar_init(&ctl->sempty[a], kEpiWarps);
         mbar_init(&ctl->mma_done, 1);
         ctl->abort = 0;
         fence_mbarrier_init();
@@ -455,8 +449,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&ctl->full[s], kStageBytes);
                     const int x = p.k0[g] + (kb0 + kb) * kBK;
+                    if constexpr (kKind == GemmKind::kVectorScaleF32) {
+                        // Wgrad: this K-block's 128 row scales and the tile's
+                        // column scales go into the scale ring as part of the
+                        // stage's transaction, so they have landed before the
+                        // stage's MMAs are issued and hence before the
+                        // epilogue sees the partial (it needs no wait of its
+                        // own); the slot is reused once the epilogue released it
+                        const uint32_t ss = it % kScaleSlots;
+                        if (ctl->abort || !mbar_wait(&ctl->sempty[ss], ((it / kScaleSlots) & 1u) ^ 1u, limit)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t b_bytes = static_cast<uint32_t>(min(kBN, p.n_cols - nt * kBN)) * 4u;
+                        float* slot = scale_ring + ss * kScaleSlotFloats;
+                        mbar_arrive_expect_tx(&ctl->full[s], kStageBytes + kBM * 4u + b_bytes);
+                        bulk_load(slot, p.sa + static_cast<int64_t>(p.sa_kb0[g] + kb0 + kb) * p.sa_ld + ya, kBM * 4u,
+                                  &ctl->full[s]);
+                        bulk_load(slot + kBM,
+                                  p.sb + p.sb_off[g] + static_cast<int64_t>(kb0 + kb) * p.sb_kstride + nt * kBN,
+                                  b_bytes, &ctl->full[s]);
+                    } else {
+                        mbar_arrive_expect_tx(&ctl->full[s], kStageBytes);
+                    }
                     tma_load_2d(sA + s * kABytes, &map_a, &ctl->full[s], x, ya);
                     tma_load_2d(sB + s * kBBytes, &map_b, &ctl->full[s], x, yb);
                 }
@@ -513,47 +529,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t drain = limit > kDrainLimitNs ? limit : kDrainLimitNs;
             mbar_wait(&ctl->mma_done, 0u, drain);
         }
-    } else if (warp == 2 && kKind == GemmKind::kVectorScaleF32) {
-        // ------------------------------------------------------------------
-        // Scale producer (Wgrad): the same K-block sequence as the TMA producer
-        // ------------------------------------------------------------------
-        uint32_t it = 0;
-        bool ok = true;
-        const int units = p.total_tiles * p.splits;
-        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-            int g, mt, nt, split, kb0, nkb;
-            decode_unit(p, u, g, mt, nt, split, kb0, nkb);
-            // lane l copies the A scales of tile rows 4l .. 4l + 3 and the
-            // column scales of tile columns 8l .. 8l + 7
-            const int arow = p.a_row0[g] + mt * kBM + 4 * lane;
-            const float* sa_src = p.sa + static_cast<int64_t>(p.sa_kb0[g] + kb0) * p.sa_ld + arow;
-            const int col = nt * kBN + 8 * lane;
-            const bool sb_in = col < p.n_cols;                 // n_cols % 128 == 0
-            const float* sb_src = p.sb + p.sb_off[g] + col + static_cast<int64_t>(kb0) * p.sb_kstride;
-            for (int kb = 0; kb < nkb; ++kb, ++it) {
-                const uint32_t s = it % kScaleSlots;
-                if (ctl->abort || !mbar_wait(&ctl->sempty[s], ((it / kScaleSlots) & 1u) ^ 1u, limit)) {
-                    ok = false;
-                    break;
-                }
-                float* slot = scale_ring + s * kScaleSlotFloats;
-                const float* a_k = sa_src + static_cast<int64_t>(kb) * p.sa_ld;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const bool in = arow + i < p.sa_rows;
-                    cp_async_4(slot + 4 * lane + i, in ? a_k + i : p.sa, in ? 4u : 0u);
-                }
-                const float* b_k = sb_src + static_cast<int64_t>(kb) * p.sb_kstride;
-                cp_async_16(slot + kBM + 8 * lane, sb_in ? b_k : p.sb, sb_in ? 16u : 0u);
-                cp_async_16(slot + kBM + 8 * lane + 4, sb_in ? b_k + 4 : p.sb, sb_in ? 16u : 0u);
-                cp_async_mbar_arrive_noinc(&ctl->sfull[s]);
-            }
-        }
-        if (!ok) {
-            if (lane == 0) record_status(p.status, FP8BS_ERR_TIMEOUT);
-            ctl->abort = 1;
-        }
-        cp_async_wait_all();   // no copy into the ring outlives the CTA
     } else if (warp >= kFirstEpiWarp) {
         // ------------------------------------------------------------------
         // Promotion epilogue

@@ -117,6 +117,17 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
     return v;
 }
 
+// Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global to shared memory; completion is signalled on `bar`
+// as transaction bytes.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // cp.async (global -> shared, asynchronous, no registers held)
 // ---------------------------------------------------------------------------
@@ -140,19 +151,6 @@ __device__ __forceinline__ void cp_async_16(void* dst, const void* src, uint32_t
 __device__ __forceinline__ void cp_async_commit()
 {
     asm volatile("cp.async.commit_group;" ::: "memory");
-}
-
-// Arrives on `bar` once every cp.async this thread has issued so far has
-// completed. The arrival does not raise the barrier's expected count, so the
-// barrier's init count includes one such arrival per issuing thread.
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all()
-{
-    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // Waits until at most kPending of this thread's most recent groups are pending.
