@@ -12,10 +12,12 @@ workload (K = 1024 ... 65536).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Timing: W untimed warm-up steps, then exactly K steps, each bracketed by CUDA
-events on the launching stream with an L2 flush (a 256 MiB write) between
-steps outside the events; a second pass of K steps with an event after every
-kernel gives the per-kernel table and the roofline figures. Under torchrun each rank runs its own replica (weak
+Timing: W untimed warm-up steps, then exactly K steps, each one replay of a
+CUDA graph of the step (--no-graph: stream launches) bracketed by CUDA
+events on the launching stream, with an L2 flush (a 256 MiB write) between
+steps outside the events; a second pass of K steps launched kernel by kernel
+with an event after every kernel gives the per-kernel table and the
+roofline figures. Under torchrun each rank runs its own replica (weak
 scaling, no collective on the data path); the step time is the max over
 ranks. Rank 0 prints one JSON line.
 """
@@ -217,6 +219,7 @@ class DenseStep:
         self.dyT, self.sdyT = e.empty_requant_128x1_T(M, N, device=device)
         self.dW = torch.empty(N, K, dtype=torch.float32, device=device)
         self.names = ["quant_128x128(W)", "quant_dual_stash(X)", "fprop", "quant_dual(dY)", "dgrad", "wgrad"]
+        self.side = torch.cuda.Stream(device)
 
     def work(self):
         return step_work(self.M, self.K, self.N)
@@ -241,6 +244,38 @@ class DenseStep:
             lambda: e.fp8_block_gemm_dgrad(self.dyq, self.sdy, self.wq, self.sw, self.dX),
             lambda: e.fp8_block_gemm_wgrad(self.dyT, self.sdyT, self.xT, self.sxT, self.dW),
         ]
+
+
+    def run_dag(self):
+        """The step with its two independent pairs on two streams: the W and
+        X casts of the forward, then Dgrad and Wgrad of the backward."""
+        torch, L = self.torch, self.launches_cached()
+        main = torch.cuda.current_stream()
+        fork = torch.cuda.Event()
+        fork.record(main)
+        self.side.wait_event(fork)
+        with torch.cuda.stream(self.side):
+            L[0]()                                  # W cast
+        w_done = torch.cuda.Event()
+        w_done.record(self.side)
+        L[1]()                                      # X cast + stash requant
+        main.wait_event(w_done)
+        L[2]()                                      # Fprop
+        L[3]()                                      # dY dual cast
+        dy_done = torch.cuda.Event()
+        dy_done.record(main)
+        self.side.wait_event(dy_done)
+        with torch.cuda.stream(self.side):
+            L[5]()                                  # Wgrad
+        wg_done = torch.cuda.Event()
+        wg_done.record(self.side)
+        L[4]()                                      # Dgrad
+        main.wait_event(wg_done)
+
+    def launches_cached(self):
+        if not hasattr(self, "_launches"):
+            self._launches = self.launches()
+        return self._launches
 
 
 class MoeStep:
@@ -409,12 +444,36 @@ def run_ours(args, world, rank, local):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
 
-    for _ in range(args.warmup):
+    def run_seq():
         for f in launches:
             f()
+
+    for _ in range(args.warmup):
+        run_seq()
     torch.cuda.synchronize()
     if fp8bs.fp8bs_device_status(reset=True) != 0:
         raise RuntimeError("device status error during warm-up")
+    # The timed steps replay one CUDA graph of the step (the same kernels,
+    # without per-launch host overhead); the dense step's graph runs its two
+    # independent pairs on two streams.
+    run_step, launch_mode = run_seq, "stream launches"
+    if not args.no_graph:
+        dag = getattr(step, "run_dag", run_seq)
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                dag()
+            torch.cuda.synchronize()
+            for _ in range(2):
+                graph.replay()
+            torch.cuda.synchronize()
+            run_step = graph.replay
+            launch_mode = ("CUDA graph, two streams (W || X casts, Dgrad || Wgrad)"
+                           if hasattr(step, "run_dag") else "CUDA graph")
+        except Exception as ex:   # capture unsupported: time the stream launches
+            launch_mode = f"stream launches (graph capture failed: {type(ex).__name__})"
+        if fp8bs.fp8bs_device_status(reset=True) != 0:
+            raise RuntimeError("device status error during graph warm-up")
 
     nk = len(launches)
     # Timed region: exactly K steps with CUDA events at the step boundaries
@@ -430,8 +489,7 @@ def run_ours(args, world, rank, local):
     for s in range(args.steps):
         flush.fill_(s & 0xFF)                      # L2 flush, outside the step's events
         sev[s][0].record(stream)
-        for f in launches:
-            f()
+        run_step()
         sev[s][1].record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -503,14 +561,16 @@ def run_ours(args, world, rank, local):
                  "longk": "synthetic (seeded uniform U(0.5, 1.5))"}[args.workload],
         "config": dict(step.describe(),
                        parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
-                       l2="flushed between steps (256 MiB write outside the step events)"),
+                       l2="flushed between steps (256 MiB write outside the step events)",
+                       launch=launch_mode),
         "quantize_gbs": round(q_bytes / (q_ms * 1e-3) / 1e9, 1),
         "quantize_frac_hbm": round(q_bytes / (q_ms * 1e-3) / 1e9 / hbm_peak, 4),
         "gemm_frac_fp8_peak": round(value / fp8_peak, 4),
         "roofline": roof, "kernels": kernels,
-        "kernels_note": ("per-kernel times from a second pass of the same K steps with an event after every "
-                         "kernel (each includes one event's cost, a few us); ms_per_step and value come from the "
-                         "timed steps with events at step boundaries only"),
+        "kernels_note": ("per-kernel times from a second pass of the same K steps launched one kernel at a "
+                         "time on one stream with an event after every kernel (each includes one event's cost, "
+                         "a few us); ms_per_step and value come from the timed steps with events at step "
+                         "boundaries only"),
         "e2e": e2e,
         "gpu_launches": nk * args.steps, "clocks": clk,
     }
@@ -784,6 +844,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time the step as stream launches instead of one CUDA graph replay")
     ap.add_argument("--workload", choices=["dense", "moe", "longk"], default="dense",
                     help="dense: the linear layer's fwd+bwd (default); moe: grouped expert pass; "
                          "longk: 256xKx256 split-K Fprop for K up to 65536")
