@@ -614,17 +614,42 @@ __global__ void __launch_bounds__(kQ3Threads, kDual ? 3 : 4) requant_128x1_T_ker
         if constexpr (kDual) {
             // Row-wise (1x128) cast of the same rows from the registers: a
             // row's 128 channels are the 16 chunks held by 16 consecutive
-            // lanes, so its absmax is a 4-step xor-shuffle over those lanes.
+            // lanes. Their absmax is a reduce-scatter butterfly over those
+            // lanes (at xor distances 8, 4, 2 a lane trades half of its
+            // running maxima and keeps the half its lane bit selects, then
+            // one more step at distance 1), after which lanes 2i and 2i + 1
+            // of the group hold row i's absmax. Each lane computes the scale
+            // of that one row, and the eight scales (and negated
+            // reciprocals) are then read back from their owners.
             uint32_t rm[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) rm[i] = absmax_bits_8(d[i]);
 #pragma unroll
-            for (int off = 8; off >= 1; off >>= 1)
+            for (int j = 0; j < 4; ++j) {
+                const bool up = (chunk & 8) != 0;
+                const uint32_t send = up ? rm[j] : rm[j + 4];
+                rm[j] = max(up ? rm[j + 4] : rm[j], __shfl_xor_sync(0xFFFFFFFFu, send, 8));
+            }
 #pragma unroll
-                for (int i = 0; i < 8; ++i) rm[i] = max(rm[i], __shfl_xor_sync(0xFFFFFFFFu, rm[i], off));
+            for (int j = 0; j < 2; ++j) {
+                const bool up = (chunk & 4) != 0;
+                const uint32_t send = up ? rm[j] : rm[j + 2];
+                rm[j] = max(up ? rm[j + 2] : rm[j], __shfl_xor_sync(0xFFFFFFFFu, send, 4));
+            }
+            {
+                const bool up = (chunk & 2) != 0;
+                const uint32_t send = up ? rm[0] : rm[1];
+                rm[0] = max(up ? rm[1] : rm[0], __shfl_xor_sync(0xFFFFFFFFu, send, 2));
+            }
+            rm[0] = max(rm[0], __shfl_xor_sync(0xFFFFFFFFu, rm[0], 1));
+            const TileScale own = tile_scale(__uint_as_float(rm[0] << 16), p.rule);   // row (chunk >> 1)
+            const int group = threadIdx.x & 16;   // first lane of this 16-lane group in the warp
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int rl = rg * 8 + i;
+                TileScale ts;
+                ts.s = __shfl_sync(0xFFFFFFFFu, own.s, group | (2 * i));
+                ts.nr = __shfl_sync(0xFFFFFFFFu, own.nr, group | (2 * i));
                 if (rl >= len) {
                     if constexpr (kStash) {
                         // padding rows: zero codes and scale, as an E4M3 source stages them
@@ -633,7 +658,6 @@ __global__ void __launch_bounds__(kQ3Threads, kDual ? 3 : 4) requant_128x1_T_ker
                     }
                     continue;
                 }
-                const TileScale ts = tile_scale(__uint_as_float(rm[i] << 16), p.rule);
                 if (chunk == 0) p.q_scales[(c0 / 128) * p.q_scale_ld + r0 + rl] = ts.s;
                 const uint2 codes = quant8(d[i], ts);
                 if (ch_ok) *reinterpret_cast<uint2*>(p.q + (r0 + rl) * p.cols + c0 + chunk * 8) = codes;
