@@ -583,7 +583,7 @@ __global__ void __launch_bounds__(kQ3Threads, kDual ? 3 : 4) requant_128x1_T_ker
     __shared__ __align__(16) uint8_t stage[128 * 128 * 2];
     __shared__ float row_scale[128];
     __shared__ float col_part[16][128];
-    __shared__ float col_scale[128];
+    __shared__ TileScale col_scale[128];   // per channel: s and its negated reciprocal
 
     const int tile = blockIdx.x;                 // padded token tile
     const int64_t c0 = (int64_t)blockIdx.y * 128;
@@ -745,7 +745,7 @@ __global__ void __launch_bounds__(kQ3Threads, kDual ? 3 : 4) requant_128x1_T_ker
 #pragma unroll
         for (int i = 0; i < 16; ++i) m = fmaxf(m, col_part[i][threadIdx.x]);
         const float s = scale_from_amax(m, p.rule);
-        col_scale[threadIdx.x] = s;
+        col_scale[threadIdx.x] = tile_scale_from_s(s);
         if (threadIdx.x < nch) p.scT[(int64_t)tile * p.cols + c0 + threadIdx.x] = s;
     }
     __syncthreads();
@@ -755,8 +755,8 @@ __global__ void __launch_bounds__(kQ3Threads, kDual ? 3 : 4) requant_128x1_T_ker
         const int j = 2 * (threadIdx.x & 63);
         const int part = threadIdx.x >> 6;
         if (j < nch) {   // nch % 16 == 0: pairs are all-in or all-out
-            const TileScale t0 = tile_scale_from_s(col_scale[j]);
-            const TileScale t1 = tile_scale_from_s(col_scale[j + 1]);
+            const TileScale t0 = col_scale[j];
+            const TileScale t1 = col_scale[j + 1];
             uint8_t* dst0 = p.qT + (c0 + j) * p.mpad + (int64_t)tile * 128 + part * 32;
             uint8_t* dst1 = dst0 + p.mpad;
             uint32_t w0[8], w1[8];
@@ -776,7 +776,7 @@ __global__ void __launch_bounds__(kQ3Threads, kDual ? 3 : 4) requant_128x1_T_ker
         if (j < nch) {
             TileScale ts[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) ts[c] = tile_scale_from_s(col_scale[j + c]);
+            for (int c = 0; c < 4; ++c) ts[c] = col_scale[j + c];
             uint8_t* dst = p.qT + (c0 + j) * p.mpad + (int64_t)tile * 128 + part * 16;
             uint32_t w[4][4];
             if (requant_quad_e4m3(stage, row_scale, part, j, ts, w)) {
