@@ -36,6 +36,7 @@ __all__ = [
     "fp8_requant_128x1_T_opts", "fp8_quant_dual_opts", "fp8_quant_1x128_sr", "fp8_quant_128x128_sr",
     "fp8_quant_dual_stash", "fp8_quant_dual_stash_opts",
     "fp8bs_mx_scale_bytes", "fp8_mx_quant_1x32", "fp8_mx_gemm", "empty_mx_quant",
+    "fp8_mx_quant_1x32_T", "fp8_mx_gemm_f32", "empty_mx_quant_T",
 ]
 
 SRC_BF16, SRC_E4M3 = 0, 1
@@ -100,6 +101,8 @@ def lib() -> ctypes.CDLL:
         "fp8bs_mx_scale_bytes": ([I64, I64], I64),
         "fp8_mx_quant_1x32": ([P, I64, I64, P, P, P], S),
         "fp8_mx_gemm": ([P, P, P, P, I64, I64, I64, P, P], S),
+        "fp8_mx_gemm_f32": ([P, P, P, P, I64, I64, I64, P, P], S),
+        "fp8_mx_quant_1x32_T": ([P, I64, I64, P, P, P], S),
         "fp8_quant_128x128_sr": ([P, I64, I64, I64, I64, P, P, P, ctypes.c_uint64, ctypes.c_uint32, P, P], S),
         "fp8_block_gemm_fprop": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_block_gemm_dgrad": ([P, P, P, P, I64, I64, I64, P, P], S),
@@ -382,16 +385,45 @@ def fp8_mx_quant_1x32(x, q, scale_atoms, stream=None) -> None:
 
 
 def fp8_mx_gemm(a, a_atoms, b, b_atoms, out, stream=None) -> None:
-    """out [M x N] (BF16) = A [M x K] . B [N x K]^T, both MXFP8 along K."""
+    """out [M x N] (BF16, or FP32 through fp8_mx_gemm_f32) = A [M x K] . B [N x K]^T,
+    both MXFP8 along K."""
+    f32 = out.dtype == torch.float32
     for t, n, d in ((a, "a", torch.uint8), (a_atoms, "a_atoms", torch.uint8), (b, "b", torch.uint8),
-                    (b_atoms, "b_atoms", torch.uint8), (out, "out", torch.bfloat16)):
+                    (b_atoms, "b_atoms", torch.uint8), (out, "out", torch.float32 if f32 else torch.bfloat16)):
         _need(t, d, n)
     M, K = a.shape
     N = b.shape[0]
     if b.shape != (N, K) or out.shape != (M, N):
         raise ValueError("shape mismatch")
-    _check("fp8_mx_gemm", lib().fp8_mx_gemm(_ptr(a), _ptr(a_atoms), _ptr(b), _ptr(b_atoms), M, N, K,
-                                            _ptr(out), _stream(stream)))
+    name = "fp8_mx_gemm_f32" if f32 else "fp8_mx_gemm"
+    _check(name, getattr(lib(), name)(_ptr(a), _ptr(a_atoms), _ptr(b), _ptr(b_atoms), M, N, K,
+                                      _ptr(out), _stream(stream)))
+
+
+def fp8_mx_gemm_f32(a, a_atoms, b, b_atoms, out, stream=None) -> None:
+    """fp8_mx_gemm with an FP32 output tensor (the Wgrad form)."""
+    _need(out, torch.float32, "out")
+    fp8_mx_gemm(a, a_atoms, b, b_atoms, out, stream)
+
+
+def empty_mx_quant_T(rows: int, cols: int, device="cuda"):
+    """(qT uint8 [cols x Mpad], scale atoms) for fp8_mx_quant_1x32_T of a
+    [rows x cols] tensor; Mpad = 128 * ceil(rows / 128)."""
+    mp = (rows + 127) // 128 * 128
+    return empty_mx_quant(cols, mp, device)
+
+
+def fp8_mx_quant_1x32_T(x, qT, scale_atoms, stream=None) -> None:
+    """Transposed MXFP8 cast of BF16 x [rows x cols]: 32-row blocks, qT [cols x Mpad]."""
+    _need(x, torch.bfloat16, "x"); _need(qT, torch.uint8, "qT"); _need(scale_atoms, torch.uint8, "scale_atoms")
+    rows, cols = x.shape
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    mp = (rows + 127) // 128 * 128
+    if qT.shape != (cols, mp) or scale_atoms.numel() < fp8bs_mx_scale_bytes(cols, mp):
+        raise ValueError("output shapes do not match empty_mx_quant_T")
+    _check("fp8_mx_quant_1x32_T", lib().fp8_mx_quant_1x32_T(_ptr(x), rows, cols, _ptr(qT), _ptr(scale_atoms),
+                                                            _stream(stream)))
 
 
 def _rule_kwargs(opts: Optional[ScaleOpts]) -> dict:

@@ -70,6 +70,12 @@ fp8bs_status device_state(DeviceState** out)
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The MXFP8 GEMM with BF16 (out_bf16) or FP32 (out_f32) output (defined
+// after the extern "C" wrappers).
+fp8bs_status mx_gemm_common(const uint8_t* a, const uint8_t* a_scale_atoms, const uint8_t* b,
+                            const uint8_t* b_scale_atoms, int64_t M, int64_t N, int64_t K, uint16_t* out_bf16,
+                            float* out_f32, void* stream);
+
 // The quantizer entry points with an optional stochastic-rounding key
 // (defined after the extern "C" wrappers).
 fp8bs_status quant_1x128_common(const void* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q,
@@ -572,9 +578,45 @@ fp8bs_status fp8_mx_quant_1x32(const void* x, int64_t rows, int64_t cols, uint8_
                                               st->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
+fp8bs_status fp8_mx_quant_1x32_T(const void* x, int64_t rows, int64_t cols, uint8_t* qT, uint8_t* scale_atoms,
+                                 void* stream)
+{
+    if (rows < 0 || cols <= 0) return FP8BS_ERR_ARG;
+    if (cols % 16 != 0 || rows > 0x7FFFFF00 || cols > 0x7FFFFF00) return FP8BS_ERR_SHAPE;
+    if (rows == 0) return FP8BS_OK;
+    if (!x || !qT || !scale_atoms) return FP8BS_ERR_ARG;
+    if (!aligned16(x) || !aligned16(qT) || !aligned16(scale_atoms)) return FP8BS_ERR_ALIGN;
+    DeviceState* st = nullptr;
+    fp8bs_status s = device_state(&st);
+    if (s != FP8BS_OK) return s;
+    return launch_status(launch_mx_quant_1x32_T(static_cast<const uint16_t*>(x), rows, cols, qT, scale_atoms,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 fp8bs_status fp8_mx_gemm(const uint8_t* a, const uint8_t* a_scale_atoms, const uint8_t* b,
                          const uint8_t* b_scale_atoms, int64_t M, int64_t N, int64_t K, void* out, void* stream)
 {
+    return mx_gemm_common(a, a_scale_atoms, b, b_scale_atoms, M, N, K, static_cast<uint16_t*>(out), nullptr,
+                          stream);
+}
+
+fp8bs_status fp8_mx_gemm_f32(const uint8_t* a, const uint8_t* a_scale_atoms, const uint8_t* b,
+                             const uint8_t* b_scale_atoms, int64_t M, int64_t N, int64_t K, float* out,
+                             void* stream)
+{
+    return mx_gemm_common(a, a_scale_atoms, b, b_scale_atoms, M, N, K, nullptr, out, stream);
+}
+
+}  // extern "C"
+
+namespace fp8bs {
+namespace {
+
+fp8bs_status mx_gemm_common(const uint8_t* a, const uint8_t* a_scale_atoms, const uint8_t* b,
+                            const uint8_t* b_scale_atoms, int64_t M, int64_t N, int64_t K, uint16_t* out_bf16,
+                            float* out_f32, void* stream)
+{
+    void* out = out_bf16 ? static_cast<void*>(out_bf16) : static_cast<void*>(out_f32);
     if (M < 0 || N <= 0 || K <= 0) return FP8BS_ERR_ARG;
     if (K % 128 != 0 || N % 256 != 0 || M > 0x7FFFFF00 || N > 0x7FFFFFFF || K > 0x7FFFFFFF)
         return FP8BS_ERR_SHAPE;
@@ -589,10 +631,15 @@ fp8bs_status fp8_mx_gemm(const uint8_t* a, const uint8_t* a_scale_atoms, const u
     CUtensorMap ma, mb;
     if (!make_map(&ma, a, K, M, K, kBM) || !make_map(&mb, b, K, N, K, kBN)) return FP8BS_ERR_ARG;
     return launch_status(launch_mx_gemm(ma, mb, a_scale_atoms, b_scale_atoms, static_cast<int>(M),
-                                        static_cast<int>(N), static_cast<int>(K), static_cast<uint16_t*>(out),
+                                        static_cast<int>(N), static_cast<int>(K), out_bf16, out_f32,
                                         g_wait_limit_ns, st->status, st->num_sms,
                                         static_cast<cudaStream_t>(stream)));
 }
+
+}  // namespace
+}  // namespace fp8bs
+
+extern "C" {
 
 size_t fp8bs_splitk_workspace_size(int op, int64_t M, int64_t N, int64_t K, int32_t splits)
 {

@@ -120,9 +120,12 @@ cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t split_stri
 // MXFP8 (mx.cu): 1x32 quantizer writing scale atoms, and the block-scaled GEMM.
 cudaError_t launch_mx_quant_1x32(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* q, uint8_t* atoms,
                                  int num_sms, cudaStream_t stream);
+cudaError_t launch_mx_quant_1x32_T(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* qT, uint8_t* atoms,
+                                   cudaStream_t stream);
+// out (BF16) or out_f32 (FP32, when not null) [M x N]
 cudaError_t launch_mx_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const uint8_t* sfa,
-                           const uint8_t* sfb, int M, int N, int K, uint16_t* out, uint64_t wait_limit_ns,
-                           unsigned int* status, int num_sms, cudaStream_t stream);
+                           const uint8_t* sfb, int M, int N, int K, uint16_t* out, float* out_f32,
+                           uint64_t wait_limit_ns, unsigned int* status, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_selftest_wait(unsigned int* status, uint64_t limit_ns, cudaStream_t stream);
 

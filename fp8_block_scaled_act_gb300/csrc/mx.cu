@@ -17,7 +17,7 @@
 //
 // GEMM: out[i, j] = sum_k A[i, k] B[j, k] with both operands blocked along
 // K (A = activations [M x K], B = the other operand [N x K]), fp32
-// accumulation in tensor memory over the whole K, BF16 output. One CTA per SM,
+// accumulation in tensor memory over the whole K, BF16 or FP32 output. One CTA per SM,
 // 128 x 256 tiles, a 4-stage TMA ring of (A, B, A scales, B scales); per
 // 128-K stage one thread copies the scales into tensor memory
 // (tcgen05.cp.32x128b.warpx4) and issues four
@@ -115,6 +115,79 @@ __global__ void __launch_bounds__(kMxQThreads) mx_quant_1x32_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// Transposed quantizer: the 1x32 cast of x^T, i.e. 32-token blocks along the
+// rows of qT [cols x rows_pad]. One CTA per (128-token tile, 128-channel
+// block): the BF16 block is staged in shared memory (coalesced along
+// channels), then each thread casts two (channel, 32-token block) units read
+// down the staged columns, and the CTA's 512 exponent bytes (exactly one
+// scale atom of qT) leave as one contiguous 512-byte write.
+// ---------------------------------------------------------------------------
+constexpr int kMxTThreads = 256;
+
+__global__ void __launch_bounds__(kMxTThreads) mx_quant_1x32_T_kernel(
+    const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t rows_pad, uint8_t* __restrict__ qT,
+    uint8_t* __restrict__ atoms)
+{
+    __shared__ __align__(16) uint16_t stage[128][128];
+    __shared__ __align__(16) uint8_t sf[512];
+    const int tile = blockIdx.x;                       // 128-token tile
+    const int cb = blockIdx.y;                         // 128-channel block
+    const int64_t r0 = static_cast<int64_t>(tile) * 128;
+    const int64_t c0 = static_cast<int64_t>(cb) * 128;
+    {
+        const int chunk = threadIdx.x & 15, rg = threadIdx.x >> 4;
+        const int64_t c = c0 + chunk * 8;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int rl = rg * 8 + i;
+            const int64_t r = r0 + rl;
+            uint4 d = make_uint4(0u, 0u, 0u, 0u);
+            if (r < rows && c < cols) d = __ldcs(reinterpret_cast<const uint4*>(x + r * cols + c));
+            *reinterpret_cast<uint4*>(&stage[rl][chunk * 8]) = d;
+        }
+    }
+    __syncthreads();
+    const int ch = threadIdx.x & 127;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int j = 2 * (threadIdx.x >> 7) + u;     // 32-token block of the tile
+        uint32_t v[32];
+        uint32_t m = 0u;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            v[k] = stage[32 * j + k][ch];
+            m = max(m, v[k] & 0x7FFFu);
+        }
+        const uint32_t E = mx_scale_byte(__uint_as_float(m << 16));
+        const float inv = E >= 1u && E <= 253u ? __uint_as_float((254u - E) << 23) : 0.0f;
+        const float X = __uint_as_float(E >= 1u ? (E << 23) : 0x00400000u);   // 2^(E - 127)
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            float f[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float val = __uint_as_float(v[4 * k + e] << 16);
+                f[e] = inv != 0.0f ? __fmul_rn(val, inv) : __fdiv_rn(val, X);
+            }
+            w[k] = cvt_e4m3x2(f[0], f[1]) | (cvt_e4m3x2(f[2], f[3]) << 16);
+        }
+        if (c0 + ch < cols) {
+            uint4* dst = reinterpret_cast<uint4*>(qT + (c0 + ch) * rows_pad + r0 + 32 * j);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+        // row ch of the atom, 32-block j: byte 16 (ch % 32) + 4 (ch / 32) + j
+        sf[16 * (ch & 31) + 4 * (ch >> 5) + j] = static_cast<uint8_t>(E);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        uint8_t* atom = atoms + (static_cast<int64_t>(cb) * (rows_pad / 128) + tile) * 512;
+        reinterpret_cast<uint4*>(atom)[threadIdx.x] = reinterpret_cast<const uint4*>(sf)[threadIdx.x];
+    }
+}
+
+// ---------------------------------------------------------------------------
 // GEMM
 // ---------------------------------------------------------------------------
 constexpr int kStages = 4;
@@ -152,7 +225,8 @@ struct MxParams {
     const uint8_t* sfb;   // B scale atoms [N/128][K/128][512]
     int m_tiles, n_tiles, kblocks;
     int M, N;
-    uint16_t* out;        // BF16 [M x N]
+    uint16_t* out;        // BF16 [M x N], or
+    float* out_f32;       // FP32 [M x N] (when not null)
     uint64_t wait_limit_ns;
     unsigned int* status;
 };
@@ -213,6 +287,8 @@ __device__ __forceinline__ void record_status(unsigned int* status, unsigned int
     atomicCAS(status, 0u, code);
 }
 
+// kF32: FP32 output (p.out_f32) instead of BF16 (p.out).
+template <bool kF32>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ MxParams p)
@@ -350,6 +426,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row = mt * kBM + quarter * 32 + lane;
             const int col0 = nt * kBN + half * 128;
             uint32_t ra[32], rb[32];
+            if constexpr (kF32) {
+                // FP32 output: each 32-column chunk goes out as it is read
+                const bool st_ok = row < p.M && col0 < p.N;
+                float4* y = reinterpret_cast<float4*>(p.out_f32 + static_cast<int64_t>(row) * p.N + col0);
+#pragma unroll
+                for (int c = 0; c < 4; c += 2) {
+                    tmem_ld_x32(tmem_base + lane_addr + half * 128 + 32 * c, ra);
+                    tmem_ld_x32(tmem_base + lane_addr + half * 128 + 32 * c + 32, rb);
+                    tmem_ld_wait(ra);
+                    tmem_ld_wait(rb);
+                    if (c == 2) {
+                        tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&ctl->tempty);
+                    }
+                    if (st_ok) {
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            y[8 * c + v] = make_float4(__uint_as_float(ra[4 * v]), __uint_as_float(ra[4 * v + 1]),
+                                                       __uint_as_float(ra[4 * v + 2]), __uint_as_float(ra[4 * v + 3]));
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            y[8 * c + 8 + v] = make_float4(__uint_as_float(rb[4 * v]), __uint_as_float(rb[4 * v + 1]),
+                                                           __uint_as_float(rb[4 * v + 2]), __uint_as_float(rb[4 * v + 3]));
+                    }
+                }
+                continue;
+            }
             uint32_t pk[64];
             tmem_ld_x32(tmem_base + lane_addr + half * 128, ra);
             tmem_ld_x32(tmem_base + lane_addr + half * 128 + 32, rb);
@@ -408,9 +512,21 @@ cudaError_t launch_mx_quant_1x32(const uint16_t* x, int64_t rows, int64_t cols, 
     return cudaGetLastError();
 }
 
+cudaError_t launch_mx_quant_1x32_T(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* qT, uint8_t* atoms,
+                                   cudaStream_t stream)
+{
+    const int64_t rows_pad = (rows + 127) / 128 * 128;
+    const int64_t tiles = rows_pad / 128, cblocks = (cols + 127) / 128;
+    if (tiles == 0 || cblocks == 0) return cudaSuccess;
+    if (tiles > 0x7FFFFFFF || cblocks > 65535) return cudaErrorInvalidValue;
+    mx_quant_1x32_T_kernel<<<dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(cblocks)), kMxTThreads, 0,
+                             stream>>>(x, rows, cols, rows_pad, qT, atoms);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_mx_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const uint8_t* sfa,
-                           const uint8_t* sfb, int M, int N, int K, uint16_t* out, uint64_t wait_limit_ns,
-                           unsigned int* status, int num_sms, cudaStream_t stream)
+                           const uint8_t* sfb, int M, int N, int K, uint16_t* out, float* out_f32,
+                           uint64_t wait_limit_ns, unsigned int* status, int num_sms, cudaStream_t stream)
 {
     static_assert(sizeof(MxCtl) <= kCtlBytes, "control block");
     MxParams p;
@@ -422,11 +538,12 @@ cudaError_t launch_mx_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, c
     p.M = M;
     p.N = N;
     p.out = out;
+    p.out_f32 = out_f32;
     p.wait_limit_ns = wait_limit_ns;
     p.status = status;
     const int total = p.m_tiles * p.n_tiles;
     if (total == 0) return cudaSuccess;
-    auto kernel = mx_gemm_kernel;
+    auto kernel = out_f32 != nullptr ? mx_gemm_kernel<true> : mx_gemm_kernel<false>;
     cudaFuncAttributes attr;
     cudaError_t e = cudaFuncGetAttributes(&attr, kernel);
     if (e != cudaSuccess) return e;

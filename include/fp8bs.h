@@ -404,6 +404,26 @@ FP8BS_API fp8bs_status fp8_mx_gemm(const uint8_t* a, const uint8_t* a_scale_atom
                                    const uint8_t* b, const uint8_t* b_scale_atoms,
                                    int64_t M, int64_t N, int64_t K, void* out, void* stream);
 
+/* The same GEMM with FP32 output [M x N] (the Wgrad form: dW = dY^T X with   */
+/* A = the transposed cast of dY and B = the transposed cast of X).          */
+FP8BS_API fp8bs_status fp8_mx_gemm_f32(const uint8_t* a, const uint8_t* a_scale_atoms,
+                                       const uint8_t* b, const uint8_t* b_scale_atoms,
+                                       int64_t M, int64_t N, int64_t K, float* out, void* stream);
+
+/* Transposed MXFP8 cast: the fp8_mx_quant_1x32 cast of x^T, i.e. blocks of  */
+/* 32 consecutive rows (tokens) of x. It gives the operands whose contraction */
+/* runs along x's rows: dY^T and X^T for Wgrad, W^T (from W [K x N]) for      */
+/* Fprop.                                                                     */
+/* x       : BF16 [rows x cols], dense, cols % 16 == 0.                       */
+/* qT      : E4M3 [cols x Mpad], Mpad = 128 * ceil(rows / 128); the padding   */
+/*           tokens are written as 0x00.                                      */
+/* scale_atoms : fp8bs_mx_scale_bytes(cols, Mpad) bytes, the atoms of qT (a   */
+/*           [cols x Mpad] matrix), padding rows 127.                          */
+/* The result is byte-identical to fp8_mx_quant_1x32 of the zero-padded       */
+/* transpose.                                                                 */
+FP8BS_API fp8bs_status fp8_mx_quant_1x32_T(const void* x, int64_t rows, int64_t cols, uint8_t* qT,
+                                           uint8_t* scale_atoms, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* S7. Grouped (MoE expert) GEMMs                                             */
 /* The dense definitions above applied to each group (expert) g, whose token  */

@@ -89,3 +89,120 @@ def test_mx_gemm_dense_fprop_sampled():
     da, db = np.abs(_dequant(oqa, oea)), np.abs(_dequant(oqb, oeb))
     absprod = np.einsum("ek,ek->e", da[ii], db[jj])
     assert_gemm_close(bf16_values(out)[ii, jj], ref, absprod, True, "mx dense fprop")
+
+
+def _pad_rows(x_cpu, mult=128):
+    R, C = x_cpu.shape
+    rp = (R + mult - 1) // mult * mult
+    out = torch.zeros((rp, C), dtype=x_cpu.dtype)
+    out[:R] = x_cpu
+    return out
+
+
+def mx_quant_T(x_cpu):
+    R, C = x_cpu.shape
+    qT, at = fp8bs.empty_mx_quant_T(R, C)
+    fp8bs.fp8_mx_quant_1x32_T(x_cpu.cuda(), qT, at)
+    torch.cuda.synchronize()
+    return qT, at
+
+
+@pytest.mark.parametrize("R,C", [(128, 128), (300, 256), (1, 16), (129, 144), (257, 400)])
+def test_mx_quant_T_matches_oracle_of_transpose(R, C):
+    """The transposed MXFP8 cast equals the oracle's 1x32 cast of the
+    zero-padded transpose: codes (padding tokens 0x00), exponent bytes, and
+    127 in the atoms' padding rows."""
+    x = _special_inputs(R, C, seed=R * 7 + C)
+    qT, at = mx_quant_T(x)
+    xt = _pad_rows(x).t().contiguous()                      # [C x Mpad]
+    Mp = xt.shape[1]
+    oq, oe = oracle.mx_quant_1x32(u16(xt))
+    assert np.array_equal(np_(qT), oq)
+    assert np.array_equal(atoms_to_rows(np_(at), C, Mp), oe)
+    pad = atoms_to_rows(np_(at), (C + 127) // 128 * 128, Mp)[C:]
+    assert np.all(pad == 127)
+
+
+def test_mx_quant_T_backward_dy_full():
+    dy = wl.backward()["dY"]                                # 4096 x 2048
+    qT, at = mx_quant_T(dy)
+    oq, oe = oracle.mx_quant_1x32(u16(dy.t().contiguous()))
+    assert np.array_equal(np_(qT), oq)
+    assert np.array_equal(atoms_to_rows(np_(at), dy.shape[1], dy.shape[0]), oe)
+
+
+def _mx_ref(a_q, a_e, b_q, b_e, ii=None, jj=None):
+    ref = oracle.mx_gemm(a_q, a_e, b_q, b_e, ii, jj)
+    da, db = np.abs(_dequant(a_q, a_e)), np.abs(_dequant(b_q, b_e))
+    absprod = da @ db.T if ii is None else np.einsum("ek,ek->e", da[ii], db[jj])
+    return ref, absprod
+
+
+@pytest.mark.parametrize("T,N,K", [(128, 128, 256), (300, 256, 512), (1, 128, 256)])
+def test_mx_wgrad_f32(T, N, K):
+    """MXFP8 Wgrad dW [N x K] = dY^T X in FP32, both operands from the
+    transposed cast (32-token blocks), against the oracle's MX GEMM of the
+    oracle's casts of the padded transposes."""
+    dy = wl.normal((T, N), std=wl.DY_STD, seed=T + N)
+    x = wl.with_outliers((T, K), fraction=0.01, seed=T + K)
+    qa, aa = mx_quant_T(dy)
+    qb, ab = mx_quant_T(x)
+    out = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    fp8bs.fp8_mx_gemm_f32(qa, aa, qb, ab, out)
+    torch.cuda.synchronize()
+    oqa, oea = oracle.mx_quant_1x32(u16(_pad_rows(dy).t().contiguous()))
+    oqb, oeb = oracle.mx_quant_1x32(u16(_pad_rows(x).t().contiguous()))
+    assert np.array_equal(np_(qa), oqa) and np.array_equal(np_(qb), oqb)
+    ref, absprod = _mx_ref(oqa, oea, oqb, oeb)
+    assert_gemm_close(np_(out), ref, absprod, False, f"mx wgrad {T}x{N}x{K}")
+
+
+def test_mx_dgrad_small():
+    """MXFP8 Dgrad dX [M x K] = dY W: A = the 1x32 cast of dY along N, B =
+    the 1x32 cast of W [K x N] along N."""
+    M, N, K = 300, 256, 512
+    dy = wl.normal((M, N), std=wl.DY_STD, seed=11)
+    w = wl.normal((K, N), std=wl.W_STD, seed=12)
+    qa, aa = mx_quant(dy)
+    qb, ab = mx_quant(w)
+    out = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    fp8bs.fp8_mx_gemm(qa, aa, qb, ab, out)
+    torch.cuda.synchronize()
+    oqa, oea = oracle.mx_quant_1x32(u16(dy))
+    oqb, oeb = oracle.mx_quant_1x32(u16(w))
+    ref, absprod = _mx_ref(oqa, oea, oqb, oeb)
+    assert_gemm_close(bf16_values(out), ref, absprod, True, "mx dgrad")
+
+
+def test_mx_fprop_with_transposed_weight_cast():
+    """MXFP8 Fprop Y = X W with B = the transposed cast of W [K x N] (no BF16
+    transpose of W needed)."""
+    M, K, N = 257, 512, 256
+    x = wl.with_outliers((M, K), fraction=0.01, seed=21)
+    w = wl.normal((K, N), std=wl.W_STD, seed=22)
+    qa, aa = mx_quant(x)
+    qb, ab = mx_quant_T(w)                                  # [N x K]
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    fp8bs.fp8_mx_gemm(qa, aa, qb, ab, out)
+    torch.cuda.synchronize()
+    oqa, oea = oracle.mx_quant_1x32(u16(x))
+    oqb, oeb = oracle.mx_quant_1x32(u16(w.t().contiguous()))
+    assert np.array_equal(np_(qb), oqb)
+    ref, absprod = _mx_ref(oqa, oea, oqb, oeb)
+    assert_gemm_close(bf16_values(out), ref, absprod, True, "mx fprop, transposed W cast")
+
+
+def test_mx_wgrad_dense_sampled():
+    """The dense layer's Wgrad in MXFP8 (T = 4096, dW 2048 x 7168), sampled."""
+    d = wl.backward()
+    dy, x = d["dY"], d["X"]
+    qa, aa = mx_quant_T(dy)
+    qb, ab = mx_quant_T(x)
+    out = torch.empty((2048, 7168), dtype=torch.float32, device="cuda")
+    fp8bs.fp8_mx_gemm_f32(qa, aa, qb, ab, out)
+    torch.cuda.synchronize()
+    oqa, oea = oracle.mx_quant_1x32(u16(dy.t().contiguous()))
+    oqb, oeb = oracle.mx_quant_1x32(u16(x.t().contiguous()))
+    ii, jj = sample_indices(2048, 7168, 4096, seed=5, tiles=((0, 0), (-1, -1)))
+    ref, absprod = _mx_ref(oqa, oea, oqb, oeb, ii, jj)
+    assert_gemm_close(np_(out)[ii, jj], ref, absprod, False, "mx dense wgrad")
