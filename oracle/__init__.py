@@ -107,6 +107,8 @@ def _load():
         lib.oracle_e4m3_encode_sr.argtypes = [ctypes.c_float, U32]
         lib.oracle_e4m3_encode_sr.restype = ctypes.c_uint8
         lib.oracle_quant_1x128_sr.argtypes = [P, I64, I64, I64, P, I64, P, I64, I64, U64, U32]
+        lib.oracle_requant_128x1_T_sr.argtypes = [I, P, I64, P, I64, I64, I64, I64,
+                                                  P, I, P, I64, P, I64, U64, U32]
         lib.oracle_quant_128x128_sr.argtypes = [P, I64, I64, I64, P, I64, P, I64, U64, U32, I64]
         lib.oracle_mx_quant_1x32.argtypes = [P, I64, I64, P, P]
         lib.oracle_mx_gemm.argtypes = [P, P, P, P, I64, I64, I64, P, P, P, I64]
@@ -307,7 +309,7 @@ def padded_tokens(rows: int, offsets=None) -> int:
     return int(_load().oracle_padded_tokens(_p(off), off.size - 1, rows))
 
 
-def requant_128x1_T(src: np.ndarray, src_scales: np.ndarray | None = None, offsets=None):
+def requant_128x1_T(src: np.ndarray, src_scales: np.ndarray | None = None, offsets=None, sr=None):
     """128x1 (token-axis) tiles of src [M x C], transposed output.
 
     src is bf16 bits (uint16, mode B) or E4M3 codes (uint8, mode Q, with its
@@ -334,9 +336,20 @@ def requant_128x1_T(src: np.ndarray, src_scales: np.ndarray | None = None, offse
     mp = padded_tokens(M, off)
     qT = np.zeros((C, mp), np.uint8)
     scT = np.zeros((mp // 128, C), np.float32)
-    _load().oracle_requant_128x1_T(mode, _p(src), C, _p(ssc), rs, ts, M, C,
-                                   _p(off), G, _p(qT), mp, _p(scT), C)
+    if sr is None:
+        _load().oracle_requant_128x1_T(mode, _p(src), C, _p(ssc), rs, ts, M, C,
+                                       _p(off), G, _p(qT), mp, _p(scT), C)
+    else:
+        _load().oracle_requant_128x1_T_sr(mode, _p(src), C, _p(ssc), rs, ts, M, C,
+                                          _p(off), G, _p(qT), mp, _p(scT), C, int(sr[0]), int(sr[1]))
     return qT, scT
+
+
+def requant_128x1_T_sr(src: np.ndarray, src_scales: np.ndarray | None = None, offsets=None, *,
+                       seed: int, salt: int = 0):
+    """requant_128x1_T with stochastic rounding: source element (r, c) takes
+    the random word of index r * C + c under (seed, salt)."""
+    return requant_128x1_T(src, src_scales, offsets, sr=(seed, salt))
 
 
 # ---------------------------------------------------------------------------

@@ -500,10 +500,13 @@ i64 oracle_padded_tokens(const int32_t* offsets, int groups, i64 rows)
  * output starts at a multiple of 128 (padded token index).
  * qT: E4M3 [cols x Mpad], row stride ldqT; padding bytes are 0x00.
  * scT: fp32 [Mpad/128 x cols], row stride ldscT. */
-void oracle_requant_128x1_T(int mode, const void* src, i64 ld_src,
-                            const float* src_sc, i64 src_rs, i64 src_ts,
-                            i64 rows, i64 cols, const int32_t* offsets, int groups,
-                            uint8_t* qT, i64 ldqT, float* scT, i64 ldscT)
+/* S3 body: with sr != 0 the codes are stochastically rounded, the element
+ * (row r, column c) of the source taking the word of index r * cols + c. */
+static void requant_impl(int mode, const void* src, i64 ld_src,
+                         const float* src_sc, i64 src_rs, i64 src_ts,
+                         i64 rows, i64 cols, const int32_t* offsets, int groups,
+                         uint8_t* qT, i64 ldqT, float* scT, i64 ldscT,
+                         int sr, uint64_t seed, uint32_t salt)
 {
     build_table();
     int ng = (offsets && groups > 0) ? groups : 1;
@@ -532,12 +535,35 @@ void oracle_requant_128x1_T(int mode, const void* src, i64 ld_src,
                 float s = tile_scale(v, len);
                 scT[(pstart / 128 + t) * ldscT + c] = s;
                 uint8_t* dst = qT + c * ldqT + pstart + t * 128;
-                tile_encode(v, len, s, dst, 1);
+                if (sr)
+                    tile_encode_sr(v, len, s, dst, 1, seed, salt, r0 * cols + c, cols);
+                else
+                    tile_encode(v, len, s, dst, 1);
                 for (int i = len; i < 128; ++i) dst[i] = 0x00;
             }
         }
         pstart += ntiles * 128;
     }
+}
+
+void oracle_requant_128x1_T(int mode, const void* src, i64 ld_src,
+                            const float* src_sc, i64 src_rs, i64 src_ts,
+                            i64 rows, i64 cols, const int32_t* offsets, int groups,
+                            uint8_t* qT, i64 ldqT, float* scT, i64 ldscT)
+{
+    requant_impl(mode, src, ld_src, src_sc, src_rs, src_ts, rows, cols, offsets, groups, qT, ldqT, scT, ldscT,
+                 0, 0, 0);
+}
+
+/* S3 with stochastic rounding (element index r * cols + c of the source). */
+void oracle_requant_128x1_T_sr(int mode, const void* src, i64 ld_src,
+                               const float* src_sc, i64 src_rs, i64 src_ts,
+                               i64 rows, i64 cols, const int32_t* offsets, int groups,
+                               uint8_t* qT, i64 ldqT, float* scT, i64 ldscT,
+                               uint64_t seed, uint32_t salt)
+{
+    requant_impl(mode, src, ld_src, src_sc, src_rs, src_ts, rows, cols, offsets, groups, qT, ldqT, scT, ldscT,
+                 1, seed, salt);
 }
 
 /* ------------------------------------------------------------------------- */

@@ -379,6 +379,76 @@ def test_sr_is_unbiased():
         assert abs(mean[j] - xv) <= 5 * se + (hi - lo) * 2.0 ** -20 + 1e-12, (j, xv, mean[j])
 
 
+def _requant_sr_input(R=200, C=64, seed=8):
+    """Columns whose token tiles all contain 448 (scale exactly 1) and
+    values off the E4M3 grid."""
+    rng = np.random.default_rng(seed)
+    x = (rng.standard_normal((R, C)) * 20.0).astype(np.float32)
+    x[::128, :] = 448.0
+    return oracle.f32_to_bf16(x)
+
+
+def test_requant_sr_brackets_and_scales():
+    """The stochastically rounded transposed cast keeps the round-to-nearest
+    scales, and every code is one of the two E4M3 neighbours of v / s (the
+    same sign), the nearest-rounded code being one of them."""
+    xb = _requant_sr_input()
+    q0, s0 = oracle.requant_128x1_T(xb)
+    q1, s1 = oracle.requant_128x1_T_sr(xb, seed=99, salt=3)
+    assert np.array_equal(s0, s1) and np.all(s0 == 1.0)
+    t = oracle.e4m3_table().astype(np.float64)
+    v = oracle.bf16_to_f32(xb).astype(np.float64).T          # [C x R], scale 1
+    R = v.shape[1]
+    a = np.abs(v)
+    pos = t[:0x7F]
+    lo = np.array([[pos[pos <= e].max() for e in row] for row in a])
+    hi = np.array([[pos[pos >= e].min() if e <= 448 else 448.0 for e in row] for row in a])
+    got = np.abs(t[q1[:, :R]])
+    assert np.all((got == lo) | (got == hi))
+    assert np.all(np.signbit(t[q1[:, :R]]) == np.signbit(v))
+    near = np.abs(t[q0[:, :R]])
+    assert np.all((near == lo) | (near == hi))
+    assert np.all(q1[:, R:] == 0)                            # padding tokens
+
+
+def test_requant_sr_word_per_source_element():
+    """Element (r, c) of the source takes the random word of index r * C + c:
+    with scale 1 the transposed SR codes equal the pinned SR encoder applied
+    with those words, and a shifted index mapping disagrees."""
+    xb = _requant_sr_input(R=130, C=32, seed=9)
+    q, _ = oracle.requant_128x1_T_sr(xb, seed=5, salt=11)
+    v = oracle.bf16_to_f32(xb)
+    R, C = v.shape
+    want = np.array([[oracle.e4m3_encode_sr(float(v[r, c]), oracle.sr_word(5, 11, r * C + c))
+                      for r in range(R)] for c in range(C)], np.uint8)
+    assert np.array_equal(q[:, :R], want)
+    shifted = np.array([[oracle.e4m3_encode_sr(float(v[r, c]), oracle.sr_word(5, 11, c * R + r))
+                         for r in range(R)] for c in range(C)], np.uint8)
+    assert not np.array_equal(q[:, :R], shifted)
+
+
+def test_requant_sr_is_unbiased():
+    """Identical columns (independent counters) average to v / s within five
+    standard errors."""
+    C = 4096
+    vals = np.array([1.0625, 1.03, 0.3, -5.7, 100.2, 0.004, -0.0011, 447.0], np.float32)
+    x = np.zeros((128, C), np.float32)
+    x[:vals.size, :] = vals[:, None]
+    x[127, :] = 448.0
+    xb = oracle.f32_to_bf16(x)
+    v = oracle.bf16_to_f32(xb)[:vals.size, 0].astype(np.float64)
+    q, s = oracle.requant_128x1_T_sr(xb, seed=2024, salt=1)
+    assert np.all(s == 1.0)
+    t = oracle.e4m3_table().astype(np.float64)
+    mean = t[q[:, :vals.size]].mean(0)
+    for j, xv in enumerate(v):
+        lo = t[:0x7F][t[:0x7F] <= abs(xv)].max()
+        hi = t[:0x7F][t[:0x7F] > abs(xv)].min() if abs(xv) < 448 else lo
+        f = (abs(xv) - lo) / (hi - lo) if hi > lo else 0.0
+        se = np.sqrt(f * (1 - f) / C) * (hi - lo)
+        assert abs(abs(mean[j]) - abs(xv)) <= 5 * se + (hi - lo) * 2.0 ** -20 + 1e-12, (j, xv, mean[j])
+
+
 def test_mx_quant_scales_and_codes():
     """MXFP8 (OCP MX v1.0 blocks of 32 with 8-bit exponent scales): each
     scale 2^(E-127) is the smallest power of two that keeps the block's
