@@ -34,7 +34,8 @@ __all__ = [
     "SRC_BF16", "SRC_E4M3", "OP_FPROP", "OP_DGRAD", "OP_WGRAD", "MAX_GROUPS",
     "SCALE_FP32", "SCALE_UE8M0", "ScaleOpts", "fp8_quant_1x128_opts", "fp8_quant_128x128_opts",
     "fp8_requant_128x1_T_opts", "fp8_quant_dual_opts", "fp8_quant_1x128_sr", "fp8_quant_128x128_sr",
-    "fp8_quant_dual_stash", "fp8_quant_dual_stash_opts",
+    "fp8_quant_dual_stash", "fp8_quant_dual_stash_opts", "fp8_requant_128x1_T_sr", "fp8_quant_dual_sr",
+    "fp8_quant_dual_stash_sr",
     "fp8bs_mx_scale_bytes", "fp8_mx_quant_1x32", "fp8_mx_gemm", "empty_mx_quant",
     "fp8_mx_quant_1x32_T", "fp8_mx_gemm_f32", "empty_mx_quant_T",
 ]
@@ -98,6 +99,9 @@ def lib() -> ctypes.CDLL:
         "fp8_quant_dual_stash": ([P, I64, I64, P, I32, P, P, P, P, P], S),
         "fp8_quant_dual_stash_opts": ([P, I64, I64, P, I32, P, P, P, P, P, P], S),
         "fp8_quant_1x128_sr": ([P, I64, I64, I64, P, P, ctypes.c_uint64, ctypes.c_uint32, P, P], S),
+        "fp8_requant_128x1_T_sr": ([I, P, P, I64, I64, P, I32, P, P, ctypes.c_uint64, ctypes.c_uint32, P, P], S),
+        "fp8_quant_dual_sr": ([P, I64, I64, P, I32, P, P, P, P, ctypes.c_uint64, ctypes.c_uint32, P, P], S),
+        "fp8_quant_dual_stash_sr": ([P, I64, I64, P, I32, P, P, P, P, ctypes.c_uint64, ctypes.c_uint32, P, P], S),
         "fp8bs_mx_scale_bytes": ([I64, I64], I64),
         "fp8_mx_quant_1x32": ([P, I64, I64, P, P, P], S),
         "fp8_mx_gemm": ([P, P, P, P, I64, I64, I64, P, P], S),
@@ -258,11 +262,20 @@ def fp8_quant_128x128(w: torch.Tensor, q: torch.Tensor, qT: Optional[torch.Tenso
                                                              _opts(rule, amax_floor, scale_floor), _stream(stream)))
 
 
+def fp8_requant_128x1_T_sr(src: torch.Tensor, src_scales: Optional[torch.Tensor], qT: torch.Tensor,
+                           scalesT: torch.Tensor, seed: int, salt: int = 0, offsets=None, stream=None,
+                           rule: int = SCALE_FP32, amax_floor: float = 0.0, scale_floor: float = 0.0) -> None:
+    """fp8_requant_128x1_T with stochastic rounding under (seed, salt); see fp8bs.h."""
+    fp8_requant_128x1_T(src, src_scales, qT, scalesT, offsets, stream, rule, amax_floor, scale_floor,
+                        sr=(seed, salt))
+
+
 def fp8_requant_128x1_T(src: torch.Tensor, src_scales: Optional[torch.Tensor], qT: torch.Tensor,
                         scalesT: torch.Tensor, offsets=None, stream=None, rule: int = SCALE_FP32,
-                        amax_floor: float = 0.0, scale_floor: float = 0.0) -> None:
+                        amax_floor: float = 0.0, scale_floor: float = 0.0, sr=None) -> None:
     """128x1 transposed requantization. src BF16 (mode B) or uint8 E4M3 with
-    its 1x128 scales (mode Q); optional host group offsets."""
+    its 1x128 scales (mode Q); optional host group offsets; sr = (seed, salt)
+    selects stochastic rounding."""
     if src.dtype == torch.bfloat16:
         mode = SRC_BF16
         _need(src, torch.bfloat16, "src")
@@ -279,9 +292,15 @@ def fp8_requant_128x1_T(src: torch.Tensor, src_scales: Optional[torch.Tensor], q
     mp = fp8bs_padded_tokens(rows, offsets)
     if qT.shape != (cols, mp) or scalesT.shape != (mp // 128, cols):
         raise ValueError("output shapes do not match empty_requant_128x1_T")
-    _check("fp8_requant_128x1_T", lib().fp8_requant_128x1_T_opts(
-        mode, _ptr(src), _ptr(src_scales if mode == SRC_E4M3 else None), rows, cols, optr, groups,
-        _ptr(qT), _ptr(scalesT), _opts(rule, amax_floor, scale_floor), _stream(stream)))
+    if sr is None:
+        _check("fp8_requant_128x1_T", lib().fp8_requant_128x1_T_opts(
+            mode, _ptr(src), _ptr(src_scales if mode == SRC_E4M3 else None), rows, cols, optr, groups,
+            _ptr(qT), _ptr(scalesT), _opts(rule, amax_floor, scale_floor), _stream(stream)))
+    else:
+        _check("fp8_requant_128x1_T_sr", lib().fp8_requant_128x1_T_sr(
+            mode, _ptr(src), _ptr(src_scales if mode == SRC_E4M3 else None), rows, cols, optr, groups,
+            _ptr(qT), _ptr(scalesT), int(sr[0]) & (2 ** 64 - 1), int(sr[1]) & 0xFFFFFFFF,
+            _opts(rule, amax_floor, scale_floor), _stream(stream)))
 
 
 def fp8_quant_dual(x: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, qT: torch.Tensor,
@@ -311,7 +330,23 @@ def fp8_quant_dual_stash_opts(x, q, scales, qT, scalesT, opts: Optional["ScaleOp
     fp8_quant_dual_stash(x, q, scales, qT, scalesT, offsets=offsets, stream=stream, **_rule_kwargs(opts))
 
 
-def _dual_common(fn, x, q, scales, qT, scalesT, offsets, stream, rule, amax_floor, scale_floor) -> None:
+def fp8_quant_dual_sr(x, q, scales, qT, scalesT, seed: int, salt: int = 0, offsets=None, stream=None,
+                      rule: int = SCALE_FP32, amax_floor: float = 0.0, scale_floor: float = 0.0) -> None:
+    """fp8_quant_dual with stochastic rounding: the 1x128 part under (seed,
+    salt), the transposed part under (seed, salt + 1); see fp8bs.h."""
+    _dual_common("fp8_quant_dual_sr", x, q, scales, qT, scalesT, offsets, stream, rule, amax_floor, scale_floor,
+                 sr=(seed, salt))
+
+
+def fp8_quant_dual_stash_sr(x, q, scales, qT, scalesT, seed: int, salt: int = 0, offsets=None, stream=None,
+                            rule: int = SCALE_FP32, amax_floor: float = 0.0, scale_floor: float = 0.0) -> None:
+    """fp8_quant_dual_stash with stochastic rounding: the 1x128 part under
+    (seed, salt), the requant of its result under (seed, salt + 1)."""
+    _dual_common("fp8_quant_dual_stash_sr", x, q, scales, qT, scalesT, offsets, stream, rule, amax_floor,
+                 scale_floor, sr=(seed, salt))
+
+
+def _dual_common(fn, x, q, scales, qT, scalesT, offsets, stream, rule, amax_floor, scale_floor, sr=None) -> None:
     _need(x, torch.bfloat16, "x")
     for t, n, d in ((q, "q", torch.uint8), (scales, "scales", torch.float32), (qT, "qT", torch.uint8),
                     (scalesT, "scalesT", torch.float32)):
@@ -329,9 +364,15 @@ def _dual_common(fn, x, q, scales, qT, scalesT, offsets, stream, rule, amax_floo
     mp = fp8bs_padded_tokens(rows, offsets)
     if qT.shape != (cols, mp) or scalesT.shape != (mp // 128, cols):
         raise ValueError("qT / scalesT shapes do not match empty_requant_128x1_T")
-    _check(fn[:-len("_opts")], getattr(lib(), fn)(
-        _ptr(x), rows, cols, optr, groups, _ptr(q), _ptr(scales), _ptr(qT), _ptr(scalesT),
-        _opts(rule, amax_floor, scale_floor), _stream(stream)))
+    if sr is None:
+        _check(fn[:-len("_opts")], getattr(lib(), fn)(
+            _ptr(x), rows, cols, optr, groups, _ptr(q), _ptr(scales), _ptr(qT), _ptr(scalesT),
+            _opts(rule, amax_floor, scale_floor), _stream(stream)))
+    else:
+        _check(fn, getattr(lib(), fn)(
+            _ptr(x), rows, cols, optr, groups, _ptr(q), _ptr(scales), _ptr(qT), _ptr(scalesT),
+            int(sr[0]) & (2 ** 64 - 1), int(sr[1]) & 0xFFFFFFFF, _opts(rule, amax_floor, scale_floor),
+            _stream(stream)))
 
 
 def fp8_quant_1x128_sr(x, q, scales, seed: int, salt: int = 0, stream=None, rule: int = SCALE_FP32,

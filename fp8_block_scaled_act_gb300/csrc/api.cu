@@ -419,7 +419,7 @@ namespace {
 fp8bs_status requant_common(int src_mode, const void* src, const float* src_scales, int64_t rows, int64_t cols,
                             const int32_t* group_offsets_host, int32_t groups, uint8_t* qT, float* scalesT,
                             uint8_t* q, float* q_scales, const fp8bs_scale_opts* opts, void* stream,
-                            bool stash = false)
+                            bool stash = false, const SrParams* sr = nullptr)
 {
     ScaleRule rule;
     if (!to_rule(opts, &rule)) return FP8BS_ERR_ARG;
@@ -456,6 +456,14 @@ fp8bs_status requant_common(int src_mode, const void* src, const float* src_scal
     p.q_scale_ld = fp8bs_scale_ld(rows);
     p.stash = stash ? 1 : 0;
     p.rule = rule;
+    if (sr) {
+        // the 1x128 part of a dual cast takes (seed, salt), the transposed
+        // part (seed, salt + 1); a plain requant's transposed cast (seed, salt)
+        p.sr = 1;
+        p.sr_seed = sr->seed;
+        p.sr_salt_rows = sr->salt;
+        p.sr_salt_cols = q ? sr->salt + 1u : sr->salt;
+    }
     if (grouped) {
         p.num_groups = groups;
         int tiles = 0;
@@ -527,6 +535,36 @@ fp8bs_status fp8_quant_dual_stash_opts(const void* x, int64_t rows, int64_t cols
     if (rows > 0 && (!q || !scales)) return FP8BS_ERR_ARG;
     return requant_common(FP8BS_SRC_BF16, x, nullptr, rows, cols, group_offsets_host, groups, qT, scalesT, q,
                           scales, opts, stream, true);
+}
+
+fp8bs_status fp8_requant_128x1_T_sr(int src_mode, const void* src, const float* src_scales, int64_t rows,
+                                    int64_t cols, const int32_t* group_offsets_host, int32_t groups, uint8_t* qT,
+                                    float* scalesT, uint64_t seed, uint32_t salt, const fp8bs_scale_opts* opts,
+                                    void* stream)
+{
+    const SrParams sr{seed, salt};
+    return requant_common(src_mode, src, src_scales, rows, cols, group_offsets_host, groups, qT, scalesT, nullptr,
+                          nullptr, opts, stream, false, &sr);
+}
+
+fp8bs_status fp8_quant_dual_sr(const void* x, int64_t rows, int64_t cols, const int32_t* group_offsets_host,
+                               int32_t groups, uint8_t* q, float* scales, uint8_t* qT, float* scalesT, uint64_t seed,
+                               uint32_t salt, const fp8bs_scale_opts* opts, void* stream)
+{
+    if (rows > 0 && (!q || !scales)) return FP8BS_ERR_ARG;
+    const SrParams sr{seed, salt};
+    return requant_common(FP8BS_SRC_BF16, x, nullptr, rows, cols, group_offsets_host, groups, qT, scalesT, q,
+                          scales, opts, stream, false, &sr);
+}
+
+fp8bs_status fp8_quant_dual_stash_sr(const void* x, int64_t rows, int64_t cols, const int32_t* group_offsets_host,
+                                     int32_t groups, uint8_t* q, float* scales, uint8_t* qT, float* scalesT,
+                                     uint64_t seed, uint32_t salt, const fp8bs_scale_opts* opts, void* stream)
+{
+    if (rows > 0 && (!q || !scales)) return FP8BS_ERR_ARG;
+    const SrParams sr{seed, salt};
+    return requant_common(FP8BS_SRC_BF16, x, nullptr, rows, cols, group_offsets_host, groups, qT, scalesT, q,
+                          scales, opts, stream, true, &sr);
 }
 
 fp8bs_status fp8_block_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wqT,

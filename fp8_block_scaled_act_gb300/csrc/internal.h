@@ -59,6 +59,12 @@ struct RequantParams {
     // from the BF16 source (the E4M3 source mode applied to q, q_scales).
     int stash;
     ScaleRule rule;
+    // Stochastic rounding (sr != 0): the 1x128 part takes (seed, salt_rows),
+    // the transposed part (seed, salt_cols); source element (r, c) uses the
+    // word of index r * cols + c.
+    int sr;
+    uint64_t sr_seed;
+    uint32_t sr_salt_rows, sr_salt_cols;
 };
 
 cudaError_t launch_requant_128x1_T(const RequantParams& p, cudaStream_t stream);

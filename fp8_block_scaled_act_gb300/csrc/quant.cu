@@ -561,6 +561,87 @@ __device__ __noinline__ void requant_quad_e4m3_exact(const uint8_t* stage, const
     }
 }
 
+// Stochastic-rounding versions of the two transposed passes above. Source
+// element (token r, channel c) takes word (r * cols + c) % 4 of
+// sr_words(key, (r * cols + c) / 4); tok0 is the source row of the part's
+// first token, cg the source column of channel j. The quotient is the same
+// correctly rounded fp32 v / s as in the nearest-rounding path (or an IEEE
+// division for scales outside its range), then rounded by sr_code.
+__device__ __forceinline__ uint32_t word_of(const uint4& r, uint32_t i)
+{
+    return i == 0 ? r.x : (i == 1 ? r.y : (i == 2 ? r.z : r.w));
+}
+
+__device__ __forceinline__ void requant_pair_bf16_sr(const uint8_t* stage, int part, int j, const TileScale& t0,
+                                                     const TileScale& t1, const SrKey& key, int64_t tok0,
+                                                     int64_t cols, int64_t cg, uint32_t (&w0)[8], uint32_t (&w1)[8])
+{
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        uint32_t x[4];
+        uint32_t r0[4], r1[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            x[e] = *reinterpret_cast<const uint32_t*>(stage + ((part * 32 + 4 * k + e) * 128 + j) * 2);
+            const uint64_t idx = static_cast<uint64_t>((tok0 + 4 * k + e) * cols + cg);   // even
+            const uint4 r = sr_words(key, idx >> 2);
+            r0[e] = word_of(r, static_cast<uint32_t>(idx & 3u));
+            r1[e] = word_of(r, static_cast<uint32_t>(idx & 3u) + 1u);
+        }
+        float q0[4], q1[4];
+        if (t0.nr != 0.0f && t1.nr != 0.0f) {
+            const float2 a01 = quotient2(make_float2(neg_bf16_lo(x[0]), neg_bf16_lo(x[1])), t0.s, t0.nr);
+            const float2 a23 = quotient2(make_float2(neg_bf16_lo(x[2]), neg_bf16_lo(x[3])), t0.s, t0.nr);
+            const float2 b01 = quotient2(make_float2(neg_bf16_hi(x[0]), neg_bf16_hi(x[1])), t1.s, t1.nr);
+            const float2 b23 = quotient2(make_float2(neg_bf16_hi(x[2]), neg_bf16_hi(x[3])), t1.s, t1.nr);
+            q0[0] = a01.x; q0[1] = a01.y; q0[2] = a23.x; q0[3] = a23.y;
+            q1[0] = b01.x; q1[1] = b01.y; q1[2] = b23.x; q1[3] = b23.y;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                q0[e] = __fdiv_rn(bf16_lo(x[e]), t0.s);
+                q1[e] = __fdiv_rn(bf16_hi(x[e]), t1.s);
+            }
+        }
+        w0[k] = sr_code(q0[0], r0[0]) | (sr_code(q0[1], r0[1]) << 8) | (sr_code(q0[2], r0[2]) << 16) |
+                (sr_code(q0[3], r0[3]) << 24);
+        w1[k] = sr_code(q1[0], r1[0]) | (sr_code(q1[1], r1[1]) << 8) | (sr_code(q1[2], r1[2]) << 16) |
+                (sr_code(q1[3], r1[3]) << 24);
+    }
+}
+
+__device__ __forceinline__ void requant_quad_e4m3_sr(const uint8_t* stage, const float* row_scale, int part,
+                                                     int j, const TileScale (&ts)[4], const SrKey& key,
+                                                     int64_t tok0, int64_t cols, int64_t cg, uint32_t (&w)[4][4])
+{
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float nv[4][4];   // [token][channel], negated
+        uint4 r[4];       // words of the token's four channels (cg % 4 == 0)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int rl = part * 16 + 4 * k + e;
+            const uint32_t x = *reinterpret_cast<const uint32_t*>(stage + rl * 128 + j);
+            decode4_scaled(x, -row_scale[rl], nv[e]);
+            r[e] = sr_words(key, static_cast<uint64_t>((tok0 + 4 * k + e) * cols + cg) >> 2);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float q[4];
+            if (ts[c].nr != 0.0f) {
+                const float2 a = quotient2(make_float2(nv[0][c], nv[1][c]), ts[c].s, ts[c].nr);
+                const float2 b = quotient2(make_float2(nv[2][c], nv[3][c]), ts[c].s, ts[c].nr);
+                q[0] = a.x; q[1] = a.y; q[2] = b.x; q[3] = b.y;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) q[e] = __fdiv_rn(-nv[e][c], ts[c].s);
+            }
+            w[c][k] = sr_code(q[0], word_of(r[0], c)) | (sr_code(q[1], word_of(r[1], c)) << 8) |
+                      (sr_code(q[2], word_of(r[2], c)) << 16) | (sr_code(q[3], word_of(r[3], c)) << 24);
+        }
+    }
+}
+
 __device__ __forceinline__ int find_group(const int32_t* tile_start, int ng, int tile)
 {
     int lo = 0, hi = ng - 1;  // last g with tile_start[g] <= tile
@@ -575,8 +656,9 @@ __device__ __forceinline__ int find_group(const int32_t* tile_start, int ng, int
 // kStash (with kDual): the transposed cast is taken from that E4M3 result
 // (decoded with its row scale, as the E4M3 source mode does) instead of
 // from the BF16 values; the 1x128 codes are staged in place of the source.
-template <bool kDual, bool kStash>
-__global__ void __launch_bounds__(kQ3Threads, kDual ? 3 : 4) requant_128x1_T_kernel(const __grid_constant__ RequantParams p)
+// kSR: stochastic rounding of both passes (keys in p).
+template <bool kDual, bool kStash, bool kSR>
+__global__ void __launch_bounds__(kQ3Threads, kSR ? 2 : (kDual ? 3 : 4)) requant_128x1_T_kernel(const __grid_constant__ RequantParams p)
 {
     static_assert(kDual || !kStash, "the stash mode is a dual cast");
     // staging: BF16 source 128 x 128 x 2 bytes, or E4M3 128 x 128 bytes + row scales
@@ -659,7 +741,15 @@ __global__ void __launch_bounds__(kQ3Threads, kDual ? 3 : 4) requant_128x1_T_ker
                     continue;
                 }
                 if (chunk == 0) p.q_scales[(c0 / 128) * p.q_scale_ld + r0 + rl] = ts.s;
-                const uint2 codes = quant8(d[i], ts);
+                uint2 codes;
+                if constexpr (kSR) {
+                    uint32_t wr[8];
+                    sr_words8(SrKey{p.sr_seed, p.sr_salt_rows},
+                              static_cast<uint64_t>((r0 + rl) * p.cols + c0 + chunk * 8), wr);
+                    codes = quant8_sr(d[i], ts, wr);
+                } else {
+                    codes = quant8(d[i], ts);
+                }
                 if (ch_ok) *reinterpret_cast<uint2*>(p.q + (r0 + rl) * p.cols + c0 + chunk * 8) = codes;
                 if constexpr (kStash) {
                     *reinterpret_cast<uint2*>(stage + rl * 128 + chunk * 8) = codes;
@@ -760,7 +850,14 @@ __global__ void __launch_bounds__(kQ3Threads, kDual ? 3 : 4) requant_128x1_T_ker
             uint8_t* dst0 = p.qT + (c0 + j) * p.mpad + (int64_t)tile * 128 + part * 32;
             uint8_t* dst1 = dst0 + p.mpad;
             uint32_t w0[8], w1[8];
-            if (requant_pair_bf16(stage, part, j, t0, t1, w0, w1)) {
+            if constexpr (kSR) {
+                requant_pair_bf16_sr(stage, part, j, t0, t1, SrKey{p.sr_seed, p.sr_salt_cols},
+                                     r0 + part * 32, p.cols, c0 + j, w0, w1);
+                reinterpret_cast<uint4*>(dst0)[0] = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+                reinterpret_cast<uint4*>(dst0)[1] = make_uint4(w0[4], w0[5], w0[6], w0[7]);
+                reinterpret_cast<uint4*>(dst1)[0] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+                reinterpret_cast<uint4*>(dst1)[1] = make_uint4(w1[4], w1[5], w1[6], w1[7]);
+            } else if (requant_pair_bf16(stage, part, j, t0, t1, w0, w1)) {
                 reinterpret_cast<uint4*>(dst0)[0] = make_uint4(w0[0], w0[1], w0[2], w0[3]);
                 reinterpret_cast<uint4*>(dst0)[1] = make_uint4(w0[4], w0[5], w0[6], w0[7]);
                 reinterpret_cast<uint4*>(dst1)[0] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
@@ -779,7 +876,13 @@ __global__ void __launch_bounds__(kQ3Threads, kDual ? 3 : 4) requant_128x1_T_ker
             for (int c = 0; c < 4; ++c) ts[c] = col_scale[j + c];
             uint8_t* dst = p.qT + (c0 + j) * p.mpad + (int64_t)tile * 128 + part * 16;
             uint32_t w[4][4];
-            if (requant_quad_e4m3(stage, row_scale, part, j, ts, w)) {
+            if constexpr (kSR) {
+                requant_quad_e4m3_sr(stage, row_scale, part, j, ts, SrKey{p.sr_seed, p.sr_salt_cols},
+                                     r0 + part * 16, p.cols, c0 + j, w);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4*>(dst + c * p.mpad) = make_uint4(w[c][0], w[c][1], w[c][2], w[c][3]);
+            } else if (requant_quad_e4m3(stage, row_scale, part, j, ts, w)) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
                     *reinterpret_cast<uint4*>(dst + c * p.mpad) = make_uint4(w[c][0], w[c][1], w[c][2], w[c][3]);
@@ -842,12 +945,22 @@ cudaError_t launch_requant_128x1_T(const RequantParams& p, cudaStream_t stream)
     if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
     const dim3 grid((unsigned)tiles, (unsigned)((p.cols + 127) / 128));
     if (grid.y > 65535) return cudaErrorInvalidValue;
-    if (p.q != nullptr && p.stash)
-        requant_128x1_T_kernel<true, true><<<grid, kQ3Threads, 0, stream>>>(p);
-    else if (p.q != nullptr)
-        requant_128x1_T_kernel<true, false><<<grid, kQ3Threads, 0, stream>>>(p);
-    else
-        requant_128x1_T_kernel<false, false><<<grid, kQ3Threads, 0, stream>>>(p);
+    const bool dual = p.q != nullptr, stash = dual && p.stash;
+    if (p.sr) {
+        if (stash)
+            requant_128x1_T_kernel<true, true, true><<<grid, kQ3Threads, 0, stream>>>(p);
+        else if (dual)
+            requant_128x1_T_kernel<true, false, true><<<grid, kQ3Threads, 0, stream>>>(p);
+        else
+            requant_128x1_T_kernel<false, false, true><<<grid, kQ3Threads, 0, stream>>>(p);
+    } else {
+        if (stash)
+            requant_128x1_T_kernel<true, true, false><<<grid, kQ3Threads, 0, stream>>>(p);
+        else if (dual)
+            requant_128x1_T_kernel<true, false, false><<<grid, kQ3Threads, 0, stream>>>(p);
+        else
+            requant_128x1_T_kernel<false, false, false><<<grid, kQ3Threads, 0, stream>>>(p);
+    }
     return cudaGetLastError();
 }
 

@@ -269,6 +269,32 @@ FP8BS_API fp8bs_status fp8_quant_128x128_sr(const void* w, int64_t batch, int64_
                                             uint64_t seed, uint32_t salt,
                                             const fp8bs_scale_opts* opts, void* stream);
 
+/* The transposed casts with stochastic rounding, under the same contract:  */
+/* element (r, c) of the source tensor [rows x cols] takes word(r * cols + c)*/
+/* (the padding tokens of qT stay 0x00).                                     */
+/* fp8_requant_128x1_T_sr: fp8_requant_128x1_T with (seed, salt).            */
+/* fp8_quant_dual_sr / fp8_quant_dual_stash_sr: the 1x128 part is            */
+/* fp8_quant_1x128_sr with (seed, salt); the transposed part uses            */
+/* (seed, salt + 1), from the BF16 values (dual) or from the stochastically  */
+/* rounded 1x128 result (stash), so each output is byte-identical to the     */
+/* corresponding separate calls. Arguments otherwise as the calls without    */
+/* _sr (opts: scale rule, NULL = default).                                    */
+FP8BS_API fp8bs_status fp8_requant_128x1_T_sr(int src_mode, const void* src, const float* src_scales,
+                                              int64_t rows, int64_t cols,
+                                              const int32_t* group_offsets_host, int32_t groups,
+                                              uint8_t* qT, float* scalesT, uint64_t seed, uint32_t salt,
+                                              const fp8bs_scale_opts* opts, void* stream);
+FP8BS_API fp8bs_status fp8_quant_dual_sr(const void* x, int64_t rows, int64_t cols,
+                                         const int32_t* group_offsets_host, int32_t groups,
+                                         uint8_t* q, float* scales, uint8_t* qT, float* scalesT,
+                                         uint64_t seed, uint32_t salt, const fp8bs_scale_opts* opts,
+                                         void* stream);
+FP8BS_API fp8bs_status fp8_quant_dual_stash_sr(const void* x, int64_t rows, int64_t cols,
+                                               const int32_t* group_offsets_host, int32_t groups,
+                                               uint8_t* q, float* scales, uint8_t* qT, float* scalesT,
+                                               uint64_t seed, uint32_t salt, const fp8bs_scale_opts* opts,
+                                               void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* S4-S6. Block-scaled E4M3 GEMMs with per-128-K fp32 promotion              */
 /* [P1] bullet 1 (all three GEMMs E4M3; BF16 activations and input grads,     */

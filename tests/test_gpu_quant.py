@@ -403,6 +403,77 @@ def test_sr_quant_128x128_batched_matches_oracle():
         assert np.array_equal(np_(sc)[e].view(np.uint32), osc.view(np.uint32))
 
 
+@pytest.mark.parametrize("M,C,counts,seed,salt", [
+    (128, 128, None, 0, 0), (300, 256, None, 2 ** 40 + 17, 3), (257, 400, None, 7, 0xFFFFFFFF),
+    (400, 128, [0, 129, 1, 0, 270], 11, 5),
+])
+def test_sr_requant_both_sources_match_oracle(M, C, counts, seed, salt):
+    """NEXT-3 on the transposed cast: stochastic rounding from BF16 and from
+    an E4M3 stash, byte- and bit-exact against the oracle (source element
+    (r, c) takes word r * C + c; ragged token tiles and groups included)."""
+    x = _special_inputs(M, C, seed=M + 13 * C)
+    off = None if counts is None else wl.offsets_from_counts(counts)
+    xd = x.cuda()
+    qT, scT = fp8bs.empty_requant_128x1_T(M, C, off)
+    fp8bs.fp8_requant_128x1_T_sr(xd, None, qT, scT, seed=seed, salt=salt, offsets=off)
+    xq, sx = fp8bs.empty_quant_1x128(M, C)
+    fp8bs.fp8_quant_1x128(xd, xq, sx)
+    qTq, scTq = fp8bs.empty_requant_128x1_T(M, C, off)
+    fp8bs.fp8_requant_128x1_T_sr(xq, sx, qTq, scTq, seed=seed, salt=salt, offsets=off)
+    torch.cuda.synchronize()
+    oqT, oscT = oracle.requant_128x1_T_sr(u16(x), offsets=off, seed=seed, salt=salt)
+    assert np.array_equal(np_(qT), oqT)
+    assert np.array_equal(np_(scT).view(np.uint32), oscT.view(np.uint32))
+    oq, osc = oracle.quant_1x128(u16(x))
+    oqTq, oscTq = oracle.requant_128x1_T_sr(oq, osc, offsets=off, seed=seed, salt=salt)
+    assert np.array_equal(np_(qTq), oqTq)
+    assert np.array_equal(np_(scTq).view(np.uint32), oscTq.view(np.uint32))
+
+
+@pytest.mark.parametrize("stash", [False, True])
+@pytest.mark.parametrize("M,C,counts", [(300, 256, None), (400, 128, [0, 129, 1, 0, 270])])
+def test_sr_dual_and_stash_match_oracle(stash, M, C, counts):
+    """The SR dual and stash casts: the 1x128 part is the oracle's SR cast
+    under (seed, salt), the transposed part the oracle's SR requant under
+    (seed, salt + 1) of the BF16 values (dual) or of that SR stash (stash)."""
+    seed, salt = 77, 9
+    x = _special_inputs(M, C, seed=M + 17 * C)
+    off = None if counts is None else wl.offsets_from_counts(counts)
+    q, sc = fp8bs.empty_quant_1x128(M, C)
+    qT, scT = fp8bs.empty_requant_128x1_T(M, C, off)
+    fn = fp8bs.fp8_quant_dual_stash_sr if stash else fp8bs.fp8_quant_dual_sr
+    fn(x.cuda(), q, sc, qT, scT, seed=seed, salt=salt, offsets=off)
+    torch.cuda.synchronize()
+    oq, osc = oracle.quant_1x128_sr(u16(x), seed=seed, salt=salt)
+    assert np.array_equal(np_(q), oq)
+    assert np.array_equal(np_(sc)[:, :M].view(np.uint32), osc[:, :M].view(np.uint32))
+    src = (oq, osc) if stash else (u16(x), None)
+    oqT, oscT = oracle.requant_128x1_T_sr(src[0], src[1], offsets=off, seed=seed, salt=salt + 1)
+    assert np.array_equal(np_(qT), oqT)
+    assert np.array_equal(np_(scT).view(np.uint32), oscT.view(np.uint32))
+
+
+def test_sr_stash_full_dense_x_sampled():
+    """The fused SR cast of the dense X (4096 x 7168) against the two separate
+    SR library calls in full and the oracle on the first two token tiles."""
+    x = wl.backward()["X"]
+    xd = x.cuda()
+    M, C = x.shape
+    q, sc = fp8bs.empty_quant_1x128(M, C)
+    qT, scT = fp8bs.empty_requant_128x1_T(M, C)
+    fp8bs.fp8_quant_dual_stash_sr(xd, q, sc, qT, scT, seed=5, salt=6)
+    q2, sc2 = fp8bs.empty_quant_1x128(M, C)
+    fp8bs.fp8_quant_1x128_sr(xd, q2, sc2, seed=5, salt=6)
+    qT2, scT2 = fp8bs.empty_requant_128x1_T(M, C)
+    fp8bs.fp8_requant_128x1_T_sr(q2, sc2, qT2, scT2, seed=5, salt=7)
+    torch.cuda.synchronize()
+    assert np.array_equal(np_(q), np_(q2)) and np.array_equal(np_(qT), np_(qT2))
+    assert np.array_equal(np_(scT).view(np.uint32), np_(scT2).view(np.uint32))
+    rows = slice(0, 256)                  # the oracle's element indices start at row 0
+    oq, osc = oracle.quant_1x128_sr(u16(x)[rows], seed=5, salt=6)
+    assert np.array_equal(np_(q)[rows], oq)
+
+
 def test_sr_full_size_and_statistics():
     """The dense activation in full under SR equals the oracle, differs from
     round-to-nearest on a sizeable fraction of elements, and another salt
