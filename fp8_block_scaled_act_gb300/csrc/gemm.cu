@@ -13,7 +13,7 @@
 // memory instead, which decouples the two halves of the work:
 //
 //   warp 0      TMA producer: one thread streams 128x128 (A) and 256x128 (B)
-//               E4M3 tiles (K-major, 128-byte swizzle) into a 4-stage
+//               E4M3 tiles (K-major, 128-byte swizzle) into a 4-stage (Wgrad: 3)
 //               shared-memory ring.
 //   warp 1      MMA issuer: one thread issues four tcgen05.mma (K = 32 each)
 //               per K-block into a fresh TMEM accumulator (the first with
@@ -46,7 +46,7 @@
 namespace fp8bs {
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 4;        // operand ring depth (Fprop / Dgrad; see num_stages)
 constexpr int kABytes = kBM * kBK;  // 16 KB
 constexpr int kBBytes = kBN * kBK;  // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
@@ -77,10 +77,18 @@ constexpr int kOutStageWarpBytes = 32 * 64 * 2;
 constexpr int kOutStageBytes = kEpiWarps * kOutStageWarpBytes;
 // Dynamic shared memory: the operand ring, the control block, then the
 // Wgrad scale ring or the Fprop / Dgrad output stage.
+// Operand ring depth per kind: Wgrad, bound by its epilogue, measured
+// faster with three stages than with four (78.5 against 80.5 us on the dense
+// workload).
+template <GemmKind kKind>
+__host__ __device__ constexpr int num_stages()
+{
+    return kKind == GemmKind::kVectorScaleF32 ? 3 : kStages;
+}
 template <GemmKind kKind>
 constexpr int smem_bytes()
 {
-    return kStages * kStageBytes + kCtlBytes +
+    return num_stages<kKind>() * kStageBytes + kCtlBytes +
            (kKind == GemmKind::kVectorScaleF32 ? kScaleBytes : kOutStageBytes) + 1024 /* alignment */;
 }
 
@@ -388,20 +396,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                              const __grid_constant__ CUtensorMap map_b,
                              const __grid_constant__ GemmParams p)
 {
+    constexpr int kS = num_stages<kKind>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;
-    uint8_t* sB = smem + kStages * kABytes;
-    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + kStages * kStageBytes);
-    uint8_t* extra = smem + kStages * kStageBytes + kCtlBytes;   // scale ring or output stage
+    uint8_t* sB = smem + kS * kABytes;
+    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + kS * kStageBytes);
+    uint8_t* extra = smem + kS * kStageBytes + kCtlBytes;   // scale ring or output stage
     float* scale_ring = reinterpret_cast<float*>(extra);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kS; ++s) {
             mbar_init(&ctl->full[s], 1);
             mbar_init(&ctl->empty[s], 1);
         }
@@ -443,8 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ya = p.a_row0[g] + mt * kBM;
                 const int yb = p.b_row0[g] + nt * kBN;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
-                    const uint32_t s = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1u;
+                    const uint32_t s = it % kS;
+                    const uint32_t ph = (it / kS) & 1u;
                     if (ctl->abort || !mbar_wait(&ctl->empty[s], ph ^ 1u, limit)) {
                         ok = false;
                         break;
@@ -482,10 +491,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ctl->abort = 1;
             }
             // drain: every issued copy has landed before the CTA can exit
-            const uint32_t first = it > kStages ? it - kStages : 0u;
+            const uint32_t first = it > kS ? it - kS : 0u;
             const uint64_t drain = limit > kDrainLimitNs ? limit : kDrainLimitNs;
             for (uint32_t j = first; j < it; ++j)
-                mbar_wait(&ctl->full[j % kStages], (j / kStages) & 1u, drain);
+                mbar_wait(&ctl->full[j % kS], (j / kS) & 1u, drain);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------
@@ -500,8 +509,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int g, mt, nt, split, kb0, nkb;
                 decode_unit(p, u, g, mt, nt, split, kb0, nkb);
                 for (int kb = 0; kb < nkb; ++kb, ++it, ++acc_it) {
-                    const uint32_t s = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1u;
+                    const uint32_t s = it % kS;
+                    const uint32_t ph = (it / kS) & 1u;
                     const uint32_t buf = acc_it & 1u;
                     const uint32_t aph = (acc_it >> 1) & 1u;
                     if (ctl->abort || !mbar_wait(&ctl->tempty[buf], aph ^ 1u, limit) ||
