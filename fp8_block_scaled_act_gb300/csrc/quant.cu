@@ -359,7 +359,7 @@ constexpr int kQ2Threads = 256;
 constexpr int kQ2Pitch = 132;  // bytes per row of the staging tile (bank-conflict padding)
 
 template <bool kSR>
-__global__ void __launch_bounds__(kQ2Threads) quant_128x128_kernel(
+__global__ void __launch_bounds__(kQ2Threads, 4) quant_128x128_kernel(
     const uint16_t* __restrict__ w, int64_t rows, int64_t cols, int64_t ldw,
     uint8_t* __restrict__ q, uint8_t* __restrict__ qT, float* __restrict__ scales, const ScaleRule rule,
     const SrKey sr)
