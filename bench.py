@@ -597,14 +597,62 @@ def load_traffic(kernel_name):
     return t.get(kernel_name)
 
 
+def _cpulist(text):
+    cpus = set()
+    for part in text.strip().split(","):
+        if not part:
+            continue
+        lo, _, hi = part.partition("-")
+        cpus.update(range(int(lo), int(hi or lo) + 1))
+    return cpus
+
+
+def gpu_local_cpus(torch, device):
+    """(NUMA node, CPUs of that node) of the host memory nearest the GPU, from
+    sysfs; (None, None) where the system does not say."""
+    try:
+        pr = torch.cuda.get_device_properties(device)
+        addr = f"{pr.pci_domain_id:04x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+        with open(f"/sys/bus/pci/devices/{addr}/numa_node") as f:
+            node = int(f.read())
+        if node < 0:
+            return None, None
+        with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+            return node, _cpulist(f.read())
+    except (AttributeError, OSError, RuntimeError, ValueError):
+        return None, None
+
+
+def alloc_pinned_near_gpu(torch, device, make):
+    """Runs `make` (which allocates the pinned host buffers) with this process
+    restricted to the CPUs of the GPU's NUMA node, so that first touch puts
+    the buffers in the host memory nearest the GPU; the affinity is restored
+    afterwards. Returns (make's result, a note on the placement)."""
+    node, cpus = gpu_local_cpus(torch, device)
+    allowed = os.sched_getaffinity(0)
+    use = (cpus or set()) & allowed
+    note = {"gpu_numa_node": node, "bound_cpus": len(use) if use else 0}
+    if not use:
+        return make(), note
+    os.sched_setaffinity(0, use)
+    try:
+        return make(), note
+    finally:
+        os.sched_setaffinity(0, allowed)
+
+
 def measure_e2e(args, fp8bs, torch, steps, device, step_flops, world, dist):
     """Same step through the public API with host buffers: every step copies
     its inputs in from pinned host memory, runs, and copies its outputs
     (Y, dX, dW) back. Consecutive steps are pipelined on three streams over
     two sets of device tensors (`steps`, two step objects): step i's host
     copies overlap step i - 1's kernels, as a data pipeline would run."""
-    h_in = [t.cpu().pin_memory() for t in steps[0].io()[0]]
-    h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in st.io()[1]] for st in steps]
+    def make():
+        h_in = [t.cpu().pin_memory() for t in steps[0].io()[0]]
+        h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in st.io()[1]] for st in steps]
+        return h_in, h_out
+
+    (h_in, h_out), placement = alloc_pinned_near_gpu(torch, device, make)
     launches = [st.launches() for st in steps]
     comp = torch.cuda.current_stream()
     h2d, d2h = torch.cuda.Stream(device), torch.cuda.Stream(device)
@@ -652,7 +700,8 @@ def measure_e2e(args, fp8bs, torch, steps, device, step_flops, world, dist):
             "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
             "ms_per_step": round(sec * 1e3 / n, 4),
             "pipeline": "host copies of step i overlap the kernels of step i-1 (three streams, two device "
-                        "buffer sets)"}
+                        "buffer sets)",
+            "host_buffers": placement}
 
 
 # ---------------------------------------------------------------------------

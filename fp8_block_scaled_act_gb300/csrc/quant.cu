@@ -658,7 +658,7 @@ __device__ __forceinline__ int find_group(const int32_t* tile_start, int ng, int
 // from the BF16 values; the 1x128 codes are staged in place of the source.
 // kSR: stochastic rounding of both passes (keys in p).
 template <bool kDual, bool kStash, bool kSR>
-__global__ void __launch_bounds__(kQ3Threads, kSR ? 2 : (kDual ? 3 : 4)) requant_128x1_T_kernel(const __grid_constant__ RequantParams p)
+__global__ void __launch_bounds__(kQ3Threads, kSR ? 2 : (kStash ? 3 : 4)) requant_128x1_T_kernel(const __grid_constant__ RequantParams p)
 {
     static_assert(kDual || !kStash, "the stash mode is a dual cast");
     // staging: BF16 source 128 x 128 x 2 bytes, or E4M3 128 x 128 bytes + row scales
@@ -693,6 +693,16 @@ __global__ void __launch_bounds__(kQ3Threads, kSR ? 2 : (kDual ? 3 : 4)) requant
         float cm[8];   // kStash: column maxima of the decoded 1x128 result
 #pragma unroll
         for (int e = 0; e < 8; ++e) cm[e] = 0.0f;
+        uint32_t mw[4] = {0u, 0u, 0u, 0u};   // otherwise: column maxima of the BF16 magnitudes
+        if constexpr (!kStash) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                mw[0] = __vmaxu2(mw[0], d[i].x & 0x7FFF7FFFu);
+                mw[1] = __vmaxu2(mw[1], d[i].y & 0x7FFF7FFFu);
+                mw[2] = __vmaxu2(mw[2], d[i].z & 0x7FFF7FFFu);
+                mw[3] = __vmaxu2(mw[3], d[i].w & 0x7FFF7FFFu);
+            }
+        }
         if constexpr (kDual) {
             // Row-wise (1x128) cast of the same rows from the registers: a
             // row's 128 channels are the 16 chunks held by 16 consecutive
@@ -741,14 +751,21 @@ __global__ void __launch_bounds__(kQ3Threads, kSR ? 2 : (kDual ? 3 : 4)) requant
                     continue;
                 }
                 if (chunk == 0) p.q_scales[(c0 / 128) * p.q_scale_ld + r0 + rl] = ts.s;
+                // the row's 8 values: from the registers in the stash mode;
+                // otherwise read back from this thread's own stage slot, so
+                // that the loaded registers are free after the maxima (four
+                // CTAs per SM at 64 registers)
+                uint4 di;
+                if constexpr (kStash) di = d[i];
+                else di = *reinterpret_cast<const uint4*>(stage + (rl * 128 + chunk * 8) * 2);
                 uint2 codes;
                 if constexpr (kSR) {
                     uint32_t wr[8];
                     sr_words8(SrKey{p.sr_seed, p.sr_salt_rows},
                               static_cast<uint64_t>((r0 + rl) * p.cols + c0 + chunk * 8), wr);
-                    codes = quant8_sr(d[i], ts, wr);
+                    codes = quant8_sr(di, ts, wr);
                 } else {
-                    codes = quant8(d[i], ts);
+                    codes = quant8(di, ts);
                 }
                 if (ch_ok) *reinterpret_cast<uint2*>(p.q + (r0 + rl) * p.cols + c0 + chunk * 8) = codes;
                 if constexpr (kStash) {
@@ -771,14 +788,6 @@ __global__ void __launch_bounds__(kQ3Threads, kSR ? 2 : (kDual ? 3 : 4)) requant
 #pragma unroll
             for (int e = 0; e < 8; ++e) col_part[rg][chunk * 8 + e] = cm[e];
         } else {
-            uint32_t mw[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                mw[0] = __vmaxu2(mw[0], d[i].x & 0x7FFF7FFFu);
-                mw[1] = __vmaxu2(mw[1], d[i].y & 0x7FFF7FFFu);
-                mw[2] = __vmaxu2(mw[2], d[i].z & 0x7FFF7FFFu);
-                mw[3] = __vmaxu2(mw[3], d[i].w & 0x7FFF7FFFu);
-            }
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 col_part[rg][chunk * 8 + 2 * k] = __uint_as_float(mw[k] << 16);

@@ -8,6 +8,7 @@ import subprocess
 import sys
 
 import pytest
+import torch
 import torch.multiprocessing as mp
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -79,3 +80,14 @@ def test_reference_arm_prints_one_json_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_cpulist_parsing_and_unbound_placement():
+    """sysfs cpulist syntax, and the pinned-buffer placement helper falls back
+    to an unbound allocation (affinity unchanged) where no GPU is visible."""
+    assert bench._cpulist("0-3,8,10-11\n") == {0, 1, 2, 3, 8, 10, 11}
+    assert bench._cpulist("") == set()
+    before = os.sched_getaffinity(0)
+    out, note = bench.alloc_pinned_near_gpu(torch, 0, lambda: 42)
+    assert out == 42 and os.sched_getaffinity(0) == before
+    assert set(note) == {"gpu_numa_node", "bound_cpus"}
