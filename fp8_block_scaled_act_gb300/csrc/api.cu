@@ -116,6 +116,20 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D map over a BF16 GEMM output [rows x cols] (row-major, 16-byte aligned
+// rows) for the epilogue's TMA stores: box of 64 columns x 32 rows, 128-byte
+// swizzle (the layout the epilogue writes into shared memory).
+bool make_out_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows)
+{
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {64u, 32u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 void init_params(GemmParams& p, DeviceState* st, int n_cols)
 {
     std::memset(&p, 0, sizeof(p));
@@ -190,6 +204,7 @@ fp8bs_status run_rowwise_gemm(bool dgrad, int32_t groups, const int32_t* off, co
         p.sa_kb0[g] = 0;
         p.sb_off[g] = static_cast<int64_t>(g) * (K / 128) * (N / 128);
         p.out_off[g] = 0;
+        p.out_row0[g] = off[g];
         tiles += ((rows + kBM - 1) / kBM) * p.n_tiles;
     }
     p.tile_start[groups] = tiles;
@@ -214,12 +229,17 @@ fp8bs_status run_rowwise_gemm(bool dgrad, int32_t groups, const int32_t* off, co
         p.ws_split_stride = M * width;
     }
 
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mo;
+    std::memset(&mo, 0, sizeof(mo));
     if (!make_map(&ma, a, contr, M, contr, kBM) ||
         !make_map(&mb, b, contr, width * groups, contr, kBN))
         return FP8BS_ERR_ARG;
+    if (used <= 1) {
+        if (!make_out_map(&mo, out, width, M)) return FP8BS_ERR_ARG;
+        p.tma_store = 1;
+    }
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    const fp8bs_status r = launch_status(launch_gemm(GemmKind::kBlockScaleBf16, ma, mb, p, st->num_sms, cs));
+    const fp8bs_status r = launch_status(launch_gemm(GemmKind::kBlockScaleBf16, ma, mb, mo, p, st->num_sms, cs));
     if (r != FP8BS_OK || used <= 1) return r;
     return launch_status(
         launch_splitk_reduce(ws, used, M * width, M * width, static_cast<uint16_t*>(out), st->num_sms, cs));
@@ -256,6 +276,7 @@ fp8bs_status run_wgrad(int32_t groups, const int32_t* off, int64_t T, const uint
         p.sa_kb0[g] = static_cast<int>(pstart / 128);
         p.sb_off[g] = (pstart / 128) * K;
         p.out_off[g] = static_cast<int64_t>(g) * N * K;
+        p.out_row0[g] = static_cast<int>(g * N);
         pstart += kb * 128;
     }
     if (pstart != T) return FP8BS_ERR_SHAPE;
@@ -271,9 +292,12 @@ fp8bs_status run_wgrad(int32_t groups, const int32_t* off, int64_t T, const uint
     p.out_ld = K;
     p.accumulate = accumulate ? 1 : 0;
 
-    CUtensorMap ma, mb;
+    // Wgrad stores its FP32 tile from registers (a TMA store through shared
+    // memory measured slower), so its output map stays unused
+    CUtensorMap ma, mb, mo;
+    std::memset(&mo, 0, sizeof(mo));
     if (!make_map(&ma, a, T, N, T, kBM) || !make_map(&mb, b, T, K, T, kBN)) return FP8BS_ERR_ARG;
-    return launch_status(launch_gemm(GemmKind::kVectorScaleF32, ma, mb, p, st->num_sms,
+    return launch_status(launch_gemm(GemmKind::kVectorScaleF32, ma, mb, mo, p, st->num_sms,
                                      static_cast<cudaStream_t>(stream)));
 }
 

@@ -75,8 +75,9 @@ constexpr int kScaleBytes = kScaleSlots * kScaleSlotFloats * 4;
 // Fprop / Dgrad output stage: per epilogue warp 32 rows x 64 BF16 columns.
 constexpr int kOutStageWarpBytes = 32 * 64 * 2;
 constexpr int kOutStageBytes = kEpiWarps * kOutStageWarpBytes;
-// Dynamic shared memory: the operand ring, the control block, then the
-// Wgrad scale ring or the Fprop / Dgrad output stage.
+// Dynamic shared memory (1024-byte aligned pieces, as the 128-byte swizzle
+// of the TMA boxes requires): the operand ring; the Fprop / Dgrad output
+// stage or the Wgrad scale ring; the control block.
 // Operand ring depth per kind: Wgrad, bound by its epilogue, measured
 // faster with three stages than with four (78.5 against 80.5 us on the dense
 // workload).
@@ -86,10 +87,16 @@ __host__ __device__ constexpr int num_stages()
     return kKind == GemmKind::kVectorScaleF32 ? 3 : kStages;
 }
 template <GemmKind kKind>
+constexpr int extra_bytes()
+{
+    return kKind == GemmKind::kVectorScaleF32 ? kScaleBytes : kOutStageBytes;
+}
+static_assert(kStageBytes % 1024 == 0 && kScaleBytes % 1024 == 0 && kOutStageBytes % 1024 == 0,
+              "shared-memory pieces keep 1024-byte alignment");
+template <GemmKind kKind>
 constexpr int smem_bytes()
 {
-    return num_stages<kKind>() * kStageBytes + kCtlBytes +
-           (kKind == GemmKind::kVectorScaleF32 ? kScaleBytes : kOutStageBytes) + 1024 /* alignment */;
+    return num_stages<kKind>() * kStageBytes + extra_bytes<kKind>() + kCtlBytes + 1024 /* alignment */;
 }
 
 struct SharedCtl {
@@ -150,7 +157,8 @@ __device__ __forceinline__ void decode_unit(const GemmParams& p, int u, int& g, 
 // 16-byte pieces of 32 different rows per instruction made those bursts
 // several times longer).
 __device__ __forceinline__ bool epilogue_block_scale(const GemmParams& p, SharedCtl* ctl, uint8_t* out_stage,
-                                                     uint32_t tmem_base, int warp, int lane, uint64_t limit)
+                                                     const CUtensorMap* map_out, uint32_t tmem_base, int warp,
+                                                     int lane, uint64_t limit)
 {
     const int ew = warp - kFirstEpiWarp;
     const int quarter = warp & 3;   // TMEM lanes this warp may access
@@ -240,14 +248,21 @@ __device__ __forceinline__ bool epilogue_block_scale(const GemmParams& p, Shared
         } else if (cols_ok) {
             // Two rounds of 64 columns: each thread writes its row's 64 values
             // as eight 16-byte chunks (chunk c of row r at slot c ^ (r % 8):
-            // conflict-free), then lanes 8q .. 8q + 7 store one row's 128
-            // contiguous bytes, four rows per instruction.
+            // conflict-free, and the 128-byte swizzle of a TMA box). When the
+            // warp's 32 rows all belong to this group, one TMA store per round
+            // writes the box while the warp goes on; otherwise lanes 8q .. 8q + 7
+            // store one row's 128 contiguous bytes, four rows per instruction.
             const int rows_left = p.a_rows[g] - (mt * kBM + quarter * 32);   // valid rows of this warp
+            const int out_row = p.out_row0[g] + mt * kBM + quarter * 32;
+            const bool tma = p.tma_store && rows_left >= 32;
             uint16_t* y0 = static_cast<uint16_t*>(p.out) + p.out_off[g] +
                            static_cast<int64_t>(p.a_row0[g] + mt * kBM + quarter * 32) * p.out_ld + col0;
             const uint32_t st_base = smem_addr(out_stage) + ew * kOutStageWarpBytes;
 #pragma unroll
             for (int rnd = 0; rnd < 2; ++rnd) {
+                // the stage's previous box has been read by its TMA store
+                if (lane == 0) bulk_wait_group_read<0>();
+                __syncwarp();
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const float2 a0 = acc[32 * rnd + 4 * c + 0];
@@ -261,16 +276,25 @@ __device__ __forceinline__ bool epilogue_block_scale(const GemmParams& p, Shared
                     pk.w = pack_bf16x2(a3.x, a3.y);
                     st_shared_v4(st_base + lane * 128 + ((c ^ (lane & 7)) << 4), pk);
                 }
-                __syncwarp();
+                if (tma) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(map_out, st_base, col0 + 64 * rnd, out_row);
+                        bulk_commit_group();
+                    }
+                } else {
+                    __syncwarp();
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int rr = 4 * i + (lane >> 3);
-                    const int c = lane & 7;
-                    const uint4 v = ld_shared_v4(st_base + rr * 128 + ((c ^ (rr & 7)) << 4));
-                    if (rr < rows_left)
-                        *reinterpret_cast<uint4*>(y0 + static_cast<int64_t>(rr) * p.out_ld + 64 * rnd + 8 * c) = v;
+                    for (int i = 0; i < 8; ++i) {
+                        const int rr = 4 * i + (lane >> 3);
+                        const int c = lane & 7;
+                        const uint4 v = ld_shared_v4(st_base + rr * 128 + ((c ^ (rr & 7)) << 4));
+                        if (rr < rows_left)
+                            *reinterpret_cast<uint4*>(y0 + static_cast<int64_t>(rr) * p.out_ld + 64 * rnd + 8 * c) = v;
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
             }
         }
     }
@@ -394,6 +418,7 @@ template <GemmKind kKind>
 __global__ void __launch_bounds__(kThreads, 1)
     block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                              const __grid_constant__ CUtensorMap map_b,
+                             const __grid_constant__ CUtensorMap map_out,
                              const __grid_constant__ GemmParams p)
 {
     constexpr int kS = num_stages<kKind>();
@@ -402,8 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + kS * kABytes;
-    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + kS * kStageBytes);
-    uint8_t* extra = smem + kS * kStageBytes + kCtlBytes;   // scale ring or output stage
+    uint8_t* extra = smem + kS * kStageBytes;   // output stage or scale ring
+    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(extra + extra_bytes<kKind>());
     float* scale_ring = reinterpret_cast<float*>(extra);
 
     const int warp = threadIdx.x >> 5;
@@ -424,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbarrier_init();
         tma_prefetch_desc(&map_a);
         tma_prefetch_desc(&map_b);
+        if (p.tma_store) tma_prefetch_desc(&map_out);
     }
     if (warp == 1) {
         tmem_alloc(&ctl->tmem_base, kTmemCols);
@@ -545,9 +571,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         setmaxnreg_inc<kEpilogueRegs>();
         bool ok;
         if constexpr (kKind == GemmKind::kBlockScaleBf16)
-            ok = epilogue_block_scale(p, ctl, extra, tmem_base, warp, lane, limit);
+            ok = epilogue_block_scale(p, ctl, extra, &map_out, tmem_base, warp, lane, limit);
         else
             ok = epilogue_vector_scale(p, ctl, scale_ring, tmem_base, warp, lane, limit);
+        // the warp's TMA stores have completed before the CTA exits
+        if (lane == 0) bulk_wait_group_all();
         if (!ok) {
             record_status(p.status, FP8BS_ERR_TIMEOUT);
             ctl->abort = 1;
@@ -601,8 +629,8 @@ __global__ void selftest_wait_kernel(unsigned int* status, uint64_t limit_ns)
 }
 
 template <GemmKind kKind>
-cudaError_t launch_kind(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmParams& p,
-                        int num_sms, cudaStream_t stream)
+cudaError_t launch_kind(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_out,
+                        const GemmParams& p, int num_sms, cudaStream_t stream)
 {
     static_assert(sizeof(SharedCtl) <= kCtlBytes, "control block");
     auto kernel = block_scaled_gemm_kernel<kKind>;
@@ -617,7 +645,7 @@ cudaError_t launch_kind(const CUtensorMap& map_a, const CUtensorMap& map_b, cons
     if (e != cudaSuccess) return e;
     const int units = p.total_tiles * p.splits;
     const int grid = units < num_sms ? units : num_sms;
-    kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_a, map_b, p);
+    kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_a, map_b, map_out, p);
     return cudaGetLastError();
 }
 
@@ -637,12 +665,12 @@ cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t split_stri
 }
 
 cudaError_t launch_gemm(GemmKind kind, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                        const GemmParams& p, int num_sms, cudaStream_t stream)
+                        const CUtensorMap& map_out, const GemmParams& p, int num_sms, cudaStream_t stream)
 {
     if (p.total_tiles <= 0) return cudaSuccess;
     if (kind == GemmKind::kBlockScaleBf16)
-        return launch_kind<GemmKind::kBlockScaleBf16>(map_a, map_b, p, num_sms, stream);
-    return launch_kind<GemmKind::kVectorScaleF32>(map_a, map_b, p, num_sms, stream);
+        return launch_kind<GemmKind::kBlockScaleBf16>(map_a, map_b, map_out, p, num_sms, stream);
+    return launch_kind<GemmKind::kVectorScaleF32>(map_a, map_b, map_out, p, num_sms, stream);
 }
 
 cudaError_t launch_selftest_wait(unsigned int* status, uint64_t limit_ns, cudaStream_t stream)

@@ -90,6 +90,7 @@ struct GemmParams {
     int32_t sa_kb0[kMaxGroups];   // first scale K-block of A
     int64_t sb_off[kMaxGroups];   // float offset of the group's B scales
     int64_t out_off[kMaxGroups];  // element offset of the group's output origin
+    int32_t out_row0[kMaxGroups]; // row of the output tensor map holding the group's output row 0
     const float* sa;              // A scale of (row, kb): sa[(sa_kb0 + kb) * sa_ld + row]
     int64_t sa_ld;
     int32_t sa_rows;              // rows that may be read from sa
@@ -98,6 +99,10 @@ struct GemmParams {
     void* out;
     int64_t out_ld;
     int accumulate;
+    // 1: the output tensor map passed with the launch is valid, and whole
+    // 32-row pieces of the BF16 output are stored from shared memory with
+    // TMA (Fprop / Dgrad without split-K)
+    int tma_store;
     int splits;                   // split-K ranges per tile (1: none)
     int kb_per_split;             // K-blocks per range
     float* ws;                    // split-K: fp32 range sums [splits][rows x out_ld], else null
@@ -111,8 +116,10 @@ enum class GemmKind {
     kVectorScaleF32,   // B scale per (K-block, column), FP32 output (Wgrad)
 };
 
+// map_out: the BF16 output [rows x out_ld] (box 64 x 32, 128-byte swizzle),
+// used when p.tma_store is set.
 cudaError_t launch_gemm(GemmKind kind, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                        const GemmParams& p, int num_sms, cudaStream_t stream);
+                        const CUtensorMap& map_out, const GemmParams& p, int num_sms, cudaStream_t stream);
 
 // GEMM tile shape and pipeline depth (exported for host-side planning).
 constexpr int kBM = 128;
