@@ -37,7 +37,7 @@ __all__ = [
     "fp8_quant_dual_stash", "fp8_quant_dual_stash_opts", "fp8_requant_128x1_T_sr", "fp8_quant_dual_sr",
     "fp8_quant_dual_stash_sr",
     "fp8bs_mx_scale_bytes", "fp8_mx_quant_1x32", "fp8_mx_gemm", "empty_mx_quant",
-    "fp8_mx_quant_1x32_T", "fp8_mx_gemm_f32", "empty_mx_quant_T",
+    "fp8_mx_quant_1x32_T", "fp8_mx_gemm_f32", "empty_mx_quant_T", "fp8_pack_ue8m0",
 ]
 
 SRC_BF16, SRC_E4M3 = 0, 1
@@ -107,6 +107,7 @@ def lib() -> ctypes.CDLL:
         "fp8_mx_gemm": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_mx_gemm_f32": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_mx_quant_1x32_T": ([P, I64, I64, P, P, P], S),
+        "fp8_pack_ue8m0": ([P, I64, I64, I32, I64, I64, P, P], S),
         "fp8_quant_128x128_sr": ([P, I64, I64, I64, I64, P, P, P, ctypes.c_uint64, ctypes.c_uint32, P, P], S),
         "fp8_block_gemm_fprop": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_block_gemm_dgrad": ([P, P, P, P, I64, I64, I64, P, P], S),
@@ -465,6 +466,25 @@ def fp8_mx_quant_1x32_T(x, qT, scale_atoms, stream=None) -> None:
         raise ValueError("output shapes do not match empty_mx_quant_T")
     _check("fp8_mx_quant_1x32_T", lib().fp8_mx_quant_1x32_T(_ptr(x), rows, cols, _ptr(qT), _ptr(scale_atoms),
                                                             _stream(stream)))
+
+
+def fp8_pack_ue8m0(scales, rows: int, K: int, row_block: int, row_stride: int, kb_stride: int,
+                   scale_atoms, stream=None) -> None:
+    """Exponent bytes of power-of-two fp32 block scales into the MX scale
+    atoms of an operand [rows x K] (each 128-element K-block's byte repeated
+    over its four 32-element blocks). The scale of (row r, K-block b) is
+    scales.flatten()[(r // row_block) * row_stride + b * kb_stride]; scales
+    that are not powers of two record FP8BS_ERR_DEVICE (fp8bs_device_status)."""
+    _need(scales, torch.float32, "scales"); _need(scale_atoms, torch.uint8, "scale_atoms")
+    rows, K = int(rows), int(K)
+    if rows > 0 and K > 0:
+        last = ((rows - 1) // int(row_block)) * int(row_stride) + (K // 128 - 1) * int(kb_stride)
+        if not scales.is_contiguous() or last >= scales.numel():
+            raise ValueError("scales do not hold every (row, K-block) index")
+        if scale_atoms.numel() < fp8bs_mx_scale_bytes(rows, K):
+            raise ValueError("scale_atoms smaller than fp8bs_mx_scale_bytes(rows, K)")
+    _check("fp8_pack_ue8m0", lib().fp8_pack_ue8m0(_ptr(scales), rows, K, int(row_block), int(row_stride),
+                                                  int(kb_stride), _ptr(scale_atoms), _stream(stream)))
 
 
 def _rule_kwargs(opts: Optional[ScaleOpts]) -> dict:

@@ -625,6 +625,22 @@ int64_t fp8bs_mx_scale_bytes(int64_t rows, int64_t cols)
     return (rows + 127) / 128 * (cols / 128) * 512;
 }
 
+fp8bs_status fp8_pack_ue8m0(const float* scales, int64_t rows, int64_t K, int32_t row_block,
+                            int64_t row_stride, int64_t kb_stride, uint8_t* scale_atoms, void* stream)
+{
+    if (rows < 0 || K <= 0 || row_stride < 0 || kb_stride < 0) return FP8BS_ERR_ARG;
+    if (row_block != 1 && row_block != 128) return FP8BS_ERR_ARG;
+    if (K % 128 != 0 || rows > 0x7FFFFF00) return FP8BS_ERR_SHAPE;
+    if (rows == 0) return FP8BS_OK;
+    if (!scales || !scale_atoms) return FP8BS_ERR_ARG;
+    if (!aligned16(scale_atoms) || (reinterpret_cast<uintptr_t>(scales) & 3u) != 0) return FP8BS_ERR_ALIGN;
+    DeviceState* st = nullptr;
+    fp8bs_status s = device_state(&st);
+    if (s != FP8BS_OK) return s;
+    return launch_status(launch_pack_ue8m0(scales, rows, K, row_block, row_stride, kb_stride, scale_atoms,
+                                           st->status, st->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
 fp8bs_status fp8_mx_quant_1x32(const void* x, int64_t rows, int64_t cols, uint8_t* q, uint8_t* scale_atoms,
                                void* stream)
 {

@@ -140,6 +140,13 @@ cudaError_t launch_mx_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, c
                            const uint8_t* sfb, int M, int N, int K, uint16_t* out, float* out_f32,
                            uint64_t wait_limit_ns, unsigned int* status, int num_sms, cudaStream_t stream);
 
+// Exponent bytes of power-of-two block scales into the MX scale atoms of an
+// operand [rows x K] (mx.cu); non-representable scales record
+// FP8BS_ERR_DEVICE in *status and write 255.
+cudaError_t launch_pack_ue8m0(const float* scales, int64_t rows, int64_t K, int row_block, int64_t row_stride,
+                              int64_t kb_stride, uint8_t* atoms, unsigned int* status, int num_sms,
+                              cudaStream_t stream);
+
 cudaError_t launch_selftest_wait(unsigned int* status, uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace fp8bs

@@ -498,6 +498,68 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Packing of power-of-two fp32 block scales into the scale-atom layout: the
+// 128-element K-blocks of the 1x128 / 128x128 recipe become four 32-element
+// blocks with the same exponent byte, so the MX GEMM applies them with the
+// tensor core's block scaling. One thread per (operand row, K-block): the
+// row's four bytes of that K-block are one 32-bit word of the atom.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+// Exponent byte of a power-of-two fp32 scale s = 2^(E - 127), 0 <= E <= 254;
+// 255 (not a number in the exponent-byte format) for any other value.
+__device__ __forceinline__ uint32_t ue8m0_of(float s)
+{
+    const uint32_t b = __float_as_uint(s);
+    const uint32_t e = b >> 23, m = b & 0x7FFFFFu;
+    if (e >= 1u && e <= 254u && m == 0u) return e;   // normal power of two: E = the biased exponent
+    if (b == 0x00400000u) return 0u;                  // 2^-127, the one subnormal in range
+    return 255u;
+}
+
+__global__ void __launch_bounds__(256) pack_ue8m0_kernel(const float* __restrict__ scales, int64_t rows,
+                                                         int64_t rows_pad, int64_t kblocks, int row_block,
+                                                         int64_t row_stride, int64_t kb_stride,
+                                                         uint8_t* __restrict__ atoms, unsigned int* status)
+{
+    const int64_t n = rows_pad * kblocks;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        // i = (row tile, K-block, row within the tile): consecutive threads
+        // fill consecutive rows of one atom
+        const int64_t m = i & 127;
+        const int64_t kb = (i >> 7) % kblocks;
+        const int64_t rt = (i >> 7) / kblocks;
+        const int64_t r = rt * 128 + m;
+        uint32_t E = 127u;   // padding rows: scale 1
+        if (r < rows) {
+            E = ue8m0_of(__ldg(scales + (r / row_block) * row_stride + kb * kb_stride));
+            if (E == 255u) atomicCAS(status, 0u, static_cast<unsigned int>(FP8BS_ERR_DEVICE));
+        }
+        *reinterpret_cast<uint32_t*>(atoms + (rt * kblocks + kb) * 512 + 16 * (m & 31) + 4 * (m >> 5)) =
+            E * 0x01010101u;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_pack_ue8m0(const float* scales, int64_t rows, int64_t K, int row_block, int64_t row_stride,
+                              int64_t kb_stride, uint8_t* atoms, unsigned int* status, int num_sms,
+                              cudaStream_t stream)
+{
+    const int64_t rows_pad = (rows + 127) / 128 * 128;
+    const int64_t n = rows_pad * (K / 128);
+    if (n == 0) return cudaSuccess;
+    int64_t blocks = (n + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    pack_ue8m0_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(scales, rows, rows_pad, K / 128, row_block,
+                                                                         row_stride, kb_stride, atoms, status);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_mx_quant_1x32(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* q, uint8_t* atoms,
                                  int num_sms, cudaStream_t stream)
 {

@@ -450,6 +450,36 @@ FP8BS_API fp8bs_status fp8_mx_gemm_f32(const uint8_t* a, const uint8_t* a_scale_
 FP8BS_API fp8bs_status fp8_mx_quant_1x32_T(const void* x, int64_t rows, int64_t cols, uint8_t* qT,
                                            uint8_t* scale_atoms, void* stream);
 
+/* NEXT-4: the packed Blackwell scale layout for power-of-two scales ([P4]  */
+/* conventions table, row "Compact formats": fp32 scale containers on Hopper, */
+/* packed exponent bytes on Blackwell, packed at the GEMM boundary). Writes   */
+/* the exponent byte E of each fp32 scale s = 2^(E - 127) of a block-scaled   */
+/* operand into the scale atoms of fp8_mx_gemm (layout above), the scale of   */
+/* each 128-element K-block repeated over its four 32-element blocks, so that */
+/* fp8_mx_gemm / fp8_mx_gemm_f32 compute the 1x128 / 128x128 recipe's GEMM    */
+/* with the tensor core applying the scales (exact for power-of-two scales:   */
+/* only the fp32 summation order differs from the promoted GEMMs above).      */
+/* Scales come from the quantizers with FP8BS_SCALE_UE8M0.                    */
+/* The operand is [rows x K], K contiguous, K % 128 == 0 (the contraction).   */
+/* The scale of (row r, K-block b) is                                          */
+/*   scales[(r / row_block) * row_stride + b * kb_stride], row_block 1 or 128: */
+/*   1x128 scales (S1 layout):      row_block 1,   row_stride 1,             */
+/*                                  kb_stride = fp8bs_scale_ld(rows);         */
+/*   128x1 transposed scales (S3):  row_block 1,   row_stride 1,             */
+/*                                  kb_stride = the operand's rows;           */
+/*   W^T [N x K] from S2 scales:    row_block 128, row_stride 1,             */
+/*                                  kb_stride = N / 128;                     */
+/*   W [K x N] (Dgrad's B, contraction N): row_block 128,                     */
+/*                                  row_stride = N / 128, kb_stride 1.        */
+/* The caller's scale array must hold every index above. scale_atoms:         */
+/* fp8bs_mx_scale_bytes(rows, K) bytes, 16-byte aligned; padding rows are     */
+/* written as 127 (scale 1). A scale that is not a power of two in            */
+/* [2^-127, 2^127] has no exponent byte: its bytes are written as 255 and     */
+/* FP8BS_ERR_DEVICE is recorded in the device status word.                    */
+FP8BS_API fp8bs_status fp8_pack_ue8m0(const float* scales, int64_t rows, int64_t K, int32_t row_block,
+                                      int64_t row_stride, int64_t kb_stride, uint8_t* scale_atoms,
+                                      void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* S7. Grouped (MoE expert) GEMMs                                             */
 /* The dense definitions above applied to each group (expert) g, whose token  */

@@ -302,6 +302,32 @@ def mx_gemm(a, sa, b, sb, ii=None, jj=None):
     return out
 
 
+def pack_ue8m0(scales, rows: int, K: int, row_block: int, row_stride: int, kb_stride: int):
+    """Exponent bytes of power-of-two block scales for the MX GEMM, in the
+    plain layout [rows x K/32] (one byte per row and 32-element block of K).
+
+    Follows the "Compact formats" row of the prime-rl conventions table
+    (Blackwell consumes the scales as packed exponent bytes) read with the
+    OCP MX v1.0 exponent-byte format: s = 2^(E - 127), E in 0..254, 255 = NaN.
+    The scale of (row r, 128-element K-block b) is
+    scales.ravel()[(r // row_block) * row_stride + b * kb_stride]; each
+    K-block's byte covers its four 32-element blocks. A scale that is not an
+    exact positive power of two in [2^-127, 2^127] has no byte: 255.
+    Returns (bytes uint8 [rows x K/32], count of scales without a byte).
+    """
+    flat = np.asarray(scales, np.float32).ravel()
+    kb = K // 128
+    r = np.arange(rows, dtype=np.int64)[:, None]
+    b = np.arange(kb, dtype=np.int64)[None, :]
+    s = flat[(r // row_block) * row_stride + b * kb_stride].astype(np.float64)   # [rows x kb]
+    with np.errstate(invalid="ignore"):
+        m, e = np.frexp(s)                  # s = m * 2^e with m in [0.5, 1) for finite s > 0
+        E = e.astype(np.int64) + 126        # s = 2^(e - 1) = 2^(E - 127) exactly when m == 0.5
+        ok = (m == 0.5) & (E >= 0) & (E <= 254)
+    byte = np.where(ok, E, 255).astype(np.uint8)
+    return np.repeat(byte, 4, axis=1), int(np.count_nonzero(~ok))
+
+
 def padded_tokens(rows: int, offsets=None) -> int:
     if offsets is None:
         return (rows + 127) // 128 * 128

@@ -792,3 +792,91 @@ def test_planted_mistake_is_caught(fault, pin):
     finally:
         oracle.set_fault(oracle.FAULT_NONE)
     assert check()
+
+
+# ---------------------------------------------------------------------------
+# Packed exponent bytes of power-of-two scales (prime-rl PR #4073 conventions
+# table, row "Compact formats"; OCP MX v1.0 exponent-byte format)
+# ---------------------------------------------------------------------------
+
+def test_pack_ue8m0_exponent_bytes_closed_form():
+    """Every exponent byte E in 0..254 is the byte of the scale 2^(E - 127)
+    (2^-127 is an fp32 subnormal and still has one); every K-block's byte
+    covers its four 32-element blocks; anything that is not a positive power
+    of two in [2^-127, 2^127] has no byte (255) and is counted."""
+    E = np.arange(255)
+    s = np.ldexp(1.0, E - 127).astype(np.float32)
+    assert np.array_equal(s.astype(np.float64), np.ldexp(1.0, E - 127))   # all exact in fp32
+    b, bad = oracle.pack_ue8m0(s, 255, 256, 1, 1, 0)
+    assert bad == 0 and b.shape == (255, 8)
+    assert np.array_equal(b[:, 0], E) and (b == b[:, :1]).all()
+    odd = np.array([0.75, 3.0, 0.0, -1.0, -0.5, np.inf, np.nan, 2.0 ** -128, 2.0 ** -149,
+                    np.float32(1.0) + np.float32(2.0 ** -23)], np.float32)
+    b, bad = oracle.pack_ue8m0(odd, odd.size, 128, 1, 1, 0)
+    assert bad == odd.size and (b == 255).all()
+
+
+def _ue8m0_operands(M=200, K=384, N=256, seed=5):
+    rng = np.random.default_rng(seed)
+    x = oracle.f32_to_bf16((rng.standard_normal((M, K)) * np.exp(2 * rng.standard_normal((M, 1)))).astype(np.float32))
+    w = oracle.f32_to_bf16((rng.standard_normal((K, N)) * 0.02).astype(np.float32))
+    with oracle.scale_rule(ue8m0=True):
+        xq, sx = oracle.quant_1x128(x)
+        wq, sw = oracle.quant_128x128(w)
+        xT, sxT = oracle.requant_128x1_T(xq, sx)
+    return xq, sx, wq, sw, xT, sxT
+
+
+def _mx_dequant(q, e):
+    """Values of an MX operand: E4M3 codes times 2^(E - 127) per 32-element block."""
+    return oracle.e4m3_decode(q).astype(np.float64) * np.ldexp(1.0, np.repeat(e.astype(np.int64) - 127, 32, axis=1))
+
+
+def test_pack_ue8m0_reproduces_the_block_dequantization():
+    """With UE8M0-rule scales, dequantizing through the packed bytes (per
+    32-element block) gives exactly the 1x128 / 128x128 dequantization (per
+    128-element block) for the four operand layouts: activation rows, the
+    transposed 128x1 operand, W^T (Fprop's B) and W (Dgrad's B); a ragged
+    row count and a wrong stride are both caught."""
+    M, K, N = 200, 384, 256
+    xq, sx, wq, sw, xT, sxT = _ue8m0_operands(M, K, N)
+    dec = lambda q: oracle.e4m3_decode(q).astype(np.float64)
+    # activation rows: scale (r, b) = sx[b, r]
+    b, bad = oracle.pack_ue8m0(sx, M, K, 1, 1, sx.shape[1])
+    assert bad == 0
+    assert np.array_equal(_mx_dequant(xq, b), dec(xq) * np.repeat(sx[:, :M].T, 128, axis=1))
+    # transposed operand [K x Mpad]: scale (k, token block t) = sxT[t, k]
+    Mp = xT.shape[1]
+    b, bad = oracle.pack_ue8m0(sxT, K, Mp, 1, 1, K)
+    assert bad == 0
+    assert np.array_equal(_mx_dequant(xT, b), dec(xT) * np.repeat(sxT.T, 128, axis=1))
+    # W^T [N x K]: scale (n, b) = sw[b, n // 128]
+    wT = np.ascontiguousarray(wq.T)
+    b, bad = oracle.pack_ue8m0(sw, N, K, 128, 1, N // 128)
+    assert bad == 0
+    assert np.array_equal(_mx_dequant(wT, b), dec(wT) * np.repeat(np.repeat(sw.T, 128, axis=0), 128, axis=1))
+    # W [K x N] with the contraction along N: scale (k, nb) = sw[k // 128, nb]
+    b, bad = oracle.pack_ue8m0(sw, K, N, 128, N // 128, 1)
+    assert bad == 0
+    assert np.array_equal(_mx_dequant(wq, b), dec(wq) * np.repeat(np.repeat(sw, 128, axis=0), 128, axis=1))
+    # a wrong stride (the row pitch of the 1x128 array off by one) is not the same operand
+    b, _ = oracle.pack_ue8m0(sx, M, K, 1, 1, sx.shape[1] - 1)
+    assert not np.array_equal(_mx_dequant(xq, b), dec(xq) * np.repeat(sx[:, :M].T, 128, axis=1))
+
+
+def test_pack_ue8m0_mx_gemm_is_the_promoted_gemm():
+    """The oracle's MX GEMM over packed UE8M0 operands agrees with the
+    oracle's per-128 promoted Fprop to fp32 summation-order accuracy: with
+    power-of-two scales the block scaling of the tensor core computes the
+    recipe's GEMM, only the order of the fp32 additions differs."""
+    M, K, N = 200, 384, 256
+    xq, sx, wq, sw, _, _ = _ue8m0_operands(M, K, N)
+    bx, _ = oracle.pack_ue8m0(sx, M, K, 1, 1, sx.shape[1])
+    bw, _ = oracle.pack_ue8m0(sw, N, K, 128, 1, N // 128)
+    y_mx = oracle.mx_gemm(xq, bx, np.ascontiguousarray(wq.T), bw).astype(np.float64)
+    y_pr = oracle.fprop(xq, sx, wq, sw).astype(np.float64)
+    a = np.abs(_mx_dequant(xq, bx))
+    bt = np.abs(_mx_dequant(np.ascontiguousarray(wq.T), bw))
+    absprod = a @ bt.T
+    assert np.all(np.abs(y_mx - y_pr) <= 2.0 ** -20 * absprod + 1e-30)
+    assert np.count_nonzero(y_pr) > 0.99 * y_pr.size
