@@ -706,9 +706,22 @@ fp8bs_status mx_gemm_common(const uint8_t* a, const uint8_t* a_scale_atoms, cons
     DeviceState* st = nullptr;
     fp8bs_status s = device_state(&st);
     if (s != FP8BS_OK) return s;
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mo;
     if (!make_map(&ma, a, K, M, K, kBM) || !make_map(&mb, b, K, N, K, kBN)) return FP8BS_ERR_ARG;
-    return launch_status(launch_mx_gemm(ma, mb, a_scale_atoms, b_scale_atoms, static_cast<int>(M),
+    {
+        // the output as boxes of 32 rows x 64 bytes (32 BF16 or 16 FP32 columns), 64-byte swizzle
+        const bool f32 = out_bf16 == nullptr;
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * (f32 ? 4 : 2)};
+        const cuuint32_t box[2] = {f32 ? 16u : 32u, 32u};
+        const cuuint32_t estr[2] = {1u, 1u};
+        if (g_encode(&mo, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return FP8BS_ERR_ARG;
+    }
+    return launch_status(launch_mx_gemm(ma, mb, &mo, a_scale_atoms, b_scale_atoms,
+                                        static_cast<int>(M),
                                         static_cast<int>(N), static_cast<int>(K), out_bf16, out_f32,
                                         g_wait_limit_ns, st->status, st->num_sms,
                                         static_cast<cudaStream_t>(stream)));

@@ -135,10 +135,13 @@ cudaError_t launch_mx_quant_1x32(const uint16_t* x, int64_t rows, int64_t cols, 
                                  int num_sms, cudaStream_t stream);
 cudaError_t launch_mx_quant_1x32_T(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* qT, uint8_t* atoms,
                                    cudaStream_t stream);
-// out (BF16) or out_f32 (FP32, when not null) [M x N]
-cudaError_t launch_mx_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const uint8_t* sfa,
-                           const uint8_t* sfb, int M, int N, int K, uint16_t* out, float* out_f32,
-                           uint64_t wait_limit_ns, unsigned int* status, int num_sms, cudaStream_t stream);
+// out (BF16) or out_f32 (FP32, when not null) [M x N]; map_out (nullable):
+// the BF16 output as boxes of 32 columns x 32 rows with the 64-byte swizzle,
+// through which whole 32-row boxes are stored with TMA.
+cudaError_t launch_mx_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap* map_out,
+                           const uint8_t* sfa, const uint8_t* sfb, int M, int N, int K, uint16_t* out,
+                           float* out_f32, uint64_t wait_limit_ns, unsigned int* status, int num_sms,
+                           cudaStream_t stream);
 
 // Exponent bytes of power-of-two block scales into the MX scale atoms of an
 // operand [rows x K] (mx.cu); non-representable scales record

@@ -26,6 +26,8 @@
 // runs once per tile.
 #include <cuda_runtime.h>
 
+#include <cstring>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -208,7 +210,14 @@ constexpr int kSfCol0 = kBN;                    // first scale column
 constexpr int kSfColsPerStage = 12;             // 4 (A) + 8 (B)
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
 constexpr int kCtlBytes = 256;
-constexpr int kSmemBytes = kStages * (kABytes + kBBytes + kSfaBytes + kSfbBytes) + kCtlBytes + 1024;
+// Output stage: per epilogue warp one box of 32 rows x 64 bytes (32 BF16 or
+// 16 FP32 columns) in the 64-byte swizzle: 16-byte chunk c of row r at slot
+// c ^ ((r / 2) % 4), conflict-free for 32 lanes writing one row each.
+constexpr int kOutBoxBytes = 32 * 32 * 2;
+constexpr int kOutStageBytes = kEpiWarps * kOutBoxBytes;
+constexpr int kRingBytes = kStages * (kABytes + kBBytes + kSfaBytes + kSfbBytes);
+static_assert(kRingBytes % 512 == 0, "the output stage needs 512-byte alignment");
+constexpr int kSmemBytes = kRingBytes + kOutStageBytes + kCtlBytes + 1024;
 
 struct MxCtl {
     uint64_t full[kStages];
@@ -227,17 +236,10 @@ struct MxParams {
     int M, N;
     uint16_t* out;        // BF16 [M x N], or
     float* out_f32;       // FP32 [M x N] (when not null)
+    int tma_store;        // whole 32-row boxes leave through the output map
     uint64_t wait_limit_ns;
     unsigned int* status;
 };
-
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_addr(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
-                 : "memory");
-}
 
 // Shared-memory descriptor of a scale atom (32 rows of 16 bytes, no swizzle;
 // 8-row core matrices 128 bytes apart).
@@ -291,7 +293,7 @@ __device__ __forceinline__ void record_status(unsigned int* status, unsigned int
 template <bool kF32>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                   const __grid_constant__ MxParams p)
+                   const __grid_constant__ CUtensorMap map_out, const __grid_constant__ MxParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -300,7 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sB = sA + kStages * kABytes;
     uint8_t* sSfa = sB + kStages * kBBytes;
     uint8_t* sSfb = sSfa + kStages * kSfaBytes;
-    MxCtl* ctl = reinterpret_cast<MxCtl*>(sSfb + kStages * kSfbBytes);
+    uint8_t* sOut = smem + kRingBytes;
+    MxCtl* ctl = reinterpret_cast<MxCtl*>(sOut + kOutStageBytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -318,6 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbarrier_init();
         tma_prefetch_desc(&map_a);
         tma_prefetch_desc(&map_b);
+        if (p.tma_store) tma_prefetch_desc(&map_out);
     }
     if (warp == 1) {
         tmem_alloc(&ctl->tmem_base, kTmemCols);
@@ -427,30 +431,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int col0 = nt * kBN + half * 128;
             uint32_t ra[32], rb[32];
             if constexpr (kF32) {
-                // FP32 output: each 32-column chunk goes out as it is read
-                const bool st_ok = row < p.M && col0 < p.N;
-                float4* y = reinterpret_cast<float4*>(p.out_f32 + static_cast<int64_t>(row) * p.N + col0);
-#pragma unroll
-                for (int c = 0; c < 4; c += 2) {
-                    tmem_ld_x32(tmem_base + lane_addr + half * 128 + 32 * c, ra);
-                    tmem_ld_x32(tmem_base + lane_addr + half * 128 + 32 * c + 32, rb);
-                    tmem_ld_wait(ra);
-                    tmem_ld_wait(rb);
-                    if (c == 2) {
-                        tc_fence_before_sync();
+                // FP32 output: the whole 128-column row in registers, the
+                // accumulator released, then (whole 32-row boxes) eight boxes
+                // of 16 columns through the warp's stage with TMA stores, or
+                // (a ragged last row tile) plain 16-byte stores
+                uint32_t rc[32], rd[32];
+                tmem_ld_x32(tmem_base + lane_addr + half * 128, ra);
+                tmem_ld_x32(tmem_base + lane_addr + half * 128 + 32, rb);
+                tmem_ld_x32(tmem_base + lane_addr + half * 128 + 64, rc);
+                tmem_ld_x32(tmem_base + lane_addr + half * 128 + 96, rd);
+                tmem_ld_wait(ra);
+                tmem_regs_ready(rb);
+                tmem_regs_ready(rc);
+                tmem_regs_ready(rd);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->tempty);
+                const int row0 = mt * kBM + quarter * 32;
+                if (p.tma_store && row0 + 32 <= p.M && col0 < p.N) {
+                    const uint32_t box = smem_addr(sOut) + ew * kOutBoxBytes;
+                    auto put = [&](const uint32_t (&r)[32], int b) {
+                        if (lane == 0) bulk_wait_group_read<0>();    // the previous box has been read
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&ctl->tempty);
-                    }
-                    if (st_ok) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const int v = 16 * (b & 1) + 4 * c;
+                            st_shared_v4(box + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4),
+                                         make_uint4(r[v], r[v + 1], r[v + 2], r[v + 3]));
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&map_out, box, col0 + 16 * b, row0);
+                            bulk_commit_group();
+                        }
+                    };
+                    put(ra, 0); put(ra, 1); put(rb, 2); put(rb, 3);
+                    put(rc, 4); put(rc, 5); put(rd, 6); put(rd, 7);
+                } else if (row < p.M && col0 < p.N) {
+                    float4* y = reinterpret_cast<float4*>(p.out_f32 + static_cast<int64_t>(row) * p.N + col0);
+                    auto put = [&](const uint32_t (&r)[32], int c) {
 #pragma unroll
                         for (int v = 0; v < 8; ++v)
-                            y[8 * c + v] = make_float4(__uint_as_float(ra[4 * v]), __uint_as_float(ra[4 * v + 1]),
-                                                       __uint_as_float(ra[4 * v + 2]), __uint_as_float(ra[4 * v + 3]));
-#pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            y[8 * c + 8 + v] = make_float4(__uint_as_float(rb[4 * v]), __uint_as_float(rb[4 * v + 1]),
-                                                           __uint_as_float(rb[4 * v + 2]), __uint_as_float(rb[4 * v + 3]));
-                    }
+                            y[8 * c + v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                                       __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                    };
+                    put(ra, 0); put(rb, 1); put(rc, 2); put(rd, 3);
                 }
                 continue;
             }
@@ -477,12 +503,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk[32 + i] = pack_bf16x2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));
                 pk[48 + i] = pack_bf16x2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1]));
             }
-            if (row < p.M && col0 < p.N) {
+            const int row0 = mt * kBM + quarter * 32;           // first row of this warp
+            if (p.tma_store && row0 + 32 <= p.M && col0 < p.N) {
+                // four boxes of 32 columns through the warp's stage, each
+                // leaving with one TMA store while the warp goes on
+                const uint32_t box = smem_addr(sOut) + ew * kOutBoxBytes;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    if (lane == 0) bulk_wait_group_read<0>();    // the previous box has been read
+                    __syncwarp();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        st_shared_v4(box + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4),
+                                     make_uint4(pk[16 * b + 4 * c], pk[16 * b + 4 * c + 1], pk[16 * b + 4 * c + 2],
+                                                pk[16 * b + 4 * c + 3]));
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&map_out, box, col0 + 32 * b, row0);
+                        bulk_commit_group();
+                    }
+                }
+            } else if (row < p.M && col0 < p.N) {
                 uint4* y = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(row) * p.N + col0);
 #pragma unroll
                 for (int v = 0; v < 16; ++v) y[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
             }
         }
+        // the warp's TMA stores have completed before the CTA exits
+        if (lane == 0) bulk_wait_group_all();
         if (!ok) {
             record_status(p.status, FP8BS_ERR_TIMEOUT);
             ctl->abort = 1;
@@ -586,9 +635,10 @@ cudaError_t launch_mx_quant_1x32_T(const uint16_t* x, int64_t rows, int64_t cols
     return cudaGetLastError();
 }
 
-cudaError_t launch_mx_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const uint8_t* sfa,
-                           const uint8_t* sfb, int M, int N, int K, uint16_t* out, float* out_f32,
-                           uint64_t wait_limit_ns, unsigned int* status, int num_sms, cudaStream_t stream)
+cudaError_t launch_mx_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap* map_out,
+                           const uint8_t* sfa, const uint8_t* sfb, int M, int N, int K, uint16_t* out,
+                           float* out_f32, uint64_t wait_limit_ns, unsigned int* status, int num_sms,
+                           cudaStream_t stream)
 {
     static_assert(sizeof(MxCtl) <= kCtlBytes, "control block");
     MxParams p;
@@ -601,6 +651,10 @@ cudaError_t launch_mx_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, c
     p.N = N;
     p.out = out;
     p.out_f32 = out_f32;
+    p.tma_store = map_out != nullptr ? 1 : 0;
+    CUtensorMap mo;
+    if (p.tma_store) mo = *map_out;
+    else std::memset(&mo, 0, sizeof(mo));
     p.wait_limit_ns = wait_limit_ns;
     p.status = status;
     const int total = p.m_tiles * p.n_tiles;
@@ -613,7 +667,7 @@ cudaError_t launch_mx_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, c
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = total < num_sms ? total : num_sms;
-    kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_a, map_b, p);
+    kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_a, map_b, mo, p);
     return cudaGetLastError();
 }
 

@@ -321,6 +321,22 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32])
         : "memory");
 }
 
+// Ties registers filled by a TMEM load that an earlier tmem_ld_wait already
+// covered (tcgen05.wait::ld waits for all of the thread's loads) to this
+// point, so that the compiler cannot move their uses above that wait.
+__device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[32])
+{
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+                   "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]),
+                   "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]),
+                   "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]),
+                   "+r"(r[31])
+                 :
+                 : "memory");
+}
+
 // Register budget changes for a whole warpgroup (all four warps execute them).
 template <uint32_t kRegs>
 __device__ __forceinline__ void setmaxnreg_dec()
