@@ -278,6 +278,81 @@ class DenseStep:
         return self._launches
 
 
+class DenseUe8m0Step(DenseStep):
+    """The dense step with power-of-two scales: the same casts under the
+    UE8M0 scale rule, each cast's scales packed into exponent bytes right
+    after it (fp8_pack_ue8m0), and the three GEMMs run on the tensor core's
+    block scaling (the MX kernel) instead of the software promotion."""
+
+    def __init__(self, fp8bs, torch, device, M, K, N, seed=0):
+        super().__init__(fp8bs, torch, device, M, K, N, seed)
+        e = fp8bs
+        self.opts = e.ScaleOpts(e.SCALE_UE8M0, 0.0, 0.0)
+        Mp = self.xT.shape[1]
+        atoms = lambda rows, k: torch.empty(e.fp8bs_mx_scale_bytes(rows, k), dtype=torch.uint8, device=device)
+        self.ax, self.awT, self.ady = atoms(M, K), atoms(N, K), atoms(M, N)
+        self.aw, self.adyT, self.axT = atoms(K, N), atoms(N, Mp), atoms(K, Mp)
+        self.names = ["quant_128x128(W)+pack", "quant_dual_stash(X)+pack", "mx_fprop", "quant_dual(dY)+pack",
+                      "mx_dgrad", "mx_wgrad"]
+        self.kernels_per_step = 12        # three casts, six packs, three GEMMs
+
+    def work(self):
+        M, K, N = self.M, self.K, self.N
+        flops, b = step_work(M, K, N)
+        Mp = self.xT.shape[1]
+        pack = lambda rows, k, scales: 4 * scales + rows * k // 32     # scales read + exponent bytes written
+        s_ld = (M + 3) // 4 * 4
+        wb = pack(N, K, (K // 128) * (N // 128)) + pack(K, N, (K // 128) * (N // 128))
+        xb = pack(M, K, (K // 128) * s_ld) + pack(K, Mp, (Mp // 128) * K)
+        yb = pack(M, N, (N // 128) * s_ld) + pack(N, Mp, (Mp // 128) * N)
+        atoms = lambda rows, k: rows * k // 32
+        bytes_ = {
+            "quant_128x128(W)+pack": b["quant_128x128(W)"] + wb,
+            "quant_dual_stash(X)+pack": b["quant_dual_stash(X)"] + xb,
+            "mx_fprop": M * K + N * K + atoms(M, K) + atoms(N, K) + 2 * M * N,
+            "quant_dual(dY)+pack": b["quant_dual(dY)"] + yb,
+            "mx_dgrad": M * N + K * N + atoms(M, N) + atoms(K, N) + 2 * M * K,
+            "mx_wgrad": N * Mp + K * Mp + atoms(N, Mp) + atoms(K, Mp) + 4 * N * K,
+        }
+        f = flops["fprop"]
+        return {"mx_fprop": f, "mx_dgrad": f, "mx_wgrad": f}, bytes_
+
+    def describe(self):
+        d = super().describe()
+        d["workload"] = (d["workload"] + ", power-of-two (UE8M0) scales, GEMMs on the tensor core's block "
+                         "scaling over packed exponent bytes")
+        return d
+
+    def launches(self):
+        e, o = self.fp8bs, self.opts
+        M, K, N = self.M, self.K, self.N
+        Mp = self.xT.shape[1]
+
+        def w_cast():
+            e.fp8_quant_128x128_opts(self.W, self.wq, self.wqT, self.sw, o)
+            e.fp8_pack_ue8m0(self.sw, N, K, 128, 1, N // 128, self.awT)       # W^T, Fprop's B
+            e.fp8_pack_ue8m0(self.sw, K, N, 128, N // 128, 1, self.aw)        # W, Dgrad's B
+
+        def x_cast():
+            e.fp8_quant_dual_stash_opts(self.X, self.xq, self.sx, self.xT, self.sxT, o)
+            e.fp8_pack_ue8m0(self.sx, M, K, 1, 1, self.sx.shape[1], self.ax)
+            e.fp8_pack_ue8m0(self.sxT, K, Mp, 1, 1, K, self.axT)
+
+        def dy_cast():
+            e.fp8_quant_dual_opts(self.dY, self.dyq, self.sdy, self.dyT, self.sdyT, o)
+            e.fp8_pack_ue8m0(self.sdy, M, N, 1, 1, self.sdy.shape[1], self.ady)
+            e.fp8_pack_ue8m0(self.sdyT, N, Mp, 1, 1, N, self.adyT)
+
+        return [
+            w_cast,
+            x_cast,
+            lambda: e.fp8_mx_gemm(self.xq, self.ax, self.wqT, self.awT, self.Y),
+            dy_cast,
+            lambda: e.fp8_mx_gemm(self.dyq, self.ady, self.wq, self.aw, self.dX),
+            lambda: e.fp8_mx_gemm_f32(self.dyT, self.adyT, self.xT, self.axT, self.dW),
+        ]
+
+
 class MoeStep:
     """Grouped MoE expert pass: 1x128 quantization of X, A and dY, batched
     128x128 quantization of the expert weights, Fprop of the up and down
@@ -439,6 +514,8 @@ def run_ours(args, world, rank, local):
             return MoeStep(fp8bs, torch, device, seed=rank)
         if args.workload == "longk":
             return LongKStep(fp8bs, torch, device, seed=rank)
+        if args.workload == "dense_ue8m0":
+            return DenseUe8m0Step(fp8bs, torch, device, M, K, N, seed=rank)
         return DenseStep(fp8bs, torch, device, M, K, N, seed=rank)
 
     step = make_step()
@@ -478,7 +555,8 @@ def run_ours(args, world, rank, local):
         if fp8bs.fp8bs_device_status(reset=True) != 0:
             raise RuntimeError("device status error during graph warm-up")
 
-    nk = len(launches)
+    nk = len(launches)                       # launch functions of a step (one per breakdown entry)
+    kernels_per_step = getattr(step, "kernels_per_step", nk)
     # Timed region: exactly K steps with CUDA events at the step boundaries
     # only (an event between two kernels costs a few microseconds on this
     # GPU, ~25 us over the dense step's seven kernels).
@@ -561,7 +639,8 @@ def run_ours(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
         "data": {"dense": "synthetic (seeded normal; 0.1% outliers in X)",
                  "moe": "synthetic (seeded normal; Dirichlet(0.5) expert counts)",
-                 "longk": "synthetic (seeded uniform U(0.5, 1.5))"}[args.workload],
+                 "longk": "synthetic (seeded uniform U(0.5, 1.5))",
+                 "dense_ue8m0": "synthetic (seeded normal; 0.1% outliers in X)"}[args.workload],
         "config": dict(step.describe(),
                        parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
                        l2="flushed between steps (256 MiB write outside the step events)",
@@ -575,7 +654,7 @@ def run_ours(args, world, rank, local):
                          "a few us); ms_per_step and value come from the timed steps with events at step "
                          "boundaries only"),
         "e2e": e2e,
-        "gpu_launches": nk * args.steps, "clocks": clk,
+        "gpu_launches": kernels_per_step * args.steps, "clocks": clk,
     }
     if rank == 0:
         if args.workload == "dense":
@@ -919,9 +998,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-graph", action="store_true",
                     help="time the step as stream launches instead of one CUDA graph replay")
-    ap.add_argument("--workload", choices=["dense", "moe", "longk"], default="dense",
+    ap.add_argument("--workload", choices=["dense", "moe", "longk", "dense_ue8m0"], default="dense",
                     help="dense: the linear layer's fwd+bwd (default); moe: grouped expert pass; "
-                         "longk: 256xKx256 split-K Fprop for K up to 65536")
+                         "longk: 256xKx256 split-K Fprop for K up to 65536; dense_ue8m0: the dense step "
+                         "with power-of-two scales, GEMMs on the tensor core's block scaling")
     ap.add_argument("--cpu-sample", type=float, default=1.0 / 16,
                     help="--impl reference: fraction of token rows the oracle runs per step")
     ap.add_argument("--cpu-baseline-sample", type=float, default=1.0,
