@@ -14,24 +14,26 @@
 //
 //   warp 0      TMA producer: one thread streams 128x128 (A) and 256x128 (B)
 //               E4M3 tiles (K-major, 128-byte swizzle) into a 4-stage (Wgrad: 3)
-//               shared-memory ring.
+//               shared-memory ring. For Wgrad it also copies each K-block's
+//               scales (the tile's 128 row scales and 256 column scales) into
+//               an 8-slot shared-memory ring with two untiled bulk copies
+//               inside the stage's transaction (Fprop / Dgrad epilogue threads
+//               need one scalar per K-block and prefetch it themselves, two
+//               K-blocks ahead).
 //   warp 1      MMA issuer: one thread issues four tcgen05.mma (K = 32 each)
 //               per K-block into a fresh TMEM accumulator (the first with
 //               accumulate = 0), double-buffered over 2 x 256 TMEM columns,
 //               and commits to mbarriers that free the smem stage and hand
 //               the partial to the epilogue.
-//               For Wgrad it also copies each K-block's scales (the
-//               tile's 128 row scales and 256 column scales) into an
-//               8-slot shared-memory ring with two untiled bulk copies per
-//               K-block (Fprop / Dgrad epilogue threads need one scalar per
-//               K-block and prefetch it themselves, two K-blocks ahead).
 //   warps 2-3   idle (they complete the first warpgroup, which gives its
 //               registers to the epilogue with setmaxnreg).
 //   warps 4-11  promotion epilogue: each warp owns 32 TMEM lanes (rows) and
 //               128 columns; per K-block it loads the fp32 partial with
 //               tcgen05.ld, releases the TMEM buffer, and does
 //               acc = fma(P_b, s_a * s_b, acc) in registers; at the end of a
-//               tile it converts and stores the accumulator.
+//               tile it converts and stores the accumulator (Fprop / Dgrad:
+//               BF16 boxes through a per-warp swizzled stage, each leaving
+//               with a TMA store; Wgrad: FP32 pairs from registers).
 //
 // The kernel is persistent (one CTA per SM, 128x256 output tiles in a
 // grid-stride order) and handles groups (MoE experts) through a per-group
@@ -307,9 +309,9 @@ __device__ __forceinline__ bool epilogue_block_scale(const GemmParams& p, Shared
 // every K-block, read as shared-memory broadcasts that cost more load
 // bandwidth than the MMA leaves room for. The 16x256b layout spreads the
 // tile as 4 rows x 32 columns per thread: a K-block then needs 4 row scales
-// and 16 column-scale pairs per thread. Scales arrive in a per-warp 3-slot
-// shared-memory ring filled by cp.async two K-blocks ahead (slot: the 32 row
-// scales of the warp's quarter, then its 128 column scales).
+// and 16 column-scale pairs per thread, read from the slot of the scale ring
+// that the TMA producer filled with the K-block's operand stage (the tile's
+// 128 row scales, then its 256 column scales).
 __device__ __forceinline__ bool epilogue_vector_scale(const GemmParams& p, SharedCtl* ctl, const float* ring,
                                                       uint32_t tmem_base, int warp, int lane, uint64_t limit)
 {
