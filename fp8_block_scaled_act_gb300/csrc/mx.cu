@@ -23,7 +23,12 @@
 // (tcgen05.cp.32x128b.warpx4) and issues four
 // tcgen05.mma.kind::mxf8f6f4.block_scale (K = 32 each, the scale byte of
 // each 32-block selected through the instruction descriptor). The epilogue
-// runs once per tile.
+// runs once per tile: it reads the accumulator into registers, hands tensor
+// memory back to the MMA issuer, and stores the tile as boxes of 32 rows x
+// 64 bytes through a per-warp stage with TMA stores (plain stores for the
+// rows of a ragged last row tile). The same kernel runs the 1x128 / 128x128
+// recipe's GEMMs when their scales are powers of two (fp8_pack_ue8m0 below
+// writes those scales into the atom layout).
 #include <cuda_runtime.h>
 
 #include <cstring>
