@@ -280,37 +280,31 @@ class DenseStep:
 
 class DenseUe8m0Step(DenseStep):
     """The dense step with power-of-two scales: the same casts under the
-    UE8M0 scale rule, each cast's scales packed into exponent bytes right
-    after it (fp8_pack_ue8m0), and the three GEMMs run on the tensor core's
-    block scaling (the MX kernel) instead of the software promotion."""
+    UE8M0 scale rule, each also writing its scales as exponent bytes in the
+    layout the MX GEMM reads (the *_packed casts), and the three GEMMs run on
+    the tensor core's block scaling (the MX kernel) instead of the software
+    promotion."""
 
     def __init__(self, fp8bs, torch, device, M, K, N, seed=0):
         super().__init__(fp8bs, torch, device, M, K, N, seed)
         e = fp8bs
-        self.opts = e.ScaleOpts(e.SCALE_UE8M0, 0.0, 0.0)
         Mp = self.xT.shape[1]
         atoms = lambda rows, k: torch.empty(e.fp8bs_mx_scale_bytes(rows, k), dtype=torch.uint8, device=device)
         self.ax, self.awT, self.ady = atoms(M, K), atoms(N, K), atoms(M, N)
         self.aw, self.adyT, self.axT = atoms(K, N), atoms(N, Mp), atoms(K, Mp)
-        self.names = ["quant_128x128(W)+pack", "quant_dual_stash(X)+pack", "mx_fprop", "quant_dual(dY)+pack",
+        self.names = ["quant_128x128(W)+atoms", "quant_dual_stash(X)+atoms", "mx_fprop", "quant_dual(dY)+atoms",
                       "mx_dgrad", "mx_wgrad"]
-        self.kernels_per_step = 12        # three casts, six packs, three GEMMs
 
     def work(self):
         M, K, N = self.M, self.K, self.N
         flops, b = step_work(M, K, N)
         Mp = self.xT.shape[1]
-        pack = lambda rows, k, scales: 4 * scales + rows * k // 32     # scales read + exponent bytes written
-        s_ld = (M + 3) // 4 * 4
-        wb = pack(N, K, (K // 128) * (N // 128)) + pack(K, N, (K // 128) * (N // 128))
-        xb = pack(M, K, (K // 128) * s_ld) + pack(K, Mp, (Mp // 128) * K)
-        yb = pack(M, N, (N // 128) * s_ld) + pack(N, Mp, (Mp // 128) * N)
-        atoms = lambda rows, k: rows * k // 32
+        atoms = lambda rows, k: rows * k // 32                            # exponent bytes of an operand
         bytes_ = {
-            "quant_128x128(W)+pack": b["quant_128x128(W)"] + wb,
-            "quant_dual_stash(X)+pack": b["quant_dual_stash(X)"] + xb,
+            "quant_128x128(W)+atoms": b["quant_128x128(W)"] + atoms(N, K) + atoms(K, N),
+            "quant_dual_stash(X)+atoms": b["quant_dual_stash(X)"] + atoms(M, K) + atoms(K, Mp),
             "mx_fprop": M * K + N * K + atoms(M, K) + atoms(N, K) + 2 * M * N,
-            "quant_dual(dY)+pack": b["quant_dual(dY)"] + yb,
+            "quant_dual(dY)+atoms": b["quant_dual(dY)"] + atoms(M, N) + atoms(N, Mp),
             "mx_dgrad": M * N + K * N + atoms(M, N) + atoms(K, N) + 2 * M * K,
             "mx_wgrad": N * Mp + K * Mp + atoms(N, Mp) + atoms(K, Mp) + 4 * N * K,
         }
@@ -320,34 +314,19 @@ class DenseUe8m0Step(DenseStep):
     def describe(self):
         d = super().describe()
         d["workload"] = (d["workload"] + ", power-of-two (UE8M0) scales, GEMMs on the tensor core's block "
-                         "scaling over packed exponent bytes")
+                         "scaling over exponent bytes the casts write")
         return d
 
     def launches(self):
-        e, o = self.fp8bs, self.opts
-        M, K, N = self.M, self.K, self.N
-        Mp = self.xT.shape[1]
-
-        def w_cast():
-            e.fp8_quant_128x128_opts(self.W, self.wq, self.wqT, self.sw, o)
-            e.fp8_pack_ue8m0(self.sw, N, K, 128, 1, N // 128, self.awT)       # W^T, Fprop's B
-            e.fp8_pack_ue8m0(self.sw, K, N, 128, N // 128, 1, self.aw)        # W, Dgrad's B
-
-        def x_cast():
-            e.fp8_quant_dual_stash_opts(self.X, self.xq, self.sx, self.xT, self.sxT, o)
-            e.fp8_pack_ue8m0(self.sx, M, K, 1, 1, self.sx.shape[1], self.ax)
-            e.fp8_pack_ue8m0(self.sxT, K, Mp, 1, 1, K, self.axT)
-
-        def dy_cast():
-            e.fp8_quant_dual_opts(self.dY, self.dyq, self.sdy, self.dyT, self.sdyT, o)
-            e.fp8_pack_ue8m0(self.sdy, M, N, 1, 1, self.sdy.shape[1], self.ady)
-            e.fp8_pack_ue8m0(self.sdyT, N, Mp, 1, 1, N, self.adyT)
-
+        e = self.fp8bs
+        # each cast writes its scales' exponent bytes into the atoms of the
+        # GEMM operands it feeds, in the same pass
         return [
-            w_cast,
-            x_cast,
+            lambda: e.fp8_quant_128x128_packed(self.W, self.wq, self.wqT, self.sw, self.awT, self.aw),
+            lambda: e.fp8_quant_dual_stash_packed(self.X, self.xq, self.sx, self.xT, self.sxT, self.ax, self.axT),
             lambda: e.fp8_mx_gemm(self.xq, self.ax, self.wqT, self.awT, self.Y),
-            dy_cast,
+            lambda: e.fp8_quant_dual_packed(self.dY, self.dyq, self.sdy, self.dyT, self.sdyT, self.ady,
+                                            self.adyT),
             lambda: e.fp8_mx_gemm(self.dyq, self.ady, self.wq, self.aw, self.dX),
             lambda: e.fp8_mx_gemm_f32(self.dyT, self.adyT, self.xT, self.axT, self.dW),
         ]

@@ -38,6 +38,7 @@ __all__ = [
     "fp8_quant_dual_stash_sr",
     "fp8bs_mx_scale_bytes", "fp8_mx_quant_1x32", "fp8_mx_gemm", "empty_mx_quant",
     "fp8_mx_quant_1x32_T", "fp8_mx_gemm_f32", "empty_mx_quant_T", "fp8_pack_ue8m0",
+    "fp8_quant_128x128_packed", "fp8_quant_dual_packed", "fp8_quant_dual_stash_packed", "empty_mx_atoms",
 ]
 
 SRC_BF16, SRC_E4M3 = 0, 1
@@ -108,6 +109,9 @@ def lib() -> ctypes.CDLL:
         "fp8_mx_gemm_f32": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_mx_quant_1x32_T": ([P, I64, I64, P, P, P], S),
         "fp8_pack_ue8m0": ([P, I64, I64, I32, I64, I64, P, P], S),
+        "fp8_quant_128x128_packed": ([P, I64, I64, I64, I64, P, P, P, P, P, P, P], S),
+        "fp8_quant_dual_packed": ([P, I64, I64, P, P, P, P, P, P, P, P], S),
+        "fp8_quant_dual_stash_packed": ([P, I64, I64, P, P, P, P, P, P, P, P], S),
         "fp8_quant_128x128_sr": ([P, I64, I64, I64, I64, P, P, P, ctypes.c_uint64, ctypes.c_uint32, P, P], S),
         "fp8_block_gemm_fprop": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_block_gemm_dgrad": ([P, P, P, P, I64, I64, I64, P, P], S),
@@ -485,6 +489,62 @@ def fp8_pack_ue8m0(scales, rows: int, K: int, row_block: int, row_stride: int, k
             raise ValueError("scale_atoms smaller than fp8bs_mx_scale_bytes(rows, K)")
     _check("fp8_pack_ue8m0", lib().fp8_pack_ue8m0(_ptr(scales), rows, K, int(row_block), int(row_stride),
                                                   int(kb_stride), _ptr(scale_atoms), _stream(stream)))
+
+
+def empty_mx_atoms(rows: int, K: int, batch: int = 1, device="cuda"):
+    """Scale atoms (uint8) of `batch` operands [rows x K] for the MX GEMM."""
+    return torch.empty(batch * max(fp8bs_mx_scale_bytes(rows, K), 0), dtype=torch.uint8, device=device)
+
+
+def fp8_quant_128x128_packed(w, q, qT, scales, atoms_wT, atoms_w, stream=None) -> None:
+    """fp8_quant_128x128 under the UE8M0 rule that also writes the scale atoms
+    of W^T [cols x rows] (atoms_wT) and of W [rows x cols] (atoms_w), per
+    batch entry; rows, cols multiples of 128."""
+    _need(w, torch.bfloat16, "w"); _need(q, torch.uint8, "q"); _need(scales, torch.float32, "scales")
+    _need(qT, torch.uint8, "qT"); _need(atoms_wT, torch.uint8, "atoms_wT"); _need(atoms_w, torch.uint8, "atoms_w")
+    batch = w.shape[0] if w.dim() == 3 else 1
+    rows, cols = w.shape[-2:]
+    nb = ((rows + 127) // 128) * ((cols + 127) // 128)
+    if (q.numel() != w.numel() or q.shape[-2:] != (rows, cols) or scales.numel() != batch * nb
+            or qT.numel() != w.numel() or qT.shape[-2:] != (cols, rows)):
+        raise ValueError("output shapes do not match empty_quant_128x128")
+    need = batch * fp8bs_mx_scale_bytes(cols, rows)
+    if atoms_wT.numel() < need or atoms_w.numel() < need:
+        raise ValueError("atoms smaller than batch * fp8bs_mx_scale_bytes(cols, rows)")
+    _check("fp8_quant_128x128_packed", lib().fp8_quant_128x128_packed(
+        _ptr(w), batch, rows, cols, cols, _ptr(q), _ptr(qT), _ptr(scales), _ptr(atoms_wT), _ptr(atoms_w),
+        _opts(SCALE_UE8M0, 0.0, 0.0), _stream(stream)))
+
+
+def _dual_packed(fn, x, q, scales, qT, scalesT, q_atoms, qT_atoms, stream) -> None:
+    _need(x, torch.bfloat16, "x")
+    for t, n, d in ((q, "q", torch.uint8), (scales, "scales", torch.float32), (qT, "qT", torch.uint8),
+                    (scalesT, "scalesT", torch.float32), (q_atoms, "q_atoms", torch.uint8),
+                    (qT_atoms, "qT_atoms", torch.uint8)):
+        _need(t, d, n)
+    rows, cols = x.shape
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    mp = fp8bs_padded_tokens(rows)
+    if (q.shape != (rows, cols) or scales.shape != ((cols + 127) // 128, fp8bs_scale_ld(rows))
+            or qT.shape != (cols, mp) or scalesT.shape != (mp // 128, cols)):
+        raise ValueError("output shapes do not match empty_quant_1x128 / empty_requant_128x1_T")
+    if q_atoms.numel() < fp8bs_mx_scale_bytes(rows, cols) or qT_atoms.numel() < fp8bs_mx_scale_bytes(cols, mp):
+        raise ValueError("atoms smaller than fp8bs_mx_scale_bytes of q / qT")
+    _check(fn, getattr(lib(), fn)(_ptr(x), rows, cols, _ptr(q), _ptr(scales), _ptr(qT), _ptr(scalesT),
+                                  _ptr(q_atoms), _ptr(qT_atoms), _opts(SCALE_UE8M0, 0.0, 0.0), _stream(stream)))
+
+
+def fp8_quant_dual_packed(x, q, scales, qT, scalesT, q_atoms, qT_atoms, stream=None) -> None:
+    """fp8_quant_dual under the UE8M0 rule that also writes the scale atoms
+    of q [rows x cols] and of qT [cols x Mpad]; dense x, cols % 128 == 0."""
+    _dual_packed("fp8_quant_dual_packed", x, q, scales, qT, scalesT, q_atoms, qT_atoms, stream)
+
+
+def fp8_quant_dual_stash_packed(x, q, scales, qT, scalesT, q_atoms, qT_atoms, stream=None) -> None:
+    """fp8_quant_dual_stash under the UE8M0 rule that also writes the scale
+    atoms of q [rows x cols] and of qT [cols x Mpad]; dense x, cols % 128 == 0."""
+    _dual_packed("fp8_quant_dual_stash_packed", x, q, scales, qT, scalesT, q_atoms, qT_atoms, stream)
 
 
 def _rule_kwargs(opts: Optional[ScaleOpts]) -> dict:

@@ -82,7 +82,7 @@ fp8bs_status quant_1x128_common(const void* x, int64_t rows, int64_t cols, int64
                                 float* scales, const fp8bs_scale_opts* opts, const SrParams* sr, void* stream);
 fp8bs_status quant_128x128_common(const void* w, int64_t batch, int64_t rows, int64_t cols, int64_t ldw,
                                   uint8_t* q, uint8_t* qT, float* scales, const fp8bs_scale_opts* opts,
-                                  const SrParams* sr, void* stream);
+                                  const SrParams* sr, void* stream, uint8_t* atoms_wT, uint8_t* atoms_w);
 
 // Public scale options -> kernel rule; false for invalid options.
 bool to_rule(const fp8bs_scale_opts* o, ScaleRule* r)
@@ -394,7 +394,7 @@ fp8bs_status fp8_quant_128x128_opts(const void* w, int64_t batch, int64_t rows, 
                                     uint8_t* q, uint8_t* qT, float* scales, const fp8bs_scale_opts* opts,
                                     void* stream)
 {
-    return quant_128x128_common(w, batch, rows, cols, ldw, q, qT, scales, opts, nullptr, stream);
+    return quant_128x128_common(w, batch, rows, cols, ldw, q, qT, scales, opts, nullptr, stream, nullptr, nullptr);
 }
 
 fp8bs_status fp8_quant_128x128_sr(const void* w, int64_t batch, int64_t rows, int64_t cols, int64_t ldw,
@@ -402,7 +402,7 @@ fp8bs_status fp8_quant_128x128_sr(const void* w, int64_t batch, int64_t rows, in
                                   const fp8bs_scale_opts* opts, void* stream)
 {
     const SrParams sr{seed, salt};
-    return quant_128x128_common(w, batch, rows, cols, ldw, q, qT, scales, opts, &sr, stream);
+    return quant_128x128_common(w, batch, rows, cols, ldw, q, qT, scales, opts, &sr, stream, nullptr, nullptr);
 }
 
 }  // extern "C"
@@ -412,7 +412,7 @@ namespace {
 
 fp8bs_status quant_128x128_common(const void* w, int64_t batch, int64_t rows, int64_t cols, int64_t ldw,
                                   uint8_t* q, uint8_t* qT, float* scales, const fp8bs_scale_opts* opts,
-                                  const SrParams* sr, void* stream)
+                                  const SrParams* sr, void* stream, uint8_t* atoms_wT, uint8_t* atoms_w)
 {
     ScaleRule rule;
     if (!to_rule(opts, &rule)) return FP8BS_ERR_ARG;
@@ -424,8 +424,9 @@ fp8bs_status quant_128x128_common(const void* w, int64_t batch, int64_t rows, in
     DeviceState* st = nullptr;
     fp8bs_status s = device_state(&st);
     if (s != FP8BS_OK) return s;
-    return launch_status(launch_quant_128x128(static_cast<const uint16_t*>(w), batch, rows, cols,
-                                              ldw, q, qT, scales, rule, sr, static_cast<cudaStream_t>(stream)));
+    return launch_status(launch_quant_128x128(static_cast<const uint16_t*>(w), batch, rows, cols, ldw, q, qT,
+                                              scales, rule, sr, static_cast<cudaStream_t>(stream), atoms_wT,
+                                              atoms_w, st->status));
 }
 
 }  // namespace
@@ -443,7 +444,8 @@ namespace {
 fp8bs_status requant_common(int src_mode, const void* src, const float* src_scales, int64_t rows, int64_t cols,
                             const int32_t* group_offsets_host, int32_t groups, uint8_t* qT, float* scalesT,
                             uint8_t* q, float* q_scales, const fp8bs_scale_opts* opts, void* stream,
-                            bool stash = false, const SrParams* sr = nullptr)
+                            bool stash = false, const SrParams* sr = nullptr, uint8_t* q_atoms = nullptr,
+                            uint8_t* qT_atoms = nullptr)
 {
     ScaleRule rule;
     if (!to_rule(opts, &rule)) return FP8BS_ERR_ARG;
@@ -480,6 +482,9 @@ fp8bs_status requant_common(int src_mode, const void* src, const float* src_scal
     p.q_scale_ld = fp8bs_scale_ld(rows);
     p.stash = stash ? 1 : 0;
     p.rule = rule;
+    p.q_atoms = q_atoms;
+    p.qT_atoms = qT_atoms;
+    p.status = st->status;
     if (sr) {
         // the 1x128 part of a dual cast takes (seed, salt), the transposed
         // part (seed, salt + 1); a plain requant's transposed cast (seed, salt)
@@ -559,6 +564,41 @@ fp8bs_status fp8_quant_dual_stash_opts(const void* x, int64_t rows, int64_t cols
     if (rows > 0 && (!q || !scales)) return FP8BS_ERR_ARG;
     return requant_common(FP8BS_SRC_BF16, x, nullptr, rows, cols, group_offsets_host, groups, qT, scalesT, q,
                           scales, opts, stream, true);
+}
+
+fp8bs_status fp8_quant_dual_packed(const void* x, int64_t rows, int64_t cols, uint8_t* q, float* scales,
+                                   uint8_t* qT, float* scalesT, uint8_t* q_atoms, uint8_t* qT_atoms,
+                                   const fp8bs_scale_opts* opts, void* stream)
+{
+    if (!opts || opts->rule != FP8BS_SCALE_UE8M0) return FP8BS_ERR_ARG;
+    if (cols % 128 != 0) return FP8BS_ERR_SHAPE;
+    if (rows > 0 && (!q || !scales || !q_atoms || !qT_atoms)) return FP8BS_ERR_ARG;
+    if ((q_atoms && !aligned16(q_atoms)) || (qT_atoms && !aligned16(qT_atoms))) return FP8BS_ERR_ALIGN;
+    return requant_common(FP8BS_SRC_BF16, x, nullptr, rows, cols, nullptr, 0, qT, scalesT, q, scales, opts, stream,
+                          false, nullptr, q_atoms, qT_atoms);
+}
+
+fp8bs_status fp8_quant_dual_stash_packed(const void* x, int64_t rows, int64_t cols, uint8_t* q, float* scales,
+                                         uint8_t* qT, float* scalesT, uint8_t* q_atoms, uint8_t* qT_atoms,
+                                         const fp8bs_scale_opts* opts, void* stream)
+{
+    if (!opts || opts->rule != FP8BS_SCALE_UE8M0) return FP8BS_ERR_ARG;
+    if (cols % 128 != 0) return FP8BS_ERR_SHAPE;
+    if (rows > 0 && (!q || !scales || !q_atoms || !qT_atoms)) return FP8BS_ERR_ARG;
+    if ((q_atoms && !aligned16(q_atoms)) || (qT_atoms && !aligned16(qT_atoms))) return FP8BS_ERR_ALIGN;
+    return requant_common(FP8BS_SRC_BF16, x, nullptr, rows, cols, nullptr, 0, qT, scalesT, q, scales, opts, stream,
+                          true, nullptr, q_atoms, qT_atoms);
+}
+
+fp8bs_status fp8_quant_128x128_packed(const void* w, int64_t batch, int64_t rows, int64_t cols, int64_t ldw,
+                                      uint8_t* q, uint8_t* qT, float* scales, uint8_t* atoms_wT, uint8_t* atoms_w,
+                                      const fp8bs_scale_opts* opts, void* stream)
+{
+    if (!opts || opts->rule != FP8BS_SCALE_UE8M0) return FP8BS_ERR_ARG;
+    if (rows % 128 != 0 || cols % 128 != 0) return FP8BS_ERR_SHAPE;
+    if (!atoms_wT || !atoms_w) return FP8BS_ERR_ARG;
+    if (!aligned16(atoms_wT) || !aligned16(atoms_w)) return FP8BS_ERR_ALIGN;
+    return quant_128x128_common(w, batch, rows, cols, ldw, q, qT, scales, opts, nullptr, stream, atoms_wT, atoms_w);
 }
 
 fp8bs_status fp8_requant_128x1_T_sr(int src_mode, const void* src, const float* src_scales, int64_t rows,

@@ -34,9 +34,15 @@ cudaError_t launch_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, in
                                uint8_t* q, float* scales, int64_t scale_ld, const ScaleRule& rule,
                                const SrParams* sr, int num_sms, cudaStream_t stream);
 
+// atoms_wT / atoms_w (nullable; rows and cols multiples of 128): the MX
+// scale atoms of the two GEMM operands the weight feeds, W^T [cols x rows]
+// and W [rows x cols] (contraction along cols), per batch entry; a scale
+// without an exponent byte records FP8BS_ERR_DEVICE in *status.
 cudaError_t launch_quant_128x128(const uint16_t* w, int64_t batch, int64_t rows, int64_t cols,
                                  int64_t ldw, uint8_t* q, uint8_t* qT, float* scales,
-                                 const ScaleRule& rule, const SrParams* sr, cudaStream_t stream);
+                                 const ScaleRule& rule, const SrParams* sr, cudaStream_t stream,
+                                 uint8_t* atoms_wT = nullptr, uint8_t* atoms_w = nullptr,
+                                 unsigned int* status = nullptr);
 
 struct RequantParams {
     int mode;                  // FP8BS_SRC_BF16 or FP8BS_SRC_E4M3
@@ -65,6 +71,12 @@ struct RequantParams {
     int sr;
     uint64_t sr_seed;
     uint32_t sr_salt_rows, sr_salt_cols;
+    // Optional (dense only): the exponent bytes of the scales in the MX
+    // scale atoms of q [rows x cols] and of qT [cols x mpad]; a scale
+    // without a byte records FP8BS_ERR_DEVICE in *status.
+    uint8_t* q_atoms;
+    uint8_t* qT_atoms;
+    unsigned int* status;
 };
 
 cudaError_t launch_requant_128x1_T(const RequantParams& p, cudaStream_t stream);

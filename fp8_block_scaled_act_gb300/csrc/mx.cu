@@ -598,17 +598,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 namespace {
 
-// Exponent byte of a power-of-two fp32 scale s = 2^(E - 127), 0 <= E <= 254;
-// 255 (not a number in the exponent-byte format) for any other value.
-__device__ __forceinline__ uint32_t ue8m0_of(float s)
-{
-    const uint32_t b = __float_as_uint(s);
-    const uint32_t e = b >> 23, m = b & 0x7FFFFFu;
-    if (e >= 1u && e <= 254u && m == 0u) return e;   // normal power of two: E = the biased exponent
-    if (b == 0x00400000u) return 0u;                  // 2^-127, the one subnormal in range
-    return 255u;
-}
-
 __global__ void __launch_bounds__(256) pack_ue8m0_kernel(const float* __restrict__ scales, int64_t rows,
                                                          int64_t rows_pad, int64_t kblocks, int row_block,
                                                          int64_t row_stride, int64_t kb_stride,

@@ -399,6 +399,28 @@ __device__ __forceinline__ float2 e4m3x2_to_f32(uint16_t v)
     return __half22float2(hh);
 }
 
+// Exponent byte of a power-of-two fp32 scale s = 2^(E - 127), 0 <= E <= 254
+// (the OCP MX exponent-byte format); 255 (not a number in that format) for
+// any other value.
+__device__ __forceinline__ uint32_t ue8m0_of(float s)
+{
+    const uint32_t b = __float_as_uint(s);
+    const uint32_t e = b >> 23, m = b & 0x7FFFFFu;
+    if (e >= 1u && e <= 254u && m == 0u) return e;   // normal power of two: E = the biased exponent
+    if (b == 0x00400000u) return 0u;                  // 2^-127, the one subnormal in range
+    return 255u;
+}
+
+// Byte offset, inside the MX scale atoms of an operand with `kblocks`
+// 128-element K-blocks, of the four exponent bytes of row r and K-block kb
+// (atom (r / 128, kb) is 512 bytes; row m = r % 128 = m0 + 32 m1 sits at
+// 16 m0 + 4 m1).
+__device__ __forceinline__ int64_t atom_offset(int64_t r, int64_t kb, int64_t kblocks)
+{
+    const int64_t m = r & 127;
+    return ((r >> 7) * kblocks + kb) * 512 + 16 * (m & 31) + 4 * (m >> 5);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     uint32_t r;

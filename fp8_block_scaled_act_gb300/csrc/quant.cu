@@ -362,7 +362,7 @@ template <bool kSR>
 __global__ void __launch_bounds__(kQ2Threads, 4) quant_128x128_kernel(
     const uint16_t* __restrict__ w, int64_t rows, int64_t cols, int64_t ldw,
     uint8_t* __restrict__ q, uint8_t* __restrict__ qT, float* __restrict__ scales, const ScaleRule rule,
-    const SrKey sr)
+    const SrKey sr, uint8_t* __restrict__ atoms_wT, uint8_t* __restrict__ atoms_w, unsigned int* status)
 {
     __shared__ uint32_t red[kQ2Threads / 32];
     __shared__ __align__(16) uint8_t tile[128 * kQ2Pitch];
@@ -400,6 +400,18 @@ __global__ void __launch_bounds__(kQ2Threads, 4) quant_128x128_kernel(
     for (int i = 0; i < kQ2Threads / 32; ++i) m = max(m, red[i]);
     const TileScale ts = tile_scale(__uint_as_float(m << 16), rule);
     if (threadIdx.x == 0) scales[b * nbr * nbc + bi * nbc + bj] = ts.s;
+    if (atoms_wT != nullptr && threadIdx.x < 64) {
+        // the block's exponent byte fills one whole atom of each operand:
+        // W^T (rows = the block's 128 columns, K-block bi) and W (rows =
+        // its 128 rows, K-block bj); 16 bytes per thread
+        const uint32_t E = ue8m0_of(ts.s);
+        if (E == 255u && threadIdx.x == 0) atomicCAS(status, 0u, static_cast<unsigned int>(FP8BS_ERR_DEVICE));
+        const uint32_t e4 = E * 0x01010101u;
+        const int64_t bo = b * nbr * nbc * 512;
+        uint8_t* atom = threadIdx.x < 32 ? atoms_wT + bo + (bj * nbr + bi) * 512
+                                         : atoms_w + bo + (bi * nbc + bj) * 512;
+        *reinterpret_cast<uint4*>(atom + 16 * (threadIdx.x & 31)) = make_uint4(e4, e4, e4, e4);
+    }
 
     uint8_t* qb = q + b * rows * cols;
 #pragma unroll
@@ -748,9 +760,19 @@ __global__ void __launch_bounds__(kQ3Threads, kSR ? 2 : (kStash ? 3 : 4)) requan
                         *reinterpret_cast<uint2*>(stage + rl * 128 + chunk * 8) = make_uint2(0u, 0u);
                         if (chunk == 0) row_scale[rl] = 0.0f;
                     }
+                    // padding rows of q's scale atoms hold scale 1
+                    if (chunk == 0 && p.q_atoms != nullptr)
+                        *reinterpret_cast<uint32_t*>(p.q_atoms + atom_offset(r0 + rl, c0 / 128, p.cols / 128)) =
+                            127u * 0x01010101u;
                     continue;
                 }
                 if (chunk == 0) p.q_scales[(c0 / 128) * p.q_scale_ld + r0 + rl] = ts.s;
+                if (chunk == 0 && p.q_atoms != nullptr) {
+                    const uint32_t E = ue8m0_of(ts.s);
+                    if (E == 255u) atomicCAS(p.status, 0u, static_cast<unsigned int>(FP8BS_ERR_DEVICE));
+                    *reinterpret_cast<uint32_t*>(p.q_atoms + atom_offset(r0 + rl, c0 / 128, p.cols / 128)) =
+                        E * 0x01010101u;
+                }
                 // the row's 8 values: from the registers in the stash mode;
                 // otherwise read back from this thread's own stage slot, so
                 // that the loaded registers are free after the maxima (four
@@ -846,6 +868,16 @@ __global__ void __launch_bounds__(kQ3Threads, kSR ? 2 : (kStash ? 3 : 4)) requan
         const float s = scale_from_amax(m, p.rule);
         col_scale[threadIdx.x] = tile_scale_from_s(s);
         if (threadIdx.x < nch) p.scT[(int64_t)tile * p.cols + c0 + threadIdx.x] = s;
+        if (p.qT_atoms != nullptr) {
+            // qT's row c0 + t, K-block = this token tile (channels past cols: scale 1)
+            uint32_t E = 127u;
+            if (threadIdx.x < nch) {
+                E = ue8m0_of(s);
+                if (E == 255u) atomicCAS(p.status, 0u, static_cast<unsigned int>(FP8BS_ERR_DEVICE));
+            }
+            *reinterpret_cast<uint32_t*>(p.qT_atoms + atom_offset(c0 + threadIdx.x, tile, p.mpad / 128)) =
+                E * 0x01010101u;
+        }
     }
     __syncthreads();
 
@@ -931,18 +963,19 @@ cudaError_t launch_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, in
 
 cudaError_t launch_quant_128x128(const uint16_t* w, int64_t batch, int64_t rows, int64_t cols,
                                  int64_t ldw, uint8_t* q, uint8_t* qT, float* scales,
-                                 const ScaleRule& rule, const SrParams* sr, cudaStream_t stream)
+                                 const ScaleRule& rule, const SrParams* sr, cudaStream_t stream,
+                                 uint8_t* atoms_wT, uint8_t* atoms_w, unsigned int* status)
 {
     const int64_t blocks = batch * ((rows + 127) / 128) * ((cols + 127) / 128);
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
     if (sr) {
         const SrKey key{sr->seed, sr->salt};
-        quant_128x128_kernel<true><<<(unsigned)blocks, kQ2Threads, 0, stream>>>(w, rows, cols, ldw, q, qT,
-                                                                               scales, rule, key);
+        quant_128x128_kernel<true><<<(unsigned)blocks, kQ2Threads, 0, stream>>>(
+            w, rows, cols, ldw, q, qT, scales, rule, key, atoms_wT, atoms_w, status);
     } else {
-        quant_128x128_kernel<false><<<(unsigned)blocks, kQ2Threads, 0, stream>>>(w, rows, cols, ldw, q, qT,
-                                                                                scales, rule, SrKey{0, 0});
+        quant_128x128_kernel<false><<<(unsigned)blocks, kQ2Threads, 0, stream>>>(
+            w, rows, cols, ldw, q, qT, scales, rule, SrKey{0, 0}, atoms_wT, atoms_w, status);
     }
     return cudaGetLastError();
 }

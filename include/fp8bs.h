@@ -480,6 +480,38 @@ FP8BS_API fp8bs_status fp8_pack_ue8m0(const float* scales, int64_t rows, int64_t
                                       int64_t row_stride, int64_t kb_stride, uint8_t* scale_atoms,
                                       void* stream);
 
+/* NEXT-4: the casts with their scales already packed. The same casts as   */
+/* fp8_quant_128x128_opts, fp8_quant_dual_opts and fp8_quant_dual_stash_opts */
+/* under the UE8M0 rule (opts->rule must be FP8BS_SCALE_UE8M0, else          */
+/* FP8BS_ERR_ARG), which in the same pass also write the exponent bytes of  */
+/* their scales into the MX scale atoms of the GEMM operands they feed,      */
+/* byte-identical to fp8_pack_ue8m0 of the fp32 scales they return (so the  */
+/* MX GEMMs can follow directly, with no packing launch in between).         */
+/*   fp8_quant_128x128_packed: W [rows x cols] per batch entry, rows and     */
+/*     cols multiples of 128 (else FP8BS_ERR_SHAPE); atoms_wT: the atoms of  */
+/*     W^T [cols x rows] (Fprop's B), atoms_w: those of W [rows x cols]      */
+/*     with the contraction along cols (Dgrad's B); each                     */
+/*     fp8bs_mx_scale_bytes(cols, rows) bytes per batch entry, entries       */
+/*     consecutive.                                                          */
+/*   fp8_quant_dual_packed / fp8_quant_dual_stash_packed: dense x only (no   */
+/*     groups), cols % 128 == 0; q_atoms: the atoms of q [rows x cols]       */
+/*     (fp8bs_mx_scale_bytes(rows, cols) bytes, padding rows 127); qT_atoms: */
+/*     those of qT [cols x Mpad] (fp8bs_mx_scale_bytes(cols, Mpad) bytes).   */
+/* Atom pointers 16-byte aligned. A scale without an exponent byte (below    */
+/* 2^-127, from a tile of tiny values) gets 255 and records FP8BS_ERR_DEVICE */
+/* in the device status word, as fp8_pack_ue8m0 does.                        */
+FP8BS_API fp8bs_status fp8_quant_128x128_packed(const void* w, int64_t batch, int64_t rows, int64_t cols,
+                                                int64_t ldw, uint8_t* q, uint8_t* qT, float* scales,
+                                                uint8_t* atoms_wT, uint8_t* atoms_w,
+                                                const fp8bs_scale_opts* opts, void* stream);
+FP8BS_API fp8bs_status fp8_quant_dual_packed(const void* x, int64_t rows, int64_t cols, uint8_t* q,
+                                             float* scales, uint8_t* qT, float* scalesT, uint8_t* q_atoms,
+                                             uint8_t* qT_atoms, const fp8bs_scale_opts* opts, void* stream);
+FP8BS_API fp8bs_status fp8_quant_dual_stash_packed(const void* x, int64_t rows, int64_t cols, uint8_t* q,
+                                                   float* scales, uint8_t* qT, float* scalesT, uint8_t* q_atoms,
+                                                   uint8_t* qT_atoms, const fp8bs_scale_opts* opts,
+                                                   void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* S7. Grouped (MoE expert) GEMMs                                             */
 /* The dense definitions above applied to each group (expert) g, whose token  */

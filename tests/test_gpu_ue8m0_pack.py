@@ -129,3 +129,70 @@ def test_ue8m0_gemms_through_the_mx_kernel(M, K, N):
     xta = np.abs(dec(h["xT"]) * np.repeat(h["sxT"].T, 128, axis=1))      # [K x Mpad]
     assert_gemm_close(np_(dw), oracle.wgrad(h["dyT"], h["sdyT"], h["xT"], h["sxT"]), dta @ xta.T, False,
                       f"ue8m0 wgrad {M}: {N}x{K}")
+
+
+@pytest.mark.parametrize("M,K,N,batch", [(200, 384, 256, 1), (513, 512, 384, 1), (128, 256, 128, 3)])
+def test_packed_casts_equal_cast_then_pack(M, K, N, batch):
+    """The casts that write their scale atoms in the same pass give the same
+    codes and scales as the UE8M0 casts, and the same atoms as
+    fp8_pack_ue8m0 of those scales (and as the oracle's packing)."""
+    x = wl.with_outliers((M, K), fraction=0.01, seed=M)
+    dy = wl.normal((M, N), std=wl.DY_STD, seed=M + 1)
+    w = wl.normal((batch, K, N) if batch > 1 else (K, N), std=wl.W_STD, seed=M + 2).cuda()
+    Mp = fp8bs.fp8bs_padded_tokens(M)
+    # weights
+    wq, wqT, sw = fp8bs.empty_quant_128x128(K, N, batch=batch)
+    fp8bs.fp8_quant_128x128_opts(w, wq, wqT, sw, UE8M0)
+    pq, pqT, psw = fp8bs.empty_quant_128x128(K, N, batch=batch)
+    aT, aW = fp8bs.empty_mx_atoms(N, K, batch), fp8bs.empty_mx_atoms(K, N, batch)
+    fp8bs.fp8_quant_128x128_packed(w, pq, pqT, psw, aT, aW)
+    torch.cuda.synchronize()
+    assert fp8bs.fp8bs_device_status(reset=True) == 0
+    assert torch.equal(wq, pq) and torch.equal(wqT, pqT) and torch.equal(sw, psw)
+    nb = fp8bs.fp8bs_mx_scale_bytes(N, K)
+    for b in range(batch):
+        swb = sw.view(batch, -1)[b].contiguous()
+        assert torch.equal(aT[b * nb:(b + 1) * nb], _pack(swb, N, K, 128, 1, N // 128)), b
+        assert torch.equal(aW[b * nb:(b + 1) * nb], _pack(swb, K, N, 128, N // 128, 1)), b
+        ref, bad = oracle.pack_ue8m0(np_(swb), N, K, 128, 1, N // 128)
+        assert bad == 0 and np.array_equal(atoms_to_rows(np_(aT[b * nb:(b + 1) * nb]), N, K), ref)
+    # activations (stash) and gradients (dual)
+    for name, src, C in (("stash", x, K), ("dual", dy, N)):
+        q, s = fp8bs.empty_quant_1x128(M, C)
+        qT, sT = fp8bs.empty_requant_128x1_T(M, C)
+        (fp8bs.fp8_quant_dual_stash_opts if name == "stash" else fp8bs.fp8_quant_dual_opts)(
+            src.cuda(), q, s, qT, sT, UE8M0)
+        pq, ps = fp8bs.empty_quant_1x128(M, C)
+        pqT, psT = fp8bs.empty_requant_128x1_T(M, C)
+        aq, aqT = fp8bs.empty_mx_atoms(M, C), fp8bs.empty_mx_atoms(C, Mp)
+        (fp8bs.fp8_quant_dual_stash_packed if name == "stash" else fp8bs.fp8_quant_dual_packed)(
+            src.cuda(), pq, ps, pqT, psT, aq, aqT)
+        torch.cuda.synchronize()
+        assert fp8bs.fp8bs_device_status(reset=True) == 0, name
+        # (the scale array's columns past row M are padding that no cast writes)
+        for a, b in ((q, pq), (s[:, :M], ps[:, :M]), (qT, pqT), (sT, psT)):
+            assert torch.equal(a, b), name
+        assert torch.equal(aq, _pack(s, M, C, 1, 1, s.shape[1])), name
+        assert torch.equal(aqT, _pack(sT, C, Mp, 1, 1, C)), name
+        ref, bad = oracle.pack_ue8m0(np_(s), M, C, 1, 1, s.shape[1])
+        assert bad == 0 and np.array_equal(atoms_to_rows(np_(aq), M, C), ref), name
+        assert np.all(atoms_to_rows(np_(aq), (M + 127) // 128 * 128, C)[M:] == 127), name
+
+
+def test_packed_cast_flags_a_scale_without_a_byte():
+    """A row tile of tiny values has a UE8M0 scale below 2^-127: the fused
+    cast writes byte 255 for it and records FP8BS_ERR_DEVICE, as the
+    separate packing does."""
+    M, C = 128, 256
+    x = wl.normal((M, C), std=1.0, seed=9)
+    x[5, 128:] = 1.0e-38                       # BF16 subnormal; amax / 448 far below 2^-127
+    q, s = fp8bs.empty_quant_1x128(M, C)
+    qT, sT = fp8bs.empty_requant_128x1_T(M, C)
+    aq, aqT = fp8bs.empty_mx_atoms(M, C), fp8bs.empty_mx_atoms(C, M)
+    fp8bs.fp8_quant_dual_packed(x.cuda(), q, s, qT, sT, aq, aqT)
+    torch.cuda.synchronize()
+    assert fp8bs.fp8bs_device_status(reset=True) == FP8BS_ERR_DEVICE
+    got = atoms_to_rows(np_(aq), M, C)
+    ref, bad = oracle.pack_ue8m0(np_(s), M, C, 1, 1, s.shape[1])
+    assert bad == 1 and np.array_equal(got, ref)
+    assert (got[5, 4:] == 255).all() and (got[5, :4] != 255).all()
