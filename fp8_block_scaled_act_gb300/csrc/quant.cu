@@ -353,7 +353,9 @@ __global__ void __launch_bounds__(kQ1Threads) quant_1x128_kernel(
 // 8-column chunk t % 16 of rows t / 16 + 16 i (i < 8), so each row's 256
 // bytes come from 16 consecutive threads. Block absmax via warp shuffles and
 // shared memory. The optional transposed payload goes through a padded
-// shared-memory tile and leaves as 16-byte row segments of qT.
+// shared-memory tile and leaves as 16-byte row segments of qT. With atoms
+// (power-of-two scales), the block's exponent byte also fills one 512-byte
+// scale atom of each of the two GEMM operands the weight feeds.
 // ---------------------------------------------------------------------------
 constexpr int kQ2Threads = 256;
 constexpr int kQ2Pitch = 132;  // bytes per row of the staging tile (bank-conflict padding)
@@ -669,6 +671,9 @@ __device__ __forceinline__ int find_group(const int32_t* tile_start, int ng, int
 // (decoded with its row scale, as the E4M3 source mode does) instead of
 // from the BF16 values; the 1x128 codes are staged in place of the source.
 // kSR: stochastic rounding of both passes (keys in p).
+// p.q_atoms / p.qT_atoms (dense, power-of-two scales): each row scale's and
+// each column scale's exponent byte also goes to the scale atoms of q and
+// qT; a CTA's rows and channels fill exactly one atom of each.
 template <bool kDual, bool kStash, bool kSR>
 __global__ void __launch_bounds__(kQ3Threads, kSR ? 2 : (kStash ? 3 : 4)) requant_128x1_T_kernel(const __grid_constant__ RequantParams p)
 {
