@@ -671,9 +671,10 @@ __device__ __forceinline__ int find_group(const int32_t* tile_start, int ng, int
 // (decoded with its row scale, as the E4M3 source mode does) instead of
 // from the BF16 values; the 1x128 codes are staged in place of the source.
 // kSR: stochastic rounding of both passes (keys in p).
-// p.q_atoms / p.qT_atoms (dense, power-of-two scales): each row scale's and
-// each column scale's exponent byte also goes to the scale atoms of q and
-// qT; a CTA's rows and channels fill exactly one atom of each.
+// p.q_atoms / p.qT_atoms (dense, power-of-two scales): the exponent bytes of
+// the row and column scales also go to the scale atoms of q and qT; a CTA's
+// rows and channels fill exactly one atom of each, written after the
+// scales are in shared memory.
 template <bool kDual, bool kStash, bool kSR>
 __global__ void __launch_bounds__(kQ3Threads, kSR ? 2 : (kStash ? 3 : 4)) requant_128x1_T_kernel(const __grid_constant__ RequantParams p)
 {
@@ -765,19 +766,13 @@ __global__ void __launch_bounds__(kQ3Threads, kSR ? 2 : (kStash ? 3 : 4)) requan
                         *reinterpret_cast<uint2*>(stage + rl * 128 + chunk * 8) = make_uint2(0u, 0u);
                         if (chunk == 0) row_scale[rl] = 0.0f;
                     }
-                    // padding rows of q's scale atoms hold scale 1
-                    if (chunk == 0 && p.q_atoms != nullptr)
-                        *reinterpret_cast<uint32_t*>(p.q_atoms + atom_offset(r0 + rl, c0 / 128, p.cols / 128)) =
-                            127u * 0x01010101u;
                     continue;
                 }
                 if (chunk == 0) p.q_scales[(c0 / 128) * p.q_scale_ld + r0 + rl] = ts.s;
-                if (chunk == 0 && p.q_atoms != nullptr) {
-                    const uint32_t E = ue8m0_of(ts.s);
-                    if (E == 255u) atomicCAS(p.status, 0u, static_cast<unsigned int>(FP8BS_ERR_DEVICE));
-                    *reinterpret_cast<uint32_t*>(p.q_atoms + atom_offset(r0 + rl, c0 / 128, p.cols / 128)) =
-                        E * 0x01010101u;
-                }
+                // the row scales go to shared memory for the atom writer below
+                // (the stash mode stages them there anyway)
+                if constexpr (!kStash)
+                    if (chunk == 0 && p.q_atoms != nullptr) row_scale[rl] = ts.s;
                 // the row's 8 values: from the registers in the stash mode;
                 // otherwise read back from this thread's own stage slot, so
                 // that the loaded registers are free after the maxima (four
@@ -873,18 +868,35 @@ __global__ void __launch_bounds__(kQ3Threads, kSR ? 2 : (kStash ? 3 : 4)) requan
         const float s = scale_from_amax(m, p.rule);
         col_scale[threadIdx.x] = tile_scale_from_s(s);
         if (threadIdx.x < nch) p.scT[(int64_t)tile * p.cols + c0 + threadIdx.x] = s;
-        if (p.qT_atoms != nullptr) {
-            // qT's row c0 + t, K-block = this token tile (channels past cols: scale 1)
-            uint32_t E = 127u;
-            if (threadIdx.x < nch) {
-                E = ue8m0_of(s);
-                if (E == 255u) atomicCAS(p.status, 0u, static_cast<unsigned int>(FP8BS_ERR_DEVICE));
-            }
-            *reinterpret_cast<uint32_t*>(p.qT_atoms + atom_offset(c0 + threadIdx.x, tile, p.mpad / 128)) =
-                E * 0x01010101u;
-        }
     }
     __syncthreads();
+
+    // Exponent-byte atoms (dense, power-of-two scales): the CTA's 128 rows
+    // fill one 512-byte atom of q (K-block c0 / 128) and its 128 channels one
+    // atom of qT (K-block = this token tile). Lane t of the first warp writes
+    // rows t, t + 32, t + 64, t + 96 of q's atom as one 16-byte word, lane t
+    // of the second warp the same channels of qT's; padding rows and
+    // channels past cols hold scale 1.
+    if (threadIdx.x < 64 && (threadIdx.x < 32 ? p.q_atoms : p.qT_atoms) != nullptr) {
+        const int t = threadIdx.x & 31;
+        const bool rows_side = threadIdx.x < 32;
+        uint32_t wv[4];
+        bool bad = false;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int i = t + 32 * k;
+            uint32_t E = 127u;
+            if (rows_side ? i < len : i < nch) {
+                E = ue8m0_of(rows_side ? row_scale[i] : col_scale[i].s);
+                bad |= E == 255u;
+            }
+            wv[k] = E * 0x01010101u;
+        }
+        if (bad) atomicCAS(p.status, 0u, static_cast<unsigned int>(FP8BS_ERR_DEVICE));
+        uint8_t* atom = rows_side ? p.q_atoms + ((r0 / 128) * (p.cols / 128) + c0 / 128) * 512
+                                  : p.qT_atoms + ((c0 / 128) * (p.mpad / 128) + tile) * 512;
+        *reinterpret_cast<uint4*>(atom + 16 * t) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    }
 
     if (p.mode == FP8BS_SRC_BF16 && !kStash) {
         // unit = (channel pair 2jp, 2jp + 1; 32-token part): 64 x 4 = 256 units
