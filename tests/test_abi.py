@@ -133,3 +133,38 @@ def test_splitk_workspace_arithmetic_and_argument_errors():
     assert L.fp8_block_gemm_splitk(7, null, null, null, null, 128, 128, 128, 2, null, null, 0, null) == 1
     assert L.fp8_block_gemm_splitk(0, null, null, null, null, 128, 128, 128, 0, null, null, 0, null) == 1
     assert L.fp8_block_gemm_splitk(0, null, null, null, null, 128, 100, 128, 2, null, null, 0, null) == 3
+
+
+def test_ue8m0_packing_argument_validation(L):
+    """NEXT-4 entries reject bad arguments on the host: the packing's row
+    block, shapes, pointers and alignment; the packed casts' rule (UE8M0
+    only), shapes and atom pointers."""
+    buf = ctypes.create_string_buffer(1 << 12)
+    a16 = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
+    mis16 = ctypes.c_void_p(a16.value + 4)
+    mis4 = ctypes.c_void_p(a16.value + 2)
+    ERR_ARG, ERR_ALIGN, ERR_SHAPE = 1, 2, 3
+    # fp8_pack_ue8m0(scales, rows, K, row_block, row_stride, kb_stride, atoms, stream)
+    assert L.fp8_pack_ue8m0(a16, 128, 256, 64, 1, 4, a16, None) == ERR_ARG      # row block 1 or 128
+    assert L.fp8_pack_ue8m0(a16, 128, 200, 1, 1, 4, a16, None) == ERR_SHAPE    # K % 128
+    assert L.fp8_pack_ue8m0(a16, -1, 256, 1, 1, 4, a16, None) == ERR_ARG
+    assert L.fp8_pack_ue8m0(a16, 128, 256, 1, -1, 4, a16, None) == ERR_ARG
+    assert L.fp8_pack_ue8m0(None, 128, 256, 1, 1, 4, a16, None) == ERR_ARG
+    assert L.fp8_pack_ue8m0(a16, 128, 256, 1, 1, 4, mis16, None) == ERR_ALIGN
+    assert L.fp8_pack_ue8m0(mis4, 128, 256, 1, 1, 4, a16, None) == ERR_ALIGN
+    assert L.fp8_pack_ue8m0(a16, 0, 256, 1, 1, 4, None, None) == 0             # empty: no work
+    ue = ctypes.pointer(fp8bs.ScaleOpts(fp8bs.SCALE_UE8M0, 0.0, 0.0))
+    f32 = ctypes.pointer(fp8bs.ScaleOpts(fp8bs.SCALE_FP32, 0.0, 0.0))
+    # fp8_quant_128x128_packed(w, batch, rows, cols, ldw, q, qT, scales, atoms_wT, atoms_w, opts, stream)
+    q2 = L.fp8_quant_128x128_packed
+    assert q2(a16, 1, 128, 128, 128, a16, a16, a16, a16, a16, None, None) == ERR_ARG   # rule required
+    assert q2(a16, 1, 128, 128, 128, a16, a16, a16, a16, a16, f32, None) == ERR_ARG
+    assert q2(a16, 1, 96, 128, 128, a16, a16, a16, a16, a16, ue, None) == ERR_SHAPE     # rows % 128
+    assert q2(a16, 1, 128, 128, 128, a16, a16, a16, None, a16, ue, None) == ERR_ARG
+    assert q2(a16, 1, 128, 128, 128, a16, a16, a16, a16, mis16, ue, None) == ERR_ALIGN
+    # fp8_quant_dual_packed / _stash_packed(x, rows, cols, q, s, qT, sT, q_atoms, qT_atoms, opts, stream)
+    for f in (L.fp8_quant_dual_packed, L.fp8_quant_dual_stash_packed):
+        assert f(a16, 4, 128, a16, a16, a16, a16, a16, a16, None, None) == ERR_ARG
+        assert f(a16, 4, 96, a16, a16, a16, a16, a16, a16, ue, None) == ERR_SHAPE      # cols % 128
+        assert f(a16, 4, 128, a16, a16, a16, a16, None, a16, ue, None) == ERR_ARG
+        assert f(a16, 4, 128, a16, a16, a16, a16, a16, mis16, ue, None) == ERR_ALIGN
