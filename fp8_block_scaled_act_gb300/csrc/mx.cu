@@ -608,17 +608,14 @@ __global__ void __launch_bounds__(256) pack_ue8m0_kernel(const float* __restrict
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         // i = (row tile, K-block, row within the tile): consecutive threads
         // fill consecutive rows of one atom
-        const int64_t m = i & 127;
         const int64_t kb = (i >> 7) % kblocks;
-        const int64_t rt = (i >> 7) / kblocks;
-        const int64_t r = rt * 128 + m;
+        const int64_t r = ((i >> 7) / kblocks) * 128 + (i & 127);
         uint32_t E = 127u;   // padding rows: scale 1
         if (r < rows) {
             E = ue8m0_of(__ldg(scales + (r / row_block) * row_stride + kb * kb_stride));
             if (E == 255u) atomicCAS(status, 0u, static_cast<unsigned int>(FP8BS_ERR_DEVICE));
         }
-        *reinterpret_cast<uint32_t*>(atoms + (rt * kblocks + kb) * 512 + 16 * (m & 31) + 4 * (m >> 5)) =
-            E * 0x01010101u;
+        *reinterpret_cast<uint32_t*>(atoms + atom_offset(r, kb, kblocks)) = E * 0x01010101u;
     }
 }
 

@@ -146,11 +146,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v)
                  : "memory");
 }
 
-__device__ __forceinline__ void st_shared_v2f(uint32_t addr, float2 v)
-{
-    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y) : "memory");
-}
-
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
 {
     uint4 v;
@@ -170,38 +165,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                      smem_addr(dst)),
                  "l"(src), "r"(bytes), "r"(smem_addr(bar))
                  : "memory");
-}
-
-// ---------------------------------------------------------------------------
-// cp.async (global -> shared, asynchronous, no registers held)
-// ---------------------------------------------------------------------------
-
-// Copies `src_bytes` (0 or 4) bytes and zero-fills the rest of the 4 bytes.
-__device__ __forceinline__ void cp_async_4(void* dst, const void* src, uint32_t src_bytes)
-{
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_addr(dst)), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-
-// Copies `src_bytes` (0 or 16) bytes and zero-fills the rest of the 16 bytes.
-__device__ __forceinline__ void cp_async_16(void* dst, const void* src, uint32_t src_bytes)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit()
-{
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-
-// Waits until at most kPending of this thread's most recent groups are pending.
-template <int kPending>
-__device__ __forceinline__ void cp_async_wait()
-{
-    asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -278,9 +241,6 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32])
         : "memory");
 }
 
-// Waits for this thread's outstanding TMEM loads. The registers written by
-// those loads are tied to the wait as in/out operands so that the compiler
-// cannot move their uses above it.
 // Two 16-lane x 32-column loads (shape 16x256b, four repetitions): the
 // lower 16 lanes of the warp's quarter at taddr into r[0..15], the upper 16
 // at taddr + (16 << 16) into r[16..31]. In each 8-column repetition j,
@@ -307,6 +267,9 @@ __device__ __forceinline__ void tmem_ld_16x256b_x4_pair(uint32_t taddr, uint32_t
         : "memory");
 }
 
+// Waits for this thread's outstanding TMEM loads. The registers written by
+// those loads are tied to the wait as in/out operands so that the compiler
+// cannot move their uses above it.
 __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32])
 {
     asm volatile(
