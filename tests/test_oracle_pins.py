@@ -880,3 +880,41 @@ def test_pack_ue8m0_mx_gemm_is_the_promoted_gemm():
     absprod = a @ bt.T
     assert np.all(np.abs(y_mx - y_pr) <= 2.0 ** -20 * absprod + 1e-30)
     assert np.count_nonzero(y_pr) > 0.99 * y_pr.size
+
+
+def test_pack_ue8m0_mx_gemm_is_the_promoted_dgrad_and_wgrad():
+    """The same agreement for Dgrad (A = dY rows, B = W with the contraction
+    along N) and Wgrad (A = dY^T, B = X^T from the transposed casts): the
+    oracle's MX GEMM over the packed operands matches its promoted GEMM to
+    fp32 summation-order accuracy, so the stride and row-block choices of
+    the packing are the ones each operand needs."""
+    rng = np.random.default_rng(11)
+    M, K, N = 256, 384, 256
+    x = oracle.f32_to_bf16((rng.standard_normal((M, K)) * np.exp(rng.standard_normal((M, 1)))).astype(np.float32))
+    w = oracle.f32_to_bf16((rng.standard_normal((K, N)) * 0.02).astype(np.float32))
+    dy = oracle.f32_to_bf16((rng.standard_normal((M, N)) * 1e-3).astype(np.float32))
+    with oracle.scale_rule(ue8m0=True):
+        xq, sx = oracle.quant_1x128(x)
+        wq, sw = oracle.quant_128x128(w)
+        dyq, sdy = oracle.quant_1x128(dy)
+        xT, sxT = oracle.requant_128x1_T(xq, sx)
+        dyT, sdyT = oracle.requant_128x1_T(dy)
+    Mp = xT.shape[1]
+    # Dgrad: dX [M x K] = dY W^T
+    ba, _ = oracle.pack_ue8m0(sdy, M, N, 1, 1, sdy.shape[1])
+    bb, _ = oracle.pack_ue8m0(sw, K, N, 128, N // 128, 1)
+    got = oracle.mx_gemm(dyq, ba, wq, bb).astype(np.float64)
+    ref = oracle.dgrad(dyq, sdy, wq, sw).astype(np.float64)
+    absprod = np.abs(_mx_dequant(dyq, ba)) @ np.abs(_mx_dequant(wq, bb)).T
+    assert np.all(np.abs(got - ref) <= 2.0 ** -20 * absprod + 1e-30)
+    # Wgrad: dW [N x K] = dY^T X over the padded tokens
+    ba, _ = oracle.pack_ue8m0(sdyT, N, Mp, 1, 1, N)
+    bb, _ = oracle.pack_ue8m0(sxT, K, Mp, 1, 1, K)
+    got = oracle.mx_gemm(dyT, ba, xT, bb).astype(np.float64)
+    ref = oracle.wgrad(dyT, sdyT, xT, sxT).astype(np.float64)
+    absprod = np.abs(_mx_dequant(dyT, ba)) @ np.abs(_mx_dequant(xT, bb)).T
+    assert np.all(np.abs(got - ref) <= 2.0 ** -20 * absprod + 1e-30)
+    # the transposed operand's per-row scales packed as if they were 128-row
+    # block scales (a plausible mix-up of the layouts) is not the same GEMM
+    bad, _ = oracle.pack_ue8m0(sxT, K, Mp, 128, 1, K)
+    assert not np.allclose(oracle.mx_gemm(dyT, ba, xT, bad), ref, rtol=1e-3, atol=0)
