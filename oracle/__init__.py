@@ -43,6 +43,8 @@ FAULT_UE8M0_DOWN = 9
 FAULT_FLOOR_AFTER = 10
 FAULT_SR_WORD = 11
 FAULT_SR_NEAREST = 12
+FAULT_SR_BLOCK_INDEX = 13
+FAULT_REQUANT_TILE_SCALE = 14
 
 
 def build(force: bool = False) -> str:

@@ -73,7 +73,10 @@ enum {
     FAULT_UE8M0_DOWN = 9,        /* UE8M0 scale rounded down, not up */
     FAULT_FLOOR_AFTER = 10,      /* amax floor applied to s instead of amax */
     FAULT_SR_WORD = 11,          /* SR takes the next Philox output word */
-    FAULT_SR_NEAREST = 12        /* SR rounds to nearest instead */
+    FAULT_SR_NEAREST = 12,       /* SR rounds to nearest instead */
+    FAULT_SR_BLOCK_INDEX = 13,   /* 128x128 SR numbers elements inside each block, not in the tensor */
+    FAULT_REQUANT_TILE_SCALE = 14  /* E4M3-source requant decodes every token of a tile with
+                                      the source scale of the tile's first token */
 };
 static int g_fault = FAULT_NONE;
 
@@ -355,9 +358,11 @@ void oracle_quant_128x128_sr(const uint16_t* x, i64 rows, i64 cols, i64 ldx,
                 v[i * nc + j] = bf16_to_f32(x[(r0 + i) * ldx + c0 + j]);
         float s = tile_scale(v, nr * nc);
         sc[bi * ldsc + bj] = s;
-        for (int i = 0; i < nr; ++i)
-            tile_encode_sr(v + i * nc, nc, s, q + (r0 + i) * ldq + c0, 1, seed, salt,
-                           idx_base + (r0 + i) * cols + c0, 1);
+        for (int i = 0; i < nr; ++i) {
+            i64 idx0 = idx_base + (r0 + i) * cols + c0;
+            if (g_fault == FAULT_SR_BLOCK_INDEX) idx0 = idx_base + blk * 128 * 128 + (i64)i * nc;
+            tile_encode_sr(v + i * nc, nc, s, q + (r0 + i) * ldq + c0, 1, seed, salt, idx0, 1);
+        }
     }
 }
 
@@ -528,7 +533,8 @@ static void requant_impl(int mode, const void* src, i64 ld_src,
                         v[i] = bf16_to_f32(((const uint16_t*)src)[r * ld_src + c]);
                     } else {
                         uint8_t code = ((const uint8_t*)src)[r * ld_src + c];
-                        float s1 = src_sc[r * src_rs + (c / 128) * src_ts];
+                        i64 rs = (g_fault == FAULT_REQUANT_TILE_SCALE) ? r0 : r;
+                        float s1 = src_sc[rs * src_rs + (c / 128) * src_ts];
                         v[i] = g_dec[code] * s1;
                     }
                 }

@@ -449,6 +449,107 @@ def test_requant_sr_is_unbiased():
         assert abs(abs(mean[j]) - abs(xv)) <= 5 * se + (hi - lo) * 2.0 ** -20 + 1e-12, (j, xv, mean[j])
 
 
+def _philox_word(seed, salt, idx):
+    """The random word of element idx, restated from the Philox4x32-10 block
+    function that the published known-answer vectors pin: counter (idx / 4
+    low, idx / 4 high, salt, 0), key (seed low, seed high), output word
+    idx % 4."""
+    c = idx // 4
+    out = oracle.philox4x32_10([c & 0xFFFFFFFF, c >> 32, salt & 0xFFFFFFFF, 0],
+                               [seed & 0xFFFFFFFF, seed >> 32])
+    return int(out[idx % 4])
+
+
+def _sr128_input():
+    """Rows of widely different magnitude (so the three column blocks and the
+    two row blocks get different scales); 128 + 16 rows leave a ragged row
+    block."""
+    rng = np.random.default_rng(31)
+    R, C = 128 + 16, 384
+    x = (rng.standard_normal((R, C)) * np.exp(rng.uniform(-3.0, 3.0, (R, 1)))).astype(np.float32)
+    return oracle.f32_to_bf16(x)
+
+
+def test_quant_128x128_sr_word_per_tensor_element():
+    """128x128 cast with stochastic rounding (prime-rl PR #4073, "SR agreement"
+    row; reading: element (r, c) of matrix b of a batch of R x C matrices takes
+    the word of index b R C + r C + c). Every code is the pinned SR encoder
+    applied to the fp32 quotient v / s, s being the round-to-nearest cast's
+    block scale, with the word restated from the pinned Philox function; a
+    block-local or a transposed element numbering disagrees."""
+    xb = _sr128_input()
+    v = oracle.bf16_to_f32(xb)
+    R, C = v.shape
+    seed, salt = 0x123456789ABC, 7
+    _, s_rn = oracle.quant_128x128(xb)
+    s_el = np.repeat(np.repeat(s_rn, 128, 0), 128, 1)[:R, :C]
+    quot = (v / s_el).astype(np.float32)              # IEEE fp32 division, round to nearest
+    for b in range(2):
+        base = b * R * C
+        q, s = oracle.quant_128x128_sr(xb, seed=seed, salt=salt, idx_base=base)
+        assert np.array_equal(s.view(np.uint32), s_rn.view(np.uint32))
+        want = np.array([[oracle.e4m3_encode_sr(float(quot[r, c]), _philox_word(seed, salt, base + r * C + c))
+                          for c in range(C)] for r in range(R)], np.uint8)
+        assert np.array_equal(q, want)
+    # the numbering matters: block-local and transposed indices give other codes
+    rows = range(4)
+    block_local = np.array([[oracle.e4m3_encode_sr(
+        float(quot[r, c]), _philox_word(seed, salt, (c // 128) * 128 * 128 + r * 128 + c % 128))
+        for c in range(C)] for r in rows], np.uint8)
+    transposed = np.array([[oracle.e4m3_encode_sr(float(quot[r, c]), _philox_word(seed, salt, c * R + r))
+                            for c in range(C)] for r in rows], np.uint8)
+    q0, _ = oracle.quant_128x128_sr(xb, seed=seed, salt=salt)
+    assert not np.array_equal(q0[:4], block_local)
+    assert not np.array_equal(q0[:4], transposed)
+
+
+def _mode_q_input():
+    """An E4M3 stash [300 x 256] with random finite codes (a row of -0 codes
+    and a zero tile included) and 1x128 scales that differ for every row and
+    column tile."""
+    rng = np.random.default_rng(32)
+    M, C = 300, 256
+    t = oracle.e4m3_table()
+    fin = np.nonzero(~np.isnan(t))[0]
+    q = rng.choice(fin, size=(M, C)).astype(np.uint8)
+    q[5, :] = 0x80
+    q[256:, 128:] = 0x00
+    sc = (np.exp2(rng.integers(-12, 4, (C // 128, M))) * rng.uniform(1.0, 2.0, (C // 128, M))).astype(np.float32)
+    ld = oracle.scale_rows_padded(M)
+    sc_tm = np.zeros((C // 128, ld), np.float32)
+    sc_tm[:, :M] = sc
+    return q, sc_tm
+
+
+def test_requant_mode_q_varying_scales_matches_torch_steps():
+    """E4M3-source 128x1 requant ("scratch: the backward pass, unrolled",
+    "What is asserted, and from where", bullet 2: the Wgrad operands are
+    re-tiled 128x1 from the saved tensors). Reading: each saved code is
+    decoded as fp32(dec(q) * s) with the 1x128 scale of its own row and
+    column tile, then quantized along tokens. Restated here with torch's own
+    E4M3 decoding, a numpy fp32 multiply and the torch-steps quantizer on the
+    transposed operand, with scales that differ for every row and tile;
+    dense and grouped (an empty group and a group of one tile + 1 token)."""
+    q, sc = _mode_q_input()
+    M, C = q.shape
+    dec = torch.from_numpy(q).view(torch.float8_e4m3fn).float().numpy()
+    s_el = np.repeat(sc[:, :M].T, 128, axis=1)
+    deq = (dec * s_el).astype(np.float32)             # one fp32 multiply per element
+    for offsets in (None, [0, 129, 129, 300]):
+        qT, scT = oracle.requant_128x1_T(q, sc, offsets=offsets)
+        segs = [(0, M)] if offsets is None else list(zip(offsets[:-1], offsets[1:]))
+        p = 0
+        for a, b in segs:
+            for t0 in range(a, b, 128):
+                n = min(t0 + 128, b) - t0
+                qr, sr = _torch_quant_rows(np.ascontiguousarray(deq[t0:t0 + n, :].T))
+                assert np.array_equal(qT[:, p:p + n], qr)
+                assert np.all(qT[:, p + n:p + 128] == 0)
+                assert np.array_equal(scT[p // 128].view(np.uint32), sr.view(np.uint32))
+                p += 128
+        assert p == qT.shape[1]
+
+
 def test_mx_quant_scales_and_codes():
     """MXFP8 (OCP MX v1.0 blocks of 32 with 8-bit exponent scales): each
     scale 2^(E-127) is the smallest power of two that keeps the block's
@@ -763,6 +864,22 @@ def _pin_sr():
         return False
 
 
+def _pin_sr128():
+    try:
+        test_quant_128x128_sr_word_per_tensor_element()
+        return True
+    except AssertionError:
+        return False
+
+
+def _pin_requant_q():
+    try:
+        test_requant_mode_q_varying_scales_matches_torch_steps()
+        return True
+    except AssertionError:
+        return False
+
+
 def _pin_gemm():
     return (_check_fprop(130, 384, 256, 21) and _check_dgrad(129, 384, 256, 22)
             and _check_wgrad(300, 256, 128, 23) and _check_fprop(64, 256, 256, 24))
@@ -781,10 +898,13 @@ def _pin_gemm():
     (oracle.FAULT_FLOOR_AFTER, "scale_rules"),
     (oracle.FAULT_SR_WORD, "sr"),
     (oracle.FAULT_SR_NEAREST, "sr"),
+    (oracle.FAULT_SR_BLOCK_INDEX, "sr128"),
+    (oracle.FAULT_REQUANT_TILE_SCALE, "requant_q"),
 ])
 def test_planted_mistake_is_caught(fault, pin):
     check = {"encoder": _pin_encoder, "quant": _pin_quant, "gemm": _pin_gemm,
-             "scale_rules": _pin_scale_rules, "sr": _pin_sr}[pin]
+             "scale_rules": _pin_scale_rules, "sr": _pin_sr, "sr128": _pin_sr128,
+             "requant_q": _pin_requant_q}[pin]
     assert check()
     oracle.set_fault(fault)
     try:
