@@ -27,7 +27,8 @@ __all__ = [
     "fp8_block_gemm_fprop", "fp8_block_gemm_dgrad", "fp8_block_gemm_wgrad",
     "fp8_block_gemm_grouped", "fp8_block_gemm_splitk", "fp8bs_splitk_workspace_size",
     "fp8bs_splitk_default_splits", "fp8_block_gemm_splitk_noalloc", "NOALLOC_SCRATCH_BYTES",
-    "fp8bs_device_status", "fp8bs_set_wait_limit_ns",
+    "fp8bs_device_status", "fp8bs_last_device_status", "fp8bs_copy_device_status", "fp8bs_set_wait_limit_ns",
+    "fp8bs_padded_tokens_max", "fp8_requant_128x1_T_dev", "fp8_quant_dual_dev", "fp8_quant_dual_stash_dev",
     "fp8bs_selftest_wait_timeout", "fp8bs_scale_ld", "fp8bs_padded_tokens",
     "fp8bs_status_str", "fp8bs_version",
     "empty_quant_1x128", "empty_quant_128x128", "empty_requant_128x1_T",
@@ -58,9 +59,10 @@ class ScaleOpts(ctypes.Structure):
 
 
 class Fp8bsError(RuntimeError):
-    def __init__(self, fn: str, code: int):
+    def __init__(self, fn: str, code: int, detail: str = ""):
         self.code = int(code)
-        super().__init__(f"{fn}: {STATUS_NAMES.get(self.code, self.code)}")
+        msg = f"{fn}: {STATUS_NAMES.get(self.code, self.code)}"
+        super().__init__(msg + (f" ({detail})" if detail else ""))
 
 
 def lib_path() -> str:
@@ -116,7 +118,13 @@ def lib() -> ctypes.CDLL:
         "fp8_block_gemm_fprop": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_block_gemm_dgrad": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_block_gemm_wgrad": ([P, P, P, P, I64, I64, I64, P, I, P], S),
-        "fp8_block_gemm_grouped": ([I, I32, P, P, P, P, P, I64, I64, P, I, P], S),
+        "fp8_block_gemm_grouped": ([I, I32, P, P, I64, P, P, P, P, I64, I64, P, I, P], S),
+        "fp8bs_padded_tokens_max": ([I64, I32], I64),
+        "fp8_requant_128x1_T_dev": ([I, P, P, I64, I64, P, I32, P, P, P, P], S),
+        "fp8_quant_dual_dev": ([P, I64, I64, P, I32, P, P, P, P, P, P], S),
+        "fp8_quant_dual_stash_dev": ([P, I64, I64, P, I32, P, P, P, P, P, P], S),
+        "fp8bs_last_device_status": ([P, I], S),
+        "fp8bs_copy_device_status": ([P, I, P], S),
         "fp8bs_splitk_workspace_size": ([I, I64, I64, I64, I32], ctypes.c_size_t),
         "fp8bs_splitk_default_splits": ([I, I64, I64, I64], I32),
         "fp8_block_gemm_splitk": ([I, P, P, P, P, I64, I64, I64, I32, P, P, ctypes.c_size_t, P], S),
@@ -156,9 +164,9 @@ def _opts(rule: int, amax_floor: float, scale_floor: float):
     return ctypes.pointer(ScaleOpts(int(rule), float(amax_floor), float(scale_floor)))
 
 
-def _check(name: str, code: int) -> None:
+def _check(name: str, code: int, detail: str = "") -> None:
     if code != 0:
-        raise Fp8bsError(name, code)
+        raise Fp8bsError(name, code, detail)
 
 
 def _need(t: torch.Tensor, dtype, name: str):
@@ -170,6 +178,19 @@ def _need(t: torch.Tensor, dtype, name: str):
         raise ValueError(f"{name} must be a CUDA tensor")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def _on_device(offsets) -> bool:
+    """Group offsets given as a CUDA tensor are read by the kernels on the
+    device (the _dev entry points); anything else is a host array."""
+    return isinstance(offsets, torch.Tensor) and offsets.is_cuda
+
+
+def _offsets_dev(offsets: torch.Tensor):
+    _need(offsets, torch.int32, "offsets")
+    if offsets.dim() != 1 or offsets.numel() < 2:
+        raise ValueError("offsets: 1-D int32 tensor of groups + 1 entries")
+    return _ptr(offsets), offsets.numel() - 1
 
 
 def _offsets_host(offsets) -> np.ndarray:
@@ -225,9 +246,25 @@ def empty_quant_128x128(rows: int, cols: int, batch: Optional[int] = None,
     return q, qT, sc
 
 
+def fp8bs_padded_tokens_max(rows: int, groups: int) -> int:
+    v = int(lib().fp8bs_padded_tokens_max(int(rows), int(groups)))
+    if v < 0:
+        raise ValueError("invalid rows or groups")
+    return v
+
+
+def _padded(rows: int, offsets) -> int:
+    """Token length of the transposed outputs: exact for host offsets, the
+    capacity bound for device offsets."""
+    if _on_device(offsets):
+        return fp8bs_padded_tokens_max(rows, offsets.numel() - 1)
+    return fp8bs_padded_tokens(rows, offsets)
+
+
 def empty_requant_128x1_T(rows: int, cols: int, offsets=None, device="cuda"):
-    """(qT uint8 [cols x Mpad], scalesT float32 [Mpad/128 x cols])."""
-    mp = fp8bs_padded_tokens(rows, offsets)
+    """(qT uint8 [cols x Mpad], scalesT float32 [Mpad/128 x cols]); with
+    device offsets Mpad is fp8bs_padded_tokens_max(rows, groups)."""
+    mp = _padded(rows, offsets)
     qT = torch.empty((cols, mp), dtype=torch.uint8, device=device)
     sc = torch.empty((mp // 128, cols), dtype=torch.float32, device=device)
     return qT, sc
@@ -289,14 +326,22 @@ def fp8_requant_128x1_T(src: torch.Tensor, src_scales: Optional[torch.Tensor], q
         _need(src, torch.uint8, "src"); _need(src_scales, torch.float32, "src_scales")
     _need(qT, torch.uint8, "qT"); _need(scalesT, torch.float32, "scalesT")
     rows, cols = src.shape
+    mp = _padded(rows, offsets)
+    if qT.shape != (cols, mp) or scalesT.shape != (mp // 128, cols):
+        raise ValueError("output shapes do not match empty_requant_128x1_T")
+    if _on_device(offsets):
+        if sr is not None:
+            raise ValueError("stochastic rounding takes host offsets")
+        optr, groups = _offsets_dev(offsets)
+        _check("fp8_requant_128x1_T_dev", lib().fp8_requant_128x1_T_dev(
+            mode, _ptr(src), _ptr(src_scales if mode == SRC_E4M3 else None), rows, cols, optr, groups,
+            _ptr(qT), _ptr(scalesT), _opts(rule, amax_floor, scale_floor), _stream(stream)))
+        return
     if offsets is not None:
         off = _offsets_host(offsets)
         optr, groups = off.ctypes.data_as(ctypes.c_void_p), off.size - 1
     else:
         off, optr, groups = None, None, 0
-    mp = fp8bs_padded_tokens(rows, offsets)
-    if qT.shape != (cols, mp) or scalesT.shape != (mp // 128, cols):
-        raise ValueError("output shapes do not match empty_requant_128x1_T")
     if sr is None:
         _check("fp8_requant_128x1_T", lib().fp8_requant_128x1_T_opts(
             mode, _ptr(src), _ptr(src_scales if mode == SRC_E4M3 else None), rows, cols, optr, groups,
@@ -351,6 +396,33 @@ def fp8_quant_dual_stash_sr(x, q, scales, qT, scalesT, seed: int, salt: int = 0,
                  scale_floor, sr=(seed, salt))
 
 
+def _require_dev(offsets):
+    if not _on_device(offsets):
+        raise ValueError("offsets_dev must be a CUDA int32 tensor")
+
+
+def fp8_requant_128x1_T_dev(src, src_scales, qT, scalesT, offsets_dev, opts: Optional["ScaleOpts"] = None,
+                            stream=None) -> None:
+    """fp8_requant_128x1_T with group offsets read on the device (outputs
+    sized by empty_requant_128x1_T with the same offsets tensor)."""
+    _require_dev(offsets_dev)
+    fp8_requant_128x1_T(src, src_scales, qT, scalesT, offsets_dev, stream, **_rule_kwargs(opts))
+
+
+def fp8_quant_dual_dev(x, q, scales, qT, scalesT, offsets_dev, opts: Optional["ScaleOpts"] = None,
+                       stream=None) -> None:
+    """fp8_quant_dual with group offsets read on the device."""
+    _require_dev(offsets_dev)
+    fp8_quant_dual(x, q, scales, qT, scalesT, offsets_dev, stream, **_rule_kwargs(opts))
+
+
+def fp8_quant_dual_stash_dev(x, q, scales, qT, scalesT, offsets_dev, opts: Optional["ScaleOpts"] = None,
+                             stream=None) -> None:
+    """fp8_quant_dual_stash with group offsets read on the device."""
+    _require_dev(offsets_dev)
+    fp8_quant_dual_stash(x, q, scales, qT, scalesT, offsets_dev, stream, **_rule_kwargs(opts))
+
+
 def _dual_common(fn, x, q, scales, qT, scalesT, offsets, stream, rule, amax_floor, scale_floor, sr=None) -> None:
     _need(x, torch.bfloat16, "x")
     for t, n, d in ((q, "q", torch.uint8), (scales, "scales", torch.float32), (qT, "qT", torch.uint8),
@@ -361,14 +433,24 @@ def _dual_common(fn, x, q, scales, qT, scalesT, offsets, stream, rule, amax_floo
         raise ValueError("x must be contiguous")
     if q.shape != (rows, cols) or scales.shape != ((cols + 127) // 128, fp8bs_scale_ld(rows)):
         raise ValueError("q / scales shapes do not match empty_quant_1x128")
+    mp = _padded(rows, offsets)
+    if qT.shape != (cols, mp) or scalesT.shape != (mp // 128, cols):
+        raise ValueError("qT / scalesT shapes do not match empty_requant_128x1_T")
+    if _on_device(offsets):
+        if sr is not None:
+            raise ValueError("stochastic rounding takes host offsets")
+        dev_fn = {"fp8_quant_dual_opts": "fp8_quant_dual_dev",
+                  "fp8_quant_dual_stash_opts": "fp8_quant_dual_stash_dev"}[fn]
+        optr, groups = _offsets_dev(offsets)
+        _check(dev_fn, getattr(lib(), dev_fn)(
+            _ptr(x), rows, cols, optr, groups, _ptr(q), _ptr(scales), _ptr(qT), _ptr(scalesT),
+            _opts(rule, amax_floor, scale_floor), _stream(stream)))
+        return
     if offsets is not None:
         off = _offsets_host(offsets)
         optr, groups = off.ctypes.data_as(ctypes.c_void_p), off.size - 1
     else:
         off, optr, groups = None, None, 0
-    mp = fp8bs_padded_tokens(rows, offsets)
-    if qT.shape != (cols, mp) or scalesT.shape != (mp // 128, cols):
-        raise ValueError("qT / scalesT shapes do not match empty_requant_128x1_T")
     if sr is None:
         _check(fn[:-len("_opts")], getattr(lib(), fn)(
             _ptr(x), rows, cols, optr, groups, _ptr(q), _ptr(scales), _ptr(qT), _ptr(scalesT),
@@ -616,15 +698,33 @@ def fp8_block_gemm_wgrad(dyqT, sdyT, xqT, sxT, dw, accumulate: bool = False, str
 
 
 def fp8_block_gemm_grouped(op: int, offsets, a, sa, b, sb, out, N: int, K: int,
-                           accumulate: bool = False, stream=None) -> None:
-    """Grouped (MoE) GEMM; see fp8bs.h for the operand layouts of each op."""
-    off = _offsets_host(offsets)
+                           accumulate: bool = False, stream=None, rows: Optional[int] = None) -> None:
+    """Grouped (MoE) GEMM; see fp8bs.h for the operand layouts of each op.
+
+    ``offsets`` (groups + 1 int32 row offsets) given as a CUDA tensor is read
+    by the kernel on the device (nothing is copied to the host, so the call
+    can sit in a CUDA graph whose routing changes between replays); any other
+    sequence is a host array. ``rows`` is the total token count: by default
+    a.shape[0] for Fprop / Dgrad and offsets[-1] for Wgrad with host offsets;
+    Wgrad with device offsets needs it."""
     for t, n, d in ((a, "a", torch.uint8), (sa, "sa", torch.float32), (b, "b", torch.uint8),
                     (sb, "sb", torch.float32)):
         _need(t, d, n)
     _need(out, torch.float32 if op == OP_WGRAD else torch.bfloat16, "out")
+    if _on_device(offsets):
+        dptr, groups = _offsets_dev(offsets)
+        hptr = None
+        if rows is None:
+            if op == OP_WGRAD:
+                raise ValueError("Wgrad with device offsets needs rows (the total token count)")
+            rows = a.shape[0]
+    else:
+        off = _offsets_host(offsets)
+        dptr, hptr, groups = None, off.ctypes.data_as(ctypes.c_void_p), off.size - 1
+        if rows is None:
+            rows = int(off[-1])
     _check("fp8_block_gemm_grouped", lib().fp8_block_gemm_grouped(
-        int(op), off.size - 1, off.ctypes.data_as(ctypes.c_void_p), _ptr(a), _ptr(sa), _ptr(b),
+        int(op), groups, dptr, hptr, int(rows), _ptr(a), _ptr(sa), _ptr(b),
         _ptr(sb), int(N), int(K), _ptr(out), int(bool(accumulate)), _stream(stream)))
 
 
@@ -691,19 +791,35 @@ def fp8_block_gemm_splitk_noalloc(op: int, a, sa, b, sb, out, splits: Optional[i
     if splits is None:
         splits = fp8bs_splitk_default_splits(op, M, N, K)
     need = fp8bs_splitk_workspace_size(op, M, N, K, splits)
+    detail = ""
     if need > NOALLOC_SCRATCH_BYTES:
-        raise ValueError(f"fp8_block_gemm_splitk_noalloc: {splits} ranges of {M} x "
-                         f"{out_shape[1]} fp32 need {need} bytes, more than the fixed "
-                         f"{NOALLOC_SCRATCH_BYTES}-byte scratch; use fewer splits or "
-                         "fp8_block_gemm_splitk with a workspace")
+        detail = (f"{splits} ranges of {M} x {out_shape[1]} fp32 need {need} bytes, more than the fixed "
+                  f"{NOALLOC_SCRATCH_BYTES}-byte scratch; use fewer splits or fp8_block_gemm_splitk "
+                  "with a workspace")
     _check("fp8_block_gemm_splitk_noalloc", lib().fp8_block_gemm_splitk_noalloc(
         int(op), _ptr(a), _ptr(sa), _ptr(b), _ptr(sb), M, N, K, int(splits), _ptr(out),
-        _stream(stream)))
+        _stream(stream)), detail)
 
 
 def fp8bs_device_status(reset: bool = True) -> int:
     """Synchronize and return the device status word (0 = OK)."""
     return int(lib().fp8bs_device_status(int(bool(reset))))
+
+
+def fp8bs_last_device_status(stream=None, reset: bool = False) -> int:
+    """The device status word as of the work issued so far on `stream`
+    (waits for that stream only, not the whole device)."""
+    return int(lib().fp8bs_last_device_status(_stream(stream), int(bool(reset))))
+
+
+def fp8bs_copy_device_status(dst: torch.Tensor, reset: bool = False, stream=None) -> None:
+    """Enqueue a copy of the device status word into dst (a CUDA int32 tensor
+    of one element) on `stream`, without waiting; capturable in a graph."""
+    _need(dst, torch.int32, "dst")
+    if dst.numel() != 1:
+        raise ValueError("dst: one int32 element")
+    _check("fp8bs_copy_device_status", lib().fp8bs_copy_device_status(_ptr(dst), int(bool(reset)),
+                                                                       _stream(stream)))
 
 
 def fp8bs_set_wait_limit_ns(ns: int) -> None:

@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -18,7 +19,7 @@ __device__ unsigned int g_device_status;
 constexpr int kMaxDevices = 64;
 
 struct DeviceState {
-    bool ready = false;
+    std::atomic<bool> ready{false};
     bool supported = false;
     int num_sms = 0;
     unsigned int* status = nullptr;
@@ -26,7 +27,7 @@ struct DeviceState {
 
 std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
-uint64_t g_wait_limit_ns = 2000000000ull;
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -43,9 +44,14 @@ fp8bs_status device_state(DeviceState** out)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return FP8BS_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_mutex);
     DeviceState& st = g_devices[dev];
-    if (!st.ready) {
+    if (st.ready.load(std::memory_order_acquire)) {   // set-up done: no lock
+        if (!st.supported || !g_encode) return FP8BS_ERR_UNSUPPORTED;
+        *out = &st;
+        return FP8BS_OK;
+    }
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!st.ready.load(std::memory_order_relaxed)) {
         cudaDeviceProp prop;
         if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return FP8BS_ERR_UNSUPPORTED;
         st.supported = (prop.major == 10 && prop.minor == 3);
@@ -61,7 +67,7 @@ fp8bs_status device_state(DeviceState** out)
                 q == cudaDriverEntryPointSuccess)
                 g_encode = reinterpret_cast<EncodeTiledFn>(fn);
         }
-        st.ready = true;
+        st.ready.store(true, std::memory_order_release);
     }
     if (!st.supported || !g_encode) return FP8BS_ERR_UNSUPPORTED;
     *out = &st;
@@ -130,6 +136,76 @@ bool make_out_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows)
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor-map cache. Encoding a map is a driver call of a microsecond or
+// two; an eager caller repeats the same few (pointer, shape) pairs, so each
+// host thread keeps a small direct-mapped cache of encoded maps keyed by the
+// device and every argument of the encoding. A hit copies the 128-byte map.
+struct MapKey {
+    int dev;
+    int kind;   // 0: E4M3 operand map, 1: BF16 output map
+    const void* base;
+    uint64_t inner, outer, row_bytes;
+    uint32_t box_outer;
+    bool operator==(const MapKey& o) const
+    {
+        return dev == o.dev && kind == o.kind && base == o.base && inner == o.inner && outer == o.outer &&
+               row_bytes == o.row_bytes && box_outer == o.box_outer;
+    }
+};
+
+struct MapSlot {
+    bool used = false;
+    MapKey key;
+    CUtensorMap map;
+};
+
+constexpr int kMapSlots = 64;
+thread_local MapSlot t_maps[kMapSlots];
+
+MapSlot& map_slot(const MapKey& k)
+{
+    uint64_t h = reinterpret_cast<uintptr_t>(k.base) >> 4;
+    h ^= k.inner * 0x9E3779B97F4A7C15ull ^ k.outer * 0xC2B2AE3D27D4EB4Full ^ k.row_bytes * 0x165667B19E3779F9ull;
+    h ^= (static_cast<uint64_t>(k.box_outer) << 32) ^ (static_cast<uint64_t>(k.dev) << 8) ^ k.kind;
+    h ^= h >> 29;
+    return t_maps[h % kMapSlots];
+}
+
+bool cached_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                uint32_t box_outer)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const MapKey k{dev, 0, base, inner, outer, row_bytes, box_outer};
+    MapSlot& sl = map_slot(k);
+    if (sl.used && sl.key == k) {
+        *m = sl.map;
+        return true;
+    }
+    if (!make_map(m, base, inner, outer, row_bytes, box_outer)) return false;
+    sl.used = true;
+    sl.key = k;
+    sl.map = *m;
+    return true;
+}
+
+bool cached_out_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const MapKey k{dev, 1, base, cols, rows, cols * 2, 32u};
+    MapSlot& sl = map_slot(k);
+    if (sl.used && sl.key == k) {
+        *m = sl.map;
+        return true;
+    }
+    if (!make_out_map(m, base, cols, rows)) return false;
+    sl.used = true;
+    sl.key = k;
+    sl.map = *m;
+    return true;
+}
+
 void init_params(GemmParams& p, DeviceState* st, int n_cols)
 {
     std::memset(&p, 0, sizeof(p));
@@ -158,6 +234,16 @@ int64_t padded_tokens(int64_t rows, const int32_t* off, int32_t groups)
     return tot;
 }
 
+// Upper bound on the padded token count of `groups` groups holding `rows`
+// tokens in total: at most k = min(groups, rows) groups are non-empty and
+// sum_g ceil(T_g / 128) <= floor((rows + 127 k) / 128).
+int64_t padded_tokens_max(int64_t rows, int32_t groups)
+{
+    const int64_t k = groups < rows ? groups : rows;
+    if (k <= 1) return (rows + 127) / 128 * 128;
+    return (rows + 127 * k) / 128 * 128;
+}
+
 // Fprop / Dgrad, dense or grouped. For Fprop the contraction length is K and
 // the output width N; for Dgrad they are N and K. `contr` and `width` are
 // those two; b rows per group = width.
@@ -172,43 +258,58 @@ void splitk_shape(int64_t nkb, int64_t splits, int& used, int& kps)
     used = static_cast<int>((nkb + kps - 1) / kps);
 }
 
+// Group offsets of a call: exactly one of host (planned on the host) and
+// dev (read by the kernel) is set; `rows` is the total token count.
+struct Offsets {
+    const int32_t* host;
+    const int32_t* dev;
+    int32_t groups;
+    int64_t rows;
+};
+
+void copy_offsets(GemmParams& p, const Offsets& o)
+{
+    p.num_groups = o.groups;
+    if (o.dev) {
+        p.off_dev = o.dev;
+    } else {
+        for (int g = 0; g <= o.groups; ++g) p.off[g] = o.host[g];
+    }
+}
+
 // Fprop / Dgrad, dense or grouped; with splits > 1 (dense only) the
 // K-blocks of every tile are cut into ranges whose fp32 sums go to the
 // workspace `ws`, followed by the reduction kernel.
-fp8bs_status run_rowwise_gemm(bool dgrad, int32_t groups, const int32_t* off, const uint8_t* a,
-                              const float* sa, const uint8_t* b, const float* sb, int64_t N,
-                              int64_t K, void* out, void* stream, int32_t splits = 1, float* ws = nullptr)
+fp8bs_status run_rowwise_gemm(bool dgrad, const Offsets& o, const uint8_t* a, const float* sa, const uint8_t* b,
+                              const float* sb, int64_t N, int64_t K, void* out, void* stream, int32_t splits = 1,
+                              float* ws = nullptr)
 {
     DeviceState* st = nullptr;
     fp8bs_status s = device_state(&st);
     if (s != FP8BS_OK) return s;
     const int64_t contr = dgrad ? N : K;
     const int64_t width = dgrad ? K : N;
-    const int64_t M = off[groups];
+    const int64_t M = o.rows;
     if (M == 0) return FP8BS_OK;
-    if (M > 0x7FFFFFFF - kBM || width * groups > 0x7FFFFFFF || contr > 0x7FFFFFFF)
+    if (M > 0x7FFFFFFF - kBM * static_cast<int64_t>(o.groups) || width * o.groups > 0x7FFFFFFF ||
+        contr > 0x7FFFFFFF)
         return FP8BS_ERR_SHAPE;
 
     GemmParams p;
     init_params(p, st, static_cast<int>(width));
-    p.num_groups = groups;
-    int tiles = 0;
-    for (int g = 0; g < groups; ++g) {
-        const int rows = off[g + 1] - off[g];
-        p.tile_start[g] = tiles;
-        p.a_row0[g] = off[g];
-        p.a_rows[g] = rows;
-        p.k0[g] = 0;
-        p.kblocks[g] = static_cast<int>(contr / kBK);
-        p.b_row0[g] = static_cast<int>(g * width);
-        p.sa_kb0[g] = 0;
-        p.sb_off[g] = static_cast<int64_t>(g) * (K / 128) * (N / 128);
-        p.out_off[g] = 0;
-        p.out_row0[g] = off[g];
-        tiles += ((rows + kBM - 1) / kBM) * p.n_tiles;
+    p.layout = kRowGroups;
+    copy_offsets(p, o);
+    p.kblocks = static_cast<int>(contr / kBK);
+    p.b_group_rows = static_cast<int>(width);
+    p.rows_total = static_cast<int>(M);
+    p.sb_group_stride = (K / 128) * (N / 128);
+    // tiles: exact from host offsets, else the bound over any split of M rows
+    int64_t row_tiles = 0;
+    if (o.host) {
+        for (int g = 0; g < o.groups; ++g) row_tiles += (o.host[g + 1] - o.host[g] + kBM - 1) / kBM;
+    } else {
+        row_tiles = padded_tokens_max(M, o.groups) / kBM;
     }
-    p.tile_start[groups] = tiles;
-    p.total_tiles = tiles;
     p.sa = sa;
     p.sa_ld = fp8bs_scale_ld(M);
     p.sa_rows = static_cast<int>(p.sa_ld);
@@ -220,7 +321,7 @@ fp8bs_status run_rowwise_gemm(bool dgrad, int32_t groups, const int32_t* off, co
     p.out_ld = width;
     p.accumulate = 0;
     int used = 1, kps = 1 << 30;
-    if (splits > 1 && groups == 1) splitk_shape(contr / kBK, splits, used, kps);
+    if (splits > 1 && o.groups == 1) splitk_shape(contr / kBK, splits, used, kps);
     if (used > 1) {
         if (!ws) return FP8BS_ERR_ARG;
         p.splits = used;
@@ -231,57 +332,43 @@ fp8bs_status run_rowwise_gemm(bool dgrad, int32_t groups, const int32_t* off, co
 
     CUtensorMap ma, mb, mo;
     std::memset(&mo, 0, sizeof(mo));
-    if (!make_map(&ma, a, contr, M, contr, kBM) ||
-        !make_map(&mb, b, contr, width * groups, contr, kBN))
+    if (!cached_map(&ma, a, contr, M, contr, kBM) || !cached_map(&mb, b, contr, width * o.groups, contr, kBN))
         return FP8BS_ERR_ARG;
     if (used <= 1) {
-        if (!make_out_map(&mo, out, width, M)) return FP8BS_ERR_ARG;
+        if (!cached_out_map(&mo, out, width, M)) return FP8BS_ERR_ARG;
         p.tma_store = 1;
     }
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    const fp8bs_status r = launch_status(launch_gemm(GemmKind::kBlockScaleBf16, ma, mb, mo, p, st->num_sms, cs));
+    const int64_t max_units = row_tiles * p.n_tiles * p.splits;
+    const fp8bs_status r =
+        launch_status(launch_gemm(GemmKind::kBlockScaleBf16, ma, mb, mo, p, max_units, st->num_sms, cs));
     if (r != FP8BS_OK || used <= 1) return r;
     return launch_status(
         launch_splitk_reduce(ws, used, M * width, M * width, static_cast<uint16_t*>(out), st->num_sms, cs));
 }
 
-// Wgrad, dense (groups = 1 over all T tokens) or grouped (padded segments).
-fp8bs_status run_wgrad(int32_t groups, const int32_t* off, int64_t T, const uint8_t* a,
-                       const float* sa, const uint8_t* b, const float* sb, int64_t N, int64_t K,
-                       float* out, int accumulate, void* stream)
+// Wgrad, dense (one group over all T tokens) or grouped (padded segments,
+// T = the padded token count of the operands).
+fp8bs_status run_wgrad(const Offsets& o, int64_t T, const uint8_t* a, const float* sa, const uint8_t* b,
+                       const float* sb, int64_t N, int64_t K, float* out, int accumulate, void* stream)
 {
     DeviceState* st = nullptr;
     fp8bs_status s = device_state(&st);
     if (s != FP8BS_OK) return s;
-    if (N > 0x7FFFFFFF || K > 0x7FFFFFFF || T > 0x7FFFFFFF) return FP8BS_ERR_SHAPE;
+    if (N > 0x7FFFFFFF || K > 0x7FFFFFFF || T > 0x7FFFFFFF || N * K * o.groups > (int64_t(1) << 62))
+        return FP8BS_ERR_SHAPE;
     if (T == 0) {
         if (accumulate) return FP8BS_OK;
-        return launch_status(cudaMemsetAsync(out, 0, sizeof(float) * N * K * groups,
+        return launch_status(cudaMemsetAsync(out, 0, sizeof(float) * N * K * o.groups,
                                              static_cast<cudaStream_t>(stream)));
     }
     GemmParams p;
     init_params(p, st, static_cast<int>(K));
-    p.num_groups = groups;
-    const int tiles_per_group = static_cast<int>((N / kBM) * p.n_tiles);
-    int64_t pstart = 0;
-    for (int g = 0; g < groups; ++g) {
-        const int64_t tg = off ? static_cast<int64_t>(off[g + 1] - off[g]) : T;
-        const int64_t kb = (tg + 127) / 128;
-        p.tile_start[g] = g * tiles_per_group;
-        p.a_row0[g] = 0;
-        p.a_rows[g] = static_cast<int>(N);
-        p.k0[g] = static_cast<int>(pstart);
-        p.kblocks[g] = static_cast<int>(kb);
-        p.b_row0[g] = 0;
-        p.sa_kb0[g] = static_cast<int>(pstart / 128);
-        p.sb_off[g] = (pstart / 128) * K;
-        p.out_off[g] = static_cast<int64_t>(g) * N * K;
-        p.out_row0[g] = static_cast<int>(g * N);
-        pstart += kb * 128;
-    }
-    if (pstart != T) return FP8BS_ERR_SHAPE;
-    p.tile_start[groups] = groups * tiles_per_group;
-    p.total_tiles = groups * tiles_per_group;
+    p.layout = kTokenGroups;
+    copy_offsets(p, o);
+    p.out_rows = static_cast<int>(N);
+    p.tcap = static_cast<int>(T);
+    p.out_group_stride = N * K;
     p.sa = sa;
     p.sa_ld = N;
     p.sa_rows = static_cast<int>(N);
@@ -296,8 +383,9 @@ fp8bs_status run_wgrad(int32_t groups, const int32_t* off, int64_t T, const uint
     // memory measured slower), so its output map stays unused
     CUtensorMap ma, mb, mo;
     std::memset(&mo, 0, sizeof(mo));
-    if (!make_map(&ma, a, T, N, T, kBM) || !make_map(&mb, b, T, K, T, kBN)) return FP8BS_ERR_ARG;
-    return launch_status(launch_gemm(GemmKind::kVectorScaleF32, ma, mb, mo, p, st->num_sms,
+    if (!cached_map(&ma, a, T, N, T, kBM) || !cached_map(&mb, b, T, K, T, kBN)) return FP8BS_ERR_ARG;
+    const int64_t max_units = static_cast<int64_t>(o.groups) * (N / kBM) * p.n_tiles;
+    return launch_status(launch_gemm(GemmKind::kVectorScaleF32, ma, mb, mo, p, max_units, st->num_sms,
                                      static_cast<cudaStream_t>(stream)));
 }
 
@@ -445,7 +533,7 @@ fp8bs_status requant_common(int src_mode, const void* src, const float* src_scal
                             const int32_t* group_offsets_host, int32_t groups, uint8_t* qT, float* scalesT,
                             uint8_t* q, float* q_scales, const fp8bs_scale_opts* opts, void* stream,
                             bool stash = false, const SrParams* sr = nullptr, uint8_t* q_atoms = nullptr,
-                            uint8_t* qT_atoms = nullptr)
+                            uint8_t* qT_atoms = nullptr, const int32_t* offsets_dev = nullptr)
 {
     ScaleRule rule;
     if (!to_rule(opts, &rule)) return FP8BS_ERR_ARG;
@@ -453,10 +541,13 @@ fp8bs_status requant_common(int src_mode, const void* src, const float* src_scal
     if (rows < 0 || cols <= 0 || groups < 0) return FP8BS_ERR_ARG;
     if (cols % 16 != 0) return FP8BS_ERR_SHAPE;
     if (rows > 0x7FFFFFFF) return FP8BS_ERR_SHAPE;
+    if (offsets_dev && (group_offsets_host || groups < 1 || groups > kMaxGroups)) return FP8BS_ERR_ARG;
+    if (offsets_dev && (reinterpret_cast<uintptr_t>(offsets_dev) & 3u) != 0) return FP8BS_ERR_ALIGN;
     const bool grouped = group_offsets_host && groups > 0;
     if (grouped && (!valid_offsets(group_offsets_host, groups) || group_offsets_host[groups] != rows))
         return FP8BS_ERR_ARG;
-    const int64_t mpad = padded_tokens(rows, grouped ? group_offsets_host : nullptr, grouped ? groups : 0);
+    const int64_t mpad = offsets_dev ? padded_tokens_max(rows, groups)
+                                     : padded_tokens(rows, grouped ? group_offsets_host : nullptr, grouped ? groups : 0);
     if (mpad == 0) return FP8BS_OK;
     if (!src || !qT || !scalesT || (src_mode == FP8BS_SRC_E4M3 && !src_scales)) return FP8BS_ERR_ARG;
     if (!aligned16(src) || !aligned16(qT) || !aligned16(scalesT) ||
@@ -493,7 +584,10 @@ fp8bs_status requant_common(int src_mode, const void* src, const float* src_scal
         p.sr_salt_rows = sr->salt;
         p.sr_salt_cols = q ? sr->salt + 1u : sr->salt;
     }
-    if (grouped) {
+    if (offsets_dev) {
+        p.num_groups = groups;
+        p.off_dev = offsets_dev;
+    } else if (grouped) {
         p.num_groups = groups;
         int tiles = 0;
         for (int g = 0; g <= groups; ++g) p.off[g] = group_offsets_host[g];
@@ -564,6 +658,35 @@ fp8bs_status fp8_quant_dual_stash_opts(const void* x, int64_t rows, int64_t cols
     if (rows > 0 && (!q || !scales)) return FP8BS_ERR_ARG;
     return requant_common(FP8BS_SRC_BF16, x, nullptr, rows, cols, group_offsets_host, groups, qT, scalesT, q,
                           scales, opts, stream, true);
+}
+
+fp8bs_status fp8_requant_128x1_T_dev(int src_mode, const void* src, const float* src_scales, int64_t rows,
+                                     int64_t cols, const int32_t* offsets_dev, int32_t groups, uint8_t* qT,
+                                     float* scalesT, const fp8bs_scale_opts* opts, void* stream)
+{
+    if (!offsets_dev) return FP8BS_ERR_ARG;
+    return requant_common(src_mode, src, src_scales, rows, cols, nullptr, groups, qT, scalesT, nullptr, nullptr,
+                          opts, stream, false, nullptr, nullptr, nullptr, offsets_dev);
+}
+
+fp8bs_status fp8_quant_dual_dev(const void* x, int64_t rows, int64_t cols, const int32_t* offsets_dev,
+                                int32_t groups, uint8_t* q, float* scales, uint8_t* qT, float* scalesT,
+                                const fp8bs_scale_opts* opts, void* stream)
+{
+    if (!offsets_dev) return FP8BS_ERR_ARG;
+    if (rows > 0 && (!q || !scales)) return FP8BS_ERR_ARG;
+    return requant_common(FP8BS_SRC_BF16, x, nullptr, rows, cols, nullptr, groups, qT, scalesT, q, scales, opts,
+                          stream, false, nullptr, nullptr, nullptr, offsets_dev);
+}
+
+fp8bs_status fp8_quant_dual_stash_dev(const void* x, int64_t rows, int64_t cols, const int32_t* offsets_dev,
+                                      int32_t groups, uint8_t* q, float* scales, uint8_t* qT, float* scalesT,
+                                      const fp8bs_scale_opts* opts, void* stream)
+{
+    if (!offsets_dev) return FP8BS_ERR_ARG;
+    if (rows > 0 && (!q || !scales)) return FP8BS_ERR_ARG;
+    return requant_common(FP8BS_SRC_BF16, x, nullptr, rows, cols, nullptr, groups, qT, scalesT, q, scales, opts,
+                          stream, true, nullptr, nullptr, nullptr, offsets_dev);
 }
 
 fp8bs_status fp8_quant_dual_packed(const void* x, int64_t rows, int64_t cols, uint8_t* q, float* scales,
@@ -642,7 +765,7 @@ fp8bs_status fp8_block_gemm_fprop(const uint8_t* xq, const float* sx, const uint
     if (!aligned16(xq) || !aligned16(sx) || !aligned16(wqT) || !aligned16(sw) || !aligned16(y))
         return FP8BS_ERR_ALIGN;
     const int32_t off[2] = {0, static_cast<int32_t>(M)};
-    return run_rowwise_gemm(false, 1, off, xq, sx, wqT, sw, N, K, y, stream);
+    return run_rowwise_gemm(false, Offsets{off, nullptr, 1, M}, xq, sx, wqT, sw, N, K, y, stream);
 }
 
 fp8bs_status fp8_block_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wq,
@@ -656,7 +779,7 @@ fp8bs_status fp8_block_gemm_dgrad(const uint8_t* dyq, const float* sdy, const ui
     if (!aligned16(dyq) || !aligned16(sdy) || !aligned16(wq) || !aligned16(sw) || !aligned16(dx))
         return FP8BS_ERR_ALIGN;
     const int32_t off[2] = {0, static_cast<int32_t>(M)};
-    return run_rowwise_gemm(true, 1, off, dyq, sdy, wq, sw, N, K, dx, stream);
+    return run_rowwise_gemm(true, Offsets{off, nullptr, 1, M}, dyq, sdy, wq, sw, N, K, dx, stream);
 }
 
 int64_t fp8bs_mx_scale_bytes(int64_t rows, int64_t cols)
@@ -818,7 +941,7 @@ fp8bs_status fp8_block_gemm_splitk(int op, const uint8_t* a, const float* sa, co
         if (!aligned16(workspace)) return FP8BS_ERR_ALIGN;
     }
     const int32_t off[2] = {0, static_cast<int32_t>(M)};
-    return run_rowwise_gemm(op == FP8BS_OP_DGRAD, 1, off, a, sa, b, sb, N, K, out, stream,
+    return run_rowwise_gemm(op == FP8BS_OP_DGRAD, Offsets{off, nullptr, 1, M}, a, sa, b, sb, N, K, out, stream,
                             need > 0 ? splits : 1, static_cast<float*>(workspace));
 }
 
@@ -833,36 +956,44 @@ fp8bs_status fp8_block_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const 
     if (!aligned16(dw) || (T > 0 && (!aligned16(dyqT) || !aligned16(sdyT) || !aligned16(xqT) ||
                                      !aligned16(sxT))))
         return FP8BS_ERR_ALIGN;
-    return run_wgrad(1, nullptr, T, dyqT, sdyT, xqT, sxT, N, K, dw, accumulate, stream);
+    const int32_t off[2] = {0, static_cast<int32_t>(T)};
+    return run_wgrad(Offsets{off, nullptr, 1, T}, T, dyqT, sdyT, xqT, sxT, N, K, dw, accumulate, stream);
 }
 
-fp8bs_status fp8_block_gemm_grouped(int op, int32_t groups, const int32_t* offsets_host,
-                                    const uint8_t* a, const float* sa, const uint8_t* b,
-                                    const float* sb, int64_t N, int64_t K, void* out,
-                                    int accumulate, void* stream)
+fp8bs_status fp8_block_gemm_grouped(int op, int32_t groups, const int32_t* offsets_dev,
+                                    const int32_t* offsets_host, int64_t rows, const uint8_t* a,
+                                    const float* sa, const uint8_t* b, const float* sb, int64_t N, int64_t K,
+                                    void* out, int accumulate, void* stream)
 {
     if (op != FP8BS_OP_FPROP && op != FP8BS_OP_DGRAD && op != FP8BS_OP_WGRAD) return FP8BS_ERR_ARG;
-    if (!valid_offsets(offsets_host, groups)) return FP8BS_ERR_ARG;
+    if (groups < 1 || groups > kMaxGroups || rows < 0) return FP8BS_ERR_ARG;
+    if ((offsets_dev == nullptr) == (offsets_host == nullptr)) return FP8BS_ERR_ARG;   // exactly one
+    if (offsets_host && (!valid_offsets(offsets_host, groups) || offsets_host[groups] != rows)) return FP8BS_ERR_ARG;
+    if (offsets_dev && (reinterpret_cast<uintptr_t>(offsets_dev) & 3u) != 0) return FP8BS_ERR_ALIGN;
     if (N <= 0 || K <= 0) return FP8BS_ERR_ARG;
     if (N % 128 != 0 || K % 128 != 0) return FP8BS_ERR_SHAPE;
+    if (rows > 0x7FFFFF00) return FP8BS_ERR_SHAPE;
     if (!out) return FP8BS_ERR_ARG;
-    const int64_t M = offsets_host[groups];
+    const Offsets o{offsets_host, offsets_dev, groups, rows};
     if (op == FP8BS_OP_WGRAD) {
-        const int64_t T = padded_tokens(M, offsets_host, groups);
+        const int64_t T = offsets_host ? padded_tokens(rows, offsets_host, groups) : padded_tokens_max(rows, groups);
         if (T > 0 && (!a || !sa || !b || !sb)) return FP8BS_ERR_ARG;
         if (!aligned16(out) || (T > 0 && (!aligned16(a) || !aligned16(sa) || !aligned16(b) ||
                                           !aligned16(sb))))
             return FP8BS_ERR_ALIGN;
-        return run_wgrad(groups, offsets_host, T, a, sa, b, sb, N, K, static_cast<float*>(out),
-                         accumulate, stream);
+        return run_wgrad(o, T, a, sa, b, sb, N, K, static_cast<float*>(out), accumulate, stream);
     }
-    if (M == 0) return FP8BS_OK;
+    if (rows == 0) return FP8BS_OK;
     if (!a || !sa || !b || !sb) return FP8BS_ERR_ARG;
     if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(out))
         return FP8BS_ERR_ALIGN;
-    if (M > 0x7FFFFF00) return FP8BS_ERR_SHAPE;
-    return run_rowwise_gemm(op == FP8BS_OP_DGRAD, groups, offsets_host, a, sa, b, sb, N, K, out,
-                            stream);
+    return run_rowwise_gemm(op == FP8BS_OP_DGRAD, o, a, sa, b, sb, N, K, out, stream);
+}
+
+int64_t fp8bs_padded_tokens_max(int64_t rows, int32_t groups)
+{
+    if (rows < 0 || groups < 0 || groups > kMaxGroups) return -1;
+    return padded_tokens_max(rows, groups);
 }
 
 fp8bs_status fp8bs_device_status(int reset)
@@ -880,6 +1011,34 @@ fp8bs_status fp8bs_device_status(int reset)
             return FP8BS_ERR_LAUNCH;
     }
     return static_cast<fp8bs_status>(v);
+}
+
+fp8bs_status fp8bs_last_device_status(void* stream, int reset)
+{
+    DeviceState* st = nullptr;
+    fp8bs_status s = device_state(&st);
+    if (s != FP8BS_OK) return s;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    unsigned int v = 0;
+    if (cudaMemcpyAsync(&v, st->status, sizeof(v), cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+        return FP8BS_ERR_LAUNCH;
+    if (reset && cudaMemsetAsync(st->status, 0, sizeof(unsigned int), cs) != cudaSuccess) return FP8BS_ERR_LAUNCH;
+    if (cudaStreamSynchronize(cs) != cudaSuccess) return FP8BS_ERR_LAUNCH;
+    return static_cast<fp8bs_status>(v);
+}
+
+fp8bs_status fp8bs_copy_device_status(unsigned int* dst, int reset, void* stream)
+{
+    if (!dst) return FP8BS_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(dst) & 3u) != 0) return FP8BS_ERR_ALIGN;
+    DeviceState* st = nullptr;
+    fp8bs_status s = device_state(&st);
+    if (s != FP8BS_OK) return s;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(dst, st->status, sizeof(unsigned int), cudaMemcpyDeviceToDevice, cs) != cudaSuccess)
+        return FP8BS_ERR_LAUNCH;
+    if (reset && cudaMemsetAsync(st->status, 0, sizeof(unsigned int), cs) != cudaSuccess) return FP8BS_ERR_LAUNCH;
+    return FP8BS_OK;
 }
 
 void fp8bs_set_wait_limit_ns(uint64_t ns)

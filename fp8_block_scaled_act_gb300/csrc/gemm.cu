@@ -42,6 +42,8 @@
 // copies and MMAs, frees its tensor memory and returns.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -57,8 +59,9 @@ constexpr int kFirstEpiWarp = 4;
 constexpr int kThreads = (kFirstEpiWarp + kEpiWarps) * 32;  // 384: three warpgroups
 // Register split: the kernel is launched with kLaunchRegs per thread (the
 // __launch_bounds__ budget); the producer warpgroup gives registers back and
-// the two epilogue warpgroups take them. The host checks the launch count
-// before the first launch so that the split never asks for more than exists.
+// the two epilogue warpgroups take them. Before the first launch on a device
+// the host checks that the compiled launch allocation covers the split, so
+// that the split never asks for more than exists.
 constexpr uint32_t kLaunchRegs = 168;
 constexpr uint32_t kProducerRegs = 40;
 constexpr uint32_t kEpilogueRegs = 232;
@@ -68,7 +71,7 @@ constexpr int kTmemCols = 2 * kBN;              // two accumulator buffers
 // Waits that drain in-flight copies and MMAs before exit use at least this
 // limit, so that a small user limit never lets a CTA exit with work in flight.
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
-constexpr int kCtlBytes = 512;                  // barriers and flags
+constexpr int kCtlBytes = 2048;                 // barriers, flags and the group table
 // Wgrad scale ring: slot = the K-block's scales of the tile's 128 rows, then
 // of its 256 columns.
 constexpr int kScaleSlots = 8;
@@ -101,6 +104,17 @@ constexpr int smem_bytes()
     return num_stages<kKind>() * kStageBytes + extra_bytes<kKind>() + kCtlBytes + 1024 /* alignment */;
 }
 
+// Per-group table built at kernel start from the group offsets: for row
+// groups the first tile of each group, for token groups the first K-block
+// of each group in the padded token axis (its tiles start at g times the
+// tiles per group). The offsets themselves are read again from the
+// parameters or device memory when a tile starts.
+struct GroupTab {
+    int32_t start[kMaxGroups + 1];
+    int32_t total_tiles;
+    int32_t valid;
+};
+
 struct SharedCtl {
     uint64_t full[kStages];
     uint64_t empty[kStages];
@@ -110,6 +124,7 @@ struct SharedCtl {
     uint64_t mma_done;        // final commit of the MMA thread (drain before exit)
     uint32_t tmem_base;
     volatile int abort;
+    GroupTab tab;
 };
 
 __device__ __forceinline__ void record_status(unsigned int* status, unsigned int code)
@@ -117,32 +132,135 @@ __device__ __forceinline__ void record_status(unsigned int* status, unsigned int
     atomicCAS(status, 0u, code);
 }
 
-__device__ __forceinline__ void decode_tile(const GemmParams& p, int t, int& g, int& mt, int& nt)
+// Everything the roles need about group g (see GroupLayout).
+struct GroupInfo {
+    int a_row0;      // first A row (= first output row)
+    int a_rows;      // output rows
+    int k0;          // first K element (TMA x coordinate)
+    int kblocks;     // 128-element K-blocks
+    int b_row0;      // first B row (TMA y coordinate)
+    int sa_kb0;      // first scale K-block of A
+    int64_t sb_off;  // float offset of the group's B scales
+    int64_t out_off; // element offset of the group's output origin
+    int out_row0;    // row of the output tensor map holding the group's output row 0
+};
+
+__device__ __forceinline__ int group_off(const GemmParams& p, int g)
 {
-    int lo = 0, hi = p.num_groups - 1;  // last g with tile_start[g] <= t
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (p.tile_start[mid] <= t) lo = mid; else hi = mid - 1;
+    return p.off_dev ? __ldg(p.off_dev + g) : p.off[g];
+}
+
+__device__ __forceinline__ GroupInfo group_info(const GemmParams& p, const GroupTab& tab, int g)
+{
+    GroupInfo gi;
+    if (p.layout == kRowGroups) {
+        const int o0 = group_off(p, g), o1 = group_off(p, g + 1);
+        gi.a_row0 = o0;
+        gi.a_rows = o1 - o0;
+        gi.k0 = 0;
+        gi.kblocks = p.kblocks;
+        gi.b_row0 = g * p.b_group_rows;
+        gi.sa_kb0 = 0;
+        gi.sb_off = static_cast<int64_t>(g) * p.sb_group_stride;
+        gi.out_off = 0;
+        gi.out_row0 = o0;
+    } else {
+        gi.a_row0 = 0;
+        gi.a_rows = p.out_rows;
+        gi.k0 = tab.start[g] * kBK;
+        gi.kblocks = tab.start[g + 1] - tab.start[g];
+        gi.b_row0 = 0;
+        gi.sa_kb0 = tab.start[g];
+        gi.sb_off = static_cast<int64_t>(tab.start[g]) * p.sb_kstride;
+        gi.out_off = static_cast<int64_t>(g) * p.out_group_stride;
+        gi.out_row0 = g * p.out_rows;
     }
-    g = lo;
-    const int local = t - p.tile_start[g];
+    return gi;
+}
+
+// Builds the group table (all threads of the CTA take part; ends with a CTA
+// barrier). Invalid offsets (off[0] != 0, a decrease, a total other than
+// rows_total for row groups, more padded tokens than tcap for token groups)
+// leave no tiles and record FP8BS_ERR_DEVICE.
+__device__ void build_group_tab(const GemmParams& p, GroupTab& tab)
+{
+    const int G = p.num_groups;
+    int bad = 0;
+    // per-group counts (row groups: tiles; token groups: K-blocks), then an
+    // exclusive scan by warp 0 (up to eight groups per lane)
+    for (int g = threadIdx.x; g < G; g += blockDim.x) {
+        const int n = group_off(p, g + 1) - group_off(p, g);
+        if (n < 0) bad = 1;
+        const int nb = n < 0 ? 0 : (n + kBK - 1) / kBK;
+        tab.start[g] = p.layout == kRowGroups ? nb * p.n_tiles : nb;
+    }
+    if (threadIdx.x == 0) {
+        if (group_off(p, 0) != 0) bad = 1;
+        if (p.layout == kRowGroups && group_off(p, G) != p.rows_total) bad = 1;
+    }
+    bad = __syncthreads_or(bad);
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const int per = (G + 31) / 32;
+        const int g0 = min(G, lane * per), g1 = min(G, g0 + per);
+        int sum = 0;
+        for (int g = g0; g < g1; ++g) sum += tab.start[g];
+        int inc = sum;   // inclusive warp scan of the lanes' sums
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+            if (lane >= d) inc += v;
+        }
+        int run = inc - sum;   // exclusive prefix of this lane's first group
+        for (int g = g0; g < g1; ++g) {
+            const int c = tab.start[g];
+            tab.start[g] = run;
+            run += c;
+        }
+        if (lane == 31) {
+            tab.start[G] = inc;
+            const int total = p.layout == kRowGroups ? inc : G * (p.out_rows / kBM) * p.n_tiles;
+            const bool over = p.layout == kTokenGroups && static_cast<int64_t>(inc) * kBK > p.tcap;
+            tab.valid = (bad || over) ? 0 : 1;
+            tab.total_tiles = (bad || over) ? 0 : total;
+            if ((bad || over) && blockIdx.x == 0) record_status(p.status, FP8BS_ERR_DEVICE);
+        }
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ void decode_tile(const GemmParams& p, const GroupTab& tab, int t, int& g, int& mt,
+                                            int& nt)
+{
+    int local;
+    if (p.layout == kRowGroups) {
+        int lo = 0, hi = p.num_groups - 1;  // last g with start[g] <= t
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (tab.start[mid] <= t) lo = mid; else hi = mid - 1;
+        }
+        g = lo;
+        local = t - tab.start[g];
+    } else {
+        const int per = (p.out_rows / kBM) * p.n_tiles;
+        g = t / per;
+        local = t - g * per;
+    }
     mt = local / p.n_tiles;
     nt = local - mt * p.n_tiles;
 }
 
-// Work unit u -> tile (group, row tile, column tile) and the range of the
-// tile's K-blocks it covers: split-K divides every tile's K-blocks into
-// p.splits contiguous ranges of p.kb_per_split (the last may be shorter);
-// without split-K a unit is a whole tile.
-__device__ __forceinline__ void decode_unit(const GemmParams& p, int u, int& g, int& mt, int& nt, int& split,
-                                            int& kb0, int& nkb)
+__device__ __forceinline__ GroupInfo decode_unit(const GemmParams& p, const GroupTab& tab, int u, int& g, int& mt,
+                                                 int& nt, int& split, int& kb0, int& nkb)
 {
     const int t = u / p.splits;
     split = u - t * p.splits;
-    decode_tile(p, t, g, mt, nt);
+    decode_tile(p, tab, t, g, mt, nt);
+    const GroupInfo gi = group_info(p, tab, g);
     kb0 = split * p.kb_per_split;
-    const int end = min(p.kblocks[g], kb0 + p.kb_per_split);
+    const int end = min(gi.kblocks, kb0 + p.kb_per_split);
     nkb = max(0, end - kb0);
+    return gi;
 }
 
 // ---------------------------------------------------------------------------
@@ -151,7 +269,8 @@ __device__ __forceinline__ void decode_unit(const GemmParams& p, int u, int& g, 
 // false when a wait gave up.
 // ---------------------------------------------------------------------------
 
-// Fprop / Dgrad: s_b is one value per 128 output columns, so a K-block's
+// Fprop / Dgrad (row groups: A rows are output rows, no K offset, B scales
+// at g * sb_group_stride): s_b is one value per 128 output columns, so a K-block's
 // scale is one scalar per thread (row) and half. Layout 32x32b: thread =
 // row, 128 columns in registers. The BF16 output goes through a per-warp
 // shared-memory stage so that every global store instruction writes four
@@ -169,17 +288,22 @@ __device__ __forceinline__ bool epilogue_block_scale(const GemmParams& p, Shared
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t acc_it = 0;
 
-    const int units = p.total_tiles * p.splits;
+    const int units = ctl->tab.total_tiles * p.splits;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
         int g, mt, nt, split, kb0, nkb;
-        decode_unit(p, u, g, mt, nt, split, kb0, nkb);
-        const int row = p.a_row0[g] + mt * kBM + r_in_tile;   // A row = output row
-        const bool row_ok = (mt * kBM + r_in_tile) < p.a_rows[g];
+        int row0, nrows;   // the group's first row and row count (row groups: A rows = output rows)
+        {
+            const GroupInfo gi = decode_unit(p, ctl->tab, u, g, mt, nt, split, kb0, nkb);
+            row0 = gi.a_row0;
+            nrows = gi.a_rows;
+        }
+        const int row = row0 + mt * kBM + r_in_tile;
+        const bool row_ok = (mt * kBM + r_in_tile) < nrows;
         const int col0 = nt * kBN + half * 128;
         const bool cols_ok = col0 < p.n_cols;                  // n_cols % 128 == 0
         const bool sa_ok = row < p.sa_rows;
-        const float* sa_ptr = p.sa + static_cast<int64_t>(p.sa_kb0[g] + kb0) * p.sa_ld + row;
-        const float* sb_ptr = p.sb + p.sb_off[g] + static_cast<int64_t>(col0 / 128) * p.sb_cstride +
+        const float* sa_ptr = p.sa + static_cast<int64_t>(kb0) * p.sa_ld + row;
+        const float* sb_ptr = p.sb + static_cast<int64_t>(g) * p.sb_group_stride + static_cast<int64_t>(col0 / 128) * p.sb_cstride +
                               static_cast<int64_t>(kb0) * p.sb_kstride;
 
         auto load_sa = [&](int kb) -> float {
@@ -254,11 +378,10 @@ __device__ __forceinline__ bool epilogue_block_scale(const GemmParams& p, Shared
             // warp's 32 rows all belong to this group, one TMA store per round
             // writes the box while the warp goes on; otherwise lanes 8q .. 8q + 7
             // store one row's 128 contiguous bytes, four rows per instruction.
-            const int rows_left = p.a_rows[g] - (mt * kBM + quarter * 32);   // valid rows of this warp
-            const int out_row = p.out_row0[g] + mt * kBM + quarter * 32;
+            const int rows_left = nrows - (mt * kBM + quarter * 32);   // valid rows of this warp
+            const int out_row = row0 + mt * kBM + quarter * 32;
             const bool tma = p.tma_store && rows_left >= 32;
-            uint16_t* y0 = static_cast<uint16_t*>(p.out) + p.out_off[g] +
-                           static_cast<int64_t>(p.a_row0[g] + mt * kBM + quarter * 32) * p.out_ld + col0;
+            uint16_t* y0 = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(out_row) * p.out_ld + col0;
             const uint32_t st_base = smem_addr(out_stage) + ew * kOutStageWarpBytes;
 #pragma unroll
             for (int rnd = 0; rnd < 2; ++rnd) {
@@ -323,10 +446,10 @@ __device__ __forceinline__ bool epilogue_vector_scale(const GemmParams& p, Share
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t acc_it = 0;
 
-    const int units = p.total_tiles * p.splits;
+    const int units = ctl->tab.total_tiles * p.splits;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
         int g, mt, nt, split, kb0, nkb;
-        decode_unit(p, u, g, mt, nt, split, kb0, nkb);
+        const GroupInfo gi = decode_unit(p, ctl->tab, u, g, mt, nt, split, kb0, nkb);
         const int qrow0 = mt * kBM + quarter * 32;             // first tile row of this quarter
         const int col0 = nt * kBN + half * 128;
         const bool cols_ok = col0 < p.n_cols;                  // n_cols % 128 == 0
@@ -397,9 +520,9 @@ __device__ __forceinline__ bool epilogue_vector_scale(const GemmParams& p, Share
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r_tile = qrow0 + g4 + 8 * i;
-                if (r_tile >= p.a_rows[g]) continue;
-                float* y = static_cast<float*>(p.out) + p.out_off[g] +
-                           static_cast<int64_t>(p.a_row0[g] + r_tile) * p.out_ld + col0 + 2 * t4;
+                if (r_tile >= gi.a_rows) continue;
+                float* y = static_cast<float*>(p.out) + gi.out_off +
+                           static_cast<int64_t>(gi.a_row0 + r_tile) * p.out_ld + col0 + 2 * t4;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     float2 v = acc[i][j];
@@ -460,6 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     tc_fence_after_sync();
+    build_group_tab(p, ctl->tab);
     const uint32_t tmem_base = ctl->tmem_base;
     const uint64_t limit = p.wait_limit_ns;
 
@@ -473,12 +597,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            const int units = p.total_tiles * p.splits;
+            const int units = ctl->tab.total_tiles * p.splits;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
                 int g, mt, nt, split, kb0, nkb;
-                decode_unit(p, u, g, mt, nt, split, kb0, nkb);
-                const int ya = p.a_row0[g] + mt * kBM;
-                const int yb = p.b_row0[g] + nt * kBN;
+                const GroupInfo gi = decode_unit(p, ctl->tab, u, g, mt, nt, split, kb0, nkb);
+                const int ya = gi.a_row0 + mt * kBM;
+                const int yb = gi.b_row0 + nt * kBN;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const uint32_t s = it % kS;
                     const uint32_t ph = (it / kS) & 1u;
@@ -486,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    const int x = p.k0[g] + (kb0 + kb) * kBK;
+                    const int x = gi.k0 + (kb0 + kb) * kBK;
                     if constexpr (kKind == GemmKind::kVectorScaleF32) {
                         // Wgrad: this K-block's 128 row scales and the tile's
                         // column scales go into the scale ring as part of the
@@ -502,10 +626,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t b_bytes = static_cast<uint32_t>(min(kBN, p.n_cols - nt * kBN)) * 4u;
                         float* slot = scale_ring + ss * kScaleSlotFloats;
                         mbar_arrive_expect_tx(&ctl->full[s], kStageBytes + kBM * 4u + b_bytes);
-                        bulk_load(slot, p.sa + static_cast<int64_t>(p.sa_kb0[g] + kb0 + kb) * p.sa_ld + ya, kBM * 4u,
+                        bulk_load(slot, p.sa + static_cast<int64_t>(gi.sa_kb0 + kb0 + kb) * p.sa_ld + ya, kBM * 4u,
                                   &ctl->full[s]);
                         bulk_load(slot + kBM,
-                                  p.sb + p.sb_off[g] + static_cast<int64_t>(kb0 + kb) * p.sb_kstride + nt * kBN,
+                                  p.sb + gi.sb_off + static_cast<int64_t>(kb0 + kb) * p.sb_kstride + nt * kBN,
                                   b_bytes, &ctl->full[s]);
                     } else {
                         mbar_arrive_expect_tx(&ctl->full[s], kStageBytes);
@@ -532,10 +656,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kBN);
             uint32_t it = 0, acc_it = 0;
             bool ok = true;
-            const int units = p.total_tiles * p.splits;
+            const int units = ctl->tab.total_tiles * p.splits;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
                 int g, mt, nt, split, kb0, nkb;
-                decode_unit(p, u, g, mt, nt, split, kb0, nkb);
+                const GroupInfo gi = decode_unit(p, ctl->tab, u, g, mt, nt, split, kb0, nkb);
                 for (int kb = 0; kb < nkb; ++kb, ++it, ++acc_it) {
                     const uint32_t s = it % kS;
                     const uint32_t ph = (it / kS) & 1u;
@@ -632,21 +756,31 @@ __global__ void selftest_wait_kernel(unsigned int* status, uint64_t limit_ns)
 
 template <GemmKind kKind>
 cudaError_t launch_kind(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_out,
-                        const GemmParams& p, int num_sms, cudaStream_t stream)
+                        const GemmParams& p, int64_t max_units, int num_sms, cudaStream_t stream)
 {
     static_assert(sizeof(SharedCtl) <= kCtlBytes, "control block");
     auto kernel = block_scaled_gemm_kernel<kKind>;
-    cudaFuncAttributes attr;
-    cudaError_t e = cudaFuncGetAttributes(&attr, kernel);
-    if (e != cudaSuccess) return e;
-    // the setmaxnreg split assumes this launch allocation (see kLaunchRegs)
-    if (static_cast<uint32_t>(attr.numRegs) != kLaunchRegs) return cudaErrorInvalidConfiguration;
     constexpr int kSmemBytes = smem_bytes<kKind>();
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    // once per device: the shared-memory opt-in, and a check that the
+    // launch allocation covers the setmaxnreg split (a split above it would
+    // wait forever)
+    static std::atomic<uint64_t> ready{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const int units = p.total_tiles * p.splits;
-    const int grid = units < num_sms ? units : num_sms;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(ready.load(std::memory_order_acquire) & bit)) {
+        cudaFuncAttributes attr;
+        e = cudaFuncGetAttributes(&attr, kernel);
+        if (e != cudaSuccess) return e;
+        if (128u * kProducerRegs + 256u * kEpilogueRegs > static_cast<uint32_t>(kThreads) * attr.numRegs)
+            return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        ready.fetch_or(bit, std::memory_order_release);
+    }
+    const int grid = max_units < num_sms ? static_cast<int>(max_units) : num_sms;
     kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_a, map_b, map_out, p);
     return cudaGetLastError();
 }
@@ -667,12 +801,13 @@ cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t split_stri
 }
 
 cudaError_t launch_gemm(GemmKind kind, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                        const CUtensorMap& map_out, const GemmParams& p, int num_sms, cudaStream_t stream)
+                        const CUtensorMap& map_out, const GemmParams& p, int64_t max_units, int num_sms,
+                        cudaStream_t stream)
 {
-    if (p.total_tiles <= 0) return cudaSuccess;
+    if (max_units <= 0) return cudaSuccess;
     if (kind == GemmKind::kBlockScaleBf16)
-        return launch_kind<GemmKind::kBlockScaleBf16>(map_a, map_b, map_out, p, num_sms, stream);
-    return launch_kind<GemmKind::kVectorScaleF32>(map_a, map_b, map_out, p, num_sms, stream);
+        return launch_kind<GemmKind::kBlockScaleBf16>(map_a, map_b, map_out, p, max_units, num_sms, stream);
+    return launch_kind<GemmKind::kVectorScaleF32>(map_a, map_b, map_out, p, max_units, num_sms, stream);
 }
 
 cudaError_t launch_selftest_wait(unsigned int* status, uint64_t limit_ns, cudaStream_t stream)

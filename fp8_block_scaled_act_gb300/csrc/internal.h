@@ -56,6 +56,11 @@ struct RequantParams {
     int num_groups;
     int32_t off[kMaxGroups + 1];         // row offsets of the groups
     int32_t tile_start[kMaxGroups + 1];  // first padded token tile of each group
+    // Device offsets (num_groups + 1 entries): when set, off / tile_start
+    // are unused and each CTA derives its group from them; the grid covers
+    // the largest padded token count any split of `rows` can need, and CTAs
+    // past the actual count do nothing.
+    const int32_t* off_dev;
     // Optional, BF16 source only: the same block's 1x128 (row-wise) cast in
     // the same pass, q [rows x cols] and its scales [cols/128 x q_scale_ld].
     uint8_t* q;
@@ -85,24 +90,34 @@ cudaError_t launch_requant_128x1_T(const RequantParams& p, cudaStream_t stream);
 // Block-scaled GEMM (tcgen05)
 // ---------------------------------------------------------------------------
 
-// One output problem of the persistent GEMM kernel is a set of groups; each
-// group g has a rectangle of output rows, a K range and its own offsets into
-// the operands, scales and output. Dense GEMMs are one group.
+// One output problem of the persistent GEMM kernel is a set of groups given
+// by row offsets off[0..num_groups] (off[0] = 0, non-decreasing). The kernel
+// derives each group's tiles, K range and operand offsets from the offsets
+// in shared memory at start-up, reading them from off_dev (device memory)
+// when it is set and from off[] otherwise. Dense GEMMs are one group.
+//   kRowGroups (Fprop / Dgrad): group g owns output rows [off[g], off[g+1]),
+//     contracts over all kblocks K-blocks, reads B rows g * b_group_rows ...
+//     and B scales at g * sb_group_stride; off[num_groups] must equal
+//     rows_total.
+//   kTokenGroups (Wgrad): group g owns tokens [off[g], off[g+1]), padded to
+//     whole 128-token K-blocks laid end to end (at most tcap tokens); every
+//     group has the same b_rows x n_cols output at g * out_group_stride.
+enum GroupLayout { kRowGroups = 0, kTokenGroups = 1 };
+
 struct GemmParams {
+    int layout;                   // GroupLayout
     int num_groups;
-    int n_cols;        // output columns (same for all groups)
-    int n_tiles;       // column tiles of BN per group
-    int total_tiles;
-    int32_t tile_start[kMaxGroups + 1];
-    int32_t a_row0[kMaxGroups];   // first A row (= first output row) of the group
-    int32_t a_rows[kMaxGroups];   // output rows of the group
-    int32_t k0[kMaxGroups];       // first K element (TMA x coordinate)
-    int32_t kblocks[kMaxGroups];  // 128-element K blocks
-    int32_t b_row0[kMaxGroups];   // first B row (TMA y coordinate)
-    int32_t sa_kb0[kMaxGroups];   // first scale K-block of A
-    int64_t sb_off[kMaxGroups];   // float offset of the group's B scales
-    int64_t out_off[kMaxGroups];  // element offset of the group's output origin
-    int32_t out_row0[kMaxGroups]; // row of the output tensor map holding the group's output row 0
+    int n_cols;                   // output columns (same for all groups)
+    int n_tiles;                  // column tiles of BN per group
+    int kblocks;                  // kRowGroups: 128-element K-blocks of the contraction
+    int b_group_rows;             // kRowGroups: B rows per group
+    int out_rows;                 // kTokenGroups: output rows per group (the A rows)
+    int rows_total;               // kRowGroups: off[num_groups] must equal this
+    int tcap;                     // kTokenGroups: padded tokens available in the operands
+    int64_t sb_group_stride;      // kRowGroups: floats between consecutive groups' B scales
+    int64_t out_group_stride;     // kTokenGroups: elements between consecutive groups' outputs
+    const int32_t* off_dev;       // device offsets (num_groups + 1), or null
+    int32_t off[kMaxGroups + 1];  // host offsets (used when off_dev is null)
     const float* sa;              // A scale of (row, kb): sa[(sa_kb0 + kb) * sa_ld + row]
     int64_t sa_ld;
     int32_t sa_rows;              // rows that may be read from sa
@@ -130,8 +145,11 @@ enum class GemmKind {
 
 // map_out: the BF16 output [rows x out_ld] (box 64 x 32, 128-byte swizzle),
 // used when p.tma_store is set.
+// max_units: an upper bound on the work units (tiles x splits), which
+// sizes the persistent grid when the offsets live on the device.
 cudaError_t launch_gemm(GemmKind kind, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                        const CUtensorMap& map_out, const GemmParams& p, int num_sms, cudaStream_t stream);
+                        const CUtensorMap& map_out, const GemmParams& p, int64_t max_units, int num_sms,
+                        cudaStream_t stream);
 
 // GEMM tile shape and pipeline depth (exported for host-side planning).
 constexpr int kBM = 128;

@@ -666,6 +666,56 @@ __device__ __forceinline__ int find_group(const int32_t* tile_start, int ng, int
     return lo;
 }
 
+// Group of padded token tile `tile` from device offsets (all threads of the
+// CTA call it; it ends with a CTA barrier, after which `scratch`, 2 KB of
+// shared memory, may be reused). Returns false when the tile lies past the
+// groups' padded total, or when the offsets are invalid (off[0] != 0, a
+// decrease, a total other than p.rows), which CTA (0, 0) records as
+// FP8BS_ERR_DEVICE.
+__device__ bool device_group(const RequantParams& p, int tile, int32_t* scratch, int& g, int64_t& r0, int& len)
+{
+    const int G = p.num_groups;
+    int32_t* off = scratch;                    // G + 1 offsets
+    int32_t* wsum = scratch + kMaxGroups + 1;  // per-warp tile sums
+    int32_t* found = wsum + 8;                 // group of this tile, its first tile
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    for (int i = t; i <= G; i += blockDim.x) off[i] = __ldg(p.off_dev + i);
+    if (t == 0) *found = -1;
+    __syncthreads();
+    int bad = 0, cnt = 0;
+    if (t < G) {
+        const int n = off[t + 1] - off[t];
+        if (n < 0) bad = 1;
+        cnt = n < 0 ? 0 : (n + 127) / 128;
+    }
+    if (t == 0 && (off[0] != 0 || static_cast<int64_t>(off[G]) != p.rows)) bad = 1;
+    int inc = cnt;   // inclusive scan of the tile counts over the CTA (one group per thread)
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+        if (lane >= d) inc += v;
+    }
+    if (lane == 31) wsum[warp] = inc;
+    __syncthreads();
+    for (int w = 0; w < warp; ++w) inc += wsum[w];
+    const int start = inc - cnt;
+    if (t < G && cnt > 0 && start <= tile && tile < inc) {
+        found[0] = t;
+        found[1] = start;
+    }
+    bad = __syncthreads_or(bad);
+    const int fg = found[0], s0 = found[1];
+    bool ok = !bad && fg >= 0;
+    if (ok) {
+        g = fg;
+        r0 = static_cast<int64_t>(off[g]) + static_cast<int64_t>(tile - s0) * 128;
+        len = static_cast<int>(min(static_cast<int64_t>(128), static_cast<int64_t>(off[g + 1]) - r0));
+    }
+    if (bad && t == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicCAS(p.status, 0u, (unsigned)FP8BS_ERR_DEVICE);
+    __syncthreads();
+    return ok;
+}
+
 // kDual: also the 1x128 cast of the same BF16 rows (p.q, p.q_scales).
 // kStash (with kDual): the transposed cast is taken from that E4M3 result
 // (decoded with its row scale, as the E4M3 source mode does) instead of
@@ -687,9 +737,16 @@ __global__ void __launch_bounds__(kQ3Threads, kSR ? 2 : (kStash ? 3 : 4)) requan
 
     const int tile = blockIdx.x;                 // padded token tile
     const int64_t c0 = (int64_t)blockIdx.y * 128;
-    const int g = find_group(p.tile_start, p.num_groups, tile);
-    const int64_t r0 = (int64_t)p.off[g] + (int64_t)(tile - p.tile_start[g]) * 128;
-    const int len = (int)min((int64_t)128, (int64_t)p.off[g + 1] - r0);
+    int g;
+    int64_t r0;
+    int len;
+    if (p.off_dev) {
+        if (!device_group(p, tile, reinterpret_cast<int32_t*>(stage), g, r0, len)) return;
+    } else {
+        g = find_group(p.tile_start, p.num_groups, tile);
+        r0 = (int64_t)p.off[g] + (int64_t)(tile - p.tile_start[g]) * 128;
+        len = (int)min((int64_t)128, (int64_t)p.off[g + 1] - r0);
+    }
     const int nch = (int)min((int64_t)128, p.cols - c0);
 
     if (p.mode == FP8BS_SRC_BF16) {

@@ -10,8 +10,15 @@
 //
 // Set-up: the first call on each device (with that device current) looks up
 // the array's device address with cudaGetSymbolAddress and keeps it; later
-// calls on that device reuse it. Make that first call before any stream
-// capture begins.
+// calls on that device reuse it. With lazy module loading that lookup is also
+// when the library's module, and with it the array, is loaded onto the
+// device, so make that first call before any stream capture begins. The
+// array is device memory that every process loading the library holds on
+// each device where the module is loaded, whether or not it calls this entry
+// point. Every call must be made with the device of `stream` current (the
+// call checks this and returns FP8BS_ERR_ARG otherwise). The kept address
+// does not survive cudaDeviceReset: a process that resets a device must not
+// call this entry point on it afterwards.
 //
 // Limits and sharing: the scratch holds kScratchBytes (32 MiB); a request
 // whose fp8bs_splitk_workspace_size exceeds that is rejected with
@@ -64,6 +71,14 @@ fp8bs_status fp8_block_gemm_splitk_noalloc(int op, const uint8_t* a, const float
     if (op != FP8BS_OP_FPROP && op != FP8BS_OP_DGRAD) return FP8BS_ERR_ARG;
     if (M < 0 || N <= 0 || K <= 0 || splits < 1) return FP8BS_ERR_ARG;
     if (fp8bs_splitk_workspace_size(op, M, N, K, splits) > kScratchBytes) return FP8BS_ERR_SHAPE;
+    if (stream) {
+        // the scratch address is the current device's: the stream must belong to it
+        int cur = 0, sdev = 0;
+        if (cudaGetDevice(&cur) != cudaSuccess ||
+            cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev) != cudaSuccess)
+            return FP8BS_ERR_ARG;
+        if (sdev != cur) return FP8BS_ERR_ARG;
+    }
     void* scratch = nullptr;
     const fp8bs_status s = scratch_pointer(&scratch);
     if (s != FP8BS_OK) return s;

@@ -29,7 +29,8 @@
  *     NULL is the legacy default stream). The returned status covers argument
  *     validation and launch errors only. Errors detected on the device (a
  *     bounded pipeline wait that gave up) are recorded in a per-device status
- *     word read by fp8bs_device_status().
+ *     word read by fp8bs_device_status(), fp8bs_last_device_status(stream) or
+ *     fp8bs_copy_device_status().
  *   - Matrices are row-major. "ld" arguments are row strides in elements.
  *   - BF16 data is passed as `const void*` (IEEE bfloat16 bit patterns), E4M3
  *     payloads as `uint8_t*` (OCP E4M3, "fn" variant: max 448, no infinities).
@@ -101,6 +102,14 @@ FP8BS_API int64_t fp8bs_scale_ld(int64_t rows);
  * (or groups == 0) the whole `rows` is one group. Returns -1 for invalid
  * offsets. */
 FP8BS_API int64_t fp8bs_padded_tokens(int64_t rows, const int32_t* group_offsets_host, int32_t groups);
+
+/* The largest value fp8bs_padded_tokens can take for `groups` groups holding
+ * `rows` tokens in total, whatever the split: with k = min(groups, rows)
+ * (the most groups that can be non-empty), 128 * floor((rows + 127 k) / 128),
+ * and rows rounded up to 128 when k <= 1. The token length of the transposed
+ * outputs of the _dev casts and of grouped Wgrad operands with device offsets.
+ * Returns -1 for rows < 0 or groups outside [0, FP8BS_MAX_GROUPS]. */
+FP8BS_API int64_t fp8bs_padded_tokens_max(int64_t rows, int32_t groups);
 
 /* ------------------------------------------------------------------------ */
 /* S1. 1x128 activation / gradient quantizer                                 */
@@ -240,6 +249,31 @@ FP8BS_API fp8bs_status fp8_quant_dual_stash_opts(const void* x, int64_t rows, in
                                                  const int32_t* group_offsets_host, int32_t groups,
                                                  uint8_t* q, float* scales, uint8_t* qT, float* scalesT,
                                                  const fp8bs_scale_opts* opts, void* stream);
+
+/* The transposed cast, the dual cast and the fused forward cast (above) with
+ * DEVICE group offsets: offsets_dev (4-byte aligned, groups + 1 entries,
+ * 1 <= groups <= FP8BS_MAX_GROUPS) is read by the kernel when it runs, so it
+ * may come from earlier device work on the same stream and the call may be
+ * captured in a CUDA graph. The outputs are laid out as with host offsets
+ * except that qT is [cols x Mcap] and scalesT [Mcap/128 x cols] with
+ * Mcap = fp8bs_padded_tokens_max(rows, groups): group g still starts at the
+ * padded column P_g (the sum of the earlier groups' padded counts); columns
+ * past the groups' padded total are not written. Invalid device offsets
+ * (offsets[0] != 0, a decrease, a total other than rows) record
+ * FP8BS_ERR_DEVICE in the device status word and nothing is written. opts as
+ * for the _opts calls (NULL: the plain rule). */
+FP8BS_API fp8bs_status fp8_requant_128x1_T_dev(int src_mode, const void* src, const float* src_scales,
+                                               int64_t rows, int64_t cols, const int32_t* offsets_dev,
+                                               int32_t groups, uint8_t* qT, float* scalesT,
+                                               const fp8bs_scale_opts* opts, void* stream);
+FP8BS_API fp8bs_status fp8_quant_dual_dev(const void* x, int64_t rows, int64_t cols, const int32_t* offsets_dev,
+                                          int32_t groups, uint8_t* q, float* scales, uint8_t* qT,
+                                          float* scalesT, const fp8bs_scale_opts* opts, void* stream);
+FP8BS_API fp8bs_status fp8_quant_dual_stash_dev(const void* x, int64_t rows, int64_t cols,
+                                                const int32_t* offsets_dev, int32_t groups, uint8_t* q,
+                                                float* scales, uint8_t* qT, float* scalesT,
+                                                const fp8bs_scale_opts* opts, void* stream);
+
 
 /* NEXT-3: stochastic rounding. The 1x128 and 128x128 casts above with the   */
 /* E4M3 rounding step made stochastic under a stateless (seed, salt,         */
@@ -388,8 +422,16 @@ FP8BS_API fp8bs_status fp8_block_gemm_splitk(int op, const uint8_t* a, const flo
 /*   FP8BS_ERR_SHAPE before any work; lower `splits` or use                  */
 /*   fp8_block_gemm_splitk with a workspace.                                  */
 /* - The first call on each device (with that device current) does a one-    */
-/*   time set-up (it looks up the array's device address); make that first   */
-/*   call before any stream capture begins.                                   */
+/*   time set-up (it looks up the array's device address; under lazy module  */
+/*   loading this is also when the array is placed on the device); make that  */
+/*   first call before any stream capture begins.                             */
+/* - Every call must be made with the device of `stream` current             */
+/*   (FP8BS_ERR_ARG otherwise), like the set-up call.                         */
+/* - The array is device memory held on every device where the library's     */
+/*   module is loaded, by every process that loads the library, whether or   */
+/*   not it calls this entry point, until the process exits.                 */
+/* - The looked-up address does not survive cudaDeviceReset; do not call this */
+/*   entry point on a device after resetting it.                             */
 /* - One array serves all calls on a device: calls whose executions overlap   */
 /*   (different streams without ordering, several host threads) race on it    */
 /*   and give undefined results. Serialize them (one stream, or events).      */
@@ -515,12 +557,27 @@ FP8BS_API fp8bs_status fp8_quant_dual_stash_packed(const void* x, int64_t rows, 
 /* ------------------------------------------------------------------------ */
 /* S7. Grouped (MoE expert) GEMMs                                             */
 /* The dense definitions above applied to each group (expert) g, whose token  */
-/* rows are [offsets[g], offsets[g+1]) (HOST int32 array, groups + 1 entries, */
-/* offsets[0] = 0, non-decreasing). Empty groups are allowed: they produce no */
-/* rows (Fprop, Dgrad) or a zero weight gradient (Wgrad).                     */
+/* rows are [offsets[g], offsets[g+1]) (int32, groups + 1 entries,            */
+/* offsets[0] = 0, non-decreasing, offsets[groups] = rows). Empty groups are  */
+/* allowed: they produce no rows (Fprop, Dgrad) or a zero weight gradient     */
+/* (Wgrad). [P1] bullet 1 (the same recipe for every linear); the MoE form is */
+/* the grouped-GEMM path of TransformerEngine PR #3573 ("Changes": grouped    */
+/* predicates and per-group paths) and prime-rl PR #4073 ("Tests": grouped    */
+/* operators with empty experts).                                             */
 /* ------------------------------------------------------------------------ */
-/* op = FP8BS_OP_FPROP:
- *   a  = Xq [M x K] (M = offsets[groups]), sa its 1x128 scales;
+/* offsets_dev / offsets_host: exactly one is non-NULL (FP8BS_ERR_ARG otherwise).
+ *   offsets_host: a HOST array; the call plans the exact tile grid on the host.
+ *   offsets_dev : a DEVICE array (4-byte aligned) that the kernel reads when it
+ *     runs, so the offsets may be produced on the device by earlier work on the
+ *     same stream (a router) and the call can be captured in a CUDA graph whose
+ *     routing changes between replays. The grid then covers the largest tile
+ *     count any split of `rows` can need; invalid device offsets (offsets[0] != 0,
+ *     a decrease, a total other than rows) record FP8BS_ERR_DEVICE in the device
+ *     status word and the kernel writes nothing.
+ * rows: total token rows M (the A rows for Fprop / Dgrad; the tokens the
+ *   transposed casts were given for Wgrad).
+ * op = FP8BS_OP_FPROP:
+ *   a  = Xq [M x K], sa its 1x128 scales;
  *   b  = stacked WqT [groups x N x K], sb = stacked sw [groups x K/128 x N/128];
  *   out = Y BF16 [M x N].
  * op = FP8BS_OP_DGRAD (N is the contraction, K the output width):
@@ -528,23 +585,44 @@ FP8BS_API fp8bs_status fp8_quant_dual_stash_packed(const void* x, int64_t rows, 
  *   b  = stacked Wq [groups x K x N], sb = stacked sw [groups x K/128 x N/128];
  *   out = dX BF16 [M x K].
  * op = FP8BS_OP_WGRAD:
- *   a  = dYqT [N x Mpad], sa = sdyT [Mpad/128 x N]  (fp8_requant_128x1_T with
- *        the same offsets), b = XqT [K x Mpad], sb = sxT [Mpad/128 x K];
+ *   a  = dYqT [N x Mpad], sa = sdyT [Mpad/128 x N], b = XqT [K x Mpad],
+ *   sb = sxT [Mpad/128 x K] from the transposed casts with the same offsets:
+ *   Mpad = fp8bs_padded_tokens(rows, offsets_host, groups) with host offsets,
+ *   fp8bs_padded_tokens_max(rows, groups) with device offsets (the layout of
+ *   the _dev casts);
  *   out = dW FP32 [groups x N x K]; accumulate as in fp8_block_gemm_wgrad.
  * Constraints: 1 <= groups <= FP8BS_MAX_GROUPS, N % 128 == 0, K % 128 == 0. */
-FP8BS_API fp8bs_status fp8_block_gemm_grouped(int op, int32_t groups, const int32_t* offsets_host,
-                                    const uint8_t* a, const float* sa,
-                                    const uint8_t* b, const float* sb,
-                                    int64_t N, int64_t K, void* out, int accumulate,
-                                    void* stream);
+FP8BS_API fp8bs_status fp8_block_gemm_grouped(int op, int32_t groups, const int32_t* offsets_dev,
+                                              const int32_t* offsets_host, int64_t rows,
+                                              const uint8_t* a, const float* sa,
+                                              const uint8_t* b, const float* sb,
+                                              int64_t N, int64_t K, void* out, int accumulate,
+                                              void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Device status and failure detection                                       */
 /* ------------------------------------------------------------------------ */
 
-/* Synchronizes the current device, then returns the first device-side error
- * recorded since the last reset (FP8BS_OK if none). reset != 0 clears it. */
+/* The device status word: one per device, holding the first device-side error
+ * (FP8BS_ERR_TIMEOUT, FP8BS_ERR_DEVICE) any kernel of this library recorded on
+ * that device since the last reset; FP8BS_OK (0) if none. */
+
+/* Synchronizes the current device, then returns the status word. reset != 0
+ * clears it. */
 FP8BS_API fp8bs_status fp8bs_device_status(int reset);
+
+/* Stream-ordered read: enqueues a copy of the status word on `stream` (and,
+ * with reset != 0, its clearing after the copy), waits for that stream only
+ * (cudaStreamSynchronize, not the whole device) and returns the value, i.e.
+ * the status as of all work issued earlier on `stream`. Work on other streams
+ * keeps running. Not for use while `stream` is being captured. */
+FP8BS_API fp8bs_status fp8bs_last_device_status(void* stream, int reset);
+
+/* Asynchronous form for graphs and pipelines: enqueues on `stream` a 4-byte
+ * device-to-device copy of the status word into `dst` (a caller-owned DEVICE
+ * word, 4-byte aligned) and, with reset != 0, its clearing. Never waits; may
+ * be captured in a CUDA graph. */
+FP8BS_API fp8bs_status fp8bs_copy_device_status(unsigned int* dst, int reset, void* stream);
 
 /* Upper bound, in nanoseconds, on any single pipeline wait inside the GEMM
  * kernels (default 2e9). A wait that exceeds it records FP8BS_ERR_TIMEOUT,

@@ -58,6 +58,32 @@ def test_host_helpers(L):
         fp8bs.fp8bs_padded_tokens(10, [0, 5, 9])           # does not end at rows
 
 
+def test_padded_tokens_max_bounds_every_split():
+    """The capacity of the device-offset layouts: 128 floor((rows + 127 k) / 128)
+    with k = min(groups, rows) is at least the padded count of every split of
+    rows into groups, and reached by some split."""
+    g = np.random.default_rng(1)
+    assert fp8bs.fp8bs_padded_tokens_max(0, 32) == 0
+    assert fp8bs.fp8bs_padded_tokens_max(1, 32) == 128
+    assert fp8bs.fp8bs_padded_tokens_max(300, 1) == 384
+    assert fp8bs.fp8bs_padded_tokens_max(8192, 32) == 128 * ((8192 + 127 * 32) // 128)
+    with pytest.raises(ValueError):
+        fp8bs.fp8bs_padded_tokens_max(-1, 2)
+    for _ in range(200):
+        G = int(g.integers(1, 40))
+        rows = int(g.integers(0, 2000))
+        cap = fp8bs.fp8bs_padded_tokens_max(rows, G)
+        cuts = np.sort(g.integers(0, rows + 1, size=G - 1))
+        off = np.concatenate([[0], cuts, [rows]]).astype(np.int32)
+        assert fp8bs.fp8bs_padded_tokens(rows, off) <= cap
+    # reached: k - 1 groups of 1 token, the rest in the last group
+    for rows, G in ((1000, 8), (129, 4), (5, 9)):
+        k = min(G, rows)
+        counts = [1] * (k - 1) + [rows - (k - 1)] + [0] * (G - k)
+        off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+        assert fp8bs.fp8bs_padded_tokens(rows, off) == fp8bs.fp8bs_padded_tokens_max(rows, G)
+
+
 def test_padded_tokens_agrees_with_oracle_geometry():
     import oracle
     g = np.random.default_rng(0)
@@ -99,10 +125,28 @@ def test_argument_validation_before_device_work(L):
     assert L.fp8_block_gemm_wgrad(a16, a16, a16, a16, 100, 128, 128, a16, 0, None) == ERR_SHAPE
     assert L.fp8_block_gemm_wgrad(a16, a16, a16, a16, 128, 128, 128, None, 0, None) == ERR_ARG
     off = (ctypes.c_int32 * 3)(0, 4, 8)
-    assert L.fp8_block_gemm_grouped(9, 2, off, a16, a16, a16, a16, 128, 128, a16, 0, None) == ERR_ARG
-    assert L.fp8_block_gemm_grouped(0, 0, off, a16, a16, a16, a16, 128, 128, a16, 0, None) == ERR_ARG
-    assert L.fp8_block_gemm_grouped(0, 300, off, a16, a16, a16, a16, 128, 128, a16, 0, None) == ERR_ARG
-    assert L.fp8_block_gemm_grouped(0, 2, off, a16, a16, a16, a16, 128, 100, a16, 0, None) == ERR_SHAPE
+    # fp8_block_gemm_grouped(op, groups, offsets_dev, offsets_host, rows, a, sa, b, sb, N, K, out, acc, stream)
+    G = L.fp8_block_gemm_grouped
+    assert G(9, 2, None, off, 8, a16, a16, a16, a16, 128, 128, a16, 0, None) == ERR_ARG
+    assert G(0, 0, None, off, 8, a16, a16, a16, a16, 128, 128, a16, 0, None) == ERR_ARG
+    assert G(0, 300, None, off, 8, a16, a16, a16, a16, 128, 128, a16, 0, None) == ERR_ARG
+    assert G(0, 2, None, off, 8, a16, a16, a16, a16, 128, 100, a16, 0, None) == ERR_SHAPE
+    assert G(0, 2, None, off, 9, a16, a16, a16, a16, 128, 128, a16, 0, None) == ERR_ARG   # rows != off[2]
+    assert G(0, 2, a16, off, 8, a16, a16, a16, a16, 128, 128, a16, 0, None) == ERR_ARG    # both offsets
+    assert G(0, 2, None, None, 8, a16, a16, a16, a16, 128, 128, a16, 0, None) == ERR_ARG  # neither
+    assert G(0, 2, ctypes.c_void_p(a16.value + 2), None, 8, a16, a16, a16, a16, 128, 128, a16, 0,
+             None) == ERR_ALIGN
+    assert G(0, 2, a16, None, -1, a16, a16, a16, a16, 128, 128, a16, 0, None) == ERR_ARG
+    # casts with device offsets: offsets required, no host offsets, groups in range
+    R = L.fp8_requant_128x1_T_dev
+    assert R(0, a16, None, 8, 32, None, 2, a16, a16, None, None) == ERR_ARG
+    assert R(0, a16, None, 8, 32, a16, 0, a16, a16, None, None) == ERR_ARG
+    assert R(0, a16, None, 8, 32, a16, 300, a16, a16, None, None) == ERR_ARG
+    assert R(0, a16, None, 8, 32, ctypes.c_void_p(a16.value + 2), 2, a16, a16, None, None) == ERR_ALIGN
+    for f in (L.fp8_quant_dual_dev, L.fp8_quant_dual_stash_dev):
+        assert f(a16, 8, 32, None, 2, a16, a16, a16, a16, None, None) == ERR_ARG
+        assert f(a16, 8, 32, a16, 2, None, a16, a16, a16, None, None) == ERR_ARG
+        assert f(a16, 8, 24, a16, 2, a16, a16, a16, a16, None, None) == ERR_SHAPE
 
 
 def test_product_path_does_not_import_oracle():

@@ -1,9 +1,17 @@
-"""fp8_block_gemm_splitk_noalloc (split-K whose workspace is the library's
-fixed scratch array), called through the C ABI. Two calls in a row on the
-same operands each match fp8_block_gemm_splitk (caller workspace) within the
-GEMM tolerance |d| <= 2e-3 * sum_k |a_k b_k| + 1e-6 plus one BF16 ulp, and a
-request larger than the scratch is rejected before any work. The file sorts
-last so the test also runs after every other GPU test in the same process."""
+"""fp8_block_gemm_splitk_noalloc, called through the C ABI: the split-K GEMM
+whose range sums live in the library's fixed scratch array, for callers that
+cannot allocate device memory (an allocator-free runtime, a loop that must
+not call cudaMalloc because it may synchronize the device, a plugin without
+a memory pool).
+
+Two calls in a row on the same operands are each byte-identical to
+fp8_block_gemm_splitk with a caller workspace and the same split count, and
+within the GEMM tolerance |d| <= 2e-3 * sum_k |a_k b_k| + 1e-6 (plus one BF16
+ulp) of the oracle's promoted GEMM. Around a call after the first, neither
+torch's allocator nor the device's free memory changes. A request larger
+than the scratch is rejected with FP8BS_ERR_SHAPE before any work. The file
+sorts last so the test also runs after every other GPU test in the same
+process; it passes alone in a fresh process as well."""
 import ctypes
 
 import numpy as np
@@ -11,6 +19,7 @@ import pytest
 import torch
 
 import fp8_block_scaled_act_gb300 as fp8bs
+import oracle
 import workloads as wl
 from parity import assert_gemm_close, bf16_values, dequant_blocks, dequant_rows, np_
 
@@ -34,19 +43,27 @@ def _quantize(x, w):
     return xq, sx, wq, wqT, sw
 
 
-def _check_two_calls(op, a, sa, b, sb, out_shape, splits, absprod, what):
+def _check_two_calls(op, a, sa, b, sb, out_shape, splits, want, absprod, what):
     ref = torch.empty(out_shape, dtype=torch.bfloat16, device="cuda")
     fp8bs.fp8_block_gemm_splitk(op, a, sa, b, sb, ref, splits=splits)
     torch.cuda.synchronize()
-    r = bf16_values(ref)
+    ref_bits = np_(ref.view(torch.int16))
+    assert_gemm_close(bf16_values(ref), want, absprod, True, f"{what}, workspace call")
     for call in range(2):
         y = torch.full(out_shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+        torch.cuda.synchronize()
+        alloc0 = torch.cuda.memory_allocated()
+        free0, _ = torch.cuda.mem_get_info()
         fp8bs.fp8_block_gemm_splitk_noalloc(op, a, sa, b, sb, y, splits=splits)
         torch.cuda.synchronize()
-        assert_gemm_close(bf16_values(y), r, absprod, True, f"{what}, call {call + 1}")
+        if call > 0:   # the first call on a device may load the module and look up the scratch
+            assert torch.cuda.memory_allocated() == alloc0, what
+            assert torch.cuda.mem_get_info()[0] == free0, what
+        assert np.array_equal(np_(y.view(torch.int16)), ref_bits), f"{what}, call {call + 1}"
+        assert_gemm_close(bf16_values(y), want, absprod, True, f"{what}, call {call + 1}")
 
 
-def test_noalloc_fprop_long_k_matches_workspace_call():
+def test_noalloc_fprop_long_k_matches_workspace_call_and_oracle():
     d = wl.longk(16384)
     xq, sx, wq, wqT, sw = _quantize(d["X"], d["W"])
     splits = fp8bs.fp8bs_splitk_default_splits(fp8bs.OP_FPROP, 256, 256, 16384)
@@ -54,16 +71,20 @@ def test_noalloc_fprop_long_k_matches_workspace_call():
     assert fp8bs.fp8bs_splitk_workspace_size(fp8bs.OP_FPROP, 256, 256, 16384, splits) <= fp8bs.NOALLOC_SCRATCH_BYTES
     a = np.abs(dequant_rows(np_(xq), np_(sx)))
     b = np.abs(dequant_blocks(np_(wq), np_(sw)))
-    _check_two_calls(fp8bs.OP_FPROP, xq, sx, wqT, sw, (256, 256), splits, a @ b, "noalloc fprop 256x16384x256")
+    want = oracle.fprop(np_(xq), np_(sx), np_(wq), np_(sw))
+    _check_two_calls(fp8bs.OP_FPROP, xq, sx, wqT, sw, (256, 256), splits, want, a @ b,
+                     "noalloc fprop 256x16384x256")
 
 
-def test_noalloc_dgrad_matches_workspace_call():
+def test_noalloc_dgrad_matches_workspace_call_and_oracle():
     dy = wl.with_outliers((300, 2048), fraction=0.01, seed=5)
     w = wl.normal((384, 2048), std=wl.W_STD, seed=6)
     dyq, sdy, wq, _, sw = _quantize(dy, w)
     a = np.abs(dequant_rows(np_(dyq), np_(sdy)))
     b = np.abs(dequant_blocks(np_(wq), np_(sw)))
-    _check_two_calls(fp8bs.OP_DGRAD, dyq, sdy, wq, sw, (300, 384), 8, a @ b.T, "noalloc dgrad 300x2048x384")
+    want = oracle.dgrad(np_(dyq), np_(sdy), np_(wq), np_(sw))
+    _check_two_calls(fp8bs.OP_DGRAD, dyq, sdy, wq, sw, (300, 384), 8, want, a @ b.T,
+                     "noalloc dgrad 300x2048x384")
 
 
 def test_noalloc_rejects_requests_larger_than_the_scratch():
@@ -77,5 +98,6 @@ def test_noalloc_rejects_requests_larger_than_the_scratch():
     xq, sx = fp8bs.empty_quant_1x128(M, K)
     wq, wqT, sw = fp8bs.empty_quant_128x128(K, N)
     y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(ValueError, match="fixed"):
+    with pytest.raises(fp8bs.Fp8bsError, match="fixed") as e:
         fp8bs.fp8_block_gemm_splitk_noalloc(fp8bs.OP_FPROP, xq, sx, wqT, sw, y, splits=splits)
+    assert e.value.code == 3
