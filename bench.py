@@ -5,10 +5,14 @@ synthetic input: the weight's 128x128 quantization (with its transposed
 copy), the 1x128 quantization of X, Fprop, the dual-orientation cast of dY
 (its 1x128 and 128x1 transposed quantizations from one read), Dgrad, the
 128x1 transposed requant of X from its E4M3 stash, and Wgrad. Default workload: X 4096x7168 (N(0,1) with 0.1% outliers),
-W 7168x2048 (N(0,0.02^2)), dY 4096x2048 (N(0,1e-3^2)). ``--workload moe``
-runs the grouped MoE expert pass instead (32 experts, 8192 routed rows);
-``--workload longk`` the 256 x K x 256 split-K Fprop of the long-contraction
-workload (K = 1024 ... 65536).
+W 7168x2048 (N(0,0.02^2)), dY 4096x2048 (N(0,1e-3^2)); its numbers are the
+line's headline keys. After it the default run times, each the same way and
+reported under its own key of ``configs``: the grouped MoE expert pass (32
+experts, 8192 routed rows, group offsets in device memory), the 256 x K x 256
+split-K Fprop of the long-contraction workload (K = 1024 ... 65536) and the
+standalone 1x128 cast of a 16384 x 16384 tensor (``--dense-only`` skips
+them). ``--workload moe|longk|quant16k|dense_ue8m0`` times one of those (or
+the dense step with power-of-two scales) as the headline instead.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -343,7 +347,10 @@ class MoeStep:
         import workloads as wl
         self.fp8bs, self.torch, self.dev = fp8bs, torch, device
         counts = wl.expert_counts(tokens, experts, seed=seed)
-        self.offsets = wl.offsets_from_counts(counts)
+        self.offsets_host = wl.offsets_from_counts(counts)
+        # the routing lives on the device: the grouped calls read it there, so
+        # the captured step needs no host copy of it
+        self.offsets = torch.tensor(self.offsets_host, dtype=torch.int32, device=device)
         self.counts = counts
         self.T, self.G, self.H, self.I, self.U = tokens, experts, hidden, inter, up
         g = torch.Generator(device=device)
@@ -373,7 +380,7 @@ class MoeStep:
     def work(self):
         T, G, H, I, U = self.T, self.G, self.H, self.I, self.U
         s_ld = (T + 3) // 4 * 4
-        mp = int(self.fp8bs.fp8bs_padded_tokens(T, self.offsets))
+        mp = int(self.fp8bs.fp8bs_padded_tokens(T, self.offsets_host))
         flops = {"grouped_fprop_up": 2.0 * T * H * U, "grouped_fprop_down": 2.0 * T * I * H,
                  "grouped_dgrad_down": 2.0 * T * H * I, "grouped_wgrad_down": 2.0 * T * H * I}
         b = {
@@ -404,7 +411,7 @@ class MoeStep:
             lambda: e.fp8_block_gemm_grouped(e.OP_DGRAD, off, self.dyq, self.sdy, self.wdq, self.swd,
                                              self.dA, H, I),
             lambda: e.fp8_block_gemm_grouped(e.OP_WGRAD, off, self.dyT, self.sdyT, self.aT, self.saT,
-                                             self.dWd, H, I),
+                                             self.dWd, H, I, rows=self.T),
         ]
 
     def io(self):
@@ -412,7 +419,8 @@ class MoeStep:
 
     def describe(self):
         return {"workload": (f"grouped MoE experts: {self.G} experts, {self.T} routed rows "
-                             f"(Dirichlet(0.5) counts), W_up {self.H}x{self.U}, W_down {self.I}x{self.H}"),
+                             f"(Dirichlet(0.5) counts), W_up {self.H}x{self.U}, W_down {self.I}x{self.H}; "
+                             "group offsets in device memory"),
                 "experts": self.G, "tokens": self.T, "hidden": self.H, "inter": self.I, "up": self.U}
 
 
@@ -477,31 +485,39 @@ class LongKStep:
                 "M": self.M, "N": self.N, "K": list(self.KS)}
 
 
-def run_ours(args, world, rank, local):
-    import torch
-    import fp8_block_scaled_act_gb300 as fp8bs
+class Quant1x128Step:
+    """The standalone 1x128 cast of the long-K workload's bandwidth case: a
+    16384 x 16384 BF16 N(0, 1) tensor to E4M3 with fp32 scales."""
 
-    fp8bs.build()
-    fp8bs.lib()
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    dist = init_dist(world, "nccl")
-    M, K, N = dense_shapes().values()
+    def __init__(self, fp8bs, torch, device, R=16384, C=16384, seed=0):
+        self.fp8bs, self.torch, self.dev = fp8bs, torch, device
+        self.R, self.C = R, C
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        self.X = torch.randn(R, C, device=device, generator=g).to(torch.bfloat16)
+        self.q, self.s = fp8bs.empty_quant_1x128(R, C, device)
+        self.names = [f"quant_1x128({R}x{C})"]
 
-    def make_step():
-        if args.workload == "moe":
-            return MoeStep(fp8bs, torch, device, seed=rank)
-        if args.workload == "longk":
-            return LongKStep(fp8bs, torch, device, seed=rank)
-        if args.workload == "dense_ue8m0":
-            return DenseUe8m0Step(fp8bs, torch, device, M, K, N, seed=rank)
-        return DenseStep(fp8bs, torch, device, M, K, N, seed=rank)
+    def work(self):
+        s_ld = (self.R + 3) // 4 * 4
+        return {}, {self.names[0]: self.R * self.C * 3 + 4 * (self.C // 128) * s_ld}
 
-    step = make_step()
+    def launches(self):
+        return [lambda: self.fp8bs.fp8_quant_1x128(self.X, self.q, self.s)]
+
+    def io(self):
+        return (self.X,), (self.q, self.s)
+
+    def describe(self):
+        return {"workload": f"standalone 1x128 cast of a {self.R}x{self.C} BF16 N(0,1) tensor",
+                "rows": self.R, "cols": self.C}
+
+
+def time_step(args, step, fp8bs, torch, dist, local, flush, stream):
+    """Warm-up, graph capture and K timed steps of one workload, then K more
+    steps launched kernel by kernel with an event after each (the kernels
+    table). Returns the step times, per-kernel times, clocks and launch mode."""
     launches = step.launches()
-    flops, kbytes = step.work()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-    stream = torch.cuda.current_stream()
 
     def run_seq():
         for f in launches:
@@ -534,8 +550,7 @@ def run_ours(args, world, rank, local):
         if fp8bs.fp8bs_device_status(reset=True) != 0:
             raise RuntimeError("device status error during graph warm-up")
 
-    nk = len(launches)                       # launch functions of a step (one per breakdown entry)
-    kernels_per_step = getattr(step, "kernels_per_step", nk)
+    nk = len(launches)
     # Timed region: exactly K steps with CUDA events at the step boundaries
     # only (an event between two kernels costs a few microseconds on this
     # GPU, ~25 us over the dense step's seven kernels).
@@ -573,10 +588,15 @@ def run_ours(args, world, rank, local):
         raise RuntimeError("device status error during the breakdown steps")
     kern_ms = {step.names[i]: [ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps)]
                for i in range(nk)}
-    total_s = max_over_ranks(dist, sum(step_ms) / 1e3, device=device)
-    step_flops = sum(flops.values())
-    value = whole_job_throughput(step_flops * args.steps, world, total_s) / 1e12
+    return {"step_ms": step_ms, "kern_ms": kern_ms, "clocks": clk, "launch_mode": launch_mode,
+            "kernels_per_step": getattr(step, "kernels_per_step", nk)}
 
+
+def summarize(step, t, total_s, steps, world):
+    """Throughput, kernels table, roofline of the dominant kernel and the
+    casts' aggregate bandwidth of one timed workload."""
+    flops, kbytes = step.work()
+    kern_ms = t["kern_ms"]
     peaks, peak_src = load_peaks()
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
     hbm_peak = peaks["hbm_gbs"]
@@ -605,36 +625,114 @@ def run_ours(args, world, rank, local):
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak,
                 "unit": "GB/s", "frac": round(ach / hbm_peak, 4), "traffic": traffic,
                 "peak_source": peak_src}
-
+    out = {"ms_per_step": round(total_s * 1e3 / steps, 5)}
+    step_flops = sum(flops.values())
+    if step_flops > 0:
+        value = whole_job_throughput(step_flops * steps, world, total_s) / 1e12
+        out.update(value=round(value, 2), unit=UNIT, gemm_frac_fp8_peak=round(value / fp8_peak, 4))
+    else:   # a cast-only workload: bandwidth
+        gbs = whole_job_throughput(sum(kbytes.values()) * steps, world, total_s) / 1e9
+        out.update(value=round(gbs, 1), unit="GB/s", frac_hbm=round(gbs / hbm_peak, 4))
     quant_names = [n for n in step.names if n not in flops]
-    q_bytes = sum(kbytes[n] for n in quant_names)
-    q_ms = sum(sum(kern_ms[n]) for n in quant_names) / args.steps
-    e2e = measure_e2e(args, fp8bs, torch, [step, make_step()], device, step_flops, world, dist)
+    if quant_names:
+        q_bytes = sum(kbytes[n] for n in quant_names)
+        q_ms = sum(sum(kern_ms[n]) for n in quant_names) / steps
+        out["quantize_gbs"] = round(q_bytes / (q_ms * 1e-3) / 1e9, 1)
+        out["quantize_frac_hbm"] = round(q_bytes / (q_ms * 1e-3) / 1e9 / hbm_peak, 4)
+    out.update(roofline=roof, kernels=kernels)
+    return out
+
+
+DATA = {"dense": "synthetic (seeded normal; 0.1% outliers in X)",
+        "moe": "synthetic (seeded normal; Dirichlet(0.5) expert counts)",
+        "longk": "synthetic (seeded uniform U(0.5, 1.5))",
+        "quant16k": "synthetic (seeded normal)",
+        "dense_ue8m0": "synthetic (seeded normal; 0.1% outliers in X)"}
+
+
+def make_workload(name, fp8bs, torch, device, rank):
+    M, K, N = dense_shapes().values()
+    if name == "moe":
+        return MoeStep(fp8bs, torch, device, seed=rank)
+    if name == "longk":
+        return LongKStep(fp8bs, torch, device, seed=rank)
+    if name == "quant16k":
+        return Quant1x128Step(fp8bs, torch, device, seed=rank)
+    if name == "dense_ue8m0":
+        return DenseUe8m0Step(fp8bs, torch, device, M, K, N, seed=rank)
+    return DenseStep(fp8bs, torch, device, M, K, N, seed=rank)
+
+
+# Workloads the default run times after the dense step, each reported under
+# its own key of "configs": the grouped MoE pass, the long-K sweep and the
+# standalone 16384 x 16384 1x128 cast.
+EXTRA_WORKLOADS = ("moe", "longk", "quant16k")
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import fp8_block_scaled_act_gb300 as fp8bs
+
+    fp8bs.build()
+    fp8bs.lib()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    M, K, N = dense_shapes().values()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    def make_step():
+        return make_workload(args.workload, fp8bs, torch, device, rank)
+
+    step = make_step()
+    t = time_step(args, step, fp8bs, torch, dist, local, flush, stream)
+    total_s = max_over_ranks(dist, sum(t["step_ms"]) / 1e3, device=device)
+    summ = summarize(step, t, total_s, args.steps, world)
+    flops, _ = step.work()
+    step_flops = sum(flops.values())
+    e2e = None
+    if step_flops > 0:
+        e2e = measure_e2e(args, fp8bs, torch, [step, make_step()], device, step_flops, world, dist)
 
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": summ["value"], "unit": summ["unit"], "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(total_s * 1e3 / args.steps, 5), "higher_is_better": True,
+        "ms_per_step": summ["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
-        "data": {"dense": "synthetic (seeded normal; 0.1% outliers in X)",
-                 "moe": "synthetic (seeded normal; Dirichlet(0.5) expert counts)",
-                 "longk": "synthetic (seeded uniform U(0.5, 1.5))",
-                 "dense_ue8m0": "synthetic (seeded normal; 0.1% outliers in X)"}[args.workload],
+        "data": DATA[args.workload],
         "config": dict(step.describe(),
                        parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
                        l2="flushed between steps (256 MiB write outside the step events)",
-                       launch=launch_mode),
-        "quantize_gbs": round(q_bytes / (q_ms * 1e-3) / 1e9, 1),
-        "quantize_frac_hbm": round(q_bytes / (q_ms * 1e-3) / 1e9 / hbm_peak, 4),
-        "gemm_frac_fp8_peak": round(value / fp8_peak, 4),
-        "roofline": roof, "kernels": kernels,
-        "kernels_note": ("per-kernel times from a second pass of the same K steps launched one kernel at a "
-                         "time on one stream with an event after every kernel (each includes one event's cost, "
-                         "a few us); ms_per_step and value come from the timed steps with events at step "
-                         "boundaries only"),
-        "e2e": e2e,
-        "gpu_launches": kernels_per_step * args.steps, "clocks": clk,
+                       launch=t["launch_mode"]),
     }
+    for k in ("quantize_gbs", "quantize_frac_hbm", "gemm_frac_fp8_peak", "frac_hbm", "roofline", "kernels"):
+        if k in summ:
+            line[k] = summ[k]
+    line["kernels_note"] = ("per-kernel times from a second pass of the same K steps launched one kernel at a "
+                            "time on one stream with an event after every kernel (each includes one event's "
+                            "cost, a few us); ms_per_step and value come from the timed steps with events at "
+                            "step boundaries only")
+    if e2e is not None:
+        line["e2e"] = e2e
+    line["gpu_launches"] = t["kernels_per_step"] * args.steps
+    line["clocks"] = t["clocks"]
+    del step
+    if args.workload == "dense" and not args.dense_only:
+        # the other configurations of the path, each timed the same way
+        configs = {}
+        for name in EXTRA_WORKLOADS:
+            st = make_workload(name, fp8bs, torch, device, rank)
+            te = time_step(args, st, fp8bs, torch, dist, local, flush, stream)
+            ts = max_over_ranks(dist, sum(te["step_ms"]) / 1e3, device=device)
+            c = {"config": st.describe(), "data": DATA[name], "launch": te["launch_mode"]}
+            c.update(summarize(st, te, ts, args.steps, world))
+            c["gpu_launches"] = te["kernels_per_step"] * args.steps
+            c["clocks"] = te["clocks"]
+            configs[name] = c
+            del st
+            torch.cuda.empty_cache()
+        line["configs"] = configs
     if rank == 0:
         if args.workload == "dense":
             line["cpu_baseline"] = cpu_baseline(M, K, N, args.cpu_baseline_sample)
@@ -977,7 +1075,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-graph", action="store_true",
                     help="time the step as stream launches instead of one CUDA graph replay")
-    ap.add_argument("--workload", choices=["dense", "moe", "longk", "dense_ue8m0"], default="dense",
+    ap.add_argument("--dense-only", action="store_true",
+                    help="time only the dense step (skip the MoE, long-K and 16384^2 cast configs)")
+    ap.add_argument("--workload", choices=["dense", "moe", "longk", "quant16k", "dense_ue8m0"], default="dense",
                     help="dense: the linear layer's fwd+bwd (default); moe: grouped expert pass; "
                          "longk: 256xKx256 split-K Fprop for K up to 65536; dense_ue8m0: the dense step "
                          "with power-of-two scales, GEMMs on the tensor core's block scaling")
