@@ -136,13 +136,27 @@ bool make_out_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows)
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D map over a BF16 cast source [rows x cols] with row pitch `row_bytes`
+// (a multiple of 16): box of 64 columns x 32 rows, 128-byte swizzle, zero
+// fill out of bounds.
+bool make_src_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes)
+{
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {64u, 32u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Tensor-map cache. Encoding a map is a driver call of a microsecond or
 // two; an eager caller repeats the same few (pointer, shape) pairs, so each
 // host thread keeps a small direct-mapped cache of encoded maps keyed by the
 // device and every argument of the encoding. A hit copies the 128-byte map.
 struct MapKey {
     int dev;
-    int kind;   // 0: E4M3 operand map, 1: BF16 output map
+    int kind;   // 0: E4M3 operand map, 1: BF16 output map, 2: BF16 cast source map
     const void* base;
     uint64_t inner, outer, row_bytes;
     uint32_t box_outer;
@@ -200,6 +214,23 @@ bool cached_out_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows)
         return true;
     }
     if (!make_out_map(m, base, cols, rows)) return false;
+    sl.used = true;
+    sl.key = k;
+    sl.map = *m;
+    return true;
+}
+
+bool cached_src_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const MapKey k{dev, 2, base, cols, rows, row_bytes, 32u};
+    MapSlot& sl = map_slot(k);
+    if (sl.used && sl.key == k) {
+        *m = sl.map;
+        return true;
+    }
+    if (!make_src_map(m, base, cols, rows, row_bytes)) return false;
     sl.used = true;
     sl.key = k;
     sl.map = *m;
@@ -462,6 +493,19 @@ fp8bs_status quant_1x128_common(const void* x, int64_t rows, int64_t cols, int64
     DeviceState* st = nullptr;
     fp8bs_status s = device_state(&st);
     if (s != FP8BS_OK) return s;
+    if (!sr && rows <= 0x7FFFFFFF && cols <= 0x7FFFFFFF) {
+        // round to nearest: the TMA-fed kernel (codes leave through a byte
+        // map with a box of 32 rows x 128 columns)
+        CUtensorMap map_x, map_q;
+        if (!cached_src_map(&map_x, x, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
+                            static_cast<uint64_t>(ldx) * 2) ||
+            !cached_map(&map_q, q, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
+                        static_cast<uint64_t>(cols), 32u))
+            return FP8BS_ERR_LAUNCH;
+        return launch_status(launch_quant_1x128_stream(map_x, map_q, rows, cols, scales, fp8bs_scale_ld(rows),
+                                                       rule, g_wait_limit_ns, st->status, st->num_sms,
+                                                       static_cast<cudaStream_t>(stream)));
+    }
     return launch_status(launch_quant_1x128(static_cast<const uint16_t*>(x), rows, cols, ldx, q,
                                             scales, fp8bs_scale_ld(rows), rule, sr, st->num_sms,
                                             static_cast<cudaStream_t>(stream)));

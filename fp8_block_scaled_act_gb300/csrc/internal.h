@@ -34,6 +34,16 @@ cudaError_t launch_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, in
                                uint8_t* q, float* scales, int64_t scale_ld, const ScaleRule& rule,
                                const SrParams* sr, int num_sms, cudaStream_t stream);
 
+// The round-to-nearest 1x128 cast fed by TMA: map_x is a BF16 map over the
+// source [rows x cols] (row pitch of the caller's leading dimension) with a
+// box of 64 columns x 32 rows, 128-byte swizzle, zero fill out of bounds;
+// map_q a byte map over the codes [rows x cols] with a box of 128 columns x
+// 32 rows, 128-byte swizzle. A load that does not land within limit_ns
+// records FP8BS_ERR_TIMEOUT in *status.
+cudaError_t launch_quant_1x128_stream(const CUtensorMap& map_x, const CUtensorMap& map_q, int64_t rows,
+                                      int64_t cols, float* scales, int64_t scale_ld, const ScaleRule& rule,
+                                      uint64_t limit, unsigned int* status, int num_sms, cudaStream_t stream);
+
 // atoms_wT / atoms_w (nullable; rows and cols multiples of 128): the MX
 // scale atoms of the two GEMM operands the weight feeds, W^T [cols x rows]
 // and W [rows x cols] (contraction along cols), per batch entry; a scale

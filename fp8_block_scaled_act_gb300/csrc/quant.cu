@@ -16,6 +16,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -346,6 +348,134 @@ __global__ void __launch_bounds__(kQ1Threads) quant_1x128_kernel(
             }
         }
     }
+}
+
+// ---------------------------------------------------------------------------
+// S1, streamed (round to nearest): the same tile recipe as
+// quant_1x128_kernel with lane = row. A persistent grid (one CTA of eight
+// warps per SM) walks 32-row x 128-column units; each warp keeps its next
+// units in flight in shared-memory slots of its own (two 64-column TMA boxes
+// per unit, 128-byte swizzled so that a lane reading its own row's 16-byte
+// chunks hits every bank once per eight lanes), copies a unit into
+// registers, refills the slot at once and then encodes. With one row per
+// lane the absmax, the scale and the reciprocal are per thread and the
+// whole row shares them: no shuffles. The codes go back through a per-warp
+// 4 KB stage (same swizzle) and leave with one TMA store per unit. Rows and
+// columns outside the tensor arrive as zeros (the load map's out-of-bounds
+// fill) and are not stored (the store map clips them).
+// ---------------------------------------------------------------------------
+constexpr int kQ1sWarps = 8;
+constexpr int kQ1sSlots = 3;
+constexpr int kQ1sUnitBytes = 32 * 128 * 2;
+constexpr int kQ1sOutBytes = 32 * 128;
+constexpr int kQ1sWarpBytes = kQ1sSlots * kQ1sUnitBytes + kQ1sOutBytes;
+constexpr uint64_t kQ1sDrainNs = 1000000000ull;
+
+__global__ void __launch_bounds__(kQ1sWarps * 32, 1) quant_1x128_stream_kernel(
+    const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_q, int64_t rows,
+    int64_t cols, float* __restrict__ scales, int64_t scale_ld, const ScaleRule rule, uint64_t limit,
+    unsigned int* status)
+{
+    extern __shared__ uint8_t q1s_smem_raw[];
+    __shared__ uint64_t full[kQ1sWarps][kQ1sSlots];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(q1s_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    uint8_t* wsm = smem + warp * kQ1sWarpBytes;              // the warp's slots, then its code stage
+    const uint32_t slots = smem_addr(wsm);
+    const uint32_t stage = slots + kQ1sSlots * kQ1sUnitBytes;
+    const uint32_t sw = static_cast<uint32_t>(lane & 7);     // 128-byte swizzle of this lane's row
+    const int64_t col_tiles = (cols + 127) / 128;
+    const int64_t units = col_tiles * ((rows + 31) / 32);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kQ1sWarps;
+    const int64_t first = static_cast<int64_t>(blockIdx.x) * kQ1sWarps + warp;
+
+    auto issue = [&](int64_t unit, int slot) {
+        const int64_t rg = unit / col_tiles;
+        const int64_t tc = unit - rg * col_tiles;
+        uint8_t* dst = wsm + slot * kQ1sUnitBytes;
+        mbar_arrive_expect_tx(&full[warp][slot], kQ1sUnitBytes);
+        tma_load_2d(dst, &map_x, &full[warp][slot], static_cast<int32_t>(tc * 128), static_cast<int32_t>(rg * 32));
+        tma_load_2d(dst + kQ1sUnitBytes / 2, &map_x, &full[warp][slot], static_cast<int32_t>(tc * 128 + 64),
+                    static_cast<int32_t>(rg * 32));
+    };
+    if (lane == 0) {
+        for (int j = 0; j < kQ1sSlots; ++j) mbar_init(&full[warp][j], 1);
+        fence_mbarrier_init();
+        if (warp == 0) {
+            tma_prefetch_desc(&map_x);
+            tma_prefetch_desc(&map_q);
+        }
+        for (int j = 0; j < kQ1sSlots; ++j)
+            if (first + j * stride < units) issue(first + j * stride, j);
+    }
+    __syncwarp();
+
+    int k = 0;
+    for (int64_t unit = first; unit < units; unit += stride, ++k) {
+        const int slot = k % kQ1sSlots;
+        if (!mbar_wait(&full[warp][slot], (k / kQ1sSlots) & 1, limit)) {
+            // a load did not land in time: record it, let every issued box
+            // land and every store finish before the CTA leaves, and stop
+            if (lane == 0) {
+                atomicCAS(status, 0u, static_cast<unsigned int>(FP8BS_ERR_TIMEOUT));
+                const uint64_t drain = limit > kQ1sDrainNs ? limit : kQ1sDrainNs;
+                for (int j = k; j < k + kQ1sSlots && first + j * stride < units; ++j)
+                    mbar_wait(&full[warp][j % kQ1sSlots], (j / kQ1sSlots) & 1, drain);
+                bulk_wait_group_all();
+            }
+            __syncwarp();
+            return;
+        }
+        const int64_t rg = unit / col_tiles;
+        const int64_t tc = unit - rg * col_tiles;
+        const int64_t row = rg * 32 + lane;
+
+        // this lane's row: chunk c of the first box (columns 8c .. 8c + 7)
+        // at slot + 128 lane + 16 (c ^ lane % 8), the second box 4 KB on
+        uint4 d[16];
+        const uint32_t rowp = slots + slot * kQ1sUnitBytes + lane * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            d[c] = ld_shared_v4(rowp + ((c ^ sw) << 4));
+            d[8 + c] = ld_shared_v4(rowp + kQ1sUnitBytes / 2 + ((c ^ sw) << 4));
+        }
+        // every lane has read the slot: refill it with the unit after next
+        __syncwarp();
+        if (lane == 0) {
+            const int64_t nxt = unit + kQ1sSlots * stride;
+            if (nxt < units) {
+                fence_proxy_async_smem();
+                issue(nxt, slot);
+            }
+        }
+
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m = max(m, absmax_bits_8(d[i]));
+        const TileScale ts = tile_scale(__uint_as_float(m << 16), rule);
+        if (row < rows) scales[tc * scale_ld + row] = ts.s;
+
+        // the previous unit's store has read the stage
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
+        const uint32_t outp = stage + lane * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint2 a = quant8(d[2 * j], ts);
+            const uint2 b = quant8(d[2 * j + 1], ts);
+            st_shared_v4(outp + ((j ^ sw) << 4), make_uint4(a.x, a.y, b.x, b.y));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(&map_q, stage, static_cast<int32_t>(tc * 128), static_cast<int32_t>(rg * 32));
+            bulk_commit_group();
+        }
+    }
+    // the warp's stores have completed before the CTA exits
+    if (lane == 0) bulk_wait_group_all();
 }
 
 // ---------------------------------------------------------------------------
@@ -1032,6 +1162,33 @@ cudaError_t launch_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, in
         quant_1x128_kernel<false><<<(unsigned)blocks, kQ1Threads, 0, stream>>>(x, rows, cols, ldx, q, scales,
                                                                               scale_ld, rule, SrKey{0, 0});
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_1x128_stream(const CUtensorMap& map_x, const CUtensorMap& map_q, int64_t rows,
+                                      int64_t cols, float* scales, int64_t scale_ld, const ScaleRule& rule,
+                                      uint64_t limit, unsigned int* status, int num_sms, cudaStream_t stream)
+{
+    if (rows == 0) return cudaSuccess;
+    constexpr int kSmem = kQ1sWarps * kQ1sWarpBytes + 1024;
+    static_assert(kSmem <= 227 * 1024, "shared memory");
+    // once per device: the shared-memory opt-in
+    static std::atomic<uint64_t> ready{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(ready.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(quant_1x128_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e != cudaSuccess) return e;
+        ready.fetch_or(bit, std::memory_order_release);
+    }
+    const int64_t units = ((cols + 127) / 128) * ((rows + 31) / 32);
+    const int64_t warps = (units + kQ1sSlots - 1) / kQ1sSlots;   // at least three units per warp when possible
+    int64_t blocks = (warps + kQ1sWarps - 1) / kQ1sWarps;
+    if (blocks > num_sms) blocks = num_sms;
+    quant_1x128_stream_kernel<<<static_cast<unsigned>(blocks), kQ1sWarps * 32, kSmem, stream>>>(
+        map_x, map_q, rows, cols, scales, scale_ld, rule, limit, status);
     return cudaGetLastError();
 }
 
