@@ -415,7 +415,13 @@ __global__ void __launch_bounds__(kQ1sWarps * 32, 1) quant_1x128_stream_kernel(
     int k = 0;
     for (int64_t unit = first; unit < units; unit += stride, ++k) {
         const int slot = k % kQ1sSlots;
-        if (!mbar_wait(&full[warp][slot], (k / kQ1sSlots) & 1, limit)) {
+        // lane 0 waits (bounded) and the warp follows its verdict; the other
+        // lanes then pass the completed phase themselves (acquire)
+        int landed = 0;
+        if (lane == 0) landed = mbar_wait(&full[warp][slot], (k / kQ1sSlots) & 1, limit) ? 1 : 0;
+        landed = __shfl_sync(0xFFFFFFFFu, landed, 0);
+        if (landed) mbar_try_wait(&full[warp][slot], (k / kQ1sSlots) & 1);
+        if (!landed) {
             // a load did not land in time: record it, let every issued box
             // land and every store finish before the CTA leaves, and stop
             if (lane == 0) {
