@@ -29,7 +29,7 @@ __all__ = [
     "fp8bs_splitk_default_splits", "fp8_block_gemm_splitk_noalloc", "NOALLOC_SCRATCH_BYTES",
     "fp8bs_device_status", "fp8bs_last_device_status", "fp8bs_copy_device_status", "fp8bs_set_wait_limit_ns",
     "fp8bs_padded_tokens_max", "fp8_requant_128x1_T_dev", "fp8_quant_dual_dev", "fp8_quant_dual_stash_dev",
-    "fp8bs_selftest_wait_timeout", "fp8bs_scale_ld", "fp8bs_padded_tokens",
+    "fp8bs_selftest_wait_timeout", "fp8bs_selftest_gemm_timeout", "fp8bs_scale_ld", "fp8bs_padded_tokens",
     "fp8bs_status_str", "fp8bs_version",
     "empty_quant_1x128", "empty_quant_128x128", "empty_requant_128x1_T",
     "SRC_BF16", "SRC_E4M3", "OP_FPROP", "OP_DGRAD", "OP_WGRAD", "MAX_GROUPS",
@@ -132,6 +132,7 @@ def lib() -> ctypes.CDLL:
         "fp8bs_device_status": ([I], S),
         "fp8bs_set_wait_limit_ns": ([ctypes.c_uint64], None),
         "fp8bs_selftest_wait_timeout": ([ctypes.c_uint64, P], S),
+        "fp8bs_selftest_gemm_timeout": ([P, P, P, P, I64, I64, I64, P, ctypes.c_uint64, P], S),
     }
     for name, (args, res) in sigs.items():
         f = getattr(L, name)
@@ -829,3 +830,17 @@ def fp8bs_set_wait_limit_ns(ns: int) -> None:
 def fp8bs_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
     _check("fp8bs_selftest_wait_timeout",
            lib().fp8bs_selftest_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+def fp8bs_selftest_gemm_timeout(xq, sx, wqT, sw, y, limit_ns: int, stream=None) -> None:
+    """fp8_block_gemm_fprop with the epilogue holding its buffers and every
+    wait bounded by limit_ns: records FP8BS_ERR_TIMEOUT (test hook)."""
+    for t, n, d in ((xq, "xq", torch.uint8), (sx, "sx", torch.float32), (wqT, "wqT", torch.uint8),
+                    (sw, "sw", torch.float32), (y, "y", torch.bfloat16)):
+        _need(t, d, n)
+    M, K = xq.shape
+    N = wqT.shape[0]
+    if wqT.shape != (N, K) or y.shape != (M, N):
+        raise ValueError("shape mismatch")
+    _check("fp8bs_selftest_gemm_timeout", lib().fp8bs_selftest_gemm_timeout(
+        _ptr(xq), _ptr(sx), _ptr(wqT), _ptr(sw), M, N, K, _ptr(y), int(limit_ns), _stream(stream)))

@@ -313,7 +313,7 @@ void copy_offsets(GemmParams& p, const Offsets& o)
 // workspace `ws`, followed by the reduction kernel.
 fp8bs_status run_rowwise_gemm(bool dgrad, const Offsets& o, const uint8_t* a, const float* sa, const uint8_t* b,
                               const float* sb, int64_t N, int64_t K, void* out, void* stream, int32_t splits = 1,
-                              float* ws = nullptr)
+                              float* ws = nullptr, uint64_t selftest_limit_ns = 0)
 {
     DeviceState* st = nullptr;
     fp8bs_status s = device_state(&st);
@@ -351,6 +351,10 @@ fp8bs_status run_rowwise_gemm(bool dgrad, const Offsets& o, const uint8_t* a, co
     p.out = out;
     p.out_ld = width;
     p.accumulate = 0;
+    if (selftest_limit_ns != 0) {   // fp8bs_selftest_gemm_timeout
+        p.hold_release = 1;
+        p.wait_limit_ns = selftest_limit_ns;
+    }
     int used = 1, kps = 1 << 30;
     if (splits > 1 && o.groups == 1) splitk_shape(contr / kBK, splits, used, kps);
     if (used > 1) {
@@ -1097,6 +1101,19 @@ fp8bs_status fp8bs_selftest_wait_timeout(uint64_t limit_ns, void* stream)
     fp8bs_status s = device_state(&st);
     if (s != FP8BS_OK) return s;
     return launch_status(launch_selftest_wait(st->status, limit_ns, static_cast<cudaStream_t>(stream)));
+}
+
+fp8bs_status fp8bs_selftest_gemm_timeout(const uint8_t* xq, const float* sx, const uint8_t* wqT, const float* sw,
+                                         int64_t M, int64_t N, int64_t K, void* y, uint64_t limit_ns, void* stream)
+{
+    if (M <= 0 || N <= 0 || K <= 0 || limit_ns == 0) return FP8BS_ERR_ARG;
+    if (K % 128 != 0 || N % 128 != 0 || M > 0x7FFFFF00 || K < 3 * 128) return FP8BS_ERR_SHAPE;
+    if (!xq || !sx || !wqT || !sw || !y) return FP8BS_ERR_ARG;
+    if (!aligned16(xq) || !aligned16(sx) || !aligned16(wqT) || !aligned16(sw) || !aligned16(y))
+        return FP8BS_ERR_ALIGN;
+    const int32_t off[2] = {0, static_cast<int32_t>(M)};
+    return run_rowwise_gemm(false, Offsets{off, nullptr, 1, M}, xq, sx, wqT, sw, N, K, y, stream, 1, nullptr,
+                            limit_ns);
 }
 
 }  // extern "C"

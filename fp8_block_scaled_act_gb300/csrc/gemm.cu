@@ -358,7 +358,7 @@ __device__ __forceinline__ bool epilogue_block_scale(const GemmParams& p, Shared
             // the partial is in registers: hand the TMEM buffer back
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
+            if (lane == 0 && !p.hold_release) mbar_arrive(&ctl->tempty[buf]);
             promote(3, rb);
         }
 
@@ -509,7 +509,7 @@ __device__ __forceinline__ bool epilogue_vector_scale(const GemmParams& p, Share
             tmem_ld_wait(rb);
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
+            if (lane == 0 && !p.hold_release) mbar_arrive(&ctl->tempty[buf]);
             promote(3, rb);
             // the slot's column scales have been read
             __syncwarp();

@@ -146,6 +146,11 @@ struct GemmParams {
     int64_t ws_split_stride;      // floats between consecutive ranges' slices
     uint64_t wait_limit_ns;
     unsigned int* status;
+    // Test hook (fp8bs_selftest_gemm_timeout only): the epilogue never hands
+    // a tensor-memory buffer back, so the MMA thread's wait for the third
+    // K-block's buffer can only give up, which exercises the bounded waits,
+    // the abort and the drain of a real GEMM without a fault.
+    int hold_release;
 };
 
 enum class GemmKind {

@@ -635,6 +635,19 @@ FP8BS_API void fp8bs_set_wait_limit_ns(uint64_t ns);
  * fault; the context stays usable. */
 FP8BS_API fp8bs_status fp8bs_selftest_wait_timeout(uint64_t limit_ns, void* stream);
 
+/* Runs fp8_block_gemm_fprop on the caller's operands (same arguments and
+ * checks; K >= 384, so that a tile needs a tensor-memory buffer a second
+ * time) with every wait bounded by limit_ns and with the promotion epilogue
+ * holding on to the buffers it has read: the MMA thread's wait for a buffer
+ * to come back can only give up. The GEMM then records FP8BS_ERR_TIMEOUT in
+ * the device status word, stops issuing, lets its copies and MMAs drain,
+ * frees its tensor memory and returns; y holds partial results. This
+ * exercises the timeout path of a real GEMM without a fault; the context
+ * stays usable. Test hook: not part of the computation. */
+FP8BS_API fp8bs_status fp8bs_selftest_gemm_timeout(const uint8_t* xq, const float* sx, const uint8_t* wqT,
+                                                   const float* sw, int64_t M, int64_t N, int64_t K, void* y,
+                                                   uint64_t limit_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
