@@ -206,3 +206,50 @@ def test_mx_wgrad_dense_sampled():
     ii, jj = sample_indices(2048, 7168, 4096, seed=5, tiles=((0, 0), (-1, -1)))
     ref, absprod = _mx_ref(oqa, oea, oqb, oeb, ii, jj)
     assert_gemm_close(np_(out)[ii, jj], ref, absprod, False, "mx dense wgrad")
+
+
+# ---------------------------------------------------------------------------
+# The tensor core's own accumulation over the whole contraction (config 5's
+# "unpromoted" counterpart on this GPU): the MX GEMM keeps one tensor-memory
+# accumulator over all of K, with the power-of-two block scales applied
+# inside the MMA, and no software promotion.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("K", wl.LONGK_VALUES)
+def test_hardware_accumulation_over_long_k(K):
+    """Long-K drift workload (X 256xK, W Kx256, U(0.5, 1.5): same-sign
+    products, so accumulation errors add up). Against the fp64 sum over the
+    dequantized MX operands, the FP32-output MX GEMM's relative error stays
+    within the worst-case bound of an fp32 accumulator over K positive terms,
+    (K - 1) 2^-24, whatever the order of the additions (E4M3 products and
+    power-of-two scalings are exact in fp32). The drift model of "FP8 动态量化
+    里的 partial sum 漂移", section 4, with a 14-bit accumulator (the oracle's
+    unpromoted sum of the 1x128 / 128x128 operands) drifts far past that
+    bound at long K; the hardware accumulator does not."""
+    d = wl.longk(K)
+    x, wt = d["X"], d["W"].t().contiguous()
+    qa, aa = mx_quant(x)
+    qb, ab = mx_quant(wt)
+    out = torch.empty((256, 256), dtype=torch.float32, device="cuda")
+    fp8bs.fp8_mx_gemm_f32(qa, aa, qb, ab, out)
+    torch.cuda.synchronize()
+    oqa, oea = oracle.mx_quant_1x32(u16(x))
+    oqb, oeb = oracle.mx_quant_1x32(u16(wt))
+    ii, jj = sample_indices(256, 256, 256, seed=K)
+    A = _dequant(oqa[np.unique(ii)], oea[np.unique(ii)])
+    B = _dequant(oqb[np.unique(jj)], oeb[np.unique(jj)])
+    ia = {r: n for n, r in enumerate(np.unique(ii))}
+    jb = {c: n for n, c in enumerate(np.unique(jj))}
+    truth = np.array([A[ia[i]] @ B[jb[j]] for i, j in zip(ii, jj)])
+    got = np_(out)[ii, jj].astype(np.float64)
+    rel_hw = np.abs(got - truth) / truth
+    assert rel_hw.max() <= (K - 1) * 2.0 ** -24, f"K={K}: hardware accumulation rel err {rel_hw.max():.3e}"
+    # the drift model's 14-bit unpromoted accumulation on the same workload
+    xq, sx = oracle.quant_1x128(u16(d["X"]))
+    wq, sw = oracle.quant_128x128(u16(d["W"]))
+    t64, u14 = oracle.fprop_reference_sums(xq, sx, wq, sw, ii[:64], jj[:64], m_bits=14)
+    rel_14 = np.abs(u14 - t64) / t64
+    print(f"K={K}: hardware fp32 accumulation max rel err {rel_hw.max():.3e} "
+          f"(bound {(K - 1) * 2.0 ** -24:.3e}); 14-bit unpromoted model {rel_14.max():.3e}")
+    if K >= 16384:
+        assert rel_14.max() > (K - 1) * 2.0 ** -24 > rel_hw.max()
