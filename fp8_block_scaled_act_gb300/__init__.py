@@ -39,6 +39,7 @@ __all__ = [
     "fp8_quant_dual_stash_sr",
     "fp8bs_mx_scale_bytes", "fp8_mx_quant_1x32", "fp8_mx_gemm", "empty_mx_quant",
     "fp8_mx_quant_1x32_T", "fp8_mx_gemm_f32", "empty_mx_quant_T", "fp8_pack_ue8m0",
+    "fp8_mx_gemm_grouped", "fp8_pack_ue8m0_grouped",
     "fp8_quant_128x128_packed", "fp8_quant_dual_packed", "fp8_quant_dual_stash_packed", "empty_mx_atoms",
 ]
 
@@ -109,6 +110,8 @@ def lib() -> ctypes.CDLL:
         "fp8_mx_quant_1x32": ([P, I64, I64, P, P, P], S),
         "fp8_mx_gemm": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_mx_gemm_f32": ([P, P, P, P, I64, I64, I64, P, P], S),
+        "fp8_mx_gemm_grouped": ([I, I32, P, P, I64, P, P, P, P, I64, I64, P, P], S),
+        "fp8_pack_ue8m0_grouped": ([P, I64, I64, I64, I32, P, P, P, P], S),
         "fp8_mx_quant_1x32_T": ([P, I64, I64, P, P, P], S),
         "fp8_pack_ue8m0": ([P, I64, I64, I32, I64, I64, P, P], S),
         "fp8_quant_128x128_packed": ([P, I64, I64, I64, I64, P, P, P, P, P, P, P], S),
@@ -727,6 +730,47 @@ def fp8_block_gemm_grouped(op: int, offsets, a, sa, b, sb, out, N: int, K: int,
     _check("fp8_block_gemm_grouped", lib().fp8_block_gemm_grouped(
         int(op), groups, dptr, hptr, int(rows), _ptr(a), _ptr(sa), _ptr(b),
         _ptr(sb), int(N), int(K), _ptr(out), int(bool(accumulate)), _stream(stream)))
+
+
+def _offsets_args(offsets, rows, default_rows):
+    """(device pointer, host pointer, groups, rows, keepalive) of an offsets argument."""
+    if _on_device(offsets):
+        dptr, groups = _offsets_dev(offsets)
+        if rows is None:
+            if default_rows is None:
+                raise ValueError("device offsets need rows (the total token count)")
+            rows = default_rows
+        return dptr, None, groups, int(rows), None
+    off = _offsets_host(offsets)
+    if rows is None:
+        rows = int(off[-1])
+    return None, off.ctypes.data_as(ctypes.c_void_p), off.size - 1, int(rows), off
+
+
+def fp8_mx_gemm_grouped(op: int, offsets, a, a_atoms, b, b_atoms, out, N: int, K: int, stream=None,
+                        rows: Optional[int] = None) -> None:
+    """Grouped (MoE) MX GEMM; see fp8bs.h for the operand and atom layouts of
+    each op. Offsets as in fp8_block_gemm_grouped (a CUDA tensor is read on
+    the device); rows defaults to a.shape[0] for Fprop / Dgrad."""
+    for t, n in ((a, "a"), (a_atoms, "a_atoms"), (b, "b"), (b_atoms, "b_atoms")):
+        _need(t, torch.uint8, n)
+    _need(out, torch.float32 if op == OP_WGRAD else torch.bfloat16, "out")
+    dptr, hptr, groups, rows, keep = _offsets_args(offsets, rows, None if op == OP_WGRAD else a.shape[0])
+    _check("fp8_mx_gemm_grouped", lib().fp8_mx_gemm_grouped(
+        int(op), groups, dptr, hptr, rows, _ptr(a), _ptr(a_atoms), _ptr(b), _ptr(b_atoms), int(N), int(K),
+        _ptr(out), _stream(stream)))
+    del keep
+
+
+def fp8_pack_ue8m0_grouped(scales, rows: int, K: int, offsets, atoms, stream=None) -> None:
+    """Exponent bytes of the 1x128 power-of-two scales [K/128 x scale_ld] of
+    grouped rows [rows x K] into the groups' tile layout of the MX atoms."""
+    _need(scales, torch.float32, "scales")
+    _need(atoms, torch.uint8, "atoms")
+    dptr, hptr, groups, rows, keep = _offsets_args(offsets, rows, rows)
+    _check("fp8_pack_ue8m0_grouped", lib().fp8_pack_ue8m0_grouped(
+        _ptr(scales), rows, int(K), int(scales.shape[1]), groups, dptr, hptr, _ptr(atoms), _stream(stream)))
+    del keep
 
 
 def _splitk_dims(op: int, a, b):

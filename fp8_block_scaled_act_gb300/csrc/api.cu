@@ -81,6 +81,9 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 fp8bs_status mx_gemm_common(const uint8_t* a, const uint8_t* a_scale_atoms, const uint8_t* b,
                             const uint8_t* b_scale_atoms, int64_t M, int64_t N, int64_t K, uint16_t* out_bf16,
                             float* out_f32, void* stream);
+fp8bs_status mx_gemm_grouped(int op, int32_t groups, const int32_t* offsets_dev, const int32_t* offsets_host,
+                             int64_t rows, const uint8_t* a, const uint8_t* a_atoms, const uint8_t* b,
+                             const uint8_t* b_atoms, int64_t N, int64_t K, void* out, void* stream);
 
 // The quantizer entry points with an optional stochastic-rounding key
 // (defined after the extern "C" wrappers).
@@ -896,10 +899,59 @@ fp8bs_status fp8_mx_gemm_f32(const uint8_t* a, const uint8_t* a_scale_atoms, con
     return mx_gemm_common(a, a_scale_atoms, b, b_scale_atoms, M, N, K, nullptr, out, stream);
 }
 
+fp8bs_status fp8_mx_gemm_grouped(int op, int32_t groups, const int32_t* offsets_dev, const int32_t* offsets_host,
+                                 int64_t rows, const uint8_t* a, const uint8_t* a_scale_atoms, const uint8_t* b,
+                                 const uint8_t* b_scale_atoms, int64_t N, int64_t K, void* out, void* stream)
+{
+    return mx_gemm_grouped(op, groups, offsets_dev, offsets_host, rows, a, a_scale_atoms, b, b_scale_atoms, N, K,
+                           out, stream);
+}
+
+fp8bs_status fp8_pack_ue8m0_grouped(const float* scales, int64_t rows, int64_t K, int64_t kb_stride,
+                                    int32_t groups, const int32_t* offsets_dev, const int32_t* offsets_host,
+                                    uint8_t* scale_atoms, void* stream)
+{
+    if (rows < 0 || K <= 0 || kb_stride < 0 || groups < 1 || groups > kMaxGroups) return FP8BS_ERR_ARG;
+    if ((offsets_dev == nullptr) == (offsets_host == nullptr)) return FP8BS_ERR_ARG;
+    if (K % 128 != 0 || rows > 0x7FFFFF00) return FP8BS_ERR_SHAPE;
+    if (offsets_dev && (reinterpret_cast<uintptr_t>(offsets_dev) & 3u) != 0) return FP8BS_ERR_ALIGN;
+    if (offsets_host && (!valid_offsets(offsets_host, groups) || offsets_host[groups] != rows))
+        return FP8BS_ERR_ARG;
+    const int64_t tiles = (offsets_dev ? padded_tokens_max(rows, groups) : padded_tokens(rows, offsets_host, groups)) / 128;
+    if (tiles == 0) return FP8BS_OK;
+    if (!scales || !scale_atoms) return FP8BS_ERR_ARG;
+    if (!aligned16(scale_atoms) || (reinterpret_cast<uintptr_t>(scales) & 3u) != 0) return FP8BS_ERR_ALIGN;
+    DeviceState* st = nullptr;
+    fp8bs_status s = device_state(&st);
+    if (s != FP8BS_OK) return s;
+    PackGroups pg;
+    std::memset(&pg, 0, sizeof(pg));
+    pg.num_groups = groups;
+    pg.rows_total = static_cast<int>(rows);
+    pg.off_dev = offsets_dev;
+    if (offsets_host)
+        for (int g = 0; g <= groups; ++g) pg.off[g] = offsets_host[g];
+    return launch_status(launch_pack_ue8m0_grouped(scales, K, kb_stride, pg, tiles, scale_atoms, st->status,
+                                                   st->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"
 
 namespace fp8bs {
 namespace {
+
+// The MX GEMM's output [rows x cols] (BF16 or FP32) as boxes of 32 rows x
+// 64 bytes (32 BF16 or 16 FP32 columns), 64-byte swizzle.
+bool make_mx_out_map(CUtensorMap* m, void* out, int64_t cols, int64_t rows, bool f32)
+{
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * (f32 ? 4 : 2)};
+    const cuuint32_t box[2] = {f32 ? 16u : 32u, 32u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return g_encode(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 fp8bs_status mx_gemm_common(const uint8_t* a, const uint8_t* a_scale_atoms, const uint8_t* b,
                             const uint8_t* b_scale_atoms, int64_t M, int64_t N, int64_t K, uint16_t* out_bf16,
@@ -919,23 +971,86 @@ fp8bs_status mx_gemm_common(const uint8_t* a, const uint8_t* a_scale_atoms, cons
     if (s != FP8BS_OK) return s;
     CUtensorMap ma, mb, mo;
     if (!make_map(&ma, a, K, M, K, kBM) || !make_map(&mb, b, K, N, K, kBN)) return FP8BS_ERR_ARG;
-    {
-        // the output as boxes of 32 rows x 64 bytes (32 BF16 or 16 FP32 columns), 64-byte swizzle
-        const bool f32 = out_bf16 == nullptr;
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * (f32 ? 4 : 2)};
-        const cuuint32_t box[2] = {f32 ? 16u : 32u, 32u};
-        const cuuint32_t estr[2] = {1u, 1u};
-        if (g_encode(&mo, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, dims,
-                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return FP8BS_ERR_ARG;
-    }
+    if (!make_mx_out_map(&mo, out, N, M, out_bf16 == nullptr)) return FP8BS_ERR_ARG;
+    MxGroups grp;
+    std::memset(&grp, 0, sizeof(grp));
+    grp.layout = kMxDense;
+    grp.kb_atoms_a = grp.kb_atoms_b = static_cast<int>(K / 128);
+    const int64_t tiles = ((M + kBM - 1) / kBM) * (N / kBN);
     return launch_status(launch_mx_gemm(ma, mb, &mo, a_scale_atoms, b_scale_atoms,
                                         static_cast<int>(M),
                                         static_cast<int>(N), static_cast<int>(K), out_bf16, out_f32,
-                                        g_wait_limit_ns, st->status, st->num_sms,
+                                        grp, tiles, g_wait_limit_ns, st->status, st->num_sms,
                                         static_cast<cudaStream_t>(stream)));
+}
+
+// Grouped MX GEMM (see fp8_mx_gemm_grouped in fp8bs.h).
+fp8bs_status mx_gemm_grouped(int op, int32_t groups, const int32_t* offsets_dev, const int32_t* offsets_host,
+                             int64_t rows, const uint8_t* a, const uint8_t* a_atoms, const uint8_t* b,
+                             const uint8_t* b_atoms, int64_t N, int64_t K, void* out, void* stream)
+{
+    if (op != FP8BS_OP_FPROP && op != FP8BS_OP_DGRAD && op != FP8BS_OP_WGRAD) return FP8BS_ERR_ARG;
+    if (groups < 1 || groups > kMaxGroups || rows < 0 || N <= 0 || K <= 0) return FP8BS_ERR_ARG;
+    if ((offsets_dev == nullptr) == (offsets_host == nullptr)) return FP8BS_ERR_ARG;
+    if (offsets_dev && (reinterpret_cast<uintptr_t>(offsets_dev) & 3u) != 0) return FP8BS_ERR_ALIGN;
+    if (offsets_host && (!valid_offsets(offsets_host, groups) || offsets_host[groups] != rows))
+        return FP8BS_ERR_ARG;
+    // contraction and output width of one group
+    const int64_t contr = op == FP8BS_OP_FPROP ? K : N;
+    const int64_t width = op == FP8BS_OP_FPROP ? N : K;
+    if (contr % 128 != 0 || width % 256 != 0 || rows > 0x7FFFFF00 || contr > 0x7FFFFFFF ||
+        width * groups > 0x7FFFFFFF || N * groups > 0x7FFFFFFF)
+        return FP8BS_ERR_SHAPE;
+    if (!out) return FP8BS_ERR_ARG;
+    DeviceState* st = nullptr;
+    fp8bs_status s = device_state(&st);
+    if (s != FP8BS_OK) return s;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const int64_t tpad = offsets_dev ? padded_tokens_max(rows, groups) : padded_tokens(rows, offsets_host, groups);
+    if (op == FP8BS_OP_WGRAD && tpad == 0) {   // no tokens: every group's dW is zero
+        if (!aligned16(out)) return FP8BS_ERR_ALIGN;
+        return launch_status(cudaMemsetAsync(out, 0, sizeof(float) * groups * N * K, cs));
+    }
+    if (op != FP8BS_OP_WGRAD && rows == 0) return FP8BS_OK;
+    if (!a || !a_atoms || !b || !b_atoms) return FP8BS_ERR_ARG;
+    if (!aligned16(a) || !aligned16(a_atoms) || !aligned16(b) || !aligned16(b_atoms) || !aligned16(out))
+        return FP8BS_ERR_ALIGN;
+    MxGroups grp;
+    std::memset(&grp, 0, sizeof(grp));
+    grp.num_groups = groups;
+    grp.off_dev = offsets_dev;
+    if (offsets_host)
+        for (int g = 0; g <= groups; ++g) grp.off[g] = offsets_host[g];
+    grp.rows_total = static_cast<int>(rows);
+    CUtensorMap ma, mb, mo;
+    if (op == FP8BS_OP_WGRAD) {
+        // a = dY^T [N x Tpad], b = X^T [K x Tpad]; out FP32 [groups x N x K]
+        if (tpad > 0x7FFFFFFF) return FP8BS_ERR_SHAPE;
+        if (!make_map(&ma, a, tpad, N, tpad, kBM) || !make_map(&mb, b, tpad, K, tpad, kBN) ||
+            !make_mx_out_map(&mo, out, K, groups * N, true))
+            return FP8BS_ERR_ARG;
+        grp.layout = kMxTokenGroups;
+        grp.out_rows = static_cast<int>(N);
+        grp.kb_atoms_a = grp.kb_atoms_b = static_cast<int>(tpad / 128);
+        grp.kb_cap = static_cast<int>(tpad / 128);
+        const int64_t tiles = static_cast<int64_t>(groups) * (N / kBM) * (K / kBN);
+        return launch_status(launch_mx_gemm(ma, mb, &mo, a_atoms, b_atoms, static_cast<int>(groups * N),
+                                            static_cast<int>(K), 0, nullptr, static_cast<float*>(out), grp, tiles,
+                                            g_wait_limit_ns, st->status, st->num_sms, cs));
+    }
+    // Fprop: a = Xq [rows x K], b = stacked WqT [groups x N x K]; Dgrad:
+    // a = dYq [rows x N], b = stacked Wq [groups x K x N]; out BF16 [rows x width]
+    if (!make_map(&ma, a, contr, rows, contr, kBM) || !make_map(&mb, b, contr, width * groups, contr, kBN) ||
+        !make_mx_out_map(&mo, out, width, rows, false))
+        return FP8BS_ERR_ARG;
+    grp.layout = kMxRowGroups;
+    grp.b_group_rows = static_cast<int>(width);
+    grp.kb_atoms_a = grp.kb_atoms_b = static_cast<int>(contr / 128);
+    const int64_t mtiles = tpad / 128;
+    return launch_status(launch_mx_gemm(ma, mb, &mo, a_atoms, b_atoms, static_cast<int>(rows),
+                                        static_cast<int>(width), static_cast<int>(contr),
+                                        static_cast<uint16_t*>(out), nullptr, grp, mtiles * (width / kBN),
+                                        g_wait_limit_ns, st->status, st->num_sms, cs));
 }
 
 }  // namespace

@@ -180,13 +180,59 @@ cudaError_t launch_mx_quant_1x32(const uint16_t* x, int64_t rows, int64_t cols, 
                                  int num_sms, cudaStream_t stream);
 cudaError_t launch_mx_quant_1x32_T(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* qT, uint8_t* atoms,
                                    cudaStream_t stream);
-// out (BF16) or out_f32 (FP32, when not null) [M x N]; map_out (nullable):
-// the BF16 output as boxes of 32 columns x 32 rows with the 64-byte swizzle,
-// through which whole 32-row boxes are stored with TMA.
+// Group layouts of the MX GEMM.
+//   kMxDense:       one problem; A atoms [ceil(M/128)][K/128], B atoms [N/128][K/128].
+//   kMxRowGroups:   Fprop / Dgrad of experts: group g owns A rows
+//                   [off[g], off[g+1]) and B rows [g * b_group_rows, + b_group_rows);
+//                   A's atoms are laid out by the groups' 128-row tiles in order
+//                   (tile t of all groups: atoms [t][K/128]), B's per group
+//                   [g][b_group_rows/128][K/128]; output rows = A rows.
+//   kMxTokenGroups: Wgrad of experts: A [out_rows x Tpad], B [N x Tpad] over
+//                   padded tokens (each group's tokens padded to 128, laid end
+//                   to end); group g contracts over its own K-blocks; its
+//                   output [out_rows x N] sits at rows g * out_rows of the output.
+enum MxLayout { kMxDense = 0, kMxRowGroups = 1, kMxTokenGroups = 2 };
+
+struct MxGroups {
+    int layout;                     // MxLayout
+    int num_groups;
+    const int32_t* off_dev;         // device offsets (num_groups + 1), or null
+    int32_t off[kMaxGroups + 1];    // host offsets (used when off_dev is null)
+    int rows_total;                 // grouped: off[num_groups] must equal this
+    int b_group_rows;               // row groups: B rows per group
+    int kb_atoms_a, kb_atoms_b;     // atoms per 128-row block along K, of A and of B
+    int out_rows;                   // token groups: output rows per group
+    int kb_cap;                     // token groups: padded K-blocks the operands hold
+};
+
+// out (BF16) or out_f32 (FP32, when not null) [M x N] (M = the output rows:
+// all tokens for row groups, groups x out_rows for token groups); map_out
+// (nullable): the output as boxes of 32 rows x 64 bytes with the 64-byte
+// swizzle, through which whole 32-row boxes are stored with TMA. K: the
+// contraction of one group (kMxDense, kMxRowGroups); unused for token groups.
+// grp: the group layout; max_tiles: an upper bound on the output tiles, which
+// sizes the persistent grid.
 cudaError_t launch_mx_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap* map_out,
                            const uint8_t* sfa, const uint8_t* sfb, int M, int N, int K, uint16_t* out,
-                           float* out_f32, uint64_t wait_limit_ns, unsigned int* status, int num_sms,
-                           cudaStream_t stream);
+                           float* out_f32, const MxGroups& grp, int64_t max_tiles, uint64_t wait_limit_ns,
+                           unsigned int* status, int num_sms, cudaStream_t stream);
+
+// Groups of a grouped packing: device offsets, or host offsets.
+struct PackGroups {
+    int num_groups;
+    int rows_total;                 // off[num_groups] must equal this
+    const int32_t* off_dev;         // device offsets (num_groups + 1), or null
+    int32_t off[kMaxGroups + 1];    // host offsets (used when off_dev is null)
+};
+
+// The exponent bytes of row-wise (1x128) power-of-two scales of grouped rows
+// [rows x K] into the MX scale atoms in the groups' tile layout (the A
+// operand of a grouped MX Fprop / Dgrad): scale of (row r, K-block b) at
+// scales[r + b * kb_stride]; atoms of tile t at [t][K/128]; tiles_cap: the
+// tile count the atom buffer holds.
+cudaError_t launch_pack_ue8m0_grouped(const float* scales, int64_t K, int64_t kb_stride, const PackGroups& pg,
+                                      int64_t tiles_cap, uint8_t* atoms, unsigned int* status, int num_sms,
+                                      cudaStream_t stream);
 
 // Exponent bytes of power-of-two block scales into the MX scale atoms of an
 // operand [rows x K] (mx.cu); non-representable scales record

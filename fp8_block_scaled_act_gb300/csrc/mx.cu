@@ -34,6 +34,7 @@
 // writes those scales into the atom layout).
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstring>
 
 #include "internal.h"
@@ -217,7 +218,7 @@ constexpr int kTmemCols = 512;                  // accumulator 256 + scale slots
 constexpr int kSfCol0 = kBN;                    // first scale column
 constexpr int kSfColsPerStage = 12;             // 4 (A) + 8 (B)
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
-constexpr int kCtlBytes = 256;
+constexpr int kCtlBytes = 2048;
 // Output stage: per epilogue warp one box of 32 rows x 64 bytes (32 BF16 or
 // 16 FP32 columns) in the 64-byte swizzle: 16-byte chunk c of row r at slot
 // c ^ ((r / 2) % 4), conflict-free for 32 lanes writing one row each.
@@ -237,11 +238,15 @@ struct MxCtl {
     uint64_t mma_done;
     uint32_t tmem_base;
     volatile int abort;
+    // groups: row groups, the first M-tile of each group (exclusive scan of
+    // their 128-row tiles); token groups, the first padded K-block of each
+    int32_t tstart[kMaxGroups + 1];
+    int32_t total_tiles;
 };
 
 struct MxParams {
-    const uint8_t* sfa;   // A scale atoms [ceil(M/128)][K/128][512]
-    const uint8_t* sfb;   // B scale atoms [N/128][K/128][512]
+    const uint8_t* sfa;   // A scale atoms (see MxGroups for the grouped layouts)
+    const uint8_t* sfb;   // B scale atoms
     int m_tiles, n_tiles, kblocks;
     int M, N;
     uint16_t* out;        // BF16 [M x N], or
@@ -249,7 +254,126 @@ struct MxParams {
     int tma_store;        // whole 32-row boxes leave through the output map
     uint64_t wait_limit_ns;
     unsigned int* status;
+    MxGroups grp;
 };
+
+// Where the tile's operands, scales and output rows are (all roles decode
+// the same tiles in the same order).
+struct MxTile {
+    int a_row, k0, b_row, nkb;     // TMA coordinates of A / B row 0 and K-block 0; K-blocks
+    int64_t sfa, sfb0, sfb1;       // byte offsets of K-block 0's atoms (then + 512 per K-block)
+    int out_row0, row_end;         // output-map row of the tile's row 0; rows from row_end on are not stored
+    int col0;                      // first output column
+};
+
+__device__ __forceinline__ int mx_group_off(const MxGroups& gp, int g)
+{
+    return gp.off_dev ? __ldg(gp.off_dev + g) : gp.off[g];
+}
+
+// Builds the group table (all threads take part; ends with a CTA barrier).
+// Invalid offsets (off[0] != 0, a decrease, a total other than rows, more
+// padded K-blocks than the operands hold) leave no tiles and record
+// FP8BS_ERR_DEVICE.
+__device__ void mx_build_tab(const MxParams& p, MxCtl* ctl)
+{
+    const MxGroups& gp = p.grp;
+    if (gp.layout == kMxDense) {
+        if (threadIdx.x == 0) ctl->total_tiles = p.m_tiles * p.n_tiles;
+        __syncthreads();
+        return;
+    }
+    const int G = gp.num_groups;
+    int bad = 0;
+    for (int g = threadIdx.x; g < G; g += blockDim.x) {
+        const int n = mx_group_off(gp, g + 1) - mx_group_off(gp, g);
+        if (n < 0) bad = 1;
+        ctl->tstart[g] = n < 0 ? 0 : (n + 127) / 128;
+    }
+    if (threadIdx.x == 0 && (mx_group_off(gp, 0) != 0 || mx_group_off(gp, G) != gp.rows_total)) bad = 1;
+    bad = __syncthreads_or(bad);
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const int per = (G + 31) / 32;
+        const int g0 = min(G, lane * per), g1 = min(G, g0 + per);
+        int sum = 0;
+        for (int g = g0; g < g1; ++g) sum += ctl->tstart[g];
+        int inc = sum;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+            if (lane >= d) inc += v;
+        }
+        int run = inc - sum;
+        for (int g = g0; g < g1; ++g) {
+            const int c = ctl->tstart[g];
+            ctl->tstart[g] = run;
+            run += c;
+        }
+        if (lane == 31) {
+            ctl->tstart[G] = inc;
+            const bool over = gp.layout == kMxTokenGroups && inc > gp.kb_cap;
+            const int total = gp.layout == kMxRowGroups ? inc * p.n_tiles : G * (gp.out_rows / kBM) * p.n_tiles;
+            ctl->total_tiles = (bad || over) ? 0 : total;
+            if ((bad || over) && blockIdx.x == 0) atomicCAS(p.status, 0u, static_cast<unsigned int>(FP8BS_ERR_DEVICE));
+        }
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ MxTile mx_tile(const MxParams& p, const MxCtl* ctl, int t)
+{
+    const MxGroups& gp = p.grp;
+    MxTile d;
+    if (gp.layout == kMxDense) {
+        const int mt = t / p.n_tiles, nt = t - mt * p.n_tiles;
+        d.a_row = mt * kBM;
+        d.k0 = 0;
+        d.b_row = nt * kBN;
+        d.nkb = p.kblocks;
+        d.sfa = static_cast<int64_t>(mt) * gp.kb_atoms_a * 512;
+        d.sfb0 = static_cast<int64_t>(2 * nt) * gp.kb_atoms_b * 512;
+        d.sfb1 = d.sfb0 + static_cast<int64_t>(gp.kb_atoms_b) * 512;
+        d.out_row0 = d.a_row;
+        d.row_end = p.M;
+        d.col0 = nt * kBN;
+    } else if (gp.layout == kMxRowGroups) {
+        const int lt = t / p.n_tiles, nt = t - lt * p.n_tiles;   // lt: M-tile over all groups
+        int lo = 0, hi = gp.num_groups - 1;                       // last g with tstart[g] <= lt
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (ctl->tstart[mid] <= lt) lo = mid; else hi = mid - 1;
+        }
+        const int g = lo, mt = lt - ctl->tstart[g];
+        const int o0 = mx_group_off(gp, g);
+        d.a_row = o0 + mt * kBM;
+        d.k0 = 0;
+        d.b_row = g * gp.b_group_rows + nt * kBN;
+        d.nkb = p.kblocks;
+        d.sfa = static_cast<int64_t>(lt) * gp.kb_atoms_a * 512;
+        d.sfb0 = (static_cast<int64_t>(g) * (gp.b_group_rows / 128) + 2 * nt) * gp.kb_atoms_b * 512;
+        d.sfb1 = d.sfb0 + static_cast<int64_t>(gp.kb_atoms_b) * 512;
+        d.out_row0 = d.a_row;
+        d.row_end = mx_group_off(gp, g + 1);
+        d.col0 = nt * kBN;
+    } else {
+        const int per = (gp.out_rows / kBM) * p.n_tiles;
+        const int g = t / per, local = t - g * per;
+        const int mt = local / p.n_tiles, nt = local - mt * p.n_tiles;
+        const int kb0 = ctl->tstart[g];
+        d.a_row = mt * kBM;
+        d.k0 = kb0 * kBK;
+        d.b_row = nt * kBN;
+        d.nkb = ctl->tstart[g + 1] - kb0;
+        d.sfa = (static_cast<int64_t>(mt) * gp.kb_atoms_a + kb0) * 512;
+        d.sfb0 = (static_cast<int64_t>(2 * nt) * gp.kb_atoms_b + kb0) * 512;
+        d.sfb1 = d.sfb0 + static_cast<int64_t>(gp.kb_atoms_b) * 512;
+        d.out_row0 = g * gp.out_rows + mt * kBM;
+        d.row_end = (g + 1) * gp.out_rows;
+        d.col0 = nt * kBN;
+    }
+    return d;
+}
 
 // Shared-memory descriptor of a scale atom (32 rows of 16 bytes, no swizzle;
 // 8-row core matrices 128 bytes apart).
@@ -317,7 +441,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int total = p.m_tiles * p.n_tiles;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -342,9 +465,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     tc_fence_after_sync();
+    mx_build_tab(p, ctl);
+    const int total = ctl->total_tiles;
     const uint32_t tmem_base = ctl->tmem_base;
     const uint64_t limit = p.wait_limit_ns;
-    const int64_t kb_atoms = p.kblocks;   // atoms per 128-row group along K
 
     if (warp < kFirstEpiWarp) setmaxnreg_dec<kProducerRegs>();
 
@@ -353,8 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const int mt = t / p.n_tiles, nt = t - (t / p.n_tiles) * p.n_tiles;
-                for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+                const MxTile d = mx_tile(p, ctl, t);
+                for (int kb = 0; kb < d.nkb; ++kb, ++it) {
                     const uint32_t s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1u;
                     if (ctl->abort || !mbar_wait(&ctl->empty[s], ph ^ 1u, limit)) {
@@ -362,14 +486,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&ctl->full[s], kABytes + kBBytes + kSfaBytes + kSfbBytes);
-                    tma_load_2d(sA + s * kABytes, &map_a, &ctl->full[s], kb * kBK, mt * kBM);
-                    tma_load_2d(sB + s * kBBytes, &map_b, &ctl->full[s], kb * kBK, nt * kBN);
-                    bulk_load(sSfa + s * kSfaBytes, p.sfa + (static_cast<int64_t>(mt) * kb_atoms + kb) * 512,
-                              kSfaBytes, &ctl->full[s]);
-                    bulk_load(sSfb + s * kSfbBytes, p.sfb + (static_cast<int64_t>(2 * nt) * kb_atoms + kb) * 512,
-                              512, &ctl->full[s]);
-                    bulk_load(sSfb + s * kSfbBytes + 512,
-                              p.sfb + (static_cast<int64_t>(2 * nt + 1) * kb_atoms + kb) * 512, 512, &ctl->full[s]);
+                    tma_load_2d(sA + s * kABytes, &map_a, &ctl->full[s], d.k0 + kb * kBK, d.a_row);
+                    tma_load_2d(sB + s * kBBytes, &map_b, &ctl->full[s], d.k0 + kb * kBK, d.b_row);
+                    bulk_load(sSfa + s * kSfaBytes, p.sfa + d.sfa + static_cast<int64_t>(kb) * 512, kSfaBytes,
+                              &ctl->full[s]);
+                    bulk_load(sSfb + s * kSfbBytes, p.sfb + d.sfb0 + static_cast<int64_t>(kb) * 512, 512,
+                              &ctl->full[s]);
+                    bulk_load(sSfb + s * kSfbBytes + 512, p.sfb + d.sfb1 + static_cast<int64_t>(kb) * 512, 512,
+                              &ctl->full[s]);
                 }
             }
             if (!ok) {
@@ -392,7 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+                const int nkb = mx_tile(p, ctl, t).nkb;   // a tile of an empty group issues no MMA
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const uint32_t s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1u;
                     if (ctl->abort || !mbar_wait(&ctl->sfull[s], ph, limit)) {
@@ -428,7 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+                const int nkb = mx_tile(p, ctl, t).nkb;
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const uint32_t s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1u;
                     if (ctl->abort || !mbar_wait(&ctl->full[s], ph, limit)) {
@@ -462,14 +588,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t tile_it = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tile_it) {
-            const int mt = t / p.n_tiles, nt = t - (t / p.n_tiles) * p.n_tiles;
+            const MxTile d = mx_tile(p, ctl, t);
             if (ctl->abort || !mbar_wait(&ctl->tfull, tile_it & 1u, limit)) {
                 ok = false;
                 break;
             }
             tc_fence_after_sync();
-            const int row = mt * kBM + quarter * 32 + lane;
-            const int col0 = nt * kBN + half * 128;
+            const int row0 = d.out_row0 + quarter * 32;           // first output row of this warp
+            const int row = row0 + lane;
+            const int col0 = d.col0 + half * 128;
+            if (d.nkb == 0) {
+                // a tile of an empty group: no MMA wrote the accumulator; its
+                // output is zero
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->tempty);
+                if (row < d.row_end) {
+                    if constexpr (kF32) {
+                        float4* y = reinterpret_cast<float4*>(p.out_f32 + static_cast<int64_t>(row) * p.N + col0);
+#pragma unroll
+                        for (int v = 0; v < 32; ++v) y[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    } else {
+                        uint4* y = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(row) * p.N + col0);
+#pragma unroll
+                        for (int v = 0; v < 16; ++v) y[v] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                continue;
+            }
             uint32_t ra[32], rb[32];
             if constexpr (kF32) {
                 // FP32 output: the whole 128-column row in registers, the
@@ -488,8 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->tempty);
-                const int row0 = mt * kBM + quarter * 32;
-                if (p.tma_store && row0 + 32 <= p.M && col0 < p.N) {
+                if (p.tma_store && row0 + 32 <= d.row_end && col0 < p.N) {
                     const uint32_t box = smem_addr(sOut) + ew * kOutBoxBytes;
                     auto put = [&](const uint32_t (&r)[32], int b) {
                         if (lane == 0) bulk_wait_group_read<0>();    // the previous box has been read
@@ -509,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     };
                     put(ra, 0); put(ra, 1); put(rb, 2); put(rb, 3);
                     put(rc, 4); put(rc, 5); put(rd, 6); put(rd, 7);
-                } else if (row < p.M && col0 < p.N) {
+                } else if (row < d.row_end && col0 < p.N) {
                     float4* y = reinterpret_cast<float4*>(p.out_f32 + static_cast<int64_t>(row) * p.N + col0);
                     auto put = [&](const uint32_t (&r)[32], int c) {
 #pragma unroll
@@ -544,8 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk[32 + i] = pack_bf16x2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));
                 pk[48 + i] = pack_bf16x2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1]));
             }
-            const int row0 = mt * kBM + quarter * 32;           // first row of this warp
-            if (p.tma_store && row0 + 32 <= p.M && col0 < p.N) {
+            if (p.tma_store && row0 + 32 <= d.row_end && col0 < p.N) {
                 // four boxes of 32 columns through the warp's stage, each
                 // leaving with one TMA store while the warp goes on
                 const uint32_t box = smem_addr(sOut) + ew * kOutBoxBytes;
@@ -565,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         bulk_commit_group();
                     }
                 }
-            } else if (row < p.M && col0 < p.N) {
+            } else if (row < d.row_end && col0 < p.N) {
                 uint4* y = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(row) * p.N + col0);
 #pragma unroll
                 for (int v = 0; v < 16; ++v) y[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
@@ -619,7 +763,80 @@ __global__ void __launch_bounds__(256) pack_ue8m0_kernel(const float* __restrict
     }
 }
 
+// Grouped rows (the A operand of a grouped MX Fprop / Dgrad): row l of
+// group g (source row off[g] + l) goes to row l % 128 of the group's tile
+// l / 128; tiles are numbered over the groups in order. One thread per
+// (tile row, K-block); rows of a group's last tile past its end get 127.
+__global__ void __launch_bounds__(256) pack_ue8m0_grouped_kernel(const float* __restrict__ scales, int64_t kblocks,
+                                                                 int64_t kb_stride, PackGroups pg, int64_t tiles_cap,
+                                                                 uint8_t* __restrict__ atoms, unsigned int* status)
+{
+    __shared__ int32_t off[kMaxGroups + 1];
+    __shared__ int32_t tstart[kMaxGroups + 1];
+    __shared__ int32_t wsum[8];
+    const int G = pg.num_groups, t = threadIdx.x;
+    for (int i = t; i <= G; i += blockDim.x) off[i] = pg.off_dev ? __ldg(pg.off_dev + i) : pg.off[i];
+    __syncthreads();
+    int bad = 0, cnt = 0;
+    if (t < G) {
+        const int n = off[t + 1] - off[t];
+        if (n < 0) bad = 1;
+        cnt = n < 0 ? 0 : (n + 127) / 128;
+    }
+    if (t == 0 && (off[0] != 0 || off[G] != pg.rows_total)) bad = 1;
+    int inc = cnt;   // inclusive scan of the tile counts (one group per thread)
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+        if ((t & 31) >= d) inc += v;
+    }
+    if ((t & 31) == 31) wsum[t >> 5] = inc;
+    __syncthreads();
+    for (int w = 0; w < (t >> 5); ++w) inc += wsum[w];
+    if (t < G) tstart[t] = inc - cnt;
+    if (t == G - 1) tstart[G] = inc;
+    bad = __syncthreads_or(bad);
+    if (bad || tstart[G] > tiles_cap) {
+        if (t == 0 && blockIdx.x == 0) atomicCAS(status, 0u, static_cast<unsigned int>(FP8BS_ERR_DEVICE));
+        return;
+    }
+    const int64_t n = static_cast<int64_t>(tstart[G]) * 128 * kblocks;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + t; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t kb = (i >> 7) % kblocks;
+        const int lt = static_cast<int>((i >> 7) / kblocks);
+        const int m = static_cast<int>(i & 127);
+        int lo = 0, hi = G - 1;   // last g with tstart[g] <= lt
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (tstart[mid] <= lt) lo = mid; else hi = mid - 1;
+        }
+        const int l = (lt - tstart[lo]) * 128 + m;
+        uint32_t E = 127u;   // padding rows: scale 1
+        if (l < off[lo + 1] - off[lo]) {
+            E = ue8m0_of(__ldg(scales + static_cast<int64_t>(off[lo] + l) + kb * kb_stride));
+            if (E == 255u) atomicCAS(status, 0u, static_cast<unsigned int>(FP8BS_ERR_DEVICE));
+        }
+        *reinterpret_cast<uint32_t*>(atoms + atom_offset(static_cast<int64_t>(lt) * 128 + m, kb, kblocks)) =
+            E * 0x01010101u;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_pack_ue8m0_grouped(const float* scales, int64_t K, int64_t kb_stride, const PackGroups& pg,
+                                      int64_t tiles_cap, uint8_t* atoms, unsigned int* status, int num_sms,
+                                      cudaStream_t stream)
+{
+    const int64_t n = tiles_cap * 128 * (K / 128);
+    if (n == 0) return cudaSuccess;
+    int64_t blocks = (n + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    pack_ue8m0_grouped_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(scales, K / 128, kb_stride, pg,
+                                                                                  tiles_cap, atoms, status);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_pack_ue8m0(const float* scales, int64_t rows, int64_t K, int row_block, int64_t row_stride,
                               int64_t kb_stride, uint8_t* atoms, unsigned int* status, int num_sms,
@@ -664,11 +881,13 @@ cudaError_t launch_mx_quant_1x32_T(const uint16_t* x, int64_t rows, int64_t cols
 
 cudaError_t launch_mx_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap* map_out,
                            const uint8_t* sfa, const uint8_t* sfb, int M, int N, int K, uint16_t* out,
-                           float* out_f32, uint64_t wait_limit_ns, unsigned int* status, int num_sms,
-                           cudaStream_t stream)
+                           float* out_f32, const MxGroups& grp, int64_t max_tiles, uint64_t wait_limit_ns,
+                           unsigned int* status, int num_sms, cudaStream_t stream)
 {
     static_assert(sizeof(MxCtl) <= kCtlBytes, "control block");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory");
     MxParams p;
+    std::memset(&p, 0, sizeof(p));
     p.sfa = sfa;
     p.sfb = sfb;
     p.m_tiles = (M + kBM - 1) / kBM;
@@ -679,21 +898,33 @@ cudaError_t launch_mx_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, c
     p.out = out;
     p.out_f32 = out_f32;
     p.tma_store = map_out != nullptr ? 1 : 0;
+    p.grp = grp;
     CUtensorMap mo;
     if (p.tma_store) mo = *map_out;
     else std::memset(&mo, 0, sizeof(mo));
     p.wait_limit_ns = wait_limit_ns;
     p.status = status;
-    const int total = p.m_tiles * p.n_tiles;
-    if (total == 0) return cudaSuccess;
+    if (max_tiles <= 0) return cudaSuccess;
     auto kernel = out_f32 != nullptr ? mx_gemm_kernel<true> : mx_gemm_kernel<false>;
-    cudaFuncAttributes attr;
-    cudaError_t e = cudaFuncGetAttributes(&attr, kernel);
+    // once per device and output type: the shared-memory opt-in, and a check
+    // that the launch allocation covers the setmaxnreg split
+    static std::atomic<uint64_t> ready[2];
+    const int var = out_f32 != nullptr ? 1 : 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (static_cast<uint32_t>(attr.numRegs) != kLaunchRegs) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    const int grid = total < num_sms ? total : num_sms;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(ready[var].load(std::memory_order_acquire) & bit)) {
+        cudaFuncAttributes attr;
+        e = cudaFuncGetAttributes(&attr, kernel);
+        if (e != cudaSuccess) return e;
+        if (128u * kProducerRegs + 256u * kEpilogueRegs > static_cast<uint32_t>(kThreads) * attr.numRegs)
+            return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        ready[var].fetch_or(bit, std::memory_order_release);
+    }
+    const int grid = max_tiles < num_sms ? static_cast<int>(max_tiles) : num_sms;
     kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_a, map_b, mo, p);
     return cudaGetLastError();
 }

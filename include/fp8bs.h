@@ -478,6 +478,40 @@ FP8BS_API fp8bs_status fp8_mx_gemm_f32(const uint8_t* a, const uint8_t* a_scale_
                                        const uint8_t* b, const uint8_t* b_scale_atoms,
                                        int64_t M, int64_t N, int64_t K, float* out, void* stream);
 
+/* NEXT-2 / NEXT-4 for experts: the MX GEMMs above applied to each group     */
+/* (expert) g, with the group offsets of fp8_block_gemm_grouped (exactly one */
+/* of offsets_dev / offsets_host; rows = the total token rows). The MoE form */
+/* is the grouped path of TransformerEngine PR #3573 ("Changes": grouped     */
+/* predicates and per-group paths; "Performance": MXFP8 at the DeepSeek-V3   */
+/* expert shapes).                                                           */
+/* op = FP8BS_OP_FPROP: a = Xq [rows x K]; b = stacked W^T codes            */
+/*   [groups x N x K]; out = Y BF16 [rows x N].                              */
+/* op = FP8BS_OP_DGRAD (contraction N, output width K): a = dYq [rows x N];  */
+/*   b = stacked W codes [groups x K x N]; out = dX BF16 [rows x K].         */
+/*   Fprop / Dgrad a_scale_atoms: the atoms of A in the groups' tile layout: */
+/*   group g's rows [offsets[g], offsets[g+1]) form ceil(n_g / 128) tiles of */
+/*   128 rows, numbered over the groups in order (tile t = tiles of earlier  */
+/*   groups + row / 128); tile t's atoms are [t][contraction/128][512]       */
+/*   (fp8_pack_ue8m0_grouped writes them); rows of a group's last tile past  */
+/*   its end are ignored. fp8bs_mx_scale_bytes(Tpad, contraction) bytes with */
+/*   Tpad = fp8bs_padded_tokens(rows, offsets_host, groups), or with device  */
+/*   offsets fp8bs_padded_tokens_max(rows, groups). b_scale_atoms: per group */
+/*   fp8bs_mx_scale_bytes(width, contraction) bytes, laid end to end.        */
+/* op = FP8BS_OP_WGRAD: a = dY^T codes [N x Tpad], b = X^T codes [K x Tpad]  */
+/*   over the padded token layout of the grouped transposed casts (Tpad as   */
+/*   above), with their atoms (fp8bs_mx_scale_bytes(N, Tpad) and             */
+/*   (K, Tpad) bytes); group g contracts over its own 128-token blocks;      */
+/*   out = dW FP32 [groups x N x K] (an empty group's dW is zero).           */
+/* Constraints: 1 <= groups <= FP8BS_MAX_GROUPS; the contraction a multiple  */
+/* of 128, the output width (N for Fprop, K for Dgrad and Wgrad) a multiple  */
+/* of 256; 16-byte aligned buffers. Invalid device offsets record            */
+/* FP8BS_ERR_DEVICE and the kernel writes nothing.                           */
+FP8BS_API fp8bs_status fp8_mx_gemm_grouped(int op, int32_t groups, const int32_t* offsets_dev,
+                                           const int32_t* offsets_host, int64_t rows, const uint8_t* a,
+                                           const uint8_t* a_scale_atoms, const uint8_t* b,
+                                           const uint8_t* b_scale_atoms, int64_t N, int64_t K, void* out,
+                                           void* stream);
+
 /* Transposed MXFP8 cast: the fp8_mx_quant_1x32 cast of x^T, i.e. blocks of  */
 /* 32 consecutive rows (tokens) of x. It gives the operands whose contraction */
 /* runs along x's rows: dY^T and X^T for Wgrad, W^T (from W [K x N]) for      */
@@ -521,6 +555,21 @@ FP8BS_API fp8bs_status fp8_mx_quant_1x32_T(const void* x, int64_t rows, int64_t 
 FP8BS_API fp8bs_status fp8_pack_ue8m0(const float* scales, int64_t rows, int64_t K, int32_t row_block,
                                       int64_t row_stride, int64_t kb_stride, uint8_t* scale_atoms,
                                       void* stream);
+
+/* NEXT-4 for experts: fp8_pack_ue8m0 for the grouped rows of a 1x128-cast   */
+/* operand [rows x K] (the A of a grouped Fprop or Dgrad), into the groups'  */
+/* tile layout that fp8_mx_gemm_grouped reads: the scale of (row r, K-block  */
+/* b) is scales[r + b * kb_stride] (the S1 layout: kb_stride =               */
+/* fp8bs_scale_ld(rows)); row l of group g goes to row l % 128 of tile       */
+/* (tiles of the groups before g) + l / 128. Rows of a group's last tile    */
+/* past its end are written as 127 (scale 1). Offsets as in                  */
+/* fp8_block_gemm_grouped (exactly one of offsets_dev / offsets_host);       */
+/* scale_atoms: fp8bs_mx_scale_bytes(Tpad, K) bytes, 16-byte aligned (Tpad   */
+/* as in fp8_mx_gemm_grouped). A scale without an exponent byte, or invalid  */
+/* device offsets, record FP8BS_ERR_DEVICE.                                  */
+FP8BS_API fp8bs_status fp8_pack_ue8m0_grouped(const float* scales, int64_t rows, int64_t K, int64_t kb_stride,
+                                              int32_t groups, const int32_t* offsets_dev,
+                                              const int32_t* offsets_host, uint8_t* scale_atoms, void* stream);
 
 /* NEXT-4: the casts with their scales already packed. The same casts as   */
 /* fp8_quant_128x128_opts, fp8_quant_dual_opts and fp8_quant_dual_stash_opts */
