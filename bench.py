@@ -11,7 +11,7 @@ reported under its own key of ``configs``: the grouped MoE expert pass (32
 experts, 8192 routed rows, group offsets in device memory), the 256 x K x 256
 split-K Fprop of the long-contraction workload (K = 1024 ... 65536) and the
 standalone 1x128 cast of a 16384 x 16384 tensor (``--dense-only`` skips
-them). ``--workload moe|longk|quant16k|dense_ue8m0`` times one of those (or
+them). ``--workload moe|moe_ue8m0|longk|quant16k|dense_ue8m0`` times one of those (or
 the dense step with power-of-two scales) as the headline instead.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -424,6 +424,88 @@ class MoeStep:
                 "experts": self.G, "tokens": self.T, "hidden": self.H, "inter": self.I, "up": self.U}
 
 
+class MoeUe8m0Step(MoeStep):
+    """The grouped MoE expert pass with power-of-two (UE8M0) scales: the same
+    casts under the UE8M0 rule (the weight casts also writing their scales'
+    exponent bytes into the MX scale atoms; the grouped activation scales
+    packed into the groups' tile layout), and the four grouped GEMMs on the
+    tensor core's block scaling (fp8_mx_gemm_grouped) instead of the software
+    promotion."""
+
+    def __init__(self, fp8bs, torch, device, **kw):
+        super().__init__(fp8bs, torch, device, **kw)
+        e = fp8bs
+        T, G, H, I, U = self.T, self.G, self.H, self.I, self.U
+        self.opts = e.ScaleOpts(e.SCALE_UE8M0, 0.0, 0.0)
+        cap = int(e.fp8bs_padded_tokens_max(T, G))
+        atoms = lambda rows, k, b=1: e.empty_mx_atoms(rows, k, batch=b, device=device)
+        self.awuT, self.awu = atoms(U, H, G), atoms(H, U, G)
+        self.awdT, self.awd = atoms(H, I, G), atoms(I, H, G)
+        self.ax, self.aa, self.ady = atoms(cap, H), atoms(cap, I), atoms(cap, H)
+        self.adyT, self.aaT = atoms(H, cap), atoms(I, cap)
+        self.cap = cap
+        # the transposed casts with device offsets write only the actual
+        # padded tokens; the scales past them are packed too, so they hold 1
+        self.saT.fill_(1.0)
+        self.sdyT.fill_(1.0)
+        self.names = ["quant_128x128(W_up)+atoms", "quant_128x128(W_down)+atoms", "quant_1x128(X)",
+                      "pack(X)", "mx_grouped_fprop_up", "quant_dual_stash(A)", "pack(A)", "pack(A^T)",
+                      "mx_grouped_fprop_down", "quant_dual(dY)", "pack(dY)", "pack(dY^T)",
+                      "mx_grouped_dgrad_down", "mx_grouped_wgrad_down"]
+
+    def work(self):
+        flops, b = super().work()
+        T, G, H, I, U = self.T, self.G, self.H, self.I, self.U
+        mp = int(self.fp8bs.fp8bs_padded_tokens(T, self.offsets_host))
+        s_ld = (T + 3) // 4 * 4
+        f = {"mx_grouped_fprop_up": flops["grouped_fprop_up"], "mx_grouped_fprop_down": flops["grouped_fprop_down"],
+             "mx_grouped_dgrad_down": flops["grouped_dgrad_down"], "mx_grouped_wgrad_down": flops["grouped_wgrad_down"]}
+        atom = lambda rows, k: rows * k // 32
+        by = {
+            "quant_128x128(W_up)+atoms": b["quant_128x128(W_up)"] + G * (atom(U, H) + atom(H, U)),
+            "quant_128x128(W_down)+atoms": b["quant_128x128(W_down)"] + G * (atom(H, I) + atom(I, H)),
+            "quant_1x128(X)": b["quant_1x128(X)"],
+            "pack(X)": 4 * (H // 128) * s_ld + atom(mp, H),
+            "mx_grouped_fprop_up": b["grouped_fprop_up"] + atom(mp, H) + G * atom(U, H),
+            "quant_dual_stash(A)": b["quant_dual_stash(A)"],
+            "pack(A)": 4 * (I // 128) * s_ld + atom(mp, I),
+            "pack(A^T)": 4 * (mp // 128) * I + atom(I, mp),
+            "mx_grouped_fprop_down": b["grouped_fprop_down"] + atom(mp, I) + G * atom(H, I),
+            "quant_dual(dY)": b["quant_dual(dY)"],
+            "pack(dY)": 4 * (H // 128) * s_ld + atom(mp, H),
+            "pack(dY^T)": 4 * (mp // 128) * H + atom(H, mp),
+            "mx_grouped_dgrad_down": b["grouped_dgrad_down"] + atom(mp, H) + G * atom(I, H),
+            "mx_grouped_wgrad_down": b["grouped_wgrad_down"] + atom(H, mp) + atom(I, mp),
+        }
+        return f, by
+
+    def launches(self):
+        e, off, G, H, I, U, T, o = self.fp8bs, self.offsets, self.G, self.H, self.I, self.U, self.T, self.opts
+        return [
+            lambda: e.fp8_quant_128x128_packed(self.Wu, self.wuq, self.wuqT, self.swu, self.awuT, self.awu),
+            lambda: e.fp8_quant_128x128_packed(self.Wd, self.wdq, self.wdqT, self.swd, self.awdT, self.awd),
+            lambda: e.fp8_quant_1x128_opts(self.X, self.xq, self.sx, o),
+            lambda: e.fp8_pack_ue8m0_grouped(self.sx, T, H, off, self.ax),
+            lambda: e.fp8_mx_gemm_grouped(e.OP_FPROP, off, self.xq, self.ax, self.wuqT, self.awuT, self.Yu, U, H),
+            lambda: e.fp8_quant_dual_stash_opts(self.A, self.aq, self.sa, self.aT, self.saT, o, offsets=off),
+            lambda: e.fp8_pack_ue8m0_grouped(self.sa, T, I, off, self.aa),
+            lambda: e.fp8_pack_ue8m0(self.saT, I, self.cap, 1, 1, I, self.aaT),
+            lambda: e.fp8_mx_gemm_grouped(e.OP_FPROP, off, self.aq, self.aa, self.wdqT, self.awdT, self.Yd, H, I),
+            lambda: e.fp8_quant_dual_opts(self.dY, self.dyq, self.sdy, self.dyT, self.sdyT, o, offsets=off),
+            lambda: e.fp8_pack_ue8m0_grouped(self.sdy, T, H, off, self.ady),
+            lambda: e.fp8_pack_ue8m0(self.sdyT, H, self.cap, 1, 1, H, self.adyT),
+            lambda: e.fp8_mx_gemm_grouped(e.OP_DGRAD, off, self.dyq, self.ady, self.wdq, self.awd, self.dA, H, I),
+            lambda: e.fp8_mx_gemm_grouped(e.OP_WGRAD, off, self.dyT, self.adyT, self.aT, self.aaT, self.dWd, H, I,
+                                          rows=T),
+        ]
+
+    def describe(self):
+        d = super().describe()
+        d["workload"] = (d["workload"] + ", power-of-two (UE8M0) scales, the grouped GEMMs on the tensor core's "
+                         "block scaling (fp8_mx_gemm_grouped)")
+        return d
+
+
 class LongKStep:
     """The long-contraction drift workload: X 256xK and W Kx256, U(0.5, 1.5),
     for K in 1024, 4096, 16384, 65536; per K the 1x128 and 128x128
@@ -647,7 +729,8 @@ DATA = {"dense": "synthetic (seeded normal; 0.1% outliers in X)",
         "moe": "synthetic (seeded normal; Dirichlet(0.5) expert counts)",
         "longk": "synthetic (seeded uniform U(0.5, 1.5))",
         "quant16k": "synthetic (seeded normal)",
-        "dense_ue8m0": "synthetic (seeded normal; 0.1% outliers in X)"}
+        "dense_ue8m0": "synthetic (seeded normal; 0.1% outliers in X)",
+        "moe_ue8m0": "synthetic (seeded normal; Dirichlet(0.5) expert counts)"}
 
 
 def make_workload(name, fp8bs, torch, device, rank):
@@ -660,13 +743,16 @@ def make_workload(name, fp8bs, torch, device, rank):
         return Quant1x128Step(fp8bs, torch, device, seed=rank)
     if name == "dense_ue8m0":
         return DenseUe8m0Step(fp8bs, torch, device, M, K, N, seed=rank)
+    if name == "moe_ue8m0":
+        return MoeUe8m0Step(fp8bs, torch, device, seed=rank)
     return DenseStep(fp8bs, torch, device, M, K, N, seed=rank)
 
 
 # Workloads the default run times after the dense step, each reported under
-# its own key of "configs": the grouped MoE pass, the long-K sweep and the
-# standalone 16384 x 16384 1x128 cast.
-EXTRA_WORKLOADS = ("moe", "longk", "quant16k")
+# its own key of "configs": the grouped MoE pass (fp32 scales with software
+# promotion, and power-of-two scales on the tensor core's block scaling), the
+# long-K sweep and the standalone 16384 x 16384 1x128 cast.
+EXTRA_WORKLOADS = ("moe", "moe_ue8m0", "longk", "quant16k")
 
 
 def run_ours(args, world, rank, local):
@@ -1077,10 +1163,11 @@ def main(argv=None):
                     help="time the step as stream launches instead of one CUDA graph replay")
     ap.add_argument("--dense-only", action="store_true",
                     help="time only the dense step (skip the MoE, long-K and 16384^2 cast configs)")
-    ap.add_argument("--workload", choices=["dense", "moe", "longk", "quant16k", "dense_ue8m0"], default="dense",
+    ap.add_argument("--workload", choices=["dense", "moe", "longk", "quant16k", "dense_ue8m0", "moe_ue8m0"],
+                    default="dense",
                     help="dense: the linear layer's fwd+bwd (default); moe: grouped expert pass; "
-                         "longk: 256xKx256 split-K Fprop for K up to 65536; dense_ue8m0: the dense step "
-                         "with power-of-two scales, GEMMs on the tensor core's block scaling")
+                         "longk: 256xKx256 split-K Fprop for K up to 65536; dense_ue8m0 / moe_ue8m0: the dense "
+                         "step / expert pass with power-of-two scales, GEMMs on the tensor core's block scaling")
     ap.add_argument("--cpu-sample", type=float, default=1.0 / 16,
                     help="--impl reference: fraction of token rows the oracle runs per step")
     ap.add_argument("--cpu-baseline-sample", type=float, default=1.0,

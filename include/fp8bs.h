@@ -501,7 +501,10 @@ FP8BS_API fp8bs_status fp8_mx_gemm_f32(const uint8_t* a, const uint8_t* a_scale_
 /*   over the padded token layout of the grouped transposed casts (Tpad as   */
 /*   above), with their atoms (fp8bs_mx_scale_bytes(N, Tpad) and             */
 /*   (K, Tpad) bytes); group g contracts over its own 128-token blocks;      */
-/*   out = dW FP32 [groups x N x K] (an empty group's dW is zero).           */
+/*   out = dW FP32 [groups x N x K] (an empty group's dW is zero). With      */
+/*   device offsets the transposed casts write only the actual padded        */
+/*   tokens: give the scales past them a power of two (e.g. 1) before they   */
+/*   are packed with fp8_pack_ue8m0, or the packing records FP8BS_ERR_DEVICE. */
 /* Constraints: 1 <= groups <= FP8BS_MAX_GROUPS; the contraction a multiple  */
 /* of 128, the output width (N for Fprop, K for Dgrad and Wgrad) a multiple  */
 /* of 256; 16-byte aligned buffers. Invalid device offsets record            */
