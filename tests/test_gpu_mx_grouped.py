@@ -181,3 +181,39 @@ def test_grouped_mx_wgrad(counts, dev):
         xa = t[oaT[:, p:p + w_e]] * np.repeat(osaT[p // 128:(p + w_e) // 128].T.astype(np.float64), 128, 1)
         assert_gemm_close(dw[e], ref, np.abs(da) @ np.abs(xa).T, False, f"grouped mx wgrad e{e}")
         p += w_e
+
+
+@pytest.mark.parametrize("bad", [[1, 129, 130, 300], [0, 200, 100, 300], [0, 100, 200, 299]])
+def test_grouped_mx_invalid_device_offsets_record_error_and_write_nothing(bad):
+    """off[0] != 0, a decrease, a total other than rows, read by the grouped
+    packing and the grouped MX GEMM when they run: FP8BS_ERR_DEVICE in the
+    status word, nothing written, and the same calls with valid offsets are
+    then byte-identical to their host-offset form."""
+    M, K, N, G = 300, 256, 384, 3
+    offd = _offs(bad, True)
+    x = wl.normal((M, K), seed=70)
+    q, s, _, _ = _cast_rows(x)
+    atoms = _pack_grouped(s, M, K, bad, True)
+    torch.cuda.synchronize()
+    assert fp8bs.fp8bs_device_status(reset=True) == 7
+    assert torch.all(atoms == 0xEE)
+    good = wl.offsets_from_counts([100, 0, 200])
+    ax = _pack_grouped(s, M, K, good, True)
+    w = wl.normal((G, K, N), std=wl.W_STD, seed=71)
+    wq, wqT, sw = fp8bs.empty_quant_128x128(K, N, batch=G)
+    awT, aw = fp8bs.empty_mx_atoms(N, K, batch=G), fp8bs.empty_mx_atoms(K, N, batch=G)
+    fp8bs.fp8_quant_128x128_packed(w.cuda(), wq, wqT, sw, awT, aw)
+    y = torch.full((M, N), 3.0, dtype=torch.bfloat16, device="cuda")
+    fp8bs.fp8_mx_gemm_grouped(fp8bs.OP_FPROP, offd, q, ax, wqT, awT, y, N, K)
+    torch.cuda.synchronize()
+    assert fp8bs.fp8bs_device_status(reset=True) == 7
+    assert torch.all(y == 3.0)
+    axh = _pack_grouped(s, M, K, good, False)
+    yh = torch.empty_like(y)
+    fp8bs.fp8_mx_gemm_grouped(fp8bs.OP_FPROP, good, q, axh, wqT, awT, yh, N, K)
+    fp8bs.fp8_mx_gemm_grouped(fp8bs.OP_FPROP, _offs(good, True), q, ax, wqT, awT, y, N, K)
+    torch.cuda.synchronize()
+    assert fp8bs.fp8bs_device_status(reset=True) == 0
+    n_host = fp8bs.fp8bs_mx_scale_bytes(fp8bs.fp8bs_padded_tokens(M, good), K)
+    assert torch.equal(ax[:n_host], axh)
+    assert torch.equal(y.view(torch.int16), yh.view(torch.int16))
