@@ -189,7 +189,7 @@ def test_grouped_mx_invalid_device_offsets_record_error_and_write_nothing(bad):
     packing and the grouped MX GEMM when they run: FP8BS_ERR_DEVICE in the
     status word, nothing written, and the same calls with valid offsets are
     then byte-identical to their host-offset form."""
-    M, K, N, G = 300, 256, 384, 3
+    M, K, N, G = 300, 256, 512, 3      # the output width a multiple of 256
     offd = _offs(bad, True)
     x = wl.normal((M, K), seed=70)
     q, s, _, _ = _cast_rows(x)
