@@ -140,13 +140,14 @@ bool make_out_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows)
 }
 
 // 2D map over a BF16 cast source [rows x cols] with row pitch `row_bytes`
-// (a multiple of 16): box of 64 columns x 32 rows, 128-byte swizzle, zero
-// fill out of bounds.
-bool make_src_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes)
+// (a multiple of 16): box of 64 columns x box_rows rows, 128-byte swizzle,
+// zero fill out of bounds.
+bool make_src_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
+                  uint32_t box_rows)
 {
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {64u, 32u};
+    const cuuint32_t box[2] = {64u, box_rows};
     const cuuint32_t estr[2] = {1u, 1u};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -223,17 +224,18 @@ bool cached_out_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows)
     return true;
 }
 
-bool cached_src_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes)
+bool cached_src_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
+                    uint32_t box_rows = 32u)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
-    const MapKey k{dev, 2, base, cols, rows, row_bytes, 32u};
+    const MapKey k{dev, 2, base, cols, rows, row_bytes, box_rows};
     MapSlot& sl = map_slot(k);
     if (sl.used && sl.key == k) {
         *m = sl.map;
         return true;
     }
-    if (!make_src_map(m, base, cols, rows, row_bytes)) return false;
+    if (!make_src_map(m, base, cols, rows, row_bytes, box_rows)) return false;
     sl.used = true;
     sl.key = k;
     sl.map = *m;
@@ -653,6 +655,17 @@ fp8bs_status requant_common(int src_mode, const void* src, const float* src_scal
         p.off[1] = static_cast<int32_t>(rows);
         p.tile_start[0] = 0;
         p.tile_start[1] = static_cast<int32_t>(mpad / 128);
+    }
+    if (q && q_scales && src_mode == FP8BS_SRC_BF16 && !sr && !grouped && !offsets_dev) {
+        // dense, round to nearest: the TMA-fed tile kernel
+        CUtensorMap map_x, map_q;
+        if (!cached_src_map(&map_x, src, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
+                            static_cast<uint64_t>(cols) * 2, 128u) ||
+            !cached_map(&map_q, q, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
+                        static_cast<uint64_t>(cols), 128u))
+            return FP8BS_ERR_LAUNCH;
+        return launch_status(
+            launch_dual_tile(map_x, map_q, p, g_wait_limit_ns, st->num_sms, static_cast<cudaStream_t>(stream)));
     }
     return launch_status(launch_requant_128x1_T(p, static_cast<cudaStream_t>(stream)));
 }

@@ -95,6 +95,12 @@ struct RequantParams {
 };
 
 cudaError_t launch_requant_128x1_T(const RequantParams& p, cudaStream_t stream);
+// The dense, round-to-nearest dual and stash casts (p.q set, p.mode BF16, no
+// groups, no stochastic rounding) on the TMA-fed tile kernel: map_x over the
+// BF16 source (box 64 columns x 128 rows, 128-byte swizzle), map_q over q
+// (box 128 bytes x 128 rows, 128-byte swizzle).
+cudaError_t launch_dual_tile(const CUtensorMap& map_x, const CUtensorMap& map_q, const RequantParams& p,
+                             uint64_t limit, int num_sms, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Block-scaled GEMM (tcgen05)

@@ -1145,6 +1145,306 @@ __global__ void __launch_bounds__(kQ3Threads, kSR ? 2 : (kStash ? 3 : 4)) requan
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// Dense dual cast (NEXT-1) and fused forward cast + stash requant (NEXT-1b)
+// with round-to-nearest codes: a persistent kernel, two CTAs of 256 threads
+// per SM, each CTA working through 128 x 128 blocks. A block arrives by TMA
+// as two boxes of 64 columns x 128 rows (128-byte swizzle: 16-byte chunk c
+// of row r at slot c ^ r % 8) into one of two buffers, so the next block
+// loads while the current one is worked on.
+//
+// Row pass: a lane takes one half (64 values) of one row straight from the
+// staged block, so the row absmax is in-thread plus one shuffle with the
+// lane holding the other half, and each lane encodes its 64 values with the
+// row's scale. The 1x128 codes go to a code stage in the same swizzle and
+// leave with one TMA store.
+//
+// Transposed pass: a thread takes a few channels over a part of the block's
+// tokens and keeps their values in registers (dual cast: a channel pair of
+// BF16 values over 32 tokens; stash cast: a channel quad of the staged codes
+// times their row scales, 16 tokens) while the parts' column maxima meet in
+// shared memory; 128 threads turn them into the channel scales, and each
+// thread then encodes its values and writes its pieces of the qT rows.
+//
+// The arithmetic is that of requant_128x1_T_kernel (the same scale,
+// quotient and decode helpers, in the same order), so the bytes are
+// identical; the work split is what differs (no shuffles for the row
+// maxima or scales, one decode of the stash per element, loads overlapped
+// with the work).
+// ---------------------------------------------------------------------------
+constexpr int kDtThreads = 256;
+constexpr int kDtXBytes = 128 * 128 * 2;                   // one BF16 block
+constexpr int kDtQOff = 2 * kDtXBytes;                     // 1x128 code stage, 128 x 128 bytes
+constexpr int kDtCpartOff = kDtQOff + 128 * 128;           // float [8][128] column partial maxima
+constexpr int kDtRowScaleOff = kDtCpartOff + 8 * 128 * 4;  // float [128]
+constexpr int kDtColTsOff = kDtRowScaleOff + 128 * 4;      // TileScale [128]
+constexpr int kDtBarOff = kDtColTsOff + 128 * 8;           // two mbarriers
+constexpr int kDtSmemBytes = kDtBarOff + 16 + 1023;        // + slack for the 1024-byte alignment
+constexpr uint64_t kDtDrainNs = 1000000000ull;
+
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+template <bool kStash>
+__global__ void __launch_bounds__(kDtThreads, 2) dual_tile_kernel(const __grid_constant__ CUtensorMap map_x,
+                                                                  const __grid_constant__ CUtensorMap map_q,
+                                                                  const __grid_constant__ RequantParams p,
+                                                                  int64_t col_tiles, int64_t tiles, uint64_t limit)
+{
+    extern __shared__ uint8_t dt_smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(dt_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t xs0 = smem_addr(smem);         // two buffers of [2 column halves][128 rows][128 bytes]
+    const uint32_t qs = xs0 + kDtQOff;            // [128 rows][128 bytes]
+    float (*cpart)[128] = reinterpret_cast<float (*)[128]>(smem + kDtCpartOff);
+    float* row_scale = reinterpret_cast<float*>(smem + kDtRowScaleOff);
+    TileScale* col_ts = reinterpret_cast<TileScale*>(smem + kDtColTsOff);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kDtBarOff);
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+
+    auto issue = [&](int64_t tile, int buf) {
+        const int64_t rt = tile / col_tiles;
+        const int64_t ct = tile - rt * col_tiles;
+        uint8_t* dst = smem + buf * kDtXBytes;
+        mbar_arrive_expect_tx(&full[buf], kDtXBytes);
+        tma_load_2d(dst, &map_x, &full[buf], static_cast<int32_t>(ct * 128), static_cast<int32_t>(rt * 128));
+        tma_load_2d(dst + kDtXBytes / 2, &map_x, &full[buf], static_cast<int32_t>(ct * 128 + 64),
+                    static_cast<int32_t>(rt * 128));
+    };
+    if (t == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        fence_mbarrier_init();
+        tma_prefetch_desc(&map_x);
+        tma_prefetch_desc(&map_q);
+        for (int j = 0; j < 2; ++j)
+            if (blockIdx.x + static_cast<int64_t>(j) * gridDim.x < tiles) issue(blockIdx.x + j * gridDim.x, j);
+    }
+    __syncthreads();
+
+    int it = 0;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++it) {
+        const int buf = it & 1;
+        const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
+        const uint32_t xs = xs0 + buf * kDtXBytes;
+        const int64_t rt = tile / col_tiles;
+        const int64_t ct = tile - rt * col_tiles;
+        const int64_t r0 = rt * 128, c0 = ct * 128;
+        const int len = static_cast<int>(min(static_cast<int64_t>(128), p.rows - r0));
+        const int nch = static_cast<int>(min(static_cast<int64_t>(128), p.cols - c0));
+
+        // thread 0 waits (bounded) for the block and for the previous store's
+        // read of the code stage; the CTA follows its verdict, and the other
+        // threads then pass the completed phase themselves (acquire)
+        int landed = 1;
+        if (t == 0) {
+            bulk_wait_group_read<0>();
+            landed = mbar_wait(&full[buf], ph, limit) ? 1 : 0;
+        }
+        landed = __syncthreads_and(landed);
+        if (!landed) {
+            if (t == 0) {
+                atomicCAS(p.status, 0u, static_cast<unsigned int>(FP8BS_ERR_TIMEOUT));
+                // the boxes in flight land before the CTA leaves
+                const uint64_t drain = limit > kDtDrainNs ? limit : kDtDrainNs;
+                for (int j = it; j < it + 2; ++j)
+                    if (blockIdx.x + static_cast<int64_t>(j) * gridDim.x < tiles)
+                        mbar_wait(&full[j & 1], static_cast<uint32_t>(j >> 1) & 1u, drain);
+                bulk_wait_group_all();
+            }
+            return;
+        }
+        mbar_try_wait(&full[buf], ph);
+
+        // ---- row pass: lane = (row, column half) ----
+        {
+            const int h = lane >> 4;
+            const int r = warp * 16 + (lane & 15);
+            const uint32_t sw = static_cast<uint32_t>(r & 7);
+            const uint32_t rowp = xs + h * (kDtXBytes / 2) + r * 128;
+            uint4 d[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) d[c] = ld_shared_v4(rowp + ((c ^ sw) << 4));
+            uint32_t m = 0;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) m = max(m, absmax_bits_8(d[c]));
+            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+            const TileScale ts = tile_scale(__uint_as_float(m << 16), p.rule);
+            const uint32_t outp = qs + r * 128;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint2 a = quant8(d[2 * j], ts);
+                const uint2 b = quant8(d[2 * j + 1], ts);
+                st_shared_v4(outp + (((4 * h + j) ^ sw) << 4), make_uint4(a.x, a.y, b.x, b.y));
+            }
+            if (h == 0) {
+                row_scale[r] = ts.s;
+                if (r < len) p.q_scales[ct * p.q_scale_ld + r0 + r] = ts.s;
+            }
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (t == 0) {
+            tma_store_2d(&map_q, qs, static_cast<int32_t>(c0), static_cast<int32_t>(r0));
+            bulk_commit_group();
+        }
+
+        // ---- transposed pass, part 1: the values and the parts' column maxima ----
+        uint32_t w[32];     // dual cast: BF16 pairs of channels (c, c + 1), tokens 32 part + k
+        float nv[16][4];    // stash cast: -dec(q) s_row of channels c .. c + 3, tokens 16 part + k
+        if constexpr (!kStash) {
+            const int c = 2 * (t & 63);
+            const int part = t >> 6;
+            const uint32_t colp = xs + (c >> 6) * (kDtXBytes / 2) + ((c & 7) << 1);
+            const uint32_t chunk = static_cast<uint32_t>((c & 63) >> 3);
+            uint32_t mm = 0;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const int r = part * 32 + k;
+                w[k] = ld_shared_u32(colp + r * 128 + ((chunk ^ static_cast<uint32_t>(r & 7)) << 4));
+                mm = __vmaxu2(mm, w[k] & 0x7FFF7FFFu);
+            }
+            cpart[part][c] = __uint_as_float(mm << 16);
+            cpart[part][c + 1] = __uint_as_float(mm & 0xFFFF0000u);
+        } else {
+            const int jq = t & 31;
+            const int part = t >> 5;
+            const int c = 4 * jq;
+            const uint32_t colp = qs + ((jq & 3) << 2);
+            const uint32_t chunk = static_cast<uint32_t>(jq >> 2);
+            float cm[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int r = part * 16 + k;
+                const uint32_t x = ld_shared_u32(colp + r * 128 + ((chunk ^ static_cast<uint32_t>(r & 7)) << 4));
+                decode4_scaled(x, -row_scale[r], nv[k]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) cm[e] = fmaxf(cm[e], fabsf(nv[k][e]));
+            }
+            *reinterpret_cast<float4*>(&cpart[part][c]) = make_float4(cm[0], cm[1], cm[2], cm[3]);
+        }
+        __syncthreads();
+        if (t < 128) {
+            float m = 0.0f;
+#pragma unroll
+            for (int i = 0; i < (kStash ? 8 : 4); ++i) m = fmaxf(m, cpart[i][t]);
+            const float s = scale_from_amax(m, p.rule);
+            col_ts[t] = tile_scale_from_s(s);
+            if (t < nch) p.scT[rt * p.cols + c0 + t] = s;
+        }
+        __syncthreads();
+        // every read of this buffer is done: load the block after next into it
+        if (t == 0 && tile + 2 * static_cast<int64_t>(gridDim.x) < tiles) {
+            fence_proxy_async_smem();
+            issue(tile + 2 * static_cast<int64_t>(gridDim.x), buf);
+        }
+
+        // exponent-byte atoms (power-of-two scales), as in requant_128x1_T_kernel
+        if (t < 64 && (t < 32 ? p.q_atoms : p.qT_atoms) != nullptr) {
+            const int l = t & 31;
+            const bool rows_side = t < 32;
+            uint32_t wv[4];
+            bool bad = false;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int i = l + 32 * k;
+                uint32_t E = 127u;
+                if (rows_side ? i < len : i < nch) {
+                    E = ue8m0_of(rows_side ? row_scale[i] : col_ts[i].s);
+                    bad |= E == 255u;
+                }
+                wv[k] = E * 0x01010101u;
+            }
+            if (bad) atomicCAS(p.status, 0u, static_cast<unsigned int>(FP8BS_ERR_DEVICE));
+            uint8_t* atom = rows_side ? p.q_atoms + (rt * (p.cols / 128) + ct) * 512
+                                      : p.qT_atoms + (ct * (p.mpad / 128) + rt) * 512;
+            *reinterpret_cast<uint4*>(atom + 16 * l) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+
+        // ---- transposed pass, part 2: encode with the channel scales ----
+        if constexpr (!kStash) {
+            const int c = 2 * (t & 63);
+            const int part = t >> 6;
+            if (c < nch) {   // nch % 16 == 0: pairs are all-in or all-out
+                const TileScale t0 = col_ts[c];
+                const TileScale t1 = col_ts[c + 1];
+                uint32_t o0[8], o1[8];
+                if (t0.nr != 0.0f && t1.nr != 0.0f) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t* x = w + 4 * k;
+                        const uint32_t a01 =
+                            encode2_fast(make_float2(neg_bf16_lo(x[0]), neg_bf16_lo(x[1])), t0.s, t0.nr);
+                        const uint32_t a23 =
+                            encode2_fast(make_float2(neg_bf16_lo(x[2]), neg_bf16_lo(x[3])), t0.s, t0.nr);
+                        const uint32_t b01 =
+                            encode2_fast(make_float2(neg_bf16_hi(x[0]), neg_bf16_hi(x[1])), t1.s, t1.nr);
+                        const uint32_t b23 =
+                            encode2_fast(make_float2(neg_bf16_hi(x[2]), neg_bf16_hi(x[3])), t1.s, t1.nr);
+                        o0[k] = __byte_perm(a01, a23, 0x5410);
+                        o1[k] = __byte_perm(b01, b23, 0x5410);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t* x = w + 4 * k;
+                        o0[k] = encode2_exact(bf16_lo(x[0]), bf16_lo(x[1]), t0.s) |
+                                (encode2_exact(bf16_lo(x[2]), bf16_lo(x[3]), t0.s) << 16);
+                        o1[k] = encode2_exact(bf16_hi(x[0]), bf16_hi(x[1]), t1.s) |
+                                (encode2_exact(bf16_hi(x[2]), bf16_hi(x[3]), t1.s) << 16);
+                    }
+                }
+                uint8_t* dst0 = p.qT + (c0 + c) * p.mpad + r0 + part * 32;
+                uint8_t* dst1 = dst0 + p.mpad;
+                reinterpret_cast<uint4*>(dst0)[0] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+                reinterpret_cast<uint4*>(dst0)[1] = make_uint4(o0[4], o0[5], o0[6], o0[7]);
+                reinterpret_cast<uint4*>(dst1)[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+                reinterpret_cast<uint4*>(dst1)[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
+            }
+        } else {
+            const int jq = t & 31;
+            const int part = t >> 5;
+            const int c = 4 * jq;
+            if (c < nch) {
+                TileScale ts[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) ts[e] = col_ts[c + e];
+                uint32_t o[4][4];
+                if (ts[0].nr != 0.0f && ts[1].nr != 0.0f && ts[2].nr != 0.0f && ts[3].nr != 0.0f) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+#pragma unroll
+                        for (int ch = 0; ch < 4; ++ch) {
+                            const uint32_t c01 = encode2_fast(make_float2(nv[4 * k][ch], nv[4 * k + 1][ch]),
+                                                              ts[ch].s, ts[ch].nr);
+                            const uint32_t c23 = encode2_fast(make_float2(nv[4 * k + 2][ch], nv[4 * k + 3][ch]),
+                                                              ts[ch].s, ts[ch].nr);
+                            o[ch][k] = __byte_perm(c01, c23, 0x5410);
+                        }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+#pragma unroll
+                        for (int ch = 0; ch < 4; ++ch)
+                            o[ch][k] = encode2_exact(-nv[4 * k][ch], -nv[4 * k + 1][ch], ts[ch].s) |
+                                       (encode2_exact(-nv[4 * k + 2][ch], -nv[4 * k + 3][ch], ts[ch].s) << 16);
+                }
+                uint8_t* dst = p.qT + (c0 + c) * p.mpad + r0 + part * 16;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch)
+                    *reinterpret_cast<uint4*>(dst + ch * p.mpad) = make_uint4(o[ch][0], o[ch][1], o[ch][2], o[ch][3]);
+            }
+        }
+    }
+    // the last code stage has been read, and every store has completed, before the CTA exits
+    if (t == 0) bulk_wait_group_all();
+}
+
 }  // namespace
 
 cudaError_t launch_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
@@ -1214,6 +1514,38 @@ cudaError_t launch_quant_128x128(const uint16_t* w, int64_t batch, int64_t rows,
         quant_128x128_kernel<false><<<(unsigned)blocks, kQ2Threads, 0, stream>>>(
             w, rows, cols, ldw, q, qT, scales, rule, SrKey{0, 0}, atoms_wT, atoms_w, status);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dual_tile(const CUtensorMap& map_x, const CUtensorMap& map_q, const RequantParams& p,
+                             uint64_t limit, int num_sms, cudaStream_t stream)
+{
+    const int64_t col_tiles = (p.cols + 127) / 128;
+    const int64_t tiles = (p.mpad / 128) * col_tiles;
+    if (tiles == 0) return cudaSuccess;
+    static_assert(2 * (kDtSmemBytes + 1024) <= 233472, "two CTAs per SM");
+    // once per device: the shared-memory opt-in of both instances
+    static std::atomic<uint64_t> ready{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(ready.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(dual_tile_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDtSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(dual_tile_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kDtSmemBytes);
+        if (e != cudaSuccess) return e;
+        ready.fetch_or(bit, std::memory_order_release);
+    }
+    int64_t blocks = 2 * static_cast<int64_t>(num_sms);   // two resident CTAs per SM
+    if (blocks > tiles) blocks = tiles;
+    if (p.stash)
+        dual_tile_kernel<true><<<static_cast<unsigned>(blocks), kDtThreads, kDtSmemBytes, stream>>>(
+            map_x, map_q, p, col_tiles, tiles, limit);
+    else
+        dual_tile_kernel<false><<<static_cast<unsigned>(blocks), kDtThreads, kDtSmemBytes, stream>>>(
+            map_x, map_q, p, col_tiles, tiles, limit);
     return cudaGetLastError();
 }
 
