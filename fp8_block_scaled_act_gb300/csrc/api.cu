@@ -160,14 +160,16 @@ bool make_src_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows
 // device and every argument of the encoding. A hit copies the 128-byte map.
 struct MapKey {
     int dev;
-    int kind;   // 0: E4M3 operand map, 1: BF16 output map, 2: BF16 cast source map
+    int kind;   // 0: E4M3 operand map, 1: BF16 output map, 2: BF16 cast source map,
+                // 3: batched BF16 weights, 4: batched E4M3 weight codes
     const void* base;
     uint64_t inner, outer, row_bytes;
     uint32_t box_outer;
+    uint64_t depth = 1;   // batch entries (three-dimensional maps)
     bool operator==(const MapKey& o) const
     {
         return dev == o.dev && kind == o.kind && base == o.base && inner == o.inner && outer == o.outer &&
-               row_bytes == o.row_bytes && box_outer == o.box_outer;
+               row_bytes == o.row_bytes && box_outer == o.box_outer && depth == o.depth;
     }
 };
 
@@ -185,6 +187,7 @@ MapSlot& map_slot(const MapKey& k)
     uint64_t h = reinterpret_cast<uintptr_t>(k.base) >> 4;
     h ^= k.inner * 0x9E3779B97F4A7C15ull ^ k.outer * 0xC2B2AE3D27D4EB4Full ^ k.row_bytes * 0x165667B19E3779F9ull;
     h ^= (static_cast<uint64_t>(k.box_outer) << 32) ^ (static_cast<uint64_t>(k.dev) << 8) ^ k.kind;
+    h ^= k.depth * 0x27D4EB2F165667C5ull;
     h ^= h >> 29;
     return t_maps[h % kMapSlots];
 }
@@ -236,6 +239,36 @@ bool cached_src_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t ro
         return true;
     }
     if (!make_src_map(m, base, cols, rows, row_bytes, box_rows)) return false;
+    sl.used = true;
+    sl.key = k;
+    sl.map = *m;
+    return true;
+}
+
+// 3D map over batched weights [batch][rows][cols] (BF16, row pitch
+// row_bytes; or E4M3 codes, dense) with boxes of one batch entry: box_cols
+// columns x 128 rows, 128-byte swizzle, zero fill out of bounds (so a box
+// never reaches into the next batch entry).
+bool cached_batch_map(CUtensorMap* m, bool bf16, const void* base, uint64_t cols, uint64_t rows, uint64_t batch,
+                      uint64_t row_bytes)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    MapKey k{dev, bf16 ? 3 : 4, base, cols, rows, row_bytes, 128u};
+    k.depth = batch;
+    MapSlot& sl = map_slot(k);
+    if (sl.used && sl.key == k) {
+        *m = sl.map;
+        return true;
+    }
+    const cuuint64_t dims[3] = {cols, rows, batch};
+    const cuuint64_t strides[2] = {row_bytes, row_bytes * rows};
+    const cuuint32_t box[3] = {bf16 ? 64u : 128u, 128u, 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    if (g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base),
+                 dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
     sl.used = true;
     sl.key = k;
     sl.map = *m;
@@ -565,6 +598,18 @@ fp8bs_status quant_128x128_common(const void* w, int64_t batch, int64_t rows, in
     DeviceState* st = nullptr;
     fp8bs_status s = device_state(&st);
     if (s != FP8BS_OK) return s;
+    if (!sr) {
+        // round to nearest: the TMA-fed tile kernel
+        CUtensorMap map_w, map_q;
+        if (!cached_batch_map(&map_w, true, w, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
+                              static_cast<uint64_t>(batch), static_cast<uint64_t>(ldw) * 2) ||
+            !cached_batch_map(&map_q, false, q, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
+                              static_cast<uint64_t>(batch), static_cast<uint64_t>(cols)))
+            return FP8BS_ERR_LAUNCH;
+        return launch_status(launch_wcast_tile(map_w, map_q, batch, rows, cols, qT, scales, rule, atoms_wT, atoms_w,
+                                               st->status, g_wait_limit_ns, st->num_sms,
+                                               static_cast<cudaStream_t>(stream)));
+    }
     return launch_status(launch_quant_128x128(static_cast<const uint16_t*>(w), batch, rows, cols, ldw, q, qT,
                                               scales, rule, sr, static_cast<cudaStream_t>(stream), atoms_wT,
                                               atoms_w, st->status));

@@ -95,6 +95,13 @@ struct RequantParams {
 };
 
 cudaError_t launch_requant_128x1_T(const RequantParams& p, cudaStream_t stream);
+// The round-to-nearest 128x128 cast on the TMA-fed tile kernel: map_w over
+// the BF16 weights as [batch][rows][cols] (box 64 columns x 128 rows x 1,
+// 128-byte swizzle), map_q over q the same way (box 128 bytes x 128 rows x 1).
+cudaError_t launch_wcast_tile(const CUtensorMap& map_w, const CUtensorMap& map_q, int64_t batch, int64_t rows,
+                              int64_t cols, uint8_t* qT, float* scales, const ScaleRule& rule, uint8_t* atoms_wT,
+                              uint8_t* atoms_w, unsigned int* status, uint64_t limit, int num_sms,
+                              cudaStream_t stream);
 // The dense, round-to-nearest dual and stash casts (p.q set, p.mode BF16, no
 // groups, no stochastic rounding) on the TMA-fed tile kernel: map_x over the
 // BF16 source (box 64 columns x 128 rows, 128-byte swizzle), map_q over q

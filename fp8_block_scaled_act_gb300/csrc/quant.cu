@@ -1445,6 +1445,201 @@ __global__ void __launch_bounds__(kDtThreads, 2) dual_tile_kernel(const __grid_c
     if (t == 0) bulk_wait_group_all();
 }
 
+
+// ---------------------------------------------------------------------------
+// S2 with round-to-nearest codes on a TMA-fed persistent kernel: two CTAs of
+// 256 threads per SM work through the 128x128 blocks of all batch entries.
+// A block arrives by TMA (three-dimensional map [batch][rows][cols], so a
+// block never reads rows of the next batch entry: they are out of bounds
+// and arrive as zeros) into one of two buffers, so the next block loads
+// while the current one is worked on. A lane holds one half (64 values) of
+// one row; the block absmax is a warp reduction plus one value per warp in
+// shared memory, and lane 0 of each warp turns it into the scale. The codes
+// go through a swizzled stage and leave with one TMA store; the transposed
+// copy is read back from the stage four channels x four tokens at a time,
+// transposed in registers with byte permutes, and written as 16-token
+// pieces of the qT rows. Same arithmetic as quant_128x128_kernel.
+// ---------------------------------------------------------------------------
+constexpr int kWtThreads = 256;
+constexpr int kWtXBytes = 128 * 128 * 2;
+constexpr int kWtQOff = 2 * kWtXBytes;
+constexpr int kWtRedOff = kWtQOff + 128 * 128;
+constexpr int kWtBarOff = kWtRedOff + 64;
+constexpr int kWtSmemBytes = kWtBarOff + 16 + 1023;
+
+// Rows of a 4 x 4 byte matrix held as four words (word i = row i, byte j =
+// column j) -> its columns (word j = column j, byte i = row i).
+__device__ __forceinline__ void transpose4x4_bytes(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
+                                                   uint32_t (&o)[4])
+{
+    const uint32_t t0 = __byte_perm(w0, w1, 0x5140);   // w0.b0 w1.b0 w0.b1 w1.b1
+    const uint32_t t1 = __byte_perm(w0, w1, 0x7362);   // w0.b2 w1.b2 w0.b3 w1.b3
+    const uint32_t t2 = __byte_perm(w2, w3, 0x5140);
+    const uint32_t t3 = __byte_perm(w2, w3, 0x7362);
+    o[0] = __byte_perm(t0, t2, 0x5410);
+    o[1] = __byte_perm(t0, t2, 0x7632);
+    o[2] = __byte_perm(t1, t3, 0x5410);
+    o[3] = __byte_perm(t1, t3, 0x7632);
+}
+
+__global__ void __launch_bounds__(kWtThreads, 2) wcast_tile_kernel(
+    const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_q, int64_t rows,
+    int64_t cols, uint8_t* __restrict__ qT, float* __restrict__ scales, const ScaleRule rule,
+    uint8_t* __restrict__ atoms_wT, uint8_t* __restrict__ atoms_w, unsigned int* status, int64_t tiles,
+    uint64_t limit)
+{
+    extern __shared__ uint8_t wt_smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(wt_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t xs0 = smem_addr(smem);
+    const uint32_t qs = xs0 + kWtQOff;
+    uint32_t* red = reinterpret_cast<uint32_t*>(smem + kWtRedOff);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kWtBarOff);
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int64_t nbr = (rows + 127) / 128, nbc = (cols + 127) / 128;
+    const int64_t per_b = nbr * nbc;
+
+    auto issue = [&](int64_t tile, int buf) {
+        const int64_t b = tile / per_b;
+        const int64_t rem = tile - b * per_b;
+        const int64_t bi = rem / nbc, bj = rem - bi * nbc;
+        uint8_t* dst = smem + buf * kWtXBytes;
+        mbar_arrive_expect_tx(&full[buf], kWtXBytes);
+        tma_load_3d(dst, &map_w, &full[buf], static_cast<int32_t>(bj * 128), static_cast<int32_t>(bi * 128),
+                    static_cast<int32_t>(b));
+        tma_load_3d(dst + kWtXBytes / 2, &map_w, &full[buf], static_cast<int32_t>(bj * 128 + 64),
+                    static_cast<int32_t>(bi * 128), static_cast<int32_t>(b));
+    };
+    if (t == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        fence_mbarrier_init();
+        tma_prefetch_desc(&map_w);
+        tma_prefetch_desc(&map_q);
+        for (int j = 0; j < 2; ++j)
+            if (blockIdx.x + static_cast<int64_t>(j) * gridDim.x < tiles) issue(blockIdx.x + j * gridDim.x, j);
+    }
+    __syncthreads();
+
+    int it = 0;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++it) {
+        const int buf = it & 1;
+        const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
+        const uint32_t xs = xs0 + buf * kWtXBytes;
+        const int64_t b = tile / per_b;
+        const int64_t rem = tile - b * per_b;
+        const int64_t bi = rem / nbc, bj = rem - bi * nbc;
+        const int64_t r0 = bi * 128, c0 = bj * 128;
+
+        int landed = 1;
+        if (t == 0) {
+            bulk_wait_group_read<0>();   // the previous block's code stage has been read
+            landed = mbar_wait(&full[buf], ph, limit) ? 1 : 0;
+        }
+        landed = __syncthreads_and(landed);
+        if (!landed) {
+            if (t == 0) {
+                atomicCAS(status, 0u, static_cast<unsigned int>(FP8BS_ERR_TIMEOUT));
+                const uint64_t drain = limit > kDtDrainNs ? limit : kDtDrainNs;
+                for (int j = it; j < it + 2; ++j)
+                    if (blockIdx.x + static_cast<int64_t>(j) * gridDim.x < tiles)
+                        mbar_wait(&full[j & 1], static_cast<uint32_t>(j >> 1) & 1u, drain);
+                bulk_wait_group_all();
+            }
+            return;
+        }
+        mbar_try_wait(&full[buf], ph);
+
+        // ---- block absmax: lane = (row, column half) ----
+        const int h = lane >> 4;
+        const int r = warp * 16 + (lane & 15);
+        const uint32_t sw = static_cast<uint32_t>(r & 7);
+        const uint32_t rowp = xs + h * (kWtXBytes / 2) + r * 128;
+        uint4 d[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) d[c] = ld_shared_v4(rowp + ((c ^ sw) << 4));
+        uint32_t m = 0;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) m = max(m, absmax_bits_8(d[c]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        if (lane == 0) red[warp] = m;
+        __syncthreads();
+        // every block is the same: lane 0 of each warp derives the scale,
+        // which the warp then shares
+        TileScale ts{0.0f, 0.0f};
+        if (lane == 0) {
+            uint32_t mb = 0;
+#pragma unroll
+            for (int i = 0; i < kWtThreads / 32; ++i) mb = max(mb, red[i]);
+            ts = tile_scale(__uint_as_float(mb << 16), rule);
+        }
+        ts.s = __shfl_sync(0xFFFFFFFFu, ts.s, 0);
+        ts.nr = __shfl_sync(0xFFFFFFFFu, ts.nr, 0);
+        if (t == 0) scales[b * per_b + bi * nbc + bj] = ts.s;
+        if (atoms_wT != nullptr && t < 64) {
+            // the block's exponent byte fills one whole atom of each operand:
+            // W^T (rows = the block's 128 columns, K-block bi) and W (rows =
+            // its 128 rows, K-block bj); 16 bytes per thread
+            const uint32_t E = ue8m0_of(ts.s);
+            if (E == 255u && t == 0) atomicCAS(status, 0u, static_cast<unsigned int>(FP8BS_ERR_DEVICE));
+            const uint32_t e4 = E * 0x01010101u;
+            const int64_t bo = b * per_b * 512;
+            uint8_t* atom = t < 32 ? atoms_wT + bo + (bj * nbr + bi) * 512 : atoms_w + bo + (bi * nbc + bj) * 512;
+            *reinterpret_cast<uint4*>(atom + 16 * (t & 31)) = make_uint4(e4, e4, e4, e4);
+        }
+        const uint32_t outp = qs + r * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint2 a = quant8(d[2 * j], ts);
+            const uint2 c = quant8(d[2 * j + 1], ts);
+            st_shared_v4(outp + (((4 * h + j) ^ sw) << 4), make_uint4(a.x, a.y, c.x, c.y));
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (t == 0) {
+            tma_store_3d(&map_q, qs, static_cast<int32_t>(c0), static_cast<int32_t>(r0), static_cast<int32_t>(b));
+            bulk_commit_group();
+            // every read of this buffer is done: load the block after next into it
+            if (tile + 2 * static_cast<int64_t>(gridDim.x) < tiles) {
+                fence_proxy_async_smem();
+                issue(tile + 2 * static_cast<int64_t>(gridDim.x), buf);
+            }
+        }
+
+        // ---- the transposed copy: channels 4 jq .. 4 jq + 3, tokens 16 part .. + 15 ----
+        if (qT != nullptr) {
+            const int jq = t & 31;
+            const int part = t >> 5;
+            const int64_t c = c0 + 4 * jq;
+            const int64_t rr = r0 + part * 16;
+            if (c < cols && rr < rows) {   // rows, cols % 16 == 0: quads and segments are all-in or all-out
+                const uint32_t colp = qs + ((jq & 3) << 2);
+                const uint32_t chunk = static_cast<uint32_t>(jq >> 2);
+                uint32_t o[4][4];   // [channel][4-token group]
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    uint32_t x[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int rl = part * 16 + 4 * k + e;
+                        x[e] = ld_shared_u32(colp + rl * 128 + ((chunk ^ static_cast<uint32_t>(rl & 7)) << 4));
+                    }
+                    uint32_t y[4];
+                    transpose4x4_bytes(x[0], x[1], x[2], x[3], y);
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) o[ch][k] = y[ch];
+                }
+                uint8_t* dst = qT + b * rows * cols + c * rows + rr;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch)
+                    *reinterpret_cast<uint4*>(dst + ch * rows) = make_uint4(o[ch][0], o[ch][1], o[ch][2], o[ch][3]);
+            }
+        }
+    }
+    if (t == 0) bulk_wait_group_all();
+}
+
 }  // namespace
 
 cudaError_t launch_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
@@ -1546,6 +1741,31 @@ cudaError_t launch_dual_tile(const CUtensorMap& map_x, const CUtensorMap& map_q,
     else
         dual_tile_kernel<false><<<static_cast<unsigned>(blocks), kDtThreads, kDtSmemBytes, stream>>>(
             map_x, map_q, p, col_tiles, tiles, limit);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wcast_tile(const CUtensorMap& map_w, const CUtensorMap& map_q, int64_t batch, int64_t rows,
+                              int64_t cols, uint8_t* qT, float* scales, const ScaleRule& rule, uint8_t* atoms_wT,
+                              uint8_t* atoms_w, unsigned int* status, uint64_t limit, int num_sms,
+                              cudaStream_t stream)
+{
+    const int64_t tiles = batch * ((rows + 127) / 128) * ((cols + 127) / 128);
+    if (tiles == 0) return cudaSuccess;
+    static_assert(2 * (kWtSmemBytes + 1024) <= 233472, "two CTAs per SM");
+    static std::atomic<uint64_t> ready{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(ready.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(wcast_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kWtSmemBytes);
+        if (e != cudaSuccess) return e;
+        ready.fetch_or(bit, std::memory_order_release);
+    }
+    int64_t blocks = 2 * static_cast<int64_t>(num_sms);
+    if (blocks > tiles) blocks = tiles;
+    wcast_tile_kernel<<<static_cast<unsigned>(blocks), kWtThreads, kWtSmemBytes, stream>>>(
+        map_w, map_q, rows, cols, qT, scales, rule, atoms_wT, atoms_w, status, tiles, limit);
     return cudaGetLastError();
 }
 
