@@ -23,6 +23,10 @@ struct DeviceState {
     bool supported = false;
     int num_sms = 0;
     unsigned int* status = nullptr;
+    // stream-K GEMM workspace: one partial 128 x 256 fp32 tile and one flag
+    // per SM (null if the allocation failed: stream-K is then not used)
+    float* sk_ws = nullptr;
+    unsigned int* sk_flags = nullptr;
 };
 
 std::mutex g_mutex;
@@ -59,6 +63,20 @@ fp8bs_status device_state(DeviceState** out)
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) return FP8BS_ERR_UNSUPPORTED;
         st.status = static_cast<unsigned int*>(ptr);
+        if (st.supported) {
+            void* ws = nullptr;
+            void* fl = nullptr;
+            const size_t ws_bytes = static_cast<size_t>(st.num_sms) * kBM * kBN * sizeof(float);
+            if (cudaMalloc(&ws, ws_bytes) == cudaSuccess && cudaMalloc(&fl, st.num_sms * sizeof(unsigned int)) == cudaSuccess &&
+                cudaMemset(fl, 0, st.num_sms * sizeof(unsigned int)) == cudaSuccess) {
+                st.sk_ws = static_cast<float*>(ws);
+                st.sk_flags = static_cast<unsigned int*>(fl);
+            } else {
+                if (ws) cudaFree(ws);
+                if (fl) cudaFree(fl);
+                cudaGetLastError();
+            }
+        }
         if (!g_encode) {
             void* fn = nullptr;
             cudaDriverEntryPointQueryResult q;
@@ -412,7 +430,25 @@ fp8bs_status run_rowwise_gemm(bool dgrad, const Offsets& o, const uint8_t* a, co
         p.tma_store = 1;
     }
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    const int64_t max_units = row_tiles * p.n_tiles * p.splits;
+    int64_t max_units = row_tiles * p.n_tiles * p.splits;
+    // Stream-K when the tiles fill the persistent grid's last round poorly
+    // (one group with host offsets, no split-K): every CTA then takes the
+    // same number of K-blocks, and a tile cut between two CTAs is finished
+    // by the first of them.
+    if (used <= 1 && o.groups == 1 && o.host && selftest_limit_ns == 0 && st->sk_ws && max_units > st->num_sms &&
+        max_units * p.kblocks < 0x7FFFFFFF - 2 * static_cast<int64_t>(st->num_sms) * p.kblocks) {
+        const int64_t grid = st->num_sms;
+        const int64_t rounds = (max_units + grid - 1) / grid;
+        if (static_cast<double>(max_units) < 0.9 * static_cast<double>(rounds * grid)) {
+            const int64_t total = max_units * p.kblocks;
+            p.sk_len = static_cast<int>((total + grid - 1) / grid);   // >= p.kblocks since max_units > grid
+            // a range of sk_len K-blocks touches at most this many tiles
+            p.sk_units = (p.sk_len + p.kblocks - 1) / p.kblocks + 1;
+            p.sk_ws = st->sk_ws;
+            p.sk_flags = st->sk_flags;
+            max_units = grid;
+        }
+    }
     const fp8bs_status r =
         launch_status(launch_gemm(GemmKind::kBlockScaleBf16, ma, mb, mo, p, max_units, st->num_sms, cs));
     if (r != FP8BS_OK || used <= 1) return r;
@@ -1230,6 +1266,9 @@ fp8bs_status fp8bs_device_status(int reset)
         const unsigned int zero = 0;
         if (cudaMemcpy(st->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
             return FP8BS_ERR_LAUNCH;
+        // a GEMM that gave up may have left stream-K partials unconsumed
+        if (st->sk_flags && cudaMemset(st->sk_flags, 0, st->num_sms * sizeof(unsigned int)) != cudaSuccess)
+            return FP8BS_ERR_LAUNCH;
     }
     return static_cast<fp8bs_status>(v);
 }
@@ -1244,6 +1283,8 @@ fp8bs_status fp8bs_last_device_status(void* stream, int reset)
     if (cudaMemcpyAsync(&v, st->status, sizeof(v), cudaMemcpyDeviceToHost, cs) != cudaSuccess)
         return FP8BS_ERR_LAUNCH;
     if (reset && cudaMemsetAsync(st->status, 0, sizeof(unsigned int), cs) != cudaSuccess) return FP8BS_ERR_LAUNCH;
+    if (reset && st->sk_flags && cudaMemsetAsync(st->sk_flags, 0, st->num_sms * sizeof(unsigned int), cs) != cudaSuccess)
+        return FP8BS_ERR_LAUNCH;
     if (cudaStreamSynchronize(cs) != cudaSuccess) return FP8BS_ERR_LAUNCH;
     return static_cast<fp8bs_status>(v);
 }
@@ -1259,6 +1300,8 @@ fp8bs_status fp8bs_copy_device_status(unsigned int* dst, int reset, void* stream
     if (cudaMemcpyAsync(dst, st->status, sizeof(unsigned int), cudaMemcpyDeviceToDevice, cs) != cudaSuccess)
         return FP8BS_ERR_LAUNCH;
     if (reset && cudaMemsetAsync(st->status, 0, sizeof(unsigned int), cs) != cudaSuccess) return FP8BS_ERR_LAUNCH;
+    if (reset && st->sk_flags && cudaMemsetAsync(st->sk_flags, 0, st->num_sms * sizeof(unsigned int), cs) != cudaSuccess)
+        return FP8BS_ERR_LAUNCH;
     return FP8BS_OK;
 }
 

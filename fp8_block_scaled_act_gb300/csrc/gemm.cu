@@ -122,6 +122,9 @@ struct SharedCtl {
     uint64_t tempty[2];
     uint64_t sempty[kScaleSlots];  // scale slot read by every epilogue warp
     uint64_t mma_done;        // final commit of the MMA thread (drain before exit)
+    uint64_t sk_part;         // stream-K: every epilogue warp has written its part of the partial
+    uint64_t sk_ready;        // stream-K: the continuation's partial has been published
+    int sk_ok;                // stream-K: verdict of the wait for it
     uint32_t tmem_base;
     volatile int abort;
     GroupTab tab;
@@ -250,9 +253,29 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, const GroupTab&
     nt = local - mt * p.n_tiles;
 }
 
+// Work unit u of the persistent loop (CTA u % gridDim.x, its (u / gridDim.x)-th
+// unit): tile u / splits and its split-K range, or with stream-K the
+// (u / gridDim.x)-th tile segment of CTA u % gridDim.x's K-block range
+// (nkb = 0 past the CTA's last segment). The host enables stream-K only when
+// tiles x K-blocks fits in 31 bits.
 __device__ __forceinline__ GroupInfo decode_unit(const GemmParams& p, const GroupTab& tab, int u, int& g, int& mt,
                                                  int& nt, int& split, int& kb0, int& nkb)
 {
+    if (p.sk_len != 0) {
+        const int c = u % static_cast<int>(gridDim.x);
+        const int j = u / static_cast<int>(gridDim.x);
+        const int nk = p.kblocks;
+        const int begin = c * p.sk_len;
+        const int end = min(tab.total_tiles * nk, begin + p.sk_len);
+        const int t0 = begin / nk;
+        const int start = j == 0 ? begin : (t0 + j) * nk;
+        const int t = min(t0 + j, tab.total_tiles - 1);
+        kb0 = start - t * nk;
+        nkb = start < end ? min(end, (t + 1) * nk) - start : 0;
+        split = 0;
+        decode_tile(p, tab, t, g, mt, nt);
+        return group_info(p, tab, g);
+    }
     const int t = u / p.splits;
     split = u - t * p.splits;
     decode_tile(p, tab, t, g, mt, nt);
@@ -261,6 +284,18 @@ __device__ __forceinline__ GroupInfo decode_unit(const GemmParams& p, const Grou
     const int end = min(gi.kblocks, kb0 + p.kb_per_split);
     nkb = max(0, end - kb0);
     return gi;
+}
+
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p)
+{
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(unsigned int* p, unsigned int v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -288,15 +323,21 @@ __device__ __forceinline__ bool epilogue_block_scale(const GemmParams& p, Shared
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t acc_it = 0;
 
-    const int units = ctl->tab.total_tiles * p.splits;
+    const int units = p.sk_len ? static_cast<int>(gridDim.x) * p.sk_units : ctl->tab.total_tiles * p.splits;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
         int g, mt, nt, split, kb0, nkb;
         int row0, nrows;   // the group's first row and row count (row groups: A rows = output rows)
+        int tile_kb;       // the tile's K-blocks (stream-K: nkb may cover part of them)
         {
             const GroupInfo gi = decode_unit(p, ctl->tab, u, g, mt, nt, split, kb0, nkb);
             row0 = gi.a_row0;
             nrows = gi.a_rows;
+            tile_kb = gi.kblocks;
         }
+        if (p.sk_len != 0 && nkb == 0) continue;   // stream-K: past this CTA's last segment
+        // stream-K role of this segment: 1 = continuation of a cut tile (the
+        // CTA's first segment), 2 = owner of a cut tile (its last), 0 = whole tile
+        const int sk_role = p.sk_len == 0 ? 0 : (kb0 > 0 ? 1 : (nkb < tile_kb ? 2 : 0));
         const int row = row0 + mt * kBM + r_in_tile;
         const bool row_ok = (mt * kBM + r_in_tile) < nrows;
         const int col0 = nt * kBN + half * 128;
@@ -360,6 +401,57 @@ __device__ __forceinline__ bool epilogue_block_scale(const GemmParams& p, Shared
             __syncwarp();
             if (lane == 0 && !p.hold_release) mbar_arrive(&ctl->tempty[buf]);
             promote(3, rb);
+        }
+
+        if (sk_role == 1) {
+            // stream-K continuation (this CTA's first segment): the fp32 sum
+            // goes to the CTA's workspace slot, float4 v of thread et at
+            // [v][et], and the slot is published for the tile's owner (CTA
+            // blockIdx.x - 1) once all eight warps have written their parts
+            const int et = ew * 32 + lane;
+            float4* slot = reinterpret_cast<float4*>(p.sk_ws) + static_cast<int64_t>(blockIdx.x) * 32 * 256;
+#pragma unroll
+            for (int v = 0; v < 32; ++v)
+                slot[v * 256 + et] = make_float4(acc[2 * v].x, acc[2 * v].y, acc[2 * v + 1].x, acc[2 * v + 1].y);
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->sk_part);
+            if (ew == 0 && lane == 0) {
+                if (!mbar_wait(&ctl->sk_part, 0u, limit)) return false;
+                st_release_gpu(p.sk_flags + blockIdx.x, 1u);
+            }
+            continue;
+        }
+        if (sk_role == 2) {
+            // stream-K owner of a cut tile (this CTA's last segment): add the
+            // rest of the tile, which CTA blockIdx.x + 1 computed first
+            if (ew == 0 && lane == 0) {
+                unsigned int* flag = p.sk_flags + blockIdx.x + 1;
+                bool got = ld_acquire_gpu(flag) == 1u;
+                const uint64_t t0 = global_timer_ns();
+                while (!got && !ctl->abort) {
+                    __nanosleep(64);
+                    got = ld_acquire_gpu(flag) == 1u;
+                    if (!got && global_timer_ns() - t0 > limit) break;
+                }
+                if (got) *flag = 0u;   // consumed: the slot is free for the next launch
+                ctl->sk_ok = got ? 1 : 0;
+                mbar_arrive(&ctl->sk_ready);
+            }
+            int ready = 0;
+            if (lane == 0) ready = mbar_wait(&ctl->sk_ready, 0u, limit) ? 1 : 0;
+            ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
+            if (ready) mbar_try_wait(&ctl->sk_ready, 0u);
+            if (!ready || !ctl->sk_ok) return false;
+            const int et = ew * 32 + lane;
+            const float4* slot =
+                reinterpret_cast<const float4*>(p.sk_ws) + static_cast<int64_t>(blockIdx.x + 1) * 32 * 256;
+#pragma unroll
+            for (int v = 0; v < 32; ++v) {
+                const float4 x = __ldcg(slot + v * 256 + et);
+                acc[2 * v] = make_float2(acc[2 * v].x + x.x, acc[2 * v].y + x.y);
+                acc[2 * v + 1] = make_float2(acc[2 * v + 1].x + x.z, acc[2 * v + 1].y + x.w);
+            }
         }
 
         if (p.ws != nullptr) {
@@ -570,6 +662,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int a = 0; a < kScaleSlots; ++a) mbar_init(&ctl->sempty[a], kEpiWarps);
         mbar_init(&ctl->mma_done, 1);
+        mbar_init(&ctl->sk_part, kEpiWarps);
+        mbar_init(&ctl->sk_ready, 1);
         ctl->abort = 0;
         fence_mbarrier_init();
         tma_prefetch_desc(&map_a);
@@ -597,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            const int units = ctl->tab.total_tiles * p.splits;
+            const int units = p.sk_len ? static_cast<int>(gridDim.x) * p.sk_units : ctl->tab.total_tiles * p.splits;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
                 int g, mt, nt, split, kb0, nkb;
                 const GroupInfo gi = decode_unit(p, ctl->tab, u, g, mt, nt, split, kb0, nkb);
@@ -656,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kBN);
             uint32_t it = 0, acc_it = 0;
             bool ok = true;
-            const int units = ctl->tab.total_tiles * p.splits;
+            const int units = p.sk_len ? static_cast<int>(gridDim.x) * p.sk_units : ctl->tab.total_tiles * p.splits;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
                 int g, mt, nt, split, kb0, nkb;
                 const GroupInfo gi = decode_unit(p, ctl->tab, u, g, mt, nt, split, kb0, nkb);

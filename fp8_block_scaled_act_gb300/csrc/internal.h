@@ -164,6 +164,16 @@ struct GemmParams {
     // K-block's buffer can only give up, which exercises the bounded waits,
     // the abort and the drain of a real GEMM without a fault.
     int hold_release;
+    // Stream-K (Fprop / Dgrad, one group, no split-K): sk_len > 0 gives CTA c
+    // the K-blocks [c sk_len, (c + 1) sk_len) of the tile-major (tile,
+    // K-block) sequence, so every CTA does the same work whatever the tile
+    // count. A tile cut between CTAs c and c + 1 (sk_len >= the tile's
+    // K-blocks, so at most one cut per tile) is finished by c, which adds the
+    // fp32 sum that c + 1 left in its workspace slot.
+    int sk_len;
+    int sk_units;                 // units per CTA (its most segments: stream-K loops run gridDim.x x sk_units)
+    float* sk_ws;                 // [grid][32][256] float4: one partial tile per CTA
+    unsigned int* sk_flags;       // [grid]: 1 while a slot holds a partial not yet added
 };
 
 enum class GemmKind {

@@ -24,7 +24,11 @@
  *
  * Common conventions
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library
- *     allocates nothing and keeps no reference after the call returns.
+ *     keeps no reference after the call returns. Its own device memory is a
+ *     status word, the fixed array of fp8_block_gemm_splitk_noalloc, and the
+ *     stream-K workspace of the GEMMs (one 128 x 256 fp32 tile and one flag
+ *     per SM, about 20 MB on a GB300), allocated once per device by the first
+ *     call on that device; make that first call before any stream capture.
  *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL is the legacy default stream). The returned status covers argument
  *     validation and launch errors only. Errors detected on the device (a
@@ -339,6 +343,14 @@ FP8BS_API fp8bs_status fp8_quant_dual_stash_sr(const void* x, int64_t rows, int6
 /* order are implementation details; results agree with the oracle within     */
 /* |d| <= 2e-3 * sum_k |a_k b_k| + 1e-6 (dequantized operands), plus one BF16 */
 /* rounding step for BF16 outputs.                                            */
+/* Fprop and Dgrad run stream-K when their output tiles would fill the last   */
+/* round of the persistent grid (one CTA per SM) below 90%: each CTA takes    */
+/* the same number of K-blocks, and a tile cut between two CTAs is summed in  */
+/* two fp32 parts. Results are deterministic for a given GPU (they depend on  */
+/* its SM count only through that summation order). A GEMM that gave up      */
+/* (FP8BS_ERR_TIMEOUT) may leave stream-K state behind: the status reset of   */
+/* fp8bs_device_status / fp8bs_last_device_status / fp8bs_copy_device_status  */
+/* clears it, and must come before the next GEMM on that device.             */
 /* ------------------------------------------------------------------------ */
 
 /* Fprop: Y[i,j] = sum_b s_x[i,b] * s_w[b, j/128] * P_b[i,j].

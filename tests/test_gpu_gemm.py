@@ -108,6 +108,31 @@ def test_fprop_dense_full_sampled():
     assert_gemm_close(y[ii, jj], ref, absprod_sampled(a, bt, ii, jj), True, "fprop dense full")
 
 
+@pytest.mark.parametrize("op", ["fprop", "dgrad"])
+def test_stream_k_every_element(op):
+    """200 output tiles (ragged rows, a half-empty last column tile) on a
+    152-SM GB300: the persistent grid's last round would be a third full,
+    so the GEMM runs stream-K, every CTA taking six K-blocks of the
+    tile-major sequence and tiles cut between two CTAs finished by the first
+    of them. Every element against the oracle; two launches bit-identical."""
+    M, C, Wd = 2483, 512, 2432          # rows, contraction, output width
+    a_src = wl.with_outliers((M, C), fraction=0.01, seed=41)
+    if op == "fprop":
+        w = wl.normal((C, Wd), std=wl.W_STD, seed=42)
+        y, (oaq, osa, owq, osw) = run_fprop(a_src, w)
+        ref = oracle.fprop(oaq, osa, owq, osw)
+        bound = np.abs(dequant_rows(oaq, osa)) @ np.abs(dequant_blocks(owq, osw))
+        again, _ = run_fprop(a_src, w)
+    else:
+        w = wl.normal((Wd, C), std=wl.W_STD, seed=43)
+        y, (oaq, osa, owq, osw) = run_dgrad(a_src, w)
+        ref = oracle.dgrad(oaq, osa, owq, osw)
+        bound = np.abs(dequant_rows(oaq, osa)) @ np.abs(dequant_blocks(owq, osw)).T
+        again, _ = run_dgrad(a_src, w)
+    assert_gemm_close(y, ref, bound, True, f"{op} stream-K {M}x{C}x{Wd}")
+    assert np.array_equal(y.view(np.uint32), again.view(np.uint32))
+
+
 # ---------------------------------------------------------------------------
 # Dgrad
 # ---------------------------------------------------------------------------
