@@ -133,6 +133,20 @@ def test_stream_k_every_element(op):
     assert np.array_equal(y.view(np.uint32), again.view(np.uint32))
 
 
+@pytest.mark.parametrize("K", [128, 384])
+def test_stream_k_short_contraction(K):
+    """Stream-K with one and three K-blocks per tile (200 tiles of 128 x 256:
+    ranges of two and four K-blocks, so with three per tile most tiles are
+    cut, some at their first K-block). Every element against the oracle."""
+    M, N = 12745, 512
+    x = wl.with_outliers((M, K), fraction=0.01, seed=K + 5)
+    w = wl.normal((K, N), std=wl.W_STD, seed=K + 6)
+    y, (oxq, osx, owq, osw) = run_fprop(x, w)
+    ref = oracle.fprop(oxq, osx, owq, osw)
+    bound = np.abs(dequant_rows(oxq, osx)) @ np.abs(dequant_blocks(owq, osw))
+    assert_gemm_close(y, ref, bound, True, f"fprop stream-K {M}x{K}x{N}")
+
+
 # ---------------------------------------------------------------------------
 # Dgrad
 # ---------------------------------------------------------------------------
