@@ -23,11 +23,41 @@ struct DeviceState {
     bool supported = false;
     int num_sms = 0;
     unsigned int* status = nullptr;
-    // stream-K GEMM workspace: one partial 128 x 256 fp32 tile and one flag
-    // per SM (null if the allocation failed: stream-K is then not used)
-    float* sk_ws = nullptr;
-    unsigned int* sk_flags = nullptr;
+    // stream-K GEMM workspaces, one per stream that has run a stream-K GEMM
+    // on this device (so that GEMMs on different streams never share one):
+    // one partial 128 x 256 fp32 tile and one flag per SM each
+    struct SkSlot {
+        cudaStream_t stream = nullptr;
+        float* ws = nullptr;
+        unsigned int* flags = nullptr;
+    };
+    static constexpr int kSkSlots = 8;
+    SkSlot sk[kSkSlots];
+    int sk_used = 0;
+    // the workspace of GEMMs captured into CUDA graphs (a capturing stream
+    // cannot allocate); allocated with the device's set-up
+    SkSlot sk_graph;
 };
+
+// One stream-K workspace (a partial tile and a flag per SM); false if the
+// allocation failed.
+bool alloc_stream_k(DeviceState& st, DeviceState::SkSlot& sl, cudaStream_t stream)
+{
+    void* ws = nullptr;
+    void* fl = nullptr;
+    const size_t ws_bytes = static_cast<size_t>(st.num_sms) * kBM * kBN * sizeof(float);
+    if (cudaMalloc(&ws, ws_bytes) != cudaSuccess || cudaMalloc(&fl, st.num_sms * sizeof(unsigned int)) != cudaSuccess ||
+        cudaMemset(fl, 0, st.num_sms * sizeof(unsigned int)) != cudaSuccess) {
+        if (ws) cudaFree(ws);
+        if (fl) cudaFree(fl);
+        cudaGetLastError();
+        return false;
+    }
+    sl.stream = stream;
+    sl.ws = static_cast<float*>(ws);
+    sl.flags = static_cast<unsigned int*>(fl);
+    return true;
+}
 
 std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
@@ -63,20 +93,7 @@ fp8bs_status device_state(DeviceState** out)
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) return FP8BS_ERR_UNSUPPORTED;
         st.status = static_cast<unsigned int*>(ptr);
-        if (st.supported) {
-            void* ws = nullptr;
-            void* fl = nullptr;
-            const size_t ws_bytes = static_cast<size_t>(st.num_sms) * kBM * kBN * sizeof(float);
-            if (cudaMalloc(&ws, ws_bytes) == cudaSuccess && cudaMalloc(&fl, st.num_sms * sizeof(unsigned int)) == cudaSuccess &&
-                cudaMemset(fl, 0, st.num_sms * sizeof(unsigned int)) == cudaSuccess) {
-                st.sk_ws = static_cast<float*>(ws);
-                st.sk_flags = static_cast<unsigned int*>(fl);
-            } else {
-                if (ws) cudaFree(ws);
-                if (fl) cudaFree(fl);
-                cudaGetLastError();
-            }
-        }
+        if (st.supported) alloc_stream_k(st, st.sk_graph, nullptr);
         if (!g_encode) {
             void* fn = nullptr;
             cudaDriverEntryPointQueryResult q;
@@ -293,6 +310,41 @@ bool cached_batch_map(CUtensorMap* m, bool bf16, const void* base, uint64_t cols
     return true;
 }
 
+// The stream-K workspace for a GEMM on `stream`: a capturing stream gets the
+// device's graph workspace; any other stream its own, allocated by its first
+// stream-K GEMM. Null when none can be had (the table is full or the
+// allocation failed): the GEMM then runs without stream-K.
+DeviceState::SkSlot* stream_k_slot(DeviceState* st, cudaStream_t stream)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (cap != cudaStreamCaptureStatusNone) return st->sk_graph.ws ? &st->sk_graph : nullptr;
+    for (int i = 0; i < st->sk_used; ++i)
+        if (st->sk[i].stream == stream) return &st->sk[i];
+    if (st->sk_used == DeviceState::kSkSlots) return nullptr;
+    if (!alloc_stream_k(*st, st->sk[st->sk_used], stream)) return nullptr;
+    return &st->sk[st->sk_used++];
+}
+
+// Clears the stream-K flags of every workspace of this device (a GEMM that
+// gave up may have left a published partial unconsumed).
+cudaError_t clear_stream_k_flags(DeviceState* st, cudaStream_t stream, bool async)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    const size_t n = st->num_sms * sizeof(unsigned int);
+    for (int i = -1; i < st->sk_used; ++i) {
+        unsigned int* f = i < 0 ? st->sk_graph.flags : st->sk[i].flags;
+        if (!f) continue;
+        const cudaError_t e = async ? cudaMemsetAsync(f, 0, n, stream) : cudaMemset(f, 0, n);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 void init_params(GemmParams& p, DeviceState* st, int n_cols)
 {
     std::memset(&p, 0, sizeof(p));
@@ -435,17 +487,19 @@ fp8bs_status run_rowwise_gemm(bool dgrad, const Offsets& o, const uint8_t* a, co
     // (one group with host offsets, no split-K): every CTA then takes the
     // same number of K-blocks, and a tile cut between two CTAs is finished
     // by the first of them.
-    if (used <= 1 && o.groups == 1 && o.host && selftest_limit_ns == 0 && st->sk_ws && max_units > st->num_sms &&
+    if (used <= 1 && o.groups == 1 && o.host && selftest_limit_ns == 0 && max_units > st->num_sms &&
         max_units * p.kblocks < 0x7FFFFFFF - 2 * static_cast<int64_t>(st->num_sms) * p.kblocks) {
         const int64_t grid = st->num_sms;
         const int64_t rounds = (max_units + grid - 1) / grid;
-        if (static_cast<double>(max_units) < 0.9 * static_cast<double>(rounds * grid)) {
+        DeviceState::SkSlot* sl = nullptr;
+        if (static_cast<double>(max_units) < 0.9 * static_cast<double>(rounds * grid) &&
+            (sl = stream_k_slot(st, cs)) != nullptr) {
             const int64_t total = max_units * p.kblocks;
             p.sk_len = static_cast<int>((total + grid - 1) / grid);   // >= p.kblocks since max_units > grid
             // a range of sk_len K-blocks touches at most this many tiles
             p.sk_units = (p.sk_len + p.kblocks - 1) / p.kblocks + 1;
-            p.sk_ws = st->sk_ws;
-            p.sk_flags = st->sk_flags;
+            p.sk_ws = sl->ws;
+            p.sk_flags = sl->flags;
             max_units = grid;
         }
     }
@@ -1267,8 +1321,7 @@ fp8bs_status fp8bs_device_status(int reset)
         if (cudaMemcpy(st->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
             return FP8BS_ERR_LAUNCH;
         // a GEMM that gave up may have left stream-K partials unconsumed
-        if (st->sk_flags && cudaMemset(st->sk_flags, 0, st->num_sms * sizeof(unsigned int)) != cudaSuccess)
-            return FP8BS_ERR_LAUNCH;
+        if (clear_stream_k_flags(st, nullptr, false) != cudaSuccess) return FP8BS_ERR_LAUNCH;
     }
     return static_cast<fp8bs_status>(v);
 }
@@ -1283,8 +1336,7 @@ fp8bs_status fp8bs_last_device_status(void* stream, int reset)
     if (cudaMemcpyAsync(&v, st->status, sizeof(v), cudaMemcpyDeviceToHost, cs) != cudaSuccess)
         return FP8BS_ERR_LAUNCH;
     if (reset && cudaMemsetAsync(st->status, 0, sizeof(unsigned int), cs) != cudaSuccess) return FP8BS_ERR_LAUNCH;
-    if (reset && st->sk_flags && cudaMemsetAsync(st->sk_flags, 0, st->num_sms * sizeof(unsigned int), cs) != cudaSuccess)
-        return FP8BS_ERR_LAUNCH;
+    if (reset && clear_stream_k_flags(st, cs, true) != cudaSuccess) return FP8BS_ERR_LAUNCH;
     if (cudaStreamSynchronize(cs) != cudaSuccess) return FP8BS_ERR_LAUNCH;
     return static_cast<fp8bs_status>(v);
 }
@@ -1300,8 +1352,7 @@ fp8bs_status fp8bs_copy_device_status(unsigned int* dst, int reset, void* stream
     if (cudaMemcpyAsync(dst, st->status, sizeof(unsigned int), cudaMemcpyDeviceToDevice, cs) != cudaSuccess)
         return FP8BS_ERR_LAUNCH;
     if (reset && cudaMemsetAsync(st->status, 0, sizeof(unsigned int), cs) != cudaSuccess) return FP8BS_ERR_LAUNCH;
-    if (reset && st->sk_flags && cudaMemsetAsync(st->sk_flags, 0, st->num_sms * sizeof(unsigned int), cs) != cudaSuccess)
-        return FP8BS_ERR_LAUNCH;
+    if (reset && clear_stream_k_flags(st, cs, true) != cudaSuccess) return FP8BS_ERR_LAUNCH;
     return FP8BS_OK;
 }
 

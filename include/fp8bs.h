@@ -26,9 +26,15 @@
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library
  *     keeps no reference after the call returns. Its own device memory is a
  *     status word, the fixed array of fp8_block_gemm_splitk_noalloc, and the
- *     stream-K workspace of the GEMMs (one 128 x 256 fp32 tile and one flag
- *     per SM, about 20 MB on a GB300), allocated once per device by the first
- *     call on that device; make that first call before any stream capture.
+ *     stream-K workspaces of Fprop / Dgrad (one 128 x 256 fp32 tile and one
+ *     flag per SM, about 20 MB on a GB300): one per stream that runs a
+ *     stream-K GEMM eagerly (up to eight per device, each allocated by the
+ *     first such GEMM on its stream; beyond eight, GEMMs on further streams
+ *     run without stream-K), and one shared by every stream-K GEMM captured
+ *     into a CUDA graph, allocated with the device's set-up by the first call
+ *     on the device. Make that first call, and the first Fprop / Dgrad on a
+ *     stream, before any stream capture begins. Graphs holding stream-K
+ *     GEMMs share their workspace: do not replay two of them concurrently.
  *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL is the legacy default stream). The returned status covers argument
  *     validation and launch errors only. Errors detected on the device (a
@@ -346,8 +352,9 @@ FP8BS_API fp8bs_status fp8_quant_dual_stash_sr(const void* x, int64_t rows, int6
 /* Fprop and Dgrad run stream-K when their output tiles would fill the last   */
 /* round of the persistent grid (one CTA per SM) below 90%: each CTA takes    */
 /* the same number of K-blocks, and a tile cut between two CTAs is summed in  */
-/* two fp32 parts. Results are deterministic for a given GPU (they depend on  */
-/* its SM count only through that summation order). A GEMM that gave up      */
+/* two fp32 parts, through a workspace private to the call's stream. Results */
+/* are deterministic for a given GPU (they depend on its SM count only       */
+/* through that summation order). A GEMM that gave up                        */
 /* (FP8BS_ERR_TIMEOUT) may leave stream-K state behind: the status reset of   */
 /* fp8bs_device_status / fp8bs_last_device_status / fp8bs_copy_device_status  */
 /* clears it, and must come before the next GEMM on that device.             */

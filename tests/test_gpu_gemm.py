@@ -133,6 +133,44 @@ def test_stream_k_every_element(op):
     assert np.array_equal(y.view(np.uint32), again.view(np.uint32))
 
 
+def test_stream_k_on_two_streams_at_once():
+    """Two stream-K Fprops issued on two streams with no ordering between
+    them each keep their own workspace: both results equal the same GEMMs
+    run one after the other."""
+    M, K, N = 2483, 512, 2432
+    runs = []
+    for seed in (51, 52):
+        x = wl.with_outliers((M, K), fraction=0.01, seed=seed)
+        w = wl.normal((K, N), std=wl.W_STD, seed=seed + 10)
+        xq, sx = fp8bs.empty_quant_1x128(M, K)
+        fp8bs.fp8_quant_1x128(x.cuda(), xq, sx)
+        wq, wqT, sw = fp8bs.empty_quant_128x128(K, N)
+        fp8bs.fp8_quant_128x128(w.cuda(), wq, wqT, sw)
+        runs.append((xq, sx, wqT, sw))
+    torch.cuda.synchronize()
+    serial = []
+    for xq, sx, wqT, sw in runs:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        fp8bs.fp8_block_gemm_fprop(xq, sx, wqT, sw, y)
+        torch.cuda.synchronize()
+        serial.append(y)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for st in streams:   # each stream's first stream-K GEMM (sets up its workspace)
+        with torch.cuda.stream(st):
+            xq, sx, wqT, sw = runs[0]
+            fp8bs.fp8_block_gemm_fprop(xq, sx, wqT, sw, torch.empty((M, N), dtype=torch.bfloat16, device="cuda"))
+    torch.cuda.synchronize()
+    outs = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in runs]
+    for _ in range(4):
+        for st, (xq, sx, wqT, sw), y in zip(streams, runs, outs):
+            with torch.cuda.stream(st):
+                fp8bs.fp8_block_gemm_fprop(xq, sx, wqT, sw, y)
+    torch.cuda.synchronize()
+    assert fp8bs.fp8bs_device_status(reset=True) == 0
+    for y, ref in zip(outs, serial):
+        assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
+
+
 @pytest.mark.parametrize("K", [128, 384])
 def test_stream_k_short_contraction(K):
     """Stream-K with one and three K-blocks per tile (200 tiles of 128 x 256:
