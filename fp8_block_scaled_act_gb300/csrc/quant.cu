@@ -1684,9 +1684,10 @@ cudaError_t launch_quant_1x128_stream(const CUtensorMap& map_x, const CUtensorMa
         if (e != cudaSuccess) return e;
         ready.fetch_or(bit, std::memory_order_release);
     }
+    // as many SMs as the units can keep busy (one unit per warp at least):
+    // a small tensor then finishes in about one unit's latency
     const int64_t units = ((cols + 127) / 128) * ((rows + 31) / 32);
-    const int64_t warps = (units + kQ1sSlots - 1) / kQ1sSlots;   // at least three units per warp when possible
-    int64_t blocks = (warps + kQ1sWarps - 1) / kQ1sWarps;
+    int64_t blocks = (units + kQ1sWarps - 1) / kQ1sWarps;
     if (blocks > num_sms) blocks = num_sms;
     quant_1x128_stream_kernel<<<static_cast<unsigned>(blocks), kQ1sWarps * 32, kSmem, stream>>>(
         map_x, map_q, rows, cols, scales, scale_ld, rule, limit, status);
