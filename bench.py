@@ -7,12 +7,14 @@ copy), the 1x128 quantization of X, Fprop, the dual-orientation cast of dY
 128x1 transposed requant of X from its E4M3 stash, and Wgrad. Default workload: X 4096x7168 (N(0,1) with 0.1% outliers),
 W 7168x2048 (N(0,0.02^2)), dY 4096x2048 (N(0,1e-3^2)); its numbers are the
 line's headline keys. After it the default run times, each the same way and
-reported under its own key of ``configs``: the grouped MoE expert pass (32
-experts, 8192 routed rows, group offsets in device memory), the 256 x K x 256
-split-K Fprop of the long-contraction workload (K = 1024 ... 65536) and the
-standalone 1x128 cast of a 16384 x 16384 tensor (``--dense-only`` skips
-them). ``--workload moe|moe_ue8m0|longk|quant16k|dense_ue8m0`` times one of those (or
-the dense step with power-of-two scales) as the headline instead.
+reported under its own key of ``configs``: the same dense step with
+power-of-two scales on the block-scaled MMA, the grouped MoE expert pass (32
+experts, 8192 routed rows, group offsets in device memory) with fp32 and
+with power-of-two scales, the 256 x K x 256 split-K Fprop of the
+long-contraction workload (K = 1024 ... 65536) and the standalone 1x128 cast
+of a 16384 x 16384 tensor (``--dense-only`` skips them).
+``--workload moe|moe_ue8m0|longk|quant16k|dense_ue8m0`` times one of those as
+the headline instead.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -752,7 +754,7 @@ def make_workload(name, fp8bs, torch, device, rank):
 # its own key of "configs": the grouped MoE pass (fp32 scales with software
 # promotion, and power-of-two scales on the tensor core's block scaling), the
 # long-K sweep and the standalone 16384 x 16384 1x128 cast.
-EXTRA_WORKLOADS = ("moe", "moe_ue8m0", "longk", "quant16k")
+EXTRA_WORKLOADS = ("dense_ue8m0", "moe", "moe_ue8m0", "longk", "quant16k")
 
 
 def run_ours(args, world, rank, local):
