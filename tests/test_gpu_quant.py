@@ -135,6 +135,21 @@ def test_quant_128x128_batched_experts():
         assert np.array_equal(sc[e], osc)
 
 
+@pytest.mark.parametrize("B,R,C", [(3, 144, 400), (2, 16, 16), (4, 272, 144)])
+def test_quant_128x128_batched_ragged(B, R, C):
+    """Batched weights whose rows are not a multiple of 128: a block at an
+    expert's ragged edge must not read the next expert's rows (they count as
+    zeros), and every expert's codes, transposed copy and scales equal the
+    oracle's cast of that expert alone."""
+    w = torch.stack([_special_inputs(R, C, seed=100 * b + R + C) for b in range(B)])
+    q, qT, sc = _gpu_quant_128x128(w)
+    for e in range(B):
+        oq, osc = oracle.quant_128x128(u16(w[e]))
+        assert np.array_equal(q[e], oq), f"expert {e}"
+        assert np.array_equal(qT[e], oq.T), f"expert {e} transposed"
+        assert np.array_equal(sc[e].view(np.uint32), osc.view(np.uint32)), f"expert {e} scales"
+
+
 def test_quant_128x128_dense_weight_full():
     w = wl.dense(M=128)["W"]
     q, qT, sc = _gpu_quant_128x128(w)
