@@ -1,4 +1,4 @@
-// mx.cu -- MXFP8 (NEXT-2): 1x32 blocks with power-of-two exponent scales,
+// mx.cu -- MXFP8: 1x32 blocks with power-of-two exponent scales,
 // and a GEMM whose block scaling runs in the tensor core.
 //
 // Format (OCP Microscaling Formats (MX) v1.0): 32 consecutive elements along

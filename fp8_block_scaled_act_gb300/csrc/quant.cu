@@ -164,7 +164,7 @@ __device__ __forceinline__ uint2 quant8(const uint4& d, const TileScale& t)
 }
 
 // ---------------------------------------------------------------------------
-// Stochastic rounding (NEXT-3). The random word of element idx (its linear
+// Stochastic rounding. The random word of element idx (its linear
 // index in the quantized tensor) under (seed, salt) is word idx % 4 of
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC 2011) with key (seed low,
 // seed high) and counter (idx / 4 low, idx / 4 high, salt, 0): stateless,
@@ -1147,7 +1147,7 @@ __global__ void __launch_bounds__(kQ3Threads, kSR ? 2 : (kStash ? 3 : 4)) requan
 
 
 // ---------------------------------------------------------------------------
-// Dense dual cast (NEXT-1) and fused forward cast + stash requant (NEXT-1b)
+// Dense dual cast and fused forward cast + stash requant
 // with round-to-nearest codes: a persistent kernel, two CTAs of 256 threads
 // per SM, each CTA working through 128 x 128 blocks. A block arrives by TMA
 // as two boxes of 64 columns x 128 rows (128-byte swizzle: 16-byte chunk c

@@ -184,7 +184,7 @@ FP8BS_API fp8bs_status fp8_requant_128x1_T(int src_mode, const void* src, const 
                                  const int32_t* group_offsets_host, int32_t groups,
                                  uint8_t* qT, float* scalesT, void* stream);
 
-/* NEXT-1: dual-orientation cast of one BF16 tensor in a single read: the    */
+/* Dual-orientation cast of one BF16 tensor in a single read: the    */
 /* 1x128 cast of fp8_quant_1x128 and the 128x1 transposed cast of            */
 /* fp8_requant_128x1_T (FP8BS_SRC_BF16), both outputs byte-identical to the  */
 /* two separate calls. [P1] "What is asserted, and from where": the output   */
@@ -203,7 +203,7 @@ FP8BS_API fp8bs_status fp8_quant_dual(const void* x, int64_t rows, int64_t cols,
                                       uint8_t* q, float* scales, uint8_t* qT, float* scalesT,
                                       void* stream);
 
-/* NEXT-4: scale rule options for the four quantizers above. The pages name  */
+/* Scale rule options for the four quantizers above. The pages name  */
 /* the conventions without fixing every detail ([P4] conventions table, rows */
 /* "Weight floors", "Two-stage weights", "Activation floors", "Compact       */
 /* formats"); the reading implemented here:                                   */
@@ -285,7 +285,7 @@ FP8BS_API fp8bs_status fp8_quant_dual_stash_dev(const void* x, int64_t rows, int
                                                 const fp8bs_scale_opts* opts, void* stream);
 
 
-/* NEXT-3: stochastic rounding. The 1x128 and 128x128 casts above with the   */
+/* Stochastic rounding. The 1x128 and 128x128 casts above with the   */
 /* E4M3 rounding step made stochastic under a stateless (seed, salt,         */
 /* element) contract ([P4] "SR agreement": a stateless seed / salt / counter */
 /* scheme with a lower / upper-magnitude rule; [P4] "Remaining differences"  */
@@ -462,7 +462,7 @@ FP8BS_API fp8bs_status fp8_block_gemm_splitk_noalloc(int op, const uint8_t* a, c
                                            int64_t M, int64_t N, int64_t K, int32_t splits,
                                            void* out, void* stream);
 
-/* NEXT-2: MXFP8, the format TransformerEngine's pages benchmark on B300    */
+/* MXFP8, the format TransformerEngine's pages benchmark on B300    */
 /* ([P3] "Changes" and "Performance": MXFP8 operands for dgrad): OCP MX v1.0 */
 /* blocks of 32 elements along K with one 8-bit exponent scale              */
 /* X = 2^(E - 127) each, E4M3 elements, and the block scaling applied by the */
@@ -497,7 +497,7 @@ FP8BS_API fp8bs_status fp8_mx_gemm_f32(const uint8_t* a, const uint8_t* a_scale_
                                        const uint8_t* b, const uint8_t* b_scale_atoms,
                                        int64_t M, int64_t N, int64_t K, float* out, void* stream);
 
-/* NEXT-2 / NEXT-4 for experts: the MX GEMMs above applied to each group     */
+/* For experts: the MX GEMMs above applied to each group     */
 /* (expert) g, with the group offsets of fp8_block_gemm_grouped (exactly one */
 /* of offsets_dev / offsets_host; rows = the total token rows). The MoE form */
 /* is the grouped path of TransformerEngine PR #3573 ("Changes": grouped     */
@@ -548,7 +548,7 @@ FP8BS_API fp8bs_status fp8_mx_gemm_grouped(int op, int32_t groups, const int32_t
 FP8BS_API fp8bs_status fp8_mx_quant_1x32_T(const void* x, int64_t rows, int64_t cols, uint8_t* qT,
                                            uint8_t* scale_atoms, void* stream);
 
-/* NEXT-4: the packed Blackwell scale layout for power-of-two scales ([P4]  */
+/* The packed Blackwell scale layout for power-of-two scales ([P4]  */
 /* conventions table, row "Compact formats": fp32 scale containers on Hopper, */
 /* packed exponent bytes on Blackwell, packed at the GEMM boundary). Writes   */
 /* the exponent byte E of each fp32 scale s = 2^(E - 127) of a block-scaled   */
@@ -578,7 +578,7 @@ FP8BS_API fp8bs_status fp8_pack_ue8m0(const float* scales, int64_t rows, int64_t
                                       int64_t row_stride, int64_t kb_stride, uint8_t* scale_atoms,
                                       void* stream);
 
-/* NEXT-4 for experts: fp8_pack_ue8m0 for the grouped rows of a 1x128-cast   */
+/* For experts: fp8_pack_ue8m0 for the grouped rows of a 1x128-cast   */
 /* operand [rows x K] (the A of a grouped Fprop or Dgrad), into the groups'  */
 /* tile layout that fp8_mx_gemm_grouped reads: the scale of (row r, K-block  */
 /* b) is scales[r + b * kb_stride] (the S1 layout: kb_stride =               */
@@ -593,7 +593,7 @@ FP8BS_API fp8bs_status fp8_pack_ue8m0_grouped(const float* scales, int64_t rows,
                                               int32_t groups, const int32_t* offsets_dev,
                                               const int32_t* offsets_host, uint8_t* scale_atoms, void* stream);
 
-/* NEXT-4: the casts with their scales already packed. The same casts as   */
+/* The casts with their scales already packed. The same casts as   */
 /* fp8_quant_128x128_opts, fp8_quant_dual_opts and fp8_quant_dual_stash_opts */
 /* under the UE8M0 rule (opts->rule must be FP8BS_SCALE_UE8M0, else          */
 /* FP8BS_ERR_ARG), which in the same pass also write the exponent bytes of  */

@@ -411,7 +411,7 @@ void oracle_quant_128x128(const uint16_t* x, i64 rows, i64 cols, i64 ldx,
 }
 
 /* ------------------------------------------------------------------------- */
-/* MXFP8 (NEXT-2): 1x32 blocks with power-of-two (UE8M0) scales.              */
+/* MXFP8: 1x32 blocks with power-of-two (UE8M0) scales.              */
 /* ------------------------------------------------------------------------- */
 
 /* OCP Microscaling Formats (MX) v1.0: a block of 32 consecutive elements

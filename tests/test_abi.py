@@ -180,7 +180,7 @@ def test_splitk_workspace_arithmetic_and_argument_errors():
 
 
 def test_ue8m0_packing_argument_validation(L):
-    """NEXT-4 entries reject bad arguments on the host: the packing's row
+    """The packing entries reject bad arguments on the host: the packing's row
     block, shapes, pointers and alignment; the packed casts' rule (UE8M0
     only), shapes and atom pointers."""
     buf = ctypes.create_string_buffer(1 << 12)

@@ -1,4 +1,4 @@
-"""GPU parity of the MXFP8 path (NEXT-2) against the oracle: the 1x32
+"""GPU parity of the MXFP8 path against the oracle: the 1x32
 quantizer byte for byte (codes and exponent bytes, read back from the scale
 atoms), and the hardware block-scaled GEMM within the GEMM tolerance
 |d| <= 2e-3 * sum_k |a_k b_k| + 1e-6 plus one BF16 ulp."""

@@ -1,5 +1,5 @@
-"""GPU parity of the grouped (MoE expert) MX path, NEXT-2 / NEXT-4 for
-experts: fp8_pack_ue8m0_grouped byte for byte against the oracle's packing of
+"""GPU parity of the grouped (MoE expert) MX path, hardware block scaling
+with power-of-two scales: fp8_pack_ue8m0_grouped byte for byte against the oracle's packing of
 each group's 1x128 power-of-two scales placed in the groups' tile layout, and
 fp8_mx_gemm_grouped (Fprop, Dgrad, Wgrad on the tensor core's block scaling)
 per expert against the oracle's promoted GEMMs of the same UE8M0-rule codes

@@ -338,7 +338,7 @@ def _oracle_rule(r):
 
 @pytest.mark.parametrize("r", RULES)
 def test_scale_rules_all_quantizers(r):
-    """NEXT-4 scale rules (UE8M0 scales, amax and scale floors) on every
+    """Scale rules (UE8M0 scales, amax and scale floors) on every
     quantizer, byte- and bit-exact against the oracle under the same rule;
     the inputs include an all-zero tile, where the floors decide the scale."""
     M, C = 300, 384
@@ -394,7 +394,7 @@ def test_scale_rule_rejects_bad_options():
 
 @pytest.mark.parametrize("R,C,seed,salt", [(300, 384, 0, 0), (129, 2048, 2 ** 40 + 17, 3), (1, 16, 7, 0xFFFFFFFF)])
 def test_sr_quant_1x128_matches_oracle(R, C, seed, salt):
-    """NEXT-3: stochastic rounding under (seed, salt), byte- and bit-exact
+    """Stochastic rounding under (seed, salt), byte- and bit-exact
     against the oracle's independent Philox4x32-10 and rounding rule."""
     x = _special_inputs(R, C, seed=R + C + 5)
     q, sc = fp8bs.empty_quant_1x128(R, C)
@@ -423,7 +423,7 @@ def test_sr_quant_128x128_batched_matches_oracle():
     (400, 128, [0, 129, 1, 0, 270], 11, 5),
 ])
 def test_sr_requant_both_sources_match_oracle(M, C, counts, seed, salt):
-    """NEXT-3 on the transposed cast: stochastic rounding from BF16 and from
+    """Stochastic rounding on the transposed cast from BF16 and from
     an E4M3 stash, byte- and bit-exact against the oracle (source element
     (r, c) takes word r * C + c; ragged token tiles and groups included)."""
     x = _special_inputs(M, C, seed=M + 13 * C)

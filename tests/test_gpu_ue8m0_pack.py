@@ -1,5 +1,5 @@
-"""GPU parity of the packed Blackwell scale layout for power-of-two scales
-(NEXT-4): fp8_pack_ue8m0 byte for byte against the oracle's packing (read
+"""GPU parity of the packed Blackwell scale layout for power-of-two scales:
+fp8_pack_ue8m0 byte for byte against the oracle's packing (read
 back from the scale atoms) for the four operand layouts, the error it
 records for a scale without an exponent byte, and the recipe's three GEMMs
 run through the MX kernel on packed UE8M0 operands against the oracle's
