@@ -24,7 +24,7 @@ from . import _build_lib
 __all__ = [
     "Fp8bsError", "build", "lib", "lib_path",
     "fp8_quant_1x128", "fp8_quant_128x128", "fp8_requant_128x1_T", "fp8_quant_dual",
-    "fp8_block_gemm_fprop", "fp8_block_gemm_dgrad", "fp8_block_gemm_wgrad",
+    "fp8_block_gemm_fprop", "fp8_block_gemm_fprop_wkn", "fp8_block_gemm_dgrad", "fp8_block_gemm_wgrad",
     "fp8_block_gemm_grouped", "fp8_block_gemm_splitk", "fp8bs_splitk_workspace_size",
     "fp8bs_splitk_default_splits", "fp8_block_gemm_splitk_noalloc", "NOALLOC_SCRATCH_BYTES",
     "fp8bs_device_status", "fp8bs_last_device_status", "fp8bs_copy_device_status", "fp8bs_set_wait_limit_ns",
@@ -32,7 +32,7 @@ __all__ = [
     "fp8bs_selftest_wait_timeout", "fp8bs_selftest_gemm_timeout", "fp8bs_scale_ld", "fp8bs_padded_tokens",
     "fp8bs_status_str", "fp8bs_version",
     "empty_quant_1x128", "empty_quant_128x128", "empty_requant_128x1_T",
-    "SRC_BF16", "SRC_E4M3", "OP_FPROP", "OP_DGRAD", "OP_WGRAD", "MAX_GROUPS",
+    "SRC_BF16", "SRC_E4M3", "OP_FPROP", "OP_DGRAD", "OP_WGRAD", "OP_FPROP_WKN", "MAX_GROUPS",
     "SCALE_FP32", "SCALE_UE8M0", "ScaleOpts", "fp8_quant_1x128_opts", "fp8_quant_128x128_opts",
     "fp8_requant_128x1_T_opts", "fp8_quant_dual_opts", "fp8_quant_1x128_sr", "fp8_quant_128x128_sr",
     "fp8_quant_dual_stash", "fp8_quant_dual_stash_opts", "fp8_requant_128x1_T_sr", "fp8_quant_dual_sr",
@@ -45,7 +45,7 @@ __all__ = [
 
 SRC_BF16, SRC_E4M3 = 0, 1
 SCALE_FP32, SCALE_UE8M0 = 0, 1
-OP_FPROP, OP_DGRAD, OP_WGRAD = 0, 1, 2
+OP_FPROP, OP_DGRAD, OP_WGRAD, OP_FPROP_WKN = 0, 1, 2, 3
 MAX_GROUPS = 256
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024   # FP8BS_NOALLOC_SCRATCH_BYTES
 STATUS_NAMES = {0: "OK", 1: "ERR_ARG", 2: "ERR_ALIGN", 3: "ERR_SHAPE", 4: "ERR_LAUNCH",
@@ -119,6 +119,7 @@ def lib() -> ctypes.CDLL:
         "fp8_quant_dual_stash_packed": ([P, I64, I64, P, P, P, P, P, P, P, P], S),
         "fp8_quant_128x128_sr": ([P, I64, I64, I64, I64, P, P, P, ctypes.c_uint64, ctypes.c_uint32, P, P], S),
         "fp8_block_gemm_fprop": ([P, P, P, P, I64, I64, I64, P, P], S),
+        "fp8_block_gemm_fprop_wkn": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_block_gemm_dgrad": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_block_gemm_wgrad": ([P, P, P, P, I64, I64, I64, P, I, P], S),
         "fp8_block_gemm_grouped": ([I, I32, P, P, I64, P, P, P, P, I64, I64, P, I, P], S),
@@ -674,6 +675,20 @@ def fp8_block_gemm_fprop(xq, sx, wqT, sw, y, stream=None) -> None:
         _ptr(xq), _ptr(sx), _ptr(wqT), _ptr(sw), M, N, K, _ptr(y), _stream(stream)))
 
 
+def fp8_block_gemm_fprop_wkn(xq, sx, wq, sw, y, stream=None) -> None:
+    """Y[M x N] (BF16) = X W from xq [M x K], sx, wq [K x N] (W's codes as
+    the 128x128 cast wrote them), sw [K/128 x N/128]."""
+    for t, n, d in ((xq, "xq", torch.uint8), (sx, "sx", torch.float32), (wq, "wq", torch.uint8),
+                    (sw, "sw", torch.float32), (y, "y", torch.bfloat16)):
+        _need(t, d, n)
+    M, K = xq.shape
+    N = wq.shape[1]
+    if wq.shape != (K, N) or y.shape != (M, N):
+        raise ValueError("shape mismatch")
+    _check("fp8_block_gemm_fprop_wkn", lib().fp8_block_gemm_fprop_wkn(
+        _ptr(xq), _ptr(sx), _ptr(wq), _ptr(sw), M, N, K, _ptr(y), _stream(stream)))
+
+
 def fp8_block_gemm_dgrad(dyq, sdy, wq, sw, dx, stream=None) -> None:
     """dX[M x K] (BF16) = dY W^T from dyq [M x N], sdy, wq [K x N], sw."""
     for t, n, d in ((dyq, "dyq", torch.uint8), (sdy, "sdy", torch.float32), (wq, "wq", torch.uint8),
@@ -781,13 +796,19 @@ def _splitk_dims(op: int, a, b):
         if b.shape != (N, K):
             raise ValueError("shape mismatch")
         return M, N, K, (M, N)
+    if op == OP_FPROP_WKN:  # a = xq [M x K], b = wq [K x N]
+        M, K = a.shape
+        N = b.shape[1]
+        if b.shape != (K, N):
+            raise ValueError("shape mismatch")
+        return M, N, K, (M, N)
     if op == OP_DGRAD:      # a = dyq [M x N], b = wq [K x N]
         M, N = a.shape
         K = b.shape[0]
         if b.shape != (K, N):
             raise ValueError("shape mismatch")
         return M, N, K, (M, K)
-    raise ValueError("split-K supports OP_FPROP and OP_DGRAD")
+    raise ValueError("split-K supports OP_FPROP, OP_FPROP_WKN and OP_DGRAD")
 
 
 def fp8bs_splitk_workspace_size(op: int, M: int, N: int, K: int, splits: int) -> int:
@@ -800,7 +821,8 @@ def fp8bs_splitk_default_splits(op: int, M: int, N: int, K: int) -> int:
 
 def fp8_block_gemm_splitk(op: int, a, sa, b, sb, out, splits: Optional[int] = None,
                           workspace: Optional[torch.Tensor] = None, stream=None) -> None:
-    """Split-K Fprop (a = xq, b = wqT) or Dgrad (a = dyq, b = wq) into BF16 `out`.
+    """Split-K Fprop (a = xq, b = wqT; OP_FPROP_WKN: b = wq) or Dgrad (a = dyq,
+    b = wq) into BF16 `out`.
 
     `splits` defaults to fp8bs_splitk_default_splits. `workspace` is a device
     buffer of at least fp8bs_splitk_workspace_size bytes; if None, one is

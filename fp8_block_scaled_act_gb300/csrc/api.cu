@@ -397,6 +397,12 @@ void splitk_shape(int64_t nkb, int64_t splits, int& used, int& kps)
     used = static_cast<int>((nkb + kps - 1) / kps);
 }
 
+// The ops of the row-wise GEMM (Fprop in either B layout, Dgrad).
+bool rowwise_op(int op)
+{
+    return op == FP8BS_OP_FPROP || op == FP8BS_OP_FPROP_WKN || op == FP8BS_OP_DGRAD;
+}
+
 // Group offsets of a call: exactly one of host (planned on the host) and
 // dev (read by the kernel) is set; `rows` is the total token count.
 struct Offsets {
@@ -419,13 +425,17 @@ void copy_offsets(GemmParams& p, const Offsets& o)
 // Fprop / Dgrad, dense or grouped; with splits > 1 (dense only) the
 // K-blocks of every tile are cut into ranges whose fp32 sums go to the
 // workspace `ws`, followed by the reduction kernel.
-fp8bs_status run_rowwise_gemm(bool dgrad, const Offsets& o, const uint8_t* a, const float* sa, const uint8_t* b,
+// op: FP8BS_OP_FPROP (b = W^T codes [N x K]), FP8BS_OP_FPROP_WKN (b = W codes
+// [K x N], read MN-major) or FP8BS_OP_DGRAD (b = W codes [K x N]).
+fp8bs_status run_rowwise_gemm(int op, const Offsets& o, const uint8_t* a, const float* sa, const uint8_t* b,
                               const float* sb, int64_t N, int64_t K, void* out, void* stream, int32_t splits = 1,
                               float* ws = nullptr, uint64_t selftest_limit_ns = 0)
 {
     DeviceState* st = nullptr;
     fp8bs_status s = device_state(&st);
     if (s != FP8BS_OK) return s;
+    const bool dgrad = op == FP8BS_OP_DGRAD;
+    const bool b_mn = op == FP8BS_OP_FPROP_WKN;
     const int64_t contr = dgrad ? N : K;
     const int64_t width = dgrad ? K : N;
     const int64_t M = o.rows;
@@ -439,7 +449,8 @@ fp8bs_status run_rowwise_gemm(bool dgrad, const Offsets& o, const uint8_t* a, co
     p.layout = kRowGroups;
     copy_offsets(p, o);
     p.kblocks = static_cast<int>(contr / kBK);
-    p.b_group_rows = static_cast<int>(width);
+    p.b_group_rows = static_cast<int>(b_mn ? contr : width);
+    p.b_mn = b_mn ? 1 : 0;
     p.rows_total = static_cast<int>(M);
     p.sb_group_stride = (K / 128) * (N / 128);
     // tiles: exact from host offsets, else the bound over any split of M rows
@@ -475,7 +486,11 @@ fp8bs_status run_rowwise_gemm(bool dgrad, const Offsets& o, const uint8_t* a, co
 
     CUtensorMap ma, mb, mo;
     std::memset(&mo, 0, sizeof(mo));
-    if (!cached_map(&ma, a, contr, M, contr, kBM) || !cached_map(&mb, b, contr, width * o.groups, contr, kBN))
+    if (!cached_map(&ma, a, contr, M, contr, kBM)) return FP8BS_ERR_ARG;
+    // B: [width x contr] K-major boxes of 256 rows, or [contr x width]
+    // (MN-major) boxes of 128 K rows x 128 columns
+    if (b_mn ? !cached_map(&mb, b, width, contr * o.groups, width, kBK)
+             : !cached_map(&mb, b, contr, width * o.groups, contr, kBN))
         return FP8BS_ERR_ARG;
     if (used <= 1) {
         if (!cached_out_map(&mo, out, width, M)) return FP8BS_ERR_ARG;
@@ -964,7 +979,21 @@ fp8bs_status fp8_block_gemm_fprop(const uint8_t* xq, const float* sx, const uint
     if (!aligned16(xq) || !aligned16(sx) || !aligned16(wqT) || !aligned16(sw) || !aligned16(y))
         return FP8BS_ERR_ALIGN;
     const int32_t off[2] = {0, static_cast<int32_t>(M)};
-    return run_rowwise_gemm(false, Offsets{off, nullptr, 1, M}, xq, sx, wqT, sw, N, K, y, stream);
+    return run_rowwise_gemm(FP8BS_OP_FPROP, Offsets{off, nullptr, 1, M}, xq, sx, wqT, sw, N, K, y, stream);
+}
+
+fp8bs_status fp8_block_gemm_fprop_wkn(const uint8_t* xq, const float* sx, const uint8_t* wq,
+                                      const float* sw, int64_t M, int64_t N, int64_t K, void* y,
+                                      void* stream)
+{
+    if (M < 0 || N <= 0 || K <= 0) return FP8BS_ERR_ARG;
+    if (K % 128 != 0 || N % 128 != 0 || M > 0x7FFFFF00) return FP8BS_ERR_SHAPE;
+    if (M == 0) return FP8BS_OK;
+    if (!xq || !sx || !wq || !sw || !y) return FP8BS_ERR_ARG;
+    if (!aligned16(xq) || !aligned16(sx) || !aligned16(wq) || !aligned16(sw) || !aligned16(y))
+        return FP8BS_ERR_ALIGN;
+    const int32_t off[2] = {0, static_cast<int32_t>(M)};
+    return run_rowwise_gemm(FP8BS_OP_FPROP_WKN, Offsets{off, nullptr, 1, M}, xq, sx, wq, sw, N, K, y, stream);
 }
 
 fp8bs_status fp8_block_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wq,
@@ -978,7 +1007,7 @@ fp8bs_status fp8_block_gemm_dgrad(const uint8_t* dyq, const float* sdy, const ui
     if (!aligned16(dyq) || !aligned16(sdy) || !aligned16(wq) || !aligned16(sw) || !aligned16(dx))
         return FP8BS_ERR_ALIGN;
     const int32_t off[2] = {0, static_cast<int32_t>(M)};
-    return run_rowwise_gemm(true, Offsets{off, nullptr, 1, M}, dyq, sdy, wq, sw, N, K, dx, stream);
+    return run_rowwise_gemm(FP8BS_OP_DGRAD, Offsets{off, nullptr, 1, M}, dyq, sdy, wq, sw, N, K, dx, stream);
 }
 
 int64_t fp8bs_mx_scale_bytes(int64_t rows, int64_t cols)
@@ -1208,7 +1237,7 @@ extern "C" {
 
 size_t fp8bs_splitk_workspace_size(int op, int64_t M, int64_t N, int64_t K, int32_t splits)
 {
-    if ((op != FP8BS_OP_FPROP && op != FP8BS_OP_DGRAD) || M <= 0 || N <= 0 || K <= 0 || splits <= 1)
+    if (!rowwise_op(op) || M <= 0 || N <= 0 || K <= 0 || splits <= 1)
         return 0;
     const int64_t contr = op == FP8BS_OP_DGRAD ? N : K;
     const int64_t width = op == FP8BS_OP_DGRAD ? K : N;
@@ -1221,7 +1250,7 @@ size_t fp8bs_splitk_workspace_size(int op, int64_t M, int64_t N, int64_t K, int3
 
 int32_t fp8bs_splitk_default_splits(int op, int64_t M, int64_t N, int64_t K)
 {
-    if ((op != FP8BS_OP_FPROP && op != FP8BS_OP_DGRAD) || M <= 0 || N <= 0 || K <= 0) return 1;
+    if (!rowwise_op(op) || M <= 0 || N <= 0 || K <= 0) return 1;
     DeviceState* st = nullptr;
     if (device_state(&st) != FP8BS_OK) return 1;
     const int64_t contr = op == FP8BS_OP_DGRAD ? N : K;
@@ -1239,7 +1268,7 @@ fp8bs_status fp8_block_gemm_splitk(int op, const uint8_t* a, const float* sa, co
                                    const float* sb, int64_t M, int64_t N, int64_t K, int32_t splits,
                                    void* out, void* workspace, size_t workspace_bytes, void* stream)
 {
-    if (op != FP8BS_OP_FPROP && op != FP8BS_OP_DGRAD) return FP8BS_ERR_ARG;
+    if (!rowwise_op(op)) return FP8BS_ERR_ARG;
     if (M < 0 || N <= 0 || K <= 0 || splits < 1) return FP8BS_ERR_ARG;
     if (K % 128 != 0 || N % 128 != 0 || M > 0x7FFFFF00) return FP8BS_ERR_SHAPE;
     if (M == 0) return FP8BS_OK;
@@ -1252,7 +1281,7 @@ fp8bs_status fp8_block_gemm_splitk(int op, const uint8_t* a, const float* sa, co
         if (!aligned16(workspace)) return FP8BS_ERR_ALIGN;
     }
     const int32_t off[2] = {0, static_cast<int32_t>(M)};
-    return run_rowwise_gemm(op == FP8BS_OP_DGRAD, Offsets{off, nullptr, 1, M}, a, sa, b, sb, N, K, out, stream,
+    return run_rowwise_gemm(op, Offsets{off, nullptr, 1, M}, a, sa, b, sb, N, K, out, stream,
                             need > 0 ? splits : 1, static_cast<float*>(workspace));
 }
 
@@ -1276,7 +1305,7 @@ fp8bs_status fp8_block_gemm_grouped(int op, int32_t groups, const int32_t* offse
                                     const float* sa, const uint8_t* b, const float* sb, int64_t N, int64_t K,
                                     void* out, int accumulate, void* stream)
 {
-    if (op != FP8BS_OP_FPROP && op != FP8BS_OP_DGRAD && op != FP8BS_OP_WGRAD) return FP8BS_ERR_ARG;
+    if (!rowwise_op(op) && op != FP8BS_OP_WGRAD) return FP8BS_ERR_ARG;
     if (groups < 1 || groups > kMaxGroups || rows < 0) return FP8BS_ERR_ARG;
     if ((offsets_dev == nullptr) == (offsets_host == nullptr)) return FP8BS_ERR_ARG;   // exactly one
     if (offsets_host && (!valid_offsets(offsets_host, groups) || offsets_host[groups] != rows)) return FP8BS_ERR_ARG;
@@ -1298,7 +1327,7 @@ fp8bs_status fp8_block_gemm_grouped(int op, int32_t groups, const int32_t* offse
     if (!a || !sa || !b || !sb) return FP8BS_ERR_ARG;
     if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(out))
         return FP8BS_ERR_ALIGN;
-    return run_rowwise_gemm(op == FP8BS_OP_DGRAD, o, a, sa, b, sb, N, K, out, stream);
+    return run_rowwise_gemm(op, o, a, sa, b, sb, N, K, out, stream);
 }
 
 int64_t fp8bs_padded_tokens_max(int64_t rows, int32_t groups)
@@ -1379,7 +1408,7 @@ fp8bs_status fp8bs_selftest_gemm_timeout(const uint8_t* xq, const float* sx, con
     if (!aligned16(xq) || !aligned16(sx) || !aligned16(wqT) || !aligned16(sw) || !aligned16(y))
         return FP8BS_ERR_ALIGN;
     const int32_t off[2] = {0, static_cast<int32_t>(M)};
-    return run_rowwise_gemm(false, Offsets{off, nullptr, 1, M}, xq, sx, wqT, sw, N, K, y, stream, 1, nullptr,
+    return run_rowwise_gemm(FP8BS_OP_FPROP, Offsets{off, nullptr, 1, M}, xq, sx, wqT, sw, N, K, y, stream, 1, nullptr,
                             limit_ns);
 }
 

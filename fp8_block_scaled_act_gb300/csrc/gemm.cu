@@ -13,7 +13,9 @@
 // memory instead, which decouples the two halves of the work:
 //
 //   warp 0      TMA producer: one thread streams 128x128 (A) and 256x128 (B)
-//               E4M3 tiles (K-major, 128-byte swizzle) into a 4-stage (Wgrad: 3)
+//               E4M3 tiles (K-major, 128-byte swizzle; Fprop's B may instead
+//               be W as stored, [K x N], which arrives MN-major in two
+//               128-column boxes) into a 4-stage (Wgrad: 3)
 //               shared-memory ring. For Wgrad it also copies each K-block's
 //               scales (the tile's 128 row scales and 256 column scales) into
 //               an 8-slot shared-memory ring with two untiled bulk copies
@@ -729,7 +731,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive_expect_tx(&ctl->full[s], kStageBytes);
                     }
                     tma_load_2d(sA + s * kABytes, &map_a, &ctl->full[s], x, ya);
-                    tma_load_2d(sB + s * kBBytes, &map_b, &ctl->full[s], x, yb);
+                    if (kKind == GemmKind::kBlockScaleBf16 && p.b_mn) {
+                        // MN-major B: K rows x 128 columns per box, the
+                        // tile's two column halves one box apart
+                        const int yk = gi.b_row0 + x;
+                        tma_load_2d(sB + s * kBBytes, &map_b, &ctl->full[s], nt * kBN, yk);
+                        tma_load_2d(sB + s * kBBytes + kBBytes / 2, &map_b, &ctl->full[s], nt * kBN + kBN / 2, yk);
+                    } else {
+                        tma_load_2d(sB + s * kBBytes, &map_b, &ctl->full[s], x, yb);
+                    }
                 }
             }
             if (!ok) {
@@ -747,7 +757,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // MMA issuer
         // ------------------------------------------------------------------
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kBN);
+            const bool b_mn = kKind == GemmKind::kBlockScaleBf16 && p.b_mn != 0;   // Fprop only
+            const uint32_t idesc = idesc_e4m3_f32(kBM, kBN) | (b_mn ? kIdescBMajorMN : 0u);
+            // start-address step of B per 32 K (in 16-byte units): 32 bytes
+            // inside the swizzle row (K-major), 32 K rows = 4096 bytes (MN-major)
+            const uint64_t b_step = b_mn ? 4096u >> 4 : 32u >> 4;
             uint32_t it = 0, acc_it = 0;
             bool ok = true;
             const int units = p.sk_len ? static_cast<int>(gridDim.x) * p.sk_units : ctl->tab.total_tiles * p.splits;
@@ -766,11 +780,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after_sync();
                     const uint64_t adesc = sdesc_kmajor_sw128(smem_addr(sA + s * kABytes));
-                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_addr(sB + s * kBBytes));
+                    const uint64_t bdesc = b_mn ? sdesc_mnmajor_sw128(smem_addr(sB + s * kBBytes), kBBytes / 2)
+                                                : sdesc_kmajor_sw128(smem_addr(sB + s * kBBytes));
                     const uint32_t d = tmem_base + buf * kBN;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 32; ++kk)
-                        mma_e4m3(d, adesc + 2u * kk, bdesc + 2u * kk, idesc, kk > 0 ? 1u : 0u);
+                        mma_e4m3(d, adesc + 2u * kk, bdesc + b_step * kk, idesc, kk > 0 ? 1u : 0u);
                     mma_commit(&ctl->empty[s]);
                     mma_commit(&ctl->tfull[buf]);
                 }

@@ -134,6 +134,13 @@ struct GemmParams {
     int n_tiles;                  // column tiles of BN per group
     int kblocks;                  // kRowGroups: 128-element K-blocks of the contraction
     int b_group_rows;             // kRowGroups: B rows per group
+    // kRowGroups: 1 when B is stored [contraction x width] with the width
+    // (output column) index contiguous, e.g. Fprop's W [K x N] as the
+    // 128x128 cast wrote it; the tile then reaches the tensor core as an
+    // MN-major operand (two 128-column TMA boxes per K-block) and B row
+    // g * b_group_rows + k holds contraction index k of group g. 0: B is
+    // stored [width x contraction] (K-major).
+    int b_mn;
     int out_rows;                 // kTokenGroups: output rows per group (the A rows)
     int rows_total;               // kRowGroups: off[num_groups] must equal this
     int tcap;                     // kTokenGroups: padded tokens available in the operands

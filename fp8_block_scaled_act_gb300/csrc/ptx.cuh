@@ -350,6 +350,28 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr)
     return d;
 }
 
+// Shared-memory matrix descriptor (tcgen05 format) for an MN-major operand
+// tile (the N index contiguous in memory) laid out by TMA with 128-byte
+// swizzling in boxes of 128 N elements x 128 K rows: each K row holds 128
+// consecutive N values (one 128-byte swizzle row), groups of 8 K rows are
+// 1024 bytes apart (stride byte offset), and consecutive 128-element spans
+// of N are `span_bytes` apart (leading byte offset: one box). The tile base
+// must be 1024-byte aligned; advancing the start address by 4096 bytes steps
+// K by 32 rows, a whole number of swizzle atoms.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t span_bytes)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
+    d |= static_cast<uint64_t>(span_bytes >> 4) << 16;     // leading byte offset: next 128 N
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;          // stride byte offset: next 8 K rows
+    d |= static_cast<uint64_t>(1u) << 46;                  // descriptor version
+    d |= static_cast<uint64_t>(2u) << 61;                  // 128-byte swizzle
+    return d;
+}
+
+// Instruction-descriptor bit selecting an MN-major ("transposed") B operand.
+constexpr uint32_t kIdescBMajorMN = 1u << 16;
+
 // Instruction descriptor for kind::f8f6f4 with E4M3 A and B (both K-major)
 // and an F32 accumulator, shape M x N (x 32).
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N)

@@ -68,7 +68,7 @@ fp8bs_status fp8_block_gemm_splitk_noalloc(int op, const uint8_t* a, const float
                                            const float* sb, int64_t M, int64_t N, int64_t K, int32_t splits,
                                            void* out, void* stream)
 {
-    if (op != FP8BS_OP_FPROP && op != FP8BS_OP_DGRAD) return FP8BS_ERR_ARG;
+    if (op != FP8BS_OP_FPROP && op != FP8BS_OP_FPROP_WKN && op != FP8BS_OP_DGRAD) return FP8BS_ERR_ARG;
     if (M < 0 || N <= 0 || K <= 0 || splits < 1) return FP8BS_ERR_ARG;
     if (fp8bs_splitk_workspace_size(op, M, N, K, splits) > kScratchBytes) return FP8BS_ERR_SHAPE;
     if (stream) {

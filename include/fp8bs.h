@@ -87,7 +87,8 @@ typedef enum {
 typedef enum {
     FP8BS_OP_FPROP = 0,
     FP8BS_OP_DGRAD = 1,
-    FP8BS_OP_WGRAD = 2
+    FP8BS_OP_WGRAD = 2,
+    FP8BS_OP_FPROP_WKN = 3      /* Fprop with W's codes as stored, [K x N] (see fp8_block_gemm_fprop_wkn) */
 } fp8bs_op;
 
 /* Largest number of groups (experts) accepted by the grouped entry points. */
@@ -370,6 +371,19 @@ FP8BS_API fp8bs_status fp8_block_gemm_fprop(const uint8_t* xq, const float* sx,
                                   const uint8_t* wqT, const float* sw,
                                   int64_t M, int64_t N, int64_t K, void* y, void* stream);
 
+/* Fprop on W's codes in their own orientation: the same result as
+ * fp8_block_gemm_fprop (bit for bit: the tensor core sees the same operand
+ * values), with B read from the q output of fp8_quant_128x128 on W [K x N]
+ * instead of its byte transpose. The tensor core takes this operand
+ * MN-major (N contiguous in shared memory), so a weight cast feeding only
+ * Fprop and Dgrad can skip qT (NULL) and write 3 bytes per element instead
+ * of 4: Fprop and Dgrad then read the same codes.
+ * wq : E4M3 [K x N], the q output of fp8_quant_128x128 on W [K x N].
+ * Other arguments and constraints as for fp8_block_gemm_fprop. */
+FP8BS_API fp8bs_status fp8_block_gemm_fprop_wkn(const uint8_t* xq, const float* sx,
+                                      const uint8_t* wq, const float* sw,
+                                      int64_t M, int64_t N, int64_t K, void* y, void* stream);
+
 /* Dgrad: dX[i,k] = sum_b s_dy[i,b] * s_w[k/128, b] * P_b[i,k], contraction
  * over the layer's N outputs.
  * dyq : E4M3 [M x N] (fp8_quant_1x128 of dY), sdy its scales.
@@ -403,8 +417,9 @@ FP8BS_API fp8bs_status fp8_block_gemm_wgrad(const uint8_t* dyqT, const float* sd
 /* the fp32 addition order, so the result differs from the unsplit call only  */
 /* by fp32 rounding and stays within the tolerance above. Deterministic.      */
 /*                                                                           */
-/* op        : FP8BS_OP_FPROP or FP8BS_OP_DGRAD; a, sa, b, sb, M, N, K, out  */
-/*             as for fp8_block_gemm_fprop (a = xq, b = wqT) or               */
+/* op        : FP8BS_OP_FPROP, FP8BS_OP_FPROP_WKN or FP8BS_OP_DGRAD; a, sa, */
+/*             b, sb, M, N, K, out as for fp8_block_gemm_fprop (a = xq,       */
+/*             b = wqT), fp8_block_gemm_fprop_wkn (a = xq, b = wq) or         */
 /*             fp8_block_gemm_dgrad (a = dyq, b = wq).                        */
 /* splits    : >= 1; values above the number of 128-blocks are clamped.      */
 /* workspace : caller-owned device buffer of at least                        */
@@ -651,6 +666,9 @@ FP8BS_API fp8bs_status fp8_quant_dual_stash_packed(const void* x, int64_t rows, 
  *   a  = Xq [M x K], sa its 1x128 scales;
  *   b  = stacked WqT [groups x N x K], sb = stacked sw [groups x K/128 x N/128];
  *   out = Y BF16 [M x N].
+ * op = FP8BS_OP_FPROP_WKN: as FP8BS_OP_FPROP with
+ *   b  = stacked Wq [groups x K x N] (the q output of the batched cast, the
+ *        same codes Dgrad reads), taken MN-major as in fp8_block_gemm_fprop_wkn.
  * op = FP8BS_OP_DGRAD (N is the contraction, K the output width):
  *   a  = dYq [M x N], sa its 1x128 scales;
  *   b  = stacked Wq [groups x K x N], sb = stacked sw [groups x K/128 x N/128];
