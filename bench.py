@@ -62,7 +62,7 @@ def step_work(M, K, N):
     gemm_flops = 2.0 * M * N * K
     s_ld = (M + 3) // 4 * 4
     b = {
-        "quant_128x128(W)": K * N * 2 + 2 * K * N + 4 * (K // 128) * (N // 128),
+        "quant_128x128(W)": K * N * 2 + K * N + 4 * (K // 128) * (N // 128),
         "quant_dual_stash(X)": M * K * 2 + M * K + 4 * (K // 128) * s_ld + M * K + 4 * (M // 128) * K,
         "fprop": M * K + N * K + 4 * (K // 128) * (s_ld + N // 128) + 2 * M * N,
         "quant_dual(dY)": M * N * 2 + M * N + 4 * (N // 128) * s_ld + M * N + 4 * (M // 128) * N,
@@ -217,7 +217,9 @@ class DenseStep:
         self.dY = (torch.randn(M, N, device=device, generator=g) * 1e-3).to(torch.bfloat16)
         e = fp8bs
         self.xq, self.sx = e.empty_quant_1x128(M, K, device)
-        self.wq, self.wqT, self.sw = e.empty_quant_128x128(K, N, device=device)
+        # Fprop reads W's codes as stored ([K x N], MN-major), so the cast
+        # writes no transposed copy
+        self.wq, self.wqT, self.sw = e.empty_quant_128x128(K, N, with_transpose=False, device=device)
         self.Y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
         self.dyq, self.sdy = e.empty_quant_1x128(M, N, device)
         self.dX = torch.empty(M, K, dtype=torch.bfloat16, device=device)
@@ -241,11 +243,11 @@ class DenseStep:
     def launches(self):
         e = self.fp8bs
         return [
-            lambda: e.fp8_quant_128x128(self.W, self.wq, self.wqT, self.sw),
+            lambda: e.fp8_quant_128x128(self.W, self.wq, None, self.sw),
             # the forward cast of X also writes the Wgrad operand: the 128x1
             # transposed requant of its E4M3 stash
             lambda: e.fp8_quant_dual_stash(self.X, self.xq, self.sx, self.xT, self.sxT),
-            lambda: e.fp8_block_gemm_fprop(self.xq, self.sx, self.wqT, self.sw, self.Y),
+            lambda: e.fp8_block_gemm_fprop_wkn(self.xq, self.sx, self.wq, self.sw, self.Y),
             lambda: e.fp8_quant_dual(self.dY, self.dyq, self.sdy, self.dyT, self.sdyT),
             lambda: e.fp8_block_gemm_dgrad(self.dyq, self.sdy, self.wq, self.sw, self.dX),
             lambda: e.fp8_block_gemm_wgrad(self.dyT, self.sdyT, self.xT, self.sxT, self.dW),
@@ -298,6 +300,7 @@ class DenseUe8m0Step(DenseStep):
         atoms = lambda rows, k: torch.empty(e.fp8bs_mx_scale_bytes(rows, k), dtype=torch.uint8, device=device)
         self.ax, self.awT, self.ady = atoms(M, K), atoms(N, K), atoms(M, N)
         self.aw, self.adyT, self.axT = atoms(K, N), atoms(N, Mp), atoms(K, Mp)
+        self.wqT = torch.empty(N, K, dtype=torch.uint8, device=device)   # the MX Fprop's K-major W^T
         self.names = ["quant_128x128(W)+atoms", "quant_dual_stash(X)+atoms", "mx_fprop", "quant_dual(dY)+atoms",
                       "mx_dgrad", "mx_wgrad"]
 
@@ -307,7 +310,7 @@ class DenseUe8m0Step(DenseStep):
         Mp = self.xT.shape[1]
         atoms = lambda rows, k: rows * k // 32                            # exponent bytes of an operand
         bytes_ = {
-            "quant_128x128(W)+atoms": b["quant_128x128(W)"] + atoms(N, K) + atoms(K, N),
+            "quant_128x128(W)+atoms": b["quant_128x128(W)"] + K * N + atoms(N, K) + atoms(K, N),
             "quant_dual_stash(X)+atoms": b["quant_dual_stash(X)"] + atoms(M, K) + atoms(K, Mp),
             "mx_fprop": M * K + N * K + atoms(M, K) + atoms(N, K) + 2 * M * N,
             "quant_dual(dY)+atoms": b["quant_dual(dY)"] + atoms(M, N) + atoms(N, Mp),
@@ -367,8 +370,12 @@ class MoeStep:
         self.xq, self.sx = e.empty_quant_1x128(tokens, hidden, device)
         self.aq, self.sa = e.empty_quant_1x128(tokens, inter, device)
         self.dyq, self.sdy = e.empty_quant_1x128(tokens, hidden, device)
-        self.wuq, self.wuqT, self.swu = e.empty_quant_128x128(hidden, up, batch=experts, device=device)
-        self.wdq, self.wdqT, self.swd = e.empty_quant_128x128(inter, hidden, batch=experts, device=device)
+        # the grouped Fprops read the experts' codes as stored (MN-major), so
+        # the batched casts write no transposed copies
+        self.wuq, self.wuqT, self.swu = e.empty_quant_128x128(hidden, up, batch=experts, with_transpose=False,
+                                                              device=device)
+        self.wdq, self.wdqT, self.swd = e.empty_quant_128x128(inter, hidden, batch=experts, with_transpose=False,
+                                                              device=device)
         self.Yu = torch.empty(tokens, up, dtype=bf, device=device)
         self.Yd = torch.empty(tokens, hidden, dtype=bf, device=device)
         self.dA = torch.empty(tokens, inter, dtype=bf, device=device)
@@ -386,8 +393,8 @@ class MoeStep:
         flops = {"grouped_fprop_up": 2.0 * T * H * U, "grouped_fprop_down": 2.0 * T * I * H,
                  "grouped_dgrad_down": 2.0 * T * H * I, "grouped_wgrad_down": 2.0 * T * H * I}
         b = {
-            "quant_128x128(W_up)": G * H * U * 4 + 4 * G * (H // 128) * (U // 128),
-            "quant_128x128(W_down)": G * I * H * 4 + 4 * G * (I // 128) * (H // 128),
+            "quant_128x128(W_up)": G * H * U * 3 + 4 * G * (H // 128) * (U // 128),
+            "quant_128x128(W_down)": G * I * H * 3 + 4 * G * (I // 128) * (H // 128),
             "quant_1x128(X)": T * H * 3 + 4 * (H // 128) * s_ld,
             "grouped_fprop_up": T * H + G * U * H + 2 * T * U,
             "quant_dual_stash(A)": T * I * 3 + 4 * (I // 128) * s_ld + I * mp + 4 * (mp // 128) * I,
@@ -401,13 +408,13 @@ class MoeStep:
     def launches(self):
         e, off, G, H, I, U = self.fp8bs, self.offsets, self.G, self.H, self.I, self.U
         return [
-            lambda: e.fp8_quant_128x128(self.Wu, self.wuq, self.wuqT, self.swu),
-            lambda: e.fp8_quant_128x128(self.Wd, self.wdq, self.wdqT, self.swd),
+            lambda: e.fp8_quant_128x128(self.Wu, self.wuq, None, self.swu),
+            lambda: e.fp8_quant_128x128(self.Wd, self.wdq, None, self.swd),
             lambda: e.fp8_quant_1x128(self.X, self.xq, self.sx),
-            lambda: e.fp8_block_gemm_grouped(e.OP_FPROP, off, self.xq, self.sx, self.wuqT, self.swu,
+            lambda: e.fp8_block_gemm_grouped(e.OP_FPROP_WKN, off, self.xq, self.sx, self.wuq, self.swu,
                                              self.Yu, U, H),
             lambda: e.fp8_quant_dual_stash(self.A, self.aq, self.sa, self.aT, self.saT, offsets=off),
-            lambda: e.fp8_block_gemm_grouped(e.OP_FPROP, off, self.aq, self.sa, self.wdqT, self.swd,
+            lambda: e.fp8_block_gemm_grouped(e.OP_FPROP_WKN, off, self.aq, self.sa, self.wdq, self.swd,
                                              self.Yd, H, I),
             lambda: e.fp8_quant_dual(self.dY, self.dyq, self.sdy, self.dyT, self.sdyT, offsets=off),
             lambda: e.fp8_block_gemm_grouped(e.OP_DGRAD, off, self.dyq, self.sdy, self.wdq, self.swd,
@@ -446,6 +453,9 @@ class MoeUe8m0Step(MoeStep):
         self.ax, self.aa, self.ady = atoms(cap, H), atoms(cap, I), atoms(cap, H)
         self.adyT, self.aaT = atoms(H, cap), atoms(I, cap)
         self.cap = cap
+        # the MX Fprops take K-major W^T codes
+        self.wuqT = torch.empty(G, U, H, dtype=torch.uint8, device=device)
+        self.wdqT = torch.empty(G, H, I, dtype=torch.uint8, device=device)
         # the transposed casts with device offsets write only the actual
         # padded tokens; the scales past them are packed too, so they hold 1
         self.saT.fill_(1.0)
@@ -464,8 +474,8 @@ class MoeUe8m0Step(MoeStep):
              "mx_grouped_dgrad_down": flops["grouped_dgrad_down"], "mx_grouped_wgrad_down": flops["grouped_wgrad_down"]}
         atom = lambda rows, k: rows * k // 32
         by = {
-            "quant_128x128(W_up)+atoms": b["quant_128x128(W_up)"] + G * (atom(U, H) + atom(H, U)),
-            "quant_128x128(W_down)+atoms": b["quant_128x128(W_down)"] + G * (atom(H, I) + atom(I, H)),
+            "quant_128x128(W_up)+atoms": b["quant_128x128(W_up)"] + G * H * U + G * (atom(U, H) + atom(H, U)),
+            "quant_128x128(W_down)+atoms": b["quant_128x128(W_down)"] + G * I * H + G * (atom(H, I) + atom(I, H)),
             "quant_1x128(X)": b["quant_1x128(X)"],
             "pack(X)": 4 * (H // 128) * s_ld + atom(mp, H),
             "mx_grouped_fprop_up": b["grouped_fprop_up"] + atom(mp, H) + G * atom(U, H),
@@ -527,9 +537,9 @@ class LongKStep:
             X = (torch.rand(M, K, device=device, generator=g) + 0.5).to(torch.bfloat16)
             W = (torch.rand(K, N, device=device, generator=g) + 0.5).to(torch.bfloat16)
             xq, sx = e.empty_quant_1x128(M, K, device)
-            wq, wqT, sw = e.empty_quant_128x128(K, N, device=device)
-            sp = e.fp8bs_splitk_default_splits(e.OP_FPROP, M, N, K)
-            ws = torch.empty(max(16, e.fp8bs_splitk_workspace_size(e.OP_FPROP, M, N, K, sp)),
+            wq, wqT, sw = e.empty_quant_128x128(K, N, with_transpose=False, device=device)
+            sp = e.fp8bs_splitk_default_splits(e.OP_FPROP_WKN, M, N, K)
+            ws = torch.empty(max(16, e.fp8bs_splitk_workspace_size(e.OP_FPROP_WKN, M, N, K, sp)),
                              dtype=torch.uint8, device=device)
             Y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
             self.cases.append(dict(K=K, X=X, W=W, xq=xq, sx=sx, wq=wq, wqT=wqT, sw=sw, sp=sp, ws=ws, Y=Y))
@@ -545,7 +555,7 @@ class LongKStep:
         for c in self.cases:
             K = c["K"]
             b[f"quant_1x128(X,K={K})"] = M * K * 3 + 4 * (K // 128) * s_ld
-            b[f"quant_128x128(W,K={K})"] = K * N * 4 + 4 * (K // 128) * (N // 128)
+            b[f"quant_128x128(W,K={K})"] = K * N * 3 + 4 * (K // 128) * (N // 128)
             flops[f"splitk_fprop(K={K},splits={c['sp']})"] = 2.0 * M * N * K
         return flops, b
 
@@ -554,8 +564,8 @@ class LongKStep:
         out = []
         for c in self.cases:
             out += [lambda c=c: e.fp8_quant_1x128(c["X"], c["xq"], c["sx"]),
-                    lambda c=c: e.fp8_quant_128x128(c["W"], c["wq"], c["wqT"], c["sw"]),
-                    lambda c=c: e.fp8_block_gemm_splitk(e.OP_FPROP, c["xq"], c["sx"], c["wqT"], c["sw"],
+                    lambda c=c: e.fp8_quant_128x128(c["W"], c["wq"], None, c["sw"]),
+                    lambda c=c: e.fp8_block_gemm_splitk(e.OP_FPROP_WKN, c["xq"], c["sx"], c["wq"], c["sw"],
                                                         c["Y"], splits=c["sp"], workspace=c["ws"])]
         return out
 
@@ -1051,10 +1061,10 @@ def run_ncu_case(name):
     if name == "fprop":
         xq, sx = e.empty_quant_1x128(M, K)
         e.fp8_quant_1x128(rnd(M, K), xq, sx)
-        wq, wqT, sw = e.empty_quant_128x128(K, N)
-        e.fp8_quant_128x128(rnd(K, N, std=0.02), wq, wqT, sw)
+        wq, _, sw = e.empty_quant_128x128(K, N, with_transpose=False)
+        e.fp8_quant_128x128(rnd(K, N, std=0.02), wq, None, sw)
         y = torch.empty(M, N, dtype=bf, device=dev)
-        runs = lambda: e.fp8_block_gemm_fprop(xq, sx, wqT, sw, y)
+        runs = lambda: e.fp8_block_gemm_fprop_wkn(xq, sx, wq, sw, y)
     elif name == "dgrad":
         dyq, sdy = e.empty_quant_1x128(M, N)
         e.fp8_quant_1x128(rnd(M, N, std=1e-3), dyq, sdy)
@@ -1075,8 +1085,8 @@ def run_ncu_case(name):
         runs = lambda: e.fp8_quant_1x128(x, q, s)
     elif name == "quant_128x128":
         w = rnd(32, 2048, 7168, std=0.02)
-        q, qT, s = e.empty_quant_128x128(2048, 7168, batch=32)
-        runs = lambda: e.fp8_quant_128x128(w, q, qT, s)
+        q, _, s = e.empty_quant_128x128(2048, 7168, batch=32, with_transpose=False)
+        runs = lambda: e.fp8_quant_128x128(w, q, None, s)
     elif name == "requant_e4m3":
         xq, sx = e.empty_quant_1x128(M, K)
         e.fp8_quant_1x128(rnd(M, K), xq, sx)
@@ -1092,10 +1102,10 @@ def run_ncu_case(name):
         if name == "fprop_dense":
             xq, sx = e.empty_quant_1x128(Md, Kd)
             e.fp8_quant_1x128(rnd(Md, Kd), xq, sx)
-            wq, wqT, sw = e.empty_quant_128x128(Kd, Nd)
-            e.fp8_quant_128x128(rnd(Kd, Nd, std=0.02), wq, wqT, sw)
+            wq, _, sw = e.empty_quant_128x128(Kd, Nd, with_transpose=False)
+            e.fp8_quant_128x128(rnd(Kd, Nd, std=0.02), wq, None, sw)
             y = torch.empty(Md, Nd, dtype=bf, device=dev)
-            runs = lambda: e.fp8_block_gemm_fprop(xq, sx, wqT, sw, y)
+            runs = lambda: e.fp8_block_gemm_fprop_wkn(xq, sx, wq, sw, y)
         elif name == "dgrad_dense":
             dyq, sdy = e.empty_quant_1x128(Md, Nd)
             e.fp8_quant_1x128(rnd(Md, Nd, std=1e-3), dyq, sdy)
@@ -1141,12 +1151,13 @@ def run_ncu_case(name):
         Kl = 65536
         xq, sx = e.empty_quant_1x128(256, Kl)
         e.fp8_quant_1x128(rnd(256, Kl), xq, sx)
-        wq, wqT, sw = e.empty_quant_128x128(Kl, 256)
-        e.fp8_quant_128x128(rnd(Kl, 256, std=0.02), wq, wqT, sw)
+        wq, _, sw = e.empty_quant_128x128(Kl, 256, with_transpose=False)
+        e.fp8_quant_128x128(rnd(Kl, 256, std=0.02), wq, None, sw)
         y = torch.empty(256, 256, dtype=bf, device=dev)
-        sp = e.fp8bs_splitk_default_splits(e.OP_FPROP, 256, 256, Kl)
-        ws = torch.empty(e.fp8bs_splitk_workspace_size(e.OP_FPROP, 256, 256, Kl, sp), dtype=torch.uint8, device=dev)
-        runs = lambda: e.fp8_block_gemm_splitk(e.OP_FPROP, xq, sx, wqT, sw, y, splits=sp, workspace=ws)
+        op = e.OP_FPROP_WKN
+        sp = e.fp8bs_splitk_default_splits(op, 256, 256, Kl)
+        ws = torch.empty(e.fp8bs_splitk_workspace_size(op, 256, 256, Kl, sp), dtype=torch.uint8, device=dev)
+        runs = lambda: e.fp8_block_gemm_splitk(op, xq, sx, wq, sw, y, splits=sp, workspace=ws)
     for _ in range(3):
         runs()
     torch.cuda.synchronize()
