@@ -300,7 +300,6 @@ class DenseUe8m0Step(DenseStep):
         atoms = lambda rows, k: torch.empty(e.fp8bs_mx_scale_bytes(rows, k), dtype=torch.uint8, device=device)
         self.ax, self.awT, self.ady = atoms(M, K), atoms(N, K), atoms(M, N)
         self.aw, self.adyT, self.axT = atoms(K, N), atoms(N, Mp), atoms(K, Mp)
-        self.wqT = torch.empty(N, K, dtype=torch.uint8, device=device)   # the MX Fprop's K-major W^T
         self.names = ["quant_128x128(W)+atoms", "quant_dual_stash(X)+atoms", "mx_fprop", "quant_dual(dY)+atoms",
                       "mx_dgrad", "mx_wgrad"]
 
@@ -310,7 +309,7 @@ class DenseUe8m0Step(DenseStep):
         Mp = self.xT.shape[1]
         atoms = lambda rows, k: rows * k // 32                            # exponent bytes of an operand
         bytes_ = {
-            "quant_128x128(W)+atoms": b["quant_128x128(W)"] + K * N + atoms(N, K) + atoms(K, N),
+            "quant_128x128(W)+atoms": b["quant_128x128(W)"] + atoms(N, K) + atoms(K, N),
             "quant_dual_stash(X)+atoms": b["quant_dual_stash(X)"] + atoms(M, K) + atoms(K, Mp),
             "mx_fprop": M * K + N * K + atoms(M, K) + atoms(N, K) + 2 * M * N,
             "quant_dual(dY)+atoms": b["quant_dual(dY)"] + atoms(M, N) + atoms(N, Mp),
@@ -331,9 +330,9 @@ class DenseUe8m0Step(DenseStep):
         # each cast writes its scales' exponent bytes into the atoms of the
         # GEMM operands it feeds, in the same pass
         return [
-            lambda: e.fp8_quant_128x128_packed(self.W, self.wq, self.wqT, self.sw, self.awT, self.aw),
+            lambda: e.fp8_quant_128x128_packed(self.W, self.wq, None, self.sw, self.awT, self.aw),
             lambda: e.fp8_quant_dual_stash_packed(self.X, self.xq, self.sx, self.xT, self.sxT, self.ax, self.axT),
-            lambda: e.fp8_mx_gemm(self.xq, self.ax, self.wqT, self.awT, self.Y),
+            lambda: e.fp8_mx_gemm_wkn(self.xq, self.ax, self.wq, self.awT, self.Y),
             lambda: e.fp8_quant_dual_packed(self.dY, self.dyq, self.sdy, self.dyT, self.sdyT, self.ady,
                                             self.adyT),
             lambda: e.fp8_mx_gemm(self.dyq, self.ady, self.wq, self.aw, self.dX),
@@ -453,9 +452,6 @@ class MoeUe8m0Step(MoeStep):
         self.ax, self.aa, self.ady = atoms(cap, H), atoms(cap, I), atoms(cap, H)
         self.adyT, self.aaT = atoms(H, cap), atoms(I, cap)
         self.cap = cap
-        # the MX Fprops take K-major W^T codes
-        self.wuqT = torch.empty(G, U, H, dtype=torch.uint8, device=device)
-        self.wdqT = torch.empty(G, H, I, dtype=torch.uint8, device=device)
         # the transposed casts with device offsets write only the actual
         # padded tokens; the scales past them are packed too, so they hold 1
         self.saT.fill_(1.0)
@@ -474,8 +470,8 @@ class MoeUe8m0Step(MoeStep):
              "mx_grouped_dgrad_down": flops["grouped_dgrad_down"], "mx_grouped_wgrad_down": flops["grouped_wgrad_down"]}
         atom = lambda rows, k: rows * k // 32
         by = {
-            "quant_128x128(W_up)+atoms": b["quant_128x128(W_up)"] + G * H * U + G * (atom(U, H) + atom(H, U)),
-            "quant_128x128(W_down)+atoms": b["quant_128x128(W_down)"] + G * I * H + G * (atom(H, I) + atom(I, H)),
+            "quant_128x128(W_up)+atoms": b["quant_128x128(W_up)"] + G * (atom(U, H) + atom(H, U)),
+            "quant_128x128(W_down)+atoms": b["quant_128x128(W_down)"] + G * (atom(H, I) + atom(I, H)),
             "quant_1x128(X)": b["quant_1x128(X)"],
             "pack(X)": 4 * (H // 128) * s_ld + atom(mp, H),
             "mx_grouped_fprop_up": b["grouped_fprop_up"] + atom(mp, H) + G * atom(U, H),
@@ -494,15 +490,15 @@ class MoeUe8m0Step(MoeStep):
     def launches(self):
         e, off, G, H, I, U, T, o = self.fp8bs, self.offsets, self.G, self.H, self.I, self.U, self.T, self.opts
         return [
-            lambda: e.fp8_quant_128x128_packed(self.Wu, self.wuq, self.wuqT, self.swu, self.awuT, self.awu),
-            lambda: e.fp8_quant_128x128_packed(self.Wd, self.wdq, self.wdqT, self.swd, self.awdT, self.awd),
+            lambda: e.fp8_quant_128x128_packed(self.Wu, self.wuq, None, self.swu, self.awuT, self.awu),
+            lambda: e.fp8_quant_128x128_packed(self.Wd, self.wdq, None, self.swd, self.awdT, self.awd),
             lambda: e.fp8_quant_1x128_opts(self.X, self.xq, self.sx, o),
             lambda: e.fp8_pack_ue8m0_grouped(self.sx, T, H, off, self.ax),
-            lambda: e.fp8_mx_gemm_grouped(e.OP_FPROP, off, self.xq, self.ax, self.wuqT, self.awuT, self.Yu, U, H),
+            lambda: e.fp8_mx_gemm_grouped(e.OP_FPROP_WKN, off, self.xq, self.ax, self.wuq, self.awuT, self.Yu, U, H),
             lambda: e.fp8_quant_dual_stash_opts(self.A, self.aq, self.sa, self.aT, self.saT, o, offsets=off),
             lambda: e.fp8_pack_ue8m0_grouped(self.sa, T, I, off, self.aa),
             lambda: e.fp8_pack_ue8m0(self.saT, I, self.cap, 1, 1, I, self.aaT),
-            lambda: e.fp8_mx_gemm_grouped(e.OP_FPROP, off, self.aq, self.aa, self.wdqT, self.awdT, self.Yd, H, I),
+            lambda: e.fp8_mx_gemm_grouped(e.OP_FPROP_WKN, off, self.aq, self.aa, self.wdq, self.awdT, self.Yd, H, I),
             lambda: e.fp8_quant_dual_opts(self.dY, self.dyq, self.sdy, self.dyT, self.sdyT, o, offsets=off),
             lambda: e.fp8_pack_ue8m0_grouped(self.sdy, T, H, off, self.ady),
             lambda: e.fp8_pack_ue8m0(self.sdyT, H, self.cap, 1, 1, H, self.adyT),

@@ -38,7 +38,7 @@ __all__ = [
     "fp8_quant_dual_stash", "fp8_quant_dual_stash_opts", "fp8_requant_128x1_T_sr", "fp8_quant_dual_sr",
     "fp8_quant_dual_stash_sr",
     "fp8bs_mx_scale_bytes", "fp8_mx_quant_1x32", "fp8_mx_gemm", "empty_mx_quant",
-    "fp8_mx_quant_1x32_T", "fp8_mx_gemm_f32", "empty_mx_quant_T", "fp8_pack_ue8m0",
+    "fp8_mx_quant_1x32_T", "fp8_mx_gemm_f32", "fp8_mx_gemm_wkn", "empty_mx_quant_T", "fp8_pack_ue8m0",
     "fp8_mx_gemm_grouped", "fp8_pack_ue8m0_grouped",
     "fp8_quant_128x128_packed", "fp8_quant_dual_packed", "fp8_quant_dual_stash_packed", "empty_mx_atoms",
 ]
@@ -109,6 +109,7 @@ def lib() -> ctypes.CDLL:
         "fp8bs_mx_scale_bytes": ([I64, I64], I64),
         "fp8_mx_quant_1x32": ([P, I64, I64, P, P, P], S),
         "fp8_mx_gemm": ([P, P, P, P, I64, I64, I64, P, P], S),
+        "fp8_mx_gemm_wkn": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_mx_gemm_f32": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_mx_gemm_grouped": ([I, I32, P, P, I64, P, P, P, P, I64, I64, P, P], S),
         "fp8_pack_ue8m0_grouped": ([P, I64, I64, I64, I32, P, P, P, P], S),
@@ -533,6 +534,20 @@ def fp8_mx_gemm(a, a_atoms, b, b_atoms, out, stream=None) -> None:
                                       _ptr(out), _stream(stream)))
 
 
+def fp8_mx_gemm_wkn(a, a_atoms, b, b_atoms, out, stream=None) -> None:
+    """out [M x N] (BF16) = A [M x K] . B with B's codes [K x N] (W as the
+    128x128 cast stores it) and B's atoms in the [N x K] layout."""
+    for t, n, d in ((a, "a", torch.uint8), (a_atoms, "a_atoms", torch.uint8), (b, "b", torch.uint8),
+                    (b_atoms, "b_atoms", torch.uint8), (out, "out", torch.bfloat16)):
+        _need(t, d, n)
+    M, K = a.shape
+    N = b.shape[1]
+    if b.shape != (K, N) or out.shape != (M, N):
+        raise ValueError("shape mismatch")
+    _check("fp8_mx_gemm_wkn", lib().fp8_mx_gemm_wkn(_ptr(a), _ptr(a_atoms), _ptr(b), _ptr(b_atoms), M, N, K,
+                                                    _ptr(out), _stream(stream)))
+
+
 def fp8_mx_gemm_f32(a, a_atoms, b, b_atoms, out, stream=None) -> None:
     """fp8_mx_gemm with an FP32 output tensor (the Wgrad form)."""
     _need(out, torch.float32, "out")
@@ -586,14 +601,17 @@ def empty_mx_atoms(rows: int, K: int, batch: int = 1, device="cuda"):
 def fp8_quant_128x128_packed(w, q, qT, scales, atoms_wT, atoms_w, stream=None) -> None:
     """fp8_quant_128x128 under the UE8M0 rule that also writes the scale atoms
     of W^T [cols x rows] (atoms_wT) and of W [rows x cols] (atoms_w), per
-    batch entry; rows, cols multiples of 128."""
+    batch entry; rows, cols multiples of 128. qT may be None (no transposed
+    codes: the MX Fprop then reads q through fp8_mx_gemm_wkn)."""
     _need(w, torch.bfloat16, "w"); _need(q, torch.uint8, "q"); _need(scales, torch.float32, "scales")
-    _need(qT, torch.uint8, "qT"); _need(atoms_wT, torch.uint8, "atoms_wT"); _need(atoms_w, torch.uint8, "atoms_w")
+    if qT is not None:
+        _need(qT, torch.uint8, "qT")
+    _need(atoms_wT, torch.uint8, "atoms_wT"); _need(atoms_w, torch.uint8, "atoms_w")
     batch = w.shape[0] if w.dim() == 3 else 1
     rows, cols = w.shape[-2:]
     nb = ((rows + 127) // 128) * ((cols + 127) // 128)
     if (q.numel() != w.numel() or q.shape[-2:] != (rows, cols) or scales.numel() != batch * nb
-            or qT.numel() != w.numel() or qT.shape[-2:] != (cols, rows)):
+            or (qT is not None and (qT.numel() != w.numel() or qT.shape[-2:] != (cols, rows)))):
         raise ValueError("output shapes do not match empty_quant_128x128")
     need = batch * fp8bs_mx_scale_bytes(cols, rows)
     if atoms_wT.numel() < need or atoms_w.numel() < need:

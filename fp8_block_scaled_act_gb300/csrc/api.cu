@@ -115,7 +115,7 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // after the extern "C" wrappers).
 fp8bs_status mx_gemm_common(const uint8_t* a, const uint8_t* a_scale_atoms, const uint8_t* b,
                             const uint8_t* b_scale_atoms, int64_t M, int64_t N, int64_t K, uint16_t* out_bf16,
-                            float* out_f32, void* stream);
+                            float* out_f32, void* stream, bool b_mn = false);
 fp8bs_status mx_gemm_grouped(int op, int32_t groups, const int32_t* offsets_dev, const int32_t* offsets_host,
                              int64_t rows, const uint8_t* a, const uint8_t* a_atoms, const uint8_t* b,
                              const uint8_t* b_atoms, int64_t N, int64_t K, void* out, void* stream);
@@ -1069,6 +1069,14 @@ fp8bs_status fp8_mx_gemm(const uint8_t* a, const uint8_t* a_scale_atoms, const u
                           stream);
 }
 
+fp8bs_status fp8_mx_gemm_wkn(const uint8_t* a, const uint8_t* a_scale_atoms, const uint8_t* b,
+                             const uint8_t* b_scale_atoms, int64_t M, int64_t N, int64_t K, void* out,
+                             void* stream)
+{
+    return mx_gemm_common(a, a_scale_atoms, b, b_scale_atoms, M, N, K, static_cast<uint16_t*>(out), nullptr,
+                          stream, true);
+}
+
 fp8bs_status fp8_mx_gemm_f32(const uint8_t* a, const uint8_t* a_scale_atoms, const uint8_t* b,
                              const uint8_t* b_scale_atoms, int64_t M, int64_t N, int64_t K, float* out,
                              void* stream)
@@ -1130,9 +1138,10 @@ bool make_mx_out_map(CUtensorMap* m, void* out, int64_t cols, int64_t rows, bool
                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// b_mn: B's codes are [K x N] (read MN-major) instead of [N x K].
 fp8bs_status mx_gemm_common(const uint8_t* a, const uint8_t* a_scale_atoms, const uint8_t* b,
                             const uint8_t* b_scale_atoms, int64_t M, int64_t N, int64_t K, uint16_t* out_bf16,
-                            float* out_f32, void* stream)
+                            float* out_f32, void* stream, bool b_mn)
 {
     void* out = out_bf16 ? static_cast<void*>(out_bf16) : static_cast<void*>(out_f32);
     if (M < 0 || N <= 0 || K <= 0) return FP8BS_ERR_ARG;
@@ -1147,11 +1156,13 @@ fp8bs_status mx_gemm_common(const uint8_t* a, const uint8_t* a_scale_atoms, cons
     fp8bs_status s = device_state(&st);
     if (s != FP8BS_OK) return s;
     CUtensorMap ma, mb, mo;
-    if (!make_map(&ma, a, K, M, K, kBM) || !make_map(&mb, b, K, N, K, kBN)) return FP8BS_ERR_ARG;
+    if (!make_map(&ma, a, K, M, K, kBM)) return FP8BS_ERR_ARG;
+    if (b_mn ? !make_map(&mb, b, N, K, N, kBK) : !make_map(&mb, b, K, N, K, kBN)) return FP8BS_ERR_ARG;
     if (!make_mx_out_map(&mo, out, N, M, out_bf16 == nullptr)) return FP8BS_ERR_ARG;
     MxGroups grp;
     std::memset(&grp, 0, sizeof(grp));
     grp.layout = kMxDense;
+    grp.b_mn = b_mn ? 1 : 0;
     grp.kb_atoms_a = grp.kb_atoms_b = static_cast<int>(K / 128);
     const int64_t tiles = ((M + kBM - 1) / kBM) * (N / kBN);
     return launch_status(launch_mx_gemm(ma, mb, &mo, a_scale_atoms, b_scale_atoms,
@@ -1166,15 +1177,16 @@ fp8bs_status mx_gemm_grouped(int op, int32_t groups, const int32_t* offsets_dev,
                              int64_t rows, const uint8_t* a, const uint8_t* a_atoms, const uint8_t* b,
                              const uint8_t* b_atoms, int64_t N, int64_t K, void* out, void* stream)
 {
-    if (op != FP8BS_OP_FPROP && op != FP8BS_OP_DGRAD && op != FP8BS_OP_WGRAD) return FP8BS_ERR_ARG;
+    if (!rowwise_op(op) && op != FP8BS_OP_WGRAD) return FP8BS_ERR_ARG;
     if (groups < 1 || groups > kMaxGroups || rows < 0 || N <= 0 || K <= 0) return FP8BS_ERR_ARG;
     if ((offsets_dev == nullptr) == (offsets_host == nullptr)) return FP8BS_ERR_ARG;
     if (offsets_dev && (reinterpret_cast<uintptr_t>(offsets_dev) & 3u) != 0) return FP8BS_ERR_ALIGN;
     if (offsets_host && (!valid_offsets(offsets_host, groups) || offsets_host[groups] != rows))
         return FP8BS_ERR_ARG;
     // contraction and output width of one group
-    const int64_t contr = op == FP8BS_OP_FPROP ? K : N;
-    const int64_t width = op == FP8BS_OP_FPROP ? N : K;
+    const bool b_mn = op == FP8BS_OP_FPROP_WKN;
+    const int64_t contr = op == FP8BS_OP_DGRAD ? N : K;
+    const int64_t width = op == FP8BS_OP_DGRAD ? K : N;
     if (contr % 128 != 0 || width % 256 != 0 || rows > 0x7FFFFF00 || contr > 0x7FFFFFFF ||
         width * groups > 0x7FFFFFFF || N * groups > 0x7FFFFFFF)
         return FP8BS_ERR_SHAPE;
@@ -1215,12 +1227,16 @@ fp8bs_status mx_gemm_grouped(int op, int32_t groups, const int32_t* offsets_dev,
                                             static_cast<int>(K), 0, nullptr, static_cast<float*>(out), grp, tiles,
                                             g_wait_limit_ns, st->status, st->num_sms, cs));
     }
-    // Fprop: a = Xq [rows x K], b = stacked WqT [groups x N x K]; Dgrad:
+    // Fprop: a = Xq [rows x K], b = stacked WqT [groups x N x K] (or, for
+    // FP8BS_OP_FPROP_WKN, stacked Wq [groups x K x N] read MN-major); Dgrad:
     // a = dYq [rows x N], b = stacked Wq [groups x K x N]; out BF16 [rows x width]
-    if (!make_map(&ma, a, contr, rows, contr, kBM) || !make_map(&mb, b, contr, width * groups, contr, kBN) ||
+    if (!make_map(&ma, a, contr, rows, contr, kBM) ||
+        (b_mn ? !make_map(&mb, b, width, contr * groups, width, kBK)
+              : !make_map(&mb, b, contr, width * groups, contr, kBN)) ||
         !make_mx_out_map(&mo, out, width, rows, false))
         return FP8BS_ERR_ARG;
     grp.layout = kMxRowGroups;
+    grp.b_mn = b_mn ? 1 : 0;
     grp.b_group_rows = static_cast<int>(width);
     grp.kb_atoms_a = grp.kb_atoms_b = static_cast<int>(contr / 128);
     const int64_t mtiles = tpad / 128;

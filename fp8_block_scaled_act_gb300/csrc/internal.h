@@ -233,6 +233,10 @@ struct MxGroups {
     int kb_atoms_a, kb_atoms_b;     // atoms per 128-row block along K, of A and of B
     int out_rows;                   // token groups: output rows per group
     int kb_cap;                     // token groups: padded K-blocks the operands hold
+    // dense and row groups: 1 when B's codes are stored [K x N] per group
+    // (N contiguous; group g's rows start at g * K) and reach the tensor core
+    // MN-major; its scale atoms keep the [N x K] layout
+    int b_mn;
 };
 
 // out (BF16) or out_f32 (FP32, when not null) [M x N] (M = the output rows:

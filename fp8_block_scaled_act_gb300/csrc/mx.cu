@@ -261,6 +261,7 @@ struct MxParams {
 // the same tiles in the same order).
 struct MxTile {
     int a_row, k0, b_row, nkb;     // TMA coordinates of A / B row 0 and K-block 0; K-blocks
+                                   // (MN-major B: b_row = the group's first K row, col0 its column)
     int64_t sfa, sfb0, sfb1;       // byte offsets of K-block 0's atoms (then + 512 per K-block)
     int out_row0, row_end;         // output-map row of the tile's row 0; rows from row_end on are not stored
     int col0;                      // first output column
@@ -321,6 +322,7 @@ __device__ void mx_build_tab(const MxParams& p, MxCtl* ctl)
     __syncthreads();
 }
 
+template <bool kBMn>
 __device__ __forceinline__ MxTile mx_tile(const MxParams& p, const MxCtl* ctl, int t)
 {
     const MxGroups& gp = p.grp;
@@ -329,7 +331,7 @@ __device__ __forceinline__ MxTile mx_tile(const MxParams& p, const MxCtl* ctl, i
         const int mt = t / p.n_tiles, nt = t - mt * p.n_tiles;
         d.a_row = mt * kBM;
         d.k0 = 0;
-        d.b_row = nt * kBN;
+        d.b_row = kBMn ? 0 : nt * kBN;
         d.nkb = p.kblocks;
         d.sfa = static_cast<int64_t>(mt) * gp.kb_atoms_a * 512;
         d.sfb0 = static_cast<int64_t>(2 * nt) * gp.kb_atoms_b * 512;
@@ -348,7 +350,7 @@ __device__ __forceinline__ MxTile mx_tile(const MxParams& p, const MxCtl* ctl, i
         const int o0 = mx_group_off(gp, g);
         d.a_row = o0 + mt * kBM;
         d.k0 = 0;
-        d.b_row = g * gp.b_group_rows + nt * kBN;
+        d.b_row = kBMn ? g * p.kblocks * kBK : g * gp.b_group_rows + nt * kBN;
         d.nkb = p.kblocks;
         d.sfa = static_cast<int64_t>(lt) * gp.kb_atoms_a * 512;
         d.sfb0 = (static_cast<int64_t>(g) * (gp.b_group_rows / 128) + 2 * nt) * gp.kb_atoms_b * 512;
@@ -423,8 +425,9 @@ __device__ __forceinline__ void record_status(unsigned int* status, unsigned int
     atomicCAS(status, 0u, code);
 }
 
-// kF32: FP32 output (p.out_f32) instead of BF16 (p.out).
-template <bool kF32>
+// kF32: FP32 output (p.out_f32) instead of BF16 (p.out). kBMn: B's codes
+// are [K x N] and reach the tensor core MN-major (p.grp.b_mn; BF16 only).
+template <bool kF32, bool kBMn>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_out, const __grid_constant__ MxParams p)
@@ -477,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const MxTile d = mx_tile(p, ctl, t);
+                const MxTile d = mx_tile<kBMn>(p, ctl, t);
                 for (int kb = 0; kb < d.nkb; ++kb, ++it) {
                     const uint32_t s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1u;
@@ -487,7 +490,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     mbar_arrive_expect_tx(&ctl->full[s], kABytes + kBBytes + kSfaBytes + kSfbBytes);
                     tma_load_2d(sA + s * kABytes, &map_a, &ctl->full[s], d.k0 + kb * kBK, d.a_row);
-                    tma_load_2d(sB + s * kBBytes, &map_b, &ctl->full[s], d.k0 + kb * kBK, d.b_row);
+                    if constexpr (kBMn) {
+                        // MN-major B: K rows x 128 columns per box, the
+                        // tile's two column halves one box apart
+                        const int yk = d.b_row + d.k0 + kb * kBK;
+                        tma_load_2d(sB + s * kBBytes, &map_b, &ctl->full[s], d.col0, yk);
+                        tma_load_2d(sB + s * kBBytes + kBBytes / 2, &map_b, &ctl->full[s], d.col0 + kBN / 2, yk);
+                    } else {
+                        tma_load_2d(sB + s * kBBytes, &map_b, &ctl->full[s], d.k0 + kb * kBK, d.b_row);
+                    }
                     bulk_load(sSfa + s * kSfaBytes, p.sfa + d.sfa + static_cast<int64_t>(kb) * 512, kSfaBytes,
                               &ctl->full[s]);
                     bulk_load(sSfb + s * kSfbBytes, p.sfb + d.sfb0 + static_cast<int64_t>(kb) * 512, 512,
@@ -509,6 +520,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t it = 0, tile_it = 0;
             bool ok = true;
+            constexpr uint32_t b_major = kBMn ? kIdescBMajorMN : 0u;
+            // start-address step of B per 32 K (16-byte units; see gemm.cu)
+            constexpr uint64_t b_step = kBMn ? 4096u >> 4 : 32u >> 4;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tile_it) {
                 // the accumulator is free once the epilogue has read the previous tile
                 if (ctl->abort || !mbar_wait(&ctl->tempty, (tile_it & 1u) ^ 1u, limit)) {
@@ -516,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                const int nkb = mx_tile(p, ctl, t).nkb;   // a tile of an empty group issues no MMA
+                const int nkb = mx_tile<kBMn>(p, ctl, t).nkb;   // a tile of an empty group issues no MMA
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const uint32_t s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1u;
@@ -528,11 +542,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sf_a = tmem_base + kSfCol0 + s * kSfColsPerStage;
                     const uint32_t sf_b = sf_a + 4;
                     const uint64_t adesc = sdesc_kmajor_sw128(smem_addr(sA + s * kABytes));
-                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_addr(sB + s * kBBytes));
+                    const uint64_t bdesc = kBMn ? sdesc_mnmajor_sw128(smem_addr(sB + s * kBBytes), kBBytes / 2)
+                                                : sdesc_kmajor_sw128(smem_addr(sB + s * kBBytes));
 #pragma unroll
                     for (int kk = 0; kk < kBK / 32; ++kk)
-                        mma_mx(tmem_base, adesc + 2u * kk, bdesc + 2u * kk, idesc_mx(kBM, kBN, kk), sf_a, sf_b,
-                               (kb > 0 || kk > 0) ? 1u : 0u);
+                        mma_mx(tmem_base, adesc + 2u * kk, bdesc + b_step * kk, idesc_mx(kBM, kBN, kk) | b_major,
+                               sf_a, sf_b, (kb > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(&ctl->empty[s]);
                 }
                 if (!ok) break;
@@ -553,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const int nkb = mx_tile(p, ctl, t).nkb;
+                const int nkb = mx_tile<kBMn>(p, ctl, t).nkb;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const uint32_t s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1u;
@@ -588,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t tile_it = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tile_it) {
-            const MxTile d = mx_tile(p, ctl, t);
+            const MxTile d = mx_tile<kBMn>(p, ctl, t);
             if (ctl->abort || !mbar_wait(&ctl->tfull, tile_it & 1u, limit)) {
                 ok = false;
                 break;
@@ -905,11 +920,14 @@ cudaError_t launch_mx_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, c
     p.wait_limit_ns = wait_limit_ns;
     p.status = status;
     if (max_tiles <= 0) return cudaSuccess;
-    auto kernel = out_f32 != nullptr ? mx_gemm_kernel<true> : mx_gemm_kernel<false>;
-    // once per device and output type: the shared-memory opt-in, and a check
-    // that the launch allocation covers the setmaxnreg split
-    static std::atomic<uint64_t> ready[2];
-    const int var = out_f32 != nullptr ? 1 : 0;
+    if (grp.b_mn && out_f32 != nullptr) return cudaErrorInvalidValue;
+    auto kernel = out_f32 != nullptr ? mx_gemm_kernel<true, false>
+                  : grp.b_mn         ? mx_gemm_kernel<false, true>
+                                     : mx_gemm_kernel<false, false>;
+    // once per device and kernel variant: the shared-memory opt-in, and a
+    // check that the launch allocation covers the setmaxnreg split
+    static std::atomic<uint64_t> ready[3];
+    const int var = out_f32 != nullptr ? 1 : grp.b_mn ? 2 : 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

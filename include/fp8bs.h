@@ -506,6 +506,14 @@ FP8BS_API fp8bs_status fp8_mx_gemm(const uint8_t* a, const uint8_t* a_scale_atom
                                    const uint8_t* b, const uint8_t* b_scale_atoms,
                                    int64_t M, int64_t N, int64_t K, void* out, void* stream);
 
+/* The same GEMM (BF16 output) with B's codes [K x N], N contiguous (W as    */
+/* the 128x128 cast stores it, the q output of fp8_quant_128x128_packed),    */
+/* read MN-major by the tensor core; b_scale_atoms keep the [N x K] layout   */
+/* (atoms_wT of that cast). Equal to fp8_mx_gemm on the byte transpose.      */
+FP8BS_API fp8bs_status fp8_mx_gemm_wkn(const uint8_t* a, const uint8_t* a_scale_atoms,
+                                       const uint8_t* b, const uint8_t* b_scale_atoms,
+                                       int64_t M, int64_t N, int64_t K, void* out, void* stream);
+
 /* The same GEMM with FP32 output [M x N] (the Wgrad form: dW = dY^T X with   */
 /* A = the transposed cast of dY and B = the transposed cast of X).          */
 FP8BS_API fp8bs_status fp8_mx_gemm_f32(const uint8_t* a, const uint8_t* a_scale_atoms,
@@ -520,6 +528,9 @@ FP8BS_API fp8bs_status fp8_mx_gemm_f32(const uint8_t* a, const uint8_t* a_scale_
 /* expert shapes).                                                           */
 /* op = FP8BS_OP_FPROP: a = Xq [rows x K]; b = stacked W^T codes            */
 /*   [groups x N x K]; out = Y BF16 [rows x N].                              */
+/* op = FP8BS_OP_FPROP_WKN: as FP8BS_OP_FPROP with b = stacked W codes       */
+/*   [groups x K x N] (read MN-major, as in fp8_mx_gemm_wkn); b_scale_atoms  */
+/*   as for FP8BS_OP_FPROP.                                                  */
 /* op = FP8BS_OP_DGRAD (contraction N, output width K): a = dYq [rows x N];  */
 /*   b = stacked W codes [groups x K x N]; out = dX BF16 [rows x K].         */
 /*   Fprop / Dgrad a_scale_atoms: the atoms of A in the groups' tile layout: */
@@ -616,7 +627,8 @@ FP8BS_API fp8bs_status fp8_pack_ue8m0_grouped(const float* scales, int64_t rows,
 /* byte-identical to fp8_pack_ue8m0 of the fp32 scales they return (so the  */
 /* MX GEMMs can follow directly, with no packing launch in between).         */
 /*   fp8_quant_128x128_packed: W [rows x cols] per batch entry, rows and     */
-/*     cols multiples of 128 (else FP8BS_ERR_SHAPE); atoms_wT: the atoms of  */
+/*     cols multiples of 128 (else FP8BS_ERR_SHAPE); qT optional (NULL when  */
+/*     Fprop reads q through fp8_mx_gemm_wkn); atoms_wT: the atoms of        */
 /*     W^T [cols x rows] (Fprop's B), atoms_w: those of W [rows x cols]      */
 /*     with the contraction along cols (Dgrad's B); each                     */
 /*     fp8bs_mx_scale_bytes(cols, rows) bytes per batch entry, entries       */

@@ -28,7 +28,8 @@ def _lib():
 
 
 def _outputs(step):
-    return (step.Y, step.dX, step.dW, step.xq, step.sx, step.xT, step.sxT, step.wq, step.wqT, step.sw,
+    # (the step's weight cast writes no transposed codes: Fprop reads W as stored)
+    return (step.Y, step.dX, step.dW, step.xq, step.sx, step.xT, step.sxT, step.wq, step.sw,
             step.dyq, step.sdy, step.dyT, step.sdyT)
 
 

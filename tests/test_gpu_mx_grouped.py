@@ -116,10 +116,14 @@ def test_grouped_mx_fprop_dgrad(counts, dev):
     ady = _pack_grouped(sdy, M, N, off, dev)
     y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
     dx = torch.full((M, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    y_kn = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
     fp8bs.fp8_mx_gemm_grouped(fp8bs.OP_FPROP, _offs(off, dev), xq, ax, wqT, awT, y, N, K)
     fp8bs.fp8_mx_gemm_grouped(fp8bs.OP_DGRAD, _offs(off, dev), dyq, ady, wq, aw, dx, N, K)
+    # Fprop on the experts' codes as stored ([G x K x N], read MN-major)
+    fp8bs.fp8_mx_gemm_grouped(fp8bs.OP_FPROP_WKN, _offs(off, dev), xq, ax, wq, awT, y_kn, N, K)
     torch.cuda.synchronize()
     assert fp8bs.fp8bs_device_status(reset=True) == 0
+    assert torch.equal(y_kn.view(torch.int16), y.view(torch.int16))
     y, dx = bf16_values(y), bf16_values(dx)
     for e in range(G):
         r0, r1 = int(off[e]), int(off[e + 1])

@@ -131,6 +131,42 @@ def test_ue8m0_gemms_through_the_mx_kernel(M, K, N):
                       f"ue8m0 wgrad {M}: {N}x{K}")
 
 
+@pytest.mark.parametrize("M,K,N", [(200, 512, 256), (129, 256, 768), (300, 1024, 512)])
+def test_mx_fprop_on_w_as_stored(M, K, N):
+    """The MX Fprop on W's codes [K x N] (fp8_mx_gemm_wkn: the tensor core
+    reads them MN-major, with the W^T atoms) equals the MX Fprop on the byte
+    transpose bit for bit, and the packed weight cast without the transpose
+    writes the same codes, scales and atoms; the result is within the GEMM
+    tolerance of the oracle's promoted Fprop on the same codes."""
+    x = wl.with_outliers((M, K), fraction=0.01, seed=M + K)
+    w = wl.normal((K, N), std=wl.W_STD, seed=N + 5)
+    xq, sx = fp8bs.empty_quant_1x128(M, K)
+    fp8bs.fp8_quant_1x128_opts(x.cuda(), xq, sx, UE8M0)
+    ax = _pack(sx, M, K, 1, 1, sx.shape[1])
+    wd = w.cuda()
+    wq, wqT, sw = fp8bs.empty_quant_128x128(K, N)
+    awT, aw = fp8bs.empty_mx_atoms(N, K), fp8bs.empty_mx_atoms(K, N)
+    fp8bs.fp8_quant_128x128_packed(wd, wq, wqT, sw, awT, aw)
+    wq2, _, sw2 = fp8bs.empty_quant_128x128(K, N, with_transpose=False)
+    awT2, aw2 = fp8bs.empty_mx_atoms(N, K), fp8bs.empty_mx_atoms(K, N)
+    fp8bs.fp8_quant_128x128_packed(wd, wq2, None, sw2, awT2, aw2)
+    y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    y2 = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    fp8bs.fp8_mx_gemm(xq, ax, wqT, awT, y)
+    fp8bs.fp8_mx_gemm_wkn(xq, ax, wq2, awT2, y2)
+    torch.cuda.synchronize()
+    assert fp8bs.fp8bs_device_status(reset=True) == 0
+    for a, b in ((wq, wq2), (sw, sw2), (awT, awT2), (aw, aw2)):
+        assert torch.equal(a, b)
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+    h = {k: np_(v) for k, v in dict(xq=xq, sx=sx, wq=wq, sw=sw).items()}
+    dec = lambda q: oracle.e4m3_decode(q).astype(np.float64)
+    xa = np.abs(dec(h["xq"]) * np.repeat(h["sx"][:, :M].T, 128, axis=1))
+    wa = np.abs(dec(h["wq"]) * np.repeat(np.repeat(h["sw"], 128, axis=0), 128, axis=1))
+    assert_gemm_close(bf16_values(y2), oracle.fprop(h["xq"], h["sx"], h["wq"], h["sw"]), xa @ wa, True,
+                      f"mx fprop on W [K x N] {M}x{K}x{N}")
+
+
 @pytest.mark.parametrize("M,K,N,batch", [(200, 384, 256, 1), (513, 512, 384, 1), (128, 256, 128, 3)])
 def test_packed_casts_equal_cast_then_pack(M, K, N, batch):
     """The casts that write their scale atoms in the same pass give the same
