@@ -806,8 +806,8 @@ fp8bs_status requant_common(int src_mode, const void* src, const float* src_scal
         p.tile_start[0] = 0;
         p.tile_start[1] = static_cast<int32_t>(mpad / 128);
     }
-    if (q && q_scales && src_mode == FP8BS_SRC_BF16 && !sr && !grouped && !offsets_dev) {
-        // dense, round to nearest: the TMA-fed tile kernel
+    if (q && q_scales && src_mode == FP8BS_SRC_BF16 && !sr) {
+        // round to nearest, dense or grouped: the TMA-fed tile kernel
         CUtensorMap map_x, map_q;
         if (!cached_src_map(&map_x, src, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
                             static_cast<uint64_t>(cols) * 2, 128u) ||

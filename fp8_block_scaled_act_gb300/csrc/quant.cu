@@ -1172,6 +1172,15 @@ __global__ void __launch_bounds__(kQ3Threads, kSR ? 2 : (kStash ? 3 : 4)) requan
 // identical; the work split is what differs (no shuffles for the row
 // maxima or scales, one decode of the stash per element, loads overlapped
 // with the work).
+//
+// Grouped form (kGrouped: expert groups from host or device offsets): block
+// rt of the padded token axis belongs to group g, whose rows start at
+// off[g]; the block is read from source row off[g] + 128 (rt - first tile of
+// g), and its rows past the group's end (the next group's rows) count as
+// zeros: the stash codes of those rows are staged as zeros, the dual cast's
+// values are masked, and a group's last block stores only its own rows of
+// the 1x128 codes (plain stores, where a whole block leaves with a TMA
+// store). The transposed output keeps the padded token index rt.
 // ---------------------------------------------------------------------------
 constexpr int kDtThreads = 256;
 constexpr int kDtXBytes = 128 * 128 * 2;                   // one BF16 block
@@ -1180,7 +1189,8 @@ constexpr int kDtCpartOff = kDtQOff + 128 * 128;           // float [8][128] col
 constexpr int kDtRowScaleOff = kDtCpartOff + 8 * 128 * 4;  // float [128]
 constexpr int kDtColTsOff = kDtRowScaleOff + 128 * 4;      // TileScale [128]
 constexpr int kDtBarOff = kDtColTsOff + 128 * 8;           // two mbarriers
-constexpr int kDtSmemBytes = kDtBarOff + 16 + 1023;        // + slack for the 1024-byte alignment
+constexpr int kDtGroupOff = kDtBarOff + 16;                // grouped form: int32 off[257], tile start[257], 8 sums
+constexpr int kDtSmemBytes = kDtGroupOff + (2 * (kMaxGroups + 1) + 8) * 4 + 1023;   // + alignment slack
 constexpr uint64_t kDtDrainNs = 1000000000ull;
 
 __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
@@ -1190,7 +1200,46 @@ __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
     return v;
 }
 
-template <bool kStash>
+// Group table of the grouped tile kernel in shared memory (all threads of
+// the CTA call it; it ends with a CTA barrier): the row offsets off[0..G]
+// (host offsets from the parameters, or device offsets) and the first padded
+// token block of each group, tstart[0..G] (tstart[G] = the blocks of all
+// groups). Returns tstart[G], or 0 when the offsets are invalid (off[0] !=
+// 0, a decrease, a total other than p.rows, more blocks than p.mpad holds),
+// which CTA 0 records as FP8BS_ERR_DEVICE.
+__device__ int dt_group_table(const RequantParams& p, int32_t* off, int32_t* tstart, int32_t* wsum)
+{
+    const int G = p.num_groups;   // <= kMaxGroups = kDtThreads
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    for (int i = t; i <= G; i += kDtThreads) off[i] = p.off_dev ? __ldg(p.off_dev + i) : p.off[i];
+    __syncthreads();
+    int bad = 0, cnt = 0;
+    if (t < G) {
+        const int n = off[t + 1] - off[t];
+        if (n < 0) bad = 1;
+        cnt = n < 0 ? 0 : (n + 127) / 128;
+    }
+    if (t == 0 && (off[0] != 0 || static_cast<int64_t>(off[G]) != p.rows)) bad = 1;
+    int inc = cnt;   // inclusive scan of the block counts (one group per thread)
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+        if (lane >= d) inc += v;
+    }
+    if (lane == 31) wsum[warp] = inc;
+    __syncthreads();
+    for (int w = 0; w < warp; ++w) inc += wsum[w];
+    if (t < G) tstart[t] = inc - cnt;
+    if (t == G - 1) tstart[G] = inc;
+    bad = __syncthreads_or(bad);
+    const int total = tstart[G];
+    if (static_cast<int64_t>(total) * 128 > p.mpad) bad = 1;
+    if (bad && t == 0 && blockIdx.x == 0) atomicCAS(p.status, 0u, static_cast<unsigned int>(FP8BS_ERR_DEVICE));
+    __syncthreads();
+    return bad ? 0 : total;
+}
+
+template <bool kStash, bool kGrouped>
 __global__ void __launch_bounds__(kDtThreads, 2) dual_tile_kernel(const __grid_constant__ CUtensorMap map_x,
                                                                   const __grid_constant__ CUtensorMap map_q,
                                                                   const __grid_constant__ RequantParams p,
@@ -1205,16 +1254,41 @@ __global__ void __launch_bounds__(kDtThreads, 2) dual_tile_kernel(const __grid_c
     float* row_scale = reinterpret_cast<float*>(smem + kDtRowScaleOff);
     TileScale* col_ts = reinterpret_cast<TileScale*>(smem + kDtColTsOff);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kDtBarOff);
+    int32_t* g_off = reinterpret_cast<int32_t*>(smem + kDtGroupOff);
+    int32_t* g_start = g_off + kMaxGroups + 1;
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    if constexpr (kGrouped) {
+        // padded token blocks past the groups' total (device offsets size the
+        // grid for the largest total) are skipped
+        const int64_t total = dt_group_table(p, g_off, g_start, g_start + kMaxGroups + 1);
+        if (total * col_tiles < tiles) tiles = total * col_tiles;
+    }
 
+    // first source row of padded token block rt (its group's rows from there on)
+    auto src_row = [&](int64_t rt, int& g) -> int64_t {
+        if constexpr (kGrouped) {
+            int lo = 0, hi = p.num_groups - 1;   // last g with g_start[g] <= rt
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (g_start[mid] <= rt) lo = mid; else hi = mid - 1;
+            }
+            g = lo;
+            return static_cast<int64_t>(g_off[lo]) + (rt - g_start[lo]) * 128;
+        } else {
+            g = 0;
+            return rt * 128;
+        }
+    };
     auto issue = [&](int64_t tile, int buf) {
         const int64_t rt = tile / col_tiles;
         const int64_t ct = tile - rt * col_tiles;
+        int g;
+        const int64_t y = src_row(rt, g);
         uint8_t* dst = smem + buf * kDtXBytes;
         mbar_arrive_expect_tx(&full[buf], kDtXBytes);
-        tma_load_2d(dst, &map_x, &full[buf], static_cast<int32_t>(ct * 128), static_cast<int32_t>(rt * 128));
+        tma_load_2d(dst, &map_x, &full[buf], static_cast<int32_t>(ct * 128), static_cast<int32_t>(y));
         tma_load_2d(dst + kDtXBytes / 2, &map_x, &full[buf], static_cast<int32_t>(ct * 128 + 64),
-                    static_cast<int32_t>(rt * 128));
+                    static_cast<int32_t>(y));
     };
     if (t == 0) {
         mbar_init(&full[0], 1);
@@ -1234,8 +1308,12 @@ __global__ void __launch_bounds__(kDtThreads, 2) dual_tile_kernel(const __grid_c
         const uint32_t xs = xs0 + buf * kDtXBytes;
         const int64_t rt = tile / col_tiles;
         const int64_t ct = tile - rt * col_tiles;
-        const int64_t r0 = rt * 128, c0 = ct * 128;
-        const int len = static_cast<int>(min(static_cast<int64_t>(128), p.rows - r0));
+        int g;
+        const int64_t r0 = src_row(rt, g);        // first source row
+        const int64_t tk0 = rt * 128;             // first padded token (qT column)
+        const int64_t c0 = ct * 128;
+        const int64_t row_end = kGrouped ? static_cast<int64_t>(g_off[g + 1]) : p.rows;
+        const int len = static_cast<int>(min(static_cast<int64_t>(128), row_end - r0));
         const int nch = static_cast<int>(min(static_cast<int64_t>(128), p.cols - c0));
 
         // thread 0 waits (bounded) for the block and for the previous store's
@@ -1276,10 +1354,13 @@ __global__ void __launch_bounds__(kDtThreads, 2) dual_tile_kernel(const __grid_c
             m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
             const TileScale ts = tile_scale(__uint_as_float(m << 16), p.rule);
             const uint32_t outp = qs + r * 128;
+            // grouped: a row of the next group is staged as zero codes
+            const bool live = !kGrouped || r < len;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const uint2 a = quant8(d[2 * j], ts);
-                const uint2 b = quant8(d[2 * j + 1], ts);
+                uint2 a = quant8(d[2 * j], ts);
+                uint2 b = quant8(d[2 * j + 1], ts);
+                if (!live) a = b = make_uint2(0u, 0u);
                 st_shared_v4(outp + (((4 * h + j) ^ sw) << 4), make_uint4(a.x, a.y, b.x, b.y));
             }
             if (h == 0) {
@@ -1289,9 +1370,23 @@ __global__ void __launch_bounds__(kDtThreads, 2) dual_tile_kernel(const __grid_c
         }
         fence_proxy_async_smem();
         __syncthreads();
-        if (t == 0) {
-            tma_store_2d(&map_q, qs, static_cast<int32_t>(c0), static_cast<int32_t>(r0));
-            bulk_commit_group();
+        // a whole block, or one whose rows run to the tensor's end (the store
+        // stops there), leaves with one TMA store; a group's last block with
+        // rows of later groups after it stores only its own rows
+        const bool whole = !kGrouped || len == 128 || r0 + len >= p.rows;
+        if (whole) {
+            if (t == 0) {
+                tma_store_2d(&map_q, qs, static_cast<int32_t>(c0), static_cast<int32_t>(r0));
+                bulk_commit_group();
+            }
+        } else {
+            for (int i = t; i < len * 8; i += kDtThreads) {
+                const int rr = i >> 3, cc = i & 7;
+                if (16 * cc < nch) {
+                    const uint4 v = ld_shared_v4(qs + rr * 128 + ((cc ^ (rr & 7)) << 4));
+                    *reinterpret_cast<uint4*>(p.q + (r0 + rr) * p.cols + c0 + 16 * cc) = v;
+                }
+            }
         }
 
         // ---- transposed pass, part 1: the values and the parts' column maxima ----
@@ -1307,6 +1402,7 @@ __global__ void __launch_bounds__(kDtThreads, 2) dual_tile_kernel(const __grid_c
             for (int k = 0; k < 32; ++k) {
                 const int r = part * 32 + k;
                 w[k] = ld_shared_u32(colp + r * 128 + ((chunk ^ static_cast<uint32_t>(r & 7)) << 4));
+                if (kGrouped && r >= len) w[k] = 0u;   // the next group's row
                 mm = __vmaxu2(mm, w[k] & 0x7FFF7FFFu);
             }
             cpart[part][c] = __uint_as_float(mm << 16);
@@ -1399,7 +1495,7 @@ __global__ void __launch_bounds__(kDtThreads, 2) dual_tile_kernel(const __grid_c
                                 (encode2_exact(bf16_hi(x[2]), bf16_hi(x[3]), t1.s) << 16);
                     }
                 }
-                uint8_t* dst0 = p.qT + (c0 + c) * p.mpad + r0 + part * 32;
+                uint8_t* dst0 = p.qT + (c0 + c) * p.mpad + tk0 + part * 32;
                 uint8_t* dst1 = dst0 + p.mpad;
                 reinterpret_cast<uint4*>(dst0)[0] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
                 reinterpret_cast<uint4*>(dst0)[1] = make_uint4(o0[4], o0[5], o0[6], o0[7]);
@@ -1434,7 +1530,7 @@ __global__ void __launch_bounds__(kDtThreads, 2) dual_tile_kernel(const __grid_c
                             o[ch][k] = encode2_exact(-nv[4 * k][ch], -nv[4 * k + 1][ch], ts[ch].s) |
                                        (encode2_exact(-nv[4 * k + 2][ch], -nv[4 * k + 3][ch], ts[ch].s) << 16);
                 }
-                uint8_t* dst = p.qT + (c0 + c) * p.mpad + r0 + part * 16;
+                uint8_t* dst = p.qT + (c0 + c) * p.mpad + tk0 + part * 16;
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch)
                     *reinterpret_cast<uint4*>(dst + ch * p.mpad) = make_uint4(o[ch][0], o[ch][1], o[ch][2], o[ch][3]);
@@ -1727,21 +1823,21 @@ cudaError_t launch_dual_tile(const CUtensorMap& map_x, const CUtensorMap& map_q,
     if (e != cudaSuccess) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(ready.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(dual_tile_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDtSmemBytes);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(dual_tile_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kDtSmemBytes);
-        if (e != cudaSuccess) return e;
+        for (auto k : {dual_tile_kernel<false, false>, dual_tile_kernel<true, false>, dual_tile_kernel<false, true>,
+                       dual_tile_kernel<true, true>}) {
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kDtSmemBytes);
+            if (e != cudaSuccess) return e;
+        }
         ready.fetch_or(bit, std::memory_order_release);
     }
     int64_t blocks = 2 * static_cast<int64_t>(num_sms);   // two resident CTAs per SM
     if (blocks > tiles) blocks = tiles;
-    if (p.stash)
-        dual_tile_kernel<true><<<static_cast<unsigned>(blocks), kDtThreads, kDtSmemBytes, stream>>>(
-            map_x, map_q, p, col_tiles, tiles, limit);
-    else
-        dual_tile_kernel<false><<<static_cast<unsigned>(blocks), kDtThreads, kDtSmemBytes, stream>>>(
-            map_x, map_q, p, col_tiles, tiles, limit);
+    // groups (more than one, or device offsets): the grouped form
+    const bool grouped = p.num_groups > 1 || p.off_dev != nullptr;
+    auto kernel = p.stash ? (grouped ? dual_tile_kernel<true, true> : dual_tile_kernel<true, false>)
+                          : (grouped ? dual_tile_kernel<false, true> : dual_tile_kernel<false, false>);
+    kernel<<<static_cast<unsigned>(blocks), kDtThreads, kDtSmemBytes, stream>>>(map_x, map_q, p, col_tiles, tiles,
+                                                                                limit);
     return cudaGetLastError();
 }
 

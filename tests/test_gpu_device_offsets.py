@@ -171,6 +171,12 @@ def test_invalid_device_offsets_record_error_and_write_nothing(bad):
     fp8bs.fp8_requant_128x1_T(x, None, qT, sT, offsets=offd)
     assert fp8bs.fp8bs_last_device_status(reset=True) == ERR_DEVICE
     assert np.all(np_(qT) == 0x5A)
+    for fn in (fp8bs.fp8_quant_dual, fp8bs.fp8_quant_dual_stash):   # the grouped tile kernel
+        q, s = fp8bs.empty_quant_1x128(M, C)
+        q.fill_(0x5A)
+        fn(x, q, s, qT, sT, offsets=offd)
+        assert fp8bs.fp8bs_last_device_status(reset=True) == ERR_DEVICE, fn.__name__
+        assert np.all(np_(qT) == 0x5A) and np.all(np_(q) == 0x5A), fn.__name__
     xq, sx = fp8bs.empty_quant_1x128(M, K)
     fp8bs.fp8_quant_1x128(wl.normal((M, K), seed=61).cuda(), xq, sx)
     wq, wqT, sw = fp8bs.empty_quant_128x128(K, N, batch=G)
