@@ -787,7 +787,8 @@ def run_ours(args, world, rank, local):
     step_flops = sum(flops.values())
     e2e = None
     if step_flops > 0:
-        e2e = measure_e2e(args, fp8bs, torch, [step, make_step()], device, step_flops, world, dist)
+        e2e = measure_e2e(args, fp8bs, torch, [step, make_step(), make_step()], device, step_flops, world,
+                          dist)
 
     line = {
         "metric": METRIC, "value": summ["value"], "unit": summ["unit"], "n_gpus": world,
@@ -895,8 +896,10 @@ def measure_e2e(args, fp8bs, torch, steps, device, step_flops, world, dist):
     """Same step through the public API with host buffers: every step copies
     its inputs in from pinned host memory, runs, and copies its outputs
     (Y, dX, dW) back. Consecutive steps are pipelined on three streams over
-    two sets of device tensors (`steps`, two step objects): step i's host
-    copies overlap step i - 1's kernels, as a data pipeline would run."""
+    len(steps) sets of device tensors (step objects, three here): step i's
+    input copy starts once step i - len(steps) has copied its outputs out,
+    so the host link carries both directions while the kernels run, as a
+    data pipeline would run it."""
     def make():
         h_in = [t.cpu().pin_memory() for t in steps[0].io()[0]]
         h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in st.io()[1]] for st in steps]
@@ -906,11 +909,12 @@ def measure_e2e(args, fp8bs, torch, steps, device, step_flops, world, dist):
     launches = [st.launches() for st in steps]
     comp = torch.cuda.current_stream()
     h2d, d2h = torch.cuda.Stream(device), torch.cuda.Stream(device)
-    free = [None, None]
+    nbuf = len(steps)
+    free = [None] * nbuf
 
     def run(n, start=None):
         for i in range(n):
-            b = i % 2
+            b = i % nbuf
             d_in, d_out = steps[b].io()
             if free[b] is not None:
                 h2d.wait_event(free[b])
@@ -933,9 +937,9 @@ def measure_e2e(args, fp8bs, torch, steps, device, step_flops, world, dist):
             free[b] = torch.cuda.Event()
             free[b].record(d2h)
 
-    run(max(2, args.warmup))
+    run(max(nbuf, args.warmup))
     torch.cuda.synchronize()
-    free[0] = free[1] = None
+    free = [None] * nbuf
     n = max(1, args.steps)
     barrier(dist, device.index)
     s = torch.cuda.Event(enable_timing=True)
@@ -949,7 +953,7 @@ def measure_e2e(args, fp8bs, torch, steps, device, step_flops, world, dist):
     return {"value": round(whole_job_throughput(step_flops * n, world, sec) / 1e12, 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
             "ms_per_step": round(sec * 1e3 / n, 4),
-            "pipeline": "host copies of step i overlap the kernels of step i-1 (three streams, two device "
+            "pipeline": f"host copies overlap the kernels of neighbouring steps (three streams, {nbuf} device "
                         "buffer sets)",
             "host_buffers": placement}
 
