@@ -185,6 +185,50 @@ def test_stream_k_short_contraction(K):
     assert_gemm_close(y, ref, bound, True, f"fprop stream-K {M}x{K}x{N}")
 
 
+@pytest.mark.parametrize("op", ["fprop", "fprop_wkn", "dgrad"])
+def test_grouped_many_tiles_host_and_device_offsets(op):
+    """220 output tiles of 128 x 256 over six experts (empty ones included),
+    two K-blocks each, more tiles than a 152-SM GPU's persistent grid: host
+    and device offsets give the same bytes, and every expert's rows match
+    the oracle."""
+    counts = [0, 300, 129, 1, 0, 2000]
+    off = wl.offsets_from_counts(counts)
+    M, G = int(off[-1]), len(counts)
+    C, Wd = 256, 2432                     # contraction, output width
+    a_src = wl.with_outliers((M, C), fraction=0.01, seed=71)
+    aq, sa, oaq, osa = q1x128(a_src)
+    if op == "dgrad":
+        w = wl.normal((G, Wd, C), std=wl.W_STD, seed=72)    # W_e [K = Wd x N = C]
+        wq, _, sw = q128(w)
+        b, N, K, opc = wq, C, Wd, fp8bs.OP_DGRAD
+    else:
+        w = wl.normal((G, C, Wd), std=wl.W_STD, seed=73)    # W_e [K = C x N = Wd]
+        wq, wqT, sw = q128(w)
+        b, N, K = (wqT, Wd, C) if op == "fprop" else (wq, Wd, C)
+        opc = fp8bs.OP_FPROP if op == "fprop" else fp8bs.OP_FPROP_WKN
+    outs = []
+    for offs in (off, torch.tensor(off, dtype=torch.int32, device="cuda")):
+        y = torch.full((M, Wd), float("nan"), dtype=torch.bfloat16, device="cuda")
+        fp8bs.fp8_block_gemm_grouped(opc, offs, aq, sa, b, sw, y, N, K)
+        outs.append(y)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    y = bf16_values(outs[0])
+    for e in range(G):
+        r0, r1 = off[e], off[e + 1]
+        if r1 == r0:
+            continue
+        owq, osw = q128_oracle(w[e])
+        oae, osae = oaq[r0:r1], np.ascontiguousarray(osa[:, r0:r1])
+        a = np.abs(dequant_rows(oae, osae))
+        bb = np.abs(dequant_blocks(owq, osw))
+        if op == "dgrad":
+            ref, bound = oracle.dgrad(oae, osae, owq, osw), a @ bb.T
+        else:
+            ref, bound = oracle.fprop(oae, osae, owq, osw), a @ bb
+        assert_gemm_close(y[r0:r1], ref, bound, True, f"grouped many tiles {op} e{e}")
+
+
 # ---------------------------------------------------------------------------
 # Dgrad
 # ---------------------------------------------------------------------------
