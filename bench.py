@@ -228,6 +228,7 @@ class DenseStep:
         self.dW = torch.empty(N, K, dtype=torch.float32, device=device)
         self.names = ["quant_128x128(W)", "quant_dual_stash(X)", "fprop", "quant_dual(dY)", "dgrad", "wgrad"]
         self.side = torch.cuda.Stream(device)
+        self.dag_desc = "CUDA graph, two streams (W || X casts, Dgrad || Wgrad)"
 
     def work(self):
         return step_work(self.M, self.K, self.N)
@@ -539,6 +540,9 @@ class LongKStep:
                              dtype=torch.uint8, device=device)
             Y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
             self.cases.append(dict(K=K, X=X, W=W, xq=xq, sx=sx, wq=wq, wqT=wqT, sw=sw, sp=sp, ws=ws, Y=Y))
+        # the four problems are independent: two streams each (X || W cast)
+        self.streams = [torch.cuda.Stream(device) for _ in range(2 * len(self.cases))]
+        self.dag_desc = "CUDA graph, the four problems on their own streams (X || W casts, then split-K Fprop)"
         self.names = []
         for c in self.cases:
             self.names += [f"quant_1x128(X,K={c['K']})", f"quant_128x128(W,K={c['K']})",
@@ -564,6 +568,38 @@ class LongKStep:
                     lambda c=c: e.fp8_block_gemm_splitk(e.OP_FPROP_WKN, c["xq"], c["sx"], c["wq"], c["sw"],
                                                         c["Y"], splits=c["sp"], workspace=c["ws"])]
         return out
+
+    def run_dag(self):
+        """The problems run side by side, the longest first: each on its own
+        stream, its W cast on a second one, so the small problems use SMs the
+        large ones leave idle (the split-K GEMMs take one SM per range)."""
+        torch, L = self.torch, self.launches_cached()
+        main = torch.cuda.current_stream()
+        fork = torch.cuda.Event()
+        fork.record(main)
+        done = []
+        for i in reversed(range(len(self.cases))):
+            sx, sw = self.streams[2 * i], self.streams[2 * i + 1]
+            sx.wait_event(fork)
+            sw.wait_event(fork)
+            with torch.cuda.stream(sw):
+                L[3 * i + 1]()                      # W cast
+            w_done = torch.cuda.Event()
+            w_done.record(sw)
+            with torch.cuda.stream(sx):
+                L[3 * i]()                          # X cast
+                sx.wait_event(w_done)
+                L[3 * i + 2]()                      # split-K Fprop (and its reduction)
+            ev = torch.cuda.Event()
+            ev.record(sx)
+            done.append(ev)
+        for ev in done:
+            main.wait_event(ev)
+
+    def launches_cached(self):
+        if not hasattr(self, "_launches"):
+            self._launches = self.launches()
+        return self._launches
 
     def io(self):
         return (tuple(t for c in self.cases for t in (c["X"], c["W"])),
@@ -633,8 +669,7 @@ def time_step(args, step, fp8bs, torch, dist, local, flush, stream):
                 graph.replay()
             torch.cuda.synchronize()
             run_step = graph.replay
-            launch_mode = ("CUDA graph, two streams (W || X casts, Dgrad || Wgrad)"
-                           if hasattr(step, "run_dag") else "CUDA graph")
+            launch_mode = getattr(step, "dag_desc", "CUDA graph")
         except Exception as ex:   # capture unsupported: time the stream launches
             launch_mode = f"stream launches (graph capture failed: {type(ex).__name__})"
         if fp8bs.fp8bs_device_status(reset=True) != 0:

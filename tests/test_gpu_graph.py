@@ -1,8 +1,9 @@
-"""The dense step captured in a CUDA graph (the form bench.py times): every
-entry point the step calls is capture-safe, and replaying the graph, whose
-two independent pairs (the W and X casts, Dgrad and Wgrad) run on two
-streams, gives byte-identical outputs to launching the same kernels one by
-one on one stream."""
+"""The benchmarked steps captured in CUDA graphs (the form bench.py times):
+every entry point they call is capture-safe, and replaying the graph gives
+byte-identical outputs to launching the same kernels one by one on one
+stream. The dense step's graph runs its two independent pairs (the W and X
+casts, Dgrad and Wgrad) on two streams; the long-contraction workload's
+graph runs its four problems side by side on their own streams."""
 import os
 import sys
 
@@ -53,4 +54,27 @@ def test_graph_replay_matches_stream_launches(M, K, N):
         graph.replay()
     torch.cuda.synchronize()
     for a, b in zip(ref, _outputs(step)):
+        assert torch.equal(a, b)
+
+
+def test_longk_graph_with_concurrent_problems_matches_stream_launches():
+    dev = torch.device("cuda", 0)
+    step = bench.LongKStep(fp8bs, torch, dev, seed=5)
+    outs = lambda: [t for c in step.cases for t in (c["Y"], c["xq"], c["sx"], c["wq"], c["sw"])]
+    for f in step.launches():
+        f()
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in outs()]
+    for t in outs():
+        t.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step.run_dag()
+    torch.cuda.synchronize()
+    for t in outs():
+        t.zero_()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(ref, outs()):
         assert torch.equal(a, b)
