@@ -441,7 +441,7 @@ fp8bs_status run_rowwise_gemm(int op, const Offsets& o, const uint8_t* a, const 
     const int64_t M = o.rows;
     if (M == 0) return FP8BS_OK;
     if (M > 0x7FFFFFFF - kBM * static_cast<int64_t>(o.groups) || width * o.groups > 0x7FFFFFFF ||
-        contr > 0x7FFFFFFF)
+        contr > 0x7FFFFFFF || (b_mn && contr * o.groups > 0x7FFFFFFF))   // MN-major B rows: contr x groups
         return FP8BS_ERR_SHAPE;
 
     GemmParams p;
@@ -1188,7 +1188,7 @@ fp8bs_status mx_gemm_grouped(int op, int32_t groups, const int32_t* offsets_dev,
     const int64_t contr = op == FP8BS_OP_DGRAD ? N : K;
     const int64_t width = op == FP8BS_OP_DGRAD ? K : N;
     if (contr % 128 != 0 || width % 256 != 0 || rows > 0x7FFFFF00 || contr > 0x7FFFFFFF ||
-        width * groups > 0x7FFFFFFF || N * groups > 0x7FFFFFFF)
+        width * groups > 0x7FFFFFFF || N * groups > 0x7FFFFFFF || (b_mn && contr * groups > 0x7FFFFFFF))
         return FP8BS_ERR_SHAPE;
     if (!out) return FP8BS_ERR_ARG;
     DeviceState* st = nullptr;
