@@ -233,17 +233,20 @@ def _moe_outputs(G, cap, dev="cuda"):
     return o
 
 
-def _moe_pass(o, offsets, inp, W):
+def _moe_pass(o, offsets, inp, W, w_as_stored=False):
     """The routed part of the MoE pass: the casts of X, of the down-projection
     input A (with the 128x1 requant of its stash) and of dY (both
-    orientations), the up and down Fprop, the down Dgrad and Wgrad."""
+    orientations), the up and down Fprop (on the weights' transposed codes,
+    or with w_as_stored on their codes as stored, read MN-major), the down
+    Dgrad and Wgrad."""
     hidden, inter, up, M = 7168, 2048, 4096, 8192
+    fprop, wu, wd = ((fp8bs.OP_FPROP_WKN, W["wuq"], W["wdq"]) if w_as_stored
+                     else (fp8bs.OP_FPROP, W["wuqT"], W["wdqT"]))
     fp8bs.fp8_quant_1x128(inp["X"], o["xq"], o["sx"])
     fp8bs.fp8_quant_dual_stash(inp["A"], o["aq"], o["sa"], o["aT"], o["saT"], offsets=offsets)
     fp8bs.fp8_quant_dual(inp["dY"], o["dyq"], o["sdy"], o["dyT"], o["sdyT"], offsets=offsets)
-    fp8bs.fp8_block_gemm_grouped(fp8bs.OP_FPROP, offsets, o["xq"], o["sx"], W["wuqT"], W["swu"], o["y"], up, hidden)
-    fp8bs.fp8_block_gemm_grouped(fp8bs.OP_FPROP, offsets, o["aq"], o["sa"], W["wdqT"], W["swd"], o["y2"],
-                                 hidden, inter)
+    fp8bs.fp8_block_gemm_grouped(fprop, offsets, o["xq"], o["sx"], wu, W["swu"], o["y"], up, hidden)
+    fp8bs.fp8_block_gemm_grouped(fprop, offsets, o["aq"], o["sa"], wd, W["swd"], o["y2"], hidden, inter)
     fp8bs.fp8_block_gemm_grouped(fp8bs.OP_DGRAD, offsets, o["dyq"], o["sdy"], W["wdq"], W["swd"], o["da"],
                                  hidden, inter)
     fp8bs.fp8_block_gemm_grouped(fp8bs.OP_WGRAD, offsets, o["dyT"], o["sdyT"], o["aT"], o["saT"], o["dw"],
@@ -303,10 +306,12 @@ def _check_moe_against_oracle(o, d, off, W_cpu, experts, seed):
 @pytest.mark.slow
 def test_moe_pass_one_graph_device_offsets_two_routings():
     """The MoE workload's routed pass captured ONCE as a CUDA graph that reads
-    its offsets from device memory; replayed under the workload's routing and
-    under a second routing written into the same offsets tensor. Each replay
-    is byte-identical to eager calls with host offsets and matches the oracle
-    on sampled elements of several experts (empty experts: exact zero dW)."""
+    its offsets from device memory, its Fprops on the experts' weight codes
+    as stored (the benchmarked form); replayed under the workload's routing
+    and under a second routing written into the same offsets tensor. Each
+    replay is byte-identical to eager calls with host offsets and the
+    transposed weight codes, and matches the oracle on sampled elements of
+    several experts (empty experts: exact zero dW)."""
     d = wl.moe()
     G, M = len(d["counts"]), 8192
     off1 = d["offsets"]
@@ -322,11 +327,11 @@ def test_moe_pass_one_graph_device_offsets_two_routings():
     cap = fp8bs.fp8bs_padded_tokens_max(M, G)
     offd = _dev(off1)
     og = _moe_outputs(G, cap)
-    _moe_pass(og, offd, inp, W)               # warm-up (first-use set-up happens outside capture)
+    _moe_pass(og, offd, inp, W, True)         # warm-up (first-use set-up happens outside capture)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        _moe_pass(og, offd, inp, W)
+        _moe_pass(og, offd, inp, W, True)
     for routing, off in ((1, off1), (2, off2)):
         offd.copy_(torch.from_numpy(off.astype(np.int32)))
         for t in og.values():
