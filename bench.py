@@ -1,8 +1,9 @@
 """Benchmark of the fine-grained FP8 linear layer on GB300.
 
 One step is one pass of the layer's whole data path over one batch of
-synthetic input: the weight's 128x128 quantization (with its transposed
-copy), the 1x128 quantization of X, Fprop, the dual-orientation cast of dY
+synthetic input: the weight's 128x128 quantization (codes and scales; Fprop
+reads the codes as stored), the 1x128 quantization of X, Fprop, the
+dual-orientation cast of dY
 (its 1x128 and 128x1 transposed quantizations from one read), Dgrad, the
 128x1 transposed requant of X from its E4M3 stash, and Wgrad. Default workload: X 4096x7168 (N(0,1) with 0.1% outliers),
 W 7168x2048 (N(0,0.02^2)), dY 4096x2048 (N(0,1e-3^2)); its numbers are the
