@@ -150,6 +150,33 @@ def test_quant_128x128_batched_ragged(B, R, C):
         assert np.array_equal(sc[e].view(np.uint32), osc.view(np.uint32)), f"expert {e} scales"
 
 
+@pytest.mark.parametrize("shape", [(7168, 2048), (3, 208, 384)])
+def test_quant_128x128_without_transpose(shape):
+    """The weight cast without its transposed copy (qT NULL: Fprop reading
+    the codes as stored): codes and scales equal the oracle's, for the dense
+    weight and for batched experts with a ragged edge, under round to nearest
+    and under stochastic rounding."""
+    w = (wl.dense(M=128)["W"] if len(shape) == 2 else
+         torch.stack([_special_inputs(shape[1], shape[2], seed=7 + b) for b in range(shape[0])]))
+    R, C = w.shape[-2:]
+    batch = w.shape[0] if w.dim() == 3 else None
+    wd = w.cuda()
+    q, _, sc = fp8bs.empty_quant_128x128(R, C, batch=batch, with_transpose=False)
+    fp8bs.fp8_quant_128x128(wd, q, None, sc)
+    q2, qT2, sc2 = fp8bs.empty_quant_128x128(R, C, batch=batch)
+    fp8bs.fp8_quant_128x128_sr(wd, q2, qT2, sc2, seed=11, salt=2)
+    qs, _, scs = fp8bs.empty_quant_128x128(R, C, batch=batch, with_transpose=False)
+    fp8bs.fp8_quant_128x128_sr(wd, qs, None, scs, seed=11, salt=2)
+    torch.cuda.synchronize()
+    assert torch.equal(qs, q2) and torch.equal(scs, sc2)   # SR codes do not depend on the transpose
+    ws = [w] if batch is None else list(w)
+    qn, scn = np_(q).reshape(-1, R, C), np_(sc).reshape(len(ws), -1)
+    for e, we in enumerate(ws):
+        oq, osc = oracle.quant_128x128(u16(we))
+        assert np.array_equal(qn[e], oq), f"entry {e}"
+        assert np.array_equal(scn[e].view(np.uint32), osc.reshape(-1).view(np.uint32)), f"entry {e} scales"
+
+
 def test_quant_128x128_dense_weight_full():
     w = wl.dense(M=128)["W"]
     q, qT, sc = _gpu_quant_128x128(w)
