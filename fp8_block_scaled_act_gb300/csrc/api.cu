@@ -481,7 +481,7 @@ fp8bs_status run_rowwise_gemm(int op, const Offsets& o, const uint8_t* a, const 
         p.splits = used;
         p.kb_per_split = kps;
         p.ws = ws;
-        p.ws_split_stride = M * width;
+        p.ws_split_stride = splitk_tile_floats(M, width);
     }
 
     CUtensorMap ma, mb, mo;
@@ -522,7 +522,7 @@ fp8bs_status run_rowwise_gemm(int op, const Offsets& o, const uint8_t* a, const 
         launch_status(launch_gemm(GemmKind::kBlockScaleBf16, ma, mb, mo, p, max_units, st->num_sms, cs));
     if (r != FP8BS_OK || used <= 1) return r;
     return launch_status(
-        launch_splitk_reduce(ws, used, M * width, M * width, static_cast<uint16_t*>(out), st->num_sms, cs));
+        launch_splitk_reduce(ws, used, M, width, static_cast<uint16_t*>(out), st->num_sms, cs));
 }
 
 // Wgrad, dense (one group over all T tokens) or grouped (padded segments,
@@ -1261,7 +1261,7 @@ size_t fp8bs_splitk_workspace_size(int op, int64_t M, int64_t N, int64_t K, int3
     int used = 1, kps = 1;
     splitk_shape(contr / 128, splits, used, kps);
     if (used <= 1) return 0;
-    return static_cast<size_t>(used) * static_cast<size_t>(M) * static_cast<size_t>(width) * sizeof(float);
+    return static_cast<size_t>(used) * static_cast<size_t>(splitk_tile_floats(M, width)) * sizeof(float);
 }
 
 int32_t fp8bs_splitk_default_splits(int op, int64_t M, int64_t N, int64_t K)

@@ -457,13 +457,17 @@ __device__ __forceinline__ bool epilogue_block_scale(const GemmParams& p, Shared
         }
 
         if (p.ws != nullptr) {
-            if (row_ok && cols_ok) {
-                // split-K: this range's fp32 sum goes to its own slice of the workspace
-                float* w = p.ws + static_cast<int64_t>(split) * p.ws_split_stride + static_cast<int64_t>(row) * p.out_ld + col0;
+            if (cols_ok) {
+                // split-K: this range's fp32 sum of the tile goes to its own
+                // slot of the workspace, float4 v of thread et at [v][et], so
+                // every warp store is 512 contiguous bytes (rows past the
+                // output hold zeros and are never read back)
+                const int et = ew * 32 + lane;
+                float4* slot = reinterpret_cast<float4*>(p.ws + static_cast<int64_t>(split) * p.ws_split_stride) +
+                               (static_cast<int64_t>(mt) * p.n_tiles + nt) * 32 * 256;
 #pragma unroll
                 for (int v = 0; v < 32; ++v)
-                    reinterpret_cast<float4*>(w)[v] =
-                        make_float4(acc[2 * v].x, acc[2 * v].y, acc[2 * v + 1].x, acc[2 * v + 1].y);
+                    slot[v * 256 + et] = make_float4(acc[2 * v].x, acc[2 * v].y, acc[2 * v + 1].x, acc[2 * v + 1].y);
             }
         } else if (cols_ok) {
             // Two rounds of 64 columns: each thread writes its row's 64 values
@@ -827,27 +831,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Split-K reduction: out = BF16(sum over splits s = 0, 1, ... of ws[s]), in
 // that order (the result does not depend on scheduling). Eight elements per
 // thread: two 16-byte loads per split, one 16-byte store.
-__global__ void __launch_bounds__(256) splitk_reduce_bf16_kernel(const float* __restrict__ ws, int splits,
-                                                                 int64_t split_stride, int64_t count,
-                                                                 uint16_t* __restrict__ out)
+// The split-K reduction: the ranges' fp32 sums of output tile t, laid out
+// by the GEMM epilogue as [v][et] float4 (thread et = epilogue warp w x 32
+// + lane holds row 32 (w % 4) + lane and columns 128 (w / 4) + 4 v .. + 3 of
+// the tile), are added in range order and rounded to BF16 once. One thread
+// per float4: reads coalesced along et, 8-byte writes of four BF16 values.
+__global__ void __launch_bounds__(256) splitk_reduce_bf16_kernel(const float4* __restrict__ ws, int splits,
+                                                                 int64_t split_stride4, int n_tiles, int64_t rows,
+                                                                 int64_t cols, uint16_t* __restrict__ out)
 {
-    const int64_t n8 = count / 8;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < split_stride4;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        float4 a = __ldcs(reinterpret_cast<const float4*>(ws) + 2 * i);
-        float4 b = __ldcs(reinterpret_cast<const float4*>(ws) + 2 * i + 1);
+        const int64_t tile = i / (32 * 256);
+        const int rem = static_cast<int>(i - tile * (32 * 256));
+        const int v = rem >> 8, et = rem & 255;
+        const int w = et >> 5, lane = et & 31;
+        const int64_t mt = tile / n_tiles, nt = tile - mt * n_tiles;
+        const int64_t row = mt * kBM + (w & 3) * 32 + lane;
+        const int64_t col = nt * kBN + (w >> 2) * 128 + 4 * v;
+        if (row >= rows || col >= cols) continue;
+        float4 a = __ldcs(ws + i);
         for (int s = 1; s < splits; ++s) {
-            const float4* w = reinterpret_cast<const float4*>(ws + s * split_stride) + 2 * i;
-            const float4 c = __ldcs(w), d = __ldcs(w + 1);
+            const float4 c = __ldcs(ws + s * split_stride4 + i);
             a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
-            b.x += d.x; b.y += d.y; b.z += d.z; b.w += d.w;
         }
-        uint4 o;
-        o.x = pack_bf16x2(a.x, a.y);
-        o.y = pack_bf16x2(a.z, a.w);
-        o.z = pack_bf16x2(b.x, b.y);
-        o.w = pack_bf16x2(b.z, b.w);
-        reinterpret_cast<uint4*>(out)[i] = o;
+        *reinterpret_cast<uint2*>(out + row * cols + col) = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
     }
 }
 
@@ -896,16 +904,17 @@ cudaError_t launch_kind(const CUtensorMap& map_a, const CUtensorMap& map_b, cons
 
 }  // namespace
 
-cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t split_stride, int64_t count,
-                                 uint16_t* out, int num_sms, cudaStream_t stream)
+cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t rows, int64_t cols, uint16_t* out, int num_sms,
+                                 cudaStream_t stream)
 {
-    if (count <= 0) return cudaSuccess;
-    const int64_t n8 = count / 8;
-    int64_t blocks = (n8 + 255) / 256;
+    const int64_t n_tiles = (cols + kBN - 1) / kBN;
+    const int64_t split_stride4 = splitk_tile_floats(rows, cols) / 4;
+    if (split_stride4 <= 0) return cudaSuccess;
+    int64_t blocks = (split_stride4 + 255) / 256;
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
     if (blocks > cap) blocks = cap;
-    splitk_reduce_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ws, splits, split_stride, count,
-                                                                                  out);
+    splitk_reduce_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        reinterpret_cast<const float4*>(ws), splits, split_stride4, static_cast<int>(n_tiles), rows, cols, out);
     return cudaGetLastError();
 }
 

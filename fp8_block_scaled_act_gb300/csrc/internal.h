@@ -162,8 +162,8 @@ struct GemmParams {
     int tma_store;
     int splits;                   // split-K ranges per tile (1: none)
     int kb_per_split;             // K-blocks per range
-    float* ws;                    // split-K: fp32 range sums [splits][rows x out_ld], else null
-    int64_t ws_split_stride;      // floats between consecutive ranges' slices
+    float* ws;                    // split-K: fp32 range sums, [splits][tiles][32][256] float4, else null
+    int64_t ws_split_stride;      // floats between consecutive ranges' slices (splitk_tile_floats)
     uint64_t wait_limit_ns;
     unsigned int* status;
     // Test hook (fp8bs_selftest_gemm_timeout only): the epilogue never hands
@@ -201,9 +201,18 @@ constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 128;
 
-// out[i] = BF16(sum_s ws[s * split_stride + i]) for i < count (count % 8 == 0).
-cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t split_stride, int64_t count,
-                                 uint16_t* out, int num_sms, cudaStream_t stream);
+// Split-K workspace: per range, one slot of 128 x 256 fp32 per output tile
+// (tile-major, the tile's values as [32][256] float4 in the GEMM epilogue's
+// thread order); this many floats per range for an output of rows x cols.
+constexpr int64_t splitk_tile_floats(int64_t rows, int64_t cols)
+{
+    return ((rows + kBM - 1) / kBM) * ((cols + kBN - 1) / kBN) * static_cast<int64_t>(kBM) * kBN;
+}
+
+// out [rows x cols] BF16 = the sum over `splits` ranges of the workspace
+// slots, in range order, rounded once.
+cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t rows, int64_t cols, uint16_t* out, int num_sms,
+                                 cudaStream_t stream);
 
 // MXFP8 (mx.cu): 1x32 quantizer writing scale atoms, and the block-scaled GEMM.
 cudaError_t launch_mx_quant_1x32(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* q, uint8_t* atoms,

@@ -161,7 +161,8 @@ def test_product_path_does_not_import_oracle():
 
 
 def test_splitk_workspace_arithmetic_and_argument_errors():
-    """Workspace size = ranges actually used x M x output width x 4 bytes, with
+    """Workspace size = ranges actually used x one 128 x 256 fp32 slot per
+    output tile (ceil(M / 128) x ceil(width / 256) tiles) x 4 bytes, with
     ranges = ceil(nblocks / ceil(nblocks / splits)); bad arguments are
     rejected before any device work."""
     L = fp8bs.lib()
@@ -170,6 +171,7 @@ def test_splitk_workspace_arithmetic_and_argument_errors():
     assert ws(fp8bs.OP_FPROP, 256, 256, 1024, 1) == 0
     assert ws(fp8bs.OP_FPROP, 256, 256, 1024, 100) == 8 * 256 * 256 * 4     # clamped to 8 blocks
     assert ws(fp8bs.OP_DGRAD, 256, 256, 1024, 4) == 2 * 256 * 1024 * 4      # contraction N = 256
+    assert ws(fp8bs.OP_FPROP, 300, 384, 1024, 4) == 4 * (3 * 2) * 128 * 256 * 4   # ragged: whole tiles
     assert ws(fp8bs.OP_WGRAD, 256, 256, 1024, 4) == 0
     assert ws(fp8bs.OP_FPROP, 0, 256, 1024, 4) == 0
     assert ws(fp8bs.OP_FPROP, 100, 256, 1000, 4) == 0                        # K % 128 != 0

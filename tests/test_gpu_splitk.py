@@ -85,7 +85,7 @@ def test_splitk_is_deterministic():
 def test_splitk_rejects_short_workspace():
     (xq, sx, wqT, sw), _ = _fprop_operands(128, 1024, 128, seed=3)
     need = fp8bs.fp8bs_splitk_workspace_size(fp8bs.OP_FPROP, 128, 128, 1024, 4)
-    assert need == 4 * 128 * 128 * 4
+    assert need == 4 * 128 * 256 * 4     # one 128 x 256 tile slot per range
     short = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
     with pytest.raises(fp8bs.Fp8bsError):
         _splitk(fp8bs.OP_FPROP, xq, sx, wqT, sw, (128, 128), 4, workspace=short)
