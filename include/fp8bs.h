@@ -429,6 +429,9 @@ FP8BS_API fp8bs_status fp8_block_gemm_wgrad(const uint8_t* dyqT, const float* sd
 /*             used by anything else until the call has completed on stream.  */
 /* Errors: FP8BS_ERR_ARG (bad op, splits < 1, NULL or too small workspace),   */
 /* FP8BS_ERR_SHAPE / FP8BS_ERR_ALIGN as for the unsplit calls.                */
+/* fp8bs_splitk_workspace_size: the ranges actually used (ceil(blocks /       */
+/* ceil(blocks / splits))) x one 128 x 256 fp32 slot per 128 x 256 output     */
+/* tile, in bytes; 0 when no split happens or the arguments are invalid.     */
 FP8BS_API size_t fp8bs_splitk_workspace_size(int op, int64_t M, int64_t N, int64_t K, int32_t splits);
 
 /* A split count for this device: about one range per idle SM when the       */
