@@ -436,11 +436,11 @@ class MoeStep:
 
 class MoeUe8m0Step(MoeStep):
     """The grouped MoE expert pass with power-of-two (UE8M0) scales: the same
-    casts under the UE8M0 rule (the weight casts also writing their scales'
-    exponent bytes into the MX scale atoms; the grouped activation scales
-    packed into the groups' tile layout), and the four grouped GEMMs on the
-    tensor core's block scaling (fp8_mx_gemm_grouped) instead of the software
-    promotion."""
+    casts under the UE8M0 rule, each writing its scales' exponent bytes into
+    the MX scale atoms in the same pass (the weight casts; the grouped dual
+    casts of A and dY, in the groups' tile layout; X's 1x128 cast is packed
+    by a separate launch), and the four grouped GEMMs on the tensor core's
+    block scaling (fp8_mx_gemm_grouped) instead of the software promotion."""
 
     def __init__(self, fp8bs, torch, device, **kw):
         super().__init__(fp8bs, torch, device, **kw)
@@ -454,14 +454,9 @@ class MoeUe8m0Step(MoeStep):
         self.ax, self.aa, self.ady = atoms(cap, H), atoms(cap, I), atoms(cap, H)
         self.adyT, self.aaT = atoms(H, cap), atoms(I, cap)
         self.cap = cap
-        # the transposed casts with device offsets write only the actual
-        # padded tokens; the scales past them are packed too, so they hold 1
-        self.saT.fill_(1.0)
-        self.sdyT.fill_(1.0)
         self.names = ["quant_128x128(W_up)+atoms", "quant_128x128(W_down)+atoms", "quant_1x128(X)",
-                      "pack(X)", "mx_grouped_fprop_up", "quant_dual_stash(A)", "pack(A)", "pack(A^T)",
-                      "mx_grouped_fprop_down", "quant_dual(dY)", "pack(dY)", "pack(dY^T)",
-                      "mx_grouped_dgrad_down", "mx_grouped_wgrad_down"]
+                      "pack(X)", "mx_grouped_fprop_up", "quant_dual_stash(A)+atoms", "mx_grouped_fprop_down",
+                      "quant_dual(dY)+atoms", "mx_grouped_dgrad_down", "mx_grouped_wgrad_down"]
 
     def work(self):
         flops, b = super().work()
@@ -477,13 +472,9 @@ class MoeUe8m0Step(MoeStep):
             "quant_1x128(X)": b["quant_1x128(X)"],
             "pack(X)": 4 * (H // 128) * s_ld + atom(mp, H),
             "mx_grouped_fprop_up": b["grouped_fprop_up"] + atom(mp, H) + G * atom(U, H),
-            "quant_dual_stash(A)": b["quant_dual_stash(A)"],
-            "pack(A)": 4 * (I // 128) * s_ld + atom(mp, I),
-            "pack(A^T)": 4 * (mp // 128) * I + atom(I, mp),
+            "quant_dual_stash(A)+atoms": b["quant_dual_stash(A)"] + atom(mp, I) + atom(I, mp),
             "mx_grouped_fprop_down": b["grouped_fprop_down"] + atom(mp, I) + G * atom(H, I),
-            "quant_dual(dY)": b["quant_dual(dY)"],
-            "pack(dY)": 4 * (H // 128) * s_ld + atom(mp, H),
-            "pack(dY^T)": 4 * (mp // 128) * H + atom(H, mp),
+            "quant_dual(dY)+atoms": b["quant_dual(dY)"] + atom(mp, H) + atom(H, mp),
             "mx_grouped_dgrad_down": b["grouped_dgrad_down"] + atom(mp, H) + G * atom(I, H),
             "mx_grouped_wgrad_down": b["grouped_wgrad_down"] + atom(H, mp) + atom(I, mp),
         }
@@ -497,13 +488,11 @@ class MoeUe8m0Step(MoeStep):
             lambda: e.fp8_quant_1x128_opts(self.X, self.xq, self.sx, o),
             lambda: e.fp8_pack_ue8m0_grouped(self.sx, T, H, off, self.ax),
             lambda: e.fp8_mx_gemm_grouped(e.OP_FPROP_WKN, off, self.xq, self.ax, self.wuq, self.awuT, self.Yu, U, H),
-            lambda: e.fp8_quant_dual_stash_opts(self.A, self.aq, self.sa, self.aT, self.saT, o, offsets=off),
-            lambda: e.fp8_pack_ue8m0_grouped(self.sa, T, I, off, self.aa),
-            lambda: e.fp8_pack_ue8m0(self.saT, I, self.cap, 1, 1, I, self.aaT),
+            lambda: e.fp8_quant_dual_stash_packed(self.A, self.aq, self.sa, self.aT, self.saT, self.aa, self.aaT,
+                                                  offsets=off),
             lambda: e.fp8_mx_gemm_grouped(e.OP_FPROP_WKN, off, self.aq, self.aa, self.wdq, self.awdT, self.Yd, H, I),
-            lambda: e.fp8_quant_dual_opts(self.dY, self.dyq, self.sdy, self.dyT, self.sdyT, o, offsets=off),
-            lambda: e.fp8_pack_ue8m0_grouped(self.sdy, T, H, off, self.ady),
-            lambda: e.fp8_pack_ue8m0(self.sdyT, H, self.cap, 1, 1, H, self.adyT),
+            lambda: e.fp8_quant_dual_packed(self.dY, self.dyq, self.sdy, self.dyT, self.sdyT, self.ady, self.adyT,
+                                            offsets=off),
             lambda: e.fp8_mx_gemm_grouped(e.OP_DGRAD, off, self.dyq, self.ady, self.wdq, self.awd, self.dA, H, I),
             lambda: e.fp8_mx_gemm_grouped(e.OP_WGRAD, off, self.dyT, self.adyT, self.aT, self.aaT, self.dWd, H, I,
                                           rows=T),

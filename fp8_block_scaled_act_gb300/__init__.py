@@ -41,6 +41,7 @@ __all__ = [
     "fp8_mx_quant_1x32_T", "fp8_mx_gemm_f32", "fp8_mx_gemm_wkn", "empty_mx_quant_T", "fp8_pack_ue8m0",
     "fp8_mx_gemm_grouped", "fp8_pack_ue8m0_grouped",
     "fp8_quant_128x128_packed", "fp8_quant_dual_packed", "fp8_quant_dual_stash_packed", "empty_mx_atoms",
+    "fp8_quant_dual_packed_grouped", "fp8_quant_dual_stash_packed_grouped",
 ]
 
 SRC_BF16, SRC_E4M3 = 0, 1
@@ -118,6 +119,8 @@ def lib() -> ctypes.CDLL:
         "fp8_quant_128x128_packed": ([P, I64, I64, I64, I64, P, P, P, P, P, P, P], S),
         "fp8_quant_dual_packed": ([P, I64, I64, P, P, P, P, P, P, P, P], S),
         "fp8_quant_dual_stash_packed": ([P, I64, I64, P, P, P, P, P, P, P, P], S),
+        "fp8_quant_dual_packed_grouped": ([P, I64, I64, P, P, I32, P, P, P, P, P, P, P, P], S),
+        "fp8_quant_dual_stash_packed_grouped": ([P, I64, I64, P, P, I32, P, P, P, P, P, P, P, P], S),
         "fp8_quant_128x128_sr": ([P, I64, I64, I64, I64, P, P, P, ctypes.c_uint64, ctypes.c_uint32, P, P], S),
         "fp8_block_gemm_fprop": ([P, P, P, P, I64, I64, I64, P, P], S),
         "fp8_block_gemm_fprop_wkn": ([P, P, P, P, I64, I64, I64, P, P], S),
@@ -621,7 +624,7 @@ def fp8_quant_128x128_packed(w, q, qT, scales, atoms_wT, atoms_w, stream=None) -
         _opts(SCALE_UE8M0, 0.0, 0.0), _stream(stream)))
 
 
-def _dual_packed(fn, x, q, scales, qT, scalesT, q_atoms, qT_atoms, stream) -> None:
+def _dual_packed(fn, x, q, scales, qT, scalesT, q_atoms, qT_atoms, stream, offsets=None) -> None:
     _need(x, torch.bfloat16, "x")
     for t, n, d in ((q, "q", torch.uint8), (scales, "scales", torch.float32), (qT, "qT", torch.uint8),
                     (scalesT, "scalesT", torch.float32), (q_atoms, "q_atoms", torch.uint8),
@@ -630,26 +633,53 @@ def _dual_packed(fn, x, q, scales, qT, scalesT, q_atoms, qT_atoms, stream) -> No
     rows, cols = x.shape
     if not x.is_contiguous():
         raise ValueError("x must be contiguous")
-    mp = fp8bs_padded_tokens(rows)
+    mp = _padded(rows, offsets)
     if (q.shape != (rows, cols) or scales.shape != ((cols + 127) // 128, fp8bs_scale_ld(rows))
             or qT.shape != (cols, mp) or scalesT.shape != (mp // 128, cols)):
         raise ValueError("output shapes do not match empty_quant_1x128 / empty_requant_128x1_T")
-    if q_atoms.numel() < fp8bs_mx_scale_bytes(rows, cols) or qT_atoms.numel() < fp8bs_mx_scale_bytes(cols, mp):
+    q_rows = rows if offsets is None else mp      # grouped: the groups' tile layout
+    if q_atoms.numel() < fp8bs_mx_scale_bytes(q_rows, cols) or qT_atoms.numel() < fp8bs_mx_scale_bytes(cols, mp):
         raise ValueError("atoms smaller than fp8bs_mx_scale_bytes of q / qT")
-    _check(fn, getattr(lib(), fn)(_ptr(x), rows, cols, _ptr(q), _ptr(scales), _ptr(qT), _ptr(scalesT),
-                                  _ptr(q_atoms), _ptr(qT_atoms), _opts(SCALE_UE8M0, 0.0, 0.0), _stream(stream)))
+    opts = _opts(SCALE_UE8M0, 0.0, 0.0)
+    if offsets is None:
+        _check(fn, getattr(lib(), fn)(_ptr(x), rows, cols, _ptr(q), _ptr(scales), _ptr(qT), _ptr(scalesT),
+                                      _ptr(q_atoms), _ptr(qT_atoms), opts, _stream(stream)))
+        return
+    dptr, hptr, groups, _, keep = _offsets_args(offsets, rows, rows)
+    gfn = fn + "_grouped"
+    _check(gfn, getattr(lib(), gfn)(_ptr(x), rows, cols, dptr, hptr, groups, _ptr(q), _ptr(scales), _ptr(qT),
+                                    _ptr(scalesT), _ptr(q_atoms), _ptr(qT_atoms), opts, _stream(stream)))
+    del keep
 
 
-def fp8_quant_dual_packed(x, q, scales, qT, scalesT, q_atoms, qT_atoms, stream=None) -> None:
+def fp8_quant_dual_packed(x, q, scales, qT, scalesT, q_atoms, qT_atoms, stream=None, offsets=None) -> None:
     """fp8_quant_dual under the UE8M0 rule that also writes the scale atoms
-    of q [rows x cols] and of qT [cols x Mpad]; dense x, cols % 128 == 0."""
-    _dual_packed("fp8_quant_dual_packed", x, q, scales, qT, scalesT, q_atoms, qT_atoms, stream)
+    of q [rows x cols] and of qT [cols x Mpad], cols % 128 == 0. With
+    ``offsets`` (host sequence or CUDA tensor, as in fp8_quant_dual) the
+    grouped form: q's atoms in the groups' tile layout."""
+    _dual_packed("fp8_quant_dual_packed", x, q, scales, qT, scalesT, q_atoms, qT_atoms, stream, offsets)
 
 
-def fp8_quant_dual_stash_packed(x, q, scales, qT, scalesT, q_atoms, qT_atoms, stream=None) -> None:
+def fp8_quant_dual_stash_packed(x, q, scales, qT, scalesT, q_atoms, qT_atoms, stream=None, offsets=None) -> None:
     """fp8_quant_dual_stash under the UE8M0 rule that also writes the scale
-    atoms of q [rows x cols] and of qT [cols x Mpad]; dense x, cols % 128 == 0."""
-    _dual_packed("fp8_quant_dual_stash_packed", x, q, scales, qT, scalesT, q_atoms, qT_atoms, stream)
+    atoms of q [rows x cols] and of qT [cols x Mpad], cols % 128 == 0. With
+    ``offsets``, the grouped form (see fp8_quant_dual_packed)."""
+    _dual_packed("fp8_quant_dual_stash_packed", x, q, scales, qT, scalesT, q_atoms, qT_atoms, stream, offsets)
+
+
+def fp8_quant_dual_packed_grouped(x, q, scales, qT, scalesT, q_atoms, qT_atoms, offsets, stream=None) -> None:
+    """The grouped form of fp8_quant_dual_packed (offsets required)."""
+    if offsets is None:
+        raise ValueError("the grouped form needs offsets")
+    fp8_quant_dual_packed(x, q, scales, qT, scalesT, q_atoms, qT_atoms, stream, offsets)
+
+
+def fp8_quant_dual_stash_packed_grouped(x, q, scales, qT, scalesT, q_atoms, qT_atoms, offsets,
+                                        stream=None) -> None:
+    """The grouped form of fp8_quant_dual_stash_packed (offsets required)."""
+    if offsets is None:
+        raise ValueError("the grouped form needs offsets")
+    fp8_quant_dual_stash_packed(x, q, scales, qT, scalesT, q_atoms, qT_atoms, stream, offsets)
 
 
 def _rule_kwargs(opts: Optional[ScaleOpts]) -> dict:

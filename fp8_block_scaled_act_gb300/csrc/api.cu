@@ -927,6 +927,42 @@ fp8bs_status fp8_quant_dual_stash_packed(const void* x, int64_t rows, int64_t co
                           true, nullptr, q_atoms, qT_atoms);
 }
 
+// The grouped forms: the tile kernel writes each block's exponent bytes into
+// the atoms of the groups' tile layout (q: padded token tile rt, K-block ct)
+// and of qT [cols x Mpad] (channel tile ct, token tile rt).
+static fp8bs_status dual_packed_grouped(bool stash, const void* x, int64_t rows, int64_t cols,
+                                        const int32_t* offsets_dev, const int32_t* offsets_host, int32_t groups,
+                                        uint8_t* q, float* scales, uint8_t* qT, float* scalesT, uint8_t* q_atoms,
+                                        uint8_t* qT_atoms, const fp8bs_scale_opts* opts, void* stream)
+{
+    if (!opts || opts->rule != FP8BS_SCALE_UE8M0) return FP8BS_ERR_ARG;
+    if (cols % 128 != 0) return FP8BS_ERR_SHAPE;
+    if ((offsets_dev == nullptr) == (offsets_host == nullptr) || groups < 1) return FP8BS_ERR_ARG;
+    if (rows > 0 && (!q || !scales || !q_atoms || !qT_atoms)) return FP8BS_ERR_ARG;
+    if ((q_atoms && !aligned16(q_atoms)) || (qT_atoms && !aligned16(qT_atoms))) return FP8BS_ERR_ALIGN;
+    return requant_common(FP8BS_SRC_BF16, x, nullptr, rows, cols, offsets_host, groups, qT, scalesT, q, scales, opts,
+                          stream, stash, nullptr, q_atoms, qT_atoms, offsets_dev);
+}
+
+fp8bs_status fp8_quant_dual_packed_grouped(const void* x, int64_t rows, int64_t cols, const int32_t* offsets_dev,
+                                           const int32_t* offsets_host, int32_t groups, uint8_t* q, float* scales,
+                                           uint8_t* qT, float* scalesT, uint8_t* q_atoms, uint8_t* qT_atoms,
+                                           const fp8bs_scale_opts* opts, void* stream)
+{
+    return dual_packed_grouped(false, x, rows, cols, offsets_dev, offsets_host, groups, q, scales, qT, scalesT,
+                               q_atoms, qT_atoms, opts, stream);
+}
+
+fp8bs_status fp8_quant_dual_stash_packed_grouped(const void* x, int64_t rows, int64_t cols,
+                                                 const int32_t* offsets_dev, const int32_t* offsets_host,
+                                                 int32_t groups, uint8_t* q, float* scales, uint8_t* qT,
+                                                 float* scalesT, uint8_t* q_atoms, uint8_t* qT_atoms,
+                                                 const fp8bs_scale_opts* opts, void* stream)
+{
+    return dual_packed_grouped(true, x, rows, cols, offsets_dev, offsets_host, groups, q, scales, qT, scalesT,
+                               q_atoms, qT_atoms, opts, stream);
+}
+
 fp8bs_status fp8_quant_128x128_packed(const void* w, int64_t batch, int64_t rows, int64_t cols, int64_t ldw,
                                       uint8_t* q, uint8_t* qT, float* scales, uint8_t* atoms_wT, uint8_t* atoms_w,
                                       const fp8bs_scale_opts* opts, void* stream)

@@ -636,8 +636,9 @@ FP8BS_API fp8bs_status fp8_pack_ue8m0_grouped(const float* scales, int64_t rows,
 /*     with the contraction along cols (Dgrad's B); each                     */
 /*     fp8bs_mx_scale_bytes(cols, rows) bytes per batch entry, entries       */
 /*     consecutive.                                                          */
-/*   fp8_quant_dual_packed / fp8_quant_dual_stash_packed: dense x only (no   */
-/*     groups), cols % 128 == 0; q_atoms: the atoms of q [rows x cols]       */
+/*   fp8_quant_dual_packed / fp8_quant_dual_stash_packed: dense x (the      */
+/*     _grouped forms below take expert groups), cols % 128 == 0; q_atoms:  */
+/*     the atoms of q [rows x cols]                                          */
 /*     (fp8bs_mx_scale_bytes(rows, cols) bytes, padding rows 127); qT_atoms: */
 /*     those of qT [cols x Mpad] (fp8bs_mx_scale_bytes(cols, Mpad) bytes).   */
 /* Atom pointers 16-byte aligned. A scale without an exponent byte (below    */
@@ -654,6 +655,29 @@ FP8BS_API fp8bs_status fp8_quant_dual_stash_packed(const void* x, int64_t rows, 
                                                    float* scales, uint8_t* qT, float* scalesT, uint8_t* q_atoms,
                                                    uint8_t* qT_atoms, const fp8bs_scale_opts* opts,
                                                    void* stream);
+
+/* The same two casts for expert groups (the MoE A and dY casts), with the   */
+/* group offsets of fp8_block_gemm_grouped (exactly one of offsets_dev /     */
+/* offsets_host, groups + 1 entries): q and scales as fp8_quant_1x128, qT   */
+/* and scalesT as the grouped fp8_requant_128x1_T ([cols x Mpad], each group */
+/* padded to 128 tokens; with device offsets Mpad is                        */
+/* fp8bs_padded_tokens_max(rows, groups) and only the groups' padded tokens */
+/* are written). q_atoms: the atoms of q in the groups' tile layout that     */
+/* fp8_pack_ue8m0_grouped writes (fp8bs_mx_scale_bytes(Mpad, cols) bytes);  */
+/* qT_atoms: those of qT [cols x Mpad] (fp8bs_mx_scale_bytes(cols, Mpad)     */
+/* bytes). Byte-identical to the grouped casts followed by                  */
+/* fp8_pack_ue8m0_grouped of scales and fp8_pack_ue8m0 of scalesT over the   */
+/* groups' padded tokens; atoms of tiles past those tokens are not written. */
+FP8BS_API fp8bs_status fp8_quant_dual_packed_grouped(const void* x, int64_t rows, int64_t cols,
+                                                     const int32_t* offsets_dev, const int32_t* offsets_host,
+                                                     int32_t groups, uint8_t* q, float* scales, uint8_t* qT,
+                                                     float* scalesT, uint8_t* q_atoms, uint8_t* qT_atoms,
+                                                     const fp8bs_scale_opts* opts, void* stream);
+FP8BS_API fp8bs_status fp8_quant_dual_stash_packed_grouped(const void* x, int64_t rows, int64_t cols,
+                                                           const int32_t* offsets_dev, const int32_t* offsets_host,
+                                                           int32_t groups, uint8_t* q, float* scales, uint8_t* qT,
+                                                           float* scalesT, uint8_t* q_atoms, uint8_t* qT_atoms,
+                                                           const fp8bs_scale_opts* opts, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* S7. Grouped (MoE expert) GEMMs                                             */

@@ -214,3 +214,12 @@ def test_ue8m0_packing_argument_validation(L):
         assert f(a16, 4, 96, a16, a16, a16, a16, a16, a16, ue, None) == ERR_SHAPE      # cols % 128
         assert f(a16, 4, 128, a16, a16, a16, a16, None, a16, ue, None) == ERR_ARG
         assert f(a16, 4, 128, a16, a16, a16, a16, a16, mis16, ue, None) == ERR_ALIGN
+    # the grouped forms (x, rows, cols, offsets_dev, offsets_host, groups, q, s, qT, sT, q_atoms, qT_atoms,
+    # opts, stream): exactly one offsets array, the UE8M0 rule, cols % 128
+    off = (ctypes.c_int32 * 3)(0, 2, 4)
+    for f in (L.fp8_quant_dual_packed_grouped, L.fp8_quant_dual_stash_packed_grouped):
+        assert f(a16, 4, 128, None, None, 2, a16, a16, a16, a16, a16, a16, ue, None) == ERR_ARG
+        assert f(a16, 4, 128, a16, off, 2, a16, a16, a16, a16, a16, a16, ue, None) == ERR_ARG
+        assert f(a16, 4, 128, None, off, 2, a16, a16, a16, a16, a16, a16, f32, None) == ERR_ARG
+        assert f(a16, 4, 96, None, off, 2, a16, a16, a16, a16, a16, a16, ue, None) == ERR_SHAPE
+        assert f(a16, 4, 128, None, off, 2, a16, a16, a16, a16, None, a16, ue, None) == ERR_ARG

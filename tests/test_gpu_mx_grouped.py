@@ -221,3 +221,45 @@ def test_grouped_mx_invalid_device_offsets_record_error_and_write_nothing(bad):
     n_host = fp8bs.fp8bs_mx_scale_bytes(fp8bs.fp8bs_padded_tokens(M, good), K)
     assert torch.equal(ax[:n_host], axh)
     assert torch.equal(y.view(torch.int16), yh.view(torch.int16))
+
+
+@pytest.mark.parametrize("stash", [False, True])
+@pytest.mark.parametrize("dev", [False, True])
+@pytest.mark.parametrize("counts", [[0, 129, 1, 0, 270], [300, 0], [5]])
+def test_grouped_packed_casts_equal_cast_then_pack(counts, dev, stash):
+    """The grouped dual and stash casts that write their scales' exponent
+    bytes in the same pass (q's atoms in the groups' tile layout, qT's over
+    the padded tokens) equal the grouped UE8M0 casts followed by
+    fp8_pack_ue8m0_grouped and fp8_pack_ue8m0, byte for byte; with device
+    offsets over the groups' padded tokens of the capacity layout."""
+    off = wl.offsets_from_counts(counts)
+    M, G, C = int(off[-1]), len(counts), 256
+    x = wl.with_outliers((M, C), fraction=0.01, seed=20 + G).cuda()
+    cast = fp8bs.fp8_quant_dual_stash_opts if stash else fp8bs.fp8_quant_dual_opts
+    fused = fp8bs.fp8_quant_dual_stash_packed if stash else fp8bs.fp8_quant_dual_packed
+    # reference: host offsets, cast then pack
+    mp = fp8bs.fp8bs_padded_tokens(M, off)
+    q, sc = fp8bs.empty_quant_1x128(M, C)
+    qT, scT = fp8bs.empty_requant_128x1_T(M, C, off)
+    cast(x, q, sc, qT, scT, UE8M0, offsets=off)
+    ra = torch.full((fp8bs.fp8bs_mx_scale_bytes(mp, C),), 0xEE, dtype=torch.uint8, device="cuda")
+    fp8bs.fp8_pack_ue8m0_grouped(sc, M, C, off, ra)
+    rT = torch.full((fp8bs.fp8bs_mx_scale_bytes(C, mp),), 0xEE, dtype=torch.uint8, device="cuda")
+    fp8bs.fp8_pack_ue8m0(scT, C, mp, 1, 1, C, rT)
+    # the fused casts
+    offs = _offs(off, dev)
+    mpd = _tpad(M, off, dev)
+    q2, sc2 = fp8bs.empty_quant_1x128(M, C)
+    qT2, scT2 = fp8bs.empty_requant_128x1_T(M, C, offs)
+    a2 = torch.full((fp8bs.fp8bs_mx_scale_bytes(mpd, C),), 0xEE, dtype=torch.uint8, device="cuda")
+    aT2 = torch.full((fp8bs.fp8bs_mx_scale_bytes(C, mpd),), 0xEE, dtype=torch.uint8, device="cuda")
+    fused(x, q2, sc2, qT2, scT2, a2, aT2, offsets=offs)
+    torch.cuda.synchronize()
+    assert fp8bs.fp8bs_device_status(reset=True) == 0
+    assert torch.equal(q2, q) and torch.equal(sc2[:, :M], sc[:, :M])
+    assert torch.equal(qT2[:, :mp], qT) and torch.equal(scT2[:mp // 128], scT)
+    nq = (mp // 128) * (C // 128) * 512
+    assert torch.equal(a2[:nq], ra[:nq])
+    t, td = mp // 128, mpd // 128
+    for ct in range(C // 128):
+        assert torch.equal(aT2[ct * td * 512:(ct * td + t) * 512], rT[ct * t * 512:(ct + 1) * t * 512]), ct
